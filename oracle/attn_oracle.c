@@ -1,0 +1,270 @@
+/*
+ * attn_oracle.c -- fp64 CPU oracle for BSR paged-KV attention.
+ *
+ * TEST INFRASTRUCTURE ONLY (tests, smoke check, CPU-baseline timing); the
+ * library path never links it. Plain single-threaded C, no BLAS, no blocking:
+ * every output is the textbook definition evaluated in double precision.
+ *
+ * Sources (FlashInfer paper digest, modb.pro page):
+ *  - "统一的 KV 缓存存储格式": the KV cache is a block-sparse row matrix; rows are
+ *    requests, blocks are pages of a configurable size, and an index array maps
+ *    logical blocks to physical pages. Its formula did not survive extraction;
+ *    the reading used is in bsr_token_ptr() below.
+ *  - "可组合格式" in the same section: several block-sparse formats take part in
+ *    one attention computation; their partial states are combined by
+ *    log-sum-exp merging (oracle_merge_states).
+ * Attention itself is softmax(q K^T * sm_scale) V (yeyulingfeng.com page,
+ * "FlashAttention 的遗产": the tiled form changes IO only, not the result).
+ *
+ * Parity pins: see the header comment of attn_oracle.h.
+ */
+#include "attn_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+double oracle_widen(uint16_t bits, int32_t dtype) {
+  if (dtype == ORACLE_BF16) {
+    /* bfloat16 is the top half of an IEEE binary32 word. */
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+  }
+  /* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+  int sign = bits >> 15;
+  int e = (bits >> 10) & 0x1f;
+  int m = bits & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24);               /* subnormal: m * 2^-24 */
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp((double)(m | 0x400), e - 25);  /* (1024 + m) * 2^(e-15-10) */
+  return sign ? -v : v;
+}
+
+/* Number of logical KV tokens of request r (BSR reading, see header). */
+static int64_t bsr_kv_len(const int32_t* kv_indptr, const int32_t* last_page_len,
+                          int32_t page_size, int32_t r) {
+  int64_t n = (int64_t)kv_indptr[r + 1] - kv_indptr[r];
+  if (n <= 0) return 0;
+  return (n - 1) * page_size + last_page_len[r];
+}
+
+/* Address of the D-vector of logical token t, kv head hk, of request r. */
+static const uint16_t* bsr_token_ptr(const uint16_t* pool, int32_t layout,
+                                     const int32_t* kv_indptr,
+                                     const int32_t* kv_indices, int32_t page_size,
+                                     int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t r, int64_t t, int32_t hk) {
+  int64_t page = kv_indices[kv_indptr[r] + t / page_size];
+  int64_t slot = t % page_size;
+  int64_t row;
+  if (layout == ORACLE_HND)
+    row = (page * num_kv_heads + hk) * page_size + slot;
+  else
+    row = (page * page_size + slot) * num_kv_heads + hk;
+  return pool + row * head_dim;
+}
+
+static int32_t check_args(const int32_t* qo_indptr, int64_t num_pages,
+                          int32_t layout, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, const int32_t* last_page_len,
+                          int32_t batch, int32_t page_size, int32_t num_qo_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t dtype) {
+  if (batch < 0 || page_size <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0)
+    return -1;
+  if (num_qo_heads % num_kv_heads != 0) return -2;
+  if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -3;
+  if (layout != ORACLE_HND && layout != ORACLE_NHD) return -4;
+  for (int32_t r = 0; r < batch; ++r) {
+    int32_t n = kv_indptr[r + 1] - kv_indptr[r];
+    if (n < 0) return -5;
+    if (n > 0 && (last_page_len[r] < 1 || last_page_len[r] > page_size)) return -6;
+    for (int32_t k = kv_indptr[r]; k < kv_indptr[r + 1]; ++k)
+      if (kv_indices[k] < 0 || kv_indices[k] >= num_pages) return -7;
+    if (qo_indptr) {
+      int64_t qo_len = (int64_t)qo_indptr[r + 1] - qo_indptr[r];
+      if (qo_len < 0) return -8;
+    }
+  }
+  return 0;
+}
+
+/*
+ * One output row, restricted to logical kv positions [kv_lo, kv_hi) of the
+ * visible set. Two passes: logits first (exact max), then the weighted sums,
+ * all in logical kv order.
+ */
+static void attention_row(const uint16_t* q, const int32_t* qo_indptr,
+                          const uint16_t* k_pool, const uint16_t* v_pool,
+                          int32_t layout, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, const int32_t* last_page_len,
+                          int32_t page_size, int32_t num_qo_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                          int32_t causal, double sm_scale, int32_t r, int32_t i,
+                          int32_t h, int64_t kv_lo, int64_t kv_hi, double* x_buf,
+                          double* q_buf, double* o, double* lse) {
+  const int32_t group = num_qo_heads / num_kv_heads;
+  const int32_t hk = h / group;
+  const int64_t qo_start = qo_indptr ? qo_indptr[r] : r;
+  const int64_t qo_len = qo_indptr ? (int64_t)qo_indptr[r + 1] - qo_indptr[r] : 1;
+  const int64_t kv_len = bsr_kv_len(kv_indptr, last_page_len, page_size, r);
+
+  /* Visible set J = [0, vis): causal rows see j <= kv_len - qo_len + i. */
+  int64_t vis = kv_len;
+  if (causal) {
+    int64_t lim = kv_len - qo_len + i + 1;
+    if (lim < vis) vis = lim;
+  }
+  if (vis < 0) vis = 0;
+  int64_t lo = kv_lo < 0 ? 0 : kv_lo;
+  int64_t hi = kv_hi < vis ? kv_hi : vis;
+
+  const uint16_t* qrow = q + ((qo_start + i) * num_qo_heads + h) * head_dim;
+  for (int32_t d = 0; d < head_dim; ++d) q_buf[d] = oracle_widen(qrow[d], dtype);
+
+  for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+  if (hi <= lo) {
+    *lse = -INFINITY;
+    return;
+  }
+
+  double m = -INFINITY;
+  for (int64_t j = lo; j < hi; ++j) {
+    const uint16_t* krow = bsr_token_ptr(k_pool, layout, kv_indptr, kv_indices,
+                                         page_size, num_kv_heads, head_dim, r, j, hk);
+    double dot = 0.0;
+    for (int32_t d = 0; d < head_dim; ++d) dot += q_buf[d] * oracle_widen(krow[d], dtype);
+    double x = sm_scale * dot;
+    x_buf[j - lo] = x;
+    if (x > m) m = x;
+  }
+  double l = 0.0;
+  for (int64_t j = lo; j < hi; ++j) {
+    double p = exp(x_buf[j - lo] - m);
+    l += p;
+    const uint16_t* vrow = bsr_token_ptr(v_pool, layout, kv_indptr, kv_indices,
+                                         page_size, num_kv_heads, head_dim, r, j, hk);
+    for (int32_t d = 0; d < head_dim; ++d) o[d] += p * oracle_widen(vrow[d], dtype);
+  }
+  for (int32_t d = 0; d < head_dim; ++d) o[d] /= l;
+  *lse = m + log(l);
+}
+
+static int64_t max_kv_len(const int32_t* kv_indptr, const int32_t* last_page_len,
+                          int32_t page_size, int32_t batch) {
+  int64_t mx = 1;
+  for (int32_t r = 0; r < batch; ++r) {
+    int64_t n = bsr_kv_len(kv_indptr, last_page_len, page_size, r);
+    if (n > mx) mx = n;
+  }
+  return mx;
+}
+
+int32_t oracle_attention_row(const uint16_t* q, const int32_t* qo_indptr,
+                             const uint16_t* k_pool, const uint16_t* v_pool,
+                             int64_t num_pages, int32_t layout,
+                             const int32_t* kv_indptr, const int32_t* kv_indices,
+                             const int32_t* last_page_len, int32_t batch,
+                             int32_t page_size, int32_t num_qo_heads,
+                             int32_t num_kv_heads, int32_t head_dim,
+                             int32_t dtype, int32_t causal, double sm_scale,
+                             int32_t r, int32_t i, int32_t h,
+                             double* o, double* lse) {
+  if (r < 0 || r >= batch || h < 0 || h >= num_qo_heads || i < 0) return -1;
+  int32_t rc = check_args(qo_indptr, num_pages, layout, kv_indptr, kv_indices,
+                          last_page_len, batch, page_size, num_qo_heads,
+                          num_kv_heads, head_dim, dtype);
+  if (rc) return rc;
+  int64_t qo_len = qo_indptr ? (int64_t)qo_indptr[r + 1] - qo_indptr[r] : 1;
+  if (i >= qo_len) return -1;
+  int64_t kv_len = bsr_kv_len(kv_indptr, last_page_len, page_size, r);
+  double* x_buf = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+  double* q_buf = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  if (!x_buf || !q_buf) {
+    free(x_buf);
+    free(q_buf);
+    return -100;
+  }
+  attention_row(q, qo_indptr, k_pool, v_pool, layout, kv_indptr, kv_indices,
+                last_page_len, page_size, num_qo_heads, num_kv_heads, head_dim,
+                dtype, causal, sm_scale, r, i, h, 0, INT64_MAX, x_buf, q_buf, o, lse);
+  free(x_buf);
+  free(q_buf);
+  return 0;
+}
+
+int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
+                               const uint16_t* k_pool, const uint16_t* v_pool,
+                               int64_t num_pages, int32_t layout,
+                               const int32_t* kv_indptr, const int32_t* kv_indices,
+                               const int32_t* last_page_len, int32_t batch,
+                               int32_t page_size, int32_t num_qo_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t dtype, int32_t causal, double sm_scale,
+                               const int32_t* kv_begin, const int32_t* kv_end,
+                               double* o, double* lse) {
+  int32_t rc = check_args(qo_indptr, num_pages, layout, kv_indptr, kv_indices,
+                          last_page_len, batch, page_size, num_qo_heads,
+                          num_kv_heads, head_dim, dtype);
+  if (rc) return rc;
+  int64_t mx = max_kv_len(kv_indptr, last_page_len, page_size, batch);
+  double* x_buf = (double*)malloc(sizeof(double) * (size_t)mx);
+  double* q_buf = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  if (!x_buf || !q_buf) {
+    free(x_buf);
+    free(q_buf);
+    return -100;
+  }
+  for (int32_t r = 0; r < batch; ++r) {
+    int64_t qo_start = qo_indptr ? qo_indptr[r] : r;
+    int64_t qo_len = qo_indptr ? (int64_t)qo_indptr[r + 1] - qo_indptr[r] : 1;
+    int64_t lo = kv_begin ? kv_begin[r] : 0;
+    int64_t hi = kv_end ? kv_end[r] : INT64_MAX;
+    for (int64_t i = 0; i < qo_len; ++i) {
+      for (int32_t h = 0; h < num_qo_heads; ++h) {
+        int64_t row = (qo_start + i) * num_qo_heads + h;
+        attention_row(q, qo_indptr, k_pool, v_pool, layout, kv_indptr, kv_indices,
+                      last_page_len, page_size, num_qo_heads, num_kv_heads,
+                      head_dim, dtype, causal, sm_scale, r, (int32_t)i, h, lo, hi,
+                      x_buf, q_buf, o + row * head_dim, lse + row);
+      }
+    }
+  }
+  free(x_buf);
+  free(q_buf);
+  return 0;
+}
+
+void oracle_merge_states(const double* o_in, const double* lse_in,
+                         int32_t n_states, int64_t rows, int32_t head_dim,
+                         double* o_out, double* lse_out) {
+  for (int64_t row = 0; row < rows; ++row) {
+    double m = -INFINITY;
+    for (int32_t s = 0; s < n_states; ++s) {
+      double v = lse_in[(int64_t)s * rows + row];
+      if (v > m) m = v;
+    }
+    double* out = o_out + row * head_dim;
+    for (int32_t d = 0; d < head_dim; ++d) out[d] = 0.0;
+    if (m == -INFINITY) {
+      lse_out[row] = -INFINITY;
+      continue;
+    }
+    double sum = 0.0;
+    for (int32_t s = 0; s < n_states; ++s)
+      sum += exp(lse_in[(int64_t)s * rows + row] - m);
+    double lse = m + log(sum);
+    for (int32_t s = 0; s < n_states; ++s) {
+      double w = exp(lse_in[(int64_t)s * rows + row] - lse);
+      const double* in = o_in + ((int64_t)s * rows + row) * head_dim;
+      for (int32_t d = 0; d < head_dim; ++d) out[d] += w * in[d];
+    }
+    lse_out[row] = lse;
+  }
+}

@@ -1,0 +1,150 @@
+"""Reference work partitioner (plan) -- TEST INFRASTRUCTURE ONLY.
+
+Restates, in plain Python, the CPU planning phase of the FlashInfer scheduler
+(modb.pro digest, section "动态负载均衡调度": a Stream-K inspired planner that
+analyses the length distribution on the CPU and assigns work units to SMs so
+that a fixed-grid persistent kernel can follow the plan). The digest gives no
+pseudo-code; the exact cut below is the reading used throughout this project:
+
+  items      (request r, kv head hk, query tile t), r-major, then hk, then t;
+             decode has one tile per request, append tiles hold
+             tq = 128 // group query tokens (group heads x tq tokens <= 128 rows)
+  pages      n = ceil(vis / P), vis = visible kv length of the tile's last row
+             (the whole kv_len unless causal)
+  weights    w = n + alpha (alpha = 1 overhead slot); prefix sums in int64,
+             W = sum w; CTA c owns positions [floor(c W / C), floor((c+1) W / C))
+  units      inside an item with base b, position b is its overhead slot and
+             b + alpha + k is page k; CTA c's intersection yields pages
+             [max(0, lo - b - alpha), min(n, hi - b - alpha)); an intersection
+             without pages is dropped, except that an item with n = 0 keeps one
+             zero-page unit, owned by the CTA that owns b
+  slots      items with >= 2 units are split; their units get partial-state
+             slots numbered in (item, page) order; merge_indptr lists them.
+
+It is written independently of the library's C++ planner; the tests require
+the two to agree bit for bit.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+ALPHA = 1
+TILE_ROWS = 128
+
+
+@dataclass
+class Plan:
+    work_indptr: List[int]
+    unit_r: List[int] = field(default_factory=list)
+    unit_hk: List[int] = field(default_factory=list)
+    unit_t: List[int] = field(default_factory=list)
+    unit_p0: List[int] = field(default_factory=list)
+    unit_p1: List[int] = field(default_factory=list)
+    unit_slot: List[int] = field(default_factory=list)
+    merge_indptr: List[int] = field(default_factory=lambda: [0])
+    merge_r: List[int] = field(default_factory=list)
+    merge_hk: List[int] = field(default_factory=list)
+    merge_t: List[int] = field(default_factory=list)
+    total_weight: int = 0
+    num_items: int = 0
+    q_tile: int = 1
+
+
+def kv_length(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size: int,
+              r: int) -> int:
+    n = kv_indptr[r + 1] - kv_indptr[r]
+    return 0 if n <= 0 else (n - 1) * page_size + last_page_len[r]
+
+
+def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size: int,
+              num_qo_heads: int, num_kv_heads: int, num_ctas: int,
+              qo_indptr: Optional[Sequence[int]] = None, causal: bool = False) -> Plan:
+    batch = len(kv_indptr) - 1
+    group = num_qo_heads // num_kv_heads
+    decode = qo_indptr is None
+    tq = 1 if decode else TILE_ROWS // group
+
+    # 1. items and their page counts
+    items = []  # (r, hk, t, n)
+    for r in range(batch):
+        kv_len = kv_length(kv_indptr, last_page_len, page_size, r)
+        qo_len = 1 if decode else qo_indptr[r + 1] - qo_indptr[r]
+        tiles = 1 if decode else -(-qo_len // tq)
+        for hk in range(num_kv_heads):
+            for t in range(tiles):
+                vis = kv_len
+                if causal and not decode:
+                    last_row = min((t + 1) * tq, qo_len) - 1
+                    vis = min(kv_len, max(0, kv_len - qo_len + last_row + 1))
+                items.append((r, hk, t, -(-vis // page_size)))
+
+    # 2. weights and CTA ranges
+    bases = []
+    total = 0
+    for it in items:
+        bases.append(total)
+        total += it[3] + ALPHA
+    C = num_ctas
+
+    def lo(c):
+        return (c * total) // C
+
+    plan = Plan(work_indptr=[0] * (C + 1), total_weight=total, num_items=len(items),
+                q_tile=tq)
+
+    # 3. units, CTA by CTA (positions are monotone, so this is item order too)
+    per_cta_units = [[] for _ in range(C)]
+    for k, (r, hk, t, n) in enumerate(items):
+        b = bases[k]
+        w = n + ALPHA
+        for c in range(C):
+            a, e = lo(c), lo(c + 1)
+            if e <= b or a >= b + w:
+                continue
+            if n == 0:
+                if a <= b < e:
+                    per_cta_units[c].append([k, r, hk, t, 0, 0])
+                continue
+            p0 = max(0, a - b - ALPHA)
+            p1 = min(n, e - b - ALPHA)
+            if p1 > p0:
+                per_cta_units[c].append([k, r, hk, t, p0, p1])
+
+    flat = []
+    for c in range(C):
+        plan.work_indptr[c + 1] = plan.work_indptr[c] + len(per_cta_units[c])
+        flat.extend(per_cta_units[c])
+
+    # 4. split items and slot numbering in (item, page) order
+    count = {}
+    for u in flat:
+        count[u[0]] = count.get(u[0], 0) + 1
+    order = sorted(range(len(flat)), key=lambda i: (flat[i][0], flat[i][4]))
+    slot_of = [-1] * len(flat)
+    next_slot = 0
+    last_item = None
+    for i in order:
+        k = flat[i][0]
+        if count[k] < 2:
+            continue
+        if k != last_item:
+            plan.merge_r.append(flat[i][1])
+            plan.merge_hk.append(flat[i][2])
+            plan.merge_t.append(flat[i][3])
+            if last_item is not None:
+                plan.merge_indptr.append(next_slot)
+            last_item = k
+        slot_of[i] = next_slot
+        next_slot += 1
+    if last_item is not None:
+        plan.merge_indptr.append(next_slot)
+
+    for i, u in enumerate(flat):
+        plan.unit_r.append(u[1])
+        plan.unit_hk.append(u[2])
+        plan.unit_t.append(u[3])
+        plan.unit_p0.append(u[4])
+        plan.unit_p1.append(u[5])
+        plan.unit_slot.append(slot_of[i])
+    return plan
