@@ -1,0 +1,235 @@
+/*
+ * attn.h -- C ABI of libattn.so: attention over a block-sparse-row (BSR)
+ * paged KV cache on one GB300 (sm_103a).
+ *
+ * The operations follow "FlashInfer: Efficient and Customizable Attention
+ * Engine for LLM Inference Serving" (arXiv 2501.01005) as summarised on the
+ * modb.pro digest page:
+ *  - "统一的 KV 缓存存储格式" (unified KV-cache storage format): the cache of a
+ *    batch is a block-sparse row matrix. Row r is request r; its blocks are
+ *    pages of `page_size` tokens listed in kv_indices[kv_indptr[r] ..
+ *    kv_indptr[r+1]); the last page holds last_page_len[r] tokens, so
+ *    kv_len_r = (n_r - 1) * page_size + last_page_len[r] for n_r > 0 pages
+ *    and 0 for n_r = 0. (The digest's formula did not survive extraction;
+ *    this is the reading used.) Contiguous caches are the one-page case.
+ *  - "可组合格式" (composable formats): several formats take part in one
+ *    attention; their partial results are combined with attn_merge_states.
+ *  - "动态负载均衡调度" (load-balanced scheduling): a CPU planning phase
+ *    (attn_plan) splits the KV of every request into work units balanced
+ *    across SMs; a persistent fixed-grid kernel (attn_*_run) follows the
+ *    plan using a preallocated workspace, so runs can be captured in CUDA
+ *    graphs.
+ * Attention is softmax(q K^T * sm_scale) V per query head, with query head h
+ * reading kv head h / (num_qo_heads / num_kv_heads) (grouped-query heads).
+ * Decode has one query row per request (gittoolsai.com page, "基本用法":
+ * q [num_qo_heads, head_dim] against k/v [kv_len, num_kv_heads, head_dim]).
+ *
+ * Conventions for every entry point:
+ *  - The caller owns all memory. The library allocates nothing and keeps no
+ *    state besides a per-device cache of attributes and per-thread error text.
+ *  - Pointers documented as "device" are CUDA device memory of the current
+ *    device; "host" pointers are CPU memory. Work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream) and is asynchronous.
+ *  - Every call returns an attn_status_t and never throws. On failure
+ *    attn_last_error() returns a message for the calling thread, and nothing
+ *    is enqueued. Argument checks happen on the host before any launch.
+ *  - head_dim must be 128. num_qo_heads must be a multiple of num_kv_heads.
+ *  - LSE outputs are natural-log log-sum-exp of the scaled logits, fp32;
+ *    an empty visible set gives O = 0 and LSE = -inf.
+ */
+#ifndef PAGED_BSR_ATTN_H
+#define PAGED_BSR_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,         /* a size, pointer or value is out of range  */
+  ATTN_ERR_UNSUPPORTED = 2,         /* valid but not implemented (e.g. head_dim) */
+  ATTN_ERR_WORKSPACE_TOO_SMALL = 3, /* a workspace is smaller than required      */
+  ATTN_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed         */
+  ATTN_ERR_TIMEOUT = 5              /* a kernel gave up waiting (bounded waits)  */
+} attn_status_t;
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/* Pool layouts. HND: [num_pages, num_kv_heads, page_size, head_dim];
+ * NHD: [num_pages, page_size, num_kv_heads, head_dim]. Both row-major. */
+typedef enum { ATTN_LAYOUT_HND = 0, ATTN_LAYOUT_NHD = 1 } attn_kv_layout_t;
+
+typedef enum { ATTN_MODE_DECODE = 0, ATTN_MODE_APPEND = 1 } attn_mode_t;
+
+/*
+ * A work plan: plain data produced by attn_plan. It records the shapes the
+ * plan was made for and where the plan's tables live inside the device
+ * workspace. Pass it unchanged to the matching run call.
+ */
+typedef struct attn_plan {
+  int32_t mode;             /* attn_mode_t                                     */
+  int32_t batch;
+  int32_t page_size;
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t causal;
+  int32_t num_ctas;         /* grid size of the persistent run kernel          */
+  int32_t q_tile;           /* query tokens per tile: 128 / group (append), 1  */
+  int32_t rows_per_item;    /* packed rows of one item: group * q_tile         */
+  int32_t num_items;        /* (request, kv head, query tile) triples          */
+  int32_t num_units;        /* work units after the balanced cut               */
+  int32_t num_split_items;  /* items cut into >= 2 units (merged after run)    */
+  int32_t num_slots;        /* partial-state slots used by split items         */
+  int32_t total_qo;         /* query rows (decode: batch)                      */
+  int32_t reserved0;
+  int64_t total_weight;     /* sum over items of (pages + 1)                   */
+  int64_t max_cta_weight;   /* largest per-CTA share of total_weight           */
+  int64_t off_work_indptr;  /* byte offsets of the tables in the workspaces    */
+  int64_t off_units;
+  int64_t off_merge_indptr;
+  int64_t off_merge_items;
+  int64_t off_partial_o;
+  int64_t off_partial_lse;
+  int64_t table_bytes;      /* bytes [0, table_bytes) copied host -> device    */
+  int64_t dev_bytes_needed; /* device workspace bytes this plan uses           */
+  uint64_t fingerprint;     /* hash of the host inputs of the plan             */
+} attn_plan_t;
+
+/*
+ * Workspace sizes able to hold any plan with at most max_batch requests,
+ * max_total_qo query rows (append; pass max_batch for decode-only use) and
+ * num_ctas CTAs. Pure host computation.
+ *   dev_bytes         : device workspace (plan tables + partial states)
+ *   pinned_host_bytes : host staging area for the plan tables (page-locked
+ *                       memory, so the table copy is asynchronous)
+ * Errors: INVALID_ARG for non-positive sizes or null outputs.
+ */
+attn_status_t attn_workspace_size(int32_t max_batch, int32_t max_total_qo,
+                                  int32_t num_qo_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t num_ctas,
+                                  size_t* dev_bytes, size_t* pinned_host_bytes);
+
+/*
+ * Default persistent grid for `mode` on CUDA device `device`: the number of
+ * SMs times the CTAs of the run kernel that fit on one SM.
+ * Errors: CUDA if the device cannot be queried; INVALID_ARG for bad mode.
+ */
+attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_ctas);
+
+/*
+ * Planning phase (host). Splits the work of a batch into units balanced over
+ * num_ctas CTAs (items (request, kv head, query tile) in request-major order;
+ * each item weighs its page count + 1; CTA c takes the weight positions
+ * [floor(c W / C), floor((c+1) W / C)) of the total W; an item cut by a CTA
+ * boundary is "split" and its units write partial states that the run merges).
+ *   qo_indptr_h     : host int32[batch+1] query row offsets (append), or NULL
+ *                     for decode (one row per request)
+ *   kv_indptr_h     : host int32[batch+1] page offsets into kv_indices
+ *   last_page_len_h : host int32[batch]; 1..page_size when the request has pages
+ *   causal          : 1 = query row i of a request with qo_len rows sees kv
+ *                     positions j <= kv_len - qo_len + i (end-aligned);
+ *                     0 = all positions. Ignored for decode.
+ *   pinned_host_ws  : host staging buffer of pinned_bytes bytes. It must stay
+ *                     untouched until the copy enqueued on `stream` has run.
+ *   dev_ws          : device workspace of dev_bytes bytes, or NULL to only
+ *                     compute the tables on the host (no CUDA call is made).
+ *   plan_out        : receives the plan.
+ * The tables are written to pinned_host_ws and copied to dev_ws with one
+ * cudaMemcpyAsync on `stream`; the copy also clears the workspace's error
+ * word. The plan depends only on the host inputs and num_ctas and is
+ * identical run to run.
+ * Errors: INVALID_ARG (negative lengths, last_page_len out of range, heads not
+ * divisible, append with kv_len < qo_len), UNSUPPORTED (head_dim != 128,
+ * group too large), WORKSPACE_TOO_SMALL, CUDA.
+ */
+attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
+                        const int32_t* last_page_len_h, int32_t batch,
+                        int32_t page_size, int32_t num_qo_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t causal,
+                        int32_t num_ctas, void* pinned_host_ws, size_t pinned_bytes,
+                        void* dev_ws, size_t dev_bytes, void* stream,
+                        attn_plan_t* plan_out);
+
+/*
+ * Batch decode over a paged cache (one query row per request), following a
+ * decode plan. Persistent kernel with plan->num_ctas CTAs; split items are
+ * merged by an LSE merge kernel in the same stream.
+ *   q          : device [batch, num_qo_heads, head_dim] of `dtype`
+ *   k_pool,
+ *   v_pool     : device pools of num_pages pages in `layout`, `dtype`
+ *   kv_indptr, kv_indices, last_page_len : device copies of the BSR table
+ *                (kv_indptr and last_page_len equal to the plan's host copies;
+ *                every kv_indices entry in [0, num_pages))
+ *   sm_scale   : logit scale (1/sqrt(head_dim) is the usual choice)
+ *   o          : device [batch, num_qo_heads, head_dim] of `dtype` (out)
+ *   lse        : device float[batch, num_qo_heads] (out) or NULL
+ *   dev_ws     : the workspace given to attn_plan (holds the plan tables)
+ * Supported: head_dim 128, group = num_qo_heads / num_kv_heads in 1..8,
+ * any page_size >= 1, both layouts, fp16 and bf16.
+ * Errors: INVALID_ARG (plan mode/shape mismatch, null pointers),
+ * UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA (launch failure).
+ */
+attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q,
+                              const void* k_pool, const void* v_pool,
+                              int64_t num_pages, int32_t layout,
+                              const int32_t* kv_indptr, const int32_t* kv_indices,
+                              const int32_t* last_page_len, int32_t dtype,
+                              float sm_scale, void* o, float* lse, void* dev_ws,
+                              size_t dev_bytes, void* stream);
+
+/*
+ * Append / prefill attention: many query rows per request (ragged, offsets
+ * qo_indptr) against that request's paged KV, which already holds the new
+ * tokens (kv_len >= qo_len), causal (end-aligned) or not, following an append
+ * plan. Tensor-core kernel (tcgen05 MMA, TMEM accumulators, TMA-fed).
+ *   q          : device [total_qo, num_qo_heads, head_dim] of `dtype`
+ *   qo_indptr  : device int32[batch+1], equal to the plan's host copy
+ *   other arguments as attn_decode_run; o is [total_qo, num_qo_heads, head_dim]
+ *   and lse float[total_qo, num_qo_heads].
+ * Supported: head_dim 128, bf16 or fp16, HND layout, page_size a multiple of
+ * 16, group in {1, 2, 4, 8, 16}.
+ * Errors: as attn_decode_run.
+ */
+attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
+                              const int32_t* qo_indptr, const void* k_pool,
+                              const void* v_pool, int64_t num_pages, int32_t layout,
+                              const int32_t* kv_indptr, const int32_t* kv_indices,
+                              const int32_t* last_page_len, int32_t dtype,
+                              int32_t causal, float sm_scale, void* o, float* lse,
+                              void* dev_ws, size_t dev_bytes, void* stream);
+
+/*
+ * Merge two attention states of the same rows by log-sum-exp ("可组合格式":
+ * combining the partial results of composable formats / split KV):
+ *   m = max(lse_a, lse_b); lse = m + ln(e^(lse_a - m) + e^(lse_b - m));
+ *   o = e^(lse_a - lse) o_a + e^(lse_b - lse) o_b.
+ * Both states empty (lse = -inf) gives o = 0, lse = -inf.
+ *   o_a, o_b, o_out  : device [n, num_heads, head_dim] of `dtype`
+ *   lse_a, lse_b     : device float[n, num_heads] (natural log)
+ *   lse_out          : device float[n, num_heads] (out) or NULL
+ * o_out may alias o_a or o_b. Any head_dim that is a multiple of 8.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+attn_status_t attn_merge_states(const void* o_a, const float* lse_a,
+                                const void* o_b, const float* lse_b, void* o_out,
+                                float* lse_out, int32_t n, int32_t num_heads,
+                                int32_t head_dim, int32_t dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads the error word that kernels set in a
+ * workspace when a bounded wait expired. *code_out receives 0 if none.
+ * Returns TIMEOUT if the word is set, CUDA on a runtime error, else OK.
+ */
+attn_status_t attn_workspace_status(const void* dev_ws, void* stream, int32_t* code_out);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGED_BSR_ATTN_H */

@@ -1,0 +1,193 @@
+"""ctypes binding of libattn.so (include/attn.h): argument marshalling only.
+
+Every function here has the name of a C entry point without the ``attn_``
+prefix and does nothing but turn torch tensors / numpy arrays into pointers,
+call the library, and raise ``AttnError`` on a non-OK status. All attention
+work runs in the library's CUDA kernels; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT = range(6)
+F16, BF16 = 0, 1
+LAYOUT_HND, LAYOUT_NHD = 0, 1
+MODE_DECODE, MODE_APPEND = 0, 1
+
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
+                4: "CUDA", 5: "TIMEOUT"}
+
+# Every symbol include/attn.h declares (checked by the tests).
+EXPORTS = ("attn_workspace_size", "attn_default_num_ctas", "attn_plan", "attn_decode_run",
+           "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Plan(ctypes.Structure):
+    """Mirror of attn_plan_t."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "mode", "batch", "page_size", "num_qo_heads", "num_kv_heads", "head_dim", "causal",
+        "num_ctas", "q_tile", "rows_per_item", "num_items", "num_units", "num_split_items",
+        "num_slots", "total_qo", "reserved0")] + [(n, ctypes.c_int64) for n in (
+        "total_weight", "max_cta_weight", "off_work_indptr", "off_units", "off_merge_indptr",
+        "off_merge_items", "off_partial_o", "off_partial_lse", "table_bytes",
+        "dev_bytes_needed")] + [("fingerprint", ctypes.c_uint64)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    i32, i64, sz, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    vp = ctypes.c_void_p
+    P = ctypes.POINTER
+    sig = {
+        "attn_workspace_size": [i32, i32, i32, i32, i32, i32, P(sz), P(sz)],
+        "attn_default_num_ctas": [i32, i32, P(i32)],
+        "attn_plan": [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, sz, vp, sz, vp,
+                      P(Plan)],
+        "attn_decode_run": [P(Plan), vp, vp, vp, i64, i32, vp, vp, vp, i32, f32, vp, vp, vp,
+                            sz, vp],
+        "attn_append_run": [P(Plan), vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, f32, vp,
+                            vp, vp, sz, vp],
+        "attn_merge_states": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp],
+        "attn_workspace_status": [vp, vp, P(i32)],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.attn_last_error.argtypes = []
+    lib.attn_last_error.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def last_error() -> str:
+    return lib.attn_last_error().decode()
+
+
+def _check(status: int):
+    if status != OK:
+        raise AttnError(status, last_error())
+
+
+def _ptr(x):
+    """Device/host address of a tensor or numpy array (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return ctypes.c_void_p(x.data_ptr())
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data_as(ctypes.c_void_p)
+    if isinstance(x, int):
+        return ctypes.c_void_p(x)
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _host_i32(x):
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return BF16
+    if t == torch.float16:
+        return F16
+    raise TypeError(f"unsupported dtype {t}; use torch.float16 or torch.bfloat16")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def workspace_size(max_batch, max_total_qo, num_qo_heads, num_kv_heads, head_dim, num_ctas):
+    dev = ctypes.c_size_t()
+    host = ctypes.c_size_t()
+    _check(lib.attn_workspace_size(max_batch, max_total_qo, num_qo_heads, num_kv_heads,
+                                   head_dim, num_ctas, ctypes.byref(dev), ctypes.byref(host)))
+    return dev.value, host.value
+
+
+def default_num_ctas(device: int = 0, mode: int = MODE_DECODE) -> int:
+    n = ctypes.c_int32()
+    _check(lib.attn_default_num_ctas(device, mode, ctypes.byref(n)))
+    return n.value
+
+
+def plan(qo_indptr_h, kv_indptr_h, last_page_len_h, page_size, num_qo_heads, num_kv_heads,
+         head_dim, causal, num_ctas, pinned_ws, dev_ws=None, stream=None) -> Plan:
+    """attn_plan. Host arrays; pinned_ws: host tensor / array; dev_ws: CUDA tensor or None."""
+    kv_indptr_h = _host_i32(kv_indptr_h)
+    last_page_len_h = _host_i32(last_page_len_h)
+    qo_indptr_h = _host_i32(qo_indptr_h)
+    batch = len(kv_indptr_h) - 1
+    host_bytes = pinned_ws.numel() * pinned_ws.element_size() if isinstance(
+        pinned_ws, torch.Tensor) else pinned_ws.nbytes
+    dev_bytes = 0 if dev_ws is None else dev_ws.numel() * dev_ws.element_size()
+    p = Plan()
+    _check(lib.attn_plan(_ptr(qo_indptr_h), _ptr(kv_indptr_h), _ptr(last_page_len_h), batch,
+                         page_size, num_qo_heads, num_kv_heads, head_dim, int(bool(causal)),
+                         num_ctas, _ptr(pinned_ws), host_bytes, _ptr(dev_ws), dev_bytes,
+                         _stream(stream) if dev_ws is not None else None, ctypes.byref(p)))
+    return p
+
+
+def decode_run(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale, o,
+               lse, dev_ws, layout=LAYOUT_HND, num_pages=None, stream=None):
+    if num_pages is None:
+        num_pages = k_pool.shape[0]
+    _check(lib.attn_decode_run(ctypes.byref(p), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                               int(num_pages), layout, _ptr(kv_indptr), _ptr(kv_indices),
+                               _ptr(last_page_len), dtype_code(q.dtype), float(sm_scale),
+                               _ptr(o), _ptr(lse), _ptr(dev_ws),
+                               dev_ws.numel() * dev_ws.element_size(), _stream(stream)))
+
+
+def append_run(p: Plan, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
+               causal, sm_scale, o, lse, dev_ws, layout=LAYOUT_HND, num_pages=None,
+               stream=None):
+    if num_pages is None:
+        num_pages = k_pool.shape[0]
+    _check(lib.attn_append_run(ctypes.byref(p), _ptr(q), _ptr(qo_indptr), _ptr(k_pool),
+                               _ptr(v_pool), int(num_pages), layout, _ptr(kv_indptr),
+                               _ptr(kv_indices), _ptr(last_page_len), dtype_code(q.dtype),
+                               int(bool(causal)), float(sm_scale), _ptr(o), _ptr(lse),
+                               _ptr(dev_ws), dev_ws.numel() * dev_ws.element_size(),
+                               _stream(stream)))
+
+
+def merge_states(o_a, lse_a, o_b, lse_b, o_out, lse_out, stream=None):
+    n, h, d = o_a.shape
+    _check(lib.attn_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out),
+                                 _ptr(lse_out), n, h, d, dtype_code(o_a.dtype), _stream(stream)))
+
+
+def workspace_status(dev_ws, stream=None) -> int:
+    code = ctypes.c_int32()
+    st = lib.attn_workspace_status(_ptr(dev_ws), _stream(stream), ctypes.byref(code))
+    if st not in (OK, ERR_TIMEOUT):
+        _check(st)
+    return code.value

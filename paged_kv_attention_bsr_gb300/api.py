@@ -1,0 +1,133 @@
+"""Torch-facing conveniences over the C ABI: workspace ownership and call order.
+
+PyTorch supplies device memory, pinned host memory and streams; every step of
+the attention itself runs in libattn.so's kernels.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _capi as C
+
+
+class PagedAttention:
+    """Owns the workspaces of one attention call site and runs plan() / run().
+
+    mode "decode": one query row per request (attn_decode_run).
+    mode "append": ragged query rows per request (attn_append_run).
+    The plan tables go through two pinned staging buffers used alternately;
+    a buffer is reused only after its previous upload has executed.
+    """
+
+    def __init__(self, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
+                 mode: str = "decode", max_batch: int = 256, max_total_qo: Optional[int] = None,
+                 num_ctas: Optional[int] = None, device=None):
+        if mode not in ("decode", "append"):
+            raise ValueError("mode must be 'decode' or 'append'")
+        self.mode = mode
+        self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
+        self.device = torch.device(device if device is not None else "cuda")
+        dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
+        cmode = C.MODE_DECODE if mode == "decode" else C.MODE_APPEND
+        self.num_ctas = num_ctas or C.default_num_ctas(dev_index, cmode)
+        self.max_batch = max_batch
+        self.max_total_qo = max_total_qo if max_total_qo is not None else max_batch
+        dev_bytes, host_bytes = C.workspace_size(max_batch, self.max_total_qo, num_qo_heads,
+                                                 num_kv_heads, head_dim, self.num_ctas)
+        self.dev_ws = torch.empty(dev_bytes, dtype=torch.uint8, device=self.device)
+        self._pinned = [torch.empty(host_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self._events = [None, None]
+        self._turn = 0
+        self.plan_info: Optional[C.Plan] = None
+
+    def plan(self, kv_indptr_h, last_page_len_h, page_size: int, qo_indptr_h=None,
+             causal: bool = False, stream=None) -> C.Plan:
+        if (self.mode == "decode") != (qo_indptr_h is None):
+            raise ValueError("decode plans take no qo_indptr; append plans need one")
+        i = self._turn
+        self._turn ^= 1
+        if self._events[i] is not None:
+            self._events[i].synchronize()
+        self.plan_info = C.plan(qo_indptr_h, kv_indptr_h, last_page_len_h, page_size,
+                                self.num_qo_heads, self.num_kv_heads, self.head_dim, causal,
+                                self.num_ctas, self._pinned[i], self.dev_ws, stream)
+        ev = torch.cuda.Event()
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+        self._events[i] = ev
+        self._causal = bool(causal)
+        return self.plan_info
+
+    def run(self, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale=None,
+            out=None, lse=None, qo_indptr=None, layout: int = C.LAYOUT_HND, num_pages=None,
+            return_lse: bool = False, stream=None):
+        if self.plan_info is None:
+            raise RuntimeError("run() before plan()")
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.head_dim)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        if self.mode == "decode":
+            C.decode_run(self.plan_info, q, k_pool, v_pool, kv_indptr, kv_indices,
+                         last_page_len, sm_scale, out, lse, self.dev_ws, layout, num_pages,
+                         stream)
+        else:
+            C.append_run(self.plan_info, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices,
+                         last_page_len, self._causal, sm_scale, out, lse, self.dev_ws, layout,
+                         num_pages, stream)
+        return (out, lse) if return_lse else out
+
+    def status(self, stream=None) -> int:
+        """Synchronise and return the workspace error word (0 = no kernel timed out)."""
+        return C.workspace_status(self.dev_ws, stream)
+
+
+_single_cache = {}
+
+
+def single_decode_with_kv_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                                sm_scale: Optional[float] = None, return_lse: bool = False):
+    """Decode attention of one request over contiguous K/V.
+
+    q [num_qo_heads, head_dim], k / v [kv_len, num_kv_heads, head_dim] (the
+    quick-start snippet's shapes); returns [num_qo_heads, head_dim]. The
+    contiguous cache is read in place as a BSR row of 16-token pages in the
+    NHD layout (pages 0..n-1 in order), so the balanced plan can split it
+    across SMs.
+    """
+    kv_len, Hk, D = k.shape
+    Hq = q.shape[0]
+    P = 16
+    n_pages = (kv_len + P - 1) // P
+    key = (q.device, Hq, Hk, D)
+    att = _single_cache.get(key)
+    if att is None:
+        att = PagedAttention(Hq, Hk, D, "decode", max_batch=1, device=q.device)
+        _single_cache[key] = att
+    kv_indptr_h = np.array([0, n_pages], np.int32)
+    last_h = np.array([kv_len - P * (n_pages - 1) if n_pages else 0], np.int32)
+    att.plan(kv_indptr_h, last_h, P)
+    kv_indptr = torch.from_numpy(kv_indptr_h).to(q.device, non_blocking=True)
+    last = torch.from_numpy(last_h).to(q.device, non_blocking=True)
+    kv_indices = torch.arange(n_pages, dtype=torch.int32, device=q.device)
+    res = att.run(q.reshape(1, Hq, D), k, v, kv_indptr, kv_indices, last, sm_scale,
+                  layout=C.LAYOUT_NHD, num_pages=n_pages, return_lse=return_lse)
+    if return_lse:
+        o, lse = res
+        return o.reshape(Hq, D), lse.reshape(Hq)
+    return res.reshape(Hq, D)
+
+
+def merge_state(o_a, lse_a, o_b, lse_b, out=None, lse_out=None):
+    """LSE merge of two attention states [n, H, D] (+ [n, H] fp32 LSE)."""
+    if out is None:
+        out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    C.merge_states(o_a, lse_a, o_b, lse_b, out, lse_out)
+    return out, lse_out

@@ -1,0 +1,316 @@
+// capi.cpp -- the extern "C" boundary of libattn.so: argument validation,
+// workspace sizing, plan upload and kernel dispatch. Declarations and the
+// contract of every entry point are in include/attn.h.
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+using namespace attn;
+
+namespace {
+
+thread_local std::string g_err;
+
+attn_status_t fail(attn_status_t s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+
+attn_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool log_enabled() {
+  static int on = [] {
+    const char* v = std::getenv("ATTN_LOG");
+    return (v && v[0] && v[0] != '0') ? 1 : 0;
+  }();
+  return on != 0;
+}
+
+attn_status_t check_plan_common(const attn_plan_t* plan, int32_t mode, const void* q,
+                                const void* k_pool, const void* v_pool, int64_t num_pages,
+                                int32_t layout, const int32_t* kv_indptr,
+                                const int32_t* kv_indices, const int32_t* last_page_len,
+                                int32_t dtype, const void* o, const void* dev_ws,
+                                size_t dev_bytes, const char* fn) {
+  std::string f(fn);
+  if (!plan) return fail(ATTN_ERR_INVALID_ARG, f + ": plan is NULL");
+  if (plan->mode != mode)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": plan was made for the other mode");
+  if (plan->head_dim != kHeadDim)
+    return fail(ATTN_ERR_UNSUPPORTED, f + ": only head_dim == 128 is implemented");
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": dtype must be ATTN_F16 or ATTN_BF16");
+  if (layout != ATTN_LAYOUT_HND && layout != ATTN_LAYOUT_NHD)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": unknown layout");
+  if (plan->batch > 0 && plan->total_qo > 0 &&
+      (!q || !o || !kv_indptr || !last_page_len))
+    return fail(ATTN_ERR_INVALID_ARG, f + ": null device pointer");
+  if (plan->num_units > 0 && (!k_pool || !v_pool || !kv_indices))
+    return fail(ATTN_ERR_INVALID_ARG, f + ": null KV pool or kv_indices");
+  if (num_pages < 0) return fail(ATTN_ERR_INVALID_ARG, f + ": num_pages < 0");
+  if (!dev_ws) return fail(ATTN_ERR_INVALID_ARG, f + ": dev_ws is NULL");
+  if (size_t(plan->dev_bytes_needed) > dev_bytes)
+    return fail(ATTN_ERR_WORKSPACE_TOO_SMALL, f + ": device workspace smaller than the plan needs");
+  if (reinterpret_cast<uintptr_t>(dev_ws) % 256 != 0)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": dev_ws must be 256-byte aligned");
+  const uintptr_t align_mask = 15;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pool) |
+       reinterpret_cast<uintptr_t>(v_pool) | reinterpret_cast<uintptr_t>(o)) & align_mask)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": q, k_pool, v_pool and o must be 16-byte aligned");
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_last_error(void) { return g_err.c_str(); }
+
+attn_status_t attn_workspace_size(int32_t max_batch, int32_t max_total_qo,
+                                  int32_t num_qo_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t num_ctas, size_t* dev_bytes,
+                                  size_t* pinned_host_bytes) {
+  if (!dev_bytes || !pinned_host_bytes)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_workspace_size: null output pointer");
+  if (max_batch < 1 || max_total_qo < 0 || num_qo_heads < 1 || num_kv_heads < 1 ||
+      num_ctas < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_workspace_size: sizes must be positive");
+  if (num_qo_heads % num_kv_heads)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "attn_workspace_size: num_qo_heads must be a multiple of num_kv_heads");
+  if (head_dim != kHeadDim)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_workspace_size: only head_dim == 128");
+  const int64_t group = num_qo_heads / num_kv_heads;
+  const bool append_ok = (kTileRows % group == 0);
+  const int64_t q_tile = append_ok ? kTileRows / group : 1;
+  int64_t items = int64_t(max_batch) * num_kv_heads;
+  if (append_ok)
+    items = std::max<int64_t>(
+        items, int64_t(num_kv_heads) * ((int64_t(max_total_qo) + q_tile - 1) / q_tile + max_batch));
+  const int64_t C = num_ctas;
+  const int64_t units = items + C - 1;
+  const int64_t split = std::min<int64_t>(items, C - 1);
+  const int64_t slots = std::min<int64_t>(units, 2 * (C - 1));
+  const int32_t rows = append_ok ? kTileRows : int32_t(group);
+  const PlanLayout L = plan_layout(num_ctas, units, split, slots, rows, head_dim);
+  *dev_bytes = size_t(L.dev_bytes);
+  *pinned_host_bytes = size_t(L.table_bytes);
+  return ATTN_OK;
+}
+
+attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_ctas) {
+  if (!num_ctas) return fail(ATTN_ERR_INVALID_ARG, "attn_default_num_ctas: null output");
+  if (mode != ATTN_MODE_DECODE && mode != ATTN_MODE_APPEND)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_default_num_ctas: unknown mode");
+  int sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_default_num_ctas");
+  const int per_sm = mode == ATTN_MODE_DECODE ? decode_ctas_per_sm() : append_ctas_per_sm();
+  *num_ctas = sms * per_sm;
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
+                        const int32_t* last_page_len_h, int32_t batch, int32_t page_size,
+                        int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t causal, int32_t num_ctas, void* pinned_host_ws,
+                        size_t pinned_bytes, void* dev_ws, size_t dev_bytes, void* stream,
+                        attn_plan_t* plan_out) {
+  const char* msg = "";
+  attn_status_t s = build_plan(qo_indptr_h, kv_indptr_h, last_page_len_h, batch, page_size,
+                               num_qo_heads, num_kv_heads, head_dim, causal, num_ctas,
+                               pinned_host_ws, pinned_bytes, plan_out, &msg);
+  if (s != ATTN_OK) return fail(s, msg);
+  if (log_enabled()) {
+    const attn_plan_t& p = *plan_out;
+    std::fprintf(stderr,
+                 "[attn] plan mode=%s batch=%d items=%d units=%d split=%d slots=%d ctas=%d "
+                 "W=%lld max_cta=%lld mean_cta=%.1f\n",
+                 p.mode == ATTN_MODE_DECODE ? "decode" : "append", p.batch, p.num_items,
+                 p.num_units, p.num_split_items, p.num_slots, p.num_ctas,
+                 (long long)p.total_weight, (long long)p.max_cta_weight,
+                 double(p.total_weight) / p.num_ctas);
+  }
+  if (!dev_ws) return ATTN_OK;  // host-only planning
+  if (size_t(plan_out->dev_bytes_needed) > dev_bytes)
+    return fail(ATTN_ERR_WORKSPACE_TOO_SMALL, "attn_plan: device workspace too small");
+  if (reinterpret_cast<uintptr_t>(dev_ws) % 256 != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_plan: dev_ws must be 256-byte aligned");
+  cudaError_t e = cudaMemcpyAsync(dev_ws, pinned_host_ws, size_t(plan_out->table_bytes),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_plan: table upload");
+  return ATTN_OK;
+}
+
+attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void* k_pool,
+                              const void* v_pool, int64_t num_pages, int32_t layout,
+                              const int32_t* kv_indptr, const int32_t* kv_indices,
+                              const int32_t* last_page_len, int32_t dtype, float sm_scale,
+                              void* o, float* lse, void* dev_ws, size_t dev_bytes,
+                              void* stream) {
+  attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
+                                      layout, kv_indptr, kv_indices, last_page_len, dtype, o,
+                                      dev_ws, dev_bytes, "attn_decode_run");
+  if (s != ATTN_OK) return s;
+  const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
+  if (group > kMaxDecodeGroup)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_run: group > 8 is not implemented");
+  if (plan->batch == 0) return ATTN_OK;
+  DecodeArgs a;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.last_page_len = last_page_len;
+  a.o = o;
+  a.lse = lse;
+  a.ws = ws_view(*plan, dev_ws);
+  a.num_ctas = plan->num_ctas;
+  a.num_units = plan->num_units;
+  a.num_split_items = plan->num_split_items;
+  a.layout = layout;
+  a.dtype = dtype;
+  a.page_size = plan->page_size;
+  a.num_qo_heads = plan->num_qo_heads;
+  a.num_kv_heads = plan->num_kv_heads;
+  a.group = group;
+  a.batch = plan->batch;
+  a.sm_scale = sm_scale;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: decode kernel launch");
+  if (plan->num_split_items > 0) {
+    SplitMergeArgs m;
+    m.ws = a.ws;
+    m.num_split_items = plan->num_split_items;
+    m.rows_per_item = plan->rows_per_item;
+    m.group = group;
+    m.q_tile = 1;
+    m.num_qo_heads = plan->num_qo_heads;
+    m.qo_indptr = nullptr;
+    m.o = o;
+    m.lse = lse;
+    m.dtype = dtype;
+    e = launch_split_merge(m, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: merge kernel launch");
+  }
+  return ATTN_OK;
+}
+
+attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
+                              const int32_t* qo_indptr, const void* k_pool,
+                              const void* v_pool, int64_t num_pages, int32_t layout,
+                              const int32_t* kv_indptr, const int32_t* kv_indices,
+                              const int32_t* last_page_len, int32_t dtype, int32_t causal,
+                              float sm_scale, void* o, float* lse, void* dev_ws,
+                              size_t dev_bytes, void* stream) {
+  attn_status_t s = check_plan_common(plan, ATTN_MODE_APPEND, q, k_pool, v_pool, num_pages,
+                                      layout, kv_indptr, kv_indices, last_page_len, dtype, o,
+                                      dev_ws, dev_bytes, "attn_append_run");
+  if (s != ATTN_OK) return s;
+  if ((causal ? 1 : 0) != plan->causal)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_append_run: causal differs from the plan's");
+  if (plan->batch > 0 && !qo_indptr)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_append_run: qo_indptr is NULL");
+  if (layout != ATTN_LAYOUT_HND)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_append_run: only the HND layout is implemented");
+  if (plan->page_size % 16 != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_append_run: page_size must be a multiple of 16");
+  if (plan->batch == 0 || plan->total_qo == 0) return ATTN_OK;
+  AppendArgs a;
+  a.q = q;
+  a.qo_indptr = qo_indptr;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.num_pages = num_pages;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.last_page_len = last_page_len;
+  a.o = o;
+  a.lse = lse;
+  a.ws = ws_view(*plan, dev_ws);
+  a.num_ctas = plan->num_ctas;
+  a.num_units = plan->num_units;
+  a.num_split_items = plan->num_split_items;
+  a.dtype = dtype;
+  a.page_size = plan->page_size;
+  a.num_qo_heads = plan->num_qo_heads;
+  a.num_kv_heads = plan->num_kv_heads;
+  a.group = plan->num_qo_heads / plan->num_kv_heads;
+  a.q_tile = plan->q_tile;
+  a.total_qo = plan->total_qo;
+  a.causal = plan->causal;
+  a.sm_scale = sm_scale;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* msg = "";
+  cudaError_t e = launch_append(a, st, &msg);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: append kernel launch");
+  if (plan->num_split_items > 0) {
+    SplitMergeArgs m;
+    m.ws = a.ws;
+    m.num_split_items = plan->num_split_items;
+    m.rows_per_item = plan->rows_per_item;
+    m.group = a.group;
+    m.q_tile = plan->q_tile;
+    m.num_qo_heads = plan->num_qo_heads;
+    m.qo_indptr = qo_indptr;
+    m.o = o;
+    m.lse = lse;
+    m.dtype = dtype;
+    e = launch_split_merge(m, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: merge kernel launch");
+  }
+  return ATTN_OK;
+}
+
+attn_status_t attn_merge_states(const void* o_a, const float* lse_a, const void* o_b,
+                                const float* lse_b, void* o_out, float* lse_out, int32_t n,
+                                int32_t num_heads, int32_t head_dim, int32_t dtype,
+                                void* stream) {
+  if (n < 0 || num_heads < 1 || head_dim < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_merge_states: sizes must be positive");
+  if (head_dim % 8 != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_merge_states: head_dim must be a multiple of 8");
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_merge_states: dtype must be ATTN_F16 or ATTN_BF16");
+  if (n == 0) return ATTN_OK;
+  if (!o_a || !o_b || !lse_a || !lse_b || !o_out)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_merge_states: null device pointer");
+  if ((reinterpret_cast<uintptr_t>(o_a) | reinterpret_cast<uintptr_t>(o_b) |
+       reinterpret_cast<uintptr_t>(o_out)) & 15)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_merge_states: o pointers must be 16-byte aligned");
+  cudaError_t e = launch_merge_states(o_a, lse_a, o_b, lse_b, o_out, lse_out,
+                                      int64_t(n) * num_heads, head_dim, dtype,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_merge_states: launch");
+  return ATTN_OK;
+}
+
+attn_status_t attn_workspace_status(const void* dev_ws, void* stream, int32_t* code_out) {
+  if (!dev_ws || !code_out)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_workspace_status: null pointer");
+  int32_t code = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_workspace_status: stream");
+  e = cudaMemcpy(&code, dev_ws, sizeof code, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_workspace_status: read");
+  *code_out = code;
+  if (code != 0) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "a kernel gave up a bounded wait (code 0x%x)", code);
+    return fail(ATTN_ERR_TIMEOUT, buf);
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

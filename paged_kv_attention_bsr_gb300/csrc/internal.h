@@ -1,0 +1,156 @@
+// internal.h -- data shared between the host planner, the C ABI and the
+// kernels of libattn.so (not part of the public interface).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+constexpr int kHeadDim = 128;
+constexpr int kTileRows = 128;      // packed query rows of one append tile
+constexpr int kMaxDecodeGroup = 8;  // query heads per kv head, decode kernel
+constexpr int kUnitInts = 8;        // int32 words per work-unit record
+constexpr int64_t kHeaderBytes = 256;
+
+// One work unit of the plan (32 bytes, 16-byte aligned in the workspace).
+struct Unit {
+  int32_t r;      // request
+  int32_t hk;     // kv head
+  int32_t t;      // query tile (append) / 0 (decode)
+  int32_t p0;     // first page (index within the request's page list)
+  int32_t p1;     // one past the last page
+  int32_t slot;   // partial-state slot, -1 if the item is not split
+  int32_t split;  // split-item index, -1 if not split
+  int32_t pad;
+};
+static_assert(sizeof(Unit) == kUnitInts * 4, "unit record size");
+
+// Workspace header (first 256 bytes of the device workspace).
+struct WsHeader {
+  int32_t error;      // set by a kernel whose bounded wait expired (0 = none)
+  int32_t reserved[63];
+};
+
+inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Pointers into a device workspace, derived from a plan.
+struct WsView {
+  int32_t* error;
+  const int32_t* work_indptr;
+  const Unit* units;
+  const int32_t* merge_indptr;
+  const int4* merge_items;  // (r, hk, t, n_units)
+  float* partial_o;         // [slots, rows_per_item, D]
+  float* partial_lse;       // [slots, rows_per_item] (log2 domain)
+};
+
+inline WsView ws_view(const attn_plan_t& p, void* ws) {
+  char* b = static_cast<char*>(ws);
+  WsView v;
+  v.error = reinterpret_cast<int32_t*>(b);
+  v.work_indptr = reinterpret_cast<const int32_t*>(b + p.off_work_indptr);
+  v.units = reinterpret_cast<const Unit*>(b + p.off_units);
+  v.merge_indptr = reinterpret_cast<const int32_t*>(b + p.off_merge_indptr);
+  v.merge_items = reinterpret_cast<const int4*>(b + p.off_merge_items);
+  v.partial_o = reinterpret_cast<float*>(b + p.off_partial_o);
+  v.partial_lse = reinterpret_cast<float*>(b + p.off_partial_lse);
+  return v;
+}
+
+// ------------------------------------------------------------------ planner
+// Sizes of the tables for a given plan shape (host).
+struct PlanLayout {
+  int64_t off_work_indptr, off_units, off_merge_indptr, off_merge_items;
+  int64_t table_bytes, off_partial_o, off_partial_lse, dev_bytes;
+};
+PlanLayout plan_layout(int32_t num_ctas, int64_t num_units, int64_t num_split,
+                       int64_t num_slots, int32_t rows_per_item, int32_t head_dim);
+
+// Builds the plan tables into `host_tables` (table_bytes of them).
+// Returns ATTN_OK or an error with a message in *msg.
+attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                         const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                         int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t causal, int32_t num_ctas, void* host_tables,
+                         size_t host_bytes, attn_plan_t* plan, const char** msg);
+
+// ---------------------------------------------------------------- launchers
+struct DecodeArgs {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* last_page_len;
+  void* o;
+  float* lse;
+  WsView ws;
+  int32_t num_ctas;
+  int32_t num_units;
+  int32_t num_split_items;
+  int32_t layout;
+  int32_t dtype;
+  int32_t page_size;
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t batch;
+  float sm_scale;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+int decode_ctas_per_sm();
+
+struct AppendArgs {
+  const void* q;
+  const int32_t* qo_indptr;
+  const void* k_pool;
+  const void* v_pool;
+  int64_t num_pages;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* last_page_len;
+  void* o;
+  float* lse;
+  WsView ws;
+  int32_t num_ctas;
+  int32_t num_units;
+  int32_t num_split_items;
+  int32_t dtype;
+  int32_t page_size;
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t q_tile;
+  int32_t total_qo;
+  int32_t causal;
+  float sm_scale;
+};
+// Returns cudaErrorNotSupported for shapes the kernel does not handle.
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char** msg);
+int append_ctas_per_sm();
+
+// Merge of split items' partial states into o / lse (after a run).
+struct SplitMergeArgs {
+  WsView ws;
+  int32_t num_split_items;
+  int32_t rows_per_item;
+  int32_t group;
+  int32_t q_tile;
+  int32_t num_qo_heads;
+  const int32_t* qo_indptr;  // NULL for decode
+  void* o;
+  float* lse;
+  int32_t dtype;
+};
+cudaError_t launch_split_merge(const SplitMergeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,
+                                const float* lse_b, void* o_out, float* lse_out,
+                                int64_t rows, int32_t head_dim, int32_t dtype,
+                                cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,258 @@
+// plan.cpp -- host planning phase: balanced split of attention work over a
+// fixed persistent grid.
+//
+// FlashInfer paper digest (modb.pro), section "动态负载均衡调度": scheduling is
+// Stream-K inspired and runs in two phases -- a CPU phase that analyses the
+// length distribution and emits a work assignment, and a GPU phase whose
+// persistent kernel (fixed grid, preallocated workspace) follows it. The page
+// gives no algorithm; the cut used here:
+//   * items (request, kv head, query tile) in request-major order; an item's
+//     cost is its visible page count n plus one overhead slot;
+//   * the items' costs are laid end to end (total W) and CTA c takes the
+//     contiguous positions [floor(c W / C), floor((c+1) W / C));
+//   * an item crossed by a CTA boundary becomes several units ("split"); each
+//     writes a partial (o, lse) state and a merge combines them.
+// Every CTA gets floor(W/C) or ceil(W/C) positions and the cut adds at most
+// C - 1 units. The result depends only on the inputs and is deterministic.
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+
+namespace attn {
+
+PlanLayout plan_layout(int32_t num_ctas, int64_t num_units, int64_t num_split,
+                       int64_t num_slots, int32_t rows_per_item, int32_t head_dim) {
+  PlanLayout L;
+  int64_t at = kHeaderBytes;
+  L.off_work_indptr = at;
+  at = align_up(at + 4 * (int64_t(num_ctas) + 1), 256);
+  L.off_units = at;
+  at = align_up(at + int64_t(sizeof(Unit)) * num_units, 256);
+  L.off_merge_indptr = at;
+  at = align_up(at + 4 * (num_split + 1), 256);
+  L.off_merge_items = at;
+  at = align_up(at + 16 * num_split, 256);
+  L.table_bytes = at;
+  L.off_partial_o = at;
+  at = align_up(at + 4 * num_slots * rows_per_item * int64_t(head_dim), 256);
+  L.off_partial_lse = at;
+  at = align_up(at + 4 * num_slots * rows_per_item, 256);
+  L.dev_bytes = at;
+  return L;
+}
+
+namespace {
+
+struct Item {
+  int32_t r, hk, t, n;
+};
+
+uint64_t fnv1a(uint64_t h, const void* data, size_t bytes) {
+  const unsigned char* p = static_cast<const unsigned char*>(data);
+  for (size_t i = 0; i < bytes; ++i) {
+    h ^= p[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+}  // namespace
+
+attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                         const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                         int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t causal, int32_t num_ctas, void* host_tables,
+                         size_t host_bytes, attn_plan_t* plan, const char** msg) {
+  *msg = "";
+  if (!kv_indptr || !plan || !host_tables || (batch > 0 && !last_page_len)) {
+    *msg = "attn_plan: null pointer argument";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  if (batch < 0 || page_size < 1 || num_qo_heads < 1 || num_kv_heads < 1 || num_ctas < 1) {
+    *msg = "attn_plan: batch, page_size, head counts and num_ctas must be positive";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  if (num_qo_heads % num_kv_heads != 0) {
+    *msg = "attn_plan: num_qo_heads must be a multiple of num_kv_heads";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  if (head_dim != kHeadDim) {
+    *msg = "attn_plan: only head_dim == 128 is implemented";
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  const bool decode = (qo_indptr == nullptr);
+  const int32_t group = num_qo_heads / num_kv_heads;
+  if (decode && group > kMaxDecodeGroup) {
+    *msg = "attn_plan: decode supports num_qo_heads / num_kv_heads <= 8";
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  if (!decode && (group > kTileRows || kTileRows % group != 0)) {
+    *msg = "attn_plan: append needs num_qo_heads / num_kv_heads to divide 128";
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  const int32_t q_tile = decode ? 1 : kTileRows / group;
+  const int32_t rows_per_item = group * q_tile;
+
+  // ---- validate the table and build items
+  if (kv_indptr[0] < 0 || (!decode && qo_indptr[0] < 0)) {
+    *msg = "attn_plan: indptr arrays must start at a non-negative offset";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  std::vector<Item> items;
+  items.reserve(size_t(batch) * num_kv_heads);
+  for (int32_t r = 0; r < batch; ++r) {
+    const int64_t n_pages = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
+    if (n_pages < 0) {
+      *msg = "attn_plan: kv_indptr must be non-decreasing";
+      return ATTN_ERR_INVALID_ARG;
+    }
+    if (n_pages > 0 && (last_page_len[r] < 1 || last_page_len[r] > page_size)) {
+      *msg = "attn_plan: last_page_len must be in [1, page_size] for a request with pages";
+      return ATTN_ERR_INVALID_ARG;
+    }
+    const int64_t kv_len = n_pages > 0 ? (n_pages - 1) * page_size + last_page_len[r] : 0;
+    int64_t qo_len = 1;
+    if (!decode) {
+      qo_len = int64_t(qo_indptr[r + 1]) - qo_indptr[r];
+      if (qo_len < 0) {
+        *msg = "attn_plan: qo_indptr must be non-decreasing";
+        return ATTN_ERR_INVALID_ARG;
+      }
+      if (causal && kv_len < qo_len) {
+        *msg = "attn_plan: causal append needs kv_len >= qo_len for every request";
+        return ATTN_ERR_INVALID_ARG;
+      }
+    }
+    const int64_t tiles = decode ? 1 : (qo_len + q_tile - 1) / q_tile;
+    for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
+      for (int64_t t = 0; t < tiles; ++t) {
+        int64_t vis = kv_len;
+        if (causal && !decode) {
+          const int64_t last_row = std::min<int64_t>((t + 1) * q_tile, qo_len) - 1;
+          vis = std::min<int64_t>(kv_len, std::max<int64_t>(0, kv_len - qo_len + last_row + 1));
+        }
+        const int64_t n = (vis + page_size - 1) / page_size;
+        items.push_back({r, hk, int32_t(t), int32_t(n)});
+      }
+    }
+  }
+
+  // ---- balanced cut of the cost line
+  constexpr int64_t kAlpha = 1;
+  int64_t W = 0;
+  for (const Item& it : items) W += it.n + kAlpha;
+  const int64_t C = num_ctas;
+  auto bound = [&](int64_t c) -> int64_t { return (c * W) / C; };
+
+  std::vector<Unit> units;
+  units.reserve(items.size() + size_t(C));
+  std::vector<int32_t> cta_of;
+  cta_of.reserve(items.size() + size_t(C));
+  std::vector<int32_t> first_unit(items.size() + 1, 0);
+
+  int64_t c = 0;
+  int64_t base = 0;
+  for (size_t k = 0; k < items.size(); ++k) {
+    const Item& it = items[k];
+    const int64_t w = it.n + kAlpha;
+    first_unit[k] = int32_t(units.size());
+    while (c + 1 < C && bound(c + 1) <= base) ++c;  // CTA owning position `base`
+    for (int64_t cc = c; cc < C && bound(cc) < base + w; ++cc) {
+      const int64_t lo = bound(cc), hi = bound(cc + 1);
+      if (hi <= lo) continue;
+      if (it.n == 0) {
+        if (lo <= base && base < hi) {
+          units.push_back({it.r, it.hk, it.t, 0, 0, -1, -1, 0});
+          cta_of.push_back(int32_t(cc));
+        }
+        continue;
+      }
+      const int64_t p0 = std::max<int64_t>(0, lo - base - kAlpha);
+      const int64_t p1 = std::min<int64_t>(it.n, hi - base - kAlpha);
+      if (p1 > p0) {
+        units.push_back({it.r, it.hk, it.t, int32_t(p0), int32_t(p1), -1, -1, 0});
+        cta_of.push_back(int32_t(cc));
+      }
+    }
+    base += w;
+  }
+  first_unit[items.size()] = int32_t(units.size());
+
+  // ---- split items, slots in (item, page) order
+  std::vector<int32_t> merge_indptr(1, 0);
+  std::vector<int4> merge_items;
+  int32_t slots = 0;
+  for (size_t k = 0; k < items.size(); ++k) {
+    const int32_t a = first_unit[k], b = first_unit[k + 1];
+    if (b - a < 2) continue;
+    const int32_t split_id = int32_t(merge_items.size());
+    for (int32_t u = a; u < b; ++u) {
+      units[u].slot = slots++;
+      units[u].split = split_id;
+    }
+    merge_items.push_back(make_int4(items[k].r, items[k].hk, items[k].t, b - a));
+    merge_indptr.push_back(slots);
+  }
+
+  // ---- per-CTA offsets (units are already in CTA order)
+  std::vector<int32_t> work_indptr(size_t(C) + 1, 0);
+  for (int32_t cc : cta_of) work_indptr[size_t(cc) + 1]++;
+  for (int64_t i = 0; i < C; ++i) work_indptr[i + 1] += work_indptr[i];
+  int64_t max_load = 0;
+  for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, bound(i + 1) - bound(i));
+
+  // ---- write tables
+  const int64_t S = int64_t(merge_items.size());
+  const PlanLayout L = plan_layout(num_ctas, int64_t(units.size()), S, slots, rows_per_item,
+                                   head_dim);
+  if (size_t(L.table_bytes) > host_bytes) {
+    *msg = "attn_plan: pinned host workspace too small for the plan tables";
+    return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  }
+  char* hb = static_cast<char*>(host_tables);
+  std::memset(hb, 0, size_t(L.table_bytes));
+  std::memcpy(hb + L.off_work_indptr, work_indptr.data(), 4 * work_indptr.size());
+  if (!units.empty()) std::memcpy(hb + L.off_units, units.data(), sizeof(Unit) * units.size());
+  std::memcpy(hb + L.off_merge_indptr, merge_indptr.data(), 4 * merge_indptr.size());
+  if (S) std::memcpy(hb + L.off_merge_items, merge_items.data(), 16 * size_t(S));
+
+  attn_plan_t p;
+  std::memset(&p, 0, sizeof p);
+  p.mode = decode ? ATTN_MODE_DECODE : ATTN_MODE_APPEND;
+  p.batch = batch;
+  p.page_size = page_size;
+  p.num_qo_heads = num_qo_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.causal = decode ? 0 : (causal ? 1 : 0);
+  p.num_ctas = num_ctas;
+  p.q_tile = q_tile;
+  p.rows_per_item = rows_per_item;
+  p.num_items = int32_t(items.size());
+  p.num_units = int32_t(units.size());
+  p.num_split_items = int32_t(S);
+  p.num_slots = slots;
+  p.total_qo = decode ? batch : (qo_indptr[batch] - qo_indptr[0]);
+  p.total_weight = W;
+  p.max_cta_weight = max_load;
+  p.off_work_indptr = L.off_work_indptr;
+  p.off_units = L.off_units;
+  p.off_merge_indptr = L.off_merge_indptr;
+  p.off_merge_items = L.off_merge_items;
+  p.off_partial_o = L.off_partial_o;
+  p.off_partial_lse = L.off_partial_lse;
+  p.table_bytes = L.table_bytes;
+  p.dev_bytes_needed = L.dev_bytes;
+  uint64_t h = 1469598103934665603ull;
+  h = fnv1a(h, kv_indptr, 4 * (size_t(batch) + 1));
+  if (batch) h = fnv1a(h, last_page_len, 4 * size_t(batch));
+  if (!decode) h = fnv1a(h, qo_indptr, 4 * (size_t(batch) + 1));
+  const int32_t shape[6] = {page_size, num_qo_heads, num_kv_heads, head_dim, p.causal, num_ctas};
+  p.fingerprint = fnv1a(h, shape, sizeof shape);
+  *plan = p;
+  return ATTN_OK;
+}
+
+}  // namespace attn

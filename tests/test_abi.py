@@ -1,0 +1,77 @@
+"""The C-ABI library loads and exports every symbol include/attn.h declares;
+host-side validation answers with status codes before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("attn_plan", "attn_decode_run", "attn_append_run", "attn_merge_states"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    lib = ctypes.CDLL(C.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) == set(C.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", C.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    for name in _declared():
+        assert re.search(rf"\bT {name}\b", out), name
+
+
+def test_workspace_size_and_validation_without_gpu():
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    dev, host = C.workspace_size(64, 64, 32, 8, 128, 304)
+    assert dev > host > 0 and dev % 256 == 0
+    with pytest.raises(C.AttnError) as ei:
+        C.workspace_size(0, 1, 32, 8, 128, 304)
+    assert ei.value.status == C.ERR_INVALID_ARG
+    with pytest.raises(C.AttnError) as ei:
+        C.workspace_size(1, 1, 32, 8, 96, 304)
+    assert ei.value.status == C.ERR_UNSUPPORTED
+    # run calls validate before touching CUDA: wrong mode, null workspace
+    buf = np.zeros(host, np.uint8)
+    p = C.plan(None, np.array([0, 1], np.int32), np.array([5], np.int32), 16, 32, 8, 128,
+               False, 304, buf)
+    st = C.lib.attn_append_run(ctypes.byref(p), None, None, None, None, 0, 0, None, None, None,
+                               1, 0, ctypes.c_float(1.0), None, None, None, 0, None)
+    assert st == C.ERR_INVALID_ARG
+    st = C.lib.attn_decode_run(ctypes.byref(p), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                               ctypes.c_void_p(16), 1, 0, ctypes.c_void_p(16),
+                               ctypes.c_void_p(16), ctypes.c_void_p(16), 1,
+                               ctypes.c_float(1.0), ctypes.c_void_p(16), None, None, 0, None)
+    assert st == C.ERR_INVALID_ARG and "dev_ws" in C.last_error()
+    st = C.lib.attn_decode_run(ctypes.byref(p), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                               ctypes.c_void_p(16), 1, 0, ctypes.c_void_p(16),
+                               ctypes.c_void_p(16), ctypes.c_void_p(16), 1,
+                               ctypes.c_float(1.0), ctypes.c_void_p(16), None,
+                               ctypes.c_void_p(256), 16, None)
+    assert st == C.ERR_WORKSPACE_TOO_SMALL
+    st = C.lib.attn_merge_states(None, None, None, None, None, None, 4, 2, 100, 1, None)
+    assert st == C.ERR_UNSUPPORTED
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_attention_bsr_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cpp", ".h", ".cuh")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "attn_oracle" not in text, f

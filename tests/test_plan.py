@@ -1,0 +1,190 @@
+"""The library's C++ planner against the reference partitioner (bit-exact) and
+against the properties the balanced cut must have. Host only: no GPU."""
+import numpy as np
+import pytest
+
+from oracle import plan_ref
+
+C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+
+
+def _tables(p, buf):
+    raw = np.frombuffer(buf.tobytes(), dtype=np.int32)
+
+    def at(off, n):
+        return raw[off // 4: off // 4 + n]
+
+    units = at(p.off_units, 8 * p.num_units).reshape(-1, 8)
+    return {
+        "work_indptr": at(p.off_work_indptr, p.num_ctas + 1).tolist(),
+        "units": units,
+        "merge_indptr": at(p.off_merge_indptr, p.num_split_items + 1).tolist(),
+        "merge_items": at(p.off_merge_items, 4 * p.num_split_items).reshape(-1, 4),
+    }
+
+
+def _lib_plan(kv_indptr, last, P, Hq, Hk, ctas, qo_indptr=None, causal=False):
+    B = len(kv_indptr) - 1
+    total_qo = int(qo_indptr[-1]) if qo_indptr is not None else B
+    _, host = C.workspace_size(max(B, 1), max(total_qo, 1), Hq, Hk, 128, ctas)
+    buf = np.zeros(host, np.uint8)
+    p = C.plan(qo_indptr, kv_indptr, last, P, Hq, Hk, 128, causal, ctas, buf)
+    return p, _tables(p, buf), buf
+
+
+def _random_case(rng, decode):
+    B = int(rng.integers(0, 40))
+    P = int(rng.choice([1, 3, 16, 128]))
+    Hk = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    kv_lens = rng.integers(0, 3000, size=B)
+    if B and rng.random() < 0.3:
+        kv_lens[rng.integers(0, B)] = 0
+    n = (kv_lens + P - 1) // P
+    kv_indptr = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    last = np.where(n > 0, kv_lens - P * (n - 1), 0).astype(np.int32)
+    qo = None
+    causal = False
+    if not decode:
+        causal = bool(rng.random() < 0.6)
+        qo_lens = np.minimum(rng.integers(0, 600, size=B), kv_lens) if causal else \
+            rng.integers(0, 600, size=B)
+        qo = np.concatenate([[0], np.cumsum(qo_lens)]).astype(np.int32)
+    ctas = int(rng.choice([1, 2, 7, 152, 304, 5000]))
+    return kv_indptr, last, P, Hk * g, Hk, ctas, qo, causal
+
+
+@pytest.mark.parametrize("decode", [True, False])
+def test_plan_bit_exact_vs_reference(decode):
+    rng = np.random.default_rng(20260002 if decode else 20260005)
+    for _ in range(60):
+        kv_indptr, last, P, Hq, Hk, ctas, qo, causal = _random_case(rng, decode)
+        p, t, _ = _lib_plan(kv_indptr, last, P, Hq, Hk, ctas, qo, causal)
+        ref = plan_ref.make_plan(kv_indptr.tolist(), last.tolist(), P, Hq, Hk, ctas,
+                                 qo_indptr=None if qo is None else qo.tolist(), causal=causal)
+        assert t["work_indptr"] == ref.work_indptr
+        u = t["units"]
+        assert u[:, 0].tolist() == ref.unit_r
+        assert u[:, 1].tolist() == ref.unit_hk
+        assert u[:, 2].tolist() == ref.unit_t
+        assert u[:, 3].tolist() == ref.unit_p0
+        assert u[:, 4].tolist() == ref.unit_p1
+        assert u[:, 5].tolist() == ref.unit_slot
+        assert t["merge_indptr"] == ref.merge_indptr
+        mi = t["merge_items"]
+        assert mi[:, 0].tolist() == ref.merge_r
+        assert mi[:, 1].tolist() == ref.merge_hk
+        assert mi[:, 2].tolist() == ref.merge_t
+        assert p.total_weight == ref.total_weight
+        assert p.num_items == ref.num_items
+        assert p.q_tile == ref.q_tile
+
+
+def _pages_of_items(kv_indptr, last, P, Hk, g, qo, causal):
+    items = {}
+    B = len(kv_indptr) - 1
+    tq = 1 if qo is None else 128 // g
+    for r in range(B):
+        kv_len = plan_ref.kv_length(kv_indptr, last, P, r)
+        qo_len = 1 if qo is None else qo[r + 1] - qo[r]
+        tiles = 1 if qo is None else -(-qo_len // tq)
+        for hk in range(Hk):
+            for t in range(tiles):
+                vis = kv_len
+                if causal and qo is not None:
+                    vis = min(kv_len, kv_len - qo_len + min((t + 1) * tq, qo_len))
+                items[(r, hk, t)] = -(-vis // P)
+    return items
+
+
+@pytest.mark.parametrize("decode", [True, False])
+def test_plan_properties(decode):
+    rng = np.random.default_rng(7 + decode)
+    for _ in range(60):
+        kv_indptr, last, P, Hq, Hk, ctas, qo, causal = _random_case(rng, decode)
+        p, t, buf = _lib_plan(kv_indptr, last, P, Hq, Hk, ctas, qo, causal)
+        items = _pages_of_items(kv_indptr.tolist(), last.tolist(), P, Hk, Hq // Hk,
+                                None if qo is None else qo.tolist(), causal)
+        u = t["units"]
+        # exact coverage: every page of every item exactly once, in order
+        covered = {}
+        for row in u:
+            key = (int(row[0]), int(row[1]), int(row[2]))
+            covered.setdefault(key, []).append((int(row[3]), int(row[4])))
+        assert set(covered) == set(items)
+        for key, n in items.items():
+            segs = sorted(covered[key])
+            if n == 0:
+                assert segs == [(0, 0)]
+                continue
+            assert segs[0][0] == 0 and segs[-1][1] == n
+            for (a0, a1), (b0, b1) in zip(segs, segs[1:]):
+                assert a1 == b0 and a0 < a1
+        # balance: the page share of every CTA is at most ceil(W / C)
+        W = p.total_weight
+        wi = t["work_indptr"]
+        cap = -(-W // ctas)
+        for c in range(ctas):
+            pages = int((u[wi[c]:wi[c + 1], 4] - u[wi[c]:wi[c + 1], 3]).sum())
+            assert pages <= cap
+        assert p.max_cta_weight <= cap
+        # the cut adds at most C - 1 units; split items carry slots in order
+        assert p.num_units - p.num_items <= ctas - 1
+        assert p.num_split_items <= ctas - 1
+        slots = [int(s) for s in u[:, 5] if s >= 0]
+        assert slots == list(range(len(slots)))
+        assert p.num_slots == len(slots)
+        # identical bytes run to run
+        p2, _, buf2 = _lib_plan(kv_indptr, last, P, Hq, Hk, ctas, qo, causal)
+        assert bytes(buf[:p.table_bytes]) == bytes(buf2[:p2.table_bytes])
+        assert p.fingerprint == p2.fingerprint
+
+
+def test_plan_skewed_workload_balance():
+    """The skewed 70B-shaped batch: 4 x 32k + 124 lognormal requests."""
+    from paged_kv_attention_bsr_gb300 import synth
+    rng = np.random.default_rng(20260003)
+    lens = synth.skewed_lengths(rng)
+    n = (lens + 15) // 16
+    kv_indptr = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    last = (lens - 16 * (n - 1)).astype(np.int32)
+    p, t, _ = _lib_plan(kv_indptr, last, 16, 64, 8, 304)
+    assert p.max_cta_weight - p.total_weight // 304 <= 1
+    assert p.num_units <= p.num_items + 303
+
+
+@pytest.mark.parametrize("bad", ["heads", "lpl_zero", "lpl_big", "indptr", "causal_short",
+                                 "head_dim", "group", "pinned"])
+def test_plan_rejects_bad_input(bad):
+    kv_indptr = np.array([0, 2, 5], np.int32)
+    last = np.array([3, 16], np.int32)
+    qo = None
+    Hq, Hk, D, P, causal = 8, 2, 128, 16, False
+    host = 1 << 20
+    want = C.ERR_INVALID_ARG
+    if bad == "heads":
+        Hq = 6
+        Hk = 4
+    elif bad == "lpl_zero":
+        last = np.array([0, 16], np.int32)
+    elif bad == "lpl_big":
+        last = np.array([17, 16], np.int32)
+    elif bad == "indptr":
+        kv_indptr = np.array([0, 5, 2], np.int32)
+    elif bad == "causal_short":
+        qo = np.array([0, 40, 41], np.int32)
+        causal = True
+    elif bad == "head_dim":
+        D = 64
+        want = C.ERR_UNSUPPORTED
+    elif bad == "group":
+        Hq, Hk = 32, 2
+        want = C.ERR_UNSUPPORTED
+    elif bad == "pinned":
+        host = 64
+        want = C.ERR_WORKSPACE_TOO_SMALL
+    buf = np.zeros(host, np.uint8)
+    with pytest.raises(C.AttnError) as ei:
+        C.plan(qo, kv_indptr, last, P, Hq, Hk, D, causal, 16, buf)
+    assert ei.value.status == want
+    assert C.last_error()
