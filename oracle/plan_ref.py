@@ -6,9 +6,11 @@ analyses the length distribution on the CPU and assigns work units to SMs so
 that a fixed-grid persistent kernel can follow the plan). The digest gives no
 pseudo-code; the exact cut below is the reading used throughout this project:
 
-  items      (request r, kv head hk, query tile t), r-major, then hk, then t;
+  items      (request r, query tile t, kv head hk), r-major, then t, then hk;
              decode has one tile per request, append tiles hold
-             tq = 128 // group query tokens (group heads x tq tokens <= 128 rows)
+             tq = 128 // group query tokens (group heads x tq tokens <= 128 rows).
+             Neighbouring CTAs thus work on the same kv head of a request at
+             the same time, so its K/V pages are shared through L2.
   pages      n = ceil(vis / P), vis = visible kv length of the tile's last row
              (the whole kv_len unless causal)
   weights    w = n + alpha (alpha = 1 overhead slot); prefix sums in int64,
@@ -71,8 +73,8 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
         kv_len = kv_length(kv_indptr, last_page_len, page_size, r)
         qo_len = 1 if decode else qo_indptr[r + 1] - qo_indptr[r]
         tiles = 1 if decode else -(-qo_len // tq)
-        for hk in range(num_kv_heads):
-            for t in range(tiles):
+        for t in range(tiles):
+            for hk in range(num_kv_heads):
                 vis = kv_len
                 if causal and not decode:
                     last_row = min((t + 1) * tq, qo_len) - 1

@@ -6,8 +6,10 @@
 // length distribution and emits a work assignment, and a GPU phase whose
 // persistent kernel (fixed grid, preallocated workspace) follows it. The page
 // gives no algorithm; the cut used here:
-//   * items (request, kv head, query tile) in request-major order; an item's
-//     cost is its visible page count n plus one overhead slot;
+//   * items (request, query tile, kv head) in request-major order, then tile,
+//     then kv head (so CTAs that run side by side read the same kv head's
+//     pages and share them through L2); an item's cost is its visible page
+//     count n plus one overhead slot;
 //   * the items' costs are laid end to end (total W) and CTA c takes the
 //     contiguous positions [floor(c W / C), floor((c+1) W / C));
 //   * an item crossed by a CTA boundary becomes several units ("split"); each
@@ -126,8 +128,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
       }
     }
     const int64_t tiles = decode ? 1 : (qo_len + q_tile - 1) / q_tile;
-    for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
-      for (int64_t t = 0; t < tiles; ++t) {
+    for (int64_t t = 0; t < tiles; ++t) {
+      for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
         int64_t vis = kv_len;
         if (causal && !decode) {
           const int64_t last_row = std::min<int64_t>((t + 1) * q_tile, qo_len) - 1;
