@@ -126,8 +126,8 @@ attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_c
  * each item weighs its page count + 1; CTA c takes the weight positions
  * [floor(c W / C), floor((c+1) W / C)) of the total W; an item cut by a CTA
  * boundary is "split" and its units write partial states that the run merges).
- *   qo_indptr_h     : host int32[batch+1] query row offsets (append), or NULL
- *                     for decode (one row per request)
+ *   qo_indptr_h     : host int32[batch+1] query row offsets (append, starting
+ *                     at 0), or NULL for decode (one row per request)
  *   kv_indptr_h     : host int32[batch+1] page offsets into kv_indices
  *   last_page_len_h : host int32[batch]; 1..page_size when the request has pages
  *   causal          : 1 = query row i of a request with qo_len rows sees kv

@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -62,7 +63,7 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-struct __align__(64) AppendParams {
+struct AppendParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
@@ -389,7 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       float m_ref = -INFINITY, l = 0.f;
       for (int i = 0; i < g.ntiles; ++i, ++jt) {
         const int sb = jt & 1;
-        if (!mbar_wait(smem_u32(&bars.s_full[sb]), (jt >> 1) & 1u, err, ERR_WAIT_MMA)) {
+        // waits are made warp-uniform: tcgen05.ld/st below are .sync.aligned
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bars.s_full[sb]), (jt >> 1) & 1u, err, ERR_WAIT_MMA))) {
           ok = false;
           break;
         }
@@ -422,21 +425,26 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
           l *= alpha;
           m_ref = m_tile;
         }
+        // probabilities, packed to the MMA input type right away (2 per word)
         float lsum = 0.f;
+        uint32_t pk[kTile / 2];
         if (m_ref != -INFINITY) {
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) {
-            s[c] = ex2(fmaf(s[c], c2, -m_ref));
-            lsum += s[c];
+          for (int c = 0; c < kTile; c += 2) {
+            const float p0 = ex2(fmaf(s[c], c2, -m_ref));
+            const float p1 = ex2(fmaf(s[c + 1], c2, -m_ref));
+            lsum += p0 + p1;
+            pk[c / 2] = pack2<BF16>(p0, p1);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) s[c] = 0.f;
+          for (int c = 0; c < kTile / 2; ++c) pk[c] = 0u;
         }
         l += lsum;
         // P_{j-1}'s MMA must be done before P is overwritten and O rescaled.
         if (i > 0) {
-          if (!mbar_wait(smem_u32(&bars.o_done), (jt - 1) & 1u, err, ERR_WAIT_MMA)) {
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bars.o_done), (jt - 1) & 1u, err, ERR_WAIT_MMA))) {
             ok = false;
             break;
           }
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         }
         // warp-uniform: tcgen05.ld/st are .sync.aligned
         if (__any_sync(0xffffffffu, rescale_o)) {
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float o[32];
             const uint32_t ta = tmem + lane_off + kColO + c * 32;
@@ -455,16 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
             tmem_st32(ta, o);
           }
         }
-        // P row -> shared memory, bf16/fp16, 128B-swizzled K-major layout
+        // P row -> shared memory, 128B-swizzled K-major layout
 #pragma unroll
         for (int ch = 0; ch < 16; ++ch) {
           const int half = ch >> 3, cc = ch & 7;
-          uint4 v;
-          v.x = pack2<BF16>(s[ch * 8 + 0], s[ch * 8 + 1]);
-          v.y = pack2<BF16>(s[ch * 8 + 2], s[ch * 8 + 3]);
-          v.z = pack2<BF16>(s[ch * 8 + 4], s[ch * 8 + 5]);
-          v.w = pack2<BF16>(s[ch * 8 + 6], s[ch * 8 + 7]);
-          *reinterpret_cast<uint4*>(pbuf + half * kHalf + rho * 128 + ((cc ^ (rho & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(pbuf + half * kHalf + rho * 128 + ((cc ^ (rho & 7)) << 4)) =
+              make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
         }
         // kv rows past the unit's end hold whatever the pool had: zero them in V
         const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
@@ -482,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       }
       if (!ok) break;
       // ---- epilogue: O / l
-      if (!mbar_wait(smem_u32(&bars.o_done), (jt - 1) & 1u, err, ERR_WAIT_MMA)) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars.o_done), (jt - 1) & 1u, err, ERR_WAIT_MMA))) {
         ok = false;
         break;
       }

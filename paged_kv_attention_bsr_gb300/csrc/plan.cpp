@@ -98,8 +98,12 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   const int32_t rows_per_item = group * q_tile;
 
   // ---- validate the table and build items
-  if (kv_indptr[0] < 0 || (!decode && qo_indptr[0] < 0)) {
-    *msg = "attn_plan: indptr arrays must start at a non-negative offset";
+  if (kv_indptr[0] < 0) {
+    *msg = "attn_plan: kv_indptr must start at a non-negative offset";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  if (!decode && qo_indptr[0] != 0) {
+    *msg = "attn_plan: qo_indptr must start at 0 (q rows are indexed from the tensor start)";
     return ATTN_ERR_INVALID_ARG;
   }
   std::vector<Item> items;
