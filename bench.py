@@ -1,0 +1,536 @@
+#!/usr/bin/env python
+"""Benchmark of the BSR paged-KV attention path on GB300.
+
+Headline (one JSON line): paged batch decode, Llama-3.1-8B attention shape
+(B = 64, Hq = 32, Hk = 8, D = 128, bf16, page_size 16, kv_len ~ U[1024, 4096],
+pages drawn from a shuffled 20000-page pool). One step = plan() on the host
+(table upload included) + one persistent decode launch (split units merged
+in-kernel). `value` is algorithmic HBM bytes per step / step time (GB/s).
+
+The line also carries, for the other workloads of the pages (single-request
+decode, skewed 70B-shaped decode, shared-prefix composable decode, causal
+append), their own time and roofline fraction under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs independent replicas (one per GPU, launched by torchrun); the only
+collectives are the timing barrier and a max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention HBM GB/s (% of ~8 TB/s); causal append TFLOP/s (% peak)"
+L2_FLUSH_BYTES = 512 << 20  # > 2 x the 126 MB L2
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_attention_bsr_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(profile_name, kernel_sources):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel source
+    has not changed since (profiles/<name> lists the source hash)."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != source_hash(*kernel_sources):
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(f"/tmp/bench_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+            time.sleep(1.0)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.out.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        os.remove(self.out.name)
+        return rows
+
+
+def summarise_clocks(rows, t0, t1):
+    if not rows:
+        return None
+    sel = []
+    for r in rows:
+        try:
+            ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+        except Exception:
+            ts = None
+        if ts is None or (t0 - 1.0 <= ts <= t1 + 1.0):
+            sel.append(r)
+    sel = sel or rows
+    sm = [float(r[2]) for r in sel if r[2].replace(".", "").isdigit()]
+    mx = [float(r[3]) for r in sel if r[3].replace(".", "").isdigit()]
+    reasons = set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in sel:
+        for k, name in enumerate(names):
+            if "Active" in r[6 + k] and "Not" not in r[6 + k]:
+                reasons.add(name)
+    return {"sm_mhz": float(np.median(sm)) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+            "samples": len(sel)}
+
+
+def decode_bytes(w):
+    c = w.cache
+    elt = 2
+    kv = int(c.kv_lens.sum()) * 2 * w.num_kv_heads * w.head_dim * elt
+    qo = 2 * w.batch * w.num_qo_heads * w.head_dim * elt + 4 * w.batch * w.num_qo_heads
+    idx = 4 * len(c.kv_indices) + 4 * (w.batch + 1) + 4 * w.batch
+    return kv + qo + idx
+
+
+def append_flops(w):
+    qo = np.diff(w.qo_indptr).astype(np.float64)
+    E = w.cache.kv_lens.astype(np.float64) - qo
+    return float(np.sum(w.num_qo_heads * 4.0 * w.head_dim * (qo * E + qo * (qo + 1) / 2)))
+
+
+def dev_cache(cache):
+    return dict(k_pool=cache.k_pool.cuda(), v_pool=cache.v_pool.cuda(),
+                kv_indptr=torch.from_numpy(cache.kv_indptr).cuda(),
+                kv_indices=torch.from_numpy(cache.kv_indices).cuda(),
+                last_page_len=torch.from_numpy(cache.last_page_len).cuda())
+
+
+# --------------------------------------------------------------- our path
+class DecodeStep:
+    """plan + run of one decode batch through the public API."""
+
+    def __init__(self, w):
+        from paged_kv_attention_bsr_gb300.api import PagedAttention
+        self.w = w
+        c = w.cache
+        self.att = PagedAttention(w.num_qo_heads, w.num_kv_heads, w.head_dim, "decode",
+                                  max_batch=w.batch)
+        self.d = dev_cache(c)
+        self.q = w.q.cuda()
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:-1], dtype=torch.float32, device="cuda")
+
+    def plan(self):
+        c = self.w.cache
+        self.att.plan(c.kv_indptr, c.last_page_len, c.page_size)
+
+    def run(self):
+        d = self.d
+        self.att.run(self.q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"],
+                     d["last_page_len"], self.w.sm_scale, out=self.o, lse=self.lse)
+
+
+def time_steps(step_fns, steps, warmup, flush, kernel_split=1):
+    """Per-step CUDA events on the current stream. step_fns: list of callables
+    run in order; events are recorded before fn[0], before fn[kernel_split]
+    and after the last, so `kernel` times fns[kernel_split:]."""
+    for _ in range(warmup):
+        flush.zero_()
+        for f in step_fns:
+            f()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()
+        evs[k][0].record()
+        for i, f in enumerate(step_fns):
+            if i == kernel_split:
+                evs[k][1].record()
+            f()
+        if kernel_split >= len(step_fns):
+            evs[k][1].record()
+        evs[k][2].record()
+    torch.cuda.synchronize()
+    step_ms = np.array([e[0].elapsed_time(e[2]) for e in evs])
+    kern_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    return step_ms, kern_ms
+
+
+def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
+    from paged_kv_attention_bsr_gb300 import merge_state, synth
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    out = {}
+    # decode workloads
+    for key in ("single_decode", "skewed_decode"):
+        w = synth.WORKLOADS[key]()
+        st = DecodeStep(w)
+        step_ms, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
+        b = decode_bytes(w)
+        k_s = float(np.mean(kern_ms)) * 1e-3
+        out[w.name] = {"kind": "decode", "bytes": b, "kernel_us": k_s * 1e6,
+                       "step_us": float(np.mean(step_ms)) * 1e3,
+                       "GB/s": b / k_s / 1e9, "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak,
+                       "units": st.att.plan_info.num_units,
+                       "split_items": st.att.plan_info.num_split_items}
+        del st
+        torch.cuda.empty_cache()
+    # causal append
+    w = synth.causal_append()
+    c = w.cache
+    att = PagedAttention(w.num_qo_heads, w.num_kv_heads, 128, "append", max_batch=w.batch,
+                         max_total_qo=int(w.qo_indptr[-1]))
+    d = dev_cache(c)
+    q = w.q.cuda()
+    qo = torch.from_numpy(w.qo_indptr).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+
+    def plan_a():
+        att.plan(c.kv_indptr, c.last_page_len, 16, qo_indptr_h=w.qo_indptr, causal=True)
+
+    def run_a():
+        att.run(q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"], d["last_page_len"],
+                w.sm_scale, out=o, lse=lse, qo_indptr=qo)
+
+    step_ms, kern_ms = time_steps([plan_a, run_a], steps, warmup, flush)
+    fl = append_flops(w)
+    k_s = float(np.mean(kern_ms)) * 1e-3
+    out[w.name] = {"kind": "append", "flops": fl, "kernel_us": k_s * 1e6,
+                   "step_us": float(np.mean(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
+                   "roofline_frac_bf16": fl / k_s / 1e12 / bf16_peak,
+                   "units": att.plan_info.num_units, "split_items": att.plan_info.num_split_items}
+    del d, att
+    torch.cuda.empty_cache()
+    # shared-prefix composable decode (prefix append + suffix decode + merge)
+    w = synth.shared_prefix_decode()
+    pre, suf = w.extra["prefix"], w.cache
+    q = w.q.cuda()
+    dp, ds = dev_cache(pre), dev_cache(suf)
+    pqo_h = w.extra["prefix_qo_indptr"]
+    pqo = torch.from_numpy(pqo_h).cuda()
+    att_p = PagedAttention(32, 8, 128, "append", max_batch=w.extra["prompts"],
+                           max_total_qo=w.batch)
+    att_s = PagedAttention(32, 8, 128, "decode", max_batch=w.batch)
+    o_p, o_s, o_m = (torch.empty_like(q) for _ in range(3))
+    l_p, l_s, l_m = (torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+                     for _ in range(3))
+
+    def plans():
+        att_p.plan(pre.kv_indptr, pre.last_page_len, pre.page_size, qo_indptr_h=pqo_h,
+                   causal=False)
+        att_s.plan(suf.kv_indptr, suf.last_page_len, suf.page_size)
+
+    def runs():
+        att_p.run(q, dp["k_pool"], dp["v_pool"], dp["kv_indptr"], dp["kv_indices"],
+                  dp["last_page_len"], w.sm_scale, out=o_p, lse=l_p, qo_indptr=pqo)
+        att_s.run(q, ds["k_pool"], ds["v_pool"], ds["kv_indptr"], ds["kv_indices"],
+                  ds["last_page_len"], w.sm_scale, out=o_s, lse=l_s)
+        merge_state(o_p, l_p, o_s, l_s, out=o_m, lse_out=l_m)
+
+    step_ms, kern_ms = time_steps([plans, runs], steps, warmup, flush)
+    kvb = 2 * 8 * 128 * 2
+    b_pre = int(pre.kv_lens.sum()) * kvb
+    b_suf = int(suf.kv_lens.sum()) * kvb
+    b_flat = int(pre.kv_lens.sum()) * w.extra["n"] * kvb + b_suf
+    k_s = float(np.mean(kern_ms)) * 1e-3
+    out[w.name] = {"kind": "composable", "bytes": b_pre + b_suf, "flat_layout_bytes": b_flat,
+                   "kernel_us": k_s * 1e6, "step_us": float(np.mean(step_ms)) * 1e3,
+                   "GB/s": (b_pre + b_suf) / k_s / 1e9,
+                   "roofline_frac_hbm": (b_pre + b_suf) / k_s / 1e9 / hbm_peak,
+                   "launches_per_step": 3}
+    del dp, ds
+    # the same logical KV as one flat P = 16 layout (prefix pages shared by the n rows)
+    flat = synth.flat_layout_of_composable(w)
+    from paged_kv_attention_bsr_gb300.synth import Workload
+    wf = Workload("flat", "decode", torch.bfloat16, 32, 8, 128, w.sm_scale, w.q, flat)
+    st = DecodeStep(wf)
+    _, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
+    out[w.name]["flat_layout_kernel_us"] = float(np.mean(kern_ms)) * 1e3
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_oracle_baseline(w, threads):
+    """The fp64 C oracle over the whole batch, requests split across threads
+    (ctypes releases the GIL, so threads run on separate cores)."""
+    import oracle
+    c = w.cache
+    B = w.batch
+    chunks = np.array_split(np.arange(B), threads)
+    odt = oracle.BF16 if w.dtype == torch.bfloat16 else oracle.F16
+
+    def job(rs):
+        if len(rs) == 0:
+            return
+        a, b = int(rs[0]), int(rs[-1]) + 1
+        oracle.batch_attention(w.q[a:b], c.k_pool, c.v_pool, c.kv_indptr[a:b + 1],
+                               c.kv_indices, c.last_page_len[a:b], c.page_size,
+                               w.num_qo_heads, w.num_kv_heads, w.head_dim, odt, w.sm_scale)
+
+    oracle.build()
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(job, chunks))
+    return time.perf_counter() - t0
+
+
+def run_ours(args, rank, world):
+    from paged_kv_attention_bsr_gb300 import synth
+    hbm_peak, bf16_peak, peak_src = peaks()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    w = synth.uniform_gqa_decode()
+    st = DecodeStep(w)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    b = decode_bytes(w)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    step_ms, kern_ms = time_steps([st.plan, st.run], args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall1 = time.time()
+    clocks = summarise_clocks(sampler.stop(), t_wall0, t_wall1) if sampler else None
+    assert st.att.status() == 0, "a kernel reported a timeout"
+
+    step_s = float(np.mean(step_ms)) * 1e-3
+    kern_s = float(np.mean(kern_ms)) * 1e-3
+    if world > 1:
+        t = torch.tensor([step_s, kern_s], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_s, kern_s = float(t[0]), float(t[1])
+    value = b * world / step_s / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if rank == 0:
+        from paged_kv_attention_bsr_gb300.api import PagedAttention
+        c = w.cache
+        att = st.att
+        q_h = w.q.pin_memory()
+        idx_h = {k: torch.from_numpy(getattr(c, k)).pin_memory()
+                 for k in ("kv_indptr", "kv_indices", "last_page_len")}
+        idx_d = {k: torch.empty_like(v, device="cuda") for k, v in idx_h.items()}
+        q_d = torch.empty_like(q_h, device="cuda")
+        o_h = torch.empty_like(q_h).pin_memory()
+        lse_h = torch.empty(q_h.shape[:-1], dtype=torch.float32).pin_memory()
+        o_d = torch.empty_like(q_d)
+        lse_d = torch.empty(q_h.shape[:-1], dtype=torch.float32, device="cuda")
+        n_e2e = max(3, min(args.steps, 200))
+        h2d = q_h.numel() * 2 + sum(v.numel() * 4 for v in idx_h.values())
+        h2d += att.plan_info.table_bytes if att.plan_info is not None else 0
+        d2h = o_h.numel() * 2 + lse_h.numel() * 4
+
+        def e2e_step():
+            q_d.copy_(q_h, non_blocking=True)
+            for k in idx_h:
+                idx_d[k].copy_(idx_h[k], non_blocking=True)
+            att.plan(c.kv_indptr, c.last_page_len, c.page_size)
+            att.run(q_d, st.d["k_pool"], st.d["v_pool"], idx_d["kv_indptr"],
+                    idx_d["kv_indices"], idx_d["last_page_len"], w.sm_scale, out=o_d,
+                    lse=lse_d)
+            o_h.copy_(o_d, non_blocking=True)
+            lse_h.copy_(lse_d, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(3):
+            flush.zero_()
+            e2e_step()
+        tot = 0.0
+        for _ in range(n_e2e):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            tot += time.perf_counter() - t0
+        e2e = {"value": b / (tot / n_e2e) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "note": "KV pool stays resident in HBM (it is the cache); per-step inputs are "
+                       "q and the page table, outputs o and lse"}
+
+    if rank != 0:
+        return None
+    traffic = profile_traffic("decode_kernel_uniform_gqa_b64.md", ["decode.cu", "ptx.cuh"])
+    achieved = b / kern_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "num_qo_heads": 32, "num_kv_heads": 8,
+                   "head_dim": 128, "page_size": 16, "kv_len": "U[1024,4096]",
+                   "pool_pages": 20000, "total_kv_tokens": int(w.cache.kv_lens.sum()),
+                   "num_ctas": st.att.num_ctas, "step": "attn_plan + attn_decode_run",
+                   "l2": "flushed between steps (512 MB write outside the timed events); "
+                         "each step also reads 677 MB of KV, > 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)",
+                     "kernel": "decode_kernel (one launch per run)",
+                     "kernel_us": kern_s * 1e6, "algorithmic_bytes_per_launch": b},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.skip_cpu:
+        threads = max(1, min(os.cpu_count() or 1, 16))
+        secs = cpu_oracle_baseline(w, threads)
+        line["cpu_baseline"] = {"value": b / secs / 1e9, "unit": "GB/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"the whole workload (64 requests x 32 heads), one "
+                                          f"step, fp64 C oracle on {threads} threads, "
+                                          f"{secs:.1f} s"}
+    if world == 1 and not args.headline_only:
+        del st
+        torch.cuda.empty_cache()
+        line["workloads"] = extra_workloads(hbm_peak, bf16_peak, flush)
+    return line
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 oracle as it stands, timed on the host cores on the same
+    workload, metric and unit; each step is a bounded sample of (request,
+    kv head) items so that the whole run stays within a few minutes."""
+    import oracle
+    from paged_kv_attention_bsr_gb300 import synth
+    w = synth.uniform_gqa_decode()
+    c = w.cache
+    threads = max(1, min(os.cpu_count() or 1, 16))
+    oracle.build()
+    budget_s = 90.0 / max(1, args.steps + args.warmup)
+    # one item (r, hk) ~ kv_len x g x D x 3 fp64 ops; calibrate with one item
+    g = w.num_qo_heads // w.num_kv_heads
+
+    def item_job(r, hk):
+        for hh in range(g):
+            oracle.attention_row(w.q, c.k_pool, c.v_pool, c.kv_indptr, c.kv_indices,
+                                 c.last_page_len, 16, 32, 8, 128, oracle.BF16, w.sm_scale, r, 0,
+                                 hk * g + hh)
+
+    t0 = time.perf_counter()
+    item_job(0, 0)
+    per_item = max(1e-4, time.perf_counter() - t0)
+    n_items = max(1, int(budget_s * threads / per_item))
+    items = [(r, hk) for r in range(w.batch) for hk in range(w.num_kv_heads)]
+    kvb = 2 * 128 * 2
+    total_b = 0
+    total_t = 0.0
+    pos = 0
+    with cf.ThreadPoolExecutor(threads) as ex:
+        for k in range(args.steps + args.warmup):
+            sel = [items[(pos + i) % len(items)] for i in range(n_items)]
+            pos += n_items
+            t0 = time.perf_counter()
+            list(ex.map(lambda rh: item_job(*rh), sel))
+            dt = time.perf_counter() - t0
+            if k >= args.warmup:
+                total_t += dt
+                total_b += sum(int(c.kv_lens[r]) * kvb + 2 * g * 256 for r, _ in sel)
+    value = total_b / total_t / 1e9
+    sample = (f"{n_items} (request, kv head) items per step of the uniform GQA decode "
+              f"workload, fp64 C oracle on {threads} threads")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads (single, skewed, shared-prefix, append)")
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.gpus > 1 and world == 1:
+        sys.exit("for --gpus > 1 launch with torch.distributed.run (one rank per GPU)")
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -92,6 +92,7 @@ typedef struct attn_plan {
   int64_t off_units;
   int64_t off_merge_indptr;
   int64_t off_merge_items;
+  int64_t off_counters;     /* per split item arrival counters (zeroed by plan) */
   int64_t off_partial_o;
   int64_t off_partial_lse;
   int64_t table_bytes;      /* bytes [0, table_bytes) copied host -> device    */
@@ -156,8 +157,8 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
 
 /*
  * Batch decode over a paged cache (one query row per request), following a
- * decode plan. Persistent kernel with plan->num_ctas CTAs; split items are
- * merged by an LSE merge kernel in the same stream.
+ * decode plan. One persistent kernel with plan->num_ctas CTAs; the last unit
+ * of a split item to finish merges the item's partial states (LSE weights).
  *   q          : device [batch, num_qo_heads, head_dim] of `dtype`
  *   k_pool,
  *   v_pool     : device pools of num_pages pages in `layout`, `dtype`

@@ -42,7 +42,7 @@ class Plan(ctypes.Structure):
         "num_ctas", "q_tile", "rows_per_item", "num_items", "num_units", "num_split_items",
         "num_slots", "total_qo", "reserved0")] + [(n, ctypes.c_int64) for n in (
         "total_weight", "max_cta_weight", "off_work_indptr", "off_units", "off_merge_indptr",
-        "off_merge_items", "off_partial_o", "off_partial_lse", "table_bytes",
+        "off_merge_items", "off_counters", "off_partial_o", "off_partial_lse", "table_bytes",
         "dev_bytes_needed")] + [("fingerprint", ctypes.c_uint64)]
 
 

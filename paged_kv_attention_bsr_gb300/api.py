@@ -19,9 +19,11 @@ class PagedAttention:
 
     mode "decode": one query row per request (attn_decode_run).
     mode "append": ragged query rows per request (attn_append_run).
-    The plan tables go through two pinned staging buffers used alternately;
-    a buffer is reused only after its previous upload has executed.
+    The plan tables go through a ring of pinned staging buffers; a buffer is
+    reused only after its previous upload has executed.
     """
+
+    RING = 4
 
     def __init__(self, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
                  mode: str = "decode", max_batch: int = 256, max_total_qo: Optional[int] = None,
@@ -39,8 +41,9 @@ class PagedAttention:
         dev_bytes, host_bytes = C.workspace_size(max_batch, self.max_total_qo, num_qo_heads,
                                                  num_kv_heads, head_dim, self.num_ctas)
         self.dev_ws = torch.empty(dev_bytes, dtype=torch.uint8, device=self.device)
-        self._pinned = [torch.empty(host_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
-        self._events = [None, None]
+        self._pinned = [torch.empty(host_bytes, dtype=torch.uint8).pin_memory()
+                        for _ in range(self.RING)]
+        self._events = [None] * self.RING
         self._turn = 0
         self.plan_info: Optional[C.Plan] = None
 
@@ -49,7 +52,7 @@ class PagedAttention:
         if (self.mode == "decode") != (qo_indptr_h is None):
             raise ValueError("decode plans take no qo_indptr; append plans need one")
         i = self._turn
-        self._turn ^= 1
+        self._turn = (self._turn + 1) % self.RING
         if self._events[i] is not None:
             self._events[i].synchronize()
         self.plan_info = C.plan(qo_indptr_h, kv_indptr_h, last_page_len_h, page_size,

@@ -185,23 +185,8 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
   a.batch = plan->batch;
   a.sm_scale = sm_scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(a, st);
+  cudaError_t e = launch_decode(a, st);  // split items are merged inside the kernel
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: decode kernel launch");
-  if (plan->num_split_items > 0) {
-    SplitMergeArgs m;
-    m.ws = a.ws;
-    m.num_split_items = plan->num_split_items;
-    m.rows_per_item = plan->rows_per_item;
-    m.group = group;
-    m.q_tile = 1;
-    m.num_qo_heads = plan->num_qo_heads;
-    m.qo_indptr = nullptr;
-    m.o = o;
-    m.lse = lse;
-    m.dtype = dtype;
-    e = launch_split_merge(m, st);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: merge kernel launch");
-  }
   return ATTN_OK;
 }
 

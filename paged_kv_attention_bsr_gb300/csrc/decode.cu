@@ -23,7 +23,8 @@
 //  * at the end of a unit the four warps' (m, l, acc) are combined in the
 //    stage's own shared memory; unsplit items write o / lse directly, split
 //    items write an fp32 partial state (o, log2-LSE) to the workspace slot
-//    the plan assigned, merged afterwards by the split-merge kernel;
+//    the plan assigned; the last of an item's units to finish (an atomic
+//    arrival count in the workspace) merges them, so a run is one launch;
 //  * every wait is bounded (ptx.cuh) and reports through the workspace
 //    error word instead of hanging.
 #include <cuda_bf16.h>
@@ -117,7 +118,7 @@ __device__ __forceinline__ float reduce_heads16(float (&v)[GM], int li) {
 }
 
 struct Geo {
-  int32_t r, hk, slot, page_base;
+  int32_t r, hk, slot, split, page_base;
   int64_t tok_begin;
   int32_t ntok, nst;
 };
@@ -130,6 +131,7 @@ __device__ __forceinline__ Geo unit_geo(const DecodeArgs& a, int ui) {
   g.r = x.x;
   g.hk = x.y;
   g.slot = y.y;
+  g.split = y.z;
   const int32_t pb = __ldg(a.kv_indptr + g.r);
   const int64_t n = int64_t(__ldg(a.kv_indptr + g.r + 1)) - pb;
   const int64_t kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
@@ -404,6 +406,49 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             const int64_t row = int64_t(g.slot) * group + h;
             a.ws.partial_o[row * kHeadDim + d] = out;
             if (d == 0) a.ws.partial_lse[row] = lse2;
+          }
+        }
+        if (g.slot >= 0) {
+          // Split item: the last of its units to finish merges every partial
+          // state (log-sum-exp weights) and resets the item's counter.
+          __threadfence();
+          mbar_arrive(cbar);
+          if (!mbar_wait(cbar, cph, err, ERR_WAIT_CONSUMER)) return;
+          cph ^= 1u;
+          volatile int* last_flag = reinterpret_cast<volatile int*>(ml + 2 * kConsumerWarps * GM);
+          if (threadIdx.x == 0) {
+            const int4 mi = __ldg(a.ws.merge_items + g.split);
+            const int old = atomicAdd(a.ws.counters + g.split, 1);
+            *last_flag = (old == mi.w - 1) ? 1 : 0;
+          }
+          mbar_arrive(cbar);
+          if (!mbar_wait(cbar, cph, err, ERR_WAIT_CONSUMER)) return;
+          cph ^= 1u;
+          if (*last_flag) {
+            __threadfence();
+            const int s0 = __ldg(a.ws.merge_indptr + g.split);
+            const int s1 = __ldg(a.ws.merge_indptr + g.split + 1);
+            for (int h = 0; h < group; ++h) {
+              float M = -INFINITY;
+              for (int sl = s0; sl < s1; ++sl)
+                M = fmaxf(M, __ldcg(a.ws.partial_lse + int64_t(sl) * group + h));
+              float out = 0.f, lse2 = -INFINITY;
+              if (M != -INFINITY) {
+                float L = 0.f, acc_d = 0.f;
+                for (int sl = s0; sl < s1; ++sl) {
+                  const int64_t prow = int64_t(sl) * group + h;
+                  const float f = ex2(__ldcg(a.ws.partial_lse + prow) - M);
+                  L += f;
+                  acc_d += f * __ldcg(a.ws.partial_o + prow * kHeadDim + d);
+                }
+                out = acc_d / L;
+                lse2 = M + lg2(L);
+              }
+              const int64_t row = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * group + h;
+              store_out<BF16>(a.o, row * kHeadDim + d, out);
+              if (d == 0 && a.lse) a.lse[row] = lse2 * kLn2;
+            }
+            if (threadIdx.x == 0) a.ws.counters[g.split] = 0;
           }
         }
         fence_proxy_async_smem();  // generic writes above precede later bulk copies

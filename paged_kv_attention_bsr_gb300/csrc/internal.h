@@ -44,6 +44,7 @@ struct WsView {
   const Unit* units;
   const int32_t* merge_indptr;
   const int4* merge_items;  // (r, hk, t, n_units)
+  int32_t* counters;        // arrivals per split item (0 between runs)
   float* partial_o;         // [slots, rows_per_item, D]
   float* partial_lse;       // [slots, rows_per_item] (log2 domain)
 };
@@ -56,6 +57,7 @@ inline WsView ws_view(const attn_plan_t& p, void* ws) {
   v.units = reinterpret_cast<const Unit*>(b + p.off_units);
   v.merge_indptr = reinterpret_cast<const int32_t*>(b + p.off_merge_indptr);
   v.merge_items = reinterpret_cast<const int4*>(b + p.off_merge_items);
+  v.counters = reinterpret_cast<int32_t*>(b + p.off_counters);
   v.partial_o = reinterpret_cast<float*>(b + p.off_partial_o);
   v.partial_lse = reinterpret_cast<float*>(b + p.off_partial_lse);
   return v;
@@ -64,7 +66,7 @@ inline WsView ws_view(const attn_plan_t& p, void* ws) {
 // ------------------------------------------------------------------ planner
 // Sizes of the tables for a given plan shape (host).
 struct PlanLayout {
-  int64_t off_work_indptr, off_units, off_merge_indptr, off_merge_items;
+  int64_t off_work_indptr, off_units, off_merge_indptr, off_merge_items, off_counters;
   int64_t table_bytes, off_partial_o, off_partial_lse, dev_bytes;
 };
 PlanLayout plan_layout(int32_t num_ctas, int64_t num_units, int64_t num_split,

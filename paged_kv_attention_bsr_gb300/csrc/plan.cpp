@@ -36,6 +36,8 @@ PlanLayout plan_layout(int32_t num_ctas, int64_t num_units, int64_t num_split,
   at = align_up(at + 4 * (num_split + 1), 256);
   L.off_merge_items = at;
   at = align_up(at + 16 * num_split, 256);
+  L.off_counters = at;
+  at = align_up(at + 4 * num_split, 256);
   L.table_bytes = at;
   L.off_partial_o = at;
   at = align_up(at + 4 * num_slots * rows_per_item * int64_t(head_dim), 256);
@@ -247,6 +249,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   p.off_units = L.off_units;
   p.off_merge_indptr = L.off_merge_indptr;
   p.off_merge_items = L.off_merge_items;
+  p.off_counters = L.off_counters;
   p.off_partial_o = L.off_partial_o;
   p.off_partial_lse = L.off_partial_lse;
   p.table_bytes = L.table_bytes;
