@@ -227,6 +227,45 @@ attn_status_t attn_merge_states(const void* o_a, const float* lse_a,
  */
 attn_status_t attn_workspace_status(const void* dev_ws, void* stream, int32_t* code_out);
 
+/*
+ * Batch decode for callers that cannot allocate device memory. The paper has
+ * no counterpart: this is a deployment convenience of this library.
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocator when it
+ * runs attention -- e.g. inside an allocator-free region of a serving engine,
+ * a plugin whose host application owns every device allocation, or a
+ * latency-critical path that must not take allocator locks or grow a memory
+ * pool. Such callers cannot provide the workspaces attn_plan and
+ * attn_decode_run need, so this entry point plans and runs in one call using
+ * a fixed 4 MiB scratch area that lives in the library's own device memory
+ * (a file-scope __device__ array held on every device that loads the library
+ * until the process exits). It calls no cudaMalloc, cudaFree or allocating
+ * routine.
+ *   kv_indptr_h, last_page_len_h : host copies of the page table (as attn_plan)
+ *   other arguments              : as attn_decode_run (device inputs/outputs,
+ *                                  q [batch, num_qo_heads, head_dim], ...)
+ * Behaviour:
+ *  - The first call on a device looks up the scratch array's address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls share the one scratch area (and one host staging area), which
+ *    keeps the previous call's contents; each call re-initialises what must
+ *    start at zero. Calls whose work overlaps on the GPU race with each other;
+ *    calls ordered on one stream are safe. Host calls are serialised.
+ *  - Batches whose plan tables and partial states exceed 4 MiB (roughly more
+ *    than 16k (request, kv head) pairs) return ATTN_ERR_WORKSPACE_TOO_SMALL
+ *    before any GPU work; use attn_plan + attn_decode_run instead.
+ * Errors: as attn_plan and attn_decode_run.
+ */
+attn_status_t attn_decode_run_noalloc(const int32_t* kv_indptr_h,
+                                      const int32_t* last_page_len_h, int32_t batch,
+                                      int32_t page_size, int32_t num_qo_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, const void* q,
+                                      const void* k_pool, const void* v_pool,
+                                      int64_t num_pages, int32_t layout,
+                                      const int32_t* kv_indptr, const int32_t* kv_indices,
+                                      const int32_t* last_page_len, int32_t dtype,
+                                      float sm_scale, void* o, float* lse, void* stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* attn_last_error(void);
 

@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_S
 
 # Every symbol include/attn.h declares (checked by the tests).
 EXPORTS = ("attn_workspace_size", "attn_default_num_ctas", "attn_plan", "attn_decode_run",
-           "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error")
+           "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error",
+           "attn_decode_run_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -66,6 +67,8 @@ def _load():
                             vp, vp, sz, vp],
         "attn_merge_states": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp],
         "attn_workspace_status": [vp, vp, P(i32)],
+        "attn_decode_run_noalloc": [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64, i32, vp,
+                                    vp, vp, i32, f32, vp, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -191,3 +194,18 @@ def workspace_status(dev_ws, stream=None) -> int:
     if st not in (OK, ERR_TIMEOUT):
         _check(st)
     return code.value
+
+
+def decode_run_noalloc(kv_indptr_h, last_page_len_h, page_size, num_qo_heads, num_kv_heads,
+                       head_dim, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
+                       sm_scale, o, lse, layout=LAYOUT_HND, num_pages=None, stream=None):
+    """attn_decode_run_noalloc: plan + decode in one call, no caller workspace."""
+    kv_indptr_h = _host_i32(kv_indptr_h)
+    last_page_len_h = _host_i32(last_page_len_h)
+    if num_pages is None:
+        num_pages = k_pool.shape[0]
+    _check(lib.attn_decode_run_noalloc(
+        _ptr(kv_indptr_h), _ptr(last_page_len_h), len(kv_indptr_h) - 1, page_size,
+        num_qo_heads, num_kv_heads, head_dim, _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        int(num_pages), layout, _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
+        dtype_code(q.dtype), float(sm_scale), _ptr(o), _ptr(lse), _stream(stream)))

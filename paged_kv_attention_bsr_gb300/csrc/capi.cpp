@@ -69,6 +69,10 @@ attn_status_t check_plan_common(const attn_plan_t* plan, int32_t mode, const voi
 
 }  // namespace
 
+namespace attn {
+void set_last_error(const std::string& msg) { g_err = msg; }
+}  // namespace attn
+
 extern "C" {
 
 const char* attn_last_error(void) { return g_err.c_str(); }

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 #include <cuda_runtime.h>
 
@@ -149,6 +150,9 @@ struct SplitMergeArgs {
   int32_t dtype;
 };
 cudaError_t launch_split_merge(const SplitMergeArgs& a, cudaStream_t stream);
+
+// Sets the text attn_last_error() returns on this thread.
+void set_last_error(const std::string& msg);
 
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,
                                 const float* lse_b, void* o_out, float* lse_out,
