@@ -211,25 +211,27 @@ def time_steps(step_fns, steps, warmup, flush, kernel_split=1):
     return step_ms, kern_ms
 
 
-def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
-    from paged_kv_attention_bsr_gb300 import merge_state, synth
+def bench_decode_workload(key, hbm_peak, bf16_peak, flush, steps, warmup):
+    from paged_kv_attention_bsr_gb300 import synth
+    w = synth.WORKLOADS[key]()
+    st = DecodeStep(w)
+    step_ms, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
+    b = decode_bytes(w)
+    k_s = float(np.mean(kern_ms)) * 1e-3
+    res = {"kind": "decode", "bytes": b, "kernel_us": k_s * 1e6,
+           "step_us": float(np.mean(step_ms)) * 1e3,
+           "GB/s": b / k_s / 1e9, "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak,
+           "units": st.att.plan_info.num_units,
+           "split_items": st.att.plan_info.num_split_items}
+    assert st.att.status() == 0
+    del st
+    torch.cuda.empty_cache()
+    return w.name, res
+
+
+def bench_causal_append(hbm_peak, bf16_peak, flush, steps, warmup):
+    from paged_kv_attention_bsr_gb300 import synth
     from paged_kv_attention_bsr_gb300.api import PagedAttention
-    out = {}
-    # decode workloads
-    for key in ("single_decode", "skewed_decode"):
-        w = synth.WORKLOADS[key]()
-        st = DecodeStep(w)
-        step_ms, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
-        b = decode_bytes(w)
-        k_s = float(np.mean(kern_ms)) * 1e-3
-        out[w.name] = {"kind": "decode", "bytes": b, "kernel_us": k_s * 1e6,
-                       "step_us": float(np.mean(step_ms)) * 1e3,
-                       "GB/s": b / k_s / 1e9, "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak,
-                       "units": st.att.plan_info.num_units,
-                       "split_items": st.att.plan_info.num_split_items}
-        del st
-        torch.cuda.empty_cache()
-    # causal append
     w = synth.causal_append()
     c = w.cache
     att = PagedAttention(w.num_qo_heads, w.num_kv_heads, 128, "append", max_batch=w.batch,
@@ -250,13 +252,23 @@ def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
     step_ms, kern_ms = time_steps([plan_a, run_a], steps, warmup, flush)
     fl = append_flops(w)
     k_s = float(np.mean(kern_ms)) * 1e-3
-    out[w.name] = {"kind": "append", "flops": fl, "kernel_us": k_s * 1e6,
-                   "step_us": float(np.mean(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
-                   "roofline_frac_bf16": fl / k_s / 1e12 / bf16_peak,
-                   "units": att.plan_info.num_units, "split_items": att.plan_info.num_split_items}
+    res = {"kind": "append", "flops": fl, "kernel_us": k_s * 1e6,
+           "step_us": float(np.mean(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
+           "roofline_frac_bf16": fl / k_s / 1e12 / bf16_peak,
+           "units": att.plan_info.num_units, "split_items": att.plan_info.num_split_items,
+           "launches_per_step": 1 + (att.plan_info.num_split_items > 0)}
+    assert att.status() == 0
     del d, att
     torch.cuda.empty_cache()
-    # shared-prefix composable decode (prefix append + suffix decode + merge)
+    return w.name, res
+
+
+def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
+    """Prefix append (P = 128, once per prompt) + suffix decode + LSE merge,
+    next to the same logical KV as one flat P = 16 decode."""
+    from paged_kv_attention_bsr_gb300 import merge_state, synth
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    from paged_kv_attention_bsr_gb300.synth import Workload
     w = synth.shared_prefix_decode()
     pre, suf = w.extra["prefix"], w.cache
     q = w.q.cuda()
@@ -288,21 +300,37 @@ def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
     b_suf = int(suf.kv_lens.sum()) * kvb
     b_flat = int(pre.kv_lens.sum()) * w.extra["n"] * kvb + b_suf
     k_s = float(np.mean(kern_ms)) * 1e-3
-    out[w.name] = {"kind": "composable", "bytes": b_pre + b_suf, "flat_layout_bytes": b_flat,
-                   "kernel_us": k_s * 1e6, "step_us": float(np.mean(step_ms)) * 1e3,
-                   "GB/s": (b_pre + b_suf) / k_s / 1e9,
-                   "roofline_frac_hbm": (b_pre + b_suf) / k_s / 1e9 / hbm_peak,
-                   "launches_per_step": 3}
+    res = {"kind": "composable", "bytes": b_pre + b_suf, "flat_layout_bytes": b_flat,
+           "kernel_us": k_s * 1e6, "step_us": float(np.mean(step_ms)) * 1e3,
+           "GB/s": (b_pre + b_suf) / k_s / 1e9,
+           "roofline_frac_hbm": (b_pre + b_suf) / k_s / 1e9 / hbm_peak,
+           "launches_per_step": 3 + (att_p.plan_info.num_split_items > 0)}
+    assert att_p.status() == 0 and att_s.status() == 0
     del dp, ds
-    # the same logical KV as one flat P = 16 layout (prefix pages shared by the n rows)
     flat = synth.flat_layout_of_composable(w)
-    from paged_kv_attention_bsr_gb300.synth import Workload
     wf = Workload("flat", "decode", torch.bfloat16, 32, 8, 128, w.sm_scale, w.q, flat)
     st = DecodeStep(wf)
     _, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
-    out[w.name]["flat_layout_kernel_us"] = float(np.mean(kern_ms)) * 1e3
+    res["flat_layout_kernel_us"] = float(np.mean(kern_ms)) * 1e3
     del st
     torch.cuda.empty_cache()
+    return w.name, res
+
+
+WORKLOAD_BENCH = {
+    "single_decode": lambda *a: bench_decode_workload("single_decode", *a),
+    "skewed_decode": lambda *a: bench_decode_workload("skewed_decode", *a),
+    "uniform_decode": lambda *a: bench_decode_workload("uniform_decode", *a),
+    "causal_append": bench_causal_append,
+    "shared_prefix": bench_shared_prefix,
+}
+
+
+def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
+    out = {}
+    for key in ("single_decode", "skewed_decode", "causal_append", "shared_prefix"):
+        name, res = WORKLOAD_BENCH[key](hbm_peak, bf16_peak, flush, steps, warmup)
+        out[name] = res
     return out
 
 
@@ -324,10 +352,15 @@ def cpu_oracle_baseline(w, threads):
                                w.num_qo_heads, w.num_kv_heads, w.head_dim, odt, w.sm_scale)
 
     oracle.build()
+    passes = 0
     t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(threads) as ex:
-        list(ex.map(job, chunks))
-    return time.perf_counter() - t0
+        while True:  # whole passes over the batch, ~10+ s of CPU work in total
+            list(ex.map(job, chunks))
+            passes += 1
+            if (time.perf_counter() - t0) * threads >= 10.0 or passes >= 64:
+                break
+    return (time.perf_counter() - t0) / passes, passes
 
 
 def run_ours(args, rank, world):
@@ -436,12 +469,12 @@ def run_ours(args, rank, world):
     }
     if world == 1 and not args.skip_cpu:
         threads = max(1, min(os.cpu_count() or 1, 16))
-        secs = cpu_oracle_baseline(w, threads)
+        secs, passes = cpu_oracle_baseline(w, threads)
         line["cpu_baseline"] = {"value": b / secs / 1e9, "unit": "GB/s", "cores": threads,
                                 "kind": "oracle",
-                                "sample": f"the whole workload (64 requests x 32 heads), one "
-                                          f"step, fp64 C oracle on {threads} threads, "
-                                          f"{secs:.1f} s"}
+                                "sample": f"{passes} whole passes over the workload (64 "
+                                          f"requests x 32 heads), fp64 C oracle on {threads} "
+                                          f"threads, {secs:.2f} s per pass"}
     if world == 1 and not args.headline_only:
         del st
         torch.cuda.empty_cache()
@@ -512,12 +545,22 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads (single, skewed, shared-prefix, append)")
     ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_BENCH),
+                    help="time one workload alone and print only its result")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.gpus > 1 and world == 1:
         sys.exit("for --gpus > 1 launch with torch.distributed.run (one rank per GPU)")
+    if args.workload:
+        # one workload alone (used for profiling captures); prints its own line
+        hbm_peak, bf16_peak, _ = peaks()
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        name, res = WORKLOAD_BENCH[args.workload](hbm_peak, bf16_peak, flush, args.steps,
+                                                  args.warmup)
+        print(json.dumps({"workload": name, **res}), flush=True)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)

@@ -123,7 +123,8 @@ attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_c
 
 /*
  * Planning phase (host). Splits the work of a batch into units balanced over
- * num_ctas CTAs (items (request, query tile, kv head) in request-major order;
+ * num_ctas CTAs (items (request, kv head, query tile) in request-major order,
+ * dealt round-robin to the CTAs first for append;
  * each item weighs its page count + 1; CTA c takes the weight positions
  * [floor(c W / C), floor((c+1) W / C)) of the total W; an item cut by a CTA
  * boundary is "split" and its units write partial states that the run merges).

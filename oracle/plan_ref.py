@@ -6,20 +6,19 @@ analyses the length distribution on the CPU and assigns work units to SMs so
 that a fixed-grid persistent kernel can follow the plan). The digest gives no
 pseudo-code; the exact cut below is the reading used throughout this project:
 
-  items      (request r, query tile t, kv head hk), r-major, then t, then hk;
+  items      (request r, kv head hk, query tile t), r-major, then hk, then t;
              decode has one tile per request, append tiles hold
-             tq = 128 // group query tokens (group heads x tq tokens <= 128 rows).
-             Neighbouring CTAs thus work on the same kv head of a request at
-             the same time, so its K/V pages are shared through L2.
-  pages      n = ceil(vis / P), vis = visible kv length of the tile's last row
-             (the whole kv_len unless causal)
-  weights    w = n + alpha (alpha = 1 overhead slot); prefix sums in int64,
-             W = sum w; CTA c owns positions [floor(c W / C), floor((c+1) W / C))
-  units      inside an item with base b, position b is its overhead slot and
-             b + alpha + k is page k; CTA c's intersection yields pages
-             [max(0, lo - b - alpha), min(n, hi - b - alpha)); an intersection
-             without pages is dropped, except that an item with n = 0 keeps one
-             zero-page unit, owned by the CTA that owns b
+             tq = 128 // group query tokens (group heads x tq tokens <= 128 rows)
+  decode     the costs w = n + alpha are laid end to end (total W) and CTA c
+             takes the positions [floor(c W / C), floor((c+1) W / C)); inside
+             an item at base b, position b is its overhead slot and b + alpha
+             + k is page k; an intersection without pages is dropped, except
+             that an item with n = 0 keeps one zero-page unit, owned by the CTA
+             that owns b
+  append     items go, in order, to the CTA with the least cost so far (ties:
+             lowest index), each CTA capped at ceil(W / C) + alpha; an item
+             that does not fit is cut at the cap (the unit takes the cap minus
+             alpha in pages) and its rest continues on the next CTA
   slots      items with >= 2 units are split; their units get partial-state
              slots numbered in (item, page) order; merge_indptr lists them.
 
@@ -73,45 +72,63 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
         kv_len = kv_length(kv_indptr, last_page_len, page_size, r)
         qo_len = 1 if decode else qo_indptr[r + 1] - qo_indptr[r]
         tiles = 1 if decode else -(-qo_len // tq)
-        for t in range(tiles):
-            for hk in range(num_kv_heads):
+        for hk in range(num_kv_heads):
+            for t in range(tiles):
                 vis = kv_len
                 if causal and not decode:
                     last_row = min((t + 1) * tq, qo_len) - 1
                     vis = min(kv_len, max(0, kv_len - qo_len + last_row + 1))
                 items.append((r, hk, t, -(-vis // page_size)))
 
-    # 2. weights and CTA ranges
-    bases = []
-    total = 0
-    for it in items:
-        bases.append(total)
-        total += it[3] + ALPHA
+    # 2. weights
+    total = sum(it[3] + ALPHA for it in items)
     C = num_ctas
-
-    def lo(c):
-        return (c * total) // C
-
     plan = Plan(work_indptr=[0] * (C + 1), total_weight=total, num_items=len(items),
                 q_tile=tq)
+    per_cta_units = [[] for _ in range(C)]  # [item index, r, hk, t, p0, p1]
 
-    # 3. units, CTA by CTA (positions are monotone, so this is item order too)
-    per_cta_units = [[] for _ in range(C)]
-    for k, (r, hk, t, n) in enumerate(items):
-        b = bases[k]
-        w = n + ALPHA
-        for c in range(C):
-            a, e = lo(c), lo(c + 1)
-            if e <= b or a >= b + w:
-                continue
-            if n == 0:
-                if a <= b < e:
-                    per_cta_units[c].append([k, r, hk, t, 0, 0])
-                continue
-            p0 = max(0, a - b - ALPHA)
-            p1 = min(n, e - b - ALPHA)
-            if p1 > p0:
-                per_cta_units[c].append([k, r, hk, t, p0, p1])
+    if decode:
+        # 3a. contiguous equal cut of the cost line
+        def lo(c):
+            return (c * total) // C
+
+        base = 0
+        for k, (r, hk, t, n) in enumerate(items):
+            w = n + ALPHA
+            for c in range(C):
+                a, e = lo(c), lo(c + 1)
+                if e <= base or a >= base + w:
+                    continue
+                if n == 0:
+                    if a <= base < e:
+                        per_cta_units[c].append([k, r, hk, t, 0, 0])
+                    continue
+                p0 = max(0, a - base - ALPHA)
+                p1 = min(n, e - base - ALPHA)
+                if p1 > p0:
+                    per_cta_units[c].append([k, r, hk, t, p0, p1])
+            base += w
+    else:
+        # 3b. time-ordered fill, capped
+        import heapq
+        cap = -(-total // C) + ALPHA
+        ready = [(0, c) for c in range(C)]
+        heapq.heapify(ready)
+        for k, (r, hk, t, n) in enumerate(items):
+            p = 0
+            while True:
+                used, c = heapq.heappop(ready)
+                avail = cap - used
+                need = ALPHA + (n - p)
+                if need <= avail:
+                    per_cta_units[c].append([k, r, hk, t, p, n])
+                    if used + need < cap:
+                        heapq.heappush(ready, (used + need, c))
+                    break
+                take = avail - ALPHA
+                if take > 0:
+                    per_cta_units[c].append([k, r, hk, t, p, p + take])
+                    p += take
 
     flat = []
     for c in range(C):

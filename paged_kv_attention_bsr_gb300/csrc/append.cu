@@ -46,17 +46,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S buffers at columns 0 and 128
 constexpr uint32_t kColO = 256;  // O at columns 256..383
 
-// Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int kOffQ = 0;                       // 2 query tiles
-constexpr int kOffK = kOffQ + 2 * kTileBytes;  // 2 K stages
-constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 V stages
-constexpr int kOffP = kOffV + 2 * kTileBytes;  // probabilities
+// Shared memory map (offsets from a 1024-byte aligned base). K and V tiles
+// travel through one ring of kSlots 32 KB slots: tile j's K takes slot use
+// 2j and its V use 2j + 1 (slot = use % kSlots), so 2.5 tiles are in flight.
+constexpr int kSlots = 5;
+constexpr int kOffQ = 0;                               // query tile
+constexpr int kOffRing = kOffQ + kTileBytes;           // K/V ring
+constexpr int kOffP = kOffRing + kSlots * kTileBytes;  // probabilities
 constexpr int kOffBar = kOffP + kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2];
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t q_full, q_empty;
+  uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full, o_done, o_free, drain;
   uint32_t tmem_base;
@@ -199,11 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
   volatile int32_t* err = a.ws.error;
 
   if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars.q_full), 1);
+    mbar_init(smem_u32(&bars.q_empty), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&bars.slot_full[i]), 1);
+      mbar_init(smem_u32(&bars.slot_empty[i]), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars.q_full[i]), 1);
-      mbar_init(smem_u32(&bars.q_empty[i]), 1);
-      mbar_init(smem_u32(&bars.kv_full[i]), 1);
-      mbar_init(smem_u32(&bars.kv_empty[i]), 1);
       mbar_init(smem_u32(&bars.s_full[i]), 1);
       mbar_init(smem_u32(&bars.s_empty[i]), 128);
     }
@@ -236,61 +240,65 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t ua = 0, jt = 0;
-      const int P = a.page_size;
-      for (int ui = u_begin; ui < u_end; ++ui) {
-        const AGeo g = append_geo(a, ui);
-        if (g.ntiles == 0) continue;
-        const int qb = ua & 1;
-        if (!mbar_wait(smem_u32(&bars.q_empty[qb]), ((ua >> 1) & 1u) ^ 1u, err, ERR_WAIT_EMPTY))
-          break;
-        const uint32_t qf = smem_u32(&bars.q_full[qb]);
+    // The whole warp runs the loop; lane c fetches the page index of the
+    // tile's 16-row chunk c and issues that chunk's boxes, so the eight index
+    // loads of a tile overlap instead of serialising.
+    uint32_t ua = 0, uses = 0;
+    const int P = a.page_size;
+    bool ok = true;
+    auto wait0 = [&](uint32_t bar, uint32_t parity) -> bool {
+      bool r = true;
+      if (lane == 0) r = mbar_wait(bar, parity, err, ERR_WAIT_EMPTY);
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    for (int ui = u_begin; ui < u_end && ok; ++ui) {
+      const AGeo g = append_geo(a, ui);
+      if (g.ntiles == 0) continue;
+      if (!wait0(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u)) break;
+      if (lane == 0) {
+        const uint32_t qf = smem_u32(&bars.q_full);
         mbar_arrive_expect_tx(qf, kTileBytes);
         const int32_t qrow = int32_t(g.qo_start + int64_t(g.t) * a.q_tile);
-        const uint32_t qdst = base + kOffQ + qb * kTileBytes;
-        tma_load_3d(qdst, &prm.tm_q, 0, g.hk * group, qrow, qf);
-        tma_load_3d(qdst + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
-        bool ok = true;
-        for (int i = 0; i < g.ntiles; ++i, ++jt) {
-          const int st = jt & 1;
-          if (!mbar_wait(smem_u32(&bars.kv_empty[st]), ((jt >> 1) & 1u) ^ 1u, err,
-                         ERR_WAIT_EMPTY)) {
+        tma_load_3d(base + kOffQ, &prm.tm_q, 0, g.hk * group, qrow, qf);
+        tma_load_3d(base + kOffQ + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
+      }
+      ++ua;
+      for (int i = 0; i < g.ntiles && ok; ++i) {
+        const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+        const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+        const int nch = (ntt + kChunk - 1) / kChunk;
+        int32_t row = 0;
+        if (lane < nch) {
+          const int64_t kvt = kv0 + int64_t(lane) * kChunk;
+          const int64_t pg = kvt / P;
+          const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+          row = int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
+        }
+        for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
+          const int slot = int(uses % kSlots);
+          if (!wait0(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
-          const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
-          const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
-          const int nch = (ntt + kChunk - 1) / kChunk;
-          const uint32_t kf = smem_u32(&bars.kv_full[st]);
-          mbar_arrive_expect_tx(kf, uint32_t(nch) * kChunk * 256u * 2u);
-          const uint32_t kdst = base + kOffK + st * kTileBytes;
-          const uint32_t vdst = base + kOffV + st * kTileBytes;
-          for (int c = 0; c < nch; ++c) {
-            const int64_t kvt = kv0 + int64_t(c) * kChunk;
-            const int64_t pg = kvt / P;
-            const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
-            const int32_t row = int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
-            const uint32_t off = uint32_t(c) * kChunk * 128u;
-            tma_load_2d(kdst + off, &prm.tm_k, 0, row, kf);
-            tma_load_2d(kdst + kHalf + off, &prm.tm_k, 64, row, kf);
-            tma_load_2d(vdst + off, &prm.tm_v, 0, row, kf);
-            tma_load_2d(vdst + kHalf + off, &prm.tm_v, 64, row, kf);
+          const uint32_t full = smem_u32(&bars.slot_full[slot]);
+          if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
+          __syncwarp();
+          if (lane < nch) {
+            const uint32_t dst = base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
+            const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                     : static_cast<const void*>(&prm.tm_v);
+            tma_load_2d(dst, tm, 0, row, full);
+            tma_load_2d(dst + kHalf, tm, 64, row, full);
           }
         }
-        ++ua;
-        if (!ok) break;
       }
-      // drain: every issued copy has landed before the CTA can exit
-      for (int i = 0; i < 2; ++i) {
-        if (uint32_t(i) < ua) {
-          const uint32_t last = ua - 1 - ((ua - 1 - i) & 1u);
-          mbar_wait(smem_u32(&bars.q_full[i]), (last >> 1) & 1u, err, ERR_WAIT_DRAIN);
-        }
-        if (uint32_t(i) < jt) {
-          const uint32_t last = jt - 1 - ((jt - 1 - i) & 1u);
-          mbar_wait(smem_u32(&bars.kv_full[i]), (last >> 1) & 1u, err, ERR_WAIT_DRAIN);
-        }
+    }
+    // drain: every issued copy has landed before the CTA can exit
+    if (lane == 0) {
+      if (ua > 0) mbar_wait(smem_u32(&bars.q_full), (ua - 1) & 1u, err, ERR_WAIT_DRAIN);
+      for (uint32_t sl = 0; sl < uint32_t(kSlots) && sl < uses; ++sl) {
+        const uint32_t last = uses - 1 - ((uses - 1 - sl) % kSlots);
+        mbar_wait(smem_u32(&bars.slot_full[sl]), (last / kSlots) & 1u, err, ERR_WAIT_DRAIN);
       }
     }
     __syncwarp();
@@ -300,13 +308,16 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       uint32_t ua = 0, jt = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t jt_pv, bool first) -> bool {
+        const uint32_t use = 2 * jt_pv + 1;
+        const int slot = int(use % kSlots);
         if (!mbar_wait(smem_u32(&bars.p_full), jt_pv & 1u, err, ERR_WAIT_SOFTMAX)) return false;
         if (first && !mbar_wait(smem_u32(&bars.o_free), (ua & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
           return false;
+        if (!mbar_wait(smem_u32(&bars.slot_full[slot]), (use / kSlots) & 1u, err, ERR_WAIT_FULL))
+          return false;
         tc_fence_after();
-        const int st = jt_pv & 1;
         const uint32_t pbase = base + kOffP;
-        const uint32_t vbase = base + kOffV + st * kTileBytes;
+        const uint32_t vbase = base + kOffRing + slot * kTileBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t ad = smem_desc(pbase + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
@@ -314,33 +325,36 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
           mma_f16(tmem + kColO, ad, bd, prm.idesc_pv, (first && k == 0) ? 0u : 1u);
         }
         mma_commit(smem_u32(&bars.o_done));
-        mma_commit(smem_u32(&bars.kv_empty[st]));
+        mma_commit(smem_u32(&bars.slot_empty[slot]));
         return true;
       };
       for (int ui = u_begin; ui < u_end && ok; ++ui) {
         const AGeo g = append_geo(a, ui);
         if (g.ntiles == 0) continue;
-        const int qb = ua & 1;
-        if (!mbar_wait(smem_u32(&bars.q_full[qb]), (ua >> 1) & 1u, err, ERR_WAIT_FULL)) break;
-        const uint32_t qbase = base + kOffQ + qb * kTileBytes;
+        if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL)) break;
+        const uint32_t qbase = base + kOffQ;
         for (int i = 0; i < g.ntiles; ++i, ++jt) {
-          const int st = jt & 1;
-          if (!mbar_wait(smem_u32(&bars.kv_full[st]), (jt >> 1) & 1u, err, ERR_WAIT_FULL) ||
-              !mbar_wait(smem_u32(&bars.s_empty[st]), ((jt >> 1) & 1u) ^ 1u, err,
+          const uint32_t use = 2 * jt;
+          const int slot = int(use % kSlots);
+          const int sb = jt & 1;
+          if (!mbar_wait(smem_u32(&bars.slot_full[slot]), (use / kSlots) & 1u, err,
+                         ERR_WAIT_FULL) ||
+              !mbar_wait(smem_u32(&bars.s_empty[sb]), ((jt >> 1) & 1u) ^ 1u, err,
                          ERR_WAIT_SOFTMAX)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t kbase = base + kOffK + st * kTileBytes;
+          const uint32_t kbase = base + kOffRing + slot * kTileBytes;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-            mma_f16(tmem + kColS + st * 128, smem_desc(qbase + koff, 16, 1024),
+            mma_f16(tmem + kColS + sb * 128, smem_desc(qbase + koff, 16, 1024),
                     smem_desc(kbase + koff, 16, 1024), prm.idesc_s, k > 0 ? 1u : 0u);
           }
-          mma_commit(smem_u32(&bars.s_full[st]));
-          if (i == g.ntiles - 1) mma_commit(smem_u32(&bars.q_empty[qb]));
+          mma_commit(smem_u32(&bars.s_full[sb]));
+          mma_commit(smem_u32(&bars.slot_empty[slot]));
+          if (i == g.ntiles - 1) mma_commit(smem_u32(&bars.q_empty));
           if (i > 0 && !issue_pv(jt - 1, i == 1)) {
             ok = false;
             break;
@@ -472,8 +486,17 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         }
         // kv rows past the unit's end hold whatever the pool had: zero them in V
         const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+        if (ntt < kTile) {
+          // wait for this tile's V to land before overwriting its tail rows
+          const uint32_t vuse = 2 * jt + 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.slot_full[vuse % kSlots]),
+                                                 (vuse / kSlots) & 1u, err, ERR_WAIT_FULL))) {
+            ok = false;
+            break;
+          }
+        }
         if (ntt < kTile && rho >= ntt) {
-          uint8_t* vrow = gbase + kOffV + (jt & 1) * kTileBytes + rho * 128;
+          uint8_t* vrow = gbase + kOffRing + (2 * jt + 1) % kSlots * kTileBytes + rho * 128;
 #pragma unroll
           for (int x = 0; x < 8; ++x) {
             *reinterpret_cast<uint4*>(vrow + x * 16) = make_uint4(0, 0, 0, 0);

@@ -99,9 +99,10 @@ attn_status_t attn_workspace_size(int32_t max_batch, int32_t max_total_qo,
     items = std::max<int64_t>(
         items, int64_t(num_kv_heads) * ((int64_t(max_total_qo) + q_tile - 1) / q_tile + max_batch));
   const int64_t C = num_ctas;
-  const int64_t units = items + C - 1;
-  const int64_t split = std::min<int64_t>(items, C - 1);
-  const int64_t slots = std::min<int64_t>(units, 2 * (C - 1));
+  // the cut adds at most C units; each extra unit cuts at most one item
+  const int64_t units = items + C;
+  const int64_t split = std::min<int64_t>(items, C);
+  const int64_t slots = std::min<int64_t>(units, 2 * C);
   const int32_t rows = append_ok ? kTileRows : int32_t(group);
   const PlanLayout L = plan_layout(num_ctas, units, split, slots, rows, head_dim);
   *dev_bytes = size_t(L.dev_bytes);

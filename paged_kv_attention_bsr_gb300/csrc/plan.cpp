@@ -6,18 +6,27 @@
 // length distribution and emits a work assignment, and a GPU phase whose
 // persistent kernel (fixed grid, preallocated workspace) follows it. The page
 // gives no algorithm; the cut used here:
-//   * items (request, query tile, kv head) in request-major order, then tile,
-//     then kv head (so CTAs that run side by side read the same kv head's
-//     pages and share them through L2); an item's cost is its visible page
-//     count n plus one overhead slot;
-//   * the items' costs are laid end to end (total W) and CTA c takes the
-//     contiguous positions [floor(c W / C), floor((c+1) W / C));
-//   * an item crossed by a CTA boundary becomes several units ("split"); each
-//     writes a partial (o, lse) state and a merge combines them.
-// Every CTA gets floor(W/C) or ceil(W/C) positions and the cut adds at most
-// C - 1 units. The result depends only on the inputs and is deterministic.
+//   * items (request, kv head, query tile) in request-major order, then kv
+//     head, then tile; an item's cost is its visible page count n plus one
+//     overhead slot; W = the sum of all costs;
+//   * decode: the costs are laid end to end and CTA c takes the contiguous
+//     positions [floor(c W / C), floor((c+1) W / C)) (Stream-K's equal cut);
+//     an item crossed by a boundary becomes several units;
+//   * append: items are dealt in order to the CTA with the least work so
+//     far (ties to the lowest index), each CTA capped at ceil(W / C) + 1; an
+//     item that does not fit is cut at the cap and continues on the next CTA.
+//     CTAs then run items in roughly the order of the list, so the query
+//     tiles of a kv head are in flight together and share its K/V pages
+//     through L2, while every CTA still gets an equal share;
+//   * units of an item cut in several ("split") write partial (o, lse)
+//     states that are merged by log-sum-exp.
+// Every CTA gets at most ceil(W/C) + 1 of the cost and the cut adds at most
+// C extra units. The result depends only on the inputs and is deterministic.
 #include <algorithm>
 #include <cstring>
+#include <functional>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
@@ -134,8 +143,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
       }
     }
     const int64_t tiles = decode ? 1 : (qo_len + q_tile - 1) / q_tile;
-    for (int64_t t = 0; t < tiles; ++t) {
-      for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
+    for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
+      for (int64_t t = 0; t < tiles; ++t) {
         int64_t vis = kv_len;
         if (causal && !decode) {
           const int64_t last_row = std::min<int64_t>((t + 1) * q_tile, qo_len) - 1;
@@ -147,69 +156,120 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
     }
   }
 
-  // ---- balanced cut of the cost line
+  // ---- cut the work into units
   constexpr int64_t kAlpha = 1;
   int64_t W = 0;
   for (const Item& it : items) W += it.n + kAlpha;
   const int64_t C = num_ctas;
   auto bound = [&](int64_t c) -> int64_t { return (c * W) / C; };
 
-  std::vector<Unit> units;
-  units.reserve(items.size() + size_t(C));
-  std::vector<int32_t> cta_of;
-  cta_of.reserve(items.size() + size_t(C));
-  std::vector<int32_t> first_unit(items.size() + 1, 0);
+  struct U {
+    Unit u;
+    int32_t cta;
+    int32_t item;
+  };
+  std::vector<U> gen;  // units in generation order
+  gen.reserve(items.size() + size_t(C));
+  std::vector<int64_t> load(size_t(C), 0);
 
-  int64_t c = 0;
-  int64_t base = 0;
-  for (size_t k = 0; k < items.size(); ++k) {
-    const Item& it = items[k];
-    const int64_t w = it.n + kAlpha;
-    first_unit[k] = int32_t(units.size());
-    while (c + 1 < C && bound(c + 1) <= base) ++c;  // CTA owning position `base`
-    for (int64_t cc = c; cc < C && bound(cc) < base + w; ++cc) {
-      const int64_t lo = bound(cc), hi = bound(cc + 1);
-      if (hi <= lo) continue;
-      if (it.n == 0) {
-        if (lo <= base && base < hi) {
-          units.push_back({it.r, it.hk, it.t, 0, 0, -1, -1, 0});
-          cta_of.push_back(int32_t(cc));
+  if (decode) {
+    // Contiguous balanced cut of the cost line (Stream-K style).
+    int64_t c = 0;
+    int64_t base = 0;
+    for (size_t k = 0; k < items.size(); ++k) {
+      const Item& it = items[k];
+      const int64_t w = it.n + kAlpha;
+      while (c + 1 < C && bound(c + 1) <= base) ++c;  // CTA owning position `base`
+      for (int64_t cc = c; cc < C && bound(cc) < base + w; ++cc) {
+        const int64_t lo = bound(cc), hi = bound(cc + 1);
+        if (hi <= lo) continue;
+        if (it.n == 0) {
+          if (lo <= base && base < hi)
+            gen.push_back({{it.r, it.hk, it.t, 0, 0, -1, -1, 0}, int32_t(cc), int32_t(k)});
+          continue;
         }
-        continue;
+        const int64_t p0 = std::max<int64_t>(0, lo - base - kAlpha);
+        const int64_t p1 = std::min<int64_t>(it.n, hi - base - kAlpha);
+        if (p1 > p0)
+          gen.push_back({{it.r, it.hk, it.t, int32_t(p0), int32_t(p1), -1, -1, 0}, int32_t(cc),
+                         int32_t(k)});
       }
-      const int64_t p0 = std::max<int64_t>(0, lo - base - kAlpha);
-      const int64_t p1 = std::min<int64_t>(it.n, hi - base - kAlpha);
-      if (p1 > p0) {
-        units.push_back({it.r, it.hk, it.t, int32_t(p0), int32_t(p1), -1, -1, 0});
-        cta_of.push_back(int32_t(cc));
+      base += w;
+    }
+    for (int64_t i = 0; i < C; ++i) load[size_t(i)] = bound(i + 1) - bound(i);
+  } else {
+    // Time-ordered fill: items go, in order, to the CTA with the least work
+    // so far (ties: lowest index), each CTA capped at ceil(W / C) + 1; an item
+    // that does not fit is cut at the cap and continues on the next CTA.
+    const int64_t cap = (W + C - 1) / C + kAlpha;
+    typedef std::pair<int64_t, int32_t> Slot;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> ready;
+    for (int32_t c = 0; c < num_ctas; ++c) ready.push(Slot(0, c));
+    for (size_t k = 0; k < items.size(); ++k) {
+      const Item& it = items[k];
+      int64_t p = 0;
+      for (;;) {
+        if (ready.empty()) {
+          *msg = "attn_plan: internal error (append fill ran out of capacity)";
+          return ATTN_ERR_INVALID_ARG;
+        }
+        const Slot top = ready.top();
+        ready.pop();
+        const int32_t c = top.second;
+        const int64_t avail = cap - top.first;
+        const int64_t need = kAlpha + (it.n - p);
+        if (need <= avail) {
+          gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(it.n), -1, -1, 0}, c,
+                         int32_t(k)});
+          load[size_t(c)] = top.first + need;
+          if (load[size_t(c)] < cap) ready.push(Slot(load[size_t(c)], c));
+          break;
+        }
+        const int64_t take = avail - kAlpha;
+        load[size_t(c)] = cap;  // this CTA is full either way
+        if (take <= 0) continue;
+        gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(p + take), -1, -1, 0}, c,
+                       int32_t(k)});
+        p += take;
       }
     }
-    base += w;
   }
-  first_unit[items.size()] = int32_t(units.size());
 
   // ---- split items, slots in (item, page) order
+  std::vector<int32_t> n_units(items.size(), 0);
+  for (const U& g : gen) n_units[size_t(g.item)]++;
+  std::vector<int32_t> split_of(items.size(), -1);
   std::vector<int32_t> merge_indptr(1, 0);
   std::vector<int4> merge_items;
-  int32_t slots = 0;
   for (size_t k = 0; k < items.size(); ++k) {
-    const int32_t a = first_unit[k], b = first_unit[k + 1];
-    if (b - a < 2) continue;
-    const int32_t split_id = int32_t(merge_items.size());
-    for (int32_t u = a; u < b; ++u) {
-      units[u].slot = slots++;
-      units[u].split = split_id;
+    if (n_units[k] < 2) continue;
+    split_of[k] = int32_t(merge_items.size());
+    merge_items.push_back(make_int4(items[k].r, items[k].hk, items[k].t, n_units[k]));
+    merge_indptr.push_back(merge_indptr.back() + n_units[k]);
+  }
+  const int32_t slots = merge_indptr.back();
+  {
+    // units of one item are generated in page order
+    std::vector<int32_t> next(merge_items.size(), 0);
+    for (U& g : gen) {
+      const int32_t sid = split_of[size_t(g.item)];
+      if (sid < 0) continue;
+      g.u.split = sid;
+      g.u.slot = merge_indptr[size_t(sid)] + next[size_t(sid)]++;
     }
-    merge_items.push_back(make_int4(items[k].r, items[k].hk, items[k].t, b - a));
-    merge_indptr.push_back(slots);
   }
 
-  // ---- per-CTA offsets (units are already in CTA order)
+  // ---- per-CTA lists (generation order within a CTA)
   std::vector<int32_t> work_indptr(size_t(C) + 1, 0);
-  for (int32_t cc : cta_of) work_indptr[size_t(cc) + 1]++;
+  for (const U& g : gen) work_indptr[size_t(g.cta) + 1]++;
   for (int64_t i = 0; i < C; ++i) work_indptr[i + 1] += work_indptr[i];
+  std::vector<Unit> units(gen.size());
+  {
+    std::vector<int32_t> at(work_indptr.begin(), work_indptr.end() - 1);
+    for (const U& g : gen) units[size_t(at[size_t(g.cta)]++)] = g.u;
+  }
   int64_t max_load = 0;
-  for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, bound(i + 1) - bound(i));
+  for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, load[size_t(i)]);
 
   // ---- write tables
   const int64_t S = int64_t(merge_items.size());

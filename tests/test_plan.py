@@ -127,12 +127,24 @@ def test_plan_properties(decode):
         for c in range(ctas):
             pages = int((u[wi[c]:wi[c + 1], 4] - u[wi[c]:wi[c + 1], 3]).sum())
             assert pages <= cap
-        assert p.max_cta_weight <= cap
-        # the cut adds at most C - 1 units; split items carry slots in order
-        assert p.num_units - p.num_items <= ctas - 1
-        assert p.num_split_items <= ctas - 1
+        assert p.max_cta_weight <= cap + (0 if qo is None else 1)
+        # the cut adds at most C - 1 units (decode) / C units (append);
+        # split items carry slots in order
+        extra = ctas - 1 if qo is None else ctas
+        assert p.num_units - p.num_items <= extra
+        assert p.num_split_items <= extra
         slots = [int(s) for s in u[:, 5] if s >= 0]
-        assert slots == list(range(len(slots)))
+        assert sorted(slots) == list(range(len(slots)))
+        if qo is None:  # decode units are already in (item, page) order
+            assert slots == list(range(len(slots)))
+        by_item = {}
+        for row in u:
+            if row[5] >= 0:
+                by_item.setdefault((int(row[0]), int(row[1]), int(row[2])), []).append(
+                    (int(row[3]), int(row[5])))
+        for segs in by_item.values():
+            segs.sort()
+            assert [s for _, s in segs] == list(range(segs[0][1], segs[0][1] + len(segs)))
         assert p.num_slots == len(slots)
         # identical bytes run to run
         p2, _, buf2 = _lib_plan(kv_indptr, last, P, Hq, Hk, ctas, qo, causal)
