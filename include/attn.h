@@ -78,14 +78,14 @@ typedef struct attn_plan {
   int32_t head_dim;
   int32_t causal;
   int32_t num_ctas;         /* grid size of the persistent run kernel          */
-  int32_t q_tile;           /* query tokens per tile: 128 / group (append), 1  */
+  int32_t q_tile;           /* query tokens per item: 256 / group (append), 1  */
   int32_t rows_per_item;    /* packed rows of one item: group * q_tile         */
   int32_t num_items;        /* (request, kv head, query tile) triples          */
   int32_t num_units;        /* work units after the balanced cut               */
   int32_t num_split_items;  /* items cut into >= 2 units (merged after run)    */
   int32_t num_slots;        /* partial-state slots used by split items         */
   int32_t total_qo;         /* query rows (decode: batch)                      */
-  int32_t reserved0;
+  int32_t max_qo_len;       /* longest query row count of a request (decode: 1) */
   int64_t total_weight;     /* sum over items of (pages + 1)                   */
   int64_t max_cta_weight;   /* largest per-CTA share of total_weight           */
   int64_t off_work_indptr;  /* byte offsets of the tables in the workspaces    */
@@ -171,7 +171,10 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
  *   lse        : device float[batch, num_qo_heads] (out) or NULL
  *   dev_ws     : the workspace given to attn_plan (holds the plan tables)
  * Supported: head_dim 128, group = num_qo_heads / num_kv_heads in 1..8,
- * any page_size >= 1, both layouts, fp16 and bf16.
+ * any page_size >= 1, both layouts, fp16 and bf16. Groups below 8 run on a
+ * CUDA-core streaming kernel; group 8 with the HND layout and page_size a
+ * multiple of 16 runs on the tensor-core (tcgen05) kernel, the group's 8
+ * query rows forming one M = 128 tile, plus a merge kernel for split items.
  * Errors: INVALID_ARG (plan mode/shape mismatch, null pointers),
  * UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA (launch failure).
  */

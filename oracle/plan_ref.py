@@ -8,7 +8,8 @@ pseudo-code; the exact cut below is the reading used throughout this project:
 
   items      (request r, kv head hk, query tile t), r-major, then hk, then t;
              decode has one tile per request, append tiles hold
-             tq = 128 // group query tokens (group heads x tq tokens <= 128 rows)
+             tq = 256 // group query tokens (group heads x tq tokens = 256 packed
+             rows: two 128-row MMA tiles), group must divide 128
   decode     the costs w = n + alpha are laid end to end (total W) and CTA c
              takes the positions [floor(c W / C), floor((c+1) W / C)); inside
              an item at base b, position b is its overhead slot and b + alpha
@@ -31,7 +32,7 @@ from dataclasses import dataclass, field
 from typing import List, Optional, Sequence
 
 ALPHA = 1
-TILE_ROWS = 128
+ITEM_ROWS = 256
 
 
 @dataclass
@@ -64,7 +65,7 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
     batch = len(kv_indptr) - 1
     group = num_qo_heads // num_kv_heads
     decode = qo_indptr is None
-    tq = 1 if decode else TILE_ROWS // group
+    tq = 1 if decode else ITEM_ROWS // group
 
     # 1. items and their page counts
     items = []  # (r, hk, t, n)

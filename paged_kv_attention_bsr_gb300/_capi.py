@@ -41,7 +41,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "mode", "batch", "page_size", "num_qo_heads", "num_kv_heads", "head_dim", "causal",
         "num_ctas", "q_tile", "rows_per_item", "num_items", "num_units", "num_split_items",
-        "num_slots", "total_qo", "reserved0")] + [(n, ctypes.c_int64) for n in (
+        "num_slots", "total_qo", "max_qo_len")] + [(n, ctypes.c_int64) for n in (
         "total_weight", "max_cta_weight", "off_work_indptr", "off_units", "off_merge_indptr",
         "off_merge_items", "off_counters", "off_partial_o", "off_partial_lse", "table_bytes",
         "dev_bytes_needed")] + [("fingerprint", ctypes.c_uint64)]

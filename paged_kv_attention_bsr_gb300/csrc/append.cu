@@ -7,23 +7,31 @@
 // 与追加"; paged KV per the modb.pro digest, "统一的 KV 缓存存储格式"). Work
 // follows the CPU plan of "动态负载均衡调度" in a persistent fixed grid.
 //
-// Tile shapes. A work unit is (request r, query tile t, kv head hk, pages
-// [p0, p1)). Its query tile packs 128 rows: tq = 128 / group query tokens x
-// the group's query heads (row = token * group + head), so one K/V tile feeds
-// every head of the GQA group. K/V tiles hold 128 kv tokens, gathered from the
-// page table in 16-row TMA boxes (page_size % 16 == 0).
+// Tile shapes. A work unit is (request r, kv head hk, item t, pages [p0, p1)).
+// An item packs 256 query rows (token x GQA head, row = token * group + head)
+// as two 128-row query tiles A and B, so every K/V tile read from L2/HBM
+// feeds both tiles and every head of the GQA group. K/V tiles hold 128 kv
+// tokens, gathered from the page table in 16-row TMA boxes
+// (page_size % 16 == 0).
 //
-// Per KV tile j (all MMAs M = 128, N = 128, bf16/fp16 in, fp32 accumulate):
-//   S_j = Q K_j^T          tcgen05.mma, A = Q (smem, K-major), B = K (smem,
-//                          K-major), D = TMEM S buffer j % 2
-//   P_j = exp2(S_j*c - m)  4 softmax warps, one TMEM lane (= row) per thread
-//   O  += P_j V_j          A = P (smem, K-major), B = V (smem, MN-major), D =
-//                          TMEM O
-// Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads, warp 1
-// allocates TMEM and issues MMAs from one thread, warps 2-5 run the softmax,
-// the lazy O rescale (only when a row max grows by more than 2^8) and the
-// epilogue. S is double-buffered in TMEM so S_{j+1} runs under softmax_j.
+// Per KV tile j (all MMAs M = N = 128, bf16/fp16 in, fp32 accumulate), for
+// each query tile x:
+//   S_x = Q_x K_j^T          A = Q_x (smem, K-major), B = K (smem, K-major),
+//                            D = TMEM S_x
+//   P_x = exp2(S_x*c - m)    softmax warpgroup x, one TMEM lane (= row) per
+//                            thread; P_x to shared memory (bf16/fp16)
+//   O_x += P_x V_j           A = P_x (smem, K-major), B = V (smem, MN-major),
+//                            D = TMEM O_x
+// Warp roles (320 threads, one CTA per SM): warps 0-3 and 4-7 are the softmax
+// warpgroups of tiles A and B (lazy O rescale only when a row max grows by
+// more than 2^8, epilogue from TMEM); warp 8 issues TMA loads through a ring
+// of three 32 KB K/V slots; warp 9 allocates TMEM and issues the MMAs from
+// one thread, S_x(j+1) as soon as softmax x has read S_x(j), so the tensor
+// core works on one tile's S while the other tile's softmax runs.
 // Every wait is bounded; TMEM is freed on every path.
+//
+// Decode mode (no qo_indptr): one query row per request; an item is the
+// group's query heads of one request (group rows of tile A).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,26 +49,46 @@ constexpr int kTile = 128;
 constexpr int kChunk = 16;                  // kv rows per TMA box
 constexpr int kHalf = kTile * 128;          // 128 rows x 128 B (64 x 16-bit)
 constexpr int kTileBytes = 2 * kHalf;       // 128 x 128 x 16-bit
-constexpr int kThreads = 192;
+constexpr int kWarpSoftmax0 = 0;            // warps 0-3: tile A, 4-7: tile B
+constexpr int kWarpLoad = 8;                // warps 8-11: load, MMA, 2 idle
+constexpr int kWarpMma = 9;
+constexpr int kThreads = 384;
+// Register split (setmaxnreg): launched at 168 per thread (384 x 168 =
+// 64512); the load/MMA warpgroup drops to 104 (frees 128 x 64 = 8192) and the
+// two softmax warpgroups rise to 192 (take 256 x 24 = 6144). Per scheduler:
+// 192 + 192 + 104 registers x 32 lanes <= 16384.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 104;
+constexpr int kRegsSoftmax = 192;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // S buffers at columns 0 and 128
-constexpr uint32_t kColO = 256;  // O at columns 256..383
+constexpr uint32_t kColS = 0;    // S_A at 0, S_B at 128
+constexpr uint32_t kColO = 256;  // O_A at 256, O_B at 384
 
-// Shared memory map (offsets from a 1024-byte aligned base). K and V tiles
-// travel through one ring of kSlots 32 KB slots: tile j's K takes slot use
-// 2j and its V use 2j + 1 (slot = use % kSlots), so 2.5 tiles are in flight.
-constexpr int kSlots = 5;
-constexpr int kOffQ = 0;                               // query tile
-constexpr int kOffRing = kOffQ + kTileBytes;           // K/V ring
-constexpr int kOffP = kOffRing + kSlots * kTileBytes;  // probabilities
-constexpr int kOffBar = kOffP + kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+// Shared memory map (offsets from a 1024-byte aligned base) for NQ query
+// tiles per item. K and V tiles travel through one ring of SLOTS 32 KB slots:
+// KV tile j's K takes slot use 2j and its V use 2j + 1 (slot = use % SLOTS).
+// With one query tile (decode mode, short queries) the second tile's Q and P
+// space becomes two more ring slots, i.e. deeper prefetch for HBM-bound runs.
+constexpr int kMaxSlots = 5;
+template <int NQ>
+struct Layout {
+  static constexpr int SLOTS = NQ == 2 ? 3 : 5;
+  static constexpr int OFF_Q = 0;                            // query tiles
+  static constexpr int OFF_P = OFF_Q + NQ * kTileBytes;      // probabilities
+  static constexpr int OFF_RING = OFF_P + NQ * kTileBytes;   // K/V ring
+  static constexpr int OFF_BAR = OFF_RING + SLOTS * kTileBytes;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;         // + barriers + alignment slack
+};
+static_assert(Layout<1>::OFF_BAR == Layout<2>::OFF_BAR, "both layouts fill 224 KB");
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t slot_full[kSlots], slot_empty[kSlots];
+  uint64_t slot_full[kMaxSlots], slot_empty[kMaxSlots];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, o_done, o_free, drain;
+  uint64_t p_full[2], o_done[2], o_free[2];
+  uint64_t drain;
   uint32_t tmem_base;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -123,6 +151,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// All 128 fp32 columns of this thread's TMEM lane: one load, one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -143,6 +184,42 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(*reinterpret_cast<unsigned long long*>(&d))
+      : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
+        "l"(*reinterpret_cast<const unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<const unsigned long long*>(&c)));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(*reinterpret_cast<unsigned long long*>(&d))
+      : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
+        "l"(*reinterpret_cast<const unsigned long long*>(&b)));
+  return d;
+}
+
+// 32 probabilities (16 packed words) of row `row` into columns [32c, 32c+32)
+// of the 128B-swizzled K-major P tile (two 64-column halves).
+__device__ __forceinline__ void store_p_chunk(uint8_t* pbuf, int row, int c,
+                                              const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int ch = c * 4 + u;  // 16-byte chunk of the 256-byte row
+    const int half = ch >> 3, cc = ch & 7;
+    *reinterpret_cast<uint4*>(pbuf + half * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) =
+        make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
+  }
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (BF16) {
@@ -157,9 +234,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // --------------------------------------------------------- unit geometry
 struct AGeo {
   int32_t r, hk, t, slot, page_base;
+  int32_t ntiles;  // 128-token KV tiles of the unit
+  int32_t nq;      // 128-row query tiles of the item that hold queries (1 or 2)
   int64_t qo_start, qo_len, kv_len;
   int64_t tok_begin, tok_end;
-  int32_t ntiles;
 };
 
 __device__ __forceinline__ AGeo append_geo(const AppendArgs& a, int ui) {
@@ -168,11 +246,16 @@ __device__ __forceinline__ AGeo append_geo(const AppendArgs& a, int ui) {
   const int4 y = __ldg(rec + 1);
   AGeo g;
   g.r = x.x;
-  g.t = x.z;
   g.hk = x.y;
+  g.t = x.z;
   g.slot = y.y;
-  g.qo_start = __ldg(a.qo_indptr + g.r);
-  g.qo_len = int64_t(__ldg(a.qo_indptr + g.r + 1)) - g.qo_start;
+  if (a.qo_indptr) {
+    g.qo_start = __ldg(a.qo_indptr + g.r);
+    g.qo_len = int64_t(__ldg(a.qo_indptr + g.r + 1)) - g.qo_start;
+  } else {  // decode mode: one query row per request
+    g.qo_start = g.r;
+    g.qo_len = 1;
+  }
   g.page_base = __ldg(a.kv_indptr + g.r);
   const int64_t n = int64_t(__ldg(a.kv_indptr + g.r + 1)) - g.page_base;
   g.kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
@@ -185,11 +268,18 @@ __device__ __forceinline__ AGeo append_geo(const AppendArgs& a, int ui) {
   g.tok_end = min(int64_t(y.x) * a.page_size, vis);
   const int64_t nt = g.tok_end - g.tok_begin;
   g.ntiles = nt > 0 ? int32_t((nt + kTile - 1) / kTile) : 0;
+  const int64_t rem = g.qo_len - int64_t(g.t) * a.q_tile;  // queries left for this item
+  g.nq = (a.q_tile > a.tile_tokens && rem > a.tile_tokens) ? 2 : 1;  // capped by NQ at use
   return g;
 }
 
-template <bool BF16>
+template <bool BF16, int NQ>
 __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_constant__ AppendParams prm) {
+  constexpr int kSlots = Layout<NQ>::SLOTS;
+  constexpr int kOffQ = Layout<NQ>::OFF_Q;
+  constexpr int kOffP = Layout<NQ>::OFF_P;
+  constexpr int kOffRing = Layout<NQ>::OFF_RING;
+  constexpr int kOffBar = Layout<NQ>::OFF_BAR;
   extern __shared__ uint8_t smem_raw[];
   const AppendArgs& a = prm.a;
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -210,19 +300,19 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
       mbar_init(smem_u32(&bars.s_empty[i]), 128);
+      mbar_init(smem_u32(&bars.p_full[i]), 128);
+      mbar_init(smem_u32(&bars.o_done[i]), 1);
+      mbar_init(smem_u32(&bars.o_free[i]), 128);
     }
-    mbar_init(smem_u32(&bars.p_full), 128);
-    mbar_init(smem_u32(&bars.o_done), 1);
-    mbar_init(smem_u32(&bars.o_free), 128);
     mbar_init(smem_u32(&bars.drain), 1);
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == kWarpLoad && lane == 0) {
     prefetch_tmap(&prm.tm_q);
     prefetch_tmap(&prm.tm_k);
     prefetch_tmap(&prm.tm_v);
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&bars.tmem_base)),
                  "r"(kTmemCols)
@@ -233,12 +323,18 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
-
-  const int u_begin = __ldg(a.ws.work_indptr + blockIdx.x);
-  const int u_end = __ldg(a.ws.work_indptr + blockIdx.x + 1);
   const int group = a.group;
 
-  if (warp == 0) {
+  // Rows per 128-row query tile that hold data (128 for append, group in
+  // decode mode) and the TMA bytes of one tile.
+  const uint32_t tile_rows = uint32_t(group * a.tile_tokens);
+
+  // A CTA runs the unit lists of plan CTAs blockIdx.x, blockIdx.x + gridDim.x,
+  // ... (the grid is at most one CTA per SM; a plan may have more CTAs).
+  if (warp >= kWarpLoad) {
+  // warpgroup 2: TMA loads, MMA issue (2 idle warps); gives registers away
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+  if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop; lane c fetches the page index of the
     // tile's 16-row chunk c and issues that chunk's boxes, so the eight index
@@ -251,16 +347,24 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       if (lane == 0) r = mbar_wait(bar, parity, err, ERR_WAIT_EMPTY);
       return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
     };
-    for (int ui = u_begin; ui < u_end && ok; ++ui) {
-      const AGeo g = append_geo(a, ui);
+    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+    for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok; ++ui) {
+      AGeo g = append_geo(a, ui);
+      g.nq = min(g.nq, NQ);
       if (g.ntiles == 0) continue;
-      if (!wait0(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u)) break;
+      if (!wait0(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u)) {
+        ok = false;
+        break;
+      }
       if (lane == 0) {
         const uint32_t qf = smem_u32(&bars.q_full);
-        mbar_arrive_expect_tx(qf, kTileBytes);
-        const int32_t qrow = int32_t(g.qo_start + int64_t(g.t) * a.q_tile);
-        tma_load_3d(base + kOffQ, &prm.tm_q, 0, g.hk * group, qrow, qf);
-        tma_load_3d(base + kOffQ + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
+        mbar_arrive_expect_tx(qf, 256u * tile_rows * uint32_t(g.nq));
+        for (int x = 0; x < g.nq; ++x) {
+          const int32_t qrow = int32_t(g.qo_start + int64_t(g.t) * a.q_tile + x * a.tile_tokens);
+          const uint32_t dst = base + kOffQ + x * kTileBytes;
+          tma_load_3d(dst, &prm.tm_q, 0, g.hk * group, qrow, qf);
+          tma_load_3d(dst + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
+        }
       }
       ++ua;
       for (int i = 0; i < g.ntiles && ok; ++i) {
@@ -302,65 +406,93 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
+    // Per KV tile i of a unit, for each live query tile x (0 = A, 1 = B):
+    //   S_x(i+1) = Q_x K_{i+1}^T as soon as softmax_x has read S_x(i), then
+    //   O_x += P_x(i) V_i as soon as softmax_x has written P_x(i).
     if (lane == 0) {
       uint32_t ua = 0, jt = 0;
+      uint32_t n_s[2] = {0, 0}, n_p[2] = {0, 0}, n_u[2] = {0, 0};
       bool ok = true;
-      auto issue_pv = [&](uint32_t jt_pv, bool first) -> bool {
-        const uint32_t use = 2 * jt_pv + 1;
-        const int slot = int(use % kSlots);
-        if (!mbar_wait(smem_u32(&bars.p_full), jt_pv & 1u, err, ERR_WAIT_SOFTMAX)) return false;
-        if (first && !mbar_wait(smem_u32(&bars.o_free), (ua & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
-          return false;
-        if (!mbar_wait(smem_u32(&bars.slot_full[slot]), (use / kSlots) & 1u, err, ERR_WAIT_FULL))
+      auto issue_s = [&](int x, uint32_t kslot) -> bool {
+        if (!mbar_wait(smem_u32(&bars.s_empty[x]), (n_s[x] & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
           return false;
         tc_fence_after();
-        const uint32_t pbase = base + kOffP;
-        const uint32_t vbase = base + kOffRing + slot * kTileBytes;
+        const uint32_t qbase = base + kOffQ + x * kTileBytes;
+        const uint32_t kbase = base + kOffRing + kslot * kTileBytes;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
+          mma_f16(tmem + kColS + x * 128, smem_desc(qbase + koff, 16, 1024),
+                  smem_desc(kbase + koff, 16, 1024), prm.idesc_s, k > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars.s_full[x]));
+        ++n_s[x];
+        return true;
+      };
+      auto issue_pv = [&](int x, uint32_t vslot, bool first) -> bool {
+        if (!mbar_wait(smem_u32(&bars.p_full[x]), n_p[x] & 1u, err, ERR_WAIT_SOFTMAX))
+          return false;
+        if (first &&
+            !mbar_wait(smem_u32(&bars.o_free[x]), (n_u[x] & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
+          return false;
+        tc_fence_after();
+        const uint32_t pbase = base + kOffP + x * kTileBytes;
+        const uint32_t vbase = base + kOffRing + vslot * kTileBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t ad = smem_desc(pbase + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
           const uint64_t bd = smem_desc(vbase + k * kChunk * 128, kHalf, 1024);
-          mma_f16(tmem + kColO, ad, bd, prm.idesc_pv, (first && k == 0) ? 0u : 1u);
+          mma_f16(tmem + kColO + x * 128, ad, bd, prm.idesc_pv, (first && k == 0) ? 0u : 1u);
         }
-        mma_commit(smem_u32(&bars.o_done));
-        mma_commit(smem_u32(&bars.slot_empty[slot]));
+        mma_commit(smem_u32(&bars.o_done[x]));
+        ++n_p[x];
         return true;
       };
-      for (int ui = u_begin; ui < u_end && ok; ++ui) {
-        const AGeo g = append_geo(a, ui);
+      auto slot_of = [](uint32_t use) { return use % kSlots; };
+      auto wait_slot = [&](uint32_t use) -> bool {
+        return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
+                         ERR_WAIT_FULL);
+      };
+      for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+      for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok; ++ui) {
+        AGeo g = append_geo(a, ui);
+        g.nq = min(g.nq, NQ);
         if (g.ntiles == 0) continue;
-        if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL)) break;
-        const uint32_t qbase = base + kOffQ;
-        for (int i = 0; i < g.ntiles; ++i, ++jt) {
-          const uint32_t use = 2 * jt;
-          const int slot = int(use % kSlots);
-          const int sb = jt & 1;
-          if (!mbar_wait(smem_u32(&bars.slot_full[slot]), (use / kSlots) & 1u, err,
-                         ERR_WAIT_FULL) ||
-              !mbar_wait(smem_u32(&bars.s_empty[sb]), ((jt >> 1) & 1u) ^ 1u, err,
-                         ERR_WAIT_SOFTMAX)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kbase = base + kOffRing + slot * kTileBytes;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-            mma_f16(tmem + kColS + sb * 128, smem_desc(qbase + koff, 16, 1024),
-                    smem_desc(kbase + koff, 16, 1024), prm.idesc_s, k > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bars.s_full[sb]));
-          mma_commit(smem_u32(&bars.slot_empty[slot]));
-          if (i == g.ntiles - 1) mma_commit(smem_u32(&bars.q_empty));
-          if (i > 0 && !issue_pv(jt - 1, i == 1)) {
-            ok = false;
-            break;
-          }
+        if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) ||
+            !wait_slot(2 * jt)) {
+          ok = false;
+          break;
         }
-        if (ok && !issue_pv(jt - 1, g.ntiles == 1)) ok = false;
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (x < g.nq && ok) ok = issue_s(x, slot_of(2 * jt));
+        mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jt)]));
+        for (int i = 0; i < g.ntiles && ok; ++i) {
+          const uint32_t jk = jt + i + 1;  // next K tile
+          const bool more = i + 1 < g.ntiles;
+          if ((more && !wait_slot(2 * jk)) || !wait_slot(2 * (jt + i) + 1)) {
+            ok = false;
+            break;
+          }
+          if (more) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+              if (x < g.nq && ok) ok = issue_s(x, slot_of(2 * jk));
+            mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jk)]));
+          }
+#pragma unroll
+          for (int x = 0; x < 2; ++x)
+            if (x < g.nq && ok) ok = issue_pv(x, slot_of(2 * (jt + i) + 1), i == 0);
+          mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * (jt + i) + 1)]));
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bars.q_empty));
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (x < g.nq) ++n_u[x];
+        jt += g.ntiles;
         ++ua;
       }
       // drain: no MMA may still be writing TMEM when it is freed
@@ -368,21 +500,32 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       mbar_wait(smem_u32(&bars.drain), 0, err, ERR_WAIT_DRAIN);
     }
     __syncwarp();
+  }
   } else {
     // ------------------------------------------------- softmax / epilogue
-    const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int rho = quarter * 32 + lane;     // row of the query tile
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int x = (warp - kWarpSoftmax0) / 4;  // query tile of this warpgroup
+    const int quarter = warp & 3;               // TMEM lanes this warp may access
+    const int rho_t = quarter * 32 + lane;      // row within the query tile
+    const int rho = x * kTile + rho_t;          // row within the item
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const uint32_t col_s = kColS + x * 128;
+    const uint32_t col_o = kColO + x * 128;
     const int tok = rho / group;
     const int hh = rho - tok * group;
     const float c2 = prm.scale_log2;
-    uint8_t* pbuf = gbase + kOffP;
-    uint32_t ua = 0, jt = 0;
-    bool ok = true;
-    for (int ui = u_begin; ui < u_end && ok; ++ui) {
-      const AGeo g = append_geo(a, ui);
+    uint8_t* pbuf = gbase + kOffP + x * kTileBytes;
+    uint32_t jt = 0, n_t = 0;
+    bool ok = x < NQ;  // a one-tile kernel leaves the second warpgroup idle
+    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+    for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok; ++ui) {
+      AGeo g = append_geo(a, ui);
+      g.nq = min(g.nq, NQ);
       const int64_t qi = int64_t(g.t) * a.q_tile + tok;
-      const bool row_ok = (tok < a.q_tile) && (qi < g.qo_len);
+      const bool row_ok = (rho < a.rows_per_item) && (qi < g.qo_len);
+      // warps whose 32 rows hold no query (short query tiles, decode mode)
+      // only keep the barrier protocol and write zero probabilities
+      const bool warp_live = __any_sync(0xffffffffu, row_ok);
       const int64_t orow = (g.qo_start + qi) * a.num_qo_heads + int64_t(g.hk) * group + hh;
       const int64_t limit = a.causal ? (g.kv_len - g.qo_len + qi) : (g.kv_len - 1);
       const int64_t row_end = row_ok ? min(g.tok_end, limit + 1) : g.tok_begin;
@@ -393,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
             for (int i = 0; i < 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
             if (a.lse) a.lse[orow] = -INFINITY;
           } else {
-            const int64_t prow = int64_t(g.slot) * kTile + rho;
+            const int64_t prow = int64_t(g.slot) * a.rows_per_item + rho;
             float4* dst = reinterpret_cast<float4*>(a.ws.partial_o + prow * kHeadDim);
             for (int i = 0; i < 32; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             a.ws.partial_lse[prow] = -INFINITY;
@@ -401,116 +544,142 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         }
         continue;
       }
+      const uint32_t jt0 = jt;
+      jt += g.ntiles;
+      if (x >= g.nq) continue;  // this query tile holds no queries for the item
       float m_ref = -INFINITY, l = 0.f;
-      for (int i = 0; i < g.ntiles; ++i, ++jt) {
-        const int sb = jt & 1;
+      for (int i = 0; i < g.ntiles; ++i, ++n_t) {
         // waits are made warp-uniform: tcgen05.ld/st below are .sync.aligned
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(smem_u32(&bars.s_full[sb]), (jt >> 1) & 1u, err, ERR_WAIT_MMA))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[x]), n_t & 1u, err,
+                                               ERR_WAIT_MMA))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float s[kTile];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float tmp[32];
-          tmem_ld32(tmem + lane_off + kColS + sb * 128 + c * 32, tmp);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) s[c * 32 + x] = tmp[x];
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.s_empty[sb]));
-
         const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
         const int nvalid = int(max(int64_t(0), min(int64_t(kTile), row_end - kv0)));
+        // the row of S_x into registers, then S_x is free for the next MMA
+        float v[kTile];
+        if (warp_live) tmem_ld128(tmem + lane_off + col_s, v);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.s_empty[x]));
+        // Tiles without masked columns (all but the causal diagonal and the
+        // unit's last tile) skip the per-element selects. Rows without a
+        // query may take the fast path too: their P row only feeds their own
+        // O row, which is never stored.
+        const bool full = __all_sync(0xffffffffu, !row_ok || nvalid == kTile);
         float mx = -INFINITY;
+        if (!warp_live) {
+        } else if (full) {
+          float m0 = fmax3(v[0], v[1], v[2]), m1 = fmax3(v[3], v[4], v[5]);
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          s[c] = (c < nvalid) ? s[c] : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+          for (int c = 6; c + 3 < kTile; c += 4) {
+            m0 = fmax3(m0, v[c], v[c + 1]);
+            m1 = fmax3(m1, v[c + 2], v[c + 3]);
+          }
+          mx = fmax3(m0, m1, fmaxf(v[kTile - 2], v[kTile - 1]));
+        } else {
+          mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, (c < nvalid) ? v[c] : -INFINITY);
         }
         const float m_tile = mx * c2;  // -inf stays -inf
         float alpha = 1.f;
         bool rescale_o = false;
         if (m_tile > m_ref + 8.f) {
           alpha = ex2(m_ref - m_tile);  // 0 when m_ref = -inf
-          rescale_o = (i > 0) && (m_ref != -INFINITY);
+          rescale_o = row_ok && (i > 0) && (m_ref != -INFINITY);
           l *= alpha;
           m_ref = m_tile;
         }
-        // probabilities, packed to the MMA input type right away (2 per word)
-        float lsum = 0.f;
-        uint32_t pk[kTile / 2];
-        if (m_ref != -INFINITY) {
-#pragma unroll
-          for (int c = 0; c < kTile; c += 2) {
-            const float p0 = ex2(fmaf(s[c], c2, -m_ref));
-            const float p1 = ex2(fmaf(s[c + 1], c2, -m_ref));
-            lsum += p0 + p1;
-            pk[c / 2] = pack2<BF16>(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kTile / 2; ++c) pk[c] = 0u;
-        }
-        l += lsum;
-        // P_{j-1}'s MMA must be done before P is overwritten and O rescaled.
+        // P_x(i-1)'s MMA must be done before P_x is overwritten and O_x rescaled.
         if (i > 0) {
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait(smem_u32(&bars.o_done), (jt - 1) & 1u, err, ERR_WAIT_MMA))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[x]), (n_t - 1) & 1u, err,
+                                                 ERR_WAIT_MMA))) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
-        // warp-uniform: tcgen05.ld/st are .sync.aligned
         if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float o[32];
-            const uint32_t ta = tmem + lane_off + kColO + c * 32;
+            const uint32_t ta = tmem + lane_off + col_o + c * 32;
             tmem_ld32(ta, o);
             const float f = rescale_o ? alpha : 1.f;
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= f;
+            for (int q = 0; q < 32; ++q) o[q] *= f;
             tmem_st32(ta, o);
           }
         }
-        // P row -> shared memory, 128B-swizzled K-major layout
+        // probabilities, packed to the MMA input type and written to shared
+        // memory in the 128B-swizzled K-major layout, 32 columns at a time
+        float2 lsum2 = make_float2(0.f, 0.f);
+        const bool live = m_ref != -INFINITY;
+        if (!warp_live) {
+          const uint32_t zero[16] = {};
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const int half = ch >> 3, cc = ch & 7;
-          *reinterpret_cast<uint4*>(pbuf + half * kHalf + rho * 128 + ((cc ^ (rho & 7)) << 4)) =
-              make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+          for (int c = 0; c < 4; ++c) store_p_chunk(pbuf, rho_t, c, zero);
+        } else if (full && __all_sync(0xffffffffu, live || !row_ok)) {
+          const float2 c2x2 = make_float2(c2, c2);
+          const float2 negm = make_float2(-m_ref, -m_ref);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              const float2 t = ffma2(make_float2(v[c * 32 + q], v[c * 32 + q + 1]), c2x2, negm);
+              const float2 pr = make_float2(ex2(t.x), ex2(t.y));
+              lsum2 = fadd2(lsum2, pr);
+              pk[q / 2] = pack2<BF16>(pr.x, pr.y);
+            }
+            store_p_chunk(pbuf, rho_t, c, pk);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              const int col = c * 32 + q;
+              float2 pr;
+              pr.x = (live && col < nvalid) ? ex2(fmaf(v[col], c2, -m_ref)) : 0.f;
+              pr.y = (live && col + 1 < nvalid) ? ex2(fmaf(v[col + 1], c2, -m_ref)) : 0.f;
+              lsum2 = fadd2(lsum2, pr);
+              pk[q / 2] = pack2<BF16>(pr.x, pr.y);
+            }
+            store_p_chunk(pbuf, rho_t, c, pk);
+          }
         }
-        // kv rows past the unit's end hold whatever the pool had: zero them in V
+        l += lsum2.x + lsum2.y;
+        // kv rows past the unit's end hold whatever the pool had: tile A's
+        // warpgroup zeroes them in V once this tile's V has landed
         const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
-        if (ntt < kTile) {
-          // wait for this tile's V to land before overwriting its tail rows
-          const uint32_t vuse = 2 * jt + 1;
+        if (x == 0 && ntt < kTile) {
+          const uint32_t vuse = 2 * (jt0 + i) + 1;
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.slot_full[vuse % kSlots]),
                                                  (vuse / kSlots) & 1u, err, ERR_WAIT_FULL))) {
             ok = false;
             break;
           }
-        }
-        if (ntt < kTile && rho >= ntt) {
-          uint8_t* vrow = gbase + kOffRing + (2 * jt + 1) % kSlots * kTileBytes + rho * 128;
+          if (rho_t >= ntt) {
+            uint8_t* vrow = gbase + kOffRing + (vuse % kSlots) * kTileBytes + rho_t * 128;
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            *reinterpret_cast<uint4*>(vrow + x * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vrow + kHalf + x * 16) = make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < 8; ++q) {
+              *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vrow + kHalf + q * 16) = make_uint4(0, 0, 0, 0);
+            }
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.p_full));
+        mbar_arrive(smem_u32(&bars.p_full[x]));
       }
       if (!ok) break;
       // ---- epilogue: O / l
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(smem_u32(&bars.o_done), (jt - 1) & 1u, err, ERR_WAIT_MMA))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[x]), (n_t - 1) & 1u, err,
+                                             ERR_WAIT_MMA))) {
         ok = false;
         break;
       }
@@ -519,28 +688,29 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       const float inv = any ? 1.f / l : 0.f;
       const float lse2 = any ? m_ref + lg2(l) : -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4 && warp_live; ++c) {
         float o[32];
-        tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+        tmem_ld32(tmem + lane_off + col_o + c * 32, o);
         if (row_ok) {
           if (g.slot < 0) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow * kHeadDim + c * 32);
+            uint4* dst =
+                reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow * kHeadDim + c * 32);
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
+            for (int q = 0; q < 4; ++q) {
               uint4 v;
-              v.x = pack2<BF16>(o[x * 8 + 0] * inv, o[x * 8 + 1] * inv);
-              v.y = pack2<BF16>(o[x * 8 + 2] * inv, o[x * 8 + 3] * inv);
-              v.z = pack2<BF16>(o[x * 8 + 4] * inv, o[x * 8 + 5] * inv);
-              v.w = pack2<BF16>(o[x * 8 + 6] * inv, o[x * 8 + 7] * inv);
-              dst[x] = v;
+              v.x = pack2<BF16>(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+              v.y = pack2<BF16>(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+              v.z = pack2<BF16>(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+              v.w = pack2<BF16>(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+              dst[q] = v;
             }
           } else {
-            const int64_t prow = int64_t(g.slot) * kTile + rho;
+            const int64_t prow = int64_t(g.slot) * a.rows_per_item + rho;
             float4* dst = reinterpret_cast<float4*>(a.ws.partial_o + prow * kHeadDim + c * 32);
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              dst[x] = make_float4(o[x * 4] * inv, o[x * 4 + 1] * inv, o[x * 4 + 2] * inv,
-                                   o[x * 4 + 3] * inv);
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(o[q * 4] * inv, o[q * 4 + 1] * inv, o[q * 4 + 2] * inv,
+                                   o[q * 4 + 3] * inv);
           }
         }
       }
@@ -548,12 +718,11 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         if (g.slot < 0) {
           if (a.lse) a.lse[orow] = lse2 * kLn2;
         } else {
-          a.ws.partial_lse[int64_t(g.slot) * kTile + rho] = lse2;
+          a.ws.partial_lse[int64_t(g.slot) * a.rows_per_item + rho] = lse2;
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.o_free));
-      ++ua;
+      mbar_arrive(smem_u32(&bars.o_free[x]));
     }
   }
 
@@ -561,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
@@ -597,16 +766,17 @@ uint32_t make_idesc(bool bf16, bool b_mn_major) {
          | ((128u >> 4) << 24);                                 // M = 128
 }
 
-template <bool BF16>
+template <bool BF16, int NQ>
 cudaError_t launch_t(AppendParams& prm, int ctas, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(append_kernel<BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(append_kernel<BF16, NQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Layout<NQ>::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  append_kernel<BF16><<<ctas, kThreads, kSmemBytes, stream>>>(prm);
+  append_kernel<BF16, NQ><<<ctas, kThreads, Layout<NQ>::SMEM, stream>>>(prm);
   return cudaGetLastError();
 }
 
@@ -615,7 +785,10 @@ cudaError_t launch_t(AppendParams& prm, int ctas, cudaStream_t stream) {
 int append_ctas_per_sm() { return 1; }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char** msg) {
-  if (a.group * a.q_tile != kTile) {
+  const bool decode_mode = a.qo_indptr == nullptr;
+  if (a.group * a.tile_tokens > kTile || a.rows_per_item != a.group * a.q_tile ||
+      (!decode_mode && (a.group * a.tile_tokens != kTile || a.q_tile != 2 * a.tile_tokens)) ||
+      (decode_mode && (a.q_tile != 1 || a.tile_tokens != 1))) {
     *msg = "attn_append_run: num_qo_heads / num_kv_heads must divide 128";
     return cudaErrorNotSupported;
   }
@@ -642,7 +815,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
                                 cuuint64_t(a.total_qo)};
     const cuuint64_t strides[2] = {cuuint64_t(kHeadDim) * 2,
                                    cuuint64_t(kHeadDim) * 2 * a.num_qo_heads};
-    const cuuint32_t box[3] = {64u, cuuint32_t(a.group), cuuint32_t(a.q_tile)};
+    const cuuint32_t box[3] = {64u, cuuint32_t(a.group), cuuint32_t(a.tile_tokens)};
     const cuuint32_t es[3] = {1, 1, 1};
     if (enc(&prm.tm_q, dt, 3, const_cast<void*>(a.q), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -670,7 +843,17 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
       return cudaErrorInvalidValue;
     }
   }
-  return bf16 ? launch_t<true>(prm, a.num_ctas, stream) : launch_t<false>(prm, a.num_ctas, stream);
+  // at most one CTA per SM (shared memory); extra plan CTAs are run in turn
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = a.num_ctas < sms ? a.num_ctas : sms;
+  // one query tile per item suffices when no request has more queries than a tile
+  const bool one_tile = decode_mode || a.max_qo_len <= a.tile_tokens;
+  if (bf16)
+    return one_tile ? launch_t<true, 1>(prm, grid, stream) : launch_t<true, 2>(prm, grid, stream);
+  return one_tile ? launch_t<false, 1>(prm, grid, stream) : launch_t<false, 2>(prm, grid, stream);
 }
 
 }  // namespace attn

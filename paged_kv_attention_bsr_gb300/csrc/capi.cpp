@@ -93,7 +93,7 @@ attn_status_t attn_workspace_size(int32_t max_batch, int32_t max_total_qo,
     return fail(ATTN_ERR_UNSUPPORTED, "attn_workspace_size: only head_dim == 128");
   const int64_t group = num_qo_heads / num_kv_heads;
   const bool append_ok = (kTileRows % group == 0);
-  const int64_t q_tile = append_ok ? kTileRows / group : 1;
+  const int64_t q_tile = append_ok ? kItemRows / group : 1;
   int64_t items = int64_t(max_batch) * num_kv_heads;
   if (append_ok)
     items = std::max<int64_t>(
@@ -103,7 +103,7 @@ attn_status_t attn_workspace_size(int32_t max_batch, int32_t max_total_qo,
   const int64_t units = items + C;
   const int64_t split = std::min<int64_t>(items, C);
   const int64_t slots = std::min<int64_t>(units, 2 * C);
-  const int32_t rows = append_ok ? kTileRows : int32_t(group);
+  const int32_t rows = append_ok ? kItemRows : int32_t(group);
   const PlanLayout L = plan_layout(num_ctas, units, split, slots, rows, head_dim);
   *dev_bytes = size_t(L.dev_bytes);
   *pinned_host_bytes = size_t(L.table_bytes);
@@ -168,6 +168,59 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
   if (group > kMaxDecodeGroup)
     return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_run: group > 8 is not implemented");
   if (plan->batch == 0) return ATTN_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (group >= kTensorDecodeGroup && layout == ATTN_LAYOUT_HND && plan->page_size % 16 == 0) {
+    // Large GQA groups: the per-token work (group heads x 128 dims, twice)
+    // outruns the CUDA cores before HBM saturates, so the group's query rows
+    // go through the tensor-core kernel as one M = 128 tile instead.
+    AppendArgs a;
+    a.q = q;
+    a.qo_indptr = nullptr;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.num_pages = num_pages;
+    a.kv_indptr = kv_indptr;
+    a.kv_indices = kv_indices;
+    a.last_page_len = last_page_len;
+    a.o = o;
+    a.lse = lse;
+    a.ws = ws_view(*plan, dev_ws);
+    a.num_ctas = plan->num_ctas;
+    a.num_units = plan->num_units;
+    a.num_split_items = plan->num_split_items;
+    a.dtype = dtype;
+    a.page_size = plan->page_size;
+    a.num_qo_heads = plan->num_qo_heads;
+    a.num_kv_heads = plan->num_kv_heads;
+    a.group = group;
+    a.q_tile = 1;
+    a.tile_tokens = 1;
+    a.rows_per_item = group;
+    a.total_qo = plan->batch;
+    a.max_qo_len = 1;
+    a.causal = 0;
+    a.sm_scale = sm_scale;
+    const char* msg = "";
+    cudaError_t e = launch_append(a, st, &msg);
+    if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: tensor-core decode launch");
+    if (plan->num_split_items > 0) {
+      SplitMergeArgs m;
+      m.ws = a.ws;
+      m.num_split_items = plan->num_split_items;
+      m.rows_per_item = plan->rows_per_item;
+      m.group = group;
+      m.q_tile = 1;
+      m.num_qo_heads = plan->num_qo_heads;
+      m.qo_indptr = nullptr;
+      m.o = o;
+      m.lse = lse;
+      m.dtype = dtype;
+      e = launch_split_merge(m, st);
+      if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: merge kernel launch");
+    }
+    return ATTN_OK;
+  }
   DecodeArgs a;
   a.q = q;
   a.k_pool = k_pool;
@@ -189,7 +242,6 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
   a.group = group;
   a.batch = plan->batch;
   a.sm_scale = sm_scale;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode(a, st);  // split items are merged inside the kernel
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: decode kernel launch");
   return ATTN_OK;
@@ -236,7 +288,10 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
   a.num_kv_heads = plan->num_kv_heads;
   a.group = plan->num_qo_heads / plan->num_kv_heads;
   a.q_tile = plan->q_tile;
+  a.tile_tokens = kTileRows / a.group;
+  a.rows_per_item = plan->rows_per_item;
   a.total_qo = plan->total_qo;
+  a.max_qo_len = plan->max_qo_len;
   a.causal = plan->causal;
   a.sm_scale = sm_scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -12,8 +12,10 @@
 namespace attn {
 
 constexpr int kHeadDim = 128;
-constexpr int kTileRows = 128;      // packed query rows of one append tile
+constexpr int kTileRows = 128;      // packed query rows of one MMA tile (M = 128)
+constexpr int kItemRows = 256;      // packed query rows of one append item (2 tiles)
 constexpr int kMaxDecodeGroup = 8;  // query heads per kv head, decode kernel
+constexpr int kTensorDecodeGroup = 8;  // decode groups >= this use the tensor-core kernel
 constexpr int kUnitInts = 8;        // int32 words per work-unit record
 constexpr int64_t kHeaderBytes = 256;
 
@@ -127,12 +129,17 @@ struct AppendArgs {
   int32_t num_qo_heads;
   int32_t num_kv_heads;
   int32_t group;
-  int32_t q_tile;
+  int32_t q_tile;          // query tokens per item (1 in decode mode)
+  int32_t tile_tokens;     // query tokens per 128-row MMA tile (1 in decode mode)
+  int32_t rows_per_item;   // group * q_tile (<= 128)
   int32_t total_qo;
+  int32_t max_qo_len;      // longest query count of a request
   int32_t causal;
   float sm_scale;
 };
-// Returns cudaErrorNotSupported for shapes the kernel does not handle.
+// qo_indptr == NULL runs the kernel in decode mode (one query row per
+// request; q is [batch, Hq, D]). Returns cudaErrorNotSupported for shapes the
+// kernel does not handle.
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char** msg);
 int append_ctas_per_sm();
 

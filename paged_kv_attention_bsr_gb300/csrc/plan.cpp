@@ -101,11 +101,11 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
     *msg = "attn_plan: decode supports num_qo_heads / num_kv_heads <= 8";
     return ATTN_ERR_UNSUPPORTED;
   }
-  if (!decode && (group > kTileRows || kTileRows % group != 0)) {
+  if (!decode && (group > kTileRows || kTileRows % group != 0)) {  // a tile holds whole tokens
     *msg = "attn_plan: append needs num_qo_heads / num_kv_heads to divide 128";
     return ATTN_ERR_UNSUPPORTED;
   }
-  const int32_t q_tile = decode ? 1 : kTileRows / group;
+  const int32_t q_tile = decode ? 1 : kItemRows / group;
   const int32_t rows_per_item = group * q_tile;
 
   // ---- validate the table and build items
@@ -119,6 +119,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   }
   std::vector<Item> items;
   items.reserve(size_t(batch) * num_kv_heads);
+  int64_t max_qo_len = decode ? 1 : 0;
   for (int32_t r = 0; r < batch; ++r) {
     const int64_t n_pages = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
     if (n_pages < 0) {
@@ -137,6 +138,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         *msg = "attn_plan: qo_indptr must be non-decreasing";
         return ATTN_ERR_INVALID_ARG;
       }
+      max_qo_len = std::max(max_qo_len, qo_len);
       if (causal && kv_len < qo_len) {
         *msg = "attn_plan: causal append needs kv_len >= qo_len for every request";
         return ATTN_ERR_INVALID_ARG;
@@ -303,6 +305,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   p.num_split_items = int32_t(S);
   p.num_slots = slots;
   p.total_qo = decode ? batch : (qo_indptr[batch] - qo_indptr[0]);
+  p.max_qo_len = int32_t(max_qo_len);
   p.total_weight = W;
   p.max_cta_weight = max_load;
   p.off_work_indptr = L.off_work_indptr;

@@ -83,7 +83,7 @@ def test_plan_bit_exact_vs_reference(decode):
 def _pages_of_items(kv_indptr, last, P, Hk, g, qo, causal):
     items = {}
     B = len(kv_indptr) - 1
-    tq = 1 if qo is None else 128 // g
+    tq = 1 if qo is None else 256 // g
     for r in range(B):
         kv_len = plan_ref.kv_length(kv_indptr, last, P, r)
         qo_len = 1 if qo is None else qo[r + 1] - qo[r]
