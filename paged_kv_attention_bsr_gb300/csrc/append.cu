@@ -19,15 +19,18 @@
 //   S_x = Q_x K_j^T          A = Q_x (smem, K-major), B = K (smem, K-major),
 //                            D = TMEM S_x
 //   P_x = exp2(S_x*c - m)    softmax warpgroup x, one TMEM lane (= row) per
-//                            thread; P_x to shared memory (bf16/fp16)
-//   O_x += P_x V_j           A = P_x (smem, K-major), B = V (smem, MN-major),
-//                            D = TMEM O_x
+//                            thread; P_x (bf16/fp16) written over S_x in TMEM
+//   O_x += P_x V_j           A = P_x (TMEM), B = V (smem, MN-major), D = TMEM O_x
+// Keeping P in tensor memory halves the shared-memory traffic of P.V (only V
+// is read from shared memory) and removes P's shared-memory writes; with
+// both MMA operands in shared memory the kernel would be bound by shared
+// memory bandwidth well before the tensor core.
 // Warp roles (320 threads, one CTA per SM): warps 0-3 and 4-7 are the softmax
 // warpgroups of tiles A and B (lazy O rescale only when a row max grows by
 // more than 2^8, epilogue from TMEM); warp 8 issues TMA loads through a ring
-// of three 32 KB K/V slots; warp 9 allocates TMEM and issues the MMAs from
-// one thread, S_x(j+1) as soon as softmax x has read S_x(j), so the tensor
-// core works on one tile's S while the other tile's softmax runs.
+// of 32 KB K/V slots; warp 9 allocates TMEM and issues the MMAs from one
+// thread (P_x(j).V then S_x(j+1) per tile x), so the tensor core works on one
+// query tile while the other tile's softmax runs.
 // Every wait is bounded; TMEM is freed on every path.
 //
 // Decode mode (no qo_indptr): one query row per request; an item is the
@@ -63,21 +66,23 @@ constexpr int kRegsSoftmax = 192;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // S_A at 0, S_B at 128
-constexpr uint32_t kColO = 256;  // O_A at 256, O_B at 384
+// TMEM columns of query tile x: S_x (then P_x, packed 16-bit, over its first
+// 64 columns) at 256 x, O_x at 256 x + 128.
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 128;
+constexpr uint32_t kColTile = 256;
 
 // Shared memory map (offsets from a 1024-byte aligned base) for NQ query
 // tiles per item. K and V tiles travel through one ring of SLOTS 32 KB slots:
 // KV tile j's K takes slot use 2j and its V use 2j + 1 (slot = use % SLOTS).
-// With one query tile (decode mode, short queries) the second tile's Q and P
-// space becomes two more ring slots, i.e. deeper prefetch for HBM-bound runs.
-constexpr int kMaxSlots = 5;
+// P never touches shared memory: it is written over S in TMEM and the P.V
+// MMA reads it from there.
+constexpr int kMaxSlots = 6;
 template <int NQ>
 struct Layout {
-  static constexpr int SLOTS = NQ == 2 ? 3 : 5;
+  static constexpr int SLOTS = NQ == 2 ? 5 : 6;
   static constexpr int OFF_Q = 0;                            // query tiles
-  static constexpr int OFF_P = OFF_Q + NQ * kTileBytes;      // probabilities
-  static constexpr int OFF_RING = OFF_P + NQ * kTileBytes;   // K/V ring
+  static constexpr int OFF_RING = OFF_Q + NQ * kTileBytes;   // K/V ring
   static constexpr int OFF_BAR = OFF_RING + SLOTS * kTileBytes;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;         // + barriers + alignment slack
 };
@@ -86,7 +91,7 @@ static_assert(Layout<1>::OFF_BAR == Layout<2>::OFF_BAR, "both layouts fill 224 K
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t slot_full[kMaxSlots], slot_empty[kMaxSlots];
-  uint64_t s_full[2], s_empty[2];
+  uint64_t s_full[2];
   uint64_t p_full[2], o_done[2], o_free[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -117,6 +122,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]: A read from tensor memory (K-major, two
+// 16-bit elements per 32-bit column, row m in lane m).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -164,6 +180,20 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -205,19 +235,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
       : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
         "l"(*reinterpret_cast<const unsigned long long*>(&b)));
   return d;
-}
-
-// 32 probabilities (16 packed words) of row `row` into columns [32c, 32c+32)
-// of the 128B-swizzled K-major P tile (two 64-column halves).
-__device__ __forceinline__ void store_p_chunk(uint8_t* pbuf, int row, int c,
-                                              const uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int ch = c * 4 + u;  // 16-byte chunk of the 256-byte row
-    const int half = ch >> 3, cc = ch & 7;
-    *reinterpret_cast<uint4*>(pbuf + half * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) =
-        make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
-  }
 }
 
 template <bool BF16>
@@ -277,7 +294,6 @@ template <bool BF16, int NQ>
 __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_constant__ AppendParams prm) {
   constexpr int kSlots = Layout<NQ>::SLOTS;
   constexpr int kOffQ = Layout<NQ>::OFF_Q;
-  constexpr int kOffP = Layout<NQ>::OFF_P;
   constexpr int kOffRing = Layout<NQ>::OFF_RING;
   constexpr int kOffBar = Layout<NQ>::OFF_BAR;
   extern __shared__ uint8_t smem_raw[];
@@ -299,7 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.s_empty[i]), 128);
       mbar_init(smem_u32(&bars.p_full[i]), 128);
       mbar_init(smem_u32(&bars.o_done[i]), 1);
       mbar_init(smem_u32(&bars.o_free[i]), 128);
@@ -408,28 +423,31 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Per KV tile i of a unit, for each live query tile x (0 = A, 1 = B):
-    //   S_x(i+1) = Q_x K_{i+1}^T as soon as softmax_x has read S_x(i), then
-    //   O_x += P_x(i) V_i as soon as softmax_x has written P_x(i).
+    // Per KV tile i of a unit, for each live query tile x (0 = A, 1 = B), in
+    // issue order: O_x += P_x(i) V_i once softmax x has written P_x(i) into
+    // TMEM, then S_x(i+1) = Q_x K_{i+1}^T into the same columns. The tensor
+    // core runs in issue order, so S_x(i+1) completing (s_full) also means
+    // P_x(i) has been consumed and O_x is up to date. While tile A's softmax
+    // runs, the tensor core works on tile B's P.V and S, and vice versa.
     if (lane == 0) {
       uint32_t ua = 0, jt = 0;
-      uint32_t n_s[2] = {0, 0}, n_p[2] = {0, 0}, n_u[2] = {0, 0};
+      uint32_t n_p[2] = {0, 0}, n_u[2] = {0, 0};
       bool ok = true;
-      auto issue_s = [&](int x, uint32_t kslot) -> bool {
-        if (!mbar_wait(smem_u32(&bars.s_empty[x]), (n_s[x] & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
-          return false;
-        tc_fence_after();
+      auto slot_of = [&](uint32_t use) { return use % kSlots; };
+      auto wait_slot = [&](uint32_t use) -> bool {
+        return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
+                         ERR_WAIT_FULL);
+      };
+      auto issue_s = [&](int x, uint32_t kslot) {
         const uint32_t qbase = base + kOffQ + x * kTileBytes;
         const uint32_t kbase = base + kOffRing + kslot * kTileBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-          mma_f16(tmem + kColS + x * 128, smem_desc(qbase + koff, 16, 1024),
+          mma_f16(tmem + x * kColTile + kColS, smem_desc(qbase + koff, 16, 1024),
                   smem_desc(kbase + koff, 16, 1024), prm.idesc_s, k > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&bars.s_full[x]));
-        ++n_s[x];
-        return true;
       };
       auto issue_pv = [&](int x, uint32_t vslot, bool first) -> bool {
         if (!mbar_wait(smem_u32(&bars.p_full[x]), n_p[x] & 1u, err, ERR_WAIT_SOFTMAX))
@@ -438,22 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
             !mbar_wait(smem_u32(&bars.o_free[x]), (n_u[x] & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
           return false;
         tc_fence_after();
-        const uint32_t pbase = base + kOffP + x * kTileBytes;
         const uint32_t vbase = base + kOffRing + vslot * kTileBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = smem_desc(pbase + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
           const uint64_t bd = smem_desc(vbase + k * kChunk * 128, kHalf, 1024);
-          mma_f16(tmem + kColO + x * 128, ad, bd, prm.idesc_pv, (first && k == 0) ? 0u : 1u);
+          mma_f16_ts(tmem + x * kColTile + kColO, tmem + x * kColTile + kColS + k * 8, bd,
+                     prm.idesc_pv, (first && k == 0) ? 0u : 1u);
         }
         mma_commit(smem_u32(&bars.o_done[x]));
         ++n_p[x];
         return true;
-      };
-      auto slot_of = [](uint32_t use) { return use % kSlots; };
-      auto wait_slot = [&](uint32_t use) -> bool {
-        return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
-                         ERR_WAIT_FULL);
       };
       for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
       for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok; ++ui) {
@@ -465,27 +477,27 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
           ok = false;
           break;
         }
+        tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x)
-          if (x < g.nq && ok) ok = issue_s(x, slot_of(2 * jt));
+          if (x < g.nq) issue_s(x, slot_of(2 * jt));
         mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jt)]));
         for (int i = 0; i < g.ntiles && ok; ++i) {
           const uint32_t jk = jt + i + 1;  // next K tile
           const bool more = i + 1 < g.ntiles;
-          if ((more && !wait_slot(2 * jk)) || !wait_slot(2 * (jt + i) + 1)) {
+          if (!wait_slot(2 * (jt + i) + 1) || (more && !wait_slot(2 * jk))) {
             ok = false;
             break;
           }
-          if (more) {
 #pragma unroll
-            for (int x = 0; x < 2; ++x)
-              if (x < g.nq && ok) ok = issue_s(x, slot_of(2 * jk));
-            mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jk)]));
+          for (int x = 0; x < 2; ++x) {
+            if (x < g.nq && ok) {
+              ok = issue_pv(x, slot_of(2 * (jt + i) + 1), i == 0);
+              if (ok && more) issue_s(x, slot_of(2 * jk));
+            }
           }
-#pragma unroll
-          for (int x = 0; x < 2; ++x)
-            if (x < g.nq && ok) ok = issue_pv(x, slot_of(2 * (jt + i) + 1), i == 0);
           mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * (jt + i) + 1)]));
+          if (more) mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jk)]));
         }
         if (!ok) break;
         mma_commit(smem_u32(&bars.q_empty));
@@ -509,12 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
     const int rho_t = quarter * 32 + lane;      // row within the query tile
     const int rho = x * kTile + rho_t;          // row within the item
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const uint32_t col_s = kColS + x * 128;
-    const uint32_t col_o = kColO + x * 128;
+    const uint32_t col_s = x * kColTile + kColS;
+    const uint32_t col_o = x * kColTile + kColO;
     const int tok = rho / group;
     const int hh = rho - tok * group;
     const float c2 = prm.scale_log2;
-    uint8_t* pbuf = gbase + kOffP + x * kTileBytes;
     uint32_t jt = 0, n_t = 0;
     bool ok = x < NQ;  // a one-tile kernel leaves the second warpgroup idle
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
@@ -524,7 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       const int64_t qi = int64_t(g.t) * a.q_tile + tok;
       const bool row_ok = (rho < a.rows_per_item) && (qi < g.qo_len);
       // warps whose 32 rows hold no query (short query tiles, decode mode)
-      // only keep the barrier protocol and write zero probabilities
+      // only keep the barrier protocol: their P rows feed O rows that are
+      // never stored
       const bool warp_live = __any_sync(0xffffffffu, row_ok);
       const int64_t orow = (g.qo_start + qi) * a.num_qo_heads + int64_t(g.hk) * group + hh;
       const int64_t limit = a.causal ? (g.kv_len - g.qo_len + qi) : (g.kv_len - 1);
@@ -558,101 +570,87 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         tc_fence_after();
         const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
         const int nvalid = int(max(int64_t(0), min(int64_t(kTile), row_end - kv0)));
-        // the row of S_x into registers, then S_x is free for the next MMA
-        float v[kTile];
-        if (warp_live) tmem_ld128(tmem + lane_off + col_s, v);
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.s_empty[x]));
-        // Tiles without masked columns (all but the causal diagonal and the
-        // unit's last tile) skip the per-element selects. Rows without a
-        // query may take the fast path too: their P row only feeds their own
-        // O row, which is never stored.
-        const bool full = __all_sync(0xffffffffu, !row_ok || nvalid == kTile);
-        float mx = -INFINITY;
-        if (!warp_live) {
-        } else if (full) {
-          float m0 = fmax3(v[0], v[1], v[2]), m1 = fmax3(v[3], v[4], v[5]);
+        if (warp_live) {
+          float v[kTile];
+          tmem_ld128(tmem + lane_off + col_s, v);
+          // Tiles without masked columns (all but the causal diagonal and the
+          // unit's last tile) skip the per-element selects; rows without a
+          // query may take that path too (their P row only feeds their own O
+          // row, which is never stored).
+          const bool full = __all_sync(0xffffffffu, !row_ok || nvalid == kTile);
+          float mx = -INFINITY;
+          if (full) {
+            float m0 = fmax3(v[0], v[1], v[2]), m1 = fmax3(v[3], v[4], v[5]);
 #pragma unroll
-          for (int c = 6; c + 3 < kTile; c += 4) {
-            m0 = fmax3(m0, v[c], v[c + 1]);
-            m1 = fmax3(m1, v[c + 2], v[c + 3]);
-          }
-          mx = fmax3(m0, m1, fmaxf(v[kTile - 2], v[kTile - 1]));
-        } else {
-          mx = -INFINITY;
+            for (int c = 6; c + 3 < kTile; c += 4) {
+              m0 = fmax3(m0, v[c], v[c + 1]);
+              m1 = fmax3(m1, v[c + 2], v[c + 3]);
+            }
+            mx = fmax3(m0, m1, fmaxf(v[kTile - 2], v[kTile - 1]));
+          } else {
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, (c < nvalid) ? v[c] : -INFINITY);
-        }
-        const float m_tile = mx * c2;  // -inf stays -inf
-        float alpha = 1.f;
-        bool rescale_o = false;
-        if (m_tile > m_ref + 8.f) {
-          alpha = ex2(m_ref - m_tile);  // 0 when m_ref = -inf
-          rescale_o = row_ok && (i > 0) && (m_ref != -INFINITY);
-          l *= alpha;
-          m_ref = m_tile;
-        }
-        // P_x(i-1)'s MMA must be done before P_x is overwritten and O_x rescaled.
-        if (i > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[x]), (n_t - 1) & 1u, err,
-                                                 ERR_WAIT_MMA))) {
-            ok = false;
-            break;
+            for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, (c < nvalid) ? v[c] : -INFINITY);
           }
-          tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, rescale_o)) {
+          const float m_tile = mx * c2;  // -inf stays -inf
+          float alpha = 1.f;
+          bool rescale_o = false;
+          if (m_tile > m_ref + 8.f) {
+            alpha = ex2(m_ref - m_tile);  // 0 when m_ref = -inf
+            rescale_o = row_ok && (i > 0) && (m_ref != -INFINITY);
+            l *= alpha;
+            m_ref = m_tile;
+          }
+          // O_x holds every earlier tile (S_x(i) completing implies P_x(i-1).V done)
+          if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            const uint32_t ta = tmem + lane_off + col_o + c * 32;
-            tmem_ld32(ta, o);
-            const float f = rescale_o ? alpha : 1.f;
+            for (int c = 0; c < 4; ++c) {
+              float o[32];
+              const uint32_t ta = tmem + lane_off + col_o + c * 32;
+              tmem_ld32(ta, o);
+              const float f = rescale_o ? alpha : 1.f;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] *= f;
-            tmem_st32(ta, o);
-          }
-        }
-        // probabilities, packed to the MMA input type and written to shared
-        // memory in the 128B-swizzled K-major layout, 32 columns at a time
-        float2 lsum2 = make_float2(0.f, 0.f);
-        const bool live = m_ref != -INFINITY;
-        if (!warp_live) {
-          const uint32_t zero[16] = {};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) store_p_chunk(pbuf, rho_t, c, zero);
-        } else if (full && __all_sync(0xffffffffu, live || !row_ok)) {
-          const float2 c2x2 = make_float2(c2, c2);
-          const float2 negm = make_float2(-m_ref, -m_ref);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int q = 0; q < 32; q += 2) {
-              const float2 t = ffma2(make_float2(v[c * 32 + q], v[c * 32 + q + 1]), c2x2, negm);
-              const float2 pr = make_float2(ex2(t.x), ex2(t.y));
-              lsum2 = fadd2(lsum2, pr);
-              pk[q / 2] = pack2<BF16>(pr.x, pr.y);
+              for (int q = 0; q < 32; ++q) o[q] *= f;
+              tmem_st32(ta, o);
             }
-            store_p_chunk(pbuf, rho_t, c, pk);
           }
-        } else {
+          // probabilities, packed to the MMA input type, written over S_x in
+          // TMEM (column c holds elements 2c, 2c+1 of the row)
+          float2 lsum2 = make_float2(0.f, 0.f);
+          const bool live = m_ref != -INFINITY;
+          if (full && __all_sync(0xffffffffu, live || !row_ok)) {
+            const float2 c2x2 = make_float2(c2, c2);
+            const float2 negm = make_float2(-m_ref, -m_ref);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
+            for (int c = 0; c < 4; ++c) {
+              uint32_t pk[16];
 #pragma unroll
-            for (int q = 0; q < 32; q += 2) {
-              const int col = c * 32 + q;
-              float2 pr;
-              pr.x = (live && col < nvalid) ? ex2(fmaf(v[col], c2, -m_ref)) : 0.f;
-              pr.y = (live && col + 1 < nvalid) ? ex2(fmaf(v[col + 1], c2, -m_ref)) : 0.f;
-              lsum2 = fadd2(lsum2, pr);
-              pk[q / 2] = pack2<BF16>(pr.x, pr.y);
+              for (int q = 0; q < 32; q += 2) {
+                const float2 t = ffma2(make_float2(v[c * 32 + q], v[c * 32 + q + 1]), c2x2, negm);
+                const float2 pr = make_float2(ex2(t.x), ex2(t.y));
+                lsum2 = fadd2(lsum2, pr);
+                pk[q / 2] = pack2<BF16>(pr.x, pr.y);
+              }
+              tmem_st16_nowait(tmem + lane_off + col_s + c * 16, pk);
             }
-            store_p_chunk(pbuf, rho_t, c, pk);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int q = 0; q < 32; q += 2) {
+                const int col = c * 32 + q;
+                float2 pr;
+                pr.x = (live && col < nvalid) ? ex2(fmaf(v[col], c2, -m_ref)) : 0.f;
+                pr.y = (live && col + 1 < nvalid) ? ex2(fmaf(v[col + 1], c2, -m_ref)) : 0.f;
+                lsum2 = fadd2(lsum2, pr);
+                pk[q / 2] = pack2<BF16>(pr.x, pr.y);
+              }
+              tmem_st16_nowait(tmem + lane_off + col_s + c * 16, pk);
+            }
           }
+          tmem_wait_st();
+          l += lsum2.x + lsum2.y;
         }
-        l += lsum2.x + lsum2.y;
         // kv rows past the unit's end hold whatever the pool had: tile A's
         // warpgroup zeroes them in V once this tile's V has landed
         const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
@@ -671,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
               *reinterpret_cast<uint4*>(vrow + kHalf + q * 16) = make_uint4(0, 0, 0, 0);
             }
           }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.p_full[x]));
       }
@@ -697,12 +695,12 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
                 reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow * kHeadDim + c * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = pack2<BF16>(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
-              v.y = pack2<BF16>(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
-              v.z = pack2<BF16>(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
-              v.w = pack2<BF16>(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
-              dst[q] = v;
+              uint4 w;
+              w.x = pack2<BF16>(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+              w.y = pack2<BF16>(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+              w.z = pack2<BF16>(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+              w.w = pack2<BF16>(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+              dst[q] = w;
             }
           } else {
             const int64_t prow = int64_t(g.slot) * a.rows_per_item + rho;
