@@ -85,62 +85,72 @@ __global__ void __launch_bounds__(256) merge_states_kernel(
   }
 }
 
-// One CTA per split item; warp w handles rows w, w+4, ...; lane owns 4 dims.
+// One warp per (split item, row): the warps of the whole grid share the
+// items' rows; lane owns 4 of the 128 dims. Each partial row is read once.
 template <bool BF16>
-__global__ void __launch_bounds__(128) split_merge_kernel(const SplitMergeArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int s = blockIdx.x; s < a.num_split_items; s += gridDim.x) {
-    const int4 item = __ldg(a.ws.merge_items + s);
-    const int r = item.x, hk = item.y, t = item.z;
-    const int slot0 = __ldg(a.ws.merge_indptr + s), slot1 = __ldg(a.ws.merge_indptr + s + 1);
-    int64_t qo_start = r, qo_len = 1;
-    if (a.qo_indptr) {
-      qo_start = __ldg(a.qo_indptr + r);
-      qo_len = int64_t(__ldg(a.qo_indptr + r + 1)) - qo_start;
+__global__ void __launch_bounds__(256) split_merge_kernel(const SplitMergeArgs a) {
+  const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= int64_t(a.num_split_items) * a.rows_per_item) return;
+  const int s = int(gw / a.rows_per_item);
+  const int rho = int(gw - int64_t(s) * a.rows_per_item);
+  const int4 item = __ldg(a.ws.merge_items + s);
+  const int r = item.x, hk = item.y, t = item.z;
+  int64_t qo_start = r, qo_len = 1;
+  if (a.qo_indptr) {
+    qo_start = __ldg(a.qo_indptr + r);
+    qo_len = int64_t(__ldg(a.qo_indptr + r + 1)) - qo_start;
+  }
+  const int tok = rho / a.group, hh = rho - tok * a.group;
+  const int64_t qi = int64_t(t) * a.q_tile + tok;
+  if (qi >= qo_len) return;
+  const int slot0 = __ldg(a.ws.merge_indptr + s), slot1 = __ldg(a.ws.merge_indptr + s + 1);
+  float lse_s[8];
+  float M = -INFINITY;
+  const int ns = slot1 - slot0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    lse_s[k] = k < ns ? __ldcg(a.ws.partial_lse + int64_t(slot0 + k) * a.rows_per_item + rho)
+                      : -INFINITY;
+    M = fmaxf(M, lse_s[k]);
+  }
+  for (int sl = slot0 + 8; sl < slot1; ++sl)
+    M = fmaxf(M, __ldcg(a.ws.partial_lse + int64_t(sl) * a.rows_per_item + rho));
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float lse2 = -INFINITY;
+  if (M != -INFINITY) {
+    float L = 0.f;
+    for (int sl = slot0; sl < slot1; ++sl) {
+      const int64_t prow = int64_t(sl) * a.rows_per_item + rho;
+      const float ls = sl - slot0 < 8 ? lse_s[(sl - slot0) & 7] : __ldcg(a.ws.partial_lse + prow);
+      const float f = ex2(ls - M);
+      L += f;
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(a.ws.partial_o + prow * kHeadDim) + lane);
+      acc[0] += f * x.x;
+      acc[1] += f * x.y;
+      acc[2] += f * x.z;
+      acc[3] += f * x.w;
     }
-    for (int rho = warp; rho < a.rows_per_item; rho += 4) {
-      const int tok = rho / a.group, hh = rho - tok * a.group;
-      const int64_t qi = int64_t(t) * a.q_tile + tok;
-      if (qi >= qo_len) continue;
-      float M = -INFINITY;
-      for (int sl = slot0; sl < slot1; ++sl)
-        M = fmaxf(M, a.ws.partial_lse[int64_t(sl) * a.rows_per_item + rho]);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      float lse2 = -INFINITY;
-      if (M != -INFINITY) {
-        float L = 0.f;
-        for (int sl = slot0; sl < slot1; ++sl) {
-          const int64_t prow = int64_t(sl) * a.rows_per_item + rho;
-          const float f = ex2(a.ws.partial_lse[prow] - M);
-          L += f;
-          const float4 x = *reinterpret_cast<const float4*>(a.ws.partial_o + prow * kHeadDim + lane * 4);
-          acc[0] += f * x.x;
-          acc[1] += f * x.y;
-          acc[2] += f * x.z;
-          acc[3] += f * x.w;
-        }
-        const float inv = 1.f / L;
+    const float inv = 1.f / L;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j] *= inv;
-        lse2 = M + lg2(L);
-      }
-      const int64_t orow = (qo_start + qi) * a.num_qo_heads + int64_t(hk) * a.group + hh;
-      uint32_t w[2];
+    for (int j = 0; j < 4; ++j) acc[j] *= inv;
+    lse2 = M + lg2(L);
+  }
+  const int64_t orow = (qo_start + qi) * a.num_qo_heads + int64_t(hk) * a.group + hh;
+  uint32_t w[2];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if constexpr (BF16) {
-          __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-          w[i] = *reinterpret_cast<uint32_t*>(&b);
-        } else {
-          __half2 h = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
-          w[i] = *reinterpret_cast<uint32_t*>(&h);
-        }
-      }
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.o) + orow * kHeadDim + lane * 4) =
-          make_uint2(w[0], w[1]);
-      if (lane == 0 && a.lse) a.lse[orow] = lse2 * kLn2;
+  for (int i = 0; i < 2; ++i) {
+    if constexpr (BF16) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&b);
+    } else {
+      __half2 h = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
     }
   }
+  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.o) + orow * kHeadDim + lane * 4) =
+      make_uint2(w[0], w[1]);
+  if (lane == 0 && a.lse) a.lse[orow] = lse2 * kLn2;
 }
 
 }  // namespace
@@ -164,11 +174,12 @@ cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void*
 
 cudaError_t launch_split_merge(const SplitMergeArgs& a, cudaStream_t stream) {
   if (a.num_split_items <= 0) return cudaSuccess;
-  const int blocks = a.num_split_items < 4096 ? a.num_split_items : 4096;
+  const int64_t warps = int64_t(a.num_split_items) * a.rows_per_item;
+  const int64_t blocks = (warps + 7) / 8;
   if (a.dtype == ATTN_BF16)
-    split_merge_kernel<true><<<blocks, 128, 0, stream>>>(a);
+    split_merge_kernel<true><<<unsigned(blocks), 256, 0, stream>>>(a);
   else
-    split_merge_kernel<false><<<blocks, 128, 0, stream>>>(a);
+    split_merge_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
