@@ -343,6 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
   // Rows per 128-row query tile that hold data (128 for append, group in
   // decode mode) and the TMA bytes of one tile.
   const uint32_t tile_rows = uint32_t(group * a.tile_tokens);
+  // TMEM columns. Two query tiles: tile x has S_x/P_x at 256 x and O_x at
+  // 256 x + 128. One query tile: S/P double-buffered at 0 and 128 (KV tile k
+  // uses buffer k & 1, so S of tile k+1 runs under the softmax of tile k), O
+  // at 256.
+  auto col_s = [](int x, uint32_t k) -> uint32_t {
+    return NQ == 2 ? uint32_t(x) * kColTile + kColS : (k & 1u) * 128u;
+  };
+  auto col_o = [](int x) -> uint32_t { return NQ == 2 ? uint32_t(x) * kColTile + kColO : 256u; };
 
   // A CTA runs the unit lists of plan CTAs blockIdx.x, blockIdx.x + gridDim.x,
   // ... (the grid is at most one CTA per SM; a plan may have more CTAs).
@@ -367,21 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       AGeo g = append_geo(a, ui);
       g.nq = min(g.nq, NQ);
       if (g.ntiles == 0) continue;
-      if (!wait0(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        const uint32_t qf = smem_u32(&bars.q_full);
-        mbar_arrive_expect_tx(qf, 256u * tile_rows * uint32_t(g.nq));
-        for (int x = 0; x < g.nq; ++x) {
-          const int32_t qrow = int32_t(g.qo_start + int64_t(g.t) * a.q_tile + x * a.tile_tokens);
-          const uint32_t dst = base + kOffQ + x * kTileBytes;
-          tma_load_3d(dst, &prm.tm_q, 0, g.hk * group, qrow, qf);
-          tma_load_3d(dst + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
-        }
-      }
-      ++ua;
       for (int i = 0; i < g.ntiles && ok; ++i) {
         const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
         const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
@@ -409,6 +402,25 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
             tma_load_2d(dst, tm, 0, row, full);
             tma_load_2d(dst + kHalf, tm, 64, row, full);
           }
+        }
+        if (i == 0 && ok) {
+          // the unit's query tile(s), once the previous unit's last S MMA is done
+          if (!wait0(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t qf = smem_u32(&bars.q_full);
+            mbar_arrive_expect_tx(qf, 256u * tile_rows * uint32_t(g.nq));
+            for (int x = 0; x < g.nq; ++x) {
+              const int32_t qrow =
+                  int32_t(g.qo_start + int64_t(g.t) * a.q_tile + x * a.tile_tokens);
+              const uint32_t dst = base + kOffQ + x * kTileBytes;
+              tma_load_3d(dst, &prm.tm_q, 0, g.hk * group, qrow, qf);
+              tma_load_3d(dst + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
+            }
+          }
+          ++ua;
         }
       }
     }
@@ -438,32 +450,37 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
                          ERR_WAIT_FULL);
       };
-      auto issue_s = [&](int x, uint32_t kslot) {
+      // S for query tile x and KV tile k (global count) from the K in kslot
+      auto issue_s = [&](int x, uint32_t kslot, uint32_t k) {
         const uint32_t qbase = base + kOffQ + x * kTileBytes;
         const uint32_t kbase = base + kOffRing + kslot * kTileBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-          mma_f16(tmem + x * kColTile + kColS, smem_desc(qbase + koff, 16, 1024),
-                  smem_desc(kbase + koff, 16, 1024), prm.idesc_s, k > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_f16(tmem + col_s(x, k), smem_desc(qbase + koff, 16, 1024),
+                  smem_desc(kbase + koff, 16, 1024), prm.idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(smem_u32(&bars.s_full[x]));
+        mma_commit(smem_u32(&bars.s_full[NQ == 2 ? x : int(k & 1u)]));
       };
-      auto issue_pv = [&](int x, uint32_t vslot, bool first) -> bool {
-        if (!mbar_wait(smem_u32(&bars.p_full[x]), n_p[x] & 1u, err, ERR_WAIT_SOFTMAX))
-          return false;
+      // O_x += P_x(k) V once softmax x has written P_x(k) into TMEM
+      auto issue_pv = [&](int x, uint32_t vslot, uint32_t k, bool first) -> bool {
+        // one query tile: the softmax of tile k+1 may finish before P(k).V is
+        // issued (S(k+1) precedes it), so tile k signals p_full[k & 1]
+        const int pb = NQ == 2 ? x : int(k & 1u);
+        const uint32_t ppar = NQ == 2 ? (n_p[x] & 1u) : ((k >> 1) & 1u);
+        if (!mbar_wait(smem_u32(&bars.p_full[pb]), ppar, err, ERR_WAIT_SOFTMAX)) return false;
         if (first &&
             !mbar_wait(smem_u32(&bars.o_free[x]), (n_u[x] & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
           return false;
         tc_fence_after();
         const uint32_t vbase = base + kOffRing + vslot * kTileBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t bd = smem_desc(vbase + k * kChunk * 128, kHalf, 1024);
-          mma_f16_ts(tmem + x * kColTile + kColO, tmem + x * kColTile + kColS + k * 8, bd,
-                     prm.idesc_pv, (first && k == 0) ? 0u : 1u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = smem_desc(vbase + kk * kChunk * 128, kHalf, 1024);
+          mma_f16_ts(tmem + col_o(x), tmem + col_s(x, k) + kk * 8, bd, prm.idesc_pv,
+                     (first && kk == 0) ? 0u : 1u);
         }
-        mma_commit(smem_u32(&bars.o_done[x]));
+        mma_commit(smem_u32(&bars.o_done[NQ == 2 ? x : int(k & 1u)]));
         ++n_p[x];
         return true;
       };
@@ -472,39 +489,87 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         AGeo g = append_geo(a, ui);
         g.nq = min(g.nq, NQ);
         if (g.ntiles == 0) continue;
+        const int n = g.ntiles;
         if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) ||
             !wait_slot(2 * jt)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if constexpr (NQ == 2) {
+          // S_A(0), S_B(0); then per KV tile i: P_A(i).V, S_A(i+1), P_B(i).V, S_B(i+1)
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
-          if (x < g.nq) issue_s(x, slot_of(2 * jt));
-        mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jt)]));
-        for (int i = 0; i < g.ntiles && ok; ++i) {
-          const uint32_t jk = jt + i + 1;  // next K tile
-          const bool more = i + 1 < g.ntiles;
-          if (!wait_slot(2 * (jt + i) + 1) || (more && !wait_slot(2 * jk))) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (x < g.nq && ok) {
-              ok = issue_pv(x, slot_of(2 * (jt + i) + 1), i == 0);
-              if (ok && more) issue_s(x, slot_of(2 * jk));
+          for (int x = 0; x < 2; ++x)
+            if (x < g.nq) issue_s(x, slot_of(2 * jt), jt);
+          mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jt)]));
+          if (n == 1) mma_commit(smem_u32(&bars.q_empty));
+          for (int i = 0; i < n && ok; ++i) {
+            const uint32_t k = jt + i;
+            const bool more = i + 1 < n;
+            if (!wait_slot(2 * k + 1)) {
+              ok = false;
+              break;
             }
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              if (x < g.nq && ok) {
+                ok = issue_pv(x, slot_of(2 * k + 1), k, i == 0);
+                if (ok && more) {
+                  if (x == 0 && !wait_slot(2 * k + 2)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  issue_s(x, slot_of(2 * k + 2), k + 1);
+                }
+              }
+            }
+            if (!ok) break;
+            if (more) {
+              mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * k + 2)]));
+              if (i + 2 == n) mma_commit(smem_u32(&bars.q_empty));  // last S issued
+            }
+            mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * k + 1)]));
           }
-          mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * (jt + i) + 1)]));
-          if (more) mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jk)]));
+        } else {
+          // S(0), S(1) into the two S buffers; then per KV tile i: P(i).V, S(i+2)
+          issue_s(0, slot_of(2 * jt), jt);
+          mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jt)]));
+          if (n > 1) {
+            if (!wait_slot(2 * jt + 2)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(0, slot_of(2 * jt + 2), jt + 1);
+            mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jt + 2)]));
+          }
+          if (n <= 2) mma_commit(smem_u32(&bars.q_empty));
+          for (int i = 0; i < n && ok; ++i) {
+            const uint32_t k = jt + i;
+            if (!wait_slot(2 * k + 1)) {
+              ok = false;
+              break;
+            }
+            ok = issue_pv(0, slot_of(2 * k + 1), k, i == 0);
+            if (ok && i + 2 < n) {
+              if (!wait_slot(2 * k + 4)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(0, slot_of(2 * k + 4), k + 2);
+              mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * k + 4)]));
+              if (i + 3 == n) mma_commit(smem_u32(&bars.q_empty));  // last S issued
+            }
+            mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * k + 1)]));
+          }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&bars.q_empty));
 #pragma unroll
         for (int x = 0; x < 2; ++x)
           if (x < g.nq) ++n_u[x];
-        jt += g.ntiles;
+        jt += n;
         ++ua;
       }
       // drain: no MMA may still be writing TMEM when it is freed
@@ -521,8 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
     const int rho_t = quarter * 32 + lane;      // row within the query tile
     const int rho = x * kTile + rho_t;          // row within the item
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const uint32_t col_s = x * kColTile + kColS;
-    const uint32_t col_o = x * kColTile + kColO;
+    const uint32_t col_ox = col_o(x);
     const int tok = rho / group;
     const int hh = rho - tok * group;
     const float c2 = prm.scale_log2;
@@ -562,7 +626,12 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       float m_ref = -INFINITY, l = 0.f;
       for (int i = 0; i < g.ntiles; ++i, ++n_t) {
         // waits are made warp-uniform: tcgen05.ld/st below are .sync.aligned
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[x]), n_t & 1u, err,
+        // S of this tile: barrier s_full[x] (two tiles) or s_full[n_t & 1] (one
+        // tile, S double-buffered: the buffer's uses alternate phases)
+        const int sb = NQ == 2 ? x : int(n_t & 1u);
+        const uint32_t sparity = NQ == 2 ? (n_t & 1u) : ((n_t >> 1) & 1u);
+        const uint32_t col_sx = col_s(x, n_t);
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[sb]), sparity, err,
                                                ERR_WAIT_MMA))) {
           ok = false;
           break;
@@ -572,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         const int nvalid = int(max(int64_t(0), min(int64_t(kTile), row_end - kv0)));
         if (warp_live) {
           float v[kTile];
-          tmem_ld128(tmem + lane_off + col_s, v);
+          tmem_ld128(tmem + lane_off + col_sx, v);
           // Tiles without masked columns (all but the causal diagonal and the
           // unit's last tile) skip the per-element selects; rows without a
           // query may take that path too (their P row only feeds their own O
@@ -600,12 +669,21 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
             l *= alpha;
             m_ref = m_tile;
           }
-          // O_x holds every earlier tile (S_x(i) completing implies P_x(i-1).V done)
+          // O_x must hold every earlier tile before it is rescaled. With two
+          // query tiles S_x(i) completing implies P_x(i-1).V is done; with one
+          // (S double-buffered) wait for that P.V explicitly.
           if (__any_sync(0xffffffffu, rescale_o)) {
+            if (NQ == 1 && i > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[(n_t - 1) & 1u]),
+                                                   ((n_t - 1) >> 1) & 1u, err, ERR_WAIT_MMA))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
               float o[32];
-              const uint32_t ta = tmem + lane_off + col_o + c * 32;
+              const uint32_t ta = tmem + lane_off + col_ox + c * 32;
               tmem_ld32(ta, o);
               const float f = rescale_o ? alpha : 1.f;
 #pragma unroll
@@ -630,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
                 lsum2 = fadd2(lsum2, pr);
                 pk[q / 2] = pack2<BF16>(pr.x, pr.y);
               }
-              tmem_st16_nowait(tmem + lane_off + col_s + c * 16, pk);
+              tmem_st16_nowait(tmem + lane_off + col_sx + c * 16, pk);
             }
           } else {
 #pragma unroll
@@ -645,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
                 lsum2 = fadd2(lsum2, pr);
                 pk[q / 2] = pack2<BF16>(pr.x, pr.y);
               }
-              tmem_st16_nowait(tmem + lane_off + col_s + c * 16, pk);
+              tmem_st16_nowait(tmem + lane_off + col_sx + c * 16, pk);
             }
           }
           tmem_wait_st();
@@ -672,11 +750,16 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
           fence_proxy_async_smem();
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.p_full[x]));
+        mbar_arrive(smem_u32(&bars.p_full[NQ == 2 ? x : int(n_t & 1u)]));
       }
       if (!ok) break;
       // ---- epilogue: O / l
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[x]), (n_t - 1) & 1u, err,
+      // P.V of the last tile: with two query tiles S_x(last) completing put
+      // O_x one P.V behind; with one, S(last) only follows P.V(last - 2), so
+      // P.V of tile k signals o_done[k & 1] and no wait is two phases behind.
+      const int od = NQ == 2 ? x : int((n_t - 1) & 1u);
+      const uint32_t opar = NQ == 2 ? ((n_t - 1) & 1u) : (((n_t - 1) >> 1) & 1u);
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[od]), opar, err,
                                              ERR_WAIT_MMA))) {
         ok = false;
         break;
@@ -688,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < 4 && warp_live; ++c) {
         float o[32];
-        tmem_ld32(tmem + lane_off + col_o + c * 32, o);
+        tmem_ld32(tmem + lane_off + col_ox + c * 32, o);
         if (row_ok) {
           if (g.slot < 0) {
             uint4* dst =
