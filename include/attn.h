@@ -171,10 +171,12 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
  *   lse        : device float[batch, num_qo_heads] (out) or NULL
  *   dev_ws     : the workspace given to attn_plan (holds the plan tables)
  * Supported: head_dim 128, group = num_qo_heads / num_kv_heads in 1..8,
- * any page_size >= 1, both layouts, fp16 and bf16. Groups below 8 run on a
- * CUDA-core streaming kernel; group 8 with the HND layout and page_size a
- * multiple of 16 runs on the tensor-core (tcgen05) kernel, the group's 8
- * query rows forming one M = 128 tile, plus a merge kernel for split items.
+ * any page_size >= 1, both layouts, fp16 and bf16. Groups 2, 4 and 8 with
+ * the HND layout and page_size a multiple of 16 run on the tensor-core
+ * (tcgen05) decode kernel (the group's query rows replicated over 32 MMA
+ * rows, 128-token K/V tiles gathered by TMA), followed by a merge kernel for
+ * split items; every other shape runs on a CUDA-core streaming kernel that
+ * merges split items itself.
  * Errors: INVALID_ARG (plan mode/shape mismatch, null pointers),
  * UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA (launch failure).
  */

@@ -12,7 +12,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn.so")
-SOURCES = ["capi.cpp", "plan.cpp", "decode.cu", "merge.cu", "append.cu", "noalloc.cu"]
+SOURCES = ["capi.cpp", "plan.cpp", "decode.cu", "decode_tc.cu", "merge.cu", "append.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

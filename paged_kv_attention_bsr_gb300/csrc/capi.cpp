@@ -169,10 +169,11 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
     return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_run: group > 8 is not implemented");
   if (plan->batch == 0) return ATTN_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (group >= kTensorDecodeGroup && layout == ATTN_LAYOUT_HND && plan->page_size % 16 == 0) {
-    // Large GQA groups: the per-token work (group heads x 128 dims, twice)
-    // outruns the CUDA cores before HBM saturates, so the group's query rows
-    // go through the tensor-core kernel as one M = 128 tile instead.
+  if (group >= kTensorDecodeGroup && (group & (group - 1)) == 0 && layout == ATTN_LAYOUT_HND &&
+      plan->page_size % 16 == 0) {
+    // Tensor-core decode: Q K^T and P V run as M = 128 MMAs over 128-token
+    // tiles gathered by TMA, the softmax on one warp (query heads replicated
+    // across the MMA rows so that each thread handles a slice of the tile).
     AppendArgs a;
     a.q = q;
     a.qo_indptr = nullptr;
@@ -201,7 +202,7 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
     a.causal = 0;
     a.sm_scale = sm_scale;
     const char* msg = "";
-    cudaError_t e = launch_append(a, st, &msg);
+    cudaError_t e = launch_decode_tc(a, st, &msg);
     if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
     if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: tensor-core decode launch");
     if (plan->num_split_items > 0) {

@@ -1,0 +1,680 @@
+// decode_tc.cu -- batch decode over a BSR paged KV cache on the tensor cores
+// (tcgen05 MMA with TMEM accumulators, TMA gathers of the K/V pages).
+//
+// Method: one new query token per request attends to that request's paged
+// KV (FlashInfer README copy on gittoolsai.com, "解码、预填充与追加"; pages
+// addressed through a block-sparse row table, modb.pro digest,
+// "统一的 KV 缓存存储格式"); the CPU plan of "动态负载均衡调度" cuts the
+// (request, kv head) items into page ranges balanced across a persistent
+// fixed grid, and split items are joined afterwards by their log-sum-exp.
+//
+// A unit (request r, kv head hk, pages [p0, p1)) multiplies the G query
+// heads of its GQA group with 128-token K/V tiles:
+//   S = Q K^T     A = Q (smem, K-major), B = K (smem, K-major), D = TMEM
+//   P = exp2(S c - m) over each row, written over S in TMEM (16-bit)
+//   O += P V      A = P (TMEM), B = V (smem, MN-major), D = TMEM
+// Only G of the 128 MMA rows would hold queries, and one thread per row
+// would exponentiate all 128 scores of a tile. Instead the G heads are
+// replicated C = 32 / G times in query rows 0..31 (row h + G c is copy c of
+// head h) and copy c owns kv columns [W c, W c + W) of every tile
+// (W = 128 / C = 4 G). One warp runs the softmax with one TMEM lane per
+// thread, W exponentials per thread and tile; the copies of a head share
+// the running max through shuffles, write P only in their own columns
+// (zeros elsewhere), and their O rows -- partial sums over disjoint tokens
+// at a common scale -- are added in the epilogue. Rows 32..127 carry no
+// queries and are never read back.
+//
+// Warps (128 threads, one CTA per SM): 0 softmax + epilogue; 1 TMA producer
+// of the K/V ring (six 32 KB slots, 16-row boxes gathered by page index);
+// 2 TMEM allocation and the MMAs (one thread: S of tile k+1 runs under the
+// softmax of tile k, S double-buffered in TMEM); 3 query loader (plain
+// loads of the next unit's G query rows into registers, stored into the
+// swizzled query tile as soon as the last S of the current unit is done).
+// Every wait is bounded; TMEM is freed on every path.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kTile = kTcTile;
+constexpr int kChunk = kTcChunk;
+constexpr int kHalf = kTcHalf;
+constexpr int kTileBytes = kTcTileBytes;
+constexpr int kThreads = 128;
+constexpr int kWarpSoftmax = 0;
+constexpr int kWarpLoad = 1;
+constexpr int kWarpMma = 2;
+constexpr int kWarpQ = 3;
+constexpr int kSlots = 6;
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kTileBytes;
+constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+constexpr int kSmem = kOffBar + 256 + 1024;  // + barriers + alignment slack
+constexpr uint32_t kTmemCols = 512;          // S buffers at 0 and 128, O at 256
+constexpr uint32_t kColO = 256;
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t slot_full[kSlots], slot_empty[kSlots];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t o_free;
+  uint64_t drain;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct DecodeTcParams {
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  AppendArgs a;
+  float scale_log2;
+  uint32_t idesc_s;
+  uint32_t idesc_pv;
+};
+
+struct DGeo {
+  int32_t r, hk, slot, page_base, ntiles;
+  int64_t tok_begin, tok_end;
+};
+
+__device__ __forceinline__ DGeo decode_geo(const AppendArgs& a, int ui) {
+  const int4* rec = reinterpret_cast<const int4*>(a.ws.units + ui);
+  const int4 x = __ldg(rec);
+  const int4 y = __ldg(rec + 1);
+  DGeo g;
+  g.r = x.x;
+  g.hk = x.y;
+  g.slot = y.y;
+  g.page_base = __ldg(a.kv_indptr + g.r);
+  const int64_t n = int64_t(__ldg(a.kv_indptr + g.r + 1)) - g.page_base;
+  const int64_t kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
+  g.tok_begin = int64_t(x.w) * a.page_size;
+  g.tok_end = min(int64_t(y.x) * a.page_size, kv_len);
+  const int64_t nt = g.tok_end - g.tok_begin;
+  g.ntiles = nt > 0 ? int32_t((nt + kTile - 1) / kTile) : 0;
+  return g;
+}
+
+template <int N>
+struct ILog2 {
+  static constexpr int value = 1 + ILog2<N / 2>::value;
+};
+template <>
+struct ILog2<1> {
+  static constexpr int value = 0;
+};
+
+// N consecutive outputs (N = 1, 2, 4 or 8) of one row, scaled: 16-bit or fp32.
+template <bool BF16, int N>
+__device__ __forceinline__ void store_out16(void* o, int64_t idx, const float* v, float scale) {
+  uint16_t* dst = static_cast<uint16_t*>(o) + idx;
+  if constexpr (N == 1) {
+    if constexpr (BF16)
+      *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(v[0] * scale);
+    else
+      *reinterpret_cast<__half*>(dst) = __float2half_rn(v[0] * scale);
+  } else {
+    uint32_t w[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) w[i] = pack2<BF16>(v[2 * i] * scale, v[2 * i + 1] * scale);
+    if constexpr (N == 2) *reinterpret_cast<uint32_t*>(dst) = w[0];
+    if constexpr (N == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    if constexpr (N == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+template <int N>
+__device__ __forceinline__ void store_out32(float* dst, const float* v, float scale) {
+  if constexpr (N == 1) dst[0] = v[0] * scale;
+  if constexpr (N == 2) *reinterpret_cast<float2*>(dst) = make_float2(v[0] * scale, v[1] * scale);
+  if constexpr (N >= 4) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4)
+      *reinterpret_cast<float4*>(dst + i) =
+          make_float4(v[i] * scale, v[i + 1] * scale, v[i + 2] * scale, v[i + 3] * scale);
+  }
+}
+
+template <bool BF16, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
+  constexpr int C = 32 / G;     // copies of each head
+  constexpr int W = kTile / C;  // kv columns per copy and tile
+  constexpr int LC = ILog2<C>::value;
+  extern __shared__ uint8_t smem_raw[];
+  const AppendArgs& a = prm.a;
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_base);
+  Bars& bars = *reinterpret_cast<Bars*>(gbase + kOffBar);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int32_t* err = a.ws.error;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars.q_full), 32);
+    mbar_init(smem_u32(&bars.q_empty), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&bars.slot_full[i]), 1);
+      mbar_init(smem_u32(&bars.slot_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars.s_full[i]), 1);
+      mbar_init(smem_u32(&bars.p_full[i]), 32);
+      mbar_init(smem_u32(&bars.o_done[i]), 1);
+    }
+    mbar_init(smem_u32(&bars.o_free), 32);
+    mbar_init(smem_u32(&bars.drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpLoad && lane == 0) {
+    prefetch_tmap(&prm.tm_k);
+    prefetch_tmap(&prm.tm_v);
+  }
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&bars.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  // A CTA runs the unit lists of plan CTAs blockIdx.x, blockIdx.x + gridDim.x,
+  // ... (the grid is at most one CTA per SM; a plan may have more CTAs).
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ TMA producer
+    // Lane c fetches the page index of the tile's 16-row chunk c and issues
+    // that chunk's boxes. The next tile's indices are loaded before this
+    // tile's slots are awaited, so their latency hides behind the wait.
+    uint32_t uses = 0;
+    const int P = a.page_size;
+    bool ok = true;
+    auto chunk_row = [&](const DGeo& g, int i) -> int32_t {
+      const int64_t kvt = g.tok_begin + int64_t(i) * kTile + int64_t(lane) * kChunk;
+      if (kvt >= g.tok_end) return 0;
+      const int64_t pg = kvt / P;
+      const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+      return int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
+    };
+    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+      for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+           ++ui) {
+        const DGeo g = decode_geo(a, ui);
+        if (g.ntiles == 0) continue;
+        int32_t row = chunk_row(g, 0);
+        for (int i = 0; i < g.ntiles && ok; ++i) {
+          const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+          const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+          const int nch = (ntt + kChunk - 1) / kChunk;
+          const int32_t row_next = i + 1 < g.ntiles ? chunk_row(g, i + 1) : 0;
+          for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
+            const int slot = int(uses % kSlots);
+            bool r = true;
+            if (lane == 0)
+              r = mbar_wait(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u, err,
+                            ERR_WAIT_EMPTY);
+            if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_u32(&bars.slot_full[slot]);
+            if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
+            __syncwarp();
+            if (lane < nch) {
+              const uint32_t dst =
+                  base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
+              const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                       : static_cast<const void*>(&prm.tm_v);
+              tma_load_2d(dst, tm, 0, row, full);
+              tma_load_2d(dst + kHalf, tm, 64, row, full);
+            }
+          }
+          row = row_next;
+        }
+      }
+    // drain: every issued copy has landed before the CTA can exit
+    if (lane == 0) {
+      for (uint32_t sl = 0; sl < uint32_t(kSlots) && sl < uses; ++sl) {
+        const uint32_t last = uses - 1 - ((uses - 1 - sl) % kSlots);
+        mbar_wait(smem_u32(&bars.slot_full[sl]), (last / kSlots) & 1u, err, ERR_WAIT_DRAIN);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpQ) {
+    // ------------------------------------------------------------ query loader
+    // The G query rows of a unit (G x 256 B) are read with plain loads one
+    // unit ahead and stored C times into the swizzled query tile.
+    constexpr int kVec = G * 16;            // 16-byte pieces of the G rows
+    constexpr int kPer = (kVec + 31) / 32;  // pieces per lane
+    uint4 qr[kPer];
+    uint32_t ua = 0;
+    auto fetch = [&](const DGeo& g) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const uint16_t*>(a.q) +
+          (int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * G) * kHeadDim);
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = lane + 32 * j;
+        if (idx < kVec) qr[j] = __ldg(src + idx);
+      }
+    };
+    // the units of this CTA that have kv tokens, in order
+    int vc = blockIdx.x, ui = vc < a.num_ctas ? __ldg(a.ws.work_indptr + vc) : 0;
+    auto next_unit = [&](DGeo& g) -> bool {
+      while (vc < a.num_ctas) {
+        if (ui < __ldg(a.ws.work_indptr + vc + 1)) {
+          g = decode_geo(a, ui++);
+          if (g.ntiles > 0) return true;
+        } else {
+          vc += gridDim.x;
+          if (vc < a.num_ctas) ui = __ldg(a.ws.work_indptr + vc);
+        }
+      }
+      return false;
+    };
+    DGeo g;
+    bool have = next_unit(g);
+    if (have) fetch(g);
+    while (have) {
+      bool r = true;
+      if (lane == 0)
+        r = mbar_wait(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u, err, ERR_WAIT_EMPTY);
+      if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) break;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = lane + 32 * j;
+        if (idx < kVec) {
+          const int h = idx >> 4, ch = idx & 15;
+          const int half = ch >> 3, j8 = ch & 7;
+#pragma unroll
+          for (int c = 0; c < C; ++c) {
+            const int row = h + G * c;
+            const int off = kOffQ + half * kHalf + row * 128 + ((j8 ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(gbase + off) = qr[j];
+          }
+        }
+      }
+      fence_proxy_async_smem();  // generic stores -> the MMA's operand reads
+      mbar_arrive(smem_u32(&bars.q_full));
+      ++ua;
+      have = next_unit(g);
+      if (have) fetch(g);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per unit: S(0), S(1) into the two S buffers; then per KV tile k:
+    // O += P(k) V once the softmax has written P(k), then S(k+2). The tensor
+    // core runs in issue order, so S(k+2) overwrites P(k) only after P(k).V.
+    if (lane == 0) {
+      uint32_t ua = 0, jt = 0, n_u = 0;
+      bool ok = true;
+      auto slot_of = [](uint32_t use) { return use % kSlots; };
+      auto wait_slot = [&](uint32_t use) -> bool {
+        return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
+                         ERR_WAIT_FULL);
+      };
+      auto issue_s = [&](uint32_t k) {
+        const uint32_t qbase = base + kOffQ;
+        const uint32_t kbase = base + kOffRing + slot_of(2 * k) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_f16(tmem + (k & 1u) * 128u, smem_desc(qbase + koff, 16, 1024),
+                  smem_desc(kbase + koff, 16, 1024), prm.idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars.s_full[k & 1u]));
+        mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * k)]));
+      };
+      // O += P(k) V over the tile's nk 16-token chunks (chunks past the
+      // unit's end are skipped: their V rows were never loaded)
+      auto issue_pv = [&](uint32_t k, int nk, bool first) -> bool {
+        if (!mbar_wait(smem_u32(&bars.p_full[k & 1u]), (k >> 1) & 1u, err, ERR_WAIT_SOFTMAX))
+          return false;
+        if (first && !mbar_wait(smem_u32(&bars.o_free), (n_u & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
+          return false;
+        tc_fence_after();
+        const uint32_t vbase = base + kOffRing + slot_of(2 * k + 1) * kTileBytes;
+        for (int kk = 0; kk < nk; ++kk) {
+          const uint64_t bd = smem_desc(vbase + kk * kChunk * 128, kHalf, 1024);
+          mma_f16_ts(tmem + kColO, tmem + (k & 1u) * 128u + kk * 8, bd, prm.idesc_pv,
+                     (first && kk == 0) ? 0u : 1u);
+        }
+        mma_commit(smem_u32(&bars.o_done[k & 1u]));
+        mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * k + 1)]));
+        return true;
+      };
+      for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+        for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+             ++ui) {
+          const DGeo g = decode_geo(a, ui);
+          if (g.ntiles == 0) continue;
+          const int n = g.ntiles;
+          if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) ||
+              !wait_slot(2 * jt)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(jt);
+          if (n > 1) {
+            if (!wait_slot(2 * jt + 2)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(jt + 1);
+          }
+          if (n <= 2) mma_commit(smem_u32(&bars.q_empty));  // last S issued
+          for (int i = 0; i < n && ok; ++i) {
+            const uint32_t k = jt + i;
+            const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+            const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+            if (!wait_slot(2 * k + 1)) {
+              ok = false;
+              break;
+            }
+            ok = issue_pv(k, (ntt + kChunk - 1) / kChunk, i == 0);
+            if (ok && i + 2 < n) {
+              if (!wait_slot(2 * k + 4)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(k + 2);
+              if (i + 3 == n) mma_commit(smem_u32(&bars.q_empty));  // last S issued
+            }
+          }
+          if (!ok) break;
+          ++n_u;
+          jt += n;
+          ++ua;
+        }
+      // drain: no MMA may still be writing TMEM when it is freed
+      mma_commit(smem_u32(&bars.drain));
+      mbar_wait(smem_u32(&bars.drain), 0, err, ERR_WAIT_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == kWarpSoftmax) {
+    // ------------------------------------------------- softmax / epilogue
+    // Thread (h, c) = lane (h = lane % G, c = lane / G) owns TMEM lane `lane`:
+    // copy c of query head h, kv columns [W c, W c + W) of every tile.
+    // Waits are made warp-uniform: the tcgen05.ld/st after them are
+    // .sync.aligned.
+    const int h = lane % G;
+    const int c = lane / G;
+    const float c2 = prm.scale_log2;
+    uint32_t n_t = 0;
+    bool ok = true;
+    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+      for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+           ++ui) {
+        const DGeo g = decode_geo(a, ui);
+        const int64_t orow = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * G + h;
+        if (g.ntiles == 0) {  // no kv: o = 0, lse = -inf
+          if (g.slot < 0) {
+            constexpr int kS = W < 8 ? W : 8;
+            float z[kS];
+#pragma unroll
+            for (int j = 0; j < kS; ++j) z[j] = 0.f;
+#pragma unroll
+            for (int j = 0; j < W; j += kS)
+              store_out16<BF16, kS>(a.o, orow * kHeadDim + W * c + j, z, 1.f);
+            if (c == 0 && a.lse) a.lse[orow] = -INFINITY;
+          } else {
+            const int64_t prow = int64_t(g.slot) * G + h;
+            float* dst = a.ws.partial_o + prow * kHeadDim + W * c;
+            for (int j = 0; j < W; ++j) dst[j] = 0.f;
+            if (c == 0) a.ws.partial_lse[prow] = -INFINITY;
+          }
+          continue;
+        }
+        float m_ref = -INFINITY, l = 0.f;
+        for (int i = 0; i < g.ntiles; ++i, ++n_t) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[n_t & 1u]),
+                                                 (n_t >> 1) & 1u, err, ERR_WAIT_MMA))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t col_s = (n_t & 1u) * 128u;
+          const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+          const int nvalid = int(min(int64_t(kTile), g.tok_end - kv0));
+          // this thread's W scores: columns [W c, W c + W) of its row
+          float s[W];
+          {
+            float v[kTile];
+            tmem_ld128(tmem + col_s, v);
+#pragma unroll
+            for (int j = 0; j < W; ++j) s[j] = v[j];
+#pragma unroll
+            for (int b = 1; b < C; ++b) {
+              const bool mine = c == b;
+#pragma unroll
+              for (int j = 0; j < W; ++j) s[j] = mine ? v[W * b + j] : s[j];
+            }
+          }
+          const bool full = nvalid == kTile;
+          float mx = -INFINITY;
+          if (full) {
+#pragma unroll
+            for (int j = 0; j < W; ++j) mx = fmaxf(mx, s[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) mx = fmaxf(mx, (W * c + j < nvalid) ? s[j] : -INFINITY);
+          }
+#pragma unroll
+          for (int st = 0; st < LC; ++st) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, G << st));
+          const float m_tile = mx * c2;  // -inf stays -inf
+          float alpha = 1.f;
+          bool rescale_o = false;
+          if (m_tile > m_ref + 8.f) {
+            alpha = ex2(m_ref - m_tile);  // 0 when m_ref = -inf
+            rescale_o = (i > 0) && (m_ref != -INFINITY);
+            l *= alpha;
+            m_ref = m_tile;
+          }
+          if (__any_sync(0xffffffffu, rescale_o)) {
+            // O must hold every earlier tile: S(k) completing only implies
+            // P(k-2).V, so wait for P(k-1).V explicitly
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[(n_t - 1) & 1u]),
+                                                   ((n_t - 1) >> 1) & 1u, err, ERR_WAIT_MMA))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int b = 0; b < 4; ++b) {
+              float o[32];
+              tmem_ld32(tmem + kColO + b * 32, o);
+              const float f = rescale_o ? alpha : 1.f;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) o[q] *= f;
+              tmem_st32(tmem + kColO + b * 32, o);
+            }
+          }
+          // probabilities of this thread's W columns, packed to 16-bit
+          uint32_t pk[W / 2];
+          float lsum = 0.f;
+          const bool live = m_ref != -INFINITY;
+#pragma unroll
+          for (int j = 0; j < W; j += 2) {
+            float p0 = ex2(fmaf(s[j], c2, -m_ref));
+            float p1 = ex2(fmaf(s[j + 1], c2, -m_ref));
+            if (!full || !live) {
+              p0 = (live && W * c + j < nvalid) ? p0 : 0.f;
+              p1 = (live && W * c + j + 1 < nvalid) ? p1 : 0.f;
+            }
+            lsum += p0 + p1;
+            pk[j / 2] = pack2<BF16>(p0, p1);
+          }
+          l += lsum;
+          // the P row: this thread's W/2 packed columns at (W/2) c, zeros elsewhere
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            uint32_t blk[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              constexpr int HW = W / 2;
+              const int pc = 16 * b + q;
+              blk[q] = (pc / HW == c) ? pk[pc % HW] : 0u;
+            }
+            tmem_st16_nowait(tmem + col_s + 16 * b, blk);
+          }
+          tmem_wait_st();
+          // V rows past the unit's end inside its last 16-row chunk hold
+          // whatever the pool had there: zero them once the tile's V has
+          // landed (whole chunks past the end are skipped by the P.V MMA)
+          const int nrow = ((nvalid + kChunk - 1) / kChunk) * kChunk;
+          if (nvalid < nrow) {
+            const uint32_t vuse = 2 * n_t + 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.slot_full[vuse % kSlots]),
+                                                   (vuse / kSlots) & 1u, err, ERR_WAIT_FULL))) {
+              ok = false;
+              break;
+            }
+            uint8_t* vslot = gbase + kOffRing + (vuse % kSlots) * kTileBytes;
+            for (int e = lane; e < (nrow - nvalid) * 16; e += 32) {
+              const int rr = nvalid + (e >> 4), q = e & 15;
+              *reinterpret_cast<uint4*>(vslot + (q >> 3) * kHalf + rr * 128 + (q & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.p_full[n_t & 1u]));
+        }
+        if (!ok) break;
+        // ---- epilogue: sum the copies, O / l
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[(n_t - 1) & 1u]),
+                                               ((n_t - 1) >> 1) & 1u, err, ERR_WAIT_MMA))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float lt = l;
+#pragma unroll
+        for (int st = 0; st < LC; ++st) lt += __shfl_xor_sync(0xffffffffu, lt, G << st);
+        const bool any = lt > 0.f;
+        const float inv = any ? 1.f / lt : 0.f;
+        const float lse2 = any ? m_ref + lg2(lt) : -INFINITY;
+        // first dim (within a 32-column chunk) that this thread holds after
+        // the transposing reduction, and how many
+        int doff = 0;
+#pragma unroll
+        for (int st = 0; st < LC; ++st) doff += ((c >> st) & 1) * (16 >> st);
+        constexpr int NF = 32 / C;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          float o[32];
+          tmem_ld32(tmem + kColO + b * 32, o);
+          // transposing butterfly over the copies: each step halves the
+          // values a thread keeps and adds the partner's matching half
+          int n = 32;
+#pragma unroll
+          for (int st = 0; st < LC; ++st) {
+            n >>= 1;
+            const bool upper = (c >> st) & 1;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              if (k < n) {
+                const float send = upper ? o[k] : o[k + n];
+                const float keep = upper ? o[k + n] : o[k];
+                o[k] = keep + __shfl_xor_sync(0xffffffffu, send, G << st);
+              }
+            }
+          }
+          const int d0 = 32 * b + doff;
+          if (g.slot < 0) {
+            store_out16<BF16, NF>(a.o, orow * kHeadDim + d0, o, inv);
+          } else {
+            const int64_t prow = int64_t(g.slot) * G + h;
+            store_out32<NF>(a.ws.partial_o + prow * kHeadDim + d0, o, inv);
+          }
+        }
+        if (c == 0) {
+          if (g.slot < 0) {
+            if (a.lse) a.lse[orow] = lse2 * kLn2;
+          } else {
+            a.ws.partial_lse[int64_t(g.slot) * G + h] = lse2;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.o_free));
+      }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+template <bool BF16, int G>
+cudaError_t launch_g(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  decode_tc_kernel<BF16, G><<<grid, kThreads, kSmem, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_dt(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
+  switch (prm.a.group) {
+    case 2: return launch_g<BF16, 2>(prm, grid, stream);
+    case 4: return launch_g<BF16, 4>(prm, grid, stream);
+    default: return launch_g<BF16, 8>(prm, grid, stream);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const char** msg) {
+  if (a.group != 2 && a.group != 4 && a.group != 8) {
+    *msg = "attn_decode_run: the tensor-core decode kernel takes groups of 2, 4 or 8";
+    return cudaErrorNotSupported;
+  }
+  if (a.page_size % kChunk != 0) {
+    *msg = "attn_decode_run: page_size must be a multiple of 16";
+    return cudaErrorNotSupported;
+  }
+  if (a.num_ctas <= 0 || a.num_units == 0) return cudaSuccess;
+  const bool bf16 = a.dtype == ATTN_BF16;
+  DecodeTcParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.a = a;
+  prm.scale_log2 = a.sm_scale * kLog2e;
+  prm.idesc_s = make_idesc(bf16, false);
+  prm.idesc_pv = make_idesc(bf16, true);
+  if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
+                    &prm.tm_k, &prm.tm_v, msg))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = a.num_ctas < sms ? a.num_ctas : sms;
+  return bf16 ? launch_dt<true>(prm, grid, stream) : launch_dt<false>(prm, grid, stream);
+}
+
+}  // namespace attn

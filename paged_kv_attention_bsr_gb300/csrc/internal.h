@@ -15,7 +15,7 @@ constexpr int kHeadDim = 128;
 constexpr int kTileRows = 128;      // packed query rows of one MMA tile (M = 128)
 constexpr int kItemRows = 256;      // packed query rows of one append item (2 tiles)
 constexpr int kMaxDecodeGroup = 8;  // query heads per kv head, decode kernel
-constexpr int kTensorDecodeGroup = 8;  // decode groups >= this use the tensor-core kernel
+constexpr int kTensorDecodeGroup = 2;  // decode groups >= this use the tensor-core kernel
 constexpr int kUnitInts = 8;        // int32 words per work-unit record
 constexpr int64_t kHeaderBytes = 256;
 
@@ -142,6 +142,10 @@ struct AppendArgs {
 // kernel does not handle.
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char** msg);
 int append_ctas_per_sm();
+// Decode (one query row per request; qo_indptr ignored) on the tensor cores
+// for groups of 2, 4 or 8 query heads per kv head, HND pools with
+// page_size % 16 == 0.
+cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const char** msg);
 
 // Merge of split items' partial states into o / lse (after a run).
 struct SplitMergeArgs {

@@ -38,3 +38,19 @@ def assert_attn_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
         d = np.abs(lse[~empty] - lse_ref[~empty])
         assert d.max() <= LSE_ABS, f"{what}: max |dLSE| = {d.max():.3e}"
     return float(err.max()), float(err.mean())
+
+
+def poison_unused_slots(cache):
+    """Fill every pool slot no request reads with NaN: a kernel that lets a
+    stale row reach its arithmetic (even multiplied by a zero probability)
+    then produces NaN instead of a plausible number."""
+    P = cache.page_size
+    valid = torch.zeros(cache.num_pages, P, dtype=torch.bool)
+    for r in range(len(cache.kv_indptr) - 1):
+        pages = cache.kv_indices[cache.kv_indptr[r]:cache.kv_indptr[r + 1]]
+        for j, pg in enumerate(pages):
+            n = P if j + 1 < len(pages) else int(cache.last_page_len[r])
+            valid[int(pg), :n] = True
+    bad = ~valid  # [pages, P] -> HND pools [pages, Hk, P, D]
+    for pool in (cache.k_pool, cache.v_pool):
+        pool.permute(0, 2, 1, 3)[bad] = float("nan")

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from paged_kv_attention_bsr_gb300 import synth
-from tests.gpu_util import assert_attn_close, oracle_dtype, to_device
+from tests.gpu_util import assert_attn_close, oracle_dtype, poison_unused_slots, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +61,20 @@ def test_append_small_parity(oracle_mod, case, num_ctas):
     o_ref, lse_ref = oracle_full(oracle_mod, w)
     o, lse, _ = run_append(w, num_ctas)
     assert_attn_close(o, lse, o_ref, lse_ref, f"append case {case} ctas {num_ctas}")
+
+
+@pytest.mark.parametrize("case", [0, 2, 4, 6])
+def test_append_stale_pool_slots_are_never_used(oracle_mod, case):
+    P, Hq, Hk, dtype, qo_lens, extra, causal = CASES[case]
+    kv_lens = [q + e for q, e in zip(qo_lens, extra)]
+    pool = sum(-(-L // P) for L in kv_lens) + 9
+    w = synth.append_workload(f"appnan{case}", qo_lens, kv_lens, P, pool, Hq, Hk, dtype,
+                              seed=900 + case, causal=causal)
+    poison_unused_slots(w.cache)
+    o_ref, lse_ref = oracle_full(oracle_mod, w)
+    for ctas in (1, None):
+        o, lse, _ = run_append(w, ctas)
+        assert_attn_close(o, lse, o_ref, lse_ref, f"append stale slots case {case} ctas {ctas}")
 
 
 def test_append_empty_kv_non_causal(oracle_mod):

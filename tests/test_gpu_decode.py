@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from paged_kv_attention_bsr_gb300 import synth
-from tests.gpu_util import assert_attn_close, oracle_dtype, to_device
+from tests.gpu_util import assert_attn_close, oracle_dtype, poison_unused_slots, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +75,8 @@ SMALL_CASES = [
     (16, 64, 8, torch.bfloat16, [3000, 17, 512, 1]),
     (16, 4, 4, torch.float16, [2048, 100]),
     (32, 10, 2, torch.bfloat16, [500, 33, 64]),
+    (16, 16, 8, torch.bfloat16, [1, 16, 31, 700, 0, 2500]),
+    (48, 8, 4, torch.float16, [47, 48, 49, 1000]),
 ]
 
 
@@ -87,6 +89,18 @@ def test_decode_small_parity(oracle_mod, case, num_ctas):
     o_ref, lse_ref = oracle_full(oracle_mod, w)
     o, lse, att = run_decode(w, num_ctas=num_ctas)
     assert_attn_close(o, lse, o_ref, lse_ref, f"case {case} ctas {num_ctas}")
+
+
+@pytest.mark.parametrize("case", [0, 1, 4, 5, 6, 8, 9])
+def test_decode_stale_pool_slots_are_never_used(oracle_mod, case):
+    P, Hq, Hk, dtype, lens = SMALL_CASES[case]
+    pool = sum(-(-L // P) for L in lens) + 11
+    w = synth.decode_workload(f"nan{case}", lens, P, pool, Hq, Hk, dtype, seed=700 + case)
+    poison_unused_slots(w.cache)
+    o_ref, lse_ref = oracle_full(oracle_mod, w)
+    for ctas in (1, None):
+        o, lse, _ = run_decode(w, num_ctas=ctas)
+        assert_attn_close(o, lse, o_ref, lse_ref, f"stale slots case {case} ctas {ctas}")
 
 
 @pytest.mark.parametrize("case", [0, 3, 5])
