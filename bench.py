@@ -38,10 +38,26 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode attention HBM GB/s (% of ~8 TB/s); causal append TFLOP/s (% peak)"
 L2_FLUSH_BYTES = 512 << 20  # > 2 x the 126 MB L2
+L2_SCRUB_BYTES = 256 << 20
 HOST_COVER_CYCLES = 2_000_000  # ~1 ms of GPU sleep before each timed step
 
 
 # ------------------------------------------------------------------ helpers
+class L2Flush:
+    """Between timed steps: write 512 MB (evicts every line of the previous
+    step), then read 256 MB of another buffer, so that the dirty lines of the
+    write are written back to HBM here and not during the next timed step
+    (which then starts with an L2 holding only clean, unrelated lines)."""
+
+    def __init__(self):
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.scrub = torch.ones(L2_SCRUB_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.buf.zero_()
+        self.scrub.max()
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -191,13 +207,13 @@ def time_steps(step_fns, steps, warmup, flush, kernel_split=1):
     run in order; events are recorded before fn[0], before fn[kernel_split]
     and after the last, so `kernel` times fns[kernel_split:]."""
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         for f in step_fns:
             f()
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for k in range(steps):
-        flush.zero_()
+        flush()
         # keep the GPU busy while the host enqueues the step, so that the
         # events time the step's device work, not the host's enqueue latency
         torch.cuda._sleep(HOST_COVER_CYCLES)
@@ -373,7 +389,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     w = synth.uniform_gqa_decode()
     st = DecodeStep(w)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     b = decode_bytes(w)
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -432,11 +448,11 @@ def run_ours(args, rank, world):
             torch.cuda.current_stream().synchronize()
 
         for _ in range(3):
-            flush.zero_()
+            flush()
             e2e_step()
         tot = 0.0
         for _ in range(n_e2e):
-            flush.zero_()
+            flush()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             e2e_step()
@@ -448,7 +464,8 @@ def run_ours(args, rank, world):
 
     if rank != 0:
         return None
-    traffic = profile_traffic("decode_kernel_uniform_gqa_b64.md", ["decode.cu", "ptx.cuh"])
+    traffic = profile_traffic("decode_tc_kernel_uniform_gqa_b64.md",
+                              ["decode_tc.cu", "tc.cuh", "ptx.cuh"])
     achieved = b / kern_s / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -459,7 +476,8 @@ def run_ours(args, rank, world):
                    "head_dim": 128, "page_size": 16, "kv_len": "U[1024,4096]",
                    "pool_pages": 20000, "total_kv_tokens": int(w.cache.kv_lens.sum()),
                    "num_ctas": st.att.num_ctas, "step": "attn_plan + attn_decode_run",
-                   "l2": "flushed between steps (512 MB write outside the timed events); "
+                   "l2": "flushed between steps outside the timed events (512 MB write, then "
+                         "a 256 MB read so the write-back happens there); "
                          "each step also reads 677 MB of KV, > 126 MB L2",
                    "timing": "CUDA events around each step; a GPU sleep before the step's "
                              "start event covers the host enqueue (outside the events)",
@@ -467,7 +485,8 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)",
-                     "kernel": "decode_kernel (one launch per run)",
+                     "kernel": "decode_tc_kernel<bf16, group 4> (one launch per run; "
+                               "split items merged inside it)",
                      "kernel_us": kern_s * 1e6, "algorithmic_bytes_per_launch": b},
         "gpu_launches": args.steps,
         "clocks": clocks,
@@ -562,7 +581,7 @@ def main():
     if args.workload:
         # one workload alone (used for profiling captures); prints its own line
         hbm_peak, bf16_peak, _ = peaks()
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        flush = L2Flush()
         name, res = WORKLOAD_BENCH[args.workload](hbm_peak, bf16_peak, flush, args.steps,
                                                   args.warmup)
         print(json.dumps({"workload": name, **res}), flush=True)

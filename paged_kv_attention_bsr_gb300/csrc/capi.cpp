@@ -202,24 +202,9 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
     a.causal = 0;
     a.sm_scale = sm_scale;
     const char* msg = "";
-    cudaError_t e = launch_decode_tc(a, st, &msg);
+    cudaError_t e = launch_decode_tc(a, st, &msg);  // merges split items itself
     if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
     if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: tensor-core decode launch");
-    if (plan->num_split_items > 0) {
-      SplitMergeArgs m;
-      m.ws = a.ws;
-      m.num_split_items = plan->num_split_items;
-      m.rows_per_item = plan->rows_per_item;
-      m.group = group;
-      m.q_tile = 1;
-      m.num_qo_heads = plan->num_qo_heads;
-      m.qo_indptr = nullptr;
-      m.o = o;
-      m.lse = lse;
-      m.dtype = dtype;
-      e = launch_split_merge(m, st);
-      if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: merge kernel launch");
-    }
     return ATTN_OK;
   }
   DecodeArgs a;

@@ -81,7 +81,7 @@ struct DecodeTcParams {
 };
 
 struct DGeo {
-  int32_t r, hk, slot, page_base, ntiles;
+  int32_t r, hk, slot, split, page_base, ntiles;
   int64_t tok_begin, tok_end;
 };
 
@@ -93,6 +93,7 @@ __device__ __forceinline__ DGeo decode_geo(const AppendArgs& a, int ui) {
   g.r = x.x;
   g.hk = x.y;
   g.slot = y.y;
+  g.split = y.z;
   g.page_base = __ldg(a.kv_indptr + g.r);
   const int64_t n = int64_t(__ldg(a.kv_indptr + g.r + 1)) - g.page_base;
   const int64_t kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
@@ -140,6 +141,57 @@ __device__ __forceinline__ void store_out32(float* dst, const float* v, float sc
       *reinterpret_cast<float4*>(dst + i) =
           make_float4(v[i] * scale, v[i + 1] * scale, v[i + 2] * scale, v[i + 3] * scale);
   }
+}
+
+// Split item: after this unit's partial state is written, the last of the
+// item's units to arrive (atomic count in the workspace) merges every
+// partial state of the item by log-sum-exp and resets the count to 0.
+// One warp: lane = head hh * (32 / G) + dl, dims [4 G dl, 4 G dl + 4 G).
+template <bool BF16, int G>
+__device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo& g) {
+  constexpr int LP = 32 / G, DL = 4 * G;
+  const int lane = threadIdx.x & 31;
+  __threadfence();  // every lane's partial stores before the arrival
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    const int4 mi = __ldg(a.ws.merge_items + g.split);
+    last = atomicAdd(a.ws.counters + g.split, 1) == mi.w - 1;
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return true;
+  __threadfence();  // the other units' partial states
+  const int hh = lane / LP, dl = lane % LP;
+  const int s0 = __ldg(a.ws.merge_indptr + g.split), s1 = __ldg(a.ws.merge_indptr + g.split + 1);
+  float M = -INFINITY;
+  for (int sl = s0; sl < s1; ++sl) M = fmaxf(M, __ldcg(a.ws.partial_lse + int64_t(sl) * G + hh));
+  float acc[DL];
+#pragma unroll
+  for (int j = 0; j < DL; ++j) acc[j] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int sl = s0; sl < s1; ++sl) {
+      const int64_t prow = int64_t(sl) * G + hh;
+      const float f = ex2(__ldcg(a.ws.partial_lse + prow) - M);
+      L += f;
+      const float4* src = reinterpret_cast<const float4*>(a.ws.partial_o + prow * kHeadDim + DL * dl);
+#pragma unroll
+      for (int j = 0; j < DL / 4; ++j) {
+        const float4 x = __ldcg(src + j);
+        acc[4 * j] += f * x.x;
+        acc[4 * j + 1] += f * x.y;
+        acc[4 * j + 2] += f * x.z;
+        acc[4 * j + 3] += f * x.w;
+      }
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int64_t orow = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * G + hh;
+#pragma unroll
+  for (int j = 0; j < DL; j += 8)
+    store_out16<BF16, 8>(a.o, orow * kHeadDim + DL * dl + j, acc + j, inv);
+  if (dl == 0 && a.lse) a.lse[orow] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
+  if (lane == 0) a.ws.counters[g.split] = 0;
+  return true;
 }
 
 template <bool BF16, int G>
@@ -436,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* dst = a.ws.partial_o + prow * kHeadDim + W * c;
             for (int j = 0; j < W; ++j) dst[j] = 0.f;
             if (c == 0) a.ws.partial_lse[prow] = -INFINITY;
+            merge_split_impl<BF16, G>(a, g);
           }
           continue;
         }
@@ -611,6 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.o_free));
+        if (g.slot >= 0 && !merge_split_impl<BF16, G>(a, g)) {
+          ok = false;
+          break;
+        }
       }
   }
 
