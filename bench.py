@@ -43,6 +43,20 @@ HOST_COVER_CYCLES = 2_000_000  # ~1 ms of GPU sleep before each timed step
 
 
 # ------------------------------------------------------------------ helpers
+def max_over_ranks(times, device):
+    """Element-wise max of per-rank times over the process group (the job
+    takes as long as its slowest replica)."""
+    t = torch.tensor(times, device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_gbs(bytes_per_step, world, step_s):
+    """Whole-job throughput: every replica moves bytes_per_step per step and
+    the step time is the slowest replica's."""
+    return bytes_per_step * world / step_s / 1e9
+
+
 class L2Flush:
     """Between timed steps: write 512 MB (evicts every line of the previous
     step), then read 256 MB of another buffer, so that the dirty lines of the
@@ -410,10 +424,8 @@ def run_ours(args, rank, world):
     step_s = float(np.mean(step_ms)) * 1e-3
     kern_s = float(np.mean(kern_ms)) * 1e-3
     if world > 1:
-        t = torch.tensor([step_s, kern_s], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_s, kern_s = float(t[0]), float(t[1])
-    value = b * world / step_s / 1e9
+        step_s, kern_s = max_over_ranks([step_s, kern_s], "cuda")
+    value = whole_job_gbs(b, world, step_s)
 
     # end to end through the public API with host buffers
     e2e = None
