@@ -234,6 +234,22 @@ attn_status_t attn_merge_states(const void* o_a, const float* lse_a,
 attn_status_t attn_workspace_status(const void* dev_ws, void* stream, int32_t* code_out);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages; it checks this
+ * library's bounded waits). Enqueues on `stream` one warp that waits, with
+ * the same bounded wait every kernel here uses, on an mbarrier that nothing
+ * arrives on. The wait gives up after limit_us microseconds and writes code
+ * 0x1ff into dev_ws's error word (unless the word already holds a code, in
+ * which case it gives up at once). The GPU never faults or hangs:
+ * attn_workspace_status then returns TIMEOUT and the context stays usable;
+ * the next attn_plan on the workspace clears the word.
+ *   dev_ws   : a workspace given to attn_plan (or any 256-byte aligned
+ *              device buffer of at least 4 bytes)
+ *   limit_us : 1 .. 10^7
+ * Errors: INVALID_ARG, CUDA.
+ */
+attn_status_t attn_wait_selftest(void* dev_ws, int32_t limit_us, void* stream);
+
+/*
  * Batch decode for callers that cannot allocate device memory. The paper has
  * no counterpart: this is a deployment convenience of this library.
  *

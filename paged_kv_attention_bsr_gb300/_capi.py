@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_S
 # Every symbol include/attn.h declares (checked by the tests).
 EXPORTS = ("attn_workspace_size", "attn_default_num_ctas", "attn_plan", "attn_decode_run",
            "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error",
-           "attn_decode_run_noalloc")
+           "attn_decode_run_noalloc", "attn_wait_selftest")
 
 
 class AttnError(RuntimeError):
@@ -67,6 +67,7 @@ def _load():
                             vp, vp, sz, vp],
         "attn_merge_states": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp],
         "attn_workspace_status": [vp, vp, P(i32)],
+        "attn_wait_selftest": [vp, i32, vp],
         "attn_decode_run_noalloc": [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64, i32, vp,
                                     vp, vp, i32, f32, vp, vp, vp],
     }
@@ -186,6 +187,11 @@ def merge_states(o_a, lse_a, o_b, lse_b, o_out, lse_out, stream=None):
     n, h, d = o_a.shape
     _check(lib.attn_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out),
                                  _ptr(lse_out), n, h, d, dtype_code(o_a.dtype), _stream(stream)))
+
+
+def wait_selftest(dev_ws, limit_us, stream=None):
+    """attn_wait_selftest: one bounded wait that nothing completes."""
+    _check(lib.attn_wait_selftest(_ptr(dev_ws), int(limit_us), _stream(stream)))
 
 
 def workspace_status(dev_ws, stream=None) -> int:

@@ -13,7 +13,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn.so")
 SOURCES = ["capi.cpp", "plan.cpp", "decode.cu", "decode_tc.cu", "merge.cu", "append.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -326,6 +326,16 @@ attn_status_t attn_merge_states(const void* o_a, const float* lse_a, const void*
   return ATTN_OK;
 }
 
+attn_status_t attn_wait_selftest(void* dev_ws, int32_t limit_us, void* stream) {
+  if (!dev_ws) return fail(ATTN_ERR_INVALID_ARG, "attn_wait_selftest: dev_ws is NULL");
+  if (limit_us < 1 || limit_us > 10000000)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_wait_selftest: limit_us must be in [1, 10^7]");
+  cudaError_t e = launch_wait_selftest(static_cast<int32_t*>(dev_ws), uint64_t(limit_us) * 1000u,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_wait_selftest: launch");
+  return ATTN_OK;
+}
+
 attn_status_t attn_workspace_status(const void* dev_ws, void* stream, int32_t* code_out) {
   if (!dev_ws || !code_out)
     return fail(ATTN_ERR_INVALID_ARG, "attn_workspace_status: null pointer");

@@ -162,6 +162,10 @@ struct SplitMergeArgs {
 };
 cudaError_t launch_split_merge(const SplitMergeArgs& a, cudaStream_t stream);
 
+// One warp waits, with the kernels' bounded wait and the given limit, on an
+// mbarrier nothing arrives on (attn_wait_selftest).
+cudaError_t launch_wait_selftest(int32_t* error_word, uint64_t limit_ns, cudaStream_t stream);
+
 // Sets the text attn_last_error() returns on this thread.
 void set_last_error(const std::string& msg);
 

@@ -58,6 +58,7 @@ enum : int32_t {
   ERR_WAIT_MMA = 0x104,
   ERR_WAIT_SOFTMAX = 0x105,
   ERR_WAIT_DRAIN = 0x106,
+  ERR_WAIT_SELFTEST = 0x1ff,  // attn_wait_selftest's wait (nothing arrives)
 };
 
 // Upper bound for any single wait inside a kernel (the slowest legitimate
@@ -65,21 +66,26 @@ enum : int32_t {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Bounded parity wait. Returns false (and records `code`) if the phase did
-// not complete within kWaitLimitNs or another warp already reported an error.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int32_t* err, int32_t code) {
+// not complete within limit_ns or another warp already reported an error.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
+                                                volatile int32_t* err, int32_t code,
+                                                uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*err != 0) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicCAS(const_cast<int32_t*>(err), 0, code);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int32_t* err, int32_t code) {
+  return mbar_wait_limit(bar, parity, err, code, kWaitLimitNs);
 }
 
 // ------------------------------------------------------- bulk async copies

@@ -65,6 +65,10 @@ def test_workspace_size_and_validation_without_gpu():
     assert st == C.ERR_WORKSPACE_TOO_SMALL
     st = C.lib.attn_merge_states(None, None, None, None, None, None, 4, 2, 100, 1, None)
     assert st == C.ERR_UNSUPPORTED
+    # the wait self-test validates before it launches anything
+    assert C.lib.attn_wait_selftest(None, 1000, None) == C.ERR_INVALID_ARG
+    assert C.lib.attn_wait_selftest(ctypes.c_void_p(256), 0, None) == C.ERR_INVALID_ARG
+    assert C.lib.attn_wait_selftest(ctypes.c_void_p(256), 10000001, None) == C.ERR_INVALID_ARG
 
 
 def test_product_path_does_not_import_the_oracle():
