@@ -93,21 +93,24 @@ def _check(status: int):
 
 
 def _ptr(x):
-    """Device/host address of a tensor or numpy array (None -> NULL)."""
+    """Device/host address of a tensor or numpy array as an int (None -> NULL);
+    the c_void_p argtypes take ints as they are."""
     if x is None:
         return None
     if isinstance(x, torch.Tensor):
-        return ctypes.c_void_p(x.data_ptr())
+        return x.data_ptr()
     if isinstance(x, np.ndarray):
-        return x.ctypes.data_as(ctypes.c_void_p)
+        return x.ctypes.data
     if isinstance(x, int):
-        return ctypes.c_void_p(x)
+        return x
     raise TypeError(f"cannot take the address of {type(x)}")
 
 
 def _host_i32(x):
     if x is None:
         return None
+    if isinstance(x, np.ndarray) and x.dtype == np.int32 and x.flags.c_contiguous:
+        return x
     if isinstance(x, torch.Tensor):
         x = x.detach().cpu().numpy()
     return np.ascontiguousarray(x, dtype=np.int32)
@@ -124,7 +127,7 @@ def dtype_code(t: torch.dtype) -> int:
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def workspace_size(max_batch, max_total_qo, num_qo_heads, num_kv_heads, head_dim, num_ctas):

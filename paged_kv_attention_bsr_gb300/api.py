@@ -43,7 +43,7 @@ class PagedAttention:
         self.dev_ws = torch.empty(dev_bytes, dtype=torch.uint8, device=self.device)
         self._pinned = [torch.empty(host_bytes, dtype=torch.uint8).pin_memory()
                         for _ in range(self.RING)]
-        self._events = [None] * self.RING
+        self._events = [None] * self.RING  # created on first use, then re-recorded
         self._turn = 0
         self.plan_info: Optional[C.Plan] = None
 
@@ -53,14 +53,17 @@ class PagedAttention:
             raise ValueError("decode plans take no qo_indptr; append plans need one")
         i = self._turn
         self._turn = (self._turn + 1) % self.RING
-        if self._events[i] is not None:
-            self._events[i].synchronize()
+        ev = self._events[i]
+        if ev is None:
+            ev = self._events[i] = torch.cuda.Event()
+        else:
+            ev.synchronize()  # the previous upload from this staging buffer has run
+        if stream is None:
+            stream = torch.cuda.current_stream()
         self.plan_info = C.plan(qo_indptr_h, kv_indptr_h, last_page_len_h, page_size,
                                 self.num_qo_heads, self.num_kv_heads, self.head_dim, causal,
                                 self.num_ctas, self._pinned[i], self.dev_ws, stream)
-        ev = torch.cuda.Event()
-        ev.record(stream if stream is not None else torch.cuda.current_stream())
-        self._events[i] = ev
+        ev.record(stream)
         self._causal = bool(causal)
         return self.plan_info
 

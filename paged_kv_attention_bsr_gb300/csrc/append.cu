@@ -742,9 +742,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
                     &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorInvalidValue;
   // at most one CTA per SM (shared memory); extra plan CTAs are run in turn
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  cudaError_t e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int grid = a.num_ctas < sms ? a.num_ctas : sms;
   // one query tile per item suffices when no request has more queries than a tile

@@ -726,9 +726,8 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
   if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
                     &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorInvalidValue;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  cudaError_t e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int grid = a.num_ctas < sms ? a.num_ctas : sms;
   return bf16 ? launch_dt<true>(prm, grid, stream) : launch_dt<false>(prm, grid, stream);

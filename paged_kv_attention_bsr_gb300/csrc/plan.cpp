@@ -117,7 +117,9 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
     *msg = "attn_plan: qo_indptr must start at 0 (q rows are indexed from the tensor start)";
     return ATTN_ERR_INVALID_ARG;
   }
-  std::vector<Item> items;
+  // scratch reused across calls on this thread (a plan runs every step)
+  thread_local std::vector<Item> items;
+  items.clear();
   items.reserve(size_t(batch) * num_kv_heads);
   int64_t max_qo_len = decode ? 1 : 0;
   for (int32_t r = 0; r < batch; ++r) {
@@ -163,16 +165,35 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   int64_t W = 0;
   for (const Item& it : items) W += it.n + kAlpha;
   const int64_t C = num_ctas;
-  auto bound = [&](int64_t c) -> int64_t { return (c * W) / C; };
+  thread_local std::vector<int64_t> bounds;  // floor(c W / C), c = 0 .. C (decode cut)
+  if (decode) {
+    // floor(c W / C) by a running quotient and remainder (one division)
+    bounds.resize(size_t(C) + 1);
+    const int64_t dq = W / C, dr = W % C;
+    int64_t q = 0, rem = 0;
+    for (int64_t c = 0; c <= C; ++c) {
+      bounds[size_t(c)] = q;
+      q += dq;
+      rem += dr;
+      if (rem >= C) {
+        ++q;
+        rem -= C;
+      }
+    }
+  }
+  const int64_t* const bnd = bounds.data();
+  auto bound = [bnd](int64_t c) -> int64_t { return bnd[c]; };
 
   struct U {
     Unit u;
     int32_t cta;
     int32_t item;
   };
-  std::vector<U> gen;  // units in generation order
+  thread_local std::vector<U> gen;  // units in generation order
+  gen.clear();
   gen.reserve(items.size() + size_t(C));
-  std::vector<int64_t> load(size_t(C), 0);
+  thread_local std::vector<int64_t> load;
+  load.assign(size_t(C), 0);
 
   if (decode) {
     // Contiguous balanced cut of the cost line (Stream-K style).
@@ -238,11 +259,13 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   }
 
   // ---- split items, slots in (item, page) order
-  std::vector<int32_t> n_units(items.size(), 0);
+  thread_local std::vector<int32_t> n_units, split_of, merge_indptr;
+  thread_local std::vector<int4> merge_items;
+  n_units.assign(items.size(), 0);
   for (const U& g : gen) n_units[size_t(g.item)]++;
-  std::vector<int32_t> split_of(items.size(), -1);
-  std::vector<int32_t> merge_indptr(1, 0);
-  std::vector<int4> merge_items;
+  split_of.assign(items.size(), -1);
+  merge_indptr.assign(1, 0);
+  merge_items.clear();
   for (size_t k = 0; k < items.size(); ++k) {
     if (n_units[k] < 2) continue;
     split_of[k] = int32_t(merge_items.size());
@@ -252,7 +275,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   const int32_t slots = merge_indptr.back();
   {
     // units of one item are generated in page order
-    std::vector<int32_t> next(merge_items.size(), 0);
+    thread_local std::vector<int32_t> next;
+    next.assign(merge_items.size(), 0);
     for (U& g : gen) {
       const int32_t sid = split_of[size_t(g.item)];
       if (sid < 0) continue;
@@ -262,12 +286,17 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   }
 
   // ---- per-CTA lists (generation order within a CTA)
-  std::vector<int32_t> work_indptr(size_t(C) + 1, 0);
+  thread_local std::vector<int32_t> work_indptr;
+  work_indptr.assign(size_t(C) + 1, 0);
   for (const U& g : gen) work_indptr[size_t(g.cta) + 1]++;
   for (int64_t i = 0; i < C; ++i) work_indptr[i + 1] += work_indptr[i];
-  std::vector<Unit> units(gen.size());
-  {
-    std::vector<int32_t> at(work_indptr.begin(), work_indptr.end() - 1);
+  thread_local std::vector<Unit> units;
+  units.resize(gen.size());
+  if (decode) {  // the contiguous cut generates units in CTA order already
+    for (size_t i = 0; i < gen.size(); ++i) units[i] = gen[i].u;
+  } else {
+    thread_local std::vector<int32_t> at;
+    at.assign(work_indptr.begin(), work_indptr.end() - 1);
     for (const U& g : gen) units[size_t(at[size_t(g.cta)]++)] = g.u;
   }
   int64_t max_load = 0;

@@ -202,7 +202,7 @@ inline uint32_t make_idesc(bool bf16, bool b_mn_major) {
 // The paged K and V pools as 2-D tensors [pages * kv heads * page_size, 128]
 // with 16-row x 64-column boxes and the 128-byte swizzle. Returns false when
 // the driver cannot describe them (message in *msg).
-inline bool make_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
+inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
                          int32_t num_kv_heads, int32_t page_size, bool bf16, CUtensorMap* tm_k,
                          CUtensorMap* tm_v, const char** msg) {
   EncodeTiledFn enc = encode_fn();
@@ -232,6 +232,48 @@ inline bool make_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pag
     }
   }
   return true;
+}
+
+// encode_kv_maps, remembering the last pools described on this thread (a
+// serving loop runs over the same pools step after step).
+inline bool make_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
+                         int32_t num_kv_heads, int32_t page_size, bool bf16, CUtensorMap* tm_k,
+                         CUtensorMap* tm_v, const char** msg) {
+  struct Key {
+    const void *k, *v;
+    int64_t pages;
+    int32_t heads, page_size, bf16;
+  };
+  thread_local Key last = {nullptr, nullptr, -1, 0, 0, 0};
+  thread_local CUtensorMap last_k, last_v;
+  const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16 ? 1 : 0};
+  if (key.k == last.k && key.v == last.v && key.pages == last.pages && key.heads == last.heads &&
+      key.page_size == last.page_size && key.bf16 == last.bf16) {
+    *tm_k = last_k;
+    *tm_v = last_v;
+    return true;
+  }
+  if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16, tm_k, tm_v, msg))
+    return false;
+  last = key;
+  last_k = *tm_k;
+  last_v = *tm_v;
+  return true;
+}
+
+// Number of SMs of the current device (cached per device on this thread).
+inline cudaError_t current_sm_count(int* sms) {
+  thread_local int cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *sms = cache[dev];
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev] = *sms;
+  return e;
 }
 
 }  // namespace attn
