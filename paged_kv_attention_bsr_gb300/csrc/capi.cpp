@@ -282,6 +282,16 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
   a.sm_scale = sm_scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const char* msg = "";
+  if (few_row_rows(a.group, a.max_qo_len) != 0) {
+    // Short appends (group x longest query count <= 16 packed rows, e.g. the
+    // n generations of a shared prefix): the few-row kernel keeps the
+    // softmax off the critical path of an HBM-bound pass and merges split
+    // items itself.
+    cudaError_t e = launch_decode_tc(a, st, &msg);
+    if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: few-row kernel launch");
+    return ATTN_OK;
+  }
   cudaError_t e = launch_append(a, st, &msg);
   if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
   if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: append kernel launch");

@@ -8,27 +8,30 @@
 // (request, kv head) items into page ranges balanced across a persistent
 // fixed grid, and split items are joined afterwards by their log-sum-exp.
 //
-// A unit (request r, kv head hk, pages [p0, p1)) multiplies the G query
-// heads of its GQA group with 128-token K/V tiles:
+// A unit (request r, kv head hk, pages [p0, p1)) multiplies the R packed
+// query rows of its item (row rho = token i x group + head h: the GQA group's
+// heads in decode, R = group; a few new tokens per request in a short
+// append, R >= qo_len x group) with 128-token K/V tiles:
 //   S = Q K^T     A = Q (smem, K-major), B = K (smem, K-major), D = TMEM
 //   P = exp2(S c - m) over each row, written over S in TMEM (16-bit)
 //   O += P V      A = P (TMEM), B = V (smem, MN-major), D = TMEM
-// Only G of the 128 MMA rows would hold queries, and one thread per row
-// would exponentiate all 128 scores of a tile. Instead the G heads are
-// replicated C = 32 / G times in query rows 0..31 (row h + G c is copy c of
-// head h) and copy c owns kv columns [W c, W c + W) of every tile
-// (W = 128 / C = 4 G). One warp runs the softmax with one TMEM lane per
-// thread, W exponentials per thread and tile; the copies of a head share
-// the running max through shuffles, write P only in their own columns
-// (zeros elsewhere), and their O rows -- partial sums over disjoint tokens
-// at a common scale -- are added in the epilogue. Rows 32..127 carry no
-// queries and are never read back.
+// Only R of the 128 MMA rows would hold queries, and one thread per row
+// would exponentiate all 128 scores of a tile. Instead the R rows are
+// replicated C = 32 / R times in query rows 0..31 (row rho + R c is copy c of
+// row rho) and copy c owns kv columns [W c, W c + W) of every tile
+// (W = 128 / C = 4 R). One warp runs the softmax with one TMEM lane per
+// thread, W exponentials per thread and tile; the copies of a row share the
+// running max through shuffles, write P only in their own columns (zeros
+// elsewhere), and their O rows -- partial sums over disjoint tokens at a
+// common scale -- are added in the epilogue. Rows 32..127 carry no queries
+// and are never read back. A causal short append masks each row at its own
+// end-aligned limit (token i of qo_len sees kv positions <= kv_len - qo_len + i).
 //
 // Warps (128 threads, one CTA per SM): 0 softmax + epilogue; 1 TMA producer
 // of the K/V ring (six 32 KB slots, 16-row boxes gathered by page index);
 // 2 TMEM allocation and the MMAs (one thread: S of tile k+1 runs under the
 // softmax of tile k, S double-buffered in TMEM); 3 query loader (plain
-// loads of the next unit's G query rows into registers, stored into the
+// loads of the next unit's R query rows into registers, stored into the
 // swizzled query tile as soon as the last S of the current unit is done).
 // Every wait is bounded; TMEM is freed on every path.
 #include <cuda.h>
@@ -81,10 +84,13 @@ struct DecodeTcParams {
 };
 
 struct DGeo {
-  int32_t r, hk, slot, split, page_base, ntiles;
+  int32_t r, hk, t, slot, split, page_base, ntiles;
+  int64_t qo_start, qo_len, kv_len;
   int64_t tok_begin, tok_end;
 };
 
+// DEC: decode (one query row per request, the whole kv visible).
+template <bool DEC>
 __device__ __forceinline__ DGeo decode_geo(const AppendArgs& a, int ui) {
   const int4* rec = reinterpret_cast<const int4*>(a.ws.units + ui);
   const int4 x = __ldg(rec);
@@ -92,16 +98,53 @@ __device__ __forceinline__ DGeo decode_geo(const AppendArgs& a, int ui) {
   DGeo g;
   g.r = x.x;
   g.hk = x.y;
+  g.t = x.z;
   g.slot = y.y;
   g.split = y.z;
+  if constexpr (!DEC) {
+    g.qo_start = __ldg(a.qo_indptr + g.r);
+    g.qo_len = int64_t(__ldg(a.qo_indptr + g.r + 1)) - g.qo_start;
+  } else {  // decode: one query row per request
+    g.qo_start = g.r;
+    g.qo_len = 1;
+  }
   g.page_base = __ldg(a.kv_indptr + g.r);
   const int64_t n = int64_t(__ldg(a.kv_indptr + g.r + 1)) - g.page_base;
-  const int64_t kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
+  g.kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
+  int64_t vis = g.kv_len;
+  if (!DEC && a.causal) {  // the item's last query row sees the most
+    const int64_t last_row = min(int64_t(g.t + 1) * a.q_tile, g.qo_len) - 1;
+    vis = min(g.kv_len, max(int64_t(0), g.kv_len - g.qo_len + last_row + 1));
+  }
   g.tok_begin = int64_t(x.w) * a.page_size;
-  g.tok_end = min(int64_t(y.x) * a.page_size, kv_len);
+  g.tok_end = min(int64_t(y.x) * a.page_size, vis);
   const int64_t nt = g.tok_end - g.tok_begin;
   g.ntiles = nt > 0 ? int32_t((nt + kTile - 1) / kTile) : 0;
   return g;
+}
+
+// Packed query row rho of a unit: its token and head, output row and the
+// last kv position it may see (ok = false for rows past the request's queries).
+struct QRow {
+  bool ok;
+  int64_t orow;   // row of q / o / lse ([tokens, Hq] flattened)
+  int64_t limit;  // last visible kv position
+};
+template <bool DEC, int R>
+__device__ __forceinline__ QRow qrow(const AppendArgs& a, const DGeo& g, int rho) {
+  QRow q;
+  if constexpr (DEC) {  // rows are the group's heads (group = R)
+    q.ok = true;
+    q.orow = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * R + rho;
+    q.limit = g.kv_len - 1;
+  } else {
+    const int tok = rho / a.group, hh = rho - tok * a.group;
+    const int64_t qi = int64_t(g.t) * a.q_tile + tok;
+    q.ok = qi < g.qo_len;
+    q.orow = (g.qo_start + qi) * a.num_qo_heads + int64_t(g.hk) * a.group + hh;
+    q.limit = a.causal ? g.kv_len - g.qo_len + qi : g.kv_len - 1;
+  }
+  return q;
 }
 
 template <int N>
@@ -113,9 +156,11 @@ struct ILog2<1> {
   static constexpr int value = 0;
 };
 
-// N consecutive outputs (N = 1, 2, 4 or 8) of one row, scaled: 16-bit or fp32.
+// N consecutive outputs (N = 1, 2, 4 or a multiple of 8) of one row,
+// scaled: 16-bit or fp32.
 template <bool BF16, int N>
 __device__ __forceinline__ void store_out16(void* o, int64_t idx, const float* v, float scale) {
+  static_assert(N == 1 || N == 2 || N == 4 || N % 8 == 0, "output run length");
   uint16_t* dst = static_cast<uint16_t*>(o) + idx;
   if constexpr (N == 1) {
     if constexpr (BF16)
@@ -128,11 +173,17 @@ __device__ __forceinline__ void store_out16(void* o, int64_t idx, const float* v
     for (int i = 0; i < N / 2; ++i) w[i] = pack2<BF16>(v[2 * i] * scale, v[2 * i + 1] * scale);
     if constexpr (N == 2) *reinterpret_cast<uint32_t*>(dst) = w[0];
     if constexpr (N == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-    if constexpr (N == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    if constexpr (N % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < N / 8; ++i)
+        reinterpret_cast<uint4*>(dst)[i] =
+            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
   }
 }
 template <int N>
 __device__ __forceinline__ void store_out32(float* dst, const float* v, float scale) {
+  static_assert(N == 1 || N == 2 || N % 4 == 0, "output run length");
   if constexpr (N == 1) dst[0] = v[0] * scale;
   if constexpr (N == 2) *reinterpret_cast<float2*>(dst) = make_float2(v[0] * scale, v[1] * scale);
   if constexpr (N >= 4) {
@@ -146,10 +197,10 @@ __device__ __forceinline__ void store_out32(float* dst, const float* v, float sc
 // Split item: after this unit's partial state is written, the last of the
 // item's units to arrive (atomic count in the workspace) merges every
 // partial state of the item by log-sum-exp and resets the count to 0.
-// One warp: lane = head hh * (32 / G) + dl, dims [4 G dl, 4 G dl + 4 G).
-template <bool BF16, int G>
+// One warp: lane = row rho * (32 / R) + dl, dims [4 R dl, 4 R dl + 4 R).
+template <bool BF16, int R, bool DEC>
 __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo& g) {
-  constexpr int LP = 32 / G, DL = 4 * G;
+  constexpr int LP = 32 / R, DL = 4 * R, kS = DL < 8 ? DL : 8;
   const int lane = threadIdx.x & 31;
   __threadfence();  // every lane's partial stores before the arrival
   __syncwarp();
@@ -160,17 +211,19 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return true;
   __threadfence();  // the other units' partial states
-  const int hh = lane / LP, dl = lane % LP;
+  const int rho = lane / LP, dl = lane % LP;
+  const QRow qr = qrow<DEC, R>(a, g, rho);
   const int s0 = __ldg(a.ws.merge_indptr + g.split), s1 = __ldg(a.ws.merge_indptr + g.split + 1);
   float M = -INFINITY;
-  for (int sl = s0; sl < s1; ++sl) M = fmaxf(M, __ldcg(a.ws.partial_lse + int64_t(sl) * G + hh));
+  for (int sl = s0; sl < s1; ++sl)
+    M = fmaxf(M, __ldcg(a.ws.partial_lse + int64_t(sl) * a.rows_per_item + rho));
   float acc[DL];
 #pragma unroll
   for (int j = 0; j < DL; ++j) acc[j] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
     for (int sl = s0; sl < s1; ++sl) {
-      const int64_t prow = int64_t(sl) * G + hh;
+      const int64_t prow = int64_t(sl) * a.rows_per_item + rho;
       const float f = ex2(__ldcg(a.ws.partial_lse + prow) - M);
       L += f;
       const float4* src = reinterpret_cast<const float4*>(a.ws.partial_o + prow * kHeadDim + DL * dl);
@@ -184,20 +237,21 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
       }
     }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int64_t orow = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * G + hh;
+  if (qr.ok) {
+    const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-  for (int j = 0; j < DL; j += 8)
-    store_out16<BF16, 8>(a.o, orow * kHeadDim + DL * dl + j, acc + j, inv);
-  if (dl == 0 && a.lse) a.lse[orow] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
+    for (int j = 0; j < DL; j += kS)
+      store_out16<BF16, kS>(a.o, qr.orow * kHeadDim + DL * dl + j, acc + j, inv);
+    if (dl == 0 && a.lse) a.lse[qr.orow] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
+  }
   if (lane == 0) a.ws.counters[g.split] = 0;
   return true;
 }
 
-template <bool BF16, int G>
+template <bool BF16, int R, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
-  constexpr int C = 32 / G;     // copies of each head
+  constexpr int C = 32 / R;     // copies of each query row
   constexpr int W = kTile / C;  // kv columns per copy and tile
   constexpr int LC = ILog2<C>::value;
   extern __shared__ uint8_t smem_raw[];
@@ -262,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
       for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
            ++ui) {
-        const DGeo g = decode_geo(a, ui);
+        const DGeo g = decode_geo<DEC>(a, ui);
         if (g.ntiles == 0) continue;
         int32_t row = chunk_row(g, 0);
         for (int i = 0; i < g.ntiles && ok; ++i) {
@@ -305,20 +359,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpQ) {
     // ------------------------------------------------------------ query loader
-    // The G query rows of a unit (G x 256 B) are read with plain loads one
-    // unit ahead and stored C times into the swizzled query tile.
-    constexpr int kVec = G * 16;            // 16-byte pieces of the G rows
+    // The R query rows of a unit (R x 256 B) are read with plain loads one
+    // unit ahead and stored C times into the swizzled query tile (rows past
+    // the request's queries as zeros).
+    constexpr int kVec = R * 16;            // 16-byte pieces of the R rows
     constexpr int kPer = (kVec + 31) / 32;  // pieces per lane
     uint4 qr[kPer];
     uint32_t ua = 0;
     auto fetch = [&](const DGeo& g) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const uint16_t*>(a.q) +
-          (int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * G) * kHeadDim);
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const int idx = lane + 32 * j;
-        if (idx < kVec) qr[j] = __ldg(src + idx);
+        if (idx < kVec) {
+          const QRow q = qrow<DEC, R>(a, g, idx >> 4);
+          qr[j] = q.ok ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                                              q.orow * kHeadDim) +
+                               (idx & 15))
+                       : make_uint4(0, 0, 0, 0);
+        }
       }
     };
     // the units of this CTA that have kv tokens, in order
@@ -326,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto next_unit = [&](DGeo& g) -> bool {
       while (vc < a.num_ctas) {
         if (ui < __ldg(a.ws.work_indptr + vc + 1)) {
-          g = decode_geo(a, ui++);
+          g = decode_geo<DEC>(a, ui++);
           if (g.ntiles > 0) return true;
         } else {
           vc += gridDim.x;
@@ -347,11 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kPer; ++j) {
         const int idx = lane + 32 * j;
         if (idx < kVec) {
-          const int h = idx >> 4, ch = idx & 15;
+          const int rho = idx >> 4, ch = idx & 15;
           const int half = ch >> 3, j8 = ch & 7;
 #pragma unroll
           for (int c = 0; c < C; ++c) {
-            const int row = h + G * c;
+            const int row = rho + R * c;
             const int off = kOffQ + half * kHalf + row * 128 + ((j8 ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(gbase + off) = qr[j];
           }
@@ -409,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
         for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
              ++ui) {
-          const DGeo g = decode_geo(a, ui);
+          const DGeo g = decode_geo<DEC>(a, ui);
           if (g.ntiles == 0) continue;
           const int n = g.ntiles;
           if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) ||
@@ -459,22 +517,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpSoftmax) {
     // ------------------------------------------------- softmax / epilogue
-    // Thread (h, c) = lane (h = lane % G, c = lane / G) owns TMEM lane `lane`:
-    // copy c of query head h, kv columns [W c, W c + W) of every tile.
-    // Waits are made warp-uniform: the tcgen05.ld/st after them are
+    // Thread (rho, c) = lane (rho = lane % R, c = lane / R) owns TMEM lane
+    // `lane`: copy c of query row rho, kv columns [W c, W c + W) of every
+    // tile. Waits are made warp-uniform: the tcgen05.ld/st after them are
     // .sync.aligned.
-    const int h = lane % G;
-    const int c = lane / G;
+    const int rho = lane % R;
+    const int c = lane / R;
     const float c2 = prm.scale_log2;
     uint32_t n_t = 0;
     bool ok = true;
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
       for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
            ++ui) {
-        const DGeo g = decode_geo(a, ui);
-        const int64_t orow = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * G + h;
+        const DGeo g = decode_geo<DEC>(a, ui);
+        const QRow qr = qrow<DEC, R>(a, g, rho);
+        const int64_t orow = qr.orow;
+        const int64_t prow = int64_t(g.slot) * a.rows_per_item + rho;  // split items
         if (g.ntiles == 0) {  // no kv: o = 0, lse = -inf
-          if (g.slot < 0) {
+          if (!qr.ok) {
+          } else if (g.slot < 0) {
             constexpr int kS = W < 8 ? W : 8;
             float z[kS];
 #pragma unroll
@@ -484,14 +545,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               store_out16<BF16, kS>(a.o, orow * kHeadDim + W * c + j, z, 1.f);
             if (c == 0 && a.lse) a.lse[orow] = -INFINITY;
           } else {
-            const int64_t prow = int64_t(g.slot) * G + h;
             float* dst = a.ws.partial_o + prow * kHeadDim + W * c;
             for (int j = 0; j < W; ++j) dst[j] = 0.f;
             if (c == 0) a.ws.partial_lse[prow] = -INFINITY;
-            merge_split_impl<BF16, G>(a, g);
           }
+          if (g.slot >= 0) merge_split_impl<BF16, R, DEC>(a, g);
           continue;
         }
+        // kv positions this row sees: [tok_begin, row_end)
+        const int64_t row_end = qr.ok ? min(g.tok_end, qr.limit + 1) : g.tok_begin;
         float m_ref = -INFINITY, l = 0.f;
         for (int i = 0; i < g.ntiles; ++i, ++n_t) {
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[n_t & 1u]),
@@ -502,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t col_s = (n_t & 1u) * 128u;
           const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
-          const int nvalid = int(min(int64_t(kTile), g.tok_end - kv0));
+          const int nvalid = int(max(int64_t(0), min(int64_t(kTile), row_end - kv0)));
           // this thread's W scores: columns [W c, W c + W) of its row
           float s[W];
           {
@@ -517,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < W; ++j) s[j] = mine ? v[W * b + j] : s[j];
             }
           }
-          const bool full = nvalid == kTile;
+          // (decode: every row sees the same columns)
+          const bool full = DEC ? nvalid == kTile : __all_sync(0xffffffffu, nvalid == kTile);
           float mx = -INFINITY;
           if (full) {
 #pragma unroll
@@ -527,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < W; ++j) mx = fmaxf(mx, (W * c + j < nvalid) ? s[j] : -INFINITY);
           }
 #pragma unroll
-          for (int st = 0; st < LC; ++st) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, G << st));
+          for (int st = 0; st < LC; ++st) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, R << st));
           const float m_tile = mx * c2;  // -inf stays -inf
           float alpha = 1.f;
           bool rescale_o = false;
@@ -588,8 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // V rows past the unit's end inside its last 16-row chunk hold
           // whatever the pool had there: zero them once the tile's V has
           // landed (whole chunks past the end are skipped by the P.V MMA)
-          const int nrow = ((nvalid + kChunk - 1) / kChunk) * kChunk;
-          if (nvalid < nrow) {
+          const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+          const int nrow = ((ntt + kChunk - 1) / kChunk) * kChunk;
+          if (ntt < nrow) {
             const uint32_t vuse = 2 * n_t + 1;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.slot_full[vuse % kSlots]),
                                                    (vuse / kSlots) & 1u, err, ERR_WAIT_FULL))) {
@@ -597,8 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             uint8_t* vslot = gbase + kOffRing + (vuse % kSlots) * kTileBytes;
-            for (int e = lane; e < (nrow - nvalid) * 16; e += 32) {
-              const int rr = nvalid + (e >> 4), q = e & 15;
+            for (int e = lane; e < (nrow - ntt) * 16; e += 32) {
+              const int rr = ntt + (e >> 4), q = e & 15;
               *reinterpret_cast<uint4*>(vslot + (q >> 3) * kHalf + rr * 128 + (q & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
@@ -617,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float lt = l;
 #pragma unroll
-        for (int st = 0; st < LC; ++st) lt += __shfl_xor_sync(0xffffffffu, lt, G << st);
+        for (int st = 0; st < LC; ++st) lt += __shfl_xor_sync(0xffffffffu, lt, R << st);
         const bool any = lt > 0.f;
         const float inv = any ? 1.f / lt : 0.f;
         const float lse2 = any ? m_ref + lg2(lt) : -INFINITY;
@@ -643,28 +707,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (k < n) {
                 const float send = upper ? o[k] : o[k + n];
                 const float keep = upper ? o[k + n] : o[k];
-                o[k] = keep + __shfl_xor_sync(0xffffffffu, send, G << st);
+                o[k] = keep + __shfl_xor_sync(0xffffffffu, send, R << st);
               }
             }
           }
           const int d0 = 32 * b + doff;
-          if (g.slot < 0) {
+          if (!qr.ok) {
+          } else if (g.slot < 0) {
             store_out16<BF16, NF>(a.o, orow * kHeadDim + d0, o, inv);
           } else {
-            const int64_t prow = int64_t(g.slot) * G + h;
             store_out32<NF>(a.ws.partial_o + prow * kHeadDim + d0, o, inv);
           }
         }
-        if (c == 0) {
+        if (c == 0 && qr.ok) {
           if (g.slot < 0) {
             if (a.lse) a.lse[orow] = lse2 * kLn2;
           } else {
-            a.ws.partial_lse[int64_t(g.slot) * G + h] = lse2;
+            a.ws.partial_lse[prow] = lse2;
           }
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.o_free));
-        if (g.slot >= 0 && !merge_split_impl<BF16, G>(a, g)) {
+        if (g.slot >= 0 && !merge_split_impl<BF16, R, DEC>(a, g)) {
           ok = false;
           break;
         }
@@ -682,37 +746,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16, int G>
-cudaError_t launch_g(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
+template <bool BF16, int R, bool DEC>
+cudaError_t launch_k(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, R, DEC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  decode_tc_kernel<BF16, G><<<grid, kThreads, kSmem, stream>>>(prm);
+  decode_tc_kernel<BF16, R, DEC><<<grid, kThreads, kSmem, stream>>>(prm);
   return cudaGetLastError();
 }
-
+// decode runs with R = group in {2, 4, 8}; short appends with R in {1..16}
 template <bool BF16>
-cudaError_t launch_dt(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
-  switch (prm.a.group) {
-    case 2: return launch_g<BF16, 2>(prm, grid, stream);
-    case 4: return launch_g<BF16, 4>(prm, grid, stream);
-    default: return launch_g<BF16, 8>(prm, grid, stream);
+cudaError_t launch_dt(const DecodeTcParams& prm, int rows, int grid, cudaStream_t stream) {
+  if (!prm.a.qo_indptr) {
+    switch (rows) {
+      case 2: return launch_k<BF16, 2, true>(prm, grid, stream);
+      case 4: return launch_k<BF16, 4, true>(prm, grid, stream);
+      default: return launch_k<BF16, 8, true>(prm, grid, stream);
+    }
+  }
+  switch (rows) {
+    case 1: return launch_k<BF16, 1, false>(prm, grid, stream);
+    case 2: return launch_k<BF16, 2, false>(prm, grid, stream);
+    case 4: return launch_k<BF16, 4, false>(prm, grid, stream);
+    case 8: return launch_k<BF16, 8, false>(prm, grid, stream);
+    default: return launch_k<BF16, 16, false>(prm, grid, stream);
   }
 }
 
 }  // namespace
 
+int few_row_rows(int32_t group, int32_t max_qo_len) {
+  const int64_t need = int64_t(group) * (max_qo_len > 0 ? max_qo_len : 1);
+  for (int r = 1; r <= kFewRowMax; r *= 2)
+    if (need <= r) return r;
+  return 0;
+}
+
 cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const char** msg) {
-  if (a.group != 2 && a.group != 4 && a.group != 8) {
-    *msg = "attn_decode_run: the tensor-core decode kernel takes groups of 2, 4 or 8";
+  const int rows = few_row_rows(a.group, a.qo_indptr ? a.max_qo_len : 1);
+  if (rows == 0 || (!a.qo_indptr && (rows < 2 || rows > 8 || rows != a.group))) {
+    *msg = "attn: the few-row tensor-core kernel takes 2, 4 or 8 heads per kv head in decode "
+           "and at most 16 packed query rows per item in append";
     return cudaErrorNotSupported;
   }
   if (a.page_size % kChunk != 0) {
-    *msg = "attn_decode_run: page_size must be a multiple of 16";
+    *msg = "attn: page_size must be a multiple of 16";
     return cudaErrorNotSupported;
   }
   if (a.num_ctas <= 0 || a.num_units == 0) return cudaSuccess;
@@ -730,7 +812,8 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
   cudaError_t e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int grid = a.num_ctas < sms ? a.num_ctas : sms;
-  return bf16 ? launch_dt<true>(prm, grid, stream) : launch_dt<false>(prm, grid, stream);
+  return bf16 ? launch_dt<true>(prm, rows, grid, stream)
+              : launch_dt<false>(prm, rows, grid, stream);
 }
 
 }  // namespace attn

@@ -142,9 +142,13 @@ struct AppendArgs {
 // kernel does not handle.
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char** msg);
 int append_ctas_per_sm();
-// Decode (one query row per request; qo_indptr ignored) on the tensor cores
-// for groups of 2, 4 or 8 query heads per kv head, HND pools with
-// page_size % 16 == 0.
+// Few-row tensor-core kernel: items of at most kFewRowMax packed query rows
+// (decode with qo_indptr == NULL: the group's heads; a short append: its
+// tokens x heads), HND pools with page_size % 16 == 0; merges split items
+// itself. few_row_rows gives the rows per item it runs with (a power of two
+// >= group x max_qo_len), or 0 if the shape needs more than kFewRowMax.
+constexpr int kFewRowMax = 16;
+int few_row_rows(int32_t group, int32_t max_qo_len);
 cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const char** msg);
 
 // Merge of split items' partial states into o / lse (after a run).

@@ -63,6 +63,46 @@ def test_append_small_parity(oracle_mod, case, num_ctas):
     assert_attn_close(o, lse, o_ref, lse_ref, f"append case {case} ctas {num_ctas}")
 
 
+# Short appends (group x longest query count <= 16 packed rows) run on the
+# few-row tensor-core kernel: causal and not, groups 1 to 8, empty kv.
+SHORT_CASES = [
+    # (P, Hq, Hk, dtype, qo_lens, extra kv, causal)
+    (16, 32, 8, torch.bfloat16, [1, 2, 4, 3, 4], [0, 5, 200, 17, 3000], True),
+    (16, 32, 8, torch.bfloat16, [4, 1, 2], [700, 0, 129], False),
+    (16, 16, 8, torch.bfloat16, [8, 5, 1], [100, 1000, 2], True),
+    (16, 8, 8, torch.float16, [16, 9], [300, 2000], True),
+    (128, 16, 2, torch.bfloat16, [2, 1, 2], [5000, 64, 127], False),
+    (32, 16, 2, torch.bfloat16, [2, 2], [-2, 40], False),  # request 0 has no kv
+]
+
+
+@pytest.mark.parametrize("case", range(len(SHORT_CASES)))
+@pytest.mark.parametrize("num_ctas", [1, 5, None])
+def test_short_append_parity(oracle_mod, case, num_ctas):
+    P, Hq, Hk, dtype, qo_lens, extra, causal = SHORT_CASES[case]
+    kv_lens = [q + e for q, e in zip(qo_lens, extra)]
+    pool = sum(-(-L // P) for L in kv_lens) + 9
+    w = synth.append_workload(f"short{case}", qo_lens, kv_lens, P, pool, Hq, Hk, dtype,
+                              seed=800 + case, causal=causal)
+    o_ref, lse_ref = oracle_full(oracle_mod, w)
+    o, lse, _ = run_append(w, num_ctas)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"short append case {case} ctas {num_ctas}")
+
+
+@pytest.mark.parametrize("case", [0, 3, 4])
+def test_short_append_stale_pool_slots_are_never_used(oracle_mod, case):
+    P, Hq, Hk, dtype, qo_lens, extra, causal = SHORT_CASES[case]
+    kv_lens = [q + e for q, e in zip(qo_lens, extra)]
+    pool = sum(-(-L // P) for L in kv_lens) + 9
+    w = synth.append_workload(f"shortnan{case}", qo_lens, kv_lens, P, pool, Hq, Hk, dtype,
+                              seed=850 + case, causal=causal)
+    poison_unused_slots(w.cache)
+    o_ref, lse_ref = oracle_full(oracle_mod, w)
+    for ctas in (1, None):
+        o, lse, _ = run_append(w, ctas)
+        assert_attn_close(o, lse, o_ref, lse_ref, f"short stale slots case {case} ctas {ctas}")
+
+
 @pytest.mark.parametrize("case", [0, 2, 4, 6])
 def test_append_stale_pool_slots_are_never_used(oracle_mod, case):
     P, Hq, Hk, dtype, qo_lens, extra, causal = CASES[case]
