@@ -274,7 +274,8 @@ attn_status_t attn_wait_selftest(void* dev_ws, int32_t limit_us, void* stream);
  *    start at zero. Calls whose work overlaps on the GPU race with each other;
  *    calls ordered on one stream are safe. Host calls are serialised.
  *  - Batches whose plan tables and partial states exceed 4 MiB (roughly more
- *    than 16k (request, kv head) pairs) return ATTN_ERR_WORKSPACE_TOO_SMALL
+ *    than 60k (request, kv head) pairs at group 8, a few more at smaller
+ *    groups) return ATTN_ERR_WORKSPACE_TOO_SMALL
  *    before any GPU work; use attn_plan + attn_decode_run instead.
  * Errors: as attn_plan and attn_decode_run.
  */

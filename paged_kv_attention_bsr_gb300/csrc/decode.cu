@@ -127,15 +127,14 @@ __device__ __forceinline__ Geo unit_geo(const DecodeArgs& a, int ui) {
   const int4* rec = reinterpret_cast<const int4*>(a.ws.units + ui);
   const int4 x = __ldg(rec);
   const int4 y = __ldg(rec + 1);
+  const int4 z = __ldg(rec + 2);
   Geo g;
   g.r = x.x;
   g.hk = x.y;
   g.slot = y.y;
   g.split = y.z;
-  const int32_t pb = __ldg(a.kv_indptr + g.r);
-  const int64_t n = int64_t(__ldg(a.kv_indptr + g.r + 1)) - pb;
-  const int64_t kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
-  g.page_base = pb;
+  const int64_t kv_len = z.x;  // the request's geometry, copied in by the planner
+  g.page_base = y.w;
   g.tok_begin = int64_t(x.w) * a.page_size;  // p0 * P
   const int64_t te = min(int64_t(y.x) * a.page_size, kv_len);
   const int64_t nt = te - g.tok_begin;

@@ -95,22 +95,17 @@ __device__ __forceinline__ DGeo decode_geo(const AppendArgs& a, int ui) {
   const int4* rec = reinterpret_cast<const int4*>(a.ws.units + ui);
   const int4 x = __ldg(rec);
   const int4 y = __ldg(rec + 1);
+  const int4 z = __ldg(rec + 2);
   DGeo g;
   g.r = x.x;
   g.hk = x.y;
   g.t = x.z;
   g.slot = y.y;
   g.split = y.z;
-  if constexpr (!DEC) {
-    g.qo_start = __ldg(a.qo_indptr + g.r);
-    g.qo_len = int64_t(__ldg(a.qo_indptr + g.r + 1)) - g.qo_start;
-  } else {  // decode: one query row per request
-    g.qo_start = g.r;
-    g.qo_len = 1;
-  }
-  g.page_base = __ldg(a.kv_indptr + g.r);
-  const int64_t n = int64_t(__ldg(a.kv_indptr + g.r + 1)) - g.page_base;
-  g.kv_len = n > 0 ? (n - 1) * a.page_size + __ldg(a.last_page_len + g.r) : 0;
+  g.page_base = y.w;  // the request's geometry, copied in by the planner
+  g.kv_len = z.x;
+  g.qo_start = z.y;
+  g.qo_len = DEC ? 1 : z.z;
   int64_t vis = g.kv_len;
   if (!DEC && a.causal) {  // the item's last query row sees the most
     const int64_t last_row = min(int64_t(g.t + 1) * a.q_tile, g.qo_len) - 1;

@@ -16,18 +16,24 @@ constexpr int kTileRows = 128;      // packed query rows of one MMA tile (M = 12
 constexpr int kItemRows = 256;      // packed query rows of one append item (2 tiles)
 constexpr int kMaxDecodeGroup = 8;  // query heads per kv head, decode kernel
 constexpr int kTensorDecodeGroup = 2;  // decode groups >= this use the tensor-core kernel
-constexpr int kUnitInts = 8;        // int32 words per work-unit record
+constexpr int kUnitInts = 12;       // int32 words per work-unit record
 constexpr int64_t kHeaderBytes = 256;
 
-// One work unit of the plan (32 bytes, 16-byte aligned in the workspace).
+// One work unit of the plan (48 bytes = three int4, 16-byte aligned in the
+// workspace). The request's geometry is copied in by the planner so that a
+// kernel learns everything about a unit from three independent loads.
 struct Unit {
-  int32_t r;      // request
-  int32_t hk;     // kv head
-  int32_t t;      // query tile (append) / 0 (decode)
-  int32_t p0;     // first page (index within the request's page list)
-  int32_t p1;     // one past the last page
-  int32_t slot;   // partial-state slot, -1 if the item is not split
-  int32_t split;  // split-item index, -1 if not split
+  int32_t r;          // request
+  int32_t hk;         // kv head
+  int32_t t;          // query tile (append) / 0 (decode)
+  int32_t p0;         // first page (index within the request's page list)
+  int32_t p1;         // one past the last page
+  int32_t slot;       // partial-state slot, -1 if the item is not split
+  int32_t split;      // split-item index, -1 if not split
+  int32_t page_base;  // kv_indptr[r]
+  int32_t kv_len;     // the request's kv tokens
+  int32_t qo_start;   // qo_indptr[r] (append) / r (decode)
+  int32_t qo_len;     // the request's query rows (decode: 1)
   int32_t pad;
 };
 static_assert(sizeof(Unit) == kUnitInts * 4, "unit record size");

@@ -23,6 +23,7 @@
 // Every CTA gets at most ceil(W/C) + 1 of the cost and the cut adds at most
 // C extra units. The result depends only on the inputs and is deterministic.
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <functional>
 #include <queue>
@@ -133,6 +134,10 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
       return ATTN_ERR_INVALID_ARG;
     }
     const int64_t kv_len = n_pages > 0 ? (n_pages - 1) * page_size + last_page_len[r] : 0;
+    if (kv_len > INT32_MAX) {
+      *msg = "attn_plan: a request's kv length must fit in 31 bits";
+      return ATTN_ERR_INVALID_ARG;
+    }
     int64_t qo_len = 1;
     if (!decode) {
       qo_len = int64_t(qo_indptr[r + 1]) - qo_indptr[r];
@@ -208,14 +213,15 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         if (hi <= lo) continue;
         if (it.n == 0) {
           if (lo <= base && base < hi)
-            gen.push_back({{it.r, it.hk, it.t, 0, 0, -1, -1, 0}, int32_t(cc), int32_t(k)});
+            gen.push_back({{it.r, it.hk, it.t, 0, 0, -1, -1, 0, 0, 0, 0, 0}, int32_t(cc),
+                           int32_t(k)});
           continue;
         }
         const int64_t p0 = std::max<int64_t>(0, lo - base - kAlpha);
         const int64_t p1 = std::min<int64_t>(it.n, hi - base - kAlpha);
         if (p1 > p0)
-          gen.push_back({{it.r, it.hk, it.t, int32_t(p0), int32_t(p1), -1, -1, 0}, int32_t(cc),
-                         int32_t(k)});
+          gen.push_back({{it.r, it.hk, it.t, int32_t(p0), int32_t(p1), -1, -1, 0, 0, 0, 0, 0},
+                         int32_t(cc), int32_t(k)});
       }
       base += w;
     }
@@ -242,7 +248,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int64_t avail = cap - top.first;
         const int64_t need = kAlpha + (it.n - p);
         if (need <= avail) {
-          gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(it.n), -1, -1, 0}, c,
+          gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(it.n), -1, -1, 0, 0, 0, 0, 0}, c,
                          int32_t(k)});
           load[size_t(c)] = top.first + need;
           if (load[size_t(c)] < cap) ready.push(Slot(load[size_t(c)], c));
@@ -251,8 +257,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int64_t take = avail - kAlpha;
         load[size_t(c)] = cap;  // this CTA is full either way
         if (take <= 0) continue;
-        gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(p + take), -1, -1, 0}, c,
-                       int32_t(k)});
+        gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(p + take), -1, -1, 0, 0, 0, 0, 0},
+                       c, int32_t(k)});
         p += take;
       }
     }
@@ -298,6 +304,14 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
     thread_local std::vector<int32_t> at;
     at.assign(work_indptr.begin(), work_indptr.end() - 1);
     for (const U& g : gen) units[size_t(at[size_t(g.cta)]++)] = g.u;
+  }
+  for (Unit& u : units) {  // the request's geometry, for the kernels
+    const int32_t r = u.r;
+    const int64_t n_pages = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
+    u.page_base = kv_indptr[r];
+    u.kv_len = n_pages > 0 ? int32_t((n_pages - 1) * page_size + last_page_len[r]) : 0;
+    u.qo_start = decode ? r : qo_indptr[r];
+    u.qo_len = decode ? 1 : qo_indptr[r + 1] - qo_indptr[r];
   }
   int64_t max_load = 0;
   for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, load[size_t(i)]);

@@ -14,7 +14,7 @@ def _tables(p, buf):
     def at(off, n):
         return raw[off // 4: off // 4 + n]
 
-    units = at(p.off_units, 8 * p.num_units).reshape(-1, 8)
+    units = at(p.off_units, 12 * p.num_units).reshape(-1, 12)
     return {
         "work_indptr": at(p.off_work_indptr, p.num_ctas + 1).tolist(),
         "units": units,
@@ -78,6 +78,15 @@ def test_plan_bit_exact_vs_reference(decode):
         assert p.total_weight == ref.total_weight
         assert p.num_items == ref.num_items
         assert p.q_tile == ref.q_tile
+        # the request geometry the planner copies into every unit record
+        for row in u:
+            r = int(row[0])
+            assert row[7] == kv_indptr[r]
+            assert row[8] == plan_ref.kv_length(kv_indptr.tolist(), last.tolist(), P, r)
+            if qo is None:
+                assert (row[9], row[10]) == (r, 1)
+            else:
+                assert (row[9], row[10]) == (qo[r], qo[r + 1] - qo[r])
 
 
 def _pages_of_items(kv_indptr, last, P, Hk, g, qo, causal):
