@@ -27,12 +27,16 @@
 // and are never read back. A causal short append masks each row at its own
 // end-aligned limit (token i of qo_len sees kv positions <= kv_len - qo_len + i).
 //
-// Warps (128 threads, one CTA per SM): 0 softmax + epilogue; 1 TMA producer
-// of the K/V ring (six 32 KB slots, 16-row boxes gathered by page index);
-// 2 TMEM allocation and the MMAs (one thread: S of tile k+1 runs under the
-// softmax of tile k, S double-buffered in TMEM); 3 query loader (plain
-// loads of the next unit's R query rows into registers, stored into the
-// swizzled query tile as soon as the last S of the current unit is done).
+// Warps (160 threads, one CTA per SM): 0 softmax; 1 TMA producer of the K/V
+// ring (six 32 KB slots, 16-row boxes gathered by page index); 2 TMEM
+// allocation and the MMAs (one thread: S of tile k+1 runs under the softmax
+// of tile k, S double-buffered in TMEM); 3 query loader (plain loads of the
+// next unit's R query rows into registers, stored into the swizzled query
+// tile as soon as the last S of the current unit is done); 4 epilogue. O is
+// double-buffered in TMEM (unit u accumulates into O[u & 1]), so while the
+// epilogue warp reads one unit's O, sums the copies, writes the output and
+// merges split items, the softmax warp is already on the next unit's tiles;
+// the softmax hands over each row's max and sum through shared memory.
 // Every wait is bounded; TMEM is freed on every path.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -51,28 +55,36 @@ constexpr int kTile = kTcTile;
 constexpr int kChunk = kTcChunk;
 constexpr int kHalf = kTcHalf;
 constexpr int kTileBytes = kTcTileBytes;
-constexpr int kThreads = 128;
+constexpr int kThreads = 160;
 constexpr int kWarpSoftmax = 0;
 constexpr int kWarpLoad = 1;
 constexpr int kWarpMma = 2;
 constexpr int kWarpQ = 3;
+constexpr int kWarpEpi = 4;  // TMEM lanes 0-31, like the softmax warp
 constexpr int kSlots = 6;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kTileBytes;
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
-constexpr int kSmem = kOffBar + 256 + 1024;  // + barriers + alignment slack
-constexpr uint32_t kTmemCols = 512;          // S buffers at 0 and 128, O at 256
+constexpr int kOffHand = kOffBar + 256;         // softmax -> epilogue row state
+constexpr int kSmem = kOffHand + 512 + 1024;    // + alignment slack
+constexpr uint32_t kTmemCols = 512;  // S buffers at 0 and 128, O buffers at 256 and 384
 constexpr uint32_t kColO = 256;
 
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[2], p_full[2], o_done[2];
-  uint64_t o_free;
+  uint64_t o_free[2];   // epilogue read O[b] (count 32)
+  uint64_t ounit[2];    // a unit's last P.V into O[b] is done (commit)
+  uint64_t ep_full[2];  // softmax wrote the row state of a unit with O[b] (count 32)
   uint64_t drain;
   uint32_t tmem_base;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
+struct Hand {
+  float m[2][32];  // per O buffer and TMEM lane: running max (log2 units)
+  float l[2][32];  // and the copy's partial sum
+};
 
 struct DecodeTcParams {
   CUtensorMap tm_k;
@@ -255,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_base);
   Bars& bars = *reinterpret_cast<Bars*>(gbase + kOffBar);
+  Hand& hand = *reinterpret_cast<Hand*>(gbase + kOffHand);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int32_t* err = a.ws.error;
@@ -271,7 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.p_full[i]), 32);
       mbar_init(smem_u32(&bars.o_done[i]), 1);
     }
-    mbar_init(smem_u32(&bars.o_free), 32);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars.o_free[i]), 32);
+      mbar_init(smem_u32(&bars.ounit[i]), 1);
+      mbar_init(smem_u32(&bars.ep_full[i]), 32);
+    }
     mbar_init(smem_u32(&bars.drain), 1);
     fence_mbar_init();
   }
@@ -446,14 +463,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](uint32_t k, int nk, bool first) -> bool {
         if (!mbar_wait(smem_u32(&bars.p_full[k & 1u]), (k >> 1) & 1u, err, ERR_WAIT_SOFTMAX))
           return false;
-        if (first && !mbar_wait(smem_u32(&bars.o_free), (n_u & 1u) ^ 1u, err, ERR_WAIT_SOFTMAX))
+        // O[n_u & 1] is free once the epilogue read it for unit n_u - 2
+        if (first && !mbar_wait(smem_u32(&bars.o_free[n_u & 1u]), ((n_u >> 1) & 1u) ^ 1u, err,
+                                ERR_WAIT_SOFTMAX))
           return false;
         tc_fence_after();
         const uint32_t vbase = base + kOffRing + slot_of(2 * k + 1) * kTileBytes;
         for (int kk = 0; kk < nk; ++kk) {
           const uint64_t bd = smem_desc(vbase + kk * kChunk * 128, kHalf, 1024);
-          mma_f16_ts(tmem + kColO, tmem + (k & 1u) * 128u + kk * 8, bd, prm.idesc_pv,
-                     (first && kk == 0) ? 0u : 1u);
+          mma_f16_ts(tmem + kColO + 128u * (n_u & 1u), tmem + (k & 1u) * 128u + kk * 8, bd,
+                     prm.idesc_pv, (first && kk == 0) ? 0u : 1u);
         }
         mma_commit(smem_u32(&bars.o_done[k & 1u]));
         mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * k + 1)]));
@@ -501,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
+          mma_commit(smem_u32(&bars.ounit[n_u & 1u]));  // the unit's O is complete
           ++n_u;
           jt += n;
           ++ua;
@@ -519,13 +539,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rho = lane % R;
     const int c = lane / R;
     const float c2 = prm.scale_log2;
-    uint32_t n_t = 0;
+    uint32_t n_t = 0, n_u = 0;  // tiles and units with tiles so far
     bool ok = true;
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
       for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
            ++ui) {
         const DGeo g = decode_geo<DEC>(a, ui);
         const QRow qr = qrow<DEC, R>(a, g, rho);
+        const uint32_t ob = n_u & 1u;  // this unit's O buffer
+        const uint32_t col_o = kColO + 128u * ob;
         const int64_t orow = qr.orow;
         const int64_t prow = int64_t(g.slot) * a.rows_per_item + rho;  // split items
         if (g.ntiles == 0) {  // no kv: o = 0, lse = -inf
@@ -607,11 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int b = 0; b < 4; ++b) {
               float o[32];
-              tmem_ld32(tmem + kColO + b * 32, o);
+              tmem_ld32(tmem + col_o + b * 32, o);
               const float f = rescale_o ? alpha : 1.f;
 #pragma unroll
               for (int q = 0; q < 32; ++q) o[q] *= f;
-              tmem_st32(tmem + kColO + b * 32, o);
+              tmem_st32(tmem + col_o + b * 32, o);
             }
           }
           // probabilities of this thread's W columns, packed to 16-bit
@@ -667,14 +689,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(smem_u32(&bars.p_full[n_t & 1u]));
         }
         if (!ok) break;
-        // ---- epilogue: sum the copies, O / l
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[(n_t - 1) & 1u]),
-                                               ((n_t - 1) >> 1) & 1u, err, ERR_WAIT_MMA))) {
+        // ---- hand the row state to the epilogue warp; the slot of O[ob]
+        // is free once the epilogue has finished unit n_u - 2
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_free[ob]),
+                                               ((n_u >> 1) & 1u) ^ 1u, err, ERR_WAIT_MMA))) {
+          ok = false;
+          break;
+        }
+        hand.m[ob][lane] = m_ref;
+        hand.l[ob][lane] = l;
+        mbar_arrive(smem_u32(&bars.ep_full[ob]));
+        ++n_u;
+      }
+  } else if (warp == kWarpEpi) {
+    // ------------------------------------------------------------ epilogue
+    // Per unit with kv tiles, in order: once the softmax handed over the row
+    // state and the unit's last P.V is done, sum the copies of every row out
+    // of O[u & 1], write o / lse (or the split item's partial state), free
+    // the buffer, and merge the item if this unit arrives last.
+    const int rho = lane % R;
+    const int c = lane / R;
+    uint32_t n_u = 0;
+    bool ok = true;
+    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+      for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+           ++ui) {
+        const DGeo g = decode_geo<DEC>(a, ui);
+        if (g.ntiles == 0) continue;  // written by the softmax warp
+        const QRow qr = qrow<DEC, R>(a, g, rho);
+        const int64_t orow = qr.orow;
+        const int64_t prow = int64_t(g.slot) * a.rows_per_item + rho;  // split items
+        const uint32_t ob = n_u & 1u;
+        const uint32_t col_o = kColO + 128u * ob;
+        const uint32_t ph = (n_u >> 1) & 1u;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bars.ep_full[ob]), ph, err, ERR_WAIT_SOFTMAX) &&
+                            mbar_wait(smem_u32(&bars.ounit[ob]), ph, err, ERR_WAIT_MMA))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float lt = l;
+        const float m_ref = hand.m[ob][lane];
+        float lt = hand.l[ob][lane];
 #pragma unroll
         for (int st = 0; st < LC; ++st) lt += __shfl_xor_sync(0xffffffffu, lt, R << st);
         const bool any = lt > 0.f;
@@ -689,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
           float o[32];
-          tmem_ld32(tmem + kColO + b * 32, o);
+          tmem_ld32(tmem + col_o + b * 32, o);
           // transposing butterfly over the copies: each step halves the
           // values a thread keeps and adds the partner's matching half
           int n = 32;
@@ -722,7 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.o_free));
+        mbar_arrive(smem_u32(&bars.o_free[ob]));
+        ++n_u;
         if (g.slot >= 0 && !merge_split_impl<BF16, R, DEC>(a, g)) {
           ok = false;
           break;
