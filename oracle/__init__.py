@@ -6,7 +6,8 @@ legs of ``bench.py`` may import this package. The library path
 
 Contents:
   * ``attn_oracle.c``  -- plain single-threaded C, double precision: BSR gather,
-    softmax attention with optional end-aligned causal mask, LSE merge.
+    softmax attention with optional end-aligned causal mask and optional
+    rotary position embedding of q and k, LSE merge.
   * ``plan_ref.py``    -- restatement of the work partition spec (plan()).
   * this module        -- builds ``liboracle.so`` with gcc and wraps it with
     ctypes over numpy arrays.
@@ -65,6 +66,12 @@ def _load():
             lib.oracle_batch_attention.argtypes = [
                 vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32, i32, i32,
                 i32, i32, dbl, vp, vp, vp, vp]
+            lib.oracle_batch_attention_rope.restype = i32
+            lib.oracle_batch_attention_rope.argtypes = [
+                vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                i32, i32, dbl, vp, vp, i64, vp, vp]
+            lib.oracle_round.restype = dbl
+            lib.oracle_round.argtypes = [dbl, i32]
             lib.oracle_merge_states.restype = None
             lib.oracle_merge_states.argtypes = [vp, vp, i32, i64, i32, vp, vp]
             _lib = lib
@@ -119,6 +126,38 @@ def batch_attention(q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
     if rc != 0:
         raise ValueError(f"oracle_batch_attention rejected its arguments (code {rc})")
     return o, lse
+
+
+def batch_attention_rope(q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
+                         page_size, num_qo_heads, num_kv_heads, head_dim, dtype,
+                         sm_scale, rope_cos, rope_sin, causal=False, qo_indptr=None,
+                         layout=HND):
+    """All rows with rotary position embedding (tables float32 [max_pos, D/2])."""
+    lib = _load()
+    q16, k16, v16 = _u16(q), _u16(k_pool), _u16(v_pool)
+    kv_indptr, kv_indices = _i32(kv_indptr), _i32(kv_indices)
+    last_page_len, qo_indptr = _i32(last_page_len), _i32(qo_indptr)
+    cos = np.ascontiguousarray(rope_cos, np.float32)
+    sin = np.ascontiguousarray(rope_sin, np.float32)
+    assert cos.shape == sin.shape and cos.shape[1] == head_dim // 2
+    batch = len(kv_indptr) - 1
+    total_qo = int(qo_indptr[-1]) if qo_indptr is not None else batch
+    num_pages = k16.size // (page_size * num_kv_heads * head_dim)
+    o = np.zeros((total_qo, num_qo_heads, head_dim), np.float64)
+    lse = np.zeros((total_qo, num_qo_heads), np.float64)
+    rc = lib.oracle_batch_attention_rope(
+        _ptr(q16), _ptr(qo_indptr), _ptr(k16), _ptr(v16), num_pages, layout,
+        _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len), batch, page_size,
+        num_qo_heads, num_kv_heads, head_dim, dtype, int(bool(causal)),
+        float(sm_scale), _ptr(cos), _ptr(sin), cos.shape[0], _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_batch_attention_rope rejected its arguments (code {rc})")
+    return o, lse
+
+
+def round_to(v: float, dtype: int) -> float:
+    """A double rounded to the 16-bit storage type (ties to even)."""
+    return _load().oracle_round(float(v), dtype)
 
 
 def attention_row(q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,

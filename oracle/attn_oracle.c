@@ -46,6 +46,33 @@ double oracle_widen(uint16_t bits, int32_t dtype) {
   return sign ? -v : v;
 }
 
+double oracle_round(double v, int32_t dtype) {
+  if (v == 0.0 || isnan(v) || isinf(v)) return v;
+  /* significand bits (with the implicit one) and the smallest normal exponent */
+  const int bits = dtype == ORACLE_BF16 ? 8 : 11;
+  const int emin = dtype == ORACLE_BF16 ? -126 : -14;
+  const double vmax = dtype == ORACLE_BF16 ? 0x1.fep127 : 65504.0;
+  int e;
+  frexp(v, &e); /* v = m 2^e, 0.5 <= |m| < 1: the leading bit has weight 2^(e-1) */
+  int q = e - bits;            /* weight of the last kept bit */
+  if (q < emin - bits + 1) q = emin - bits + 1; /* subnormals: fixed quantum */
+  double r = ldexp(nearbyint(ldexp(v, -q)), q); /* default mode: ties to even */
+  if (fabs(r) > vmax) return v > 0 ? INFINITY : -INFINITY;
+  return r;
+}
+
+/* Rotary embedding of one D-vector at table row `pos` (see the header). */
+static void rope_rotate(double* x, int32_t head_dim, const float* rope_cos,
+                        const float* rope_sin, int64_t pos, int32_t dtype) {
+  const int32_t half = head_dim / 2;
+  for (int32_t d = 0; d < half; ++d) {
+    const double c = rope_cos[pos * half + d], s = rope_sin[pos * half + d];
+    const double a = x[d], b = x[d + half];
+    x[d] = oracle_round(a * c - b * s, dtype);
+    x[d + half] = oracle_round(b * c + a * s, dtype);
+  }
+}
+
 /* Number of logical KV tokens of request r (BSR reading, see header). */
 static int64_t bsr_kv_len(const int32_t* kv_indptr, const int32_t* last_page_len,
                           int32_t page_size, int32_t r) {
@@ -108,7 +135,8 @@ static void attention_row(const uint16_t* q, const int32_t* qo_indptr,
                           int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
                           int32_t causal, double sm_scale, int32_t r, int32_t i,
                           int32_t h, int64_t kv_lo, int64_t kv_hi, double* x_buf,
-                          double* q_buf, double* o, double* lse) {
+                          double* q_buf, const float* rope_cos, const float* rope_sin,
+                          double* o, double* lse) {
   const int32_t group = num_qo_heads / num_kv_heads;
   const int32_t hk = h / group;
   const int64_t qo_start = qo_indptr ? qo_indptr[r] : r;
@@ -127,19 +155,27 @@ static void attention_row(const uint16_t* q, const int32_t* qo_indptr,
 
   const uint16_t* qrow = q + ((qo_start + i) * num_qo_heads + h) * head_dim;
   for (int32_t d = 0; d < head_dim; ++d) q_buf[d] = oracle_widen(qrow[d], dtype);
+  double* k_buf = q_buf + head_dim; /* rotated key (RoPE only) */
 
   for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
   if (hi <= lo) {
     *lse = -INFINITY;
     return;
   }
+  if (rope_cos) rope_rotate(q_buf, head_dim, rope_cos, rope_sin, kv_len - qo_len + i, dtype);
 
   double m = -INFINITY;
   for (int64_t j = lo; j < hi; ++j) {
     const uint16_t* krow = bsr_token_ptr(k_pool, layout, kv_indptr, kv_indices,
                                          page_size, num_kv_heads, head_dim, r, j, hk);
     double dot = 0.0;
-    for (int32_t d = 0; d < head_dim; ++d) dot += q_buf[d] * oracle_widen(krow[d], dtype);
+    if (rope_cos) {
+      for (int32_t d = 0; d < head_dim; ++d) k_buf[d] = oracle_widen(krow[d], dtype);
+      rope_rotate(k_buf, head_dim, rope_cos, rope_sin, j, dtype);
+      for (int32_t d = 0; d < head_dim; ++d) dot += q_buf[d] * k_buf[d];
+    } else {
+      for (int32_t d = 0; d < head_dim; ++d) dot += q_buf[d] * oracle_widen(krow[d], dtype);
+    }
     double x = sm_scale * dot;
     x_buf[j - lo] = x;
     if (x > m) m = x;
@@ -185,7 +221,7 @@ int32_t oracle_attention_row(const uint16_t* q, const int32_t* qo_indptr,
   if (i >= qo_len) return -1;
   int64_t kv_len = bsr_kv_len(kv_indptr, last_page_len, page_size, r);
   double* x_buf = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
-  double* q_buf = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  double* q_buf = (double*)malloc(sizeof(double) * 2 * (size_t)head_dim);
   if (!x_buf || !q_buf) {
     free(x_buf);
     free(q_buf);
@@ -193,13 +229,14 @@ int32_t oracle_attention_row(const uint16_t* q, const int32_t* qo_indptr,
   }
   attention_row(q, qo_indptr, k_pool, v_pool, layout, kv_indptr, kv_indices,
                 last_page_len, page_size, num_qo_heads, num_kv_heads, head_dim,
-                dtype, causal, sm_scale, r, i, h, 0, INT64_MAX, x_buf, q_buf, o, lse);
+                dtype, causal, sm_scale, r, i, h, 0, INT64_MAX, x_buf, q_buf, NULL, NULL,
+                o, lse);
   free(x_buf);
   free(q_buf);
   return 0;
 }
 
-int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
+static int32_t batch_attention(const uint16_t* q, const int32_t* qo_indptr,
                                const uint16_t* k_pool, const uint16_t* v_pool,
                                int64_t num_pages, int32_t layout,
                                const int32_t* kv_indptr, const int32_t* kv_indices,
@@ -208,6 +245,7 @@ int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
                                int32_t num_kv_heads, int32_t head_dim,
                                int32_t dtype, int32_t causal, double sm_scale,
                                const int32_t* kv_begin, const int32_t* kv_end,
+                               const float* rope_cos, const float* rope_sin,
                                double* o, double* lse) {
   int32_t rc = check_args(qo_indptr, num_pages, layout, kv_indptr, kv_indices,
                           last_page_len, batch, page_size, num_qo_heads,
@@ -215,7 +253,7 @@ int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
   if (rc) return rc;
   int64_t mx = max_kv_len(kv_indptr, last_page_len, page_size, batch);
   double* x_buf = (double*)malloc(sizeof(double) * (size_t)mx);
-  double* q_buf = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  double* q_buf = (double*)malloc(sizeof(double) * 2 * (size_t)head_dim);
   if (!x_buf || !q_buf) {
     free(x_buf);
     free(q_buf);
@@ -232,13 +270,55 @@ int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
         attention_row(q, qo_indptr, k_pool, v_pool, layout, kv_indptr, kv_indices,
                       last_page_len, page_size, num_qo_heads, num_kv_heads,
                       head_dim, dtype, causal, sm_scale, r, (int32_t)i, h, lo, hi,
-                      x_buf, q_buf, o + row * head_dim, lse + row);
+                      x_buf, q_buf, rope_cos, rope_sin, o + row * head_dim, lse + row);
       }
     }
   }
   free(x_buf);
   free(q_buf);
   return 0;
+}
+
+int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
+                               const uint16_t* k_pool, const uint16_t* v_pool,
+                               int64_t num_pages, int32_t layout,
+                               const int32_t* kv_indptr, const int32_t* kv_indices,
+                               const int32_t* last_page_len, int32_t batch,
+                               int32_t page_size, int32_t num_qo_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t dtype, int32_t causal, double sm_scale,
+                               const int32_t* kv_begin, const int32_t* kv_end,
+                               double* o, double* lse) {
+  return batch_attention(q, qo_indptr, k_pool, v_pool, num_pages, layout, kv_indptr,
+                         kv_indices, last_page_len, batch, page_size, num_qo_heads,
+                         num_kv_heads, head_dim, dtype, causal, sm_scale, kv_begin,
+                         kv_end, NULL, NULL, o, lse);
+}
+
+int32_t oracle_batch_attention_rope(const uint16_t* q, const int32_t* qo_indptr,
+                                    const uint16_t* k_pool, const uint16_t* v_pool,
+                                    int64_t num_pages, int32_t layout,
+                                    const int32_t* kv_indptr, const int32_t* kv_indices,
+                                    const int32_t* last_page_len, int32_t batch,
+                                    int32_t page_size, int32_t num_qo_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t dtype, int32_t causal, double sm_scale,
+                                    const float* rope_cos, const float* rope_sin,
+                                    int64_t rope_max_pos, double* o, double* lse) {
+  if (!rope_cos || !rope_sin || head_dim % 2 != 0) return -1;
+  /* every key position (< kv_len) and query position (kv_len - qo_len + i
+     <= kv_len - 1) must have a table row */
+  int64_t mx = max_kv_len(kv_indptr, last_page_len, page_size, batch);
+  if (batch > 0 && mx > rope_max_pos) return -9;
+  for (int32_t r = 0; r < batch; ++r) {
+    int64_t kv_len = bsr_kv_len(kv_indptr, last_page_len, page_size, r);
+    int64_t qo_len = qo_indptr ? (int64_t)qo_indptr[r + 1] - qo_indptr[r] : 1;
+    if (kv_len > 0 && kv_len < qo_len) return -9; /* query positions must be >= 0 */
+  }
+  return batch_attention(q, qo_indptr, k_pool, v_pool, num_pages, layout, kv_indptr,
+                         kv_indices, last_page_len, batch, page_size, num_qo_heads,
+                         num_kv_heads, head_dim, dtype, causal, sm_scale, NULL, NULL,
+                         rope_cos, rope_sin, o, lse);
 }
 
 void oracle_merge_states(const double* o_in, const double* lse_in,

@@ -82,6 +82,37 @@ int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
                                double* o, double* lse);
 
 /*
+ * oracle_batch_attention with rotary position embedding applied to the
+ * queries and keys first ("RoPE: LLaMA-style rotary position embedding",
+ * feature list of the gittoolsai.com README copy; fused into the attention
+ * kernel as a query / key transform, apply_rope(q, k, cos, sin, pos), in
+ * "可定制的注意力模板" of the modb.pro digest). Readings:
+ *  - LLaMA style = "rotate half": dims d and d + D/2 form a pair,
+ *      x'_d       = x_d c - x_{d+D/2} s,   x'_{d+D/2} = x_{d+D/2} c + x_d s,
+ *    with c = rope_cos[pos * (D/2) + d], s = rope_sin[pos * (D/2) + d];
+ *  - key j of a request sits at position j; query row i of a request with
+ *    qo_len rows at position kv_len - qo_len + i (decode: kv_len - 1);
+ *  - the rotated q and k are rounded to the storage dtype (round to nearest,
+ *    ties to even), as a kernel producing rotated 16-bit tensors would.
+ *   rope_cos/rope_sin: float[rope_max_pos, D/2]; every position used must be
+ *   < rope_max_pos (else -9 is returned). D must be even.
+ */
+int32_t oracle_batch_attention_rope(const uint16_t* q, const int32_t* qo_indptr,
+                                    const uint16_t* k_pool, const uint16_t* v_pool,
+                                    int64_t num_pages, int32_t layout,
+                                    const int32_t* kv_indptr, const int32_t* kv_indices,
+                                    const int32_t* last_page_len, int32_t batch,
+                                    int32_t page_size, int32_t num_qo_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t dtype, int32_t causal, double sm_scale,
+                                    const float* rope_cos, const float* rope_sin,
+                                    int64_t rope_max_pos, double* o, double* lse);
+
+/* Round a double to the nearest value of the 16-bit storage type (ties to
+ * even; overflow to +-inf). */
+double oracle_round(double v, int32_t dtype);
+
+/*
  * Log-sum-exp merge of n_states attention states per row:
  *   o_in  : double[n_states, rows, D], lse_in: double[n_states, rows]
  *   o_out : double[rows, D],           lse_out: double[rows]

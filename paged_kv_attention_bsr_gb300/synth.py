@@ -128,6 +128,31 @@ def append_workload(name, qo_lens, kv_lens, page_size, pool_pages, num_qo_heads,
                     q, cache, qo_indptr=qo_indptr, causal=causal)
 
 
+def rope_tables(max_pos: int, head_dim: int = HEAD_DIM, theta: float = 500000.0,
+                llama31: bool = True, factor: float = 8.0, low_freq_factor: float = 1.0,
+                high_freq_factor: float = 4.0, original_max_pos: int = 8192):
+    """cos / sin tables float32 [max_pos, head_dim / 2] of LLaMA-style rotary
+    position embedding (the pages' feature list: "LLaMA-style rotary position
+    embedding, including LLaMA 3.1"). Pair i turns by pos * f_i with
+    f_i = theta^(-2 i / head_dim); with llama31, the LLaMA 3.1 frequency
+    rescaling for long contexts: wavelengths 2 pi / f_i shorter than
+    original_max_pos / high_freq_factor keep f_i, those longer than
+    original_max_pos / low_freq_factor use f_i / factor, and the band between
+    blends the two linearly in original_max_pos / wavelength. Angles and
+    their cosines / sines are evaluated in float64, then rounded once."""
+    half = head_dim // 2
+    f = theta ** (-2.0 * np.arange(half, dtype=np.float64) / head_dim)
+    if llama31:
+        wavelen = 2.0 * math.pi / f
+        lo_wl = original_max_pos / low_freq_factor
+        hi_wl = original_max_pos / high_freq_factor
+        smooth = (original_max_pos / wavelen - low_freq_factor) / (high_freq_factor - low_freq_factor)
+        blended = (1.0 - smooth) * f / factor + smooth * f
+        f = np.where(wavelen < hi_wl, f, np.where(wavelen > lo_wl, f / factor, blended))
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * f[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
 # --------------------------------------------------------------------------
 # The five benchmark workloads (seed = 20260000 + workload number).
 # --------------------------------------------------------------------------
