@@ -98,6 +98,7 @@ typedef struct attn_plan {
   int64_t table_bytes;      /* bytes [0, table_bytes) copied host -> device    */
   int64_t dev_bytes_needed; /* device workspace bytes this plan uses           */
   uint64_t fingerprint;     /* hash of the host inputs of the plan             */
+  int64_t max_kv_len;       /* longest kv length of a request                  */
 } attn_plan_t;
 
 /*
@@ -187,6 +188,40 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q,
                               const int32_t* last_page_len, int32_t dtype,
                               float sm_scale, void* o, float* lse, void* dev_ws,
                               size_t dev_bytes, void* stream);
+
+/*
+ * attn_decode_run with rotary position embedding fused in: the kernel turns
+ * q and each key as it streams the pages, so the cache keeps keys without
+ * RoPE and no separate RoPE pass reads or writes them. The pages count
+ * LLaMA-style RoPE, the LLaMA 3.1 variant included, among the supported
+ * features (README copy on gittoolsai.com, feature list) and use it as their
+ * example of a per-query / per-key transform that the attention template
+ * applies inside the kernel (modb.pro digest, "可定制的注意力模板").
+ * Readings: dims d and d + 64 form a pair ("rotate half"),
+ *   x'_d = x_d cos - x_{d+64} sin,   x'_{d+64} = x_{d+64} cos + x_d sin,
+ * with cos / sin = rope_cos / rope_sin[pos * 64 + d]; key j of a request sits
+ * at position j and the query at position kv_len - 1; the turned q and k are
+ * rounded to `dtype` before the products.
+ *   rope_cos, rope_sin : device float[rope_max_pos, 64], row-major and
+ *                        contiguous, 16-byte aligned (caller-built tables,
+ *                        e.g. LLaMA 3.1 frequencies); rope_max_pos must be at
+ *                        least the plan's max_kv_len; read only
+ *   other arguments    : as attn_decode_run
+ * Supported: the shapes attn_decode_run runs on the tensor-core kernel (HND,
+ * page_size % 16 == 0, 2, 4 or 8 query heads per kv head); others return
+ * UNSUPPORTED.
+ * Errors: as attn_decode_run; INVALID_ARG for missing, misaligned or too
+ * short tables.
+ */
+attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q,
+                                   const void* k_pool, const void* v_pool,
+                                   int64_t num_pages, int32_t layout,
+                                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* last_page_len, int32_t dtype,
+                                   float sm_scale, const float* rope_cos,
+                                   const float* rope_sin, int64_t rope_max_pos,
+                                   void* o, float* lse, void* dev_ws, size_t dev_bytes,
+                                   void* stream);
 
 /*
  * Append / prefill attention: many query rows per request (ragged, offsets

@@ -14,7 +14,7 @@
  * yeyulingfeng.com page, section "FlashAttention 的遗产". The tiling there is
  * an IO optimisation only; the oracle computes the untiled definition.
  *
- * Readings taken where the pages are silent (each is restated in the design doc):
+ * Readings taken where the pages are silent:
  *  - the BSR index formula is missing from the digest: logical token t of
  *    request r lives in page kv_indices[kv_indptr[r] + t / P], slot t % P;
  *    kv_len_r = (n_r - 1) * P + last_page_len[r] with n_r pages (0 if n_r = 0);
@@ -83,10 +83,11 @@ int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
 
 /*
  * oracle_batch_attention with rotary position embedding applied to the
- * queries and keys first ("RoPE: LLaMA-style rotary position embedding",
- * feature list of the gittoolsai.com README copy; fused into the attention
- * kernel as a query / key transform, apply_rope(q, k, cos, sin, pos), in
- * "可定制的注意力模板" of the modb.pro digest). Readings:
+ * queries and keys first. The pages count LLaMA-style RoPE among the
+ * supported features (gittoolsai.com README copy, feature list) and give it
+ * as the example of a query / key transform that the attention template
+ * applies inside the kernel (modb.pro digest, "可定制的注意力模板"). The
+ * pages leave the pairing, positions and precision open; the readings taken:
  *  - LLaMA style = "rotate half": dims d and d + D/2 form a pair,
  *      x'_d       = x_d c - x_{d+D/2} s,   x'_{d+D/2} = x_{d+D/2} c + x_d s,
  *    with c = rope_cos[pos * (D/2) + d], s = rope_sin[pos * (D/2) + d];

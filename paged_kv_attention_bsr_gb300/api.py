@@ -69,7 +69,9 @@ class PagedAttention:
 
     def run(self, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale=None,
             out=None, lse=None, qo_indptr=None, layout: int = C.LAYOUT_HND, num_pages=None,
-            return_lse: bool = False, stream=None):
+            return_lse: bool = False, stream=None, rope=None):
+        """rope: optional (cos, sin) device float32 tables [max_pos, head_dim / 2]
+        (decode only): rotary position embedding fused into the kernel."""
         if self.plan_info is None:
             raise RuntimeError("run() before plan()")
         if sm_scale is None:
@@ -78,7 +80,13 @@ class PagedAttention:
             out = torch.empty_like(q)
         if lse is None and return_lse:
             lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-        if self.mode == "decode":
+        if self.mode == "decode" and rope is not None:
+            C.decode_run_rope(self.plan_info, q, k_pool, v_pool, kv_indptr, kv_indices,
+                              last_page_len, sm_scale, rope[0], rope[1], out, lse,
+                              self.dev_ws, layout, num_pages, stream)
+        elif rope is not None:
+            raise ValueError("fused RoPE is implemented for decode runs")
+        elif self.mode == "decode":
             C.decode_run(self.plan_info, q, k_pool, v_pool, kv_indptr, kv_indices,
                          last_page_len, sm_scale, out, lse, self.dev_ws, layout, num_pages,
                          stream)

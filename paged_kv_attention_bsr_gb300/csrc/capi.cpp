@@ -73,6 +73,57 @@ namespace attn {
 void set_last_error(const std::string& msg) { g_err = msg; }
 }  // namespace attn
 
+namespace {
+
+// Arguments of the few-row tensor-core kernel for a decode plan.
+attn::AppendArgs decode_tc_args(const attn_plan_t* plan, const void* q, const void* k_pool,
+                                const void* v_pool, int64_t num_pages,
+                                const int32_t* kv_indptr, const int32_t* kv_indices,
+                                const int32_t* last_page_len, int32_t dtype, float sm_scale,
+                                void* o, float* lse, void* dev_ws) {
+  const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
+  attn::AppendArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.qo_indptr = nullptr;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.num_pages = num_pages;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.last_page_len = last_page_len;
+  a.o = o;
+  a.lse = lse;
+  a.ws = attn::ws_view(*plan, dev_ws);
+  a.num_ctas = plan->num_ctas;
+  a.num_units = plan->num_units;
+  a.num_split_items = plan->num_split_items;
+  a.dtype = dtype;
+  a.page_size = plan->page_size;
+  a.num_qo_heads = plan->num_qo_heads;
+  a.num_kv_heads = plan->num_kv_heads;
+  a.group = group;
+  a.q_tile = 1;
+  a.tile_tokens = 1;
+  a.rows_per_item = group;
+  a.total_qo = plan->batch;
+  a.max_qo_len = 1;
+  a.causal = 0;
+  a.sm_scale = sm_scale;
+  a.rope_cos = nullptr;
+  a.rope_sin = nullptr;
+  return a;
+}
+
+// The few-row tensor-core kernel takes this decode shape.
+bool decode_tc_shape(const attn_plan_t* plan, int32_t layout) {
+  const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
+  return group >= attn::kTensorDecodeGroup && (group & (group - 1)) == 0 &&
+         layout == ATTN_LAYOUT_HND && plan->page_size % 16 == 0;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* attn_last_error(void) { return g_err.c_str(); }
@@ -169,38 +220,13 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
     return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_run: group > 8 is not implemented");
   if (plan->batch == 0) return ATTN_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (group >= kTensorDecodeGroup && (group & (group - 1)) == 0 && layout == ATTN_LAYOUT_HND &&
-      plan->page_size % 16 == 0) {
+  if (decode_tc_shape(plan, layout)) {
     // Tensor-core decode: Q K^T and P V run as M = 128 MMAs over 128-token
     // tiles gathered by TMA, the softmax on one warp (query heads replicated
     // across the MMA rows so that each thread handles a slice of the tile).
-    AppendArgs a;
-    a.q = q;
-    a.qo_indptr = nullptr;
-    a.k_pool = k_pool;
-    a.v_pool = v_pool;
-    a.num_pages = num_pages;
-    a.kv_indptr = kv_indptr;
-    a.kv_indices = kv_indices;
-    a.last_page_len = last_page_len;
-    a.o = o;
-    a.lse = lse;
-    a.ws = ws_view(*plan, dev_ws);
-    a.num_ctas = plan->num_ctas;
-    a.num_units = plan->num_units;
-    a.num_split_items = plan->num_split_items;
-    a.dtype = dtype;
-    a.page_size = plan->page_size;
-    a.num_qo_heads = plan->num_qo_heads;
-    a.num_kv_heads = plan->num_kv_heads;
-    a.group = group;
-    a.q_tile = 1;
-    a.tile_tokens = 1;
-    a.rows_per_item = group;
-    a.total_qo = plan->batch;
-    a.max_qo_len = 1;
-    a.causal = 0;
-    a.sm_scale = sm_scale;
+    const AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, kv_indptr,
+                                        kv_indices, last_page_len, dtype, sm_scale, o, lse,
+                                        dev_ws);
     const char* msg = "";
     cudaError_t e = launch_decode_tc(a, st, &msg);  // merges split items itself
     if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
@@ -233,6 +259,41 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
   return ATTN_OK;
 }
 
+attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q, const void* k_pool,
+                                   const void* v_pool, int64_t num_pages, int32_t layout,
+                                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* last_page_len, int32_t dtype, float sm_scale,
+                                   const float* rope_cos, const float* rope_sin,
+                                   int64_t rope_max_pos, void* o, float* lse, void* dev_ws,
+                                   size_t dev_bytes, void* stream) {
+  attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
+                                      layout, kv_indptr, kv_indices, last_page_len, dtype, o,
+                                      dev_ws, dev_bytes, "attn_decode_run_rope");
+  if (s != ATTN_OK) return s;
+  if (!rope_cos || !rope_sin)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_rope: null cos / sin table");
+  if ((reinterpret_cast<uintptr_t>(rope_cos) | reinterpret_cast<uintptr_t>(rope_sin)) & 15u)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_rope: cos / sin tables must be 16-byte aligned");
+  if (rope_max_pos < plan->max_kv_len)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "attn_decode_run_rope: the cos / sin tables must cover every kv position "
+                "(rope_max_pos >= the plan's longest kv length)");
+  if (!decode_tc_shape(plan, layout))
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "attn_decode_run_rope: fused RoPE needs the HND layout, page_size % 16 == 0 "
+                "and 2, 4 or 8 query heads per kv head");
+  if (plan->batch == 0) return ATTN_OK;
+  AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, kv_indptr, kv_indices,
+                                last_page_len, dtype, sm_scale, o, lse, dev_ws);
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  const char* msg = "";
+  cudaError_t e = launch_decode_tc(a, static_cast<cudaStream_t>(stream), &msg);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run_rope: kernel launch");
+  return ATTN_OK;
+}
+
 attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
                               const int32_t* qo_indptr, const void* k_pool,
                               const void* v_pool, int64_t num_pages, int32_t layout,
@@ -254,6 +315,7 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
     return fail(ATTN_ERR_UNSUPPORTED, "attn_append_run: page_size must be a multiple of 16");
   if (plan->batch == 0 || plan->total_qo == 0) return ATTN_OK;
   AppendArgs a;
+  std::memset(&a, 0, sizeof a);
   a.q = q;
   a.qo_indptr = qo_indptr;
   a.k_pool = k_pool;

@@ -55,12 +55,14 @@ constexpr int kTile = kTcTile;
 constexpr int kChunk = kTcChunk;
 constexpr int kHalf = kTcHalf;
 constexpr int kTileBytes = kTcTileBytes;
-constexpr int kThreads = 160;
 constexpr int kWarpSoftmax = 0;
 constexpr int kWarpLoad = 1;
 constexpr int kWarpMma = 2;
 constexpr int kWarpQ = 3;
 constexpr int kWarpEpi = 4;  // TMEM lanes 0-31, like the softmax warp
+constexpr int kWarpRope0 = 5;  // warps 5-8 turn K tiles when RoPE is fused in
+template <bool ROPE>
+constexpr int block_threads() { return ROPE ? 288 : 160; }
 constexpr int kSlots = 6;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kTileBytes;
@@ -77,6 +79,7 @@ struct Bars {
   uint64_t o_free[2];   // epilogue read O[b] (count 32)
   uint64_t ounit[2];    // a unit's last P.V into O[b] is done (commit)
   uint64_t ep_full[2];  // softmax wrote the row state of a unit with O[b] (count 32)
+  uint64_t k_rot[kSlots / 2];  // RoPE: K tile k is turned in its slot (count 128)
   uint64_t drain;
   uint32_t tmem_base;
 };
@@ -255,8 +258,41 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
   return true;
 }
 
-template <bool BF16, int R, bool DEC>
-__global__ void __launch_bounds__(kThreads, 1)
+// Rotary embedding of 8 consecutive dims of a row: `mine` holds dims
+// [8 j, 8 j + 8) of one half of the row, `other` the same dims of the other
+// half; first: mine is the lower half (x' = x cos - y sin), else the upper
+// (y' = y cos + x sin). cs / sn: the 8 cos / sin of the pair indices.
+template <bool BF16>
+__device__ __forceinline__ uint4 rope8(uint4 mine, uint4 other, bool first, const float4 c0,
+                                       const float4 c1, const float4 s0, const float4 s1) {
+  const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  const uint32_t mw[4] = {mine.x, mine.y, mine.z, mine.w};
+  const uint32_t ow[4] = {other.x, other.y, other.z, other.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float m0, m1, o0, o1;
+    if constexpr (BF16) {
+      m0 = __uint_as_float(mw[i] << 16);
+      m1 = __uint_as_float(mw[i] & 0xffff0000u);
+      o0 = __uint_as_float(ow[i] << 16);
+      o1 = __uint_as_float(ow[i] & 0xffff0000u);
+    } else {
+      const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mw[i]));
+      const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ow[i]));
+      m0 = mf.x, m1 = mf.y, o0 = of.x, o1 = of.y;
+    }
+    const float sg = first ? -1.f : 1.f;  // x' = x c - y s;  y' = y c + x s
+    const float r0 = fmaf(sg * o0, sn[2 * i], m0 * cs[2 * i]);
+    const float r1 = fmaf(sg * o1, sn[2 * i + 1], m1 * cs[2 * i + 1]);
+    out[i] = pack2<BF16>(r0, r1);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <bool BF16, int R, bool DEC, bool ROPE>
+__global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
   constexpr int C = 32 / R;     // copies of each query row
   constexpr int W = kTile / C;  // kv columns per copy and tile
@@ -289,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.ounit[i]), 1);
       mbar_init(smem_u32(&bars.ep_full[i]), 32);
     }
+    for (int i = 0; i < kSlots / 2; ++i) mbar_init(smem_u32(&bars.k_rot[i]), 128);
     mbar_init(smem_u32(&bars.drain), 1);
     fence_mbar_init();
   }
@@ -382,12 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const int idx = lane + 32 * j;
+        qr[j] = make_uint4(0, 0, 0, 0);
         if (idx < kVec) {
           const QRow q = qrow<DEC, R>(a, g, idx >> 4);
-          qr[j] = q.ok ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
-                                                              q.orow * kHeadDim) +
-                               (idx & 15))
-                       : make_uint4(0, 0, 0, 0);
+          if (q.ok)
+            qr[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                                         q.orow * kHeadDim) +
+                          (idx & 15));
         }
       }
     };
@@ -416,6 +454,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const int idx = lane + 32 * j;
+        uint4 val = qr[j];
+        if constexpr (ROPE) {
+          // the query at position kv_len - 1: dims d and d + 64 sit in the
+          // pieces ch and ch + 8 of a row, i.e. in lanes l and l ^ 8
+          uint4 oth;
+          oth.x = __shfl_xor_sync(0xffffffffu, val.x, 8);
+          oth.y = __shfl_xor_sync(0xffffffffu, val.y, 8);
+          oth.z = __shfl_xor_sync(0xffffffffu, val.z, 8);
+          oth.w = __shfl_xor_sync(0xffffffffu, val.w, 8);
+          if (idx < kVec) {
+            const int ch = idx & 15;
+            const int64_t pos = g.kv_len - 1;
+            const float4* cp =
+                reinterpret_cast<const float4*>(a.rope_cos + pos * (kHeadDim / 2) + 8 * (ch & 7));
+            const float4* sp =
+                reinterpret_cast<const float4*>(a.rope_sin + pos * (kHeadDim / 2) + 8 * (ch & 7));
+            val = rope8<BF16>(val, oth, ch < 8, __ldg(cp), __ldg(cp + 1), __ldg(sp), __ldg(sp + 1));
+          }
+        }
         if (idx < kVec) {
           const int rho = idx >> 4, ch = idx & 15;
           const int half = ch >> 3, j8 = ch & 7;
@@ -423,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < C; ++c) {
             const int row = rho + R * c;
             const int off = kOffQ + half * kHalf + row * 128 + ((j8 ^ (row & 7)) << 4);
-            *reinterpret_cast<uint4*>(gbase + off) = qr[j];
+            *reinterpret_cast<uint4*>(gbase + off) = val;
           }
         }
       }
@@ -445,6 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_slot = [&](uint32_t use) -> bool {
         return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
                          ERR_WAIT_FULL);
+      };
+      // K tile k in its slot (and, with RoPE, turned by the rope warps)
+      auto wait_k = [&](uint32_t k) -> bool {
+        if constexpr (ROPE)
+          return mbar_wait(smem_u32(&bars.k_rot[k % (kSlots / 2)]), (k / (kSlots / 2)) & 1u, err,
+                           ERR_WAIT_FULL);
+        else
+          return wait_slot(2 * k);
       };
       auto issue_s = [&](uint32_t k) {
         const uint32_t qbase = base + kOffQ;
@@ -484,15 +549,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const DGeo g = decode_geo<DEC>(a, ui);
           if (g.ntiles == 0) continue;
           const int n = g.ntiles;
-          if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) ||
-              !wait_slot(2 * jt)) {
+          if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) || !wait_k(jt)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_s(jt);
           if (n > 1) {
-            if (!wait_slot(2 * jt + 2)) {
+            if (!wait_k(jt + 1)) {
               ok = false;
               break;
             }
@@ -510,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = issue_pv(k, (ntt + kChunk - 1) / kChunk, i == 0);
             if (ok && i + 2 < n) {
-              if (!wait_slot(2 * k + 4)) {
+              if (!wait_k(k + 2)) {
                 ok = false;
                 break;
               }
@@ -787,6 +851,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
   }
 
+  if constexpr (ROPE) {
+    if (warp >= kWarpRope0 && warp < kWarpRope0 + 4) {
+      // ------------------------------------------------------------ rope warps
+      // Thread t turns row t (kv position kv0 + t) of every K tile in place
+      // once the tile has landed, then releases it to the MMA warp.
+      const int t = threadIdx.x - kWarpRope0 * 32;
+      uint32_t k = 0;
+      bool ok = true;
+      for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+        for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+             ++ui) {
+          const DGeo g = decode_geo<DEC>(a, ui);
+          for (int i = 0; i < g.ntiles; ++i, ++k) {
+            const uint32_t use = 2 * k, slot = use % kSlots;
+            if (!mbar_wait(smem_u32(&bars.slot_full[slot]), (use / kSlots) & 1u, err,
+                           ERR_WAIT_FULL)) {
+              ok = false;
+              break;
+            }
+            const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+            if (kv0 + t < g.tok_end) {
+              const int64_t pos = kv0 + t;
+              uint8_t* row = gbase + kOffRing + slot * kTileBytes + t * 128;
+              const float4* cp = reinterpret_cast<const float4*>(a.rope_cos + pos * (kHeadDim / 2));
+              const float4* sp = reinterpret_cast<const float4*>(a.rope_sin + pos * (kHeadDim / 2));
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint4* lo = reinterpret_cast<uint4*>(row + ((j ^ (t & 7)) << 4));
+                uint4* hi = reinterpret_cast<uint4*>(row + kHalf + ((j ^ (t & 7)) << 4));
+                const uint4 x = *lo, y = *hi;
+                const float4 c0 = __ldg(cp + 2 * j), c1 = __ldg(cp + 2 * j + 1);
+                const float4 s0 = __ldg(sp + 2 * j), s1 = __ldg(sp + 2 * j + 1);
+                *lo = rope8<BF16>(x, y, true, c0, c1, s0, s1);
+                *hi = rope8<BF16>(y, x, false, c0, c1, s0, s1);
+              }
+            }
+            fence_proxy_async_smem();  // generic stores -> the MMA's operand reads
+            mbar_arrive(smem_u32(&bars.k_rot[k % (kSlots / 2)]));
+          }
+        }
+    }
+  }
+
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
@@ -798,21 +905,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16, int R, bool DEC>
+template <bool BF16, int R, bool DEC, bool ROPE = false>
 cudaError_t launch_k(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, R, DEC>,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, R, DEC, ROPE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  decode_tc_kernel<BF16, R, DEC><<<grid, kThreads, kSmem, stream>>>(prm);
+  decode_tc_kernel<BF16, R, DEC, ROPE><<<grid, block_threads<ROPE>(), kSmem, stream>>>(prm);
   return cudaGetLastError();
 }
 // decode runs with R = group in {2, 4, 8}; short appends with R in {1..16}
 template <bool BF16>
 cudaError_t launch_dt(const DecodeTcParams& prm, int rows, int grid, cudaStream_t stream) {
+  if (!prm.a.qo_indptr && prm.a.rope_cos) {  // decode with fused RoPE
+    switch (rows) {
+      case 2: return launch_k<BF16, 2, true, true>(prm, grid, stream);
+      case 4: return launch_k<BF16, 4, true, true>(prm, grid, stream);
+      default: return launch_k<BF16, 8, true, true>(prm, grid, stream);
+    }
+  }
   if (!prm.a.qo_indptr) {
     switch (rows) {
       case 2: return launch_k<BF16, 2, true>(prm, grid, stream);

@@ -142,6 +142,10 @@ struct AppendArgs {
   int32_t max_qo_len;      // longest query count of a request
   int32_t causal;
   float sm_scale;
+  // rotary position embedding of q and k (few-row kernel only): cos / sin
+  // tables float[max_pos, 64]; NULL = none
+  const float* rope_cos;
+  const float* rope_sin;
 };
 // qo_indptr == NULL runs the kernel in decode mode (one query row per
 // request; q is [batch, Hq, D]). Returns cudaErrorNotSupported for shapes the

@@ -123,6 +123,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   items.clear();
   items.reserve(size_t(batch) * num_kv_heads);
   int64_t max_qo_len = decode ? 1 : 0;
+  int64_t max_kv_len = 0;
   for (int32_t r = 0; r < batch; ++r) {
     const int64_t n_pages = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
     if (n_pages < 0) {
@@ -138,6 +139,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
       *msg = "attn_plan: a request's kv length must fit in 31 bits";
       return ATTN_ERR_INVALID_ARG;
     }
+    max_kv_len = std::max(max_kv_len, kv_len);
     int64_t qo_len = 1;
     if (!decode) {
       qo_len = int64_t(qo_indptr[r + 1]) - qo_indptr[r];
@@ -366,6 +368,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   if (!decode) h = fnv1a(h, qo_indptr, 4 * (size_t(batch) + 1));
   const int32_t shape[6] = {page_size, num_qo_heads, num_kv_heads, head_dim, p.causal, num_ctas};
   p.fingerprint = fnv1a(h, shape, sizeof shape);
+  p.max_kv_len = max_kv_len;
   *plan = p;
   return ATTN_OK;
 }

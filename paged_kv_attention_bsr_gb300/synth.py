@@ -132,8 +132,8 @@ def rope_tables(max_pos: int, head_dim: int = HEAD_DIM, theta: float = 500000.0,
                 llama31: bool = True, factor: float = 8.0, low_freq_factor: float = 1.0,
                 high_freq_factor: float = 4.0, original_max_pos: int = 8192):
     """cos / sin tables float32 [max_pos, head_dim / 2] of LLaMA-style rotary
-    position embedding (the pages' feature list: "LLaMA-style rotary position
-    embedding, including LLaMA 3.1"). Pair i turns by pos * f_i with
+    position embedding, the LLaMA 3.1 variant included (README copy on
+    gittoolsai.com, feature list). Pair i turns by pos * f_i with
     f_i = theta^(-2 i / head_dim); with llama31, the LLaMA 3.1 frequency
     rescaling for long contexts: wavelengths 2 pi / f_i shorter than
     original_max_pos / high_freq_factor keep f_i, those longer than

@@ -65,6 +65,19 @@ def test_workspace_size_and_validation_without_gpu():
     assert st == C.ERR_WORKSPACE_TOO_SMALL
     st = C.lib.attn_merge_states(None, None, None, None, None, None, 4, 2, 100, 1, None)
     assert st == C.ERR_UNSUPPORTED
+    # fused RoPE decode: tables checked before anything runs
+    kvi = np.array([0, 2, 5], np.int32)
+    lpl = np.array([3, 16], np.int32)
+    buf = np.zeros(1 << 16, np.uint8)
+    pr = C.plan(None, kvi, lpl, 16, 8, 2, 128, False, 4, buf)
+    assert pr.max_kv_len == 48  # lengths 16+3 and 2*16+16
+    fake = ctypes.c_void_p(256)
+    args = lambda cos, n, layout: (ctypes.byref(pr), fake, fake, fake, 8, layout, fake, fake,
+                                   fake, 1, ctypes.c_float(0.1), cos, cos, n, fake, None, fake,
+                                   1 << 30, None)
+    assert C.lib.attn_decode_run_rope(*args(None, 100, 0)) == C.ERR_INVALID_ARG
+    assert C.lib.attn_decode_run_rope(*args(fake, 47, 0)) == C.ERR_INVALID_ARG
+    assert C.lib.attn_decode_run_rope(*args(fake, 48, 1)) == C.ERR_UNSUPPORTED
     # the wait self-test validates before it launches anything
     assert C.lib.attn_wait_selftest(None, 1000, None) == C.ERR_INVALID_ARG
     assert C.lib.attn_wait_selftest(ctypes.c_void_p(256), 0, None) == C.ERR_INVALID_ARG

@@ -1,0 +1,87 @@
+"""Decode with rotary position embedding fused into the kernel
+(attn_decode_run_rope) against the fp64 oracle with the same cos / sin
+tables (oracle_batch_attention_rope)."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_attention_bsr_gb300 import synth
+from tests.gpu_util import assert_attn_close, oracle_dtype, poison_unused_slots, to_device
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # (page_size, Hq, Hk, dtype, lens)
+    (16, 8, 2, torch.bfloat16, [1, 15, 16, 17, 200, 1000, 0, 129]),
+    (16, 32, 4, torch.bfloat16, [3000, 64, 511, 2]),
+    (48, 8, 4, torch.float16, [47, 48, 49, 1000]),
+    (128, 16, 2, torch.bfloat16, [128, 129, 1000, 5]),
+]
+
+
+def run_rope(w, cos, sin, num_ctas=None):
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    c = w.cache
+    att = PagedAttention(w.num_qo_heads, w.num_kv_heads, 128, "decode",
+                         max_batch=max(w.batch, 1), num_ctas=num_ctas)
+    att.plan(c.kv_indptr, c.last_page_len, c.page_size)
+    d = to_device(c)
+    q = w.q.cuda()
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
+    att.run(q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"], d["last_page_len"],
+            w.sm_scale, out=o, lse=lse, rope=(torch.from_numpy(cos).cuda(),
+                                             torch.from_numpy(sin).cuda()))
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    return o, lse
+
+
+def oracle_rope(oracle_mod, w, cos, sin):
+    c = w.cache
+    return oracle_mod.batch_attention_rope(w.q, c.k_pool, c.v_pool, c.kv_indptr, c.kv_indices,
+                                           c.last_page_len, c.page_size, w.num_qo_heads,
+                                           w.num_kv_heads, 128, oracle_dtype(oracle_mod, w.dtype),
+                                           w.sm_scale, cos, sin)
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("num_ctas", [1, 7, None])
+def test_rope_decode_parity(oracle_mod, case, num_ctas):
+    P, Hq, Hk, dtype, lens = CASES[case]
+    pool = sum(-(-L // P) for L in lens) + 11
+    w = synth.decode_workload(f"rope{case}", lens, P, pool, Hq, Hk, dtype, seed=600 + case)
+    cos, sin = synth.rope_tables(max(lens) + 3)
+    o_ref, lse_ref = oracle_rope(oracle_mod, w, cos, sin)
+    o, lse = run_rope(w, cos, sin, num_ctas)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"rope case {case} ctas {num_ctas}")
+
+
+def test_rope_decode_stale_pool_slots(oracle_mod):
+    P, Hq, Hk, dtype, lens = CASES[0]
+    pool = sum(-(-L // P) for L in lens) + 11
+    w = synth.decode_workload("ropenan", lens, P, pool, Hq, Hk, dtype, seed=650)
+    poison_unused_slots(w.cache)
+    cos, sin = synth.rope_tables(max(lens))
+    o_ref, lse_ref = oracle_rope(oracle_mod, w, cos, sin)
+    o, lse = run_rope(w, cos, sin)
+    assert_attn_close(o, lse, o_ref, lse_ref, "rope stale slots")
+
+
+def test_rope_identity_table_equals_plain_decode():
+    from tests.test_gpu_decode import run_decode
+    P, Hq, Hk, dtype, lens = CASES[1]
+    pool = sum(-(-L // P) for L in lens) + 11
+    w = synth.decode_workload("ropeid", lens, P, pool, Hq, Hk, dtype, seed=660)
+    n = max(lens)
+    o1, l1 = run_rope(w, np.ones((n, 64), np.float32), np.zeros((n, 64), np.float32))
+    o2, l2, _ = run_decode(w)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_rope_decode_full_size_uniform(oracle_mod):
+    w = synth.uniform_gqa_decode()
+    cos, sin = synth.rope_tables(int(w.cache.kv_lens.max()))
+    o, lse = run_rope(w, cos, sin)
+    o_ref, lse_ref = oracle_rope(oracle_mod, w, cos, sin)
+    assert_attn_close(o, lse, o_ref, lse_ref, "rope uniform full size")
