@@ -195,9 +195,10 @@ def dev_cache(cache):
 class DecodeStep:
     """plan + run of one decode batch through the public API."""
 
-    def __init__(self, w):
+    def __init__(self, w, rope=None):
         from paged_kv_attention_bsr_gb300.api import PagedAttention
         self.w = w
+        self.rope = rope
         c = w.cache
         self.att = PagedAttention(w.num_qo_heads, w.num_kv_heads, w.head_dim, "decode",
                                   max_batch=w.batch)
@@ -213,7 +214,8 @@ class DecodeStep:
     def run(self):
         d = self.d
         self.att.run(self.q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"],
-                     d["last_page_len"], self.w.sm_scale, out=self.o, lse=self.lse)
+                     d["last_page_len"], self.w.sm_scale, out=self.o, lse=self.lse,
+                     rope=self.rope)
 
 
 def time_steps(step_fns, steps, warmup, flush, kernel_split=1):
@@ -351,18 +353,45 @@ def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
     return w.name, res
 
 
+def bench_rope_decode(hbm_peak, bf16_peak, flush, steps, warmup):
+    """The uniform GQA decode batch with LLaMA 3.1 RoPE fused into the kernel
+    (keys cached un-rotated, turned in shared memory), beside the same batch
+    without RoPE."""
+    from paged_kv_attention_bsr_gb300 import synth
+    w = synth.uniform_gqa_decode()
+    max_pos = int(w.cache.kv_lens.max())
+    cos, sin = synth.rope_tables(max_pos)
+    rope = (torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda())
+    st = DecodeStep(w, rope=rope)
+    step_ms, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
+    b = decode_bytes(w) + 2 * max_pos * 64 * 4  # + the cos / sin rows
+    k_s = float(np.mean(kern_ms)) * 1e-3
+    res = {"kind": "decode+rope", "bytes": b, "kernel_us": k_s * 1e6,
+           "step_us": float(np.mean(step_ms)) * 1e3,
+           "GB/s": b / k_s / 1e9, "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak}
+    assert st.att.status() == 0
+    plain = DecodeStep(w)
+    _, kern_plain = time_steps([plain.plan, plain.run], steps, warmup, flush)
+    res["without_rope_kernel_us"] = float(np.mean(kern_plain)) * 1e3
+    del st, plain
+    torch.cuda.empty_cache()
+    return w.name + "_rope", res
+
+
 WORKLOAD_BENCH = {
     "single_decode": lambda *a: bench_decode_workload("single_decode", *a),
     "skewed_decode": lambda *a: bench_decode_workload("skewed_decode", *a),
     "uniform_decode": lambda *a: bench_decode_workload("uniform_decode", *a),
     "causal_append": bench_causal_append,
     "shared_prefix": bench_shared_prefix,
+    "rope_decode": bench_rope_decode,
 }
 
 
 def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
     out = {}
-    for key in ("single_decode", "skewed_decode", "causal_append", "shared_prefix"):
+    for key in ("single_decode", "skewed_decode", "causal_append", "shared_prefix",
+                "rope_decode"):
         name, res = WORKLOAD_BENCH[key](hbm_peak, bf16_peak, flush, steps, warmup)
         out[name] = res
     return out

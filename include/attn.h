@@ -203,9 +203,17 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q,
  * at position j and the query at position kv_len - 1; the turned q and k are
  * rounded to `dtype` before the products.
  *   rope_cos, rope_sin : device float[rope_max_pos, 64], row-major and
- *                        contiguous, 16-byte aligned (caller-built tables,
- *                        e.g. LLaMA 3.1 frequencies); rope_max_pos must be at
- *                        least the plan's max_kv_len; read only
+ *                        contiguous, 16-byte aligned, read only: the cos /
+ *                        sin of the angles pos * theta_d for some per-pair
+ *                        frequencies theta_d (plain LLaMA, or LLaMA 3.1 with
+ *                        its rescaled frequencies); rope_max_pos must be at
+ *                        least the plan's max_kv_len
+ * The query reads its table row directly. Keys read a few rows per 128-key
+ * tile and derive the others with the angle-sum identities
+ * (cos((B + o) t) = cos(B t) cos(o t) - sin(B t) sin(o t), likewise for sin),
+ * so tables that are not of that form (e.g. with a magnitude factor folded
+ * in; fold such a factor into sm_scale instead) give other keys. The derived
+ * values differ from direct rows by a few fp32 ulps.
  *   other arguments    : as attn_decode_run
  * Supported: the shapes attn_decode_run runs on the tensor-core kernel (HND,
  * page_size % 16 == 0, 2, 4 or 8 query heads per kv head); others return

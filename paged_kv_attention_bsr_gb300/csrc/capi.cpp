@@ -287,6 +287,7 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q, const
                                 last_page_len, dtype, sm_scale, o, lse, dev_ws);
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;
+  a.rope_rows = rope_max_pos;
   const char* msg = "";
   cudaError_t e = launch_decode_tc(a, static_cast<cudaStream_t>(stream), &msg);
   if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);

@@ -65,6 +65,13 @@ template <bool ROPE>
 constexpr int block_threads() { return ROPE ? 288 : 160; }
 constexpr int kSlots = 6;
 constexpr int kOffQ = 0;
+// RoPE key angles: cos / sin of the offset rows o = 0, 2, .., 14 (8 x 64
+// floats each) in query-tile rows 32-63 of the lower half, which hold no
+// query (the few-row kernel's queries sit in rows 0-31; the MMA's output
+// lanes of rows 32-127 are never read)
+constexpr int kOffRopeCos = kOffQ + 32 * 128;
+constexpr int kOffRopeSin = kOffRopeCos + 8 * 64 * 4;
+static_assert(kOffRopeSin + 8 * 64 * 4 <= kOffQ + kTcHalf, "RoPE offset rows fit the spare query rows");
 constexpr int kOffRing = kTileBytes;
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
 constexpr int kOffHand = kOffBar + 256;         // softmax -> epilogue row state
@@ -258,37 +265,79 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
   return true;
 }
 
-// Rotary embedding of 8 consecutive dims of a row: `mine` holds dims
-// [8 j, 8 j + 8) of one half of the row, `other` the same dims of the other
-// half; first: mine is the lower half (x' = x cos - y sin), else the upper
-// (y' = y cos + x sin). cs / sn: the 8 cos / sin of the pair indices.
+// Rotary embedding of one 32-bit word (two consecutive dims) of a row:
+// `mine` holds dims (d, d + 1) of one half of the row, `other` the same dims
+// of the other half; first: mine is the lower half (x' = x cos - y sin), else
+// the upper (y' = y cos + x sin). Products and sums in fp32, then rounded to
+// the storage type.
+template <bool BF16>
+__device__ __forceinline__ uint32_t rope_word(uint32_t mine, uint32_t other, bool first, float c0,
+                                              float c1, float s0, float s1) {
+  float m0, m1, o0, o1;
+  if constexpr (BF16) {
+    m0 = __uint_as_float(mine << 16);
+    m1 = __uint_as_float(mine & 0xffff0000u);
+    o0 = __uint_as_float(other << 16);
+    o1 = __uint_as_float(other & 0xffff0000u);
+  } else {
+    const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mine));
+    const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&other));
+    m0 = mf.x, m1 = mf.y, o0 = of.x, o1 = of.y;
+  }
+  const float sg = first ? -1.f : 1.f;
+  return pack2<BF16>(fmaf(sg * o0, s0, m0 * c0), fmaf(sg * o1, s1, m1 * c1));
+}
+
+// 8 consecutive dims (one 16-byte piece); c0 / c1, s0 / s1: their cos / sin
 template <bool BF16>
 __device__ __forceinline__ uint4 rope8(uint4 mine, uint4 other, bool first, const float4 c0,
                                        const float4 c1, const float4 s0, const float4 s1) {
-  const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  const uint32_t mw[4] = {mine.x, mine.y, mine.z, mine.w};
-  const uint32_t ow[4] = {other.x, other.y, other.z, other.w};
-  uint32_t out[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float m0, m1, o0, o1;
-    if constexpr (BF16) {
-      m0 = __uint_as_float(mw[i] << 16);
-      m1 = __uint_as_float(mw[i] & 0xffff0000u);
-      o0 = __uint_as_float(ow[i] << 16);
-      o1 = __uint_as_float(ow[i] & 0xffff0000u);
-    } else {
-      const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mw[i]));
-      const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ow[i]));
-      m0 = mf.x, m1 = mf.y, o0 = of.x, o1 = of.y;
-    }
-    const float sg = first ? -1.f : 1.f;  // x' = x c - y s;  y' = y c + x s
-    const float r0 = fmaf(sg * o0, sn[2 * i], m0 * cs[2 * i]);
-    const float r1 = fmaf(sg * o1, sn[2 * i + 1], m1 * cs[2 * i + 1]);
-    out[i] = pack2<BF16>(r0, r1);
+  return make_uint4(rope_word<BF16>(mine.x, other.x, first, c0.x, c0.y, s0.x, s0.y),
+                    rope_word<BF16>(mine.y, other.y, first, c0.z, c0.w, s0.z, s0.w),
+                    rope_word<BF16>(mine.z, other.z, first, c1.x, c1.y, s1.x, s1.y),
+                    rope_word<BF16>(mine.w, other.w, first, c1.z, c1.w, s1.z, s1.w));
+}
+
+// 4 consecutive dims (8 bytes); c / s: their cos / sin
+template <bool BF16>
+__device__ __forceinline__ uint2 rope4(uint2 mine, uint2 other, bool first, const float4 c,
+                                       const float4 s) {
+  return make_uint2(rope_word<BF16>(mine.x, other.x, first, c.x, c.y, s.x, s.y),
+                    rope_word<BF16>(mine.y, other.y, first, c.z, c.w, s.z, s.w));
+}
+
+// The two 16-bit values of a word as floats.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
   }
-  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Key rotation of 4 pairs (dims d..d+3 with d+64..d+67) at an angle B + o:
+// x / y hold the lower / upper dims, (cb, sb, nsb) = (cos, sin, -sin) of
+// B theta and (oc, os) = (cos, sin) of o theta for the 4 pairs. The angle
+// sums and the turn run on packed fp32x2 arithmetic.
+template <bool BF16>
+__device__ __forceinline__ void rope_key4(uint2& x, uint2& y, float4 cb, float4 sb, float4 nsb,
+                                          float4 oc, float4 os) {
+  const float2 oc0 = make_float2(oc.x, oc.y), oc1 = make_float2(oc.z, oc.w);
+  const float2 os0 = make_float2(os.x, os.y), os1 = make_float2(os.z, os.w);
+  // cos((B + o) t) = cos B cos o - sin B sin o;  sin((B + o) t) = sin B cos o + cos B sin o
+  const float2 c0 = ffma2(make_float2(cb.x, cb.y), oc0, fmul2(make_float2(nsb.x, nsb.y), os0));
+  const float2 c1 = ffma2(make_float2(cb.z, cb.w), oc1, fmul2(make_float2(nsb.z, nsb.w), os1));
+  const float2 s0 = ffma2(make_float2(sb.x, sb.y), oc0, fmul2(make_float2(cb.x, cb.y), os0));
+  const float2 s1 = ffma2(make_float2(sb.z, sb.w), oc1, fmul2(make_float2(cb.z, cb.w), os1));
+  const float2 x0 = unpack2<BF16>(x.x), x1 = unpack2<BF16>(x.y);
+  const float2 y0 = unpack2<BF16>(y.x), y1 = unpack2<BF16>(y.y);
+  const float2 ns0 = make_float2(-s0.x, -s0.y), ns1 = make_float2(-s1.x, -s1.y);
+  // x' = x cos - y sin;  y' = y cos + x sin
+  const float2 xr0 = ffma2(x0, c0, fmul2(y0, ns0)), xr1 = ffma2(x1, c1, fmul2(y1, ns1));
+  const float2 yr0 = ffma2(y0, c0, fmul2(x0, s0)), yr1 = ffma2(y1, c1, fmul2(x1, s1));
+  x = make_uint2(pack2<BF16>(xr0.x, xr0.y), pack2<BF16>(xr1.x, xr1.y));
+  y = make_uint2(pack2<BF16>(yr0.x, yr0.y), pack2<BF16>(yr1.x, yr1.y));
 }
 
 template <bool BF16, int R, bool DEC, bool ROPE>
@@ -854,43 +903,134 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
   if constexpr (ROPE) {
     if (warp >= kWarpRope0 && warp < kWarpRope0 + 4) {
       // ------------------------------------------------------------ rope warps
-      // Thread t turns row t (kv position kv0 + t) of every K tile in place
-      // once the tile has landed, then releases it to the MMA warp.
-      const int t = threadIdx.x - kWarpRope0 * 32;
-      uint32_t k = 0;
-      bool ok = true;
-      for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
-        for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
-             ++ui) {
-          const DGeo g = decode_geo<DEC>(a, ui);
-          for (int i = 0; i < g.ntiles; ++i, ++k) {
-            const uint32_t use = 2 * k, slot = use % kSlots;
-            if (!mbar_wait(smem_u32(&bars.slot_full[slot]), (use / kSlots) & 1u, err,
-                           ERR_WAIT_FULL)) {
-              ok = false;
-              break;
-            }
-            const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
-            if (kv0 + t < g.tok_end) {
-              const int64_t pos = kv0 + t;
-              uint8_t* row = gbase + kOffRing + slot * kTileBytes + t * 128;
-              const float4* cp = reinterpret_cast<const float4*>(a.rope_cos + pos * (kHeadDim / 2));
-              const float4* sp = reinterpret_cast<const float4*>(a.rope_sin + pos * (kHeadDim / 2));
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                uint4* lo = reinterpret_cast<uint4*>(row + ((j ^ (t & 7)) << 4));
-                uint4* hi = reinterpret_cast<uint4*>(row + kHalf + ((j ^ (t & 7)) << 4));
-                const uint4 x = *lo, y = *hi;
-                const float4 c0 = __ldg(cp + 2 * j), c1 = __ldg(cp + 2 * j + 1);
-                const float4 s0 = __ldg(sp + 2 * j), s1 = __ldg(sp + 2 * j + 1);
-                *lo = rope8<BF16>(x, y, true, c0, c1, s0, s1);
-                *hi = rope8<BF16>(y, x, false, c0, c1, s0, s1);
-              }
-            }
-            fence_proxy_async_smem();  // generic stores -> the MMA's operand reads
-            mbar_arrive(smem_u32(&bars.k_rot[k % (kSlots / 2)]));
+      // Warp w turns rows [32 w, 32 w + 32) of every K tile in place once the
+      // tile has landed, then releases it to the MMA warp: a half-warp per
+      // row, lane l on pairs 4 (l % 16) .. + 3. The angles are pos * theta_i,
+      // so the cos / sin of row B + o follow from those of rows B and o by
+      // the angle-sum identities. A lane's rows are B_h + 2 it (it < 8) for
+      // two bases B_h per tile: it keeps the 8 offset rows o = 2 it for its
+      // pairs in registers, and loads a tile's two base rows (512 B per
+      // half-warp) one tile ahead, so no table read waits on a tile.
+      const int wr = warp - kWarpRope0;
+      const int hrow = lane >> 4, p0 = 4 * (lane & 15);
+      const int kbyte = (((lane & 15) >> 1) << 4) | ((lane & 1) << 3);  // piece, byte in it
+      int vc = blockIdx.x, ui = vc < a.num_ctas ? __ldg(a.ws.work_indptr + vc) : 0;
+      auto next_unit = [&](DGeo& g) -> bool {
+        while (vc < a.num_ctas) {
+          if (ui < __ldg(a.ws.work_indptr + vc + 1)) {
+            g = decode_geo<DEC>(a, ui++);
+            if (g.ntiles > 0) return true;
+          } else {
+            vc += gridDim.x;
+            if (vc < a.num_ctas) ui = __ldg(a.ws.work_indptr + vc);
           }
         }
+        return false;
+      };
+      constexpr int kIt = 8;  // row pairs per warp and half tile
+      auto row_c = [&](int64_t pos) {
+        return __ldg(reinterpret_cast<const float4*>(a.rope_cos + pos * (kHeadDim / 2) + p0));
+      };
+      auto row_s = [&](int64_t pos) {
+        return __ldg(reinterpret_cast<const float4*>(a.rope_sin + pos * (kHeadDim / 2) + p0));
+      };
+      // offset rows 2 it into shared memory (only those below the table's
+      // length can be needed: a row B + 2 it in use is below it and B >= 0)
+      {
+        const int t = threadIdx.x - kWarpRope0 * 32;
+        float* oc_s = reinterpret_cast<float*>(gbase + kOffRopeCos);
+        float* os_s = reinterpret_cast<float*>(gbase + kOffRopeSin);
+        for (int idx = t; idx < 8 * 64; idx += 128) {
+          const int o = 2 * (idx >> 6);
+          const bool ok_row = o < a.rope_rows;
+          oc_s[idx] = ok_row ? __ldg(a.rope_cos + o * (kHeadDim / 2) + (idx & 63)) : 1.f;
+          os_s[idx] = ok_row ? __ldg(a.rope_sin + o * (kHeadDim / 2) + (idx & 63)) : 0.f;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four rope warps
+      }
+      // base rows of tile i of unit g: B_h = kv0 + 32 w + 16 h + (l >> 4)
+      float4 bc[2], bs[2], nbc[2], nbs[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) bc[h] = bs[h] = nbc[h] = nbs[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+      auto fetch = [&](const DGeo& g, int i, float4 (&c)[2], float4 (&sn)[2]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t base = g.tok_begin + int64_t(i) * kTile + 32 * wr + 2 * kIt * h + hrow;
+          if (base < g.tok_end) {
+            c[h] = row_c(base);
+            sn[h] = row_s(base);
+          }
+        }
+      };
+      DGeo g, gn;
+      int i = 0, in = 0;
+      bool have = next_unit(g), have_n = false;
+      auto advance = [&]() {  // (gn, in) = the tile after (g, i)
+        if (i + 1 < g.ntiles) {
+          gn = g;
+          in = i + 1;
+          have_n = true;
+        } else {
+          in = 0;
+          have_n = next_unit(gn);
+        }
+      };
+      if (have) {
+        fetch(g, 0, bc, bs);
+        advance();
+      }
+      for (uint32_t k = 0; have; ++k) {
+        const uint32_t use = 2 * k, slot = use % kSlots;
+        if (!mbar_wait(smem_u32(&bars.slot_full[slot]), (use / kSlots) & 1u, err, ERR_WAIT_FULL))
+          break;
+        if (have_n) fetch(gn, in, nbc, nbs);
+        const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+        uint8_t* tile = gbase + kOffRing + slot * kTileBytes;
+        // a compact loop (the block's nine warps run six different loops, so
+        // code size matters): kStep rows per step, all read before any is
+        // written back
+        constexpr int kStep = 2;
+#pragma unroll 1
+        for (int st = 0; st < 2 * kIt / kStep; ++st) {
+          const int h = st / (kIt / kStep);  // half tile
+          const float4 cb = h ? bc[1] : bc[0], sb = h ? bs[1] : bs[0];
+          const float4 nsb = make_float4(-sb.x, -sb.y, -sb.z, -sb.w);
+          uint2 x[kStep], y[kStep];
+          float4 oci[kStep], osi[kStep];
+          int off[kStep];
+          bool use[kStep];
+#pragma unroll
+          for (int u = 0; u < kStep; ++u) {
+            const int it = kStep * (st % (kIt / kStep)) + u;  // offset row 2 it
+            const int row = 32 * wr + 2 * kIt * h + 2 * it + hrow;
+            off[u] = row * 128 + (kbyte ^ ((row & 7) << 4));
+            use[u] = kv0 + row < g.tok_end;
+            if (use[u]) {
+              x[u] = *reinterpret_cast<const uint2*>(tile + off[u]);
+              y[u] = *reinterpret_cast<const uint2*>(tile + kHalf + off[u]);
+              oci[u] = *reinterpret_cast<const float4*>(gbase + kOffRopeCos + it * 256 + p0 * 4);
+              osi[u] = *reinterpret_cast<const float4*>(gbase + kOffRopeSin + it * 256 + p0 * 4);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kStep; ++u) {
+            if (use[u]) {
+              rope_key4<BF16>(x[u], y[u], cb, sb, nsb, oci[u], osi[u]);
+              *reinterpret_cast<uint2*>(tile + off[u]) = x[u];
+              *reinterpret_cast<uint2*>(tile + kHalf + off[u]) = y[u];
+            }
+          }
+        }
+        fence_proxy_async_smem();  // generic stores -> the MMA's operand reads
+        mbar_arrive(smem_u32(&bars.k_rot[k % (kSlots / 2)]));
+        have = have_n;
+        if (have) {
+          g = gn;
+          i = in;
+          bc[0] = nbc[0], bc[1] = nbc[1], bs[0] = nbs[0], bs[1] = nbs[1];
+          advance();
+        }
+      }
     }
   }
 

@@ -143,9 +143,10 @@ struct AppendArgs {
   int32_t causal;
   float sm_scale;
   // rotary position embedding of q and k (few-row kernel only): cos / sin
-  // tables float[max_pos, 64]; NULL = none
+  // tables float[rope_rows, 64] of the angles pos * theta_i; NULL = none
   const float* rope_cos;
   const float* rope_sin;
+  int64_t rope_rows;
 };
 // qo_indptr == NULL runs the kernel in decode mode (one query row per
 // request; q is [batch, Hq, D]). Returns cudaErrorNotSupported for shapes the

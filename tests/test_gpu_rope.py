@@ -57,6 +57,18 @@ def test_rope_decode_parity(oracle_mod, case, num_ctas):
     assert_attn_close(o, lse, o_ref, lse_ref, f"rope case {case} ctas {num_ctas}")
 
 
+@pytest.mark.parametrize("lens", [[1, 2, 3, 7], [1], [14, 15, 16]])
+def test_rope_decode_short_table(oracle_mod, lens):
+    """Tables exactly as long as the longest request, shorter than the key
+    offset rows a tile derives its angles from."""
+    pool = sum(-(-L // 16) for L in lens) + 5
+    w = synth.decode_workload("ropeshort", lens, 16, pool, 16, 4, torch.bfloat16, seed=640)
+    cos, sin = synth.rope_tables(max(lens))
+    o_ref, lse_ref = oracle_rope(oracle_mod, w, cos, sin)
+    o, lse = run_rope(w, cos, sin)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"rope short table {lens}")
+
+
 def test_rope_decode_stale_pool_slots(oracle_mod):
     P, Hq, Hk, dtype, lens = CASES[0]
     pool = sum(-(-L // P) for L in lens) + 11
