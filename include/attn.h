@@ -99,6 +99,8 @@ typedef struct attn_plan {
   int64_t dev_bytes_needed; /* device workspace bytes this plan uses           */
   uint64_t fingerprint;     /* hash of the host inputs of the plan             */
   int64_t max_kv_len;       /* longest kv length of a request                  */
+  int64_t min_kv_minus_qo;  /* smallest kv_len - qo_len over requests with kv
+                               tokens (INT64_MAX if none)                      */
 } attn_plan_t;
 
 /*
@@ -230,6 +232,29 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q,
                                    const float* rope_sin, int64_t rope_max_pos,
                                    void* o, float* lse, void* dev_ws, size_t dev_bytes,
                                    void* stream);
+
+/*
+ * attn_append_run with rotary position embedding fused in (as
+ * attn_decode_run_rope): query row i of a request with qo_len rows sits at
+ * position kv_len - qo_len + i, key j at position j.
+ *   rope_cos, rope_sin, rope_max_pos : as attn_decode_run_rope
+ *   other arguments                  : as attn_append_run
+ * Supported: the short appends the few-row tensor-core kernel runs (group x
+ * the longest query count <= 16, e.g. speculative or multi-token decode, or
+ * the n generations of a shared prefix; HND, page_size % 16 == 0). Longer
+ * appends return UNSUPPORTED.
+ * Errors: as attn_append_run and attn_decode_run_rope; INVALID_ARG if a
+ * request with kv tokens has kv_len < qo_len (a query would sit before
+ * position 0).
+ */
+attn_status_t attn_append_run_rope(const attn_plan_t* plan, const void* q,
+                                   const int32_t* qo_indptr, const void* k_pool,
+                                   const void* v_pool, int64_t num_pages, int32_t layout,
+                                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* last_page_len, int32_t dtype,
+                                   int32_t causal, float sm_scale, const float* rope_cos,
+                                   const float* rope_sin, int64_t rope_max_pos, void* o,
+                                   float* lse, void* dev_ws, size_t dev_bytes, void* stream);
 
 /*
  * Append / prefill attention: many query rows per request (ragged, offsets

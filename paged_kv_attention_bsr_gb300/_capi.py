@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_S
 # Every symbol include/attn.h declares (checked by the tests).
 EXPORTS = ("attn_workspace_size", "attn_default_num_ctas", "attn_plan", "attn_decode_run",
            "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error",
-           "attn_decode_run_noalloc", "attn_wait_selftest", "attn_decode_run_rope")
+           "attn_decode_run_noalloc", "attn_wait_selftest", "attn_decode_run_rope",
+           "attn_append_run_rope")
 
 
 class AttnError(RuntimeError):
@@ -44,7 +45,8 @@ class Plan(ctypes.Structure):
         "num_slots", "total_qo", "max_qo_len")] + [(n, ctypes.c_int64) for n in (
         "total_weight", "max_cta_weight", "off_work_indptr", "off_units", "off_merge_indptr",
         "off_merge_items", "off_counters", "off_partial_o", "off_partial_lse", "table_bytes",
-        "dev_bytes_needed")] + [("fingerprint", ctypes.c_uint64), ("max_kv_len", ctypes.c_int64)]
+        "dev_bytes_needed")] + [("fingerprint", ctypes.c_uint64), ("max_kv_len", ctypes.c_int64),
+                              ("min_kv_minus_qo", ctypes.c_int64)]
 
 
 def _load():
@@ -70,6 +72,8 @@ def _load():
         "attn_wait_selftest": [vp, i32, vp],
         "attn_decode_run_rope": [P(Plan), vp, vp, vp, i64, i32, vp, vp, vp, i32, f32, vp, vp,
                                  i64, vp, vp, vp, sz, vp],
+        "attn_append_run_rope": [P(Plan), vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, f32,
+                                 vp, vp, i64, vp, vp, vp, sz, vp],
         "attn_decode_run_noalloc": [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64, i32, vp,
                                     vp, vp, i32, f32, vp, vp, vp],
     }
@@ -175,15 +179,19 @@ def decode_run(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
                                dev_ws.numel() * dev_ws.element_size(), _stream(stream)))
 
 
-def decode_run_rope(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale,
-                    rope_cos, rope_sin, o, lse, dev_ws, layout=LAYOUT_HND, num_pages=None,
-                    stream=None):
-    """attn_decode_run_rope: rope_cos / rope_sin device float32 [max_pos, 64]."""
+def _check_rope_tables(rope_cos, rope_sin):
     for t in (rope_cos, rope_sin):
         if t.dtype != torch.float32 or t.dim() != 2 or t.shape[1] != 64 or not t.is_contiguous():
             raise ValueError("rope tables must be contiguous float32 [max_pos, 64]")
     if rope_sin.shape != rope_cos.shape:
         raise ValueError("rope_cos and rope_sin differ in shape")
+
+
+def decode_run_rope(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale,
+                    rope_cos, rope_sin, o, lse, dev_ws, layout=LAYOUT_HND, num_pages=None,
+                    stream=None):
+    """attn_decode_run_rope: rope_cos / rope_sin device float32 [max_pos, 64]."""
+    _check_rope_tables(rope_cos, rope_sin)
     if num_pages is None:
         num_pages = k_pool.shape[0]
     _check(lib.attn_decode_run_rope(ctypes.byref(p), _ptr(q), _ptr(k_pool), _ptr(v_pool),
@@ -205,6 +213,22 @@ def append_run(p: Plan, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices, las
                                int(bool(causal)), float(sm_scale), _ptr(o), _ptr(lse),
                                _ptr(dev_ws), dev_ws.numel() * dev_ws.element_size(),
                                _stream(stream)))
+
+
+def append_run_rope(p: Plan, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices,
+                    last_page_len, causal, sm_scale, rope_cos, rope_sin, o, lse, dev_ws,
+                    layout=LAYOUT_HND, num_pages=None, stream=None):
+    """attn_append_run_rope: rope_cos / rope_sin device float32 [max_pos, 64]."""
+    _check_rope_tables(rope_cos, rope_sin)
+    if num_pages is None:
+        num_pages = k_pool.shape[0]
+    _check(lib.attn_append_run_rope(ctypes.byref(p), _ptr(q), _ptr(qo_indptr), _ptr(k_pool),
+                                    _ptr(v_pool), int(num_pages), layout, _ptr(kv_indptr),
+                                    _ptr(kv_indices), _ptr(last_page_len), dtype_code(q.dtype),
+                                    int(bool(causal)), float(sm_scale), _ptr(rope_cos),
+                                    _ptr(rope_sin), int(rope_cos.shape[0]), _ptr(o), _ptr(lse),
+                                    _ptr(dev_ws), dev_ws.numel() * dev_ws.element_size(),
+                                    _stream(stream)))
 
 
 def merge_states(o_a, lse_a, o_b, lse_b, o_out, lse_out, stream=None):

@@ -71,7 +71,8 @@ class PagedAttention:
             out=None, lse=None, qo_indptr=None, layout: int = C.LAYOUT_HND, num_pages=None,
             return_lse: bool = False, stream=None, rope=None):
         """rope: optional (cos, sin) device float32 tables [max_pos, head_dim / 2]
-        (decode only): rotary position embedding fused into the kernel."""
+        of the angles pos * theta_d: rotary position embedding fused into the
+        kernel (decode; append when group x the longest query count <= 16)."""
         if self.plan_info is None:
             raise RuntimeError("run() before plan()")
         if sm_scale is None:
@@ -85,7 +86,9 @@ class PagedAttention:
                               last_page_len, sm_scale, rope[0], rope[1], out, lse,
                               self.dev_ws, layout, num_pages, stream)
         elif rope is not None:
-            raise ValueError("fused RoPE is implemented for decode runs")
+            C.append_run_rope(self.plan_info, q, qo_indptr, k_pool, v_pool, kv_indptr,
+                              kv_indices, last_page_len, self._causal, sm_scale, rope[0],
+                              rope[1], out, lse, self.dev_ws, layout, num_pages, stream)
         elif self.mode == "decode":
             C.decode_run(self.plan_info, q, k_pool, v_pool, kv_indptr, kv_indices,
                          last_page_len, sm_scale, out, lse, self.dev_ws, layout, num_pages,

@@ -115,6 +115,78 @@ attn::AppendArgs decode_tc_args(const attn_plan_t* plan, const void* q, const vo
   return a;
 }
 
+// Validation shared by the append entry points.
+attn_status_t check_append(const attn_plan_t* plan, const void* q, const int32_t* qo_indptr,
+                           const void* k_pool, const void* v_pool, int64_t num_pages,
+                           int32_t layout, const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* last_page_len, int32_t dtype, int32_t causal, void* o,
+                           void* dev_ws, size_t dev_bytes, const char* fn) {
+  attn_status_t s = check_plan_common(plan, ATTN_MODE_APPEND, q, k_pool, v_pool, num_pages,
+                                      layout, kv_indptr, kv_indices, last_page_len, dtype, o,
+                                      dev_ws, dev_bytes, fn);
+  if (s != ATTN_OK) return s;
+  if ((causal ? 1 : 0) != plan->causal)
+    return fail(ATTN_ERR_INVALID_ARG, std::string(fn) + ": causal differs from the plan's");
+  if (plan->batch > 0 && !qo_indptr)
+    return fail(ATTN_ERR_INVALID_ARG, std::string(fn) + ": qo_indptr is NULL");
+  if (layout != ATTN_LAYOUT_HND)
+    return fail(ATTN_ERR_UNSUPPORTED, std::string(fn) + ": only the HND layout is implemented");
+  if (plan->page_size % 16 != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, std::string(fn) + ": page_size must be a multiple of 16");
+  return ATTN_OK;
+}
+
+// Kernel arguments of an append run (no RoPE).
+attn::AppendArgs append_args(const attn_plan_t* plan, const void* q, const int32_t* qo_indptr,
+                             const void* k_pool, const void* v_pool, int64_t num_pages,
+                             const int32_t* kv_indptr, const int32_t* kv_indices,
+                             const int32_t* last_page_len, int32_t dtype, float sm_scale,
+                             void* o, float* lse, void* dev_ws) {
+  attn::AppendArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.qo_indptr = qo_indptr;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.num_pages = num_pages;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.last_page_len = last_page_len;
+  a.o = o;
+  a.lse = lse;
+  a.ws = ws_view(*plan, dev_ws);
+  a.num_ctas = plan->num_ctas;
+  a.num_units = plan->num_units;
+  a.num_split_items = plan->num_split_items;
+  a.dtype = dtype;
+  a.page_size = plan->page_size;
+  a.num_qo_heads = plan->num_qo_heads;
+  a.num_kv_heads = plan->num_kv_heads;
+  a.group = plan->num_qo_heads / plan->num_kv_heads;
+  a.q_tile = plan->q_tile;
+  a.tile_tokens = attn::kTileRows / a.group;
+  a.rows_per_item = plan->rows_per_item;
+  a.total_qo = plan->total_qo;
+  a.max_qo_len = plan->max_qo_len;
+  a.causal = plan->causal;
+  a.sm_scale = sm_scale;
+  return a;
+}
+
+// Checks of the cos / sin tables of a RoPE run.
+attn_status_t check_rope(const attn_plan_t* plan, const float* rope_cos, const float* rope_sin,
+                         int64_t rope_max_pos, const char* fn) {
+  if (!rope_cos || !rope_sin)
+    return fail(ATTN_ERR_INVALID_ARG, std::string(fn) + ": null cos / sin table");
+  if ((reinterpret_cast<uintptr_t>(rope_cos) | reinterpret_cast<uintptr_t>(rope_sin)) & 15u)
+    return fail(ATTN_ERR_INVALID_ARG, std::string(fn) + ": cos / sin tables must be 16-byte aligned");
+  if (rope_max_pos < plan->max_kv_len)
+    return fail(ATTN_ERR_INVALID_ARG,
+                std::string(fn) + ": the cos / sin tables must cover every kv position "
+                                  "(rope_max_pos >= the plan's longest kv length)");
+  return ATTN_OK;
+}
+
 // The few-row tensor-core kernel takes this decode shape.
 bool decode_tc_shape(const attn_plan_t* plan, int32_t layout) {
   const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
@@ -270,14 +342,8 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q, const
                                       layout, kv_indptr, kv_indices, last_page_len, dtype, o,
                                       dev_ws, dev_bytes, "attn_decode_run_rope");
   if (s != ATTN_OK) return s;
-  if (!rope_cos || !rope_sin)
-    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_rope: null cos / sin table");
-  if ((reinterpret_cast<uintptr_t>(rope_cos) | reinterpret_cast<uintptr_t>(rope_sin)) & 15u)
-    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_rope: cos / sin tables must be 16-byte aligned");
-  if (rope_max_pos < plan->max_kv_len)
-    return fail(ATTN_ERR_INVALID_ARG,
-                "attn_decode_run_rope: the cos / sin tables must cover every kv position "
-                "(rope_max_pos >= the plan's longest kv length)");
+  s = check_rope(plan, rope_cos, rope_sin, rope_max_pos, "attn_decode_run_rope");
+  if (s != ATTN_OK) return s;
   if (!decode_tc_shape(plan, layout))
     return fail(ATTN_ERR_UNSUPPORTED,
                 "attn_decode_run_rope: fused RoPE needs the HND layout, page_size % 16 == 0 "
@@ -302,47 +368,13 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
                               const int32_t* last_page_len, int32_t dtype, int32_t causal,
                               float sm_scale, void* o, float* lse, void* dev_ws,
                               size_t dev_bytes, void* stream) {
-  attn_status_t s = check_plan_common(plan, ATTN_MODE_APPEND, q, k_pool, v_pool, num_pages,
-                                      layout, kv_indptr, kv_indices, last_page_len, dtype, o,
-                                      dev_ws, dev_bytes, "attn_append_run");
+  attn_status_t s = check_append(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout,
+                                 kv_indptr, kv_indices, last_page_len, dtype, causal, o,
+                                 dev_ws, dev_bytes, "attn_append_run");
   if (s != ATTN_OK) return s;
-  if ((causal ? 1 : 0) != plan->causal)
-    return fail(ATTN_ERR_INVALID_ARG, "attn_append_run: causal differs from the plan's");
-  if (plan->batch > 0 && !qo_indptr)
-    return fail(ATTN_ERR_INVALID_ARG, "attn_append_run: qo_indptr is NULL");
-  if (layout != ATTN_LAYOUT_HND)
-    return fail(ATTN_ERR_UNSUPPORTED, "attn_append_run: only the HND layout is implemented");
-  if (plan->page_size % 16 != 0)
-    return fail(ATTN_ERR_UNSUPPORTED, "attn_append_run: page_size must be a multiple of 16");
   if (plan->batch == 0 || plan->total_qo == 0) return ATTN_OK;
-  AppendArgs a;
-  std::memset(&a, 0, sizeof a);
-  a.q = q;
-  a.qo_indptr = qo_indptr;
-  a.k_pool = k_pool;
-  a.v_pool = v_pool;
-  a.num_pages = num_pages;
-  a.kv_indptr = kv_indptr;
-  a.kv_indices = kv_indices;
-  a.last_page_len = last_page_len;
-  a.o = o;
-  a.lse = lse;
-  a.ws = ws_view(*plan, dev_ws);
-  a.num_ctas = plan->num_ctas;
-  a.num_units = plan->num_units;
-  a.num_split_items = plan->num_split_items;
-  a.dtype = dtype;
-  a.page_size = plan->page_size;
-  a.num_qo_heads = plan->num_qo_heads;
-  a.num_kv_heads = plan->num_kv_heads;
-  a.group = plan->num_qo_heads / plan->num_kv_heads;
-  a.q_tile = plan->q_tile;
-  a.tile_tokens = kTileRows / a.group;
-  a.rows_per_item = plan->rows_per_item;
-  a.total_qo = plan->total_qo;
-  a.max_qo_len = plan->max_qo_len;
-  a.causal = plan->causal;
-  a.sm_scale = sm_scale;
+  AppendArgs a = append_args(plan, q, qo_indptr, k_pool, v_pool, num_pages, kv_indptr,
+                             kv_indices, last_page_len, dtype, sm_scale, o, lse, dev_ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const char* msg = "";
   if (few_row_rows(a.group, a.max_qo_len) != 0) {
@@ -373,6 +405,42 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
     e = launch_split_merge(m, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: merge kernel launch");
   }
+  return ATTN_OK;
+}
+
+attn_status_t attn_append_run_rope(const attn_plan_t* plan, const void* q,
+                                   const int32_t* qo_indptr, const void* k_pool,
+                                   const void* v_pool, int64_t num_pages, int32_t layout,
+                                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* last_page_len, int32_t dtype,
+                                   int32_t causal, float sm_scale, const float* rope_cos,
+                                   const float* rope_sin, int64_t rope_max_pos, void* o,
+                                   float* lse, void* dev_ws, size_t dev_bytes, void* stream) {
+  attn_status_t s = check_append(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout,
+                                 kv_indptr, kv_indices, last_page_len, dtype, causal, o,
+                                 dev_ws, dev_bytes, "attn_append_run_rope");
+  if (s != ATTN_OK) return s;
+  s = check_rope(plan, rope_cos, rope_sin, rope_max_pos, "attn_append_run_rope");
+  if (s != ATTN_OK) return s;
+  if (plan->min_kv_minus_qo < 0)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "attn_append_run_rope: a request has fewer kv tokens than queries, so a "
+                "query would sit before position 0");
+  const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
+  if (few_row_rows(group, plan->max_qo_len) == 0)
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "attn_append_run_rope: fused RoPE runs on short appends (group x the longest "
+                "query count <= 16)");
+  if (plan->batch == 0 || plan->total_qo == 0) return ATTN_OK;
+  AppendArgs a = append_args(plan, q, qo_indptr, k_pool, v_pool, num_pages, kv_indptr,
+                             kv_indices, last_page_len, dtype, sm_scale, o, lse, dev_ws);
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  a.rope_rows = rope_max_pos;
+  const char* msg = "";
+  cudaError_t e = launch_decode_tc(a, static_cast<cudaStream_t>(stream), &msg);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_append_run_rope: kernel launch");
   return ATTN_OK;
 }
 

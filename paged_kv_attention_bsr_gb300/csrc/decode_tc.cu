@@ -146,6 +146,7 @@ struct QRow {
   bool ok;
   int64_t orow;   // row of q / o / lse ([tokens, Hq] flattened)
   int64_t limit;  // last visible kv position
+  int64_t pos;    // the query's own position (RoPE): kv_len - qo_len + i
 };
 template <bool DEC, int R>
 __device__ __forceinline__ QRow qrow(const AppendArgs& a, const DGeo& g, int rho) {
@@ -154,12 +155,14 @@ __device__ __forceinline__ QRow qrow(const AppendArgs& a, const DGeo& g, int rho
     q.ok = true;
     q.orow = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * R + rho;
     q.limit = g.kv_len - 1;
+    q.pos = g.kv_len - 1;
   } else {
     const int tok = rho / a.group, hh = rho - tok * a.group;
     const int64_t qi = int64_t(g.t) * a.q_tile + tok;
     q.ok = qi < g.qo_len;
     q.orow = (g.qo_start + qi) * a.num_qo_heads + int64_t(g.hk) * a.group + hh;
     q.limit = a.causal ? g.kv_len - g.qo_len + qi : g.kv_len - 1;
+    q.pos = g.kv_len - g.qo_len + qi;
   }
   return q;
 }
@@ -463,14 +466,17 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     constexpr int kVec = R * 16;            // 16-byte pieces of the R rows
     constexpr int kPer = (kVec + 31) / 32;  // pieces per lane
     uint4 qr[kPer];
+    int32_t qpos[kPer];  // RoPE position of the piece's row (< 2^31); -1: not turned
     uint32_t ua = 0;
     auto fetch = [&](const DGeo& g) {
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const int idx = lane + 32 * j;
         qr[j] = make_uint4(0, 0, 0, 0);
+        qpos[j] = -1;
         if (idx < kVec) {
           const QRow q = qrow<DEC, R>(a, g, idx >> 4);
+          if (q.ok && q.pos >= 0 && q.pos < a.rope_rows) qpos[j] = int32_t(q.pos);
           if (q.ok)
             qr[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
                                                          q.orow * kHeadDim) +
@@ -512,9 +518,9 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
           oth.y = __shfl_xor_sync(0xffffffffu, val.y, 8);
           oth.z = __shfl_xor_sync(0xffffffffu, val.z, 8);
           oth.w = __shfl_xor_sync(0xffffffffu, val.w, 8);
-          if (idx < kVec) {
+          if (idx < kVec && qpos[j] >= 0) {
             const int ch = idx & 15;
-            const int64_t pos = g.kv_len - 1;
+            const int64_t pos = qpos[j];
             const float4* cp =
                 reinterpret_cast<const float4*>(a.rope_cos + pos * (kHeadDim / 2) + 8 * (ch & 7));
             const float4* sp =
@@ -1065,6 +1071,15 @@ cudaError_t launch_dt(const DecodeTcParams& prm, int rows, int grid, cudaStream_
       case 2: return launch_k<BF16, 2, true, true>(prm, grid, stream);
       case 4: return launch_k<BF16, 4, true, true>(prm, grid, stream);
       default: return launch_k<BF16, 8, true, true>(prm, grid, stream);
+    }
+  }
+  if (prm.a.rope_cos) {  // short append with fused RoPE
+    switch (rows) {
+      case 1: return launch_k<BF16, 1, false, true>(prm, grid, stream);
+      case 2: return launch_k<BF16, 2, false, true>(prm, grid, stream);
+      case 4: return launch_k<BF16, 4, false, true>(prm, grid, stream);
+      case 8: return launch_k<BF16, 8, false, true>(prm, grid, stream);
+      default: return launch_k<BF16, 16, false, true>(prm, grid, stream);
     }
   }
   if (!prm.a.qo_indptr) {

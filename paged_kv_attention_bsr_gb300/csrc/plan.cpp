@@ -124,6 +124,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   items.reserve(size_t(batch) * num_kv_heads);
   int64_t max_qo_len = decode ? 1 : 0;
   int64_t max_kv_len = 0;
+  int64_t min_kv_minus_qo = INT64_MAX;  // over requests with kv tokens
   for (int32_t r = 0; r < batch; ++r) {
     const int64_t n_pages = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
     if (n_pages < 0) {
@@ -153,6 +154,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         return ATTN_ERR_INVALID_ARG;
       }
     }
+    if (kv_len > 0) min_kv_minus_qo = std::min(min_kv_minus_qo, kv_len - qo_len);
     const int64_t tiles = decode ? 1 : (qo_len + q_tile - 1) / q_tile;
     for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
       for (int64_t t = 0; t < tiles; ++t) {
@@ -369,6 +371,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   const int32_t shape[6] = {page_size, num_qo_heads, num_kv_heads, head_dim, p.causal, num_ctas};
   p.fingerprint = fnv1a(h, shape, sizeof shape);
   p.max_kv_len = max_kv_len;
+  p.min_kv_minus_qo = min_kv_minus_qo;
   *plan = p;
   return ATTN_OK;
 }

@@ -78,6 +78,18 @@ def test_workspace_size_and_validation_without_gpu():
     assert C.lib.attn_decode_run_rope(*args(None, 100, 0)) == C.ERR_INVALID_ARG
     assert C.lib.attn_decode_run_rope(*args(fake, 47, 0)) == C.ERR_INVALID_ARG
     assert C.lib.attn_decode_run_rope(*args(fake, 48, 1)) == C.ERR_UNSUPPORTED
+    # fused RoPE append: kv_len >= qo_len, short appends only
+    def append_rope(qo, causal, cos=fake):
+        pa = C.plan(np.array(qo, np.int32), kvi, lpl, 16, 8, 2, 128, causal, 4, buf)
+        return pa, C.lib.attn_append_run_rope(
+            ctypes.byref(pa), fake, fake, fake, fake, 8, 0, fake, fake, fake, 1, int(causal),
+            ctypes.c_float(0.1), cos, cos, 48, fake, None, fake, 1 << 30, None)
+    pa, st = append_rope([0, 30, 31], False)  # request 0: 19 kv tokens, 30 queries
+    assert pa.min_kv_minus_qo == -11 and st == C.ERR_INVALID_ARG
+    pa, st = append_rope([0, 5, 6], True)  # group 4 x 5 queries = 20 rows > 16
+    assert pa.min_kv_minus_qo == 14 and st == C.ERR_UNSUPPORTED
+    _, st = append_rope([0, 2, 3], True, ctypes.c_void_p(260))  # misaligned tables
+    assert st == C.ERR_INVALID_ARG
     # the wait self-test validates before it launches anything
     assert C.lib.attn_wait_selftest(None, 1000, None) == C.ERR_INVALID_ARG
     assert C.lib.attn_wait_selftest(ctypes.c_void_p(256), 0, None) == C.ERR_INVALID_ARG

@@ -97,3 +97,54 @@ def test_rope_decode_full_size_uniform(oracle_mod):
     o, lse = run_rope(w, cos, sin)
     o_ref, lse_ref = oracle_rope(oracle_mod, w, cos, sin)
     assert_attn_close(o, lse, o_ref, lse_ref, "rope uniform full size")
+
+
+# Short appends (group x the longest query count <= 16) with fused RoPE:
+# query row i at position kv_len - qo_len + i, key j at position j.
+APPEND_CASES = [
+    # (P, Hq, Hk, dtype, qo_lens, extra kv, causal)
+    (16, 32, 8, torch.bfloat16, [1, 2, 4, 3, 4], [0, 5, 200, 17, 3000], True),
+    (16, 32, 8, torch.bfloat16, [4, 1, 2], [700, 0, 129], False),
+    (16, 16, 8, torch.bfloat16, [8, 5, 1], [100, 1000, 2], True),
+    (16, 8, 8, torch.float16, [16, 9], [300, 2000], True),
+    (128, 16, 2, torch.bfloat16, [2, 1, 2], [5000, 64, 127], False),
+    (32, 16, 2, torch.bfloat16, [2, 2], [-2, 40], False),  # request 0 has no kv
+]
+
+
+def run_append_rope(w, cos, sin, num_ctas=None):
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    c = w.cache
+    att = PagedAttention(w.num_qo_heads, w.num_kv_heads, 128, "append", max_batch=w.batch,
+                         max_total_qo=int(w.qo_indptr[-1]), num_ctas=num_ctas)
+    att.plan(c.kv_indptr, c.last_page_len, c.page_size, qo_indptr_h=w.qo_indptr,
+             causal=w.causal)
+    d = to_device(c)
+    q = w.q.cuda()
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
+    att.run(q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"], d["last_page_len"],
+            w.sm_scale, out=o, lse=lse, qo_indptr=torch.from_numpy(w.qo_indptr).cuda(),
+            rope=(torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda()))
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("case", range(len(APPEND_CASES)))
+@pytest.mark.parametrize("num_ctas", [1, None])
+def test_rope_short_append_parity(oracle_mod, case, num_ctas):
+    P, Hq, Hk, dtype, qo_lens, extra, causal = APPEND_CASES[case]
+    kv_lens = [max(q + e, 0) for q, e in zip(qo_lens, extra)]
+    pool = sum(-(-L // P) for L in kv_lens) + 9
+    w = synth.append_workload(f"ropeapp{case}", qo_lens, kv_lens, P, pool, Hq, Hk, dtype,
+                              seed=700 + case, causal=causal)
+    poison_unused_slots(w.cache)
+    cos, sin = synth.rope_tables(max(kv_lens))
+    c = w.cache
+    o_ref, lse_ref = oracle_mod.batch_attention_rope(
+        w.q, c.k_pool, c.v_pool, c.kv_indptr, c.kv_indices, c.last_page_len, P, Hq, Hk, 128,
+        oracle_dtype(oracle_mod, dtype), w.sm_scale, cos, sin, causal=causal,
+        qo_indptr=w.qo_indptr)
+    o, lse = run_append_rope(w, cos, sin, num_ctas)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"rope append case {case} ctas {num_ctas}")
