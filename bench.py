@@ -385,13 +385,14 @@ WORKLOAD_BENCH = {
     "causal_append": bench_causal_append,
     "shared_prefix": bench_shared_prefix,
     "rope_decode": bench_rope_decode,
+    "sparse_decode": lambda *a: bench_decode_workload("sparse_decode", *a),
 }
 
 
 def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
     out = {}
     for key in ("single_decode", "skewed_decode", "causal_append", "shared_prefix",
-                "rope_decode"):
+                "rope_decode", "sparse_decode"):
         name, res = WORKLOAD_BENCH[key](hbm_peak, bf16_peak, flush, steps, warmup)
         out[name] = res
     return out

@@ -131,8 +131,6 @@ attn_status_t check_append(const attn_plan_t* plan, const void* q, const int32_t
     return fail(ATTN_ERR_INVALID_ARG, std::string(fn) + ": qo_indptr is NULL");
   if (layout != ATTN_LAYOUT_HND)
     return fail(ATTN_ERR_UNSUPPORTED, std::string(fn) + ": only the HND layout is implemented");
-  if (plan->page_size % 16 != 0)
-    return fail(ATTN_ERR_UNSUPPORTED, std::string(fn) + ": page_size must be a multiple of 16");
   return ATTN_OK;
 }
 
@@ -190,8 +188,8 @@ attn_status_t check_rope(const attn_plan_t* plan, const float* rope_cos, const f
 // The few-row tensor-core kernel takes this decode shape.
 bool decode_tc_shape(const attn_plan_t* plan, int32_t layout) {
   const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
-  return group >= attn::kTensorDecodeGroup && (group & (group - 1)) == 0 &&
-         layout == ATTN_LAYOUT_HND && plan->page_size % 16 == 0;
+  return group >= attn::kTensorDecodeGroup && (group & (group - 1)) == 0 && group <= 8 &&
+         layout == ATTN_LAYOUT_HND;
 }
 
 }  // namespace
@@ -346,8 +344,8 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q, const
   if (s != ATTN_OK) return s;
   if (!decode_tc_shape(plan, layout))
     return fail(ATTN_ERR_UNSUPPORTED,
-                "attn_decode_run_rope: fused RoPE needs the HND layout, page_size % 16 == 0 "
-                "and 2, 4 or 8 query heads per kv head");
+                "attn_decode_run_rope: fused RoPE needs the HND layout and 2, 4 or 8 query "
+                "heads per kv head");
   if (plan->batch == 0) return ATTN_OK;
   AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, kv_indptr, kv_indices,
                                 last_page_len, dtype, sm_scale, o, lse, dev_ws);
@@ -387,6 +385,9 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
     if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: few-row kernel launch");
     return ATTN_OK;
   }
+  if (plan->page_size % 16 != 0)
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "attn_append_run: appends past 16 packed rows need page_size % 16 == 0");
   cudaError_t e = launch_append(a, st, &msg);
   if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
   if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: append kernel launch");

@@ -103,6 +103,7 @@ struct DecodeTcParams {
   float scale_log2;
   uint32_t idesc_s;
   uint32_t idesc_pv;
+  int32_t gather;  // K / V rows gathered 4 at a time (page_size % 16 != 0)
 };
 
 struct DGeo {
@@ -401,30 +402,60 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
   // ... (the grid is at most one CTA per SM; a plan may have more CTAs).
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
-    // Lane c fetches the page index of the tile's 16-row chunk c and issues
-    // that chunk's boxes. The next tile's indices are loaded before this
-    // tile's slots are awaited, so their latency hides behind the wait.
+    // Page sizes that are a multiple of 16: lane c fetches the page index of
+    // the tile's 16-row chunk c and issues that chunk's boxes. Other page
+    // sizes (down to one token per page, i.e. vector-sparse rows): lane c
+    // resolves tokens 4 c .. 4 c + 3 through the page table and gathers the
+    // four rows with one tile::gather4 per 64-dim half; a group's tokens past
+    // the unit's end repeat its last token (every row read lies in the pool;
+    // those columns are masked, and such V rows are zeroed before P.V). The
+    // next tile's rows are resolved before this tile's slots are awaited, so
+    // the index loads hide behind the wait.
     uint32_t uses = 0;
     const int P = a.page_size;
+    const bool gather = prm.gather != 0;
     bool ok = true;
-    auto chunk_row = [&](const DGeo& g, int i) -> int32_t {
-      const int64_t kvt = g.tok_begin + int64_t(i) * kTile + int64_t(lane) * kChunk;
-      if (kvt >= g.tok_end) return 0;
+    auto token_row = [&](const DGeo& g, int64_t kvt) -> int32_t {
       const int64_t pg = kvt / P;
       const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
       return int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
+    };
+    auto chunk_row = [&](const DGeo& g, int i) -> int32_t {
+      const int64_t kvt = g.tok_begin + int64_t(i) * kTile + int64_t(lane) * kChunk;
+      if (kvt >= g.tok_end) return 0;
+      return token_row(g, kvt);
+    };
+    // the 4 rows of lane c's group of tile i (gather mode)
+    auto group_rows = [&](const DGeo& g, int i, int32_t (&rw)[4]) {
+      const int64_t kv0 = g.tok_begin + int64_t(i) * kTile + 4 * lane;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t kvt = min(kv0 + u, g.tok_end - 1);
+        rw[u] = kv0 < g.tok_end ? token_row(g, kvt) : 0;
+      }
     };
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
       for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
            ++ui) {
         const DGeo g = decode_geo<DEC>(a, ui);
         if (g.ntiles == 0) continue;
-        int32_t row = chunk_row(g, 0);
+        int32_t row = 0, grow[4] = {0, 0, 0, 0};
+        if (gather)
+          group_rows(g, 0, grow);
+        else
+          row = chunk_row(g, 0);
         for (int i = 0; i < g.ntiles && ok; ++i) {
           const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
           const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
           const int nch = (ntt + kChunk - 1) / kChunk;
-          const int32_t row_next = i + 1 < g.ntiles ? chunk_row(g, i + 1) : 0;
+          const int ngr = (ntt + 3) / 4;  // gathered groups of 4 rows
+          int32_t row_next = 0, grow_next[4] = {0, 0, 0, 0};
+          if (i + 1 < g.ntiles) {
+            if (gather)
+              group_rows(g, i + 1, grow_next);
+            else
+              row_next = chunk_row(g, i + 1);
+          }
           for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
             const int slot = int(uses % kSlots);
             bool r = true;
@@ -436,18 +467,30 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
               break;
             }
             const uint32_t full = smem_u32(&bars.slot_full[slot]);
-            if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
-            __syncwarp();
-            if (lane < nch) {
-              const uint32_t dst =
-                  base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
-              const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
-                                       : static_cast<const void*>(&prm.tm_v);
-              tma_load_2d(dst, tm, 0, row, full);
-              tma_load_2d(dst + kHalf, tm, 64, row, full);
+            const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                     : static_cast<const void*>(&prm.tm_v);
+            if (gather) {
+              if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(ngr) * 4u * 256u);
+              __syncwarp();
+              if (lane < ngr) {
+                const uint32_t dst = base + kOffRing + slot * kTileBytes + uint32_t(lane) * 4u * 128u;
+                tma_gather4(dst, tm, 0, grow[0], grow[1], grow[2], grow[3], full);
+                tma_gather4(dst + kHalf, tm, 64, grow[0], grow[1], grow[2], grow[3], full);
+              }
+            } else {
+              if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
+              __syncwarp();
+              if (lane < nch) {
+                const uint32_t dst =
+                    base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
+                tma_load_2d(dst, tm, 0, row, full);
+                tma_load_2d(dst + kHalf, tm, 64, row, full);
+              }
             }
           }
           row = row_next;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) grow[u] = grow_next[u];
         }
       }
     // drain: every issued copy has landed before the CTA can exit
@@ -1114,8 +1157,8 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
            "and at most 16 packed query rows per item in append";
     return cudaErrorNotSupported;
   }
-  if (a.page_size % kChunk != 0) {
-    *msg = "attn: page_size must be a multiple of 16";
+  if (a.page_size <= 0) {
+    *msg = "attn: page_size must be positive";
     return cudaErrorNotSupported;
   }
   if (a.num_ctas <= 0 || a.num_units == 0) return cudaSuccess;
@@ -1126,8 +1169,9 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
   prm.scale_log2 = a.sm_scale * kLog2e;
   prm.idesc_s = make_idesc(bf16, false);
   prm.idesc_pv = make_idesc(bf16, true);
+  prm.gather = a.page_size % kChunk != 0 ? 1 : 0;
   if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
-                    &prm.tm_k, &prm.tm_v, msg))
+                    prm.gather ? 1u : uint32_t(kChunk), &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorInvalidValue;
   int sms = 0;
   cudaError_t e = current_sm_count(&sms);

@@ -126,6 +126,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+// Four rows r0..r3 (each one box: `c0` plus the box width) of a 2-D tensor
+// map whose box is one row high, gathered into 4 consecutive box rows of
+// shared memory.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t c0,
+                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

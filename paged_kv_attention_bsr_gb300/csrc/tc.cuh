@@ -210,9 +210,11 @@ inline uint32_t make_idesc(bool bf16, bool b_mn_major) {
 // The paged K and V pools as 2-D tensors [pages * kv heads * page_size, 128]
 // with 16-row x 64-column boxes and the 128-byte swizzle. Returns false when
 // the driver cannot describe them (message in *msg).
+// box_rows: 16 (16-row boxes within a page) or 1 (rows gathered one by one
+// with tile::gather4, for page sizes that are not a multiple of 16).
 inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
-                         int32_t num_kv_heads, int32_t page_size, bool bf16, CUtensorMap* tm_k,
-                         CUtensorMap* tm_v, const char** msg) {
+                         int32_t num_kv_heads, int32_t page_size, bool bf16, uint32_t box_rows,
+                         CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     *msg = "cuTensorMapEncodeTiled is unavailable";
@@ -228,7 +230,7 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
   for (int which = 0; which < 2; ++which) {
     const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
     const cuuint64_t strides[1] = {cuuint64_t(kHeadDim) * 2};
-    const cuuint32_t box[2] = {64u, cuuint32_t(kTcChunk)};
+    const cuuint32_t box[2] = {64u, box_rows};
     const cuuint32_t es[2] = {1, 1};
     CUtensorMap* tm = which == 0 ? tm_k : tm_v;
     void* ptr = const_cast<void*>(which == 0 ? k_pool : v_pool);
@@ -245,23 +247,25 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
 // encode_kv_maps, remembering the last pools described on this thread (a
 // serving loop runs over the same pools step after step).
 inline bool make_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
-                         int32_t num_kv_heads, int32_t page_size, bool bf16, CUtensorMap* tm_k,
-                         CUtensorMap* tm_v, const char** msg) {
+                         int32_t num_kv_heads, int32_t page_size, bool bf16, uint32_t box_rows,
+                         CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
   struct Key {
     const void *k, *v;
     int64_t pages;
     int32_t heads, page_size, bf16;
+    uint32_t box_rows;
   };
-  thread_local Key last = {nullptr, nullptr, -1, 0, 0, 0};
+  thread_local Key last = {nullptr, nullptr, -1, 0, 0, 0, 0};
   thread_local CUtensorMap last_k, last_v;
-  const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16 ? 1 : 0};
+  const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16 ? 1 : 0, box_rows};
   if (key.k == last.k && key.v == last.v && key.pages == last.pages && key.heads == last.heads &&
-      key.page_size == last.page_size && key.bf16 == last.bf16) {
+      key.page_size == last.page_size && key.bf16 == last.bf16 && key.box_rows == last.box_rows) {
     *tm_k = last_k;
     *tm_v = last_v;
     return true;
   }
-  if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16, tm_k, tm_v, msg))
+  if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16, box_rows, tm_k,
+                      tm_v, msg))
     return false;
   last = key;
   last_k = *tm_k;

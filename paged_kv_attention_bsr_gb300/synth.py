@@ -183,6 +183,18 @@ def uniform_gqa_decode(seed: int = SEED_BASE + 2, batch: int = 64,
     return w
 
 
+def vector_sparse_decode(seed: int = SEED_BASE + 6, batch: int = 64,
+                         pool_pages: int = 200000) -> Workload:
+    """The uniform GQA decode batch (B = 64, Hq = 32, Hk = 8, bf16,
+    kv_len ~ U[1024, 4096]) stored at page_size 1: every token is its own
+    page, drawn without replacement from a shuffled pool of 200000 one-token
+    pages (vector-level sparsity, the BSR format at block size 1)."""
+    rng = np.random.default_rng(seed)
+    kv_lens = rng.integers(1024, 4096, size=batch, endpoint=True)
+    return decode_workload("vector_sparse_decode_b64_h32kv8_p1_bf16", kv_lens, 1, pool_pages,
+                           32, 8, torch.bfloat16, seed)
+
+
 def skewed_lengths(rng: np.random.Generator, n_long=4, n_short=124):
     short = np.floor(np.exp(rng.normal(math.log(512.0), 0.75, size=n_short)))
     short = np.clip(short, 16, 4096).astype(np.int64)
@@ -285,4 +297,5 @@ WORKLOADS = {
     "skewed_decode": skewed_gqa_decode,
     "shared_prefix": shared_prefix_decode,
     "causal_append": causal_append,
+    "sparse_decode": vector_sparse_decode,
 }
