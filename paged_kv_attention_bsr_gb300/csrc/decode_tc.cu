@@ -71,7 +71,15 @@ constexpr int kOffQ = 0;
 // lanes of rows 32-127 are never read)
 constexpr int kOffRopeCos = kOffQ + 32 * 128;
 constexpr int kOffRopeSin = kOffRopeCos + 8 * 64 * 4;
-static_assert(kOffRopeSin + 8 * 64 * 4 <= kOffQ + kTcHalf, "RoPE offset rows fit the spare query rows");
+static_assert(kOffRopeSin + 8 * 64 * 4 <= kOffQ + 64 * 128, "RoPE offset rows fit query rows 32-63");
+// Gathered rows: the page index of each token of a tile (128 int32), copied
+// kIdxDepth tiles ahead into a ring of kIdxDepth + 1 slots (the slot being
+// read is never the one being filled) in query-tile rows 64-127 of the
+// lower half.
+constexpr int kIdxDepth = 4;
+constexpr int kIdxSlots = kIdxDepth + 1;
+constexpr int kOffIdxRing = kOffQ + 64 * 128;
+static_assert(kOffIdxRing + kIdxSlots * kTcTile * 4 <= kOffQ + kTcHalf, "index ring fits the spare query rows");
 constexpr int kOffRing = kTileBytes;
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
 constexpr int kOffHand = kOffBar + 256;         // softmax -> epilogue row state
@@ -403,14 +411,15 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
     // Page sizes that are a multiple of 16: lane c fetches the page index of
-    // the tile's 16-row chunk c and issues that chunk's boxes. Other page
-    // sizes (down to one token per page, i.e. vector-sparse rows): lane c
-    // resolves tokens 4 c .. 4 c + 3 through the page table and gathers the
-    // four rows with one tile::gather4 per 64-dim half; a group's tokens past
-    // the unit's end repeat its last token (every row read lies in the pool;
-    // those columns are masked, and such V rows are zeroed before P.V). The
-    // next tile's rows are resolved before this tile's slots are awaited, so
-    // the index loads hide behind the wait.
+    // the tile's 16-row chunk c and issues that chunk's boxes; the next
+    // tile's indices are loaded before this tile's slots are awaited. Other
+    // page sizes (down to one token per page, i.e. vector-sparse rows): lane
+    // c gathers the rows of tokens 4 c .. 4 c + 3 with one tile::gather4 per
+    // 64-dim half; a group's tokens past the unit's end repeat its last token
+    // (every row read lies in the pool; those columns are masked, and such V
+    // rows are zeroed before P.V). Their page indices are copied kIdxDepth
+    // tiles ahead with cp.async into a shared ring (each lane its own 16
+    // bytes per tile), so no index load waits on the critical path.
     uint32_t uses = 0;
     const int P = a.page_size;
     const bool gather = prm.gather != 0;
@@ -425,14 +434,42 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
       if (kvt >= g.tok_end) return 0;
       return token_row(g, kvt);
     };
-    // the 4 rows of lane c's group of tile i (gather mode)
-    auto group_rows = [&](const DGeo& g, int i, int32_t (&rw)[4]) {
+    // gather mode: (page, slot) of lane c's tokens kv0 + u of tile i, u < 4,
+    // clamped to the unit's last token (positions < 2^31: 32-bit division)
+    const uint32_t idx_lane = base + kOffIdxRing + uint32_t(lane) * 16u;
+    auto for_group = [&](const DGeo& g, int i, auto&& f) {
       const int64_t kv0 = g.tok_begin + int64_t(i) * kTile + 4 * lane;
+      uint32_t pg = uint32_t(kv0) / uint32_t(P), sl = uint32_t(kv0) - pg * uint32_t(P);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int64_t kvt = min(kv0 + u, g.tok_end - 1);
-        rw[u] = kv0 < g.tok_end ? token_row(g, kvt) : 0;
+        if (u > 0 && kv0 + u < g.tok_end && ++sl == uint32_t(P)) {
+          sl = 0;
+          ++pg;
+        }
+        f(u, pg, sl);
       }
+    };
+    // copy tile i's page indices into ring slot i % kIdxSlots (one commit
+    // group per call, empty past the unit's tiles)
+    auto idx_issue = [&](const DGeo& g, int i) {
+      if (i < g.ntiles && g.tok_begin + int64_t(i) * kTile + 4 * lane < g.tok_end)
+        for_group(g, i, [&](int u, uint32_t pg, uint32_t) {
+          cp_async4(idx_lane + uint32_t(i % kIdxSlots) * (kTile * 4) + 4u * u,
+                    a.kv_indices + g.page_base + pg);
+        });
+      cp_async_commit();
+    };
+    // the 4 pool rows of lane c's tokens of tile i (its indices have landed)
+    auto group_rows = [&](const DGeo& g, int i, int32_t (&rw)[4]) {
+      if (g.tok_begin + int64_t(i) * kTile + 4 * lane >= g.tok_end) {
+        rw[0] = rw[1] = rw[2] = rw[3] = 0;
+        return;
+      }
+      const uint8_t* ring = gbase + kOffIdxRing + lane * 16 + (i % kIdxSlots) * (kTile * 4);
+      for_group(g, i, [&](int u, uint32_t, uint32_t sl) {
+        const int64_t phys = *reinterpret_cast<const int32_t*>(ring + 4 * u);
+        rw[u] = int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
+      });
     };
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
       for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
@@ -440,21 +477,23 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
         const DGeo g = decode_geo<DEC>(a, ui);
         if (g.ntiles == 0) continue;
         int32_t row = 0, grow[4] = {0, 0, 0, 0};
-        if (gather)
-          group_rows(g, 0, grow);
-        else
+        if (gather) {
+          for (int j = 0; j < kIdxDepth; ++j) idx_issue(g, j);
+        } else {
           row = chunk_row(g, 0);
+        }
         for (int i = 0; i < g.ntiles && ok; ++i) {
           const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
           const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
           const int nch = (ntt + kChunk - 1) / kChunk;
           const int ngr = (ntt + 3) / 4;  // gathered groups of 4 rows
-          int32_t row_next = 0, grow_next[4] = {0, 0, 0, 0};
-          if (i + 1 < g.ntiles) {
-            if (gather)
-              group_rows(g, i + 1, grow_next);
-            else
-              row_next = chunk_row(g, i + 1);
+          int32_t row_next = 0;
+          if (gather) {
+            idx_issue(g, i + kIdxDepth);
+            cp_async_wait<kIdxDepth>();  // tile i's indices have landed
+            group_rows(g, i, grow);
+          } else if (i + 1 < g.ntiles) {
+            row_next = chunk_row(g, i + 1);
           }
           for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
             const int slot = int(uses % kSlots);
@@ -489,11 +528,10 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
             }
           }
           row = row_next;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) grow[u] = grow_next[u];
         }
       }
     // drain: every issued copy has landed before the CTA can exit
+    cp_async_wait<0>();  // this lane's index copies (they always complete)
     if (lane == 0) {
       for (uint32_t sl = 0; sl < uint32_t(kSlots) && sl < uses; ++sl) {
         const uint32_t last = uses - 1 - ((uses - 1 - sl) % kSlots);
