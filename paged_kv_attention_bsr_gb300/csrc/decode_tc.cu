@@ -43,6 +43,7 @@
 #include <cuda_fp16.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -422,7 +423,6 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     // bytes per tile), so no index load waits on the critical path.
     uint32_t uses = 0;
     const int P = a.page_size;
-    const bool gather = prm.gather != 0;
     bool ok = true;
     auto token_row = [&](const DGeo& g, int64_t kvt) -> int32_t {
       const int64_t pg = kvt / P;
@@ -471,65 +471,73 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
         rw[u] = int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
       });
     };
-    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
-      for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
-           ++ui) {
-        const DGeo g = decode_geo<DEC>(a, ui);
-        if (g.ntiles == 0) continue;
-        int32_t row = 0, grow[4] = {0, 0, 0, 0};
-        if (gather) {
-          for (int j = 0; j < kIdxDepth; ++j) idx_issue(g, j);
-        } else {
-          row = chunk_row(g, 0);
-        }
-        for (int i = 0; i < g.ntiles && ok; ++i) {
-          const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
-          const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
-          const int nch = (ntt + kChunk - 1) / kChunk;
-          const int ngr = (ntt + 3) / 4;  // gathered groups of 4 rows
-          int32_t row_next = 0;
-          if (gather) {
-            idx_issue(g, i + kIdxDepth);
-            cp_async_wait<kIdxDepth>();  // tile i's indices have landed
-            group_rows(g, i, grow);
-          } else if (i + 1 < g.ntiles) {
-            row_next = chunk_row(g, i + 1);
+    // one loop per mode, so that each keeps only its own code
+    auto produce = [&](auto gather_mode) {
+      constexpr bool G = decltype(gather_mode)::value;
+      for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+        for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+             ++ui) {
+          const DGeo g = decode_geo<DEC>(a, ui);
+          if (g.ntiles == 0) continue;
+          int32_t row = 0, grow[4] = {0, 0, 0, 0};
+          if constexpr (G) {
+            for (int j = 0; j < kIdxDepth; ++j) idx_issue(g, j);
+          } else {
+            row = chunk_row(g, 0);
           }
-          for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
-            const int slot = int(uses % kSlots);
-            bool r = true;
-            if (lane == 0)
-              r = mbar_wait(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u, err,
-                            ERR_WAIT_EMPTY);
-            if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) {
-              ok = false;
-              break;
-            }
-            const uint32_t full = smem_u32(&bars.slot_full[slot]);
-            const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
-                                     : static_cast<const void*>(&prm.tm_v);
-            if (gather) {
-              if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(ngr) * 4u * 256u);
-              __syncwarp();
-              if (lane < ngr) {
-                const uint32_t dst = base + kOffRing + slot * kTileBytes + uint32_t(lane) * 4u * 128u;
-                tma_gather4(dst, tm, 0, grow[0], grow[1], grow[2], grow[3], full);
-                tma_gather4(dst + kHalf, tm, 64, grow[0], grow[1], grow[2], grow[3], full);
-              }
+          for (int i = 0; i < g.ntiles && ok; ++i) {
+            const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+            const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+            int32_t row_next = 0;
+            if constexpr (G) {
+              idx_issue(g, i + kIdxDepth);
+              cp_async_wait<kIdxDepth>();  // tile i's indices have landed
+              group_rows(g, i, grow);
             } else {
-              if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
-              __syncwarp();
-              if (lane < nch) {
-                const uint32_t dst =
-                    base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
-                tma_load_2d(dst, tm, 0, row, full);
-                tma_load_2d(dst + kHalf, tm, 64, row, full);
+              if (i + 1 < g.ntiles) row_next = chunk_row(g, i + 1);
+            }
+            for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
+              const int slot = int(uses % kSlots);
+              bool r = true;
+              if (lane == 0)
+                r = mbar_wait(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u, err,
+                              ERR_WAIT_EMPTY);
+              if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) {
+                ok = false;
+                break;
+              }
+              const uint32_t full = smem_u32(&bars.slot_full[slot]);
+              const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                       : static_cast<const void*>(&prm.tm_v);
+              const uint32_t sdst = base + kOffRing + slot * kTileBytes;
+              if constexpr (G) {
+                const int ngr = (ntt + 3) / 4;  // gathered groups of 4 rows
+                if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(ngr) * 4u * 256u);
+                __syncwarp();
+                if (lane < ngr) {
+                  const uint32_t dst = sdst + uint32_t(lane) * 4u * 128u;
+                  tma_gather4(dst, tm, 0, grow[0], grow[1], grow[2], grow[3], full);
+                  tma_gather4(dst + kHalf, tm, 64, grow[0], grow[1], grow[2], grow[3], full);
+                }
+              } else {
+                const int nch = (ntt + kChunk - 1) / kChunk;
+                if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
+                __syncwarp();
+                if (lane < nch) {
+                  const uint32_t dst = sdst + uint32_t(lane) * kChunk * 128u;
+                  tma_load_2d(dst, tm, 0, row, full);
+                  tma_load_2d(dst + kHalf, tm, 64, row, full);
+                }
               }
             }
+            row = row_next;
           }
-          row = row_next;
         }
-      }
+    };
+    if (prm.gather)
+      produce(std::true_type{});
+    else
+      produce(std::false_type{});
     // drain: every issued copy has landed before the CTA can exit
     cp_async_wait<0>();  // this lane's index copies (they always complete)
     if (lane == 0) {
@@ -557,7 +565,8 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
         qpos[j] = -1;
         if (idx < kVec) {
           const QRow q = qrow<DEC, R>(a, g, idx >> 4);
-          if (q.ok && q.pos >= 0 && q.pos < a.rope_rows) qpos[j] = int32_t(q.pos);
+          if constexpr (ROPE)
+            if (q.ok && q.pos >= 0 && q.pos < a.rope_rows) qpos[j] = int32_t(q.pos);
           if (q.ok)
             qr[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
                                                          q.orow * kHeadDim) +
