@@ -175,11 +175,11 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
  *   dev_ws     : the workspace given to attn_plan (holds the plan tables)
  * Supported: head_dim 128, group = num_qo_heads / num_kv_heads in 1..8,
  * any page_size >= 1, both layouts, fp16 and bf16. Groups 2, 4 and 8 with
- * the HND layout and page_size a multiple of 16 run on the tensor-core
- * (tcgen05) decode kernel (the group's query rows replicated over 32 MMA
- * rows, 128-token K/V tiles gathered by TMA), followed by a merge kernel for
- * split items; every other shape runs on a CUDA-core streaming kernel that
- * merges split items itself.
+ * the HND layout run on the tensor-core (tcgen05) decode kernel at any page
+ * size (the group's query rows replicated over 32 MMA rows; 128-token K/V
+ * tiles loaded by TMA in 16-row boxes when page_size % 16 == 0, else row by
+ * row with gathers, down to one token per page); every other shape runs on a
+ * CUDA-core streaming kernel. Both merge split items inside the kernel.
  * Errors: INVALID_ARG (plan mode/shape mismatch, null pointers),
  * UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA (launch failure).
  */
@@ -218,7 +218,7 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q,
  * values differ from direct rows by a few fp32 ulps.
  *   other arguments    : as attn_decode_run
  * Supported: the shapes attn_decode_run runs on the tensor-core kernel (HND,
- * page_size % 16 == 0, 2, 4 or 8 query heads per kv head); others return
+ * 2, 4 or 8 query heads per kv head, any page size); others return
  * UNSUPPORTED.
  * Errors: as attn_decode_run; INVALID_ARG for missing, misaligned or too
  * short tables.
@@ -241,8 +241,8 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q,
  *   other arguments                  : as attn_append_run
  * Supported: the short appends the few-row tensor-core kernel runs (group x
  * the longest query count <= 16, e.g. speculative or multi-token decode, or
- * the n generations of a shared prefix; HND, page_size % 16 == 0). Longer
- * appends return UNSUPPORTED.
+ * the n generations of a shared prefix; HND, any page size). Longer appends
+ * return UNSUPPORTED.
  * Errors: as attn_append_run and attn_decode_run_rope; INVALID_ARG if a
  * request with kv tokens has kv_len < qo_len (a query would sit before
  * position 0).
@@ -265,8 +265,10 @@ attn_status_t attn_append_run_rope(const attn_plan_t* plan, const void* q,
  *   qo_indptr  : device int32[batch+1], equal to the plan's host copy
  *   other arguments as attn_decode_run; o is [total_qo, num_qo_heads, head_dim]
  *   and lse float[total_qo, num_qo_heads].
- * Supported: head_dim 128, bf16 or fp16, HND layout, page_size a multiple of
- * 16, group in {1, 2, 4, 8, 16}.
+ * Supported: head_dim 128, bf16 or fp16, HND layout, group in {1, 2, 4, 8,
+ * 16}. Short appends (group x the longest query count <= 16) run on the
+ * few-row tensor-core kernel at any page size; longer ones need page_size a
+ * multiple of 16 (UNSUPPORTED otherwise).
  * Errors: as attn_decode_run.
  */
 attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,

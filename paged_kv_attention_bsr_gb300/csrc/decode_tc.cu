@@ -28,7 +28,9 @@
 // end-aligned limit (token i of qo_len sees kv positions <= kv_len - qo_len + i).
 //
 // Warps (160 threads, one CTA per SM): 0 softmax; 1 TMA producer of the K/V
-// ring (six 32 KB slots, 16-row boxes gathered by page index); 2 TMEM
+// ring (six 32 KB slots; 16-row boxes by page index when the page size is a
+// multiple of 16, else rows gathered four at a time, down to one token per
+// page); 2 TMEM
 // allocation and the MMAs (one thread: S of tile k+1 runs under the softmax
 // of tile k, S double-buffered in TMEM); 3 query loader (plain loads of the
 // next unit's R query rows into registers, stored into the swizzled query
@@ -37,6 +39,9 @@
 // epilogue warp reads one unit's O, sums the copies, writes the output and
 // merges split items, the softmax warp is already on the next unit's tiles;
 // the softmax hands over each row's max and sum through shared memory.
+// With rotary position embedding fused in (288 threads), the query loader
+// turns each query row at its position, and warps 5-8 turn every K tile in
+// shared memory between its TMA landing and the S MMA.
 // Every wait is bounded; TMEM is freed on every path.
 #include <cuda.h>
 #include <cuda_bf16.h>

@@ -155,7 +155,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
 int append_ctas_per_sm();
 // Few-row tensor-core kernel: items of at most kFewRowMax packed query rows
 // (decode with qo_indptr == NULL: the group's heads; a short append: its
-// tokens x heads), HND pools with page_size % 16 == 0; merges split items
+// tokens x heads), HND pools of any page size; merges split items
 // itself. few_row_rows gives the rows per item it runs with (a power of two
 // >= group x max_qo_len), or 0 if the shape needs more than kFewRowMax.
 constexpr int kFewRowMax = 16;
