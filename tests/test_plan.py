@@ -209,3 +209,20 @@ def test_plan_rejects_bad_input(bad):
         C.plan(qo, kv_indptr, last, P, Hq, Hk, D, causal, 16, buf)
     assert ei.value.status == want
     assert C.last_error()
+
+
+@pytest.mark.parametrize("decode", [True, False])
+def test_plan_length_summaries(decode):
+    """max_kv_len and min_kv_minus_qo (what the RoPE entry points check
+    against) follow from the page tables: kv_len = (n - 1) P + last."""
+    rng = np.random.default_rng(20260011 if decode else 20260012)
+    for _ in range(40):
+        kv_indptr, last, P, Hq, Hk, ctas, qo, causal = _random_case(rng, decode)
+        p, _, _ = _lib_plan(kv_indptr, last, P, Hq, Hk, ctas, qo, causal)
+        n = np.diff(kv_indptr.astype(np.int64))
+        kv_len = np.where(n > 0, (n - 1) * P + last, 0)
+        qo_len = np.ones_like(kv_len) if qo is None else np.diff(qo.astype(np.int64))
+        assert p.max_kv_len == (int(kv_len.max()) if len(kv_len) else 0)
+        has_kv = kv_len > 0
+        want = int((kv_len - qo_len)[has_kv].min()) if has_kv.any() else np.iinfo(np.int64).max
+        assert p.min_kv_minus_qo == want
