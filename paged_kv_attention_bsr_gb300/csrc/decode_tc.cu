@@ -48,7 +48,6 @@
 #include <cuda_fp16.h>
 
 #include <cstring>
-#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -358,6 +357,97 @@ __device__ __forceinline__ void rope_key4(uint2& x, uint2& y, float4 cb, float4 
   y = make_uint2(pack2<BF16>(yr0.x, yr0.y), pack2<BF16>(yr1.x, yr1.y));
 }
 
+// Producer of gathered rows (page sizes that are not a multiple of 16): lane
+// c gathers the rows of tokens 4 c .. 4 c + 3 of each 128-token tile with one
+// tile::gather4 per 64-dim half; a group's tokens past the unit's end repeat
+// its last token (every row read lies in the pool; those columns are
+// masked, and such V rows are zeroed before P.V). Each lane's page indices
+// are copied kIdxDepth tiles ahead with cp.async into a shared ring (its own
+// 16 bytes per tile), so no index load waits on the critical path. Kept out
+// of line: the kernel body (nine warps' loops) stays as compact as without
+// this mode.
+template <bool DEC>
+__device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bars, uint32_t base,
+                                            const uint8_t* gbase, int lane,
+                                            volatile int32_t* err, uint32_t& uses, bool& ok) {
+  const AppendArgs& a = prm.a;
+  const int P = a.page_size;
+  // (page, slot) of lane c's tokens kv0 + u of tile i, u < 4, clamped to the
+  // unit's last token (positions < 2^31: 32-bit division)
+  const uint32_t idx_lane = base + kOffIdxRing + uint32_t(lane) * 16u;
+  auto for_group = [&](const DGeo& g, int i, auto&& f) {
+    const int64_t kv0 = g.tok_begin + int64_t(i) * kTile + 4 * lane;
+    uint32_t pg = uint32_t(kv0) / uint32_t(P), sl = uint32_t(kv0) - pg * uint32_t(P);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (u > 0 && kv0 + u < g.tok_end && ++sl == uint32_t(P)) {
+        sl = 0;
+        ++pg;
+      }
+      f(u, pg, sl);
+    }
+  };
+  // copy tile i's page indices into ring slot i % kIdxSlots (one commit
+  // group per call, empty past the unit's tiles)
+  auto idx_issue = [&](const DGeo& g, int i) {
+    if (i < g.ntiles && g.tok_begin + int64_t(i) * kTile + 4 * lane < g.tok_end)
+      for_group(g, i, [&](int u, uint32_t pg, uint32_t) {
+        cp_async4(idx_lane + uint32_t(i % kIdxSlots) * (kTile * 4) + 4u * u,
+                  a.kv_indices + g.page_base + pg);
+      });
+    cp_async_commit();
+  };
+  // the 4 pool rows of lane c's tokens of tile i (its indices have landed)
+  auto group_rows = [&](const DGeo& g, int i, int32_t (&rw)[4]) {
+    if (g.tok_begin + int64_t(i) * kTile + 4 * lane >= g.tok_end) {
+      rw[0] = rw[1] = rw[2] = rw[3] = 0;
+      return;
+    }
+    const uint8_t* ring = gbase + kOffIdxRing + lane * 16 + (i % kIdxSlots) * (kTile * 4);
+    for_group(g, i, [&](int u, uint32_t, uint32_t sl) {
+      const int64_t phys = *reinterpret_cast<const int32_t*>(ring + 4 * u);
+      rw[u] = int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
+    });
+  };
+  for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+    for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+         ++ui) {
+      const DGeo g = decode_geo<DEC>(a, ui);
+      if (g.ntiles == 0) continue;
+      int32_t grow[4] = {0, 0, 0, 0};
+      for (int j = 0; j < kIdxDepth; ++j) idx_issue(g, j);
+      for (int i = 0; i < g.ntiles && ok; ++i) {
+        const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+        const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+        const int ngr = (ntt + 3) / 4;  // gathered groups of 4 rows
+        idx_issue(g, i + kIdxDepth);
+        cp_async_wait<kIdxDepth>();  // tile i's indices have landed
+        group_rows(g, i, grow);
+        for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
+          const int slot = int(uses % kSlots);
+          bool r = true;
+          if (lane == 0)
+            r = mbar_wait(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u, err,
+                          ERR_WAIT_EMPTY);
+          if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bars.slot_full[slot]);
+          if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(ngr) * 4u * 256u);
+          __syncwarp();
+          if (lane < ngr) {
+            const uint32_t dst = base + kOffRing + slot * kTileBytes + uint32_t(lane) * 4u * 128u;
+            const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                     : static_cast<const void*>(&prm.tm_v);
+            tma_gather4(dst, tm, 0, grow[0], grow[1], grow[2], grow[3], full);
+            tma_gather4(dst + kHalf, tm, 64, grow[0], grow[1], grow[2], grow[3], full);
+          }
+        }
+      }
+    }
+}
+
 template <bool BF16, int R, bool DEC, bool ROPE>
 __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
@@ -418,89 +508,32 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     // ------------------------------------------------------------ TMA producer
     // Page sizes that are a multiple of 16: lane c fetches the page index of
     // the tile's 16-row chunk c and issues that chunk's boxes; the next
-    // tile's indices are loaded before this tile's slots are awaited. Other
-    // page sizes (down to one token per page, i.e. vector-sparse rows): lane
-    // c gathers the rows of tokens 4 c .. 4 c + 3 with one tile::gather4 per
-    // 64-dim half; a group's tokens past the unit's end repeat its last token
-    // (every row read lies in the pool; those columns are masked, and such V
-    // rows are zeroed before P.V). Their page indices are copied kIdxDepth
-    // tiles ahead with cp.async into a shared ring (each lane its own 16
-    // bytes per tile), so no index load waits on the critical path.
+    // tile's indices are loaded before this tile's slots are awaited, so
+    // their latency hides behind the wait. Other page sizes: produce_gather.
     uint32_t uses = 0;
-    const int P = a.page_size;
     bool ok = true;
-    auto token_row = [&](const DGeo& g, int64_t kvt) -> int32_t {
-      const int64_t pg = kvt / P;
-      const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
-      return int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
-    };
-    auto chunk_row = [&](const DGeo& g, int i) -> int32_t {
-      const int64_t kvt = g.tok_begin + int64_t(i) * kTile + int64_t(lane) * kChunk;
-      if (kvt >= g.tok_end) return 0;
-      return token_row(g, kvt);
-    };
-    // gather mode: (page, slot) of lane c's tokens kv0 + u of tile i, u < 4,
-    // clamped to the unit's last token (positions < 2^31: 32-bit division)
-    const uint32_t idx_lane = base + kOffIdxRing + uint32_t(lane) * 16u;
-    auto for_group = [&](const DGeo& g, int i, auto&& f) {
-      const int64_t kv0 = g.tok_begin + int64_t(i) * kTile + 4 * lane;
-      uint32_t pg = uint32_t(kv0) / uint32_t(P), sl = uint32_t(kv0) - pg * uint32_t(P);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (u > 0 && kv0 + u < g.tok_end && ++sl == uint32_t(P)) {
-          sl = 0;
-          ++pg;
-        }
-        f(u, pg, sl);
-      }
-    };
-    // copy tile i's page indices into ring slot i % kIdxSlots (one commit
-    // group per call, empty past the unit's tiles)
-    auto idx_issue = [&](const DGeo& g, int i) {
-      if (i < g.ntiles && g.tok_begin + int64_t(i) * kTile + 4 * lane < g.tok_end)
-        for_group(g, i, [&](int u, uint32_t pg, uint32_t) {
-          cp_async4(idx_lane + uint32_t(i % kIdxSlots) * (kTile * 4) + 4u * u,
-                    a.kv_indices + g.page_base + pg);
-        });
-      cp_async_commit();
-    };
-    // the 4 pool rows of lane c's tokens of tile i (its indices have landed)
-    auto group_rows = [&](const DGeo& g, int i, int32_t (&rw)[4]) {
-      if (g.tok_begin + int64_t(i) * kTile + 4 * lane >= g.tok_end) {
-        rw[0] = rw[1] = rw[2] = rw[3] = 0;
-        return;
-      }
-      const uint8_t* ring = gbase + kOffIdxRing + lane * 16 + (i % kIdxSlots) * (kTile * 4);
-      for_group(g, i, [&](int u, uint32_t, uint32_t sl) {
-        const int64_t phys = *reinterpret_cast<const int32_t*>(ring + 4 * u);
-        rw[u] = int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
-      });
-    };
-    // one loop per mode, so that each keeps only its own code
-    auto produce = [&](auto gather_mode) {
-      constexpr bool G = decltype(gather_mode)::value;
+    if (prm.gather) {
+      produce_gather<DEC>(prm, bars, base, gbase, lane, err, uses, ok);
+    } else {
+      const int P = a.page_size;
+      auto chunk_row = [&](const DGeo& g, int i) -> int32_t {
+        const int64_t kvt = g.tok_begin + int64_t(i) * kTile + int64_t(lane) * kChunk;
+        if (kvt >= g.tok_end) return 0;
+        const int64_t pg = kvt / P;
+        const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+        return int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
+      };
       for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
         for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
              ++ui) {
           const DGeo g = decode_geo<DEC>(a, ui);
           if (g.ntiles == 0) continue;
-          int32_t row = 0, grow[4] = {0, 0, 0, 0};
-          if constexpr (G) {
-            for (int j = 0; j < kIdxDepth; ++j) idx_issue(g, j);
-          } else {
-            row = chunk_row(g, 0);
-          }
+          int32_t row = chunk_row(g, 0);
           for (int i = 0; i < g.ntiles && ok; ++i) {
             const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
             const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
-            int32_t row_next = 0;
-            if constexpr (G) {
-              idx_issue(g, i + kIdxDepth);
-              cp_async_wait<kIdxDepth>();  // tile i's indices have landed
-              group_rows(g, i, grow);
-            } else {
-              if (i + 1 < g.ntiles) row_next = chunk_row(g, i + 1);
-            }
+            const int nch = (ntt + kChunk - 1) / kChunk;
+            const int32_t row_next = i + 1 < g.ntiles ? chunk_row(g, i + 1) : 0;
             for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
               const int slot = int(uses % kSlots);
               bool r = true;
@@ -512,37 +545,21 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
                 break;
               }
               const uint32_t full = smem_u32(&bars.slot_full[slot]);
-              const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
-                                       : static_cast<const void*>(&prm.tm_v);
-              const uint32_t sdst = base + kOffRing + slot * kTileBytes;
-              if constexpr (G) {
-                const int ngr = (ntt + 3) / 4;  // gathered groups of 4 rows
-                if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(ngr) * 4u * 256u);
-                __syncwarp();
-                if (lane < ngr) {
-                  const uint32_t dst = sdst + uint32_t(lane) * 4u * 128u;
-                  tma_gather4(dst, tm, 0, grow[0], grow[1], grow[2], grow[3], full);
-                  tma_gather4(dst + kHalf, tm, 64, grow[0], grow[1], grow[2], grow[3], full);
-                }
-              } else {
-                const int nch = (ntt + kChunk - 1) / kChunk;
-                if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
-                __syncwarp();
-                if (lane < nch) {
-                  const uint32_t dst = sdst + uint32_t(lane) * kChunk * 128u;
-                  tma_load_2d(dst, tm, 0, row, full);
-                  tma_load_2d(dst + kHalf, tm, 64, row, full);
-                }
+              if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
+              __syncwarp();
+              if (lane < nch) {
+                const uint32_t dst =
+                    base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
+                const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                         : static_cast<const void*>(&prm.tm_v);
+                tma_load_2d(dst, tm, 0, row, full);
+                tma_load_2d(dst + kHalf, tm, 64, row, full);
               }
             }
             row = row_next;
           }
         }
-    };
-    if (prm.gather)
-      produce(std::true_type{});
-    else
-      produce(std::false_type{});
+    }
     // drain: every issued copy has landed before the CTA can exit
     cp_async_wait<0>();  // this lane's index copies (they always complete)
     if (lane == 0) {
