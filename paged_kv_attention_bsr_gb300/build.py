@@ -25,7 +25,8 @@ def nvcc() -> str:
 
 
 def _flags(src: str):
-    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", INCLUDE]
+    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-semantic-interposition",
+              "-I", CSRC, "-I", INCLUDE]
     if src.endswith(".cu"):
         return common + ARCH + ["-lineinfo", "--expt-relaxed-constexpr"]
     return common

@@ -59,9 +59,31 @@ PlanLayout plan_layout(int32_t num_ctas, int64_t num_units, int64_t num_split,
 
 namespace {
 
+// An item and its request's geometry (copied into each of its units).
 struct Item {
   int32_t r, hk, t, n;
+  int32_t page_base, kv_len, qo_start, qo_len;
 };
+
+// Per-thread scratch reused across calls (a plan runs every step). One
+// thread_local object, bound to a reference once per call: in a shared
+// library every access to a thread_local may otherwise go through a TLS
+// lookup call.
+struct Scratch {
+  std::vector<Item> items;
+  std::vector<int64_t> bounds;   // floor(c W / C), c = 0 .. C (decode cut)
+  std::vector<Unit> gen;         // units in generation order
+  std::vector<int32_t> gen_cta;  // and their CTA and item
+  std::vector<int32_t> gen_item;
+  std::vector<int64_t> load;
+  std::vector<int32_t> n_units, split_of, merge_indptr, next, work_indptr, at;
+  std::vector<int4> merge_items;
+  std::vector<Unit> units;       // CTA order (append)
+};
+Scratch& scratch() {
+  thread_local Scratch s;
+  return s;
+}
 
 uint64_t fnv1a(uint64_t h, const void* data, size_t bytes) {
   const unsigned char* p = static_cast<const unsigned char*>(data);
@@ -118,8 +140,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
     *msg = "attn_plan: qo_indptr must start at 0 (q rows are indexed from the tensor start)";
     return ATTN_ERR_INVALID_ARG;
   }
-  // scratch reused across calls on this thread (a plan runs every step)
-  thread_local std::vector<Item> items;
+  Scratch& sc = scratch();
+  std::vector<Item>& items = sc.items;
   items.clear();
   items.reserve(size_t(batch) * num_kv_heads);
   int64_t max_qo_len = decode ? 1 : 0;
@@ -164,7 +186,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
           vis = std::min<int64_t>(kv_len, std::max<int64_t>(0, kv_len - qo_len + last_row + 1));
         }
         const int64_t n = (vis + page_size - 1) / page_size;
-        items.push_back({r, hk, int32_t(t), int32_t(n)});
+        items.push_back({r, hk, int32_t(t), int32_t(n), kv_indptr[r], int32_t(kv_len),
+                         decode ? r : qo_indptr[r], int32_t(qo_len)});
       }
     }
   }
@@ -174,7 +197,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   int64_t W = 0;
   for (const Item& it : items) W += it.n + kAlpha;
   const int64_t C = num_ctas;
-  thread_local std::vector<int64_t> bounds;  // floor(c W / C), c = 0 .. C (decode cut)
+  std::vector<int64_t>& bounds = sc.bounds;
   if (decode) {
     // floor(c W / C) by a running quotient and remainder (one division)
     bounds.resize(size_t(C) + 1);
@@ -193,15 +216,43 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   const int64_t* const bnd = bounds.data();
   auto bound = [bnd](int64_t c) -> int64_t { return bnd[c]; };
 
-  struct U {
-    Unit u;
-    int32_t cta;
-    int32_t item;
+  // units in generation order (decode: already CTA order), with their CTA
+  // and item, and the request's geometry filled in
+  std::vector<Unit>& gen = sc.gen;
+  std::vector<int32_t>& gen_cta = sc.gen_cta;
+  std::vector<int32_t>& gen_item = sc.gen_item;
+  // at most one unit per item plus one per CTA boundary (either cut)
+  const size_t max_units = items.size() + size_t(C);
+  if (gen.size() < max_units) {
+    gen.resize(max_units);
+    gen_cta.resize(max_units);
+    gen_item.resize(max_units);
+  }
+  size_t num_units = 0;
+  bool overflow = false;
+  auto emit = [&](const Item& it, size_t k, int64_t p0, int64_t p1, int64_t cta) {
+    if (num_units >= max_units) {
+      overflow = true;
+      return;
+    }
+    Unit& u = gen[num_units];
+    u.r = it.r;
+    u.hk = it.hk;
+    u.t = it.t;
+    u.p0 = int32_t(p0);
+    u.p1 = int32_t(p1);
+    u.slot = -1;
+    u.split = -1;
+    u.page_base = it.page_base;
+    u.kv_len = it.kv_len;
+    u.qo_start = it.qo_start;
+    u.qo_len = it.qo_len;
+    u.pad = 0;
+    gen_cta[num_units] = int32_t(cta);
+    gen_item[num_units] = int32_t(k);
+    ++num_units;
   };
-  thread_local std::vector<U> gen;  // units in generation order
-  gen.clear();
-  gen.reserve(items.size() + size_t(C));
-  thread_local std::vector<int64_t> load;
+  std::vector<int64_t>& load = sc.load;
   load.assign(size_t(C), 0);
 
   if (decode) {
@@ -216,16 +267,12 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int64_t lo = bound(cc), hi = bound(cc + 1);
         if (hi <= lo) continue;
         if (it.n == 0) {
-          if (lo <= base && base < hi)
-            gen.push_back({{it.r, it.hk, it.t, 0, 0, -1, -1, 0, 0, 0, 0, 0}, int32_t(cc),
-                           int32_t(k)});
+          if (lo <= base && base < hi) emit(it, k, 0, 0, cc);
           continue;
         }
         const int64_t p0 = std::max<int64_t>(0, lo - base - kAlpha);
         const int64_t p1 = std::min<int64_t>(it.n, hi - base - kAlpha);
-        if (p1 > p0)
-          gen.push_back({{it.r, it.hk, it.t, int32_t(p0), int32_t(p1), -1, -1, 0, 0, 0, 0, 0},
-                         int32_t(cc), int32_t(k)});
+        if (p1 > p0) emit(it, k, p0, p1, cc);
       }
       base += w;
     }
@@ -252,8 +299,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int64_t avail = cap - top.first;
         const int64_t need = kAlpha + (it.n - p);
         if (need <= avail) {
-          gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(it.n), -1, -1, 0, 0, 0, 0, 0}, c,
-                         int32_t(k)});
+          emit(it, k, p, it.n, c);
           load[size_t(c)] = top.first + need;
           if (load[size_t(c)] < cap) ready.push(Slot(load[size_t(c)], c));
           break;
@@ -261,18 +307,24 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int64_t take = avail - kAlpha;
         load[size_t(c)] = cap;  // this CTA is full either way
         if (take <= 0) continue;
-        gen.push_back({{it.r, it.hk, it.t, int32_t(p), int32_t(p + take), -1, -1, 0, 0, 0, 0, 0},
-                       c, int32_t(k)});
+        emit(it, k, p, p + take, c);
         p += take;
       }
     }
   }
 
+  if (overflow) {
+    *msg = "attn_plan: internal error (more units than items + CTAs)";
+    return ATTN_ERR_INVALID_ARG;
+  }
+
   // ---- split items, slots in (item, page) order
-  thread_local std::vector<int32_t> n_units, split_of, merge_indptr;
-  thread_local std::vector<int4> merge_items;
+  std::vector<int32_t>& n_units = sc.n_units;
+  std::vector<int32_t>& split_of = sc.split_of;
+  std::vector<int32_t>& merge_indptr = sc.merge_indptr;
+  std::vector<int4>& merge_items = sc.merge_items;
   n_units.assign(items.size(), 0);
-  for (const U& g : gen) n_units[size_t(g.item)]++;
+  for (size_t i = 0; i < num_units; ++i) n_units[size_t(gen_item[i])]++;
   split_of.assign(items.size(), -1);
   merge_indptr.assign(1, 0);
   merge_items.clear();
@@ -285,44 +337,36 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   const int32_t slots = merge_indptr.back();
   {
     // units of one item are generated in page order
-    thread_local std::vector<int32_t> next;
+    std::vector<int32_t>& next = sc.next;
     next.assign(merge_items.size(), 0);
-    for (U& g : gen) {
-      const int32_t sid = split_of[size_t(g.item)];
+    for (size_t i = 0; i < num_units; ++i) {
+      const int32_t sid = split_of[size_t(gen_item[i])];
       if (sid < 0) continue;
-      g.u.split = sid;
-      g.u.slot = merge_indptr[size_t(sid)] + next[size_t(sid)]++;
+      gen[i].split = sid;
+      gen[i].slot = merge_indptr[size_t(sid)] + next[size_t(sid)]++;
     }
   }
 
   // ---- per-CTA lists (generation order within a CTA)
-  thread_local std::vector<int32_t> work_indptr;
+  std::vector<int32_t>& work_indptr = sc.work_indptr;
   work_indptr.assign(size_t(C) + 1, 0);
-  for (const U& g : gen) work_indptr[size_t(g.cta) + 1]++;
+  for (size_t i = 0; i < num_units; ++i) work_indptr[size_t(gen_cta[i]) + 1]++;
   for (int64_t i = 0; i < C; ++i) work_indptr[i + 1] += work_indptr[i];
-  thread_local std::vector<Unit> units;
-  units.resize(gen.size());
-  if (decode) {  // the contiguous cut generates units in CTA order already
-    for (size_t i = 0; i < gen.size(); ++i) units[i] = gen[i].u;
-  } else {
-    thread_local std::vector<int32_t> at;
+  const Unit* unit_table = gen.data();  // decode: the cut emits units in CTA order
+  if (!decode) {
+    std::vector<Unit>& units = sc.units;
+    units.resize(num_units);
+    std::vector<int32_t>& at = sc.at;
     at.assign(work_indptr.begin(), work_indptr.end() - 1);
-    for (const U& g : gen) units[size_t(at[size_t(g.cta)]++)] = g.u;
-  }
-  for (Unit& u : units) {  // the request's geometry, for the kernels
-    const int32_t r = u.r;
-    const int64_t n_pages = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
-    u.page_base = kv_indptr[r];
-    u.kv_len = n_pages > 0 ? int32_t((n_pages - 1) * page_size + last_page_len[r]) : 0;
-    u.qo_start = decode ? r : qo_indptr[r];
-    u.qo_len = decode ? 1 : qo_indptr[r + 1] - qo_indptr[r];
+    for (size_t i = 0; i < num_units; ++i) units[size_t(at[size_t(gen_cta[i])]++)] = gen[i];
+    unit_table = units.data();
   }
   int64_t max_load = 0;
   for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, load[size_t(i)]);
 
   // ---- write tables
   const int64_t S = int64_t(merge_items.size());
-  const PlanLayout L = plan_layout(num_ctas, int64_t(units.size()), S, slots, rows_per_item,
+  const PlanLayout L = plan_layout(num_ctas, int64_t(num_units), S, slots, rows_per_item,
                                    head_dim);
   if (size_t(L.table_bytes) > host_bytes) {
     *msg = "attn_plan: pinned host workspace too small for the plan tables";
@@ -331,7 +375,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   char* hb = static_cast<char*>(host_tables);
   std::memset(hb, 0, size_t(L.table_bytes));
   std::memcpy(hb + L.off_work_indptr, work_indptr.data(), 4 * work_indptr.size());
-  if (!units.empty()) std::memcpy(hb + L.off_units, units.data(), sizeof(Unit) * units.size());
+  if (num_units) std::memcpy(hb + L.off_units, unit_table, sizeof(Unit) * num_units);
   std::memcpy(hb + L.off_merge_indptr, merge_indptr.data(), 4 * merge_indptr.size());
   if (S) std::memcpy(hb + L.off_merge_items, merge_items.data(), 16 * size_t(S));
 
@@ -348,7 +392,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   p.q_tile = q_tile;
   p.rows_per_item = rows_per_item;
   p.num_items = int32_t(items.size());
-  p.num_units = int32_t(units.size());
+  p.num_units = int32_t(num_units);
   p.num_split_items = int32_t(S);
   p.num_slots = slots;
   p.total_qo = decode ? batch : (qo_indptr[batch] - qo_indptr[0]);
