@@ -174,11 +174,11 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
  *   lse        : device float[batch, num_qo_heads] (out) or NULL
  *   dev_ws     : the workspace given to attn_plan (holds the plan tables)
  * Supported: head_dim 128, group = num_qo_heads / num_kv_heads in 1..8,
- * any page_size >= 1, both layouts, fp16 and bf16. Groups 2, 4 and 8 with
- * the HND layout run on the tensor-core (tcgen05) decode kernel at any page
- * size (the group's query rows replicated over 32 MMA rows; 128-token K/V
- * tiles loaded by TMA in 16-row boxes when page_size % 16 == 0, else row by
- * row with gathers, down to one token per page); every other shape runs on a
+ * any page_size >= 1, both layouts, fp16 and bf16. Groups 2, 4 and 8 run on
+ * the tensor-core (tcgen05) decode kernel at any page size and either layout
+ * (the group's query rows replicated over 32 MMA rows; 128-token K/V tiles
+ * loaded by TMA in 16-row boxes when page_size % 16 == 0, else row by row
+ * with gathers, down to one token per page); groups 1, 3, 5, 6 and 7 run on a
  * CUDA-core streaming kernel. Both merge split items inside the kernel.
  * Errors: INVALID_ARG (plan mode/shape mismatch, null pointers),
  * UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA (launch failure).
@@ -217,8 +217,8 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q,
  * in; fold such a factor into sm_scale instead) give other keys. The derived
  * values differ from direct rows by a few fp32 ulps.
  *   other arguments    : as attn_decode_run
- * Supported: the shapes attn_decode_run runs on the tensor-core kernel (HND,
- * 2, 4 or 8 query heads per kv head, any page size); others return
+ * Supported: the shapes attn_decode_run runs on the tensor-core kernel (2, 4
+ * or 8 query heads per kv head, any page size, either layout); others return
  * UNSUPPORTED.
  * Errors: as attn_decode_run; INVALID_ARG for missing, misaligned or too
  * short tables.

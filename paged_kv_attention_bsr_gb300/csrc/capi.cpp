@@ -77,7 +77,7 @@ namespace {
 
 // Arguments of the few-row tensor-core kernel for a decode plan.
 attn::AppendArgs decode_tc_args(const attn_plan_t* plan, const void* q, const void* k_pool,
-                                const void* v_pool, int64_t num_pages,
+                                const void* v_pool, int64_t num_pages, int32_t layout,
                                 const int32_t* kv_indptr, const int32_t* kv_indices,
                                 const int32_t* last_page_len, int32_t dtype, float sm_scale,
                                 void* o, float* lse, void* dev_ws) {
@@ -112,6 +112,7 @@ attn::AppendArgs decode_tc_args(const attn_plan_t* plan, const void* q, const vo
   a.sm_scale = sm_scale;
   a.rope_cos = nullptr;
   a.rope_sin = nullptr;
+  a.layout = layout;
   return a;
 }
 
@@ -189,7 +190,7 @@ attn_status_t check_rope(const attn_plan_t* plan, const float* rope_cos, const f
 bool decode_tc_shape(const attn_plan_t* plan, int32_t layout) {
   const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
   return group >= attn::kTensorDecodeGroup && (group & (group - 1)) == 0 && group <= 8 &&
-         layout == ATTN_LAYOUT_HND;
+         (layout == ATTN_LAYOUT_HND || layout == ATTN_LAYOUT_NHD);
 }
 
 }  // namespace
@@ -294,7 +295,7 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
     // Tensor-core decode: Q K^T and P V run as M = 128 MMAs over 128-token
     // tiles gathered by TMA, the softmax on one warp (query heads replicated
     // across the MMA rows so that each thread handles a slice of the tile).
-    const AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, kv_indptr,
+    const AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, layout, kv_indptr,
                                         kv_indices, last_page_len, dtype, sm_scale, o, lse,
                                         dev_ws);
     const char* msg = "";
@@ -344,11 +345,10 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q, const
   if (s != ATTN_OK) return s;
   if (!decode_tc_shape(plan, layout))
     return fail(ATTN_ERR_UNSUPPORTED,
-                "attn_decode_run_rope: fused RoPE needs the HND layout and 2, 4 or 8 query "
-                "heads per kv head");
+                "attn_decode_run_rope: fused RoPE needs 2, 4 or 8 query heads per kv head");
   if (plan->batch == 0) return ATTN_OK;
-  AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, kv_indptr, kv_indices,
-                                last_page_len, dtype, sm_scale, o, lse, dev_ws);
+  AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, layout, kv_indptr,
+                                kv_indices, last_page_len, dtype, sm_scale, o, lse, dev_ws);
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;
   a.rope_rows = rope_max_pos;

@@ -117,6 +117,7 @@ struct DecodeTcParams {
   uint32_t idesc_s;
   uint32_t idesc_pv;
   int32_t gather;  // K / V rows gathered 4 at a time (page_size % 16 != 0)
+  int32_t nhd;     // pools are NHD [pages, P, Hk, 128] (else HND [pages, Hk, P, 128])
 };
 
 struct DGeo {
@@ -406,7 +407,8 @@ __device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bar
     const uint8_t* ring = gbase + kOffIdxRing + lane * 16 + (i % kIdxSlots) * (kTile * 4);
     for_group(g, i, [&](int u, uint32_t, uint32_t sl) {
       const int64_t phys = *reinterpret_cast<const int32_t*>(ring + 4 * u);
-      rw[u] = int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
+      rw[u] = prm.nhd ? int32_t((phys * P + sl) * a.num_kv_heads + g.hk)
+                      : int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
     });
   };
   for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
@@ -444,6 +446,61 @@ __device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bar
             tma_gather4(dst + kHalf, tm, 64, grow[0], grow[1], grow[2], grow[3], full);
           }
         }
+      }
+    }
+}
+
+// Producer of 16-row boxes from NHD pools (page sizes that are a multiple of
+// 16): as the HND box producer, with a 3-D map [tokens, Hk, 128] whose box is
+// 16 tokens x 1 head x 64 dims, so the tile rows land as in HND. Kept out of
+// line like produce_gather.
+template <bool DEC>
+__device__ __noinline__ void produce_nhd_box(const DecodeTcParams& prm, Bars& bars, uint32_t base,
+                                             int lane, volatile int32_t* err, uint32_t& uses,
+                                             bool& ok) {
+  const AppendArgs& a = prm.a;
+  const int P = a.page_size;
+  // token row (phys * P + slot) of the tile's 16-row chunk c = lane
+  auto chunk_tok = [&](const DGeo& g, int i) -> int32_t {
+    const int64_t kvt = g.tok_begin + int64_t(i) * kTile + int64_t(lane) * kChunk;
+    if (kvt >= g.tok_end) return 0;
+    const int64_t pg = kvt / P;
+    const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+    return int32_t(phys * P + (kvt - pg * P));
+  };
+  for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+    for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
+         ++ui) {
+      const DGeo g = decode_geo<DEC>(a, ui);
+      if (g.ntiles == 0) continue;
+      int32_t tok = chunk_tok(g, 0);
+      for (int i = 0; i < g.ntiles && ok; ++i) {
+        const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+        const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+        const int nch = (ntt + kChunk - 1) / kChunk;
+        const int32_t tok_next = i + 1 < g.ntiles ? chunk_tok(g, i + 1) : 0;
+        for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
+          const int slot = int(uses % kSlots);
+          bool r = true;
+          if (lane == 0)
+            r = mbar_wait(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u, err,
+                          ERR_WAIT_EMPTY);
+          if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bars.slot_full[slot]);
+          if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
+          __syncwarp();
+          if (lane < nch) {
+            const uint32_t dst = base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
+            const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                     : static_cast<const void*>(&prm.tm_v);
+            tma_load_3d(dst, tm, 0, g.hk, tok, full);
+            tma_load_3d(dst + kHalf, tm, 64, g.hk, tok, full);
+          }
+        }
+        tok = tok_next;
       }
     }
 }
@@ -514,6 +571,8 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     bool ok = true;
     if (prm.gather) {
       produce_gather<DEC>(prm, bars, base, gbase, lane, err, uses, ok);
+    } else if (prm.nhd) {
+      produce_nhd_box<DEC>(prm, bars, base, lane, err, uses, ok);
     } else {
       const int P = a.page_size;
       auto chunk_row = [&](const DGeo& g, int i) -> int32_t {
@@ -1239,8 +1298,9 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
   prm.idesc_s = make_idesc(bf16, false);
   prm.idesc_pv = make_idesc(bf16, true);
   prm.gather = a.page_size % kChunk != 0 ? 1 : 0;
+  prm.nhd = a.layout == ATTN_LAYOUT_NHD ? 1 : 0;
   if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
-                    prm.gather ? 1u : uint32_t(kChunk), &prm.tm_k, &prm.tm_v, msg))
+                    prm.gather ? 1u : uint32_t(kChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorInvalidValue;
   int sms = 0;
   cudaError_t e = current_sm_count(&sms);

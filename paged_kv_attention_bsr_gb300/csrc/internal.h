@@ -147,6 +147,7 @@ struct AppendArgs {
   const float* rope_cos;
   const float* rope_sin;
   int64_t rope_rows;
+  int32_t layout;  // KV pool layout (few-row kernel): ATTN_LAYOUT_HND or ATTN_LAYOUT_NHD
 };
 // qo_indptr == NULL runs the kernel in decode mode (one query row per
 // request; q is [batch, Hq, D]). Returns cudaErrorNotSupported for shapes the

@@ -211,10 +211,14 @@ inline uint32_t make_idesc(bool bf16, bool b_mn_major) {
 // with 16-row x 64-column boxes and the 128-byte swizzle. Returns false when
 // the driver cannot describe them (message in *msg).
 // box_rows: 16 (16-row boxes within a page) or 1 (rows gathered one by one
-// with tile::gather4, for page sizes that are not a multiple of 16).
+// with tile::gather4, for page sizes that are not a multiple of 16). Rows are
+// the 256-byte (token, head) vectors: HND [pages, Hk, P, 128] and NHD
+// [pages, P, Hk, 128] pools are both [pages * Hk * P, 128] row arrays, and
+// 16-row boxes of one head in NHD take a 3-D map [tokens, Hk, 128] (box
+// 16 x 1 x 64), which lands the same 16 swizzled rows.
 inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
                          int32_t num_kv_heads, int32_t page_size, bool bf16, uint32_t box_rows,
-                         CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
+                         bool nhd, CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     *msg = "cuTensorMapEncodeTiled is unavailable";
@@ -227,15 +231,23 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
   }
   const CUtensorMapDataType dt =
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const bool three_d = nhd && box_rows > 1;
   for (int which = 0; which < 2; ++which) {
-    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
-    const cuuint64_t strides[1] = {cuuint64_t(kHeadDim) * 2};
-    const cuuint32_t box[2] = {64u, box_rows};
-    const cuuint32_t es[2] = {1, 1};
+    const cuuint64_t dims2[2] = {cuuint64_t(kHeadDim), rows};
+    const cuuint64_t strides2[1] = {cuuint64_t(kHeadDim) * 2};
+    const cuuint32_t box2[2] = {64u, box_rows};
+    const cuuint64_t dims3[3] = {cuuint64_t(kHeadDim), cuuint64_t(num_kv_heads),
+                                 cuuint64_t(num_pages) * page_size};
+    const cuuint64_t strides3[2] = {cuuint64_t(kHeadDim) * 2,
+                                    cuuint64_t(kHeadDim) * 2 * cuuint64_t(num_kv_heads)};
+    const cuuint32_t box3[3] = {64u, 1u, box_rows};
+    const cuuint32_t es[3] = {1, 1, 1};
     CUtensorMap* tm = which == 0 ? tm_k : tm_v;
     void* ptr = const_cast<void*>(which == 0 ? k_pool : v_pool);
-    if (enc(tm, dt, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (enc(tm, dt, three_d ? 3 : 2, ptr, three_d ? dims3 : dims2,
+            three_d ? strides3 : strides2, three_d ? box3 : box2, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       *msg = "cannot describe the KV pool for TMA";
       return false;
@@ -248,24 +260,27 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
 // serving loop runs over the same pools step after step).
 inline bool make_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
                          int32_t num_kv_heads, int32_t page_size, bool bf16, uint32_t box_rows,
-                         CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
+                         bool nhd, CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
   struct Key {
     const void *k, *v;
     int64_t pages;
     int32_t heads, page_size, bf16;
     uint32_t box_rows;
+    int32_t nhd;
   };
-  thread_local Key last = {nullptr, nullptr, -1, 0, 0, 0, 0};
+  thread_local Key last = {nullptr, nullptr, -1, 0, 0, 0, 0, 0};
   thread_local CUtensorMap last_k, last_v;
-  const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16 ? 1 : 0, box_rows};
+  const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16 ? 1 : 0, box_rows,
+                   nhd ? 1 : 0};
   if (key.k == last.k && key.v == last.v && key.pages == last.pages && key.heads == last.heads &&
-      key.page_size == last.page_size && key.bf16 == last.bf16 && key.box_rows == last.box_rows) {
+      key.page_size == last.page_size && key.bf16 == last.bf16 && key.box_rows == last.box_rows &&
+      key.nhd == last.nhd) {
     *tm_k = last_k;
     *tm_v = last_v;
     return true;
   }
-  if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16, box_rows, tm_k,
-                      tm_v, msg))
+  if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16, box_rows, nhd,
+                      tm_k, tm_v, msg))
     return false;
   last = key;
   last_k = *tm_k;

@@ -77,7 +77,10 @@ def test_workspace_size_and_validation_without_gpu():
                                    1 << 30, None)
     assert C.lib.attn_decode_run_rope(*args(None, 100, 0)) == C.ERR_INVALID_ARG
     assert C.lib.attn_decode_run_rope(*args(fake, 47, 0)) == C.ERR_INVALID_ARG
-    assert C.lib.attn_decode_run_rope(*args(fake, 48, 1)) == C.ERR_UNSUPPORTED
+    pr3 = C.plan(None, kvi, lpl, 16, 6, 2, 128, False, 4, buf)  # group 3: CUDA cores only
+    assert C.lib.attn_decode_run_rope(ctypes.byref(pr3), fake, fake, fake, 8, 0, fake, fake,
+                                      fake, 1, ctypes.c_float(0.1), fake, fake, 48, fake, None,
+                                      fake, 1 << 30, None) == C.ERR_UNSUPPORTED
     # fused RoPE append: kv_len >= qo_len, short appends only
     def append_rope(qo, causal, cos=fake):
         pa = C.plan(np.array(qo, np.int32), kvi, lpl, 16, 8, 2, 128, causal, 4, buf)

@@ -103,15 +103,16 @@ def test_decode_stale_pool_slots_are_never_used(oracle_mod, case):
         assert_attn_close(o, lse, o_ref, lse_ref, f"stale slots case {case} ctas {ctas}")
 
 
-@pytest.mark.parametrize("case", [0, 3, 5])
-def test_decode_nhd_layout(oracle_mod, case):
+@pytest.mark.parametrize("case", [0, 1, 3, 4, 5, 9])
+@pytest.mark.parametrize("num_ctas", [1, None])
+def test_decode_nhd_layout(oracle_mod, case, num_ctas):
     C, _ = _api()
     P, Hq, Hk, dtype, lens = SMALL_CASES[case]
     pool = sum(-(-L // P) for L in lens) + 11
     w = synth.decode_workload(f"nhd{case}", lens, P, pool, Hq, Hk, dtype, seed=300 + case)
     o_ref, lse_ref = oracle_full(oracle_mod, w)
-    o, lse, _ = run_decode(w, num_ctas=None, layout=C.LAYOUT_NHD)
-    assert_attn_close(o, lse, o_ref, lse_ref, "nhd")
+    o, lse, _ = run_decode(w, num_ctas=num_ctas, layout=C.LAYOUT_NHD)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"nhd case {case} ctas {num_ctas}")
 
 
 def test_decode_graph_replay_and_determinism(oracle_mod):

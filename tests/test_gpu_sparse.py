@@ -132,3 +132,15 @@ def test_sparse_rope_decode_parity(oracle_mod, P):
     o_ref, lse_ref = oracle_rope(oracle_mod, w, cos, sin)
     o, lse = run_rope(w, cos, sin)
     assert_attn_close(o, lse, o_ref, lse_ref, f"sparse rope P {P}")
+
+
+@pytest.mark.parametrize("case", [0, 3, 5])
+def test_sparse_decode_nhd_layout(oracle_mod, case):
+    """Gathered rows from an NHD pool [pages, P, Hk, 128]."""
+    from paged_kv_attention_bsr_gb300 import _capi as C
+    P, Hq, Hk, dtype, lens = CASES[case]
+    pool = sum(-(-L // P) for L in lens) + 13
+    w = synth.decode_workload(f"sparsenhd{case}", lens, P, pool, Hq, Hk, dtype, seed=930 + case)
+    o_ref, lse_ref = oracle_full(oracle_mod, w)
+    o, lse, _ = run_decode(w, layout=C.LAYOUT_NHD)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"sparse nhd case {case}")
