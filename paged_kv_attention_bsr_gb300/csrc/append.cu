@@ -735,7 +735,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
   }
   if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
                     kTcChunk, false, &prm.tm_k, &prm.tm_v, msg))
-    return cudaErrorInvalidValue;
+    return cudaErrorNotSupported;  // *msg says why
   // at most one CTA per SM (shared memory); extra plan CTAs are run in turn
   int sms = 0;
   cudaError_t e = current_sm_count(&sms);

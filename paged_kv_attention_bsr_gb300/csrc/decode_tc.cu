@@ -1301,7 +1301,7 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
   prm.nhd = a.layout == ATTN_LAYOUT_NHD ? 1 : 0;
   if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
                     prm.gather ? 1u : uint32_t(kChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
-    return cudaErrorInvalidValue;
+    return cudaErrorNotSupported;  // *msg says why
   int sms = 0;
   cudaError_t e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;

@@ -219,14 +219,15 @@ inline uint32_t make_idesc(bool bf16, bool b_mn_major) {
 inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
                          int32_t num_kv_heads, int32_t page_size, bool bf16, uint32_t box_rows,
                          bool nhd, CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) {
-    *msg = "cuTensorMapEncodeTiled is unavailable";
-    return false;
-  }
   const cuuint64_t rows = cuuint64_t(num_pages) * num_kv_heads * page_size;
   if (rows == 0 || rows > 0x7fffffffull) {
-    *msg = "pool too large for 32-bit TMA row coordinates";
+    *msg = "attn: the pool has no rows or more than 2^31 (page, head, slot) rows (32-bit TMA "
+           "row coordinates)";
+    return false;
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    *msg = "attn: cuTensorMapEncodeTiled is unavailable";
     return false;
   }
   const CUtensorMapDataType dt =
@@ -249,7 +250,7 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-      *msg = "cannot describe the KV pool for TMA";
+      *msg = "attn: cannot describe the KV pool for TMA";
       return false;
     }
   }

@@ -93,6 +93,12 @@ def test_workspace_size_and_validation_without_gpu():
     assert pa.min_kv_minus_qo == 14 and st == C.ERR_UNSUPPORTED
     _, st = append_rope([0, 2, 3], True, ctypes.c_void_p(260))  # misaligned tables
     assert st == C.ERR_INVALID_ARG
+    # a pool past 2^31 (page, head, slot) rows: UNSUPPORTED with the reason,
+    # found on the host before any CUDA call
+    huge = (1 << 31) // (2 * 16) + 1  # pages x Hk (2) x P (16) > 2^31
+    st = C.lib.attn_decode_run(ctypes.byref(pr), fake, fake, fake, huge, 0, fake, fake, fake, 1,
+                               ctypes.c_float(0.1), fake, None, fake, 1 << 30, None)
+    assert st == C.ERR_UNSUPPORTED and "2^31" in C.last_error()
     # the wait self-test validates before it launches anything
     assert C.lib.attn_wait_selftest(None, 1000, None) == C.ERR_INVALID_ARG
     assert C.lib.attn_wait_selftest(ctypes.c_void_p(256), 0, None) == C.ERR_INVALID_ARG
