@@ -1085,9 +1085,11 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
       // row, lane l on pairs 4 (l % 16) .. + 3. The angles are pos * theta_i,
       // so the cos / sin of row B + o follow from those of rows B and o by
       // the angle-sum identities. A lane's rows are B_h + 2 it (it < 8) for
-      // two bases B_h per tile: it keeps the 8 offset rows o = 2 it for its
-      // pairs in registers, and loads a tile's two base rows (512 B per
-      // half-warp) one tile ahead, so no table read waits on a tile.
+      // two bases B_h per tile: the 8 offset rows o = 2 it sit in shared
+      // memory (written once by the rope warps), and a lane loads a tile's
+      // two base rows (512 B per half-warp) one tile ahead, so no table read
+      // waits on a tile. The rotation itself runs on packed fp32x2 math in
+      // a rolled loop of two-row steps (code size matters with nine warps).
       const int wr = warp - kWarpRope0;
       const int hrow = lane >> 4, p0 = 4 * (lane & 15);
       const int kbyte = (((lane & 15) >> 1) << 4) | ((lane & 1) << 3);  // piece, byte in it
