@@ -113,3 +113,15 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "attn_oracle" not in text, f
+
+
+def test_rope_table_checks_in_the_binding():
+    """The binding rejects malformed cos / sin tables before calling the library."""
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    import torch
+    good = torch.zeros(10, 64, dtype=torch.float32)
+    for cos, sin in [(good.double(), good), (torch.zeros(10, 32), torch.zeros(10, 32)),
+                     (good, torch.zeros(11, 64)), (torch.zeros(64, 10).t(), good)]:
+        with pytest.raises(ValueError):
+            C._check_rope_tables(cos, sin)
+    C._check_rope_tables(good, good.clone())
