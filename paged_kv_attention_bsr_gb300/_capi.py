@@ -168,10 +168,28 @@ def plan(qo_indptr_h, kv_indptr_h, last_page_len_h, page_size, num_qo_heads, num
     return p
 
 
+def _check_sizes(p: Plan, q, k_pool, v_pool, o, lse, num_pages, rows):
+    """Tensor sizes and dtypes against the plan, before the library is called:
+    the kernels address the pools with the plan's heads and page size, so a
+    smaller pool would be read past its end."""
+    per_row = p.num_qo_heads * p.head_dim
+    need_kv = int(num_pages) * p.num_kv_heads * p.page_size * p.head_dim
+    if num_pages < 1 or k_pool.numel() < need_kv or v_pool.numel() < need_kv:
+        raise ValueError(f"k_pool / v_pool hold fewer than num_pages ({num_pages}) x "
+                         f"{p.num_kv_heads} heads x {p.page_size} slots x {p.head_dim} elements")
+    if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype or o.dtype != q.dtype:
+        raise ValueError("q, k_pool, v_pool and out must share one dtype")
+    if q.numel() < rows * per_row or o.numel() < rows * per_row:
+        raise ValueError(f"q / out need {rows} rows x {p.num_qo_heads} heads x {p.head_dim}")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() < rows * p.num_qo_heads):
+        raise ValueError(f"lse must be float32 with {rows} x {p.num_qo_heads} elements")
+
+
 def decode_run(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale, o,
                lse, dev_ws, layout=LAYOUT_HND, num_pages=None, stream=None):
     if num_pages is None:
         num_pages = k_pool.shape[0]
+    _check_sizes(p, q, k_pool, v_pool, o, lse, num_pages, p.batch)
     _check(lib.attn_decode_run(ctypes.byref(p), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                int(num_pages), layout, _ptr(kv_indptr), _ptr(kv_indices),
                                _ptr(last_page_len), dtype_code(q.dtype), float(sm_scale),
@@ -194,6 +212,7 @@ def decode_run_rope(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page
     _check_rope_tables(rope_cos, rope_sin)
     if num_pages is None:
         num_pages = k_pool.shape[0]
+    _check_sizes(p, q, k_pool, v_pool, o, lse, num_pages, p.batch)
     _check(lib.attn_decode_run_rope(ctypes.byref(p), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                     int(num_pages), layout, _ptr(kv_indptr), _ptr(kv_indices),
                                     _ptr(last_page_len), dtype_code(q.dtype), float(sm_scale),
@@ -207,6 +226,7 @@ def append_run(p: Plan, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices, las
                stream=None):
     if num_pages is None:
         num_pages = k_pool.shape[0]
+    _check_sizes(p, q, k_pool, v_pool, o, lse, num_pages, p.total_qo)
     _check(lib.attn_append_run(ctypes.byref(p), _ptr(q), _ptr(qo_indptr), _ptr(k_pool),
                                _ptr(v_pool), int(num_pages), layout, _ptr(kv_indptr),
                                _ptr(kv_indices), _ptr(last_page_len), dtype_code(q.dtype),
@@ -222,6 +242,7 @@ def append_run_rope(p: Plan, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices
     _check_rope_tables(rope_cos, rope_sin)
     if num_pages is None:
         num_pages = k_pool.shape[0]
+    _check_sizes(p, q, k_pool, v_pool, o, lse, num_pages, p.total_qo)
     _check(lib.attn_append_run_rope(ctypes.byref(p), _ptr(q), _ptr(qo_indptr), _ptr(k_pool),
                                     _ptr(v_pool), int(num_pages), layout, _ptr(kv_indptr),
                                     _ptr(kv_indices), _ptr(last_page_len), dtype_code(q.dtype),

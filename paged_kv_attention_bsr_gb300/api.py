@@ -113,13 +113,16 @@ def single_decode_with_kv_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
 
     q [num_qo_heads, head_dim], k / v [kv_len, num_kv_heads, head_dim] (the
     quick-start snippet's shapes); returns [num_qo_heads, head_dim]. The
-    contiguous cache is read in place as a BSR row of 16-token pages in the
-    NHD layout (pages 0..n-1 in order), so the balanced plan can split it
-    across SMs.
+    contiguous cache is read in place as a BSR row of pages in the NHD layout
+    (pages 0..n-1 in order), so the balanced plan can split it across SMs.
+    The page size is the largest power of two up to 16 that divides kv_len,
+    so the pages cover exactly the caller's tensors.
     """
     kv_len, Hk, D = k.shape
     Hq = q.shape[0]
     P = 16
+    while P > 1 and kv_len % P:
+        P //= 2
     n_pages = (kv_len + P - 1) // P
     key = (q.device, Hq, Hk, D)
     att = _single_cache.get(key)

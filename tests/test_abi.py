@@ -125,3 +125,29 @@ def test_rope_table_checks_in_the_binding():
         with pytest.raises(ValueError):
             C._check_rope_tables(cos, sin)
     C._check_rope_tables(good, good.clone())
+
+
+def test_run_size_checks_in_the_binding():
+    """Pools, q, out and lse too small for the plan are rejected before the
+    library is called (the kernels would read past a smaller pool)."""
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    import torch
+    _, host = C.workspace_size(4, 4, 8, 2, 128, 4)
+    p = C.plan(None, np.array([0, 2, 3], np.int32), np.array([5, 16], np.int32), 16, 8, 2, 128,
+               False, 4, np.zeros(host, np.uint8))
+    bf = torch.bfloat16
+    q = torch.zeros(2, 8, 128, dtype=bf)
+    pool = torch.zeros(3, 2, 16, 128, dtype=bf)
+    lse = torch.zeros(2, 8)
+    C._check_sizes(p, q, pool, pool, q, lse, 3, p.batch)  # consistent: no error
+    bad = [
+        (q, torch.zeros(3, 1, 16, 128, dtype=bf), pool, q, lse, 3),  # fewer heads
+        (q, pool, pool, q, lse, 4),                                   # pool smaller than num_pages
+        (q, pool.half(), pool, q, lse, 3),                            # dtype mismatch
+        (q[:1], pool, pool, q, lse, 3),                               # too few q rows
+        (q, pool, pool, q, lse.double(), 3),                          # lse dtype
+        (q, pool, pool, q, lse, 0),                                   # no pages
+    ]
+    for qq, kp, vp, oo, ll, n in bad:
+        with pytest.raises(ValueError):
+            C._check_sizes(p, qq, kp, vp, oo, ll, n, p.batch)
