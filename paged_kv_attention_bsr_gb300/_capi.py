@@ -254,6 +254,12 @@ def append_run_rope(p: Plan, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices
 
 def merge_states(o_a, lse_a, o_b, lse_b, o_out, lse_out, stream=None):
     n, h, d = o_a.shape
+    for t in (o_b, o_out):
+        if t.shape != o_a.shape or t.dtype != o_a.dtype:
+            raise ValueError("o_a, o_b and o_out must share shape [n, H, D] and dtype")
+    for t in (lse_a, lse_b, lse_out):
+        if tuple(t.shape) != (n, h) or t.dtype != torch.float32:
+            raise ValueError("lse_a, lse_b and lse_out must be float32 [n, H]")
     _check(lib.attn_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out),
                                  _ptr(lse_out), n, h, d, dtype_code(o_a.dtype), _stream(stream)))
 

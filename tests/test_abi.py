@@ -151,3 +151,14 @@ def test_run_size_checks_in_the_binding():
     for qq, kp, vp, oo, ll, n in bad:
         with pytest.raises(ValueError):
             C._check_sizes(p, qq, kp, vp, oo, ll, n, p.batch)
+
+
+def test_merge_shape_checks_in_the_binding():
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    import torch
+    o = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    l = torch.zeros(4, 2)
+    for args in [(o, l, o[:3], l, o, l), (o, l, o, l[:3], o, l), (o, l, o, l, o.half(), l),
+                 (o, l, o, l.double(), o, l)]:
+        with pytest.raises(ValueError):
+            C.merge_states(*args)
