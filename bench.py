@@ -300,9 +300,10 @@ def bench_causal_append(hbm_peak, bf16_peak, flush, steps, warmup):
 
 
 def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
-    """Prefix append (P = 128, once per prompt) + suffix decode + LSE merge,
-    next to the same logical KV as one flat P = 16 decode."""
-    from paged_kv_attention_bsr_gb300 import merge_state, synth
+    """Prefix append (P = 128, once per prompt) and suffix decode on two
+    streams (CascadeAttention) + LSE merge, next to the same logical KV as one
+    flat P = 16 decode."""
+    from paged_kv_attention_bsr_gb300 import synth
     from paged_kv_attention_bsr_gb300.api import PagedAttention
     from paged_kv_attention_bsr_gb300.synth import Workload
     w = synth.shared_prefix_decode()
@@ -311,24 +312,18 @@ def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
     dp, ds = dev_cache(pre), dev_cache(suf)
     pqo_h = w.extra["prefix_qo_indptr"]
     pqo = torch.from_numpy(pqo_h).cuda()
-    att_p = PagedAttention(32, 8, 128, "append", max_batch=w.extra["prompts"],
-                           max_total_qo=w.batch)
-    att_s = PagedAttention(32, 8, 128, "decode", max_batch=w.batch)
-    o_p, o_s, o_m = (torch.empty_like(q) for _ in range(3))
-    l_p, l_s, l_m = (torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
-                     for _ in range(3))
+    from paged_kv_attention_bsr_gb300.api import CascadeAttention
+    ca = CascadeAttention(32, 8, 128, max_prompts=w.extra["prompts"], max_batch=w.batch)
+    att_p, att_s = ca.prefix, ca.suffix
+    o_m = torch.empty_like(q)
+    l_m = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
 
     def plans():
-        att_p.plan(pre.kv_indptr, pre.last_page_len, pre.page_size, qo_indptr_h=pqo_h,
-                   causal=False)
-        att_s.plan(suf.kv_indptr, suf.last_page_len, suf.page_size)
+        ca.plan(pqo_h, pre.kv_indptr, pre.last_page_len, pre.page_size, suf.kv_indptr,
+                suf.last_page_len, suf.page_size)
 
     def runs():
-        att_p.run(q, dp["k_pool"], dp["v_pool"], dp["kv_indptr"], dp["kv_indices"],
-                  dp["last_page_len"], w.sm_scale, out=o_p, lse=l_p, qo_indptr=pqo)
-        att_s.run(q, ds["k_pool"], ds["v_pool"], ds["kv_indptr"], ds["kv_indices"],
-                  ds["last_page_len"], w.sm_scale, out=o_s, lse=l_s)
-        merge_state(o_p, l_p, o_s, l_s, out=o_m, lse_out=l_m)
+        ca.run(q, dp, ds, pqo, w.sm_scale, out=o_m, lse=l_m)
 
     step_ms, kern_ms = time_steps([plans, runs], steps, warmup, flush)
     kvb = 2 * 8 * 128 * 2
@@ -340,7 +335,8 @@ def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
            "kernel_us": k_s * 1e6, "step_us": float(np.mean(step_ms)) * 1e3,
            "GB/s": (b_pre + b_suf) / k_s / 1e9,
            "roofline_frac_hbm": (b_pre + b_suf) / k_s / 1e9 / hbm_peak,
-           "launches_per_step": 3 + (att_p.plan_info.num_split_items > 0)}
+           "launches_per_step": 3 + (att_p.plan_info.num_split_items > 0),
+           "streams": "prefix pass and suffix pass on two streams, merge after the join"}
     assert att_p.status() == 0 and att_s.status() == 0
     del dp, ds
     flat = synth.flat_layout_of_composable(w)
@@ -378,6 +374,118 @@ def bench_rope_decode(hbm_peak, bf16_peak, flush, steps, warmup):
     return w.name + "_rope", res
 
 
+def bench_rope_append(hbm_peak, bf16_peak, flush, steps, warmup):
+    """The causal append with LLaMA 3.1 RoPE fused into the append kernel
+    (keys cached un-rotated, turned in shared memory by the rope warps),
+    beside the same batch without RoPE."""
+    from paged_kv_attention_bsr_gb300 import synth
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    w = synth.causal_append()
+    c = w.cache
+    cos, sin = synth.rope_tables(int(c.kv_lens.max()))
+    rope = (torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda())
+    att = PagedAttention(w.num_qo_heads, w.num_kv_heads, 128, "append", max_batch=w.batch,
+                         max_total_qo=int(w.qo_indptr[-1]))
+    d = dev_cache(c)
+    q = w.q.cuda()
+    qo = torch.from_numpy(w.qo_indptr).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+
+    def plan_a():
+        att.plan(c.kv_indptr, c.last_page_len, 16, qo_indptr_h=w.qo_indptr, causal=True)
+
+    def run_rope():
+        att.run(q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"], d["last_page_len"],
+                w.sm_scale, out=o, lse=lse, qo_indptr=qo, rope=rope)
+
+    def run_plain():
+        att.run(q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"], d["last_page_len"],
+                w.sm_scale, out=o, lse=lse, qo_indptr=qo)
+
+    step_ms, kern_ms = time_steps([plan_a, run_rope], steps, warmup, flush)
+    assert att.status() == 0
+    _, kern_plain = time_steps([plan_a, run_plain], steps, warmup, flush)
+    fl = append_flops(w)
+    k_s = float(np.mean(kern_ms)) * 1e-3
+    res = {"kind": "append+rope", "flops": fl, "kernel_us": k_s * 1e6,
+           "step_us": float(np.mean(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
+           "roofline_frac_bf16": fl / k_s / 1e12 / bf16_peak,
+           "without_rope_kernel_us": float(np.mean(kern_plain)) * 1e3}
+    del d, att
+    torch.cuda.empty_cache()
+    return w.name + "_rope", res
+
+
+def bench_pod_mixed(hbm_peak, bf16_peak, flush, steps, warmup):
+    """POD-style: one batch of 16 causal prefill chunks and 64 decodes, run
+    as one plan and one persistent launch, beside the same batch run as two
+    launches (the prefill requests on the append kernel, the decode requests
+    on the decode kernel)."""
+    from paged_kv_attention_bsr_gb300 import synth
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    w = synth.pod_mixed_batch()
+    c = w.cache
+    d = dev_cache(c)
+    q = w.q.cuda()
+    qo = torch.from_numpy(w.qo_indptr).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+    att = PagedAttention(32, 8, 128, "append", max_batch=w.batch,
+                         max_total_qo=int(w.qo_indptr[-1]))
+
+    def plan_f():
+        att.plan(c.kv_indptr, c.last_page_len, 16, qo_indptr_h=w.qo_indptr, causal=True)
+
+    def run_f():
+        att.run(q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"], d["last_page_len"],
+                w.sm_scale, out=o, lse=lse, qo_indptr=qo)
+
+    step_ms, kern_ms = time_steps([plan_f, run_f], steps, warmup, flush)
+    assert att.status() == 0
+    fused_us = float(np.mean(kern_ms)) * 1e3
+    # the same requests as two batches: prefill (append kernel), decode (decode kernel)
+    wa = synth.sub_batch(w, w.extra["prefill"])
+    wd = synth.sub_batch(w, w.extra["decode"], as_decode=True)
+    da = {k: torch.from_numpy(getattr(wa.cache, k)).cuda()
+          for k in ("kv_indptr", "kv_indices", "last_page_len")}
+    dd = {k: torch.from_numpy(getattr(wd.cache, k)).cuda()
+          for k in ("kv_indptr", "kv_indices", "last_page_len")}
+    qa, qd = wa.q.cuda(), wd.q.cuda()
+    qoa = torch.from_numpy(wa.qo_indptr).cuda()
+    oa, od = torch.empty_like(qa), torch.empty_like(qd)
+    la = torch.empty(qa.shape[:-1], dtype=torch.float32, device="cuda")
+    ld = torch.empty(qd.shape[:-1], dtype=torch.float32, device="cuda")
+    att_a = PagedAttention(32, 8, 128, "append", max_batch=wa.batch,
+                           max_total_qo=int(wa.qo_indptr[-1]))
+    att_d = PagedAttention(32, 8, 128, "decode", max_batch=wd.batch)
+
+    def plans():
+        att_a.plan(wa.cache.kv_indptr, wa.cache.last_page_len, 16, qo_indptr_h=wa.qo_indptr,
+                   causal=True)
+        att_d.plan(wd.cache.kv_indptr, wd.cache.last_page_len, 16)
+
+    def runs():
+        att_a.run(qa, d["k_pool"], d["v_pool"], da["kv_indptr"], da["kv_indices"],
+                  da["last_page_len"], w.sm_scale, out=oa, lse=la, qo_indptr=qoa)
+        att_d.run(qd, d["k_pool"], d["v_pool"], dd["kv_indptr"], dd["kv_indices"],
+                  dd["last_page_len"], w.sm_scale, out=od, lse=ld)
+
+    _, kern_sep = time_steps([plans, runs], steps, warmup, flush)
+    assert att_a.status() == 0 and att_d.status() == 0
+    sep_us = float(np.mean(kern_sep)) * 1e3
+    fl = append_flops(wa)
+    kv_dec = int(wd.cache.kv_lens.sum()) * 2 * 8 * 128 * 2
+    res = {"kind": "pod", "prefill_flops": fl, "decode_kv_bytes": kv_dec,
+           "kernel_us": fused_us, "step_us": float(np.mean(step_ms)) * 1e3,
+           "separate_two_launches_kernel_us": sep_us, "fused_speedup": sep_us / fused_us,
+           "launches_per_step": 1 + (att.plan_info.num_split_items > 0),
+           "units": att.plan_info.num_units, "split_items": att.plan_info.num_split_items}
+    del d, att, att_a, att_d
+    torch.cuda.empty_cache()
+    return w.name, res
+
+
 WORKLOAD_BENCH = {
     "single_decode": lambda *a: bench_decode_workload("single_decode", *a),
     "skewed_decode": lambda *a: bench_decode_workload("skewed_decode", *a),
@@ -386,13 +494,15 @@ WORKLOAD_BENCH = {
     "shared_prefix": bench_shared_prefix,
     "rope_decode": bench_rope_decode,
     "sparse_decode": lambda *a: bench_decode_workload("sparse_decode", *a),
+    "pod_mixed": bench_pod_mixed,
+    "rope_append": bench_rope_append,
 }
 
 
 def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
     out = {}
     for key in ("single_decode", "skewed_decode", "causal_append", "shared_prefix",
-                "rope_decode", "sparse_decode"):
+                "rope_decode", "rope_append", "sparse_decode", "pod_mixed"):
         name, res = WORKLOAD_BENCH[key](hbm_peak, bf16_peak, flush, steps, warmup)
         out[name] = res
     return out
@@ -425,6 +535,161 @@ def cpu_oracle_baseline(w, threads):
             if (time.perf_counter() - t0) * threads >= 10.0 or passes >= 64:
                 break
     return (time.perf_counter() - t0) / passes, passes
+
+
+def _decode_oracle_job(w, odt):
+    """A callable that runs the fp64 oracle over requests [a, b) of a decode
+    workload."""
+    import oracle
+    c = w.cache
+
+    def job(rs):
+        if len(rs) == 0:
+            return
+        a, b = int(rs[0]), int(rs[-1]) + 1
+        oracle.batch_attention(w.q[a:b], c.k_pool, c.v_pool, c.kv_indptr[a:b + 1],
+                               c.kv_indices, c.last_page_len[a:b], c.page_size,
+                               w.num_qo_heads, w.num_kv_heads, w.head_dim, odt, w.sm_scale)
+    return job
+
+
+def _timed_pass(job, units, threads):
+    """Seconds for one pass of `job` over `units` split into `threads` chunks."""
+    chunks = np.array_split(np.asarray(units), threads)
+    t0 = time.perf_counter()
+    if threads == 1:
+        job(chunks[0])
+    else:
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(job, chunks))
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_per_workload(threads):
+    """The fp64 oracle as it stands on the host cores, per workload of the
+    pages: single-threaded and on `threads` threads (requests split across
+    threads). Workloads 1-4 run in full; the causal append runs on a fixed
+    seeded subset of (request, query head) pairs and is extrapolated by
+    unmasked FLOPs, and labelled so."""
+    import oracle
+    from paged_kv_attention_bsr_gb300 import synth
+    oracle.build()
+    out = {}
+    for key in ("single_decode", "uniform_decode", "skewed_decode"):
+        w = synth.WORKLOADS[key]()
+        odt = oracle.BF16 if w.dtype == torch.bfloat16 else oracle.F16
+        b = decode_bytes(w)
+        if w.batch >= threads:  # requests split across threads
+            job = _decode_oracle_job(w, odt)
+            units = np.arange(w.batch)
+        else:  # fewer requests than threads: (request, head) rows split across threads
+            c = w.cache
+            units = np.arange(w.batch * w.num_qo_heads)
+
+            def job(idx, w=w, c=c, odt=odt):
+                for u in idx:
+                    r, h = divmod(int(u), w.num_qo_heads)
+                    oracle.attention_row(w.q, c.k_pool, c.v_pool, c.kv_indptr, c.kv_indices,
+                                         c.last_page_len, c.page_size, w.num_qo_heads,
+                                         w.num_kv_heads, w.head_dim, odt, w.sm_scale, r, 0, h)
+        t1 = _timed_pass(job, units, 1)
+        tn = _timed_pass(job, units, threads)
+        out[w.name] = {"unit": "GB/s", "threads_1": b / t1 / 1e9, f"threads_{threads}": b / tn / 1e9,
+                       "sample": "whole workload, one pass"}
+    # shared prefix: prefix pass (qo_len = n per prompt, non-causal) + suffix
+    # decode + LSE merge, over the bytes the composable layout reads
+    w = synth.shared_prefix_decode()
+    pre, suf = w.extra["prefix"], w.cache
+    n = w.extra["n"]
+    pqo = w.extra["prefix_qo_indptr"]
+
+    def comp_job(ps):
+        for p_ in ps:
+            p_ = int(p_)
+            rs = slice(p_ * n, (p_ + 1) * n)
+            op, lp = oracle.batch_attention(
+                w.q[rs], pre.k_pool, pre.v_pool, pre.kv_indptr[p_:p_ + 2], pre.kv_indices,
+                pre.last_page_len[p_:p_ + 1], pre.page_size, 32, 8, 128, oracle.BF16, w.sm_scale,
+                qo_indptr=pqo[p_:p_ + 2] - pqo[p_])
+            os_, ls = oracle.batch_attention(
+                w.q[rs], suf.k_pool, suf.v_pool, suf.kv_indptr[p_ * n:(p_ + 1) * n + 1],
+                suf.kv_indices, suf.last_page_len[rs], suf.page_size, 32, 8, 128, oracle.BF16,
+                w.sm_scale)
+            oracle.merge_states(np.stack([op.reshape(-1, 128), os_.reshape(-1, 128)]),
+                                np.stack([lp.reshape(-1), ls.reshape(-1)]))
+
+    kvb = 2 * 8 * 128 * 2
+    b = (int(pre.kv_lens.sum()) + int(suf.kv_lens.sum())) * kvb
+    t1 = _timed_pass(comp_job, np.arange(w.extra["prompts"]), 1)
+    tn = _timed_pass(comp_job, np.arange(w.extra["prompts"]), threads)
+    out[w.name] = {"unit": "GB/s", "threads_1": b / t1 / 1e9, f"threads_{threads}": b / tn / 1e9,
+                   "sample": "whole workload, one pass (prefix + suffix + merge)"}
+    # causal append: a seeded subset of (request, head) pairs, every query row
+    w = synth.causal_append()
+    c = w.cache
+    qo = np.diff(w.qo_indptr)
+    E = c.kv_lens - qo
+    rng = np.random.default_rng(20260005)
+    pairs = [(int(rng.integers(w.batch)), int(rng.integers(w.num_qo_heads)))
+             for _ in range(threads)]
+
+    def pair_flops(r):
+        L = float(qo[r])
+        return 4.0 * w.head_dim * (L * E[r] + L * (L + 1) / 2)
+
+    def app_job(idx):
+        for k in idx:
+            r, h = pairs[int(k)]
+            for i in range(int(qo[r])):
+                oracle.attention_row(w.q, c.k_pool, c.v_pool, c.kv_indptr, c.kv_indices,
+                                     c.last_page_len, 16, 32, 8, 128, oracle.BF16, w.sm_scale,
+                                     r, i, h, causal=True, qo_indptr=w.qo_indptr)
+
+    f1 = pair_flops(pairs[0][0])
+    t1 = _timed_pass(app_job, [0], 1)
+    fn = sum(pair_flops(r) for r, _ in pairs)
+    tn = _timed_pass(app_job, np.arange(len(pairs)), threads)
+    total = append_flops(w)
+    out[w.name] = {"unit": "TFLOP/s", "threads_1": f1 / t1 / 1e12,
+                   f"threads_{threads}": fn / tn / 1e12,
+                   "sample": f"subset: 1 (request, head) pair single-threaded, {len(pairs)} pairs "
+                             f"on {threads} threads (seeded), every query row of each pair; "
+                             f"extrapolated to the whole workload ({total / 1e12:.3f} TFLOP) by "
+                             f"unmasked FLOPs",
+                   "extrapolated_whole_workload_s": {"threads_1": total / (f1 / t1),
+                                                     f"threads_{threads}": total / (fn / tn)}}
+    return out
+
+
+def plan_times(w, num_ctas):
+    """Host planning time of the headline batch: attn_plan through the C ABI
+    with no device workspace (the planner alone), and the public API's plan()
+    (planner + table upload enqueue), median over repeated calls."""
+    from paged_kv_attention_bsr_gb300 import _capi as C
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    c = w.cache
+    _, host = C.workspace_size(w.batch, w.batch, w.num_qo_heads, w.num_kv_heads, 128, num_ctas)
+    buf = np.zeros(host, np.uint8)
+    kvi = np.ascontiguousarray(c.kv_indptr, np.int32)
+    lpl = np.ascontiguousarray(c.last_page_len, np.int32)
+    t = []
+    for _ in range(300):
+        t0 = time.perf_counter()
+        C.plan(None, kvi, lpl, c.page_size, w.num_qo_heads, w.num_kv_heads, 128, False,
+               num_ctas, buf)
+        t.append(time.perf_counter() - t0)
+    att = PagedAttention(w.num_qo_heads, w.num_kv_heads, 128, "decode", max_batch=w.batch,
+                         num_ctas=num_ctas)
+    t2 = []
+    for _ in range(300):
+        t0 = time.perf_counter()
+        att.plan(kvi, lpl, c.page_size)
+        t2.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    return {"c_abi_host_only_us": float(np.median(t)) * 1e6,
+            "api_plan_with_upload_us": float(np.median(t2)) * 1e6,
+            "note": "median of 300 calls on the host (ctypes call included); the upload is an "
+                    "asynchronous copy enqueued on the stream"}
 
 
 def run_ours(args, rank, world):
@@ -550,6 +815,8 @@ def run_ours(args, rank, world):
         "clocks": clocks,
         "e2e": e2e,
     }
+    if rank == 0:
+        line["plan_us"] = plan_times(w, st.att.num_ctas)
     if world == 1 and not args.skip_cpu:
         threads = max(1, min(os.cpu_count() or 1, 16))
         secs, passes = cpu_oracle_baseline(w, threads)
@@ -557,7 +824,8 @@ def run_ours(args, rank, world):
                                 "kind": "oracle",
                                 "sample": f"{passes} whole passes over the workload (64 "
                                           f"requests x 32 heads), fp64 C oracle on {threads} "
-                                          f"threads, {secs:.2f} s per pass"}
+                                          f"threads, {secs:.2f} s per pass",
+                                "per_workload": cpu_oracle_per_workload(threads)}
     if world == 1 and not args.headline_only:
         del st
         torch.cuda.empty_cache()

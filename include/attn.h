@@ -126,11 +126,16 @@ attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_c
 
 /*
  * Planning phase (host). Splits the work of a batch into units balanced over
- * num_ctas CTAs (items (request, kv head, query tile) in request-major order,
- * dealt round-robin to the CTAs first for append;
- * each item weighs its page count + 1; CTA c takes the weight positions
- * [floor(c W / C), floor((c+1) W / C)) of the total W; an item cut by a CTA
- * boundary is "split" and its units write partial states that the run merges).
+ * num_ctas CTAs. Items are (request, kv head, query tile) triples in
+ * request-major order, then kv head, then tile; an item weighs its visible
+ * page count + 1, and W is the sum of the weights over all items.
+ *  - decode: the weights are laid end to end and CTA c takes the positions
+ *    [floor(c W / C), floor((c+1) W / C));
+ *  - append: items are dealt in order to the CTA with the least weight so
+ *    far (ties to the lowest index), each CTA capped at ceil(W / C) + 1; an
+ *    item that does not fit is cut at the cap and continues on the next CTA.
+ * An item cut into several units is "split": its units write partial states
+ * that the run merges by log-sum-exp.
  *   qo_indptr_h     : host int32[batch+1] query row offsets (append, starting
  *                     at 0), or NULL for decode (one row per request)
  *   kv_indptr_h     : host int32[batch+1] page offsets into kv_indices
@@ -239,10 +244,14 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q,
  * position kv_len - qo_len + i, key j at position j.
  *   rope_cos, rope_sin, rope_max_pos : as attn_decode_run_rope
  *   other arguments                  : as attn_append_run
- * Supported: the short appends the few-row tensor-core kernel runs (group x
- * the longest query count <= 16, e.g. speculative or multi-token decode, or
- * the n generations of a shared prefix; HND, any page size). Longer appends
- * return UNSUPPORTED.
+ * Supported: every shape attn_append_run takes. Short appends (group x the
+ * longest query count <= 16) run on the few-row kernel, whose rope warps
+ * derive most key angles by the angle-sum identities (as in
+ * attn_decode_run_rope); longer ones on the append kernel, whose two rope
+ * warps turn each unit's query rows once and every K tile in shared memory,
+ * reading a table row every 16 positions and stepping the angle by theta_d
+ * (table row 1) in between -- so the tables must hold cos / sin of
+ * pos * theta_d there too.
  * Errors: as attn_append_run and attn_decode_run_rope; INVALID_ARG if a
  * request with kv tokens has kv_len < qo_len (a query would sit before
  * position 0).
@@ -265,10 +274,12 @@ attn_status_t attn_append_run_rope(const attn_plan_t* plan, const void* q,
  *   qo_indptr  : device int32[batch+1], equal to the plan's host copy
  *   other arguments as attn_decode_run; o is [total_qo, num_qo_heads, head_dim]
  *   and lse float[total_qo, num_qo_heads].
- * Supported: head_dim 128, bf16 or fp16, HND layout, group in {1, 2, 4, 8,
- * 16}. Short appends (group x the longest query count <= 16) run on the
- * few-row tensor-core kernel at any page size; longer ones need page_size a
- * multiple of 16 (UNSUPPORTED otherwise).
+ * Supported: head_dim 128, bf16 or fp16, HND or NHD layout, any page_size
+ * >= 1, group in {1, 2, 4, 8, 16}. Short appends (group x the longest query
+ * count <= 16) run on the few-row tensor-core kernel; longer ones on the
+ * append kernel. Both load K / V by TMA in 16-row boxes when
+ * page_size % 16 == 0 and gather rows four at a time otherwise (down to one
+ * token per page).
  * Errors: as attn_decode_run.
  */
 attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
@@ -347,6 +358,9 @@ attn_status_t attn_wait_selftest(void* dev_ws, int32_t limit_us, void* stream);
  *    than 60k (request, kv head) pairs at group 8, a few more at smaller
  *    groups) return ATTN_ERR_WORKSPACE_TOO_SMALL
  *    before any GPU work; use attn_plan + attn_decode_run instead.
+ *  - The kernel's bounded waits report into an error word at the head of the
+ *    scratch area; attn_decode_run_noalloc_status reads it. The next call's
+ *    table upload clears the word, so read it before the next call.
  * Errors: as attn_plan and attn_decode_run.
  */
 attn_status_t attn_decode_run_noalloc(const int32_t* kv_indptr_h,
@@ -358,6 +372,27 @@ attn_status_t attn_decode_run_noalloc(const int32_t* kv_indptr_h,
                                       const int32_t* kv_indptr, const int32_t* kv_indices,
                                       const int32_t* last_page_len, int32_t dtype,
                                       float sm_scale, void* o, float* lse, void* stream);
+
+/*
+ * Status of the no-allocation path on the current device (no counterpart in
+ * the paper: this reads the library's own failure detection). Synchronises
+ * `stream`, then reads the error word at the head of the scratch area that
+ * attn_decode_run_noalloc uses; *code_out receives 0 if no kernel gave up a
+ * bounded wait since the last attn_decode_run_noalloc call on this device.
+ * Allocates nothing (the first call on a device looks up the scratch
+ * address, like attn_decode_run_noalloc).
+ * Returns TIMEOUT if the word is set, CUDA on a runtime error, else OK.
+ */
+attn_status_t attn_decode_run_noalloc_status(void* stream, int32_t* code_out);
+
+/*
+ * attn_wait_selftest aimed at the no-allocation scratch area (no counterpart
+ * in the paper): one bounded wait that nothing completes, whose code 0x1ff
+ * lands in the error word attn_decode_run_noalloc_status reads.
+ *   limit_us : 1 .. 10^7
+ * Errors: INVALID_ARG, CUDA.
+ */
+attn_status_t attn_wait_selftest_noalloc(int32_t limit_us, void* stream);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* attn_last_error(void);

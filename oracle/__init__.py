@@ -70,6 +70,10 @@ def _load():
             lib.oracle_batch_attention_rope.argtypes = [
                 vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32, i32, i32,
                 i32, i32, dbl, vp, vp, i64, vp, vp]
+            lib.oracle_attention_row_rope.restype = i32
+            lib.oracle_attention_row_rope.argtypes = [
+                vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                i32, i32, dbl, vp, vp, i64, i32, i32, i32, vp, vp]
             lib.oracle_round.restype = dbl
             lib.oracle_round.argtypes = [dbl, i32]
             lib.oracle_merge_states.restype = None
@@ -180,6 +184,32 @@ def attention_row(q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
         float(sm_scale), int(r), int(i), int(h), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_attention_row rejected its arguments (code {rc})")
+    return o, float(lse[0])
+
+
+def attention_row_rope(q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
+                       page_size, num_qo_heads, num_kv_heads, head_dim, dtype,
+                       sm_scale, rope_cos, rope_sin, r, i, h, causal=False, qo_indptr=None,
+                       layout=HND):
+    """One row of batch_attention_rope. Returns (o float64 [D], lse float)."""
+    lib = _load()
+    q16, k16, v16 = _u16(q), _u16(k_pool), _u16(v_pool)
+    kv_indptr, kv_indices = _i32(kv_indptr), _i32(kv_indices)
+    last_page_len, qo_indptr = _i32(last_page_len), _i32(qo_indptr)
+    cos = np.ascontiguousarray(rope_cos, np.float32)
+    sin = np.ascontiguousarray(rope_sin, np.float32)
+    batch = len(kv_indptr) - 1
+    num_pages = k16.size // (page_size * num_kv_heads * head_dim)
+    o = np.zeros(head_dim, np.float64)
+    lse = np.zeros(1, np.float64)
+    rc = lib.oracle_attention_row_rope(
+        _ptr(q16), _ptr(qo_indptr), _ptr(k16), _ptr(v16), num_pages, layout,
+        _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len), batch, page_size,
+        num_qo_heads, num_kv_heads, head_dim, dtype, int(bool(causal)),
+        float(sm_scale), _ptr(cos), _ptr(sin), cos.shape[0], int(r), int(i), int(h),
+        _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_row_rope rejected its arguments (code {rc})")
     return o, float(lse[0])
 
 

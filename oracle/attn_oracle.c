@@ -236,6 +236,45 @@ int32_t oracle_attention_row(const uint16_t* q, const int32_t* qo_indptr,
   return 0;
 }
 
+int32_t oracle_attention_row_rope(const uint16_t* q, const int32_t* qo_indptr,
+                                  const uint16_t* k_pool, const uint16_t* v_pool,
+                                  int64_t num_pages, int32_t layout,
+                                  const int32_t* kv_indptr, const int32_t* kv_indices,
+                                  const int32_t* last_page_len, int32_t batch,
+                                  int32_t page_size, int32_t num_qo_heads,
+                                  int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t dtype, int32_t causal, double sm_scale,
+                                  const float* rope_cos, const float* rope_sin,
+                                  int64_t rope_max_pos, int32_t r, int32_t i, int32_t h,
+                                  double* o, double* lse) {
+  if (!rope_cos || !rope_sin || head_dim % 2 != 0) return -1;
+  if (r < 0 || r >= batch || h < 0 || h >= num_qo_heads || i < 0) return -1;
+  int32_t rc = check_args(qo_indptr, num_pages, layout, kv_indptr, kv_indices,
+                          last_page_len, batch, page_size, num_qo_heads,
+                          num_kv_heads, head_dim, dtype);
+  if (rc) return rc;
+  int64_t qo_len = qo_indptr ? (int64_t)qo_indptr[r + 1] - qo_indptr[r] : 1;
+  if (i >= qo_len) return -1;
+  int64_t kv_len = bsr_kv_len(kv_indptr, last_page_len, page_size, r);
+  /* this row's key positions (< kv_len) and query position must have table
+     rows, and the query position must be >= 0 */
+  if (kv_len > rope_max_pos || (kv_len > 0 && kv_len < qo_len)) return -9;
+  double* x_buf = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+  double* q_buf = (double*)malloc(sizeof(double) * 2 * (size_t)head_dim);
+  if (!x_buf || !q_buf) {
+    free(x_buf);
+    free(q_buf);
+    return -100;
+  }
+  attention_row(q, qo_indptr, k_pool, v_pool, layout, kv_indptr, kv_indices,
+                last_page_len, page_size, num_qo_heads, num_kv_heads, head_dim,
+                dtype, causal, sm_scale, r, i, h, 0, INT64_MAX, x_buf, q_buf, rope_cos,
+                rope_sin, o, lse);
+  free(x_buf);
+  free(q_buf);
+  return 0;
+}
+
 static int32_t batch_attention(const uint16_t* q, const int32_t* qo_indptr,
                                const uint16_t* k_pool, const uint16_t* v_pool,
                                int64_t num_pages, int32_t layout,

@@ -98,6 +98,22 @@ int32_t oracle_batch_attention(const uint16_t* q, const int32_t* qo_indptr,
  *   rope_cos/rope_sin: float[rope_max_pos, D/2]; every position used must be
  *   < rope_max_pos (else -9 is returned). D must be even.
  */
+/*
+ * One row of oracle_batch_attention_rope (request r, query row i, query head
+ * h), with the same tables and checks restricted to request r.
+ */
+int32_t oracle_attention_row_rope(const uint16_t* q, const int32_t* qo_indptr,
+                                  const uint16_t* k_pool, const uint16_t* v_pool,
+                                  int64_t num_pages, int32_t layout,
+                                  const int32_t* kv_indptr, const int32_t* kv_indices,
+                                  const int32_t* last_page_len, int32_t batch,
+                                  int32_t page_size, int32_t num_qo_heads,
+                                  int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t dtype, int32_t causal, double sm_scale,
+                                  const float* rope_cos, const float* rope_sin,
+                                  int64_t rope_max_pos, int32_t r, int32_t i, int32_t h,
+                                  double* o, double* lse);
+
 int32_t oracle_batch_attention_rope(const uint16_t* q, const int32_t* qo_indptr,
                                     const uint16_t* k_pool, const uint16_t* v_pool,
                                     int64_t num_pages, int32_t layout,

@@ -16,10 +16,15 @@ pseudo-code; the exact cut below is the reading used throughout this project:
              + k is page k; an intersection without pages is dropped, except
              that an item with n = 0 keeps one zero-page unit, owned by the CTA
              that owns b
-  append     items go, in order, to the CTA with the least cost so far (ties:
-             lowest index), each CTA capped at ceil(W / C) + alpha; an item
-             that does not fit is cut at the cap (the unit takes the cap minus
-             alpha in pages) and its rest continues on the next CTA
+  append     the items of requests with at most 16 query rows (group x
+             qo_len: "decode-like") and the other items keep their own order
+             and are interleaved by weight (next from the class with the
+             smaller fraction of its total weight done, ties to the
+             non-decode-like class); in that order items go to the CTA with
+             the least cost so far (ties: lowest index), each CTA capped at
+             ceil(W / C) + alpha; an item that does not fit is cut at the cap
+             (the unit takes the cap minus alpha in pages) and its rest
+             continues on the next CTA
   slots      items with >= 2 units are split; their units get partial-state
              slots numbered in (item, page) order; merge_indptr lists them.
 
@@ -33,6 +38,7 @@ from typing import List, Optional, Sequence
 
 ALPHA = 1
 ITEM_ROWS = 256
+FEW_ROWS = 16
 
 
 @dataclass
@@ -67,8 +73,9 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
     decode = qo_indptr is None
     tq = 1 if decode else ITEM_ROWS // group
 
-    # 1. items and their page counts
+    # 1. items, their page counts and their class
     items = []  # (r, hk, t, n)
+    few = []    # the request has at most FEW_ROWS query rows
     for r in range(batch):
         kv_len = kv_length(kv_indptr, last_page_len, page_size, r)
         qo_len = 1 if decode else qo_indptr[r + 1] - qo_indptr[r]
@@ -80,9 +87,11 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
                     last_row = min((t + 1) * tq, qo_len) - 1
                     vis = min(kv_len, max(0, kv_len - qo_len + last_row + 1))
                 items.append((r, hk, t, -(-vis // page_size)))
+                few.append(group * qo_len <= FEW_ROWS)
 
     # 2. weights
-    total = sum(it[3] + ALPHA for it in items)
+    weight = [it[3] + ALPHA for it in items]
+    total = sum(weight)
     C = num_ctas
     plan = Plan(work_indptr=[0] * (C + 1), total_weight=total, num_items=len(items),
                 q_tile=tq)
@@ -110,12 +119,28 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
                     per_cta_units[c].append([k, r, hk, t, p0, p1])
             base += w
     else:
-        # 3b. time-ordered fill, capped
+        # 3b. interleave the two classes by weight, then the time-ordered fill
         import heapq
+        dense = [k for k in range(len(items)) if not few[k]]
+        light = [k for k in range(len(items)) if few[k]]
+        wd = sum(weight[k] for k in dense)
+        wf = sum(weight[k] for k in light)
+        order, i, j, dd, df = [], 0, 0, 0, 0
+        while i < len(dense) or j < len(light):
+            # class fractions done: dd / wd against df / wf (cross-multiplied)
+            if j >= len(light) or (i < len(dense) and dd * wf <= df * wd):
+                order.append(dense[i])
+                dd += weight[dense[i]]
+                i += 1
+            else:
+                order.append(light[j])
+                df += weight[light[j]]
+                j += 1
         cap = -(-total // C) + ALPHA
         ready = [(0, c) for c in range(C)]
         heapq.heapify(ready)
-        for k, (r, hk, t, n) in enumerate(items):
+        for k in order:
+            r, hk, t, n = items[k]
             p = 0
             while True:
                 used, c = heapq.heappop(ready)

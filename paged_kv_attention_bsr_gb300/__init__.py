@@ -6,8 +6,9 @@ tcgen05 append / prefill kernel and LSE merge kernels. This package is the
 thin Python binding over it:
 
   * ``_capi``  -- ctypes marshalling, one function per C entry point;
-  * ``api``    -- workspace ownership (PagedAttention), the single-request
-                  decode of the quick-start snippet, merge_state;
+  * ``api``    -- workspace ownership (PagedAttention), composable shared-prefix
+                  decode (CascadeAttention), the single-request decode of the
+                  quick-start snippet, merge_state;
   * ``synth``  -- seeded synthetic inputs (no attention arithmetic);
   * ``build``  -- nvcc build of libattn.so for sm_103a.
 
@@ -15,11 +16,13 @@ Importing the binding raises ImportError if libattn.so has not been built;
 there is no CPU or PyTorch fallback.
 """
 
-__all__ = ["PagedAttention", "single_decode_with_kv_cache", "merge_state", "AttnError"]
+__all__ = ["PagedAttention", "CascadeAttention", "single_decode_with_kv_cache", "merge_state",
+           "AttnError"]
 
 
 def __getattr__(name):
-    if name in ("PagedAttention", "single_decode_with_kv_cache", "merge_state"):
+    if name in ("PagedAttention", "CascadeAttention", "single_decode_with_kv_cache",
+                "merge_state"):
         from . import api
         return getattr(api, name)
     if name == "AttnError":

@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_S
 EXPORTS = ("attn_workspace_size", "attn_default_num_ctas", "attn_plan", "attn_decode_run",
            "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error",
            "attn_decode_run_noalloc", "attn_wait_selftest", "attn_decode_run_rope",
-           "attn_append_run_rope")
+           "attn_append_run_rope", "attn_decode_run_noalloc_status",
+           "attn_wait_selftest_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -76,6 +77,8 @@ def _load():
                                  vp, vp, i64, vp, vp, vp, sz, vp],
         "attn_decode_run_noalloc": [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64, i32, vp,
                                     vp, vp, i32, f32, vp, vp, vp],
+        "attn_decode_run_noalloc_status": [vp, P(i32)],
+        "attn_wait_selftest_noalloc": [i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -168,21 +171,40 @@ def plan(qo_indptr_h, kv_indptr_h, last_page_len_h, page_size, num_qo_heads, num
     return p
 
 
-def _check_sizes(p: Plan, q, k_pool, v_pool, o, lse, num_pages, rows):
-    """Tensor sizes and dtypes against the plan, before the library is called:
-    the kernels address the pools with the plan's heads and page size, so a
-    smaller pool would be read past its end."""
-    per_row = p.num_qo_heads * p.head_dim
-    need_kv = int(num_pages) * p.num_kv_heads * p.page_size * p.head_dim
-    if num_pages < 1 or k_pool.numel() < need_kv or v_pool.numel() < need_kv:
+def _check_dense(**tensors):
+    """The kernels address every tensor as a dense row-major block starting at
+    its data pointer, so a strided view (a slice of a larger KV tensor, a
+    transpose) would be read with the wrong layout."""
+    for name, t in tensors.items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (dense row-major); "
+                             f"call .contiguous() on it first")
+
+
+def _check_shapes(num_qo_heads, num_kv_heads, page_size, head_dim, needs_pool, q, k_pool,
+                  v_pool, o, lse, num_pages, rows):
+    """Tensor sizes, dtypes and layout against the shapes the kernels will
+    use, before the library is called: the kernels address the pools with
+    those heads and page size, so a smaller pool would be read past its end."""
+    _check_dense(q=q, k_pool=k_pool, v_pool=v_pool, out=o, lse=lse)
+    per_row = num_qo_heads * head_dim
+    need_kv = int(num_pages) * num_kv_heads * page_size * head_dim
+    if (needs_pool and num_pages < 1) or k_pool.numel() < need_kv or v_pool.numel() < need_kv:
         raise ValueError(f"k_pool / v_pool hold fewer than num_pages ({num_pages}) x "
-                         f"{p.num_kv_heads} heads x {p.page_size} slots x {p.head_dim} elements")
+                         f"{num_kv_heads} heads x {page_size} slots x {head_dim} elements")
     if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype or o.dtype != q.dtype:
         raise ValueError("q, k_pool, v_pool and out must share one dtype")
     if q.numel() < rows * per_row or o.numel() < rows * per_row:
-        raise ValueError(f"q / out need {rows} rows x {p.num_qo_heads} heads x {p.head_dim}")
-    if lse is not None and (lse.dtype != torch.float32 or lse.numel() < rows * p.num_qo_heads):
-        raise ValueError(f"lse must be float32 with {rows} x {p.num_qo_heads} elements")
+        raise ValueError(f"q / out need {rows} rows x {num_qo_heads} heads x {head_dim}")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() < rows * num_qo_heads):
+        raise ValueError(f"lse must be float32 with {rows} x {num_qo_heads} elements")
+
+
+def _check_sizes(p: Plan, q, k_pool, v_pool, o, lse, num_pages, rows):
+    """_check_shapes with the plan's shapes; the pool may be empty only when
+    the plan's requests hold no kv tokens at all."""
+    _check_shapes(p.num_qo_heads, p.num_kv_heads, p.page_size, p.head_dim,
+                  p.total_weight > p.num_items, q, k_pool, v_pool, o, lse, num_pages, rows)
 
 
 def decode_run(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale, o,
@@ -253,6 +275,7 @@ def append_run_rope(p: Plan, q, qo_indptr, k_pool, v_pool, kv_indptr, kv_indices
 
 
 def merge_states(o_a, lse_a, o_b, lse_b, o_out, lse_out, stream=None):
+    _check_dense(o_a=o_a, lse_a=lse_a, o_b=o_b, lse_b=lse_b, o_out=o_out, lse_out=lse_out)
     n, h, d = o_a.shape
     for t in (o_b, o_out):
         if t.shape != o_a.shape or t.dtype != o_a.dtype:
@@ -285,8 +308,28 @@ def decode_run_noalloc(kv_indptr_h, last_page_len_h, page_size, num_qo_heads, nu
     last_page_len_h = _host_i32(last_page_len_h)
     if num_pages is None:
         num_pages = k_pool.shape[0]
+    batch = len(kv_indptr_h) - 1
+    has_pages = batch > 0 and int(kv_indptr_h[-1]) > int(kv_indptr_h[0])
+    _check_shapes(num_qo_heads, num_kv_heads, page_size, head_dim, has_pages, q, k_pool, v_pool,
+                  o, lse, num_pages, batch)
     _check(lib.attn_decode_run_noalloc(
         _ptr(kv_indptr_h), _ptr(last_page_len_h), len(kv_indptr_h) - 1, page_size,
         num_qo_heads, num_kv_heads, head_dim, _ptr(q), _ptr(k_pool), _ptr(v_pool),
         int(num_pages), layout, _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
         dtype_code(q.dtype), float(sm_scale), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def decode_run_noalloc_status(stream=None) -> int:
+    """attn_decode_run_noalloc_status: synchronise, then the no-allocation
+    scratch area's error word on the current device (0 = no kernel gave up)."""
+    code = ctypes.c_int32()
+    st = lib.attn_decode_run_noalloc_status(_stream(stream), ctypes.byref(code))
+    if st not in (OK, ERR_TIMEOUT):
+        _check(st)
+    return code.value
+
+
+def wait_selftest_noalloc(limit_us, stream=None):
+    """attn_wait_selftest_noalloc: one bounded wait that nothing completes,
+    reporting into the no-allocation scratch area's error word."""
+    _check(lib.attn_wait_selftest_noalloc(int(limit_us), _stream(stream)))

@@ -104,6 +104,74 @@ class PagedAttention:
         return C.workspace_status(self.dev_ws, stream)
 
 
+class CascadeAttention:
+    """Composable formats (shared prefix + unique suffix) for decode.
+
+    The prompt's common prefix is stored once in a pool with large pages and
+    read once for its n generations: a non-causal short append with the n
+    generations' query rows per prompt (qo_indptr_prefix). Each generation's
+    own suffix lives in a second pool (small pages) and is read by a decode
+    pass. The two partial states are combined by attn_merge_states. The
+    prefix and suffix passes are independent, so they are enqueued on two
+    streams (the suffix on a side stream forked from and joined back into the
+    caller's stream): the second launch fills the SMs the first one's tail
+    leaves idle instead of waiting for it. The merge runs on the caller's
+    stream after the join.
+    """
+
+    def __init__(self, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
+                 max_prompts: int = 64, max_batch: int = 256, device=None):
+        self.prefix = PagedAttention(num_qo_heads, num_kv_heads, head_dim, "append",
+                                     max_batch=max_prompts, max_total_qo=max_batch,
+                                     device=device)
+        self.suffix = PagedAttention(num_qo_heads, num_kv_heads, head_dim, "decode",
+                                     max_batch=max_batch, device=device)
+        self.side = torch.cuda.Stream(device=self.prefix.device)
+        self._fork = torch.cuda.Event()
+        self._join = torch.cuda.Event()
+        self._bufs = None
+
+    def plan(self, qo_indptr_prefix_h, kv_indptr_prefix_h, last_page_len_prefix_h,
+             page_size_prefix: int, kv_indptr_suffix_h, last_page_len_suffix_h,
+             page_size_suffix: int, stream=None):
+        """Plans both passes; the tables are uploaded on `stream`."""
+        self.prefix.plan(kv_indptr_prefix_h, last_page_len_prefix_h, page_size_prefix,
+                         qo_indptr_h=qo_indptr_prefix_h, causal=False, stream=stream)
+        self.suffix.plan(kv_indptr_suffix_h, last_page_len_suffix_h, page_size_suffix,
+                         stream=stream)
+
+    def run(self, q, prefix, suffix, qo_indptr_prefix, sm_scale=None, out=None, lse=None,
+            return_lse: bool = False):
+        """q [batch, Hq, D] (one row per generation, grouped by prompt);
+        prefix / suffix: dicts with k_pool, v_pool, kv_indptr, kv_indices,
+        last_page_len device tensors. Returns o (and lse)."""
+        stream = torch.cuda.current_stream()
+        if self._bufs is None or self._bufs[0].shape != q.shape or \
+                self._bufs[0].dtype != q.dtype:
+            mk = lambda: torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+            self._bufs = (torch.empty_like(q), mk(), torch.empty_like(q), mk())
+        o_p, l_p, o_s, l_s = self._bufs
+        self._fork.record(stream)
+        self.side.wait_event(self._fork)
+        with torch.cuda.stream(self.side):
+            self.suffix.run(q, suffix["k_pool"], suffix["v_pool"], suffix["kv_indptr"],
+                            suffix["kv_indices"], suffix["last_page_len"], sm_scale, out=o_s,
+                            lse=l_s, stream=self.side)
+            self._join.record(self.side)
+        self.prefix.run(q, prefix["k_pool"], prefix["v_pool"], prefix["kv_indptr"],
+                        prefix["kv_indices"], prefix["last_page_len"], sm_scale, out=o_p,
+                        lse=l_p, qo_indptr=qo_indptr_prefix, stream=stream)
+        stream.wait_event(self._join)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        C.merge_states(o_p, l_p, o_s, l_s, out, lse, stream=stream)
+        return (out, lse) if return_lse else out
+
+
 _single_cache = {}
 
 
@@ -116,8 +184,10 @@ def single_decode_with_kv_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
     contiguous cache is read in place as a BSR row of pages in the NHD layout
     (pages 0..n-1 in order), so the balanced plan can split it across SMs.
     The page size is the largest power of two up to 16 that divides kv_len,
-    so the pages cover exactly the caller's tensors.
+    so the pages cover exactly the caller's tensors. Strided k / v / q are
+    copied to dense tensors first. kv_len = 0 gives O = 0 and LSE = -inf.
     """
+    k, v, q = k.contiguous(), v.contiguous(), q.contiguous()  # read in place as dense pages
     kv_len, Hk, D = k.shape
     Hq = q.shape[0]
     P = 16

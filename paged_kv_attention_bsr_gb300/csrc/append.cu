@@ -11,8 +11,9 @@
 // An item packs 256 query rows (token x GQA head, row = token * group + head)
 // as two 128-row query tiles A and B, so every K/V tile read from L2/HBM
 // feeds both tiles and every head of the GQA group. K/V tiles hold 128 kv
-// tokens, gathered from the page table in 16-row TMA boxes
-// (page_size % 16 == 0).
+// tokens, gathered from the page table in 16-row TMA boxes when
+// page_size % 16 == 0, else four rows at a time with TMA gathers (any page
+// size down to one token per page: vector-level sparsity); HND or NHD pools.
 //
 // Per KV tile j (all MMAs M = N = 128, bf16/fp16 in, fp32 accumulate), for
 // each query tile x:
@@ -56,16 +57,22 @@ constexpr int kTileBytes = 2 * kHalf;       // 128 x 128 x 16-bit
 constexpr int kWarpSoftmax0 = 0;            // warps 0-3: tile A, 4-7: tile B
 constexpr int kWarpLoad = 8;                // warps 8-11: load, MMA, 2 idle
 constexpr int kWarpMma = 9;
+constexpr int kWarpRope0 = 10;              // RoPE: warps 10-11 turn q and K rows
 constexpr int kThreads = 384;
 // Register split (setmaxnreg): launched at 168 per thread (384 x 168 =
-// 64512); the load/MMA warpgroup drops to 104 (frees 128 x 64 = 8192) and the
-// two softmax warpgroups rise to 192 (take 256 x 24 = 6144). Per scheduler:
-// 192 + 192 + 104 registers x 32 lanes <= 16384.
+// 64512); the load/MMA/rope warpgroup drops to 104 (frees 128 x 64 = 8192)
+// and the two softmax warpgroups rise to 192 (take 256 x 24 = 6144). Per
+// scheduler: 192 + 192 + 104 registers x 32 lanes <= 16384.
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsControl = 104;
 constexpr int kRegsSoftmax = 192;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
+// K tiles in flight between the TMA and the S MMA are at most three (the
+// ring holds at most 2.5 K/V tile pairs), so three k_rot barriers, used by
+// K tile kt as k_rot[kt % 3] with parity (kt / 3) & 1, never run ahead of
+// their waiter.
+constexpr int kKRot = 3;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of query tile x: S_x (then P_x, packed 16-bit, over its first
 // 64 columns) at 256 x, O_x at 256 x + 128.
@@ -95,6 +102,8 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2], o_done[2], o_free[2];
   uint64_t drain;
+  uint64_t q_rot;          // RoPE: the unit's query rows are turned (count 64)
+  uint64_t k_rot[kKRot];   // RoPE: K tile kt is turned in its slot (count 64)
   uint32_t tmem_base;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -107,7 +116,33 @@ struct AppendParams {
   float scale_log2;
   uint32_t idesc_s;
   uint32_t idesc_pv;
+  int32_t gather;  // K / V rows gathered 4 at a time (page_size % 16 != 0)
+  int32_t nhd;     // pools are NHD [pages, P, Hk, 128] (else HND [pages, Hk, P, 128])
 };
+
+// The two 16-bit values of a word as floats.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+}
+
+// Rotary embedding of 4 pairs (dims d..d+3 with d+64..d+67) of a row: x / y
+// hold the lower / upper dims, c / s the cos / sin of the pairs' angles at
+// the row's position; x' = x cos - y sin, y' = y cos + x sin in fp32, then
+// rounded to the storage type.
+template <bool BF16>
+__device__ __forceinline__ void rope_pairs4(uint2& x, uint2& y, const float4 c, const float4 s) {
+  const float2 x0 = unpack2<BF16>(x.x), x1 = unpack2<BF16>(x.y);
+  const float2 y0 = unpack2<BF16>(y.x), y1 = unpack2<BF16>(y.y);
+  x = make_uint2(pack2<BF16>(fmaf(-y0.x, s.x, x0.x * c.x), fmaf(-y0.y, s.y, x0.y * c.y)),
+                 pack2<BF16>(fmaf(-y1.x, s.z, x1.x * c.z), fmaf(-y1.y, s.w, x1.y * c.w)));
+  y = make_uint2(pack2<BF16>(fmaf(x0.x, s.x, y0.x * c.x), fmaf(x0.y, s.y, y0.y * c.y)),
+                 pack2<BF16>(fmaf(x1.x, s.z, y1.x * c.z), fmaf(x1.y, s.w, y1.y * c.w)));
+}
 
 // --------------------------------------------------------- unit geometry
 struct AGeo {
@@ -146,7 +181,137 @@ __device__ __forceinline__ AGeo append_geo(const AppendArgs& a, int ui) {
   return g;
 }
 
-template <bool BF16, int NQ>
+// K / V producer modes: 16-row boxes of HND pools, 16-row boxes of NHD pools
+// (a 3-D map [tokens, Hk, 128] whose box is 16 tokens of one head), rows
+// gathered four at a time (page sizes that are not a multiple of 16).
+constexpr int kModeHndBox = 0;
+constexpr int kModeNhdBox = 1;
+constexpr int kModeGather = 2;
+
+// The TMA producer warp: per KV tile of each unit, K then V into the next
+// ring slots, and after tile 0's K / V the unit's query tile(s) once the
+// previous unit's last S MMA has read the query buffer. Boxes: lane c
+// fetches the page index of the tile's 16-row chunk c and issues that
+// chunk's boxes, so the tile's index loads overlap. Gathers: lane c fetches
+// the rows of tokens 4c .. 4c+3 with one tile::gather4 per 64-dim half,
+// tokens past the unit's end repeating its last token (every row read lies
+// in the pool; those K columns are masked, those V rows zeroed).
+struct ProducerEnd {
+  uint32_t ua;    // units whose query tiles were loaded
+  uint32_t uses;  // ring slot uses (K and V tiles) issued
+  bool ok;        // no wait gave up
+};
+
+template <int NQ, int MODE>
+__device__ __forceinline__ ProducerEnd produce_kv(const AppendParams& prm, Bars& bars,
+                                                  uint32_t base, int lane,
+                                                  volatile int32_t* err) {
+  uint32_t ua = 0, uses = 0;
+  bool ok = true;
+  constexpr int kSlots = Layout<NQ>::SLOTS;
+  constexpr int kOffQ = Layout<NQ>::OFF_Q;
+  constexpr int kOffRing = Layout<NQ>::OFF_RING;
+  constexpr uint32_t kRowsPerLd = MODE == kModeGather ? 4u : uint32_t(kChunk);
+  const AppendArgs& a = prm.a;
+  const int P = a.page_size;
+  const int Hk = a.num_kv_heads;
+  const int group = a.group;
+  const uint32_t tile_rows = uint32_t(group * a.tile_tokens);
+  auto wait0 = [&](uint32_t bar, uint32_t parity) -> bool {
+    bool r = true;
+    if (lane == 0) r = mbar_wait(bar, parity, err, ERR_WAIT_EMPTY);
+    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+  };
+  for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+  for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok; ++ui) {
+    AGeo g = append_geo(a, ui);
+    g.nq = min(g.nq, NQ);
+    if (g.ntiles == 0) continue;
+    for (int i = 0; i < g.ntiles && ok; ++i) {
+      const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+      const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+      const int nld = MODE == kModeGather ? (ntt + 3) / 4 : (ntt + kChunk - 1) / kChunk;
+      int32_t row[MODE == kModeGather ? 4 : 1];
+#pragma unroll
+      for (int u = 0; u < int(sizeof(row) / sizeof(row[0])); ++u) row[u] = 0;
+      if (lane < nld) {
+        if constexpr (MODE == kModeGather) {
+          const int64_t t0 = kv0 + 4 * lane;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int64_t t = min(t0 + u, g.tok_end - 1);
+            const int64_t pg = t / P;
+            const int64_t sl = t - pg * P;
+            const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+            row[u] = prm.nhd ? int32_t((phys * P + sl) * Hk + g.hk)
+                             : int32_t((phys * Hk + g.hk) * P + sl);
+          }
+        } else {
+          const int64_t kvt = kv0 + int64_t(lane) * kChunk;
+          const int64_t pg = kvt / P;
+          const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+          row[0] = MODE == kModeNhdBox ? int32_t(phys * P + (kvt - pg * P))  // token row
+                                       : int32_t((phys * Hk + g.hk) * P + (kvt - pg * P));
+        }
+      }
+      for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
+        const int slot = int(uses % kSlots);
+        if (!wait0(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_u32(&bars.slot_full[slot]);
+        if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nld) * kRowsPerLd * 256u);
+        __syncwarp();
+        if (lane < nld) {
+          const uint32_t dst =
+              base + kOffRing + slot * kTileBytes + uint32_t(lane) * kRowsPerLd * 128u;
+          const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
+                                   : static_cast<const void*>(&prm.tm_v);
+          if constexpr (MODE == kModeGather) {
+            tma_gather4(dst, tm, 0, row[0], row[1], row[2], row[3], full);
+            tma_gather4(dst + kHalf, tm, 64, row[0], row[1], row[2], row[3], full);
+          } else if constexpr (MODE == kModeNhdBox) {
+            tma_load_3d(dst, tm, 0, g.hk, row[0], full);
+            tma_load_3d(dst + kHalf, tm, 64, g.hk, row[0], full);
+          } else {
+            tma_load_2d(dst, tm, 0, row[0], full);
+            tma_load_2d(dst + kHalf, tm, 64, row[0], full);
+          }
+        }
+      }
+      if (i == 0 && ok) {
+        // the unit's query tile(s), once the previous unit's last S MMA is done
+        if (!wait0(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t qf = smem_u32(&bars.q_full);
+          mbar_arrive_expect_tx(qf, 256u * tile_rows * uint32_t(g.nq));
+          for (int x = 0; x < g.nq; ++x) {
+            const int32_t qrow =
+                int32_t(g.qo_start + int64_t(g.t) * a.q_tile + x * a.tile_tokens);
+            const uint32_t dst = base + kOffQ + x * kTileBytes;
+            tma_load_3d(dst, &prm.tm_q, 0, g.hk * group, qrow, qf);
+            tma_load_3d(dst + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
+          }
+        }
+        ++ua;
+      }
+    }
+  }
+  return {ua, uses, ok};
+}
+
+template <int NQ, int MODE>
+__device__ __noinline__ ProducerEnd produce_kv_outlined(const AppendParams& prm, Bars& bars,
+                                                        uint32_t base, int lane,
+                                                        volatile int32_t* err) {
+  return produce_kv<NQ, MODE>(prm, bars, base, lane, err);
+}
+
+template <bool BF16, int NQ, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_constant__ AppendParams prm) {
   constexpr int kSlots = Layout<NQ>::SLOTS;
   constexpr int kOffQ = Layout<NQ>::OFF_Q;
@@ -176,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       mbar_init(smem_u32(&bars.o_free[i]), 128);
     }
     mbar_init(smem_u32(&bars.drain), 1);
+    mbar_init(smem_u32(&bars.q_rot), 64);
+    for (int i = 0; i < kKRot; ++i) mbar_init(smem_u32(&bars.k_rot[i]), 64);
     fence_mbar_init();
   }
   if (warp == kWarpLoad && lane == 0) {
@@ -196,9 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
   const uint32_t tmem = bars.tmem_base;
   const int group = a.group;
 
-  // Rows per 128-row query tile that hold data (128 for append, group in
-  // decode mode) and the TMA bytes of one tile.
-  const uint32_t tile_rows = uint32_t(group * a.tile_tokens);
   // TMEM columns. Two query tiles: tile x has S_x/P_x at 256 x and O_x at
   // 256 x + 128. One query tile: S/P double-buffered at 0 and 128 (KV tile k
   // uses buffer k & 1, so S of tile k+1 runs under the softmax of tile k), O
@@ -211,75 +375,19 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
   // A CTA runs the unit lists of plan CTAs blockIdx.x, blockIdx.x + gridDim.x,
   // ... (the grid is at most one CTA per SM; a plan may have more CTAs).
   if (warp >= kWarpLoad) {
-  // warpgroup 2: TMA loads, MMA issue (2 idle warps); gives registers away
+  // warpgroup 2: TMA loads, MMA issue, two warps idle (or turning q and K rows
+  // with RoPE); gives registers away
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
-    // The whole warp runs the loop; lane c fetches the page index of the
-    // tile's 16-row chunk c and issues that chunk's boxes, so the eight index
-    // loads of a tile overlap instead of serialising.
-    uint32_t ua = 0, uses = 0;
-    const int P = a.page_size;
-    bool ok = true;
-    auto wait0 = [&](uint32_t bar, uint32_t parity) -> bool {
-      bool r = true;
-      if (lane == 0) r = mbar_wait(bar, parity, err, ERR_WAIT_EMPTY);
-      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
-    };
-    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
-    for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok; ++ui) {
-      AGeo g = append_geo(a, ui);
-      g.nq = min(g.nq, NQ);
-      if (g.ntiles == 0) continue;
-      for (int i = 0; i < g.ntiles && ok; ++i) {
-        const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
-        const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
-        const int nch = (ntt + kChunk - 1) / kChunk;
-        int32_t row = 0;
-        if (lane < nch) {
-          const int64_t kvt = kv0 + int64_t(lane) * kChunk;
-          const int64_t pg = kvt / P;
-          const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
-          row = int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
-        }
-        for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
-          const int slot = int(uses % kSlots);
-          if (!wait0(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u)) {
-            ok = false;
-            break;
-          }
-          const uint32_t full = smem_u32(&bars.slot_full[slot]);
-          if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
-          __syncwarp();
-          if (lane < nch) {
-            const uint32_t dst = base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
-            const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
-                                     : static_cast<const void*>(&prm.tm_v);
-            tma_load_2d(dst, tm, 0, row, full);
-            tma_load_2d(dst + kHalf, tm, 64, row, full);
-          }
-        }
-        if (i == 0 && ok) {
-          // the unit's query tile(s), once the previous unit's last S MMA is done
-          if (!wait0(smem_u32(&bars.q_empty), (ua & 1u) ^ 1u)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            const uint32_t qf = smem_u32(&bars.q_full);
-            mbar_arrive_expect_tx(qf, 256u * tile_rows * uint32_t(g.nq));
-            for (int x = 0; x < g.nq; ++x) {
-              const int32_t qrow =
-                  int32_t(g.qo_start + int64_t(g.t) * a.q_tile + x * a.tile_tokens);
-              const uint32_t dst = base + kOffQ + x * kTileBytes;
-              tma_load_3d(dst, &prm.tm_q, 0, g.hk * group, qrow, qf);
-              tma_load_3d(dst + kHalf, &prm.tm_q, 64, g.hk * group, qrow, qf);
-            }
-          }
-          ++ua;
-        }
-      }
-    }
+    // HND pools at page sizes that are a multiple of 16 (the common case)
+    // inline; NHD pools and gathered rows out of line, so that the kernel
+    // body the softmax warps run from stays as compact as without them.
+    const ProducerEnd pe =
+        prm.gather ? produce_kv_outlined<NQ, kModeGather>(prm, bars, base, lane, err)
+        : prm.nhd  ? produce_kv_outlined<NQ, kModeNhdBox>(prm, bars, base, lane, err)
+                   : produce_kv<NQ, kModeHndBox>(prm, bars, base, lane, err);
+    const uint32_t ua = pe.ua, uses = pe.uses;
     // drain: every issued copy has landed before the CTA can exit
     if (lane == 0) {
       if (ua > 0) mbar_wait(smem_u32(&bars.q_full), (ua - 1) & 1u, err, ERR_WAIT_DRAIN);
@@ -305,6 +413,14 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       auto wait_slot = [&](uint32_t use) -> bool {
         return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
                          ERR_WAIT_FULL);
+      };
+      // K tile kt (slot use 2 kt) has landed and, with RoPE, been turned
+      auto wait_k = [&](uint32_t kt) -> bool {
+        if constexpr (ROPE)
+          return mbar_wait(smem_u32(&bars.k_rot[kt % kKRot]), (kt / kKRot) & 1u, err,
+                           ERR_WAIT_FULL);
+        else
+          return wait_slot(2 * kt);
       };
       // S for query tile x and KV tile k (global count) from the K in kslot
       auto issue_s = [&](int x, uint32_t kslot, uint32_t k) {
@@ -346,8 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         g.nq = min(g.nq, NQ);
         if (g.ntiles == 0) continue;
         const int n = g.ntiles;
-        if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) ||
-            !wait_slot(2 * jt)) {
+        if (!mbar_wait(smem_u32(ROPE ? &bars.q_rot : &bars.q_full), ua & 1u, err,
+                       ERR_WAIT_FULL) ||
+            !wait_k(jt)) {
           ok = false;
           break;
         }
@@ -371,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
               if (x < g.nq && ok) {
                 ok = issue_pv(x, slot_of(2 * k + 1), k, i == 0);
                 if (ok && more) {
-                  if (x == 0 && !wait_slot(2 * k + 2)) {
+                  if (x == 0 && !wait_k(k + 1)) {
                     ok = false;
                     break;
                   }
@@ -392,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
           issue_s(0, slot_of(2 * jt), jt);
           mma_commit(smem_u32(&bars.slot_empty[slot_of(2 * jt)]));
           if (n > 1) {
-            if (!wait_slot(2 * jt + 2)) {
+            if (!wait_k(jt + 1)) {
               ok = false;
               break;
             }
@@ -409,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
             }
             ok = issue_pv(0, slot_of(2 * k + 1), k, i == 0);
             if (ok && i + 2 < n) {
-              if (!wait_slot(2 * k + 4)) {
+              if (!wait_k(k + 2)) {
                 ok = false;
                 break;
               }
@@ -433,6 +550,105 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
       mbar_wait(smem_u32(&bars.drain), 0, err, ERR_WAIT_DRAIN);
     }
     __syncwarp();
+  } else if (ROPE && warp >= kWarpRope0) {
+    // ------------------------------------------------------------ rope warps
+    // Warps 10-11 turn each unit's query rows once (between the query TMA
+    // and the unit's first S MMA; query i of a request at position
+    // kv_len - qo_len + i) and every K tile in its ring slot (between its
+    // TMA and the S MMAs that read it; key j at position j). A half-warp
+    // takes a row: lane l holds the pairs (d, d + 64), d = 4 (l % 16) .. + 3,
+    // one 8-byte piece in each 64-dim half of the 128B-swizzled tile, at the
+    // same offset in both halves. The tables hold cos / sin of pos * theta_d,
+    // so a half-warp walks consecutive positions by turning its (cos, sin)
+    // by theta_d (table row 1) at each step and reloads the table every 16
+    // positions: one table row per 16 tile rows. The MMA warp waits on
+    // q_rot / k_rot instead of the TMA barriers.
+    const int hq = (warp - kWarpRope0) * 2 + (lane >> 4);  // half-warp 0..3
+    const int l16 = lane & 15;
+    const int kbyte = ((l16 >> 1) << 4) | ((l16 & 1) << 3);  // piece, byte in it
+    auto table_row = [&](int64_t pos, float4& c, float4& sn) {
+      c = __ldg(reinterpret_cast<const float4*>(a.rope_cos + pos * (kHeadDim / 2) + 4 * l16));
+      sn = __ldg(reinterpret_cast<const float4*>(a.rope_sin + pos * (kHeadDim / 2) + 4 * l16));
+    };
+    float4 ct = make_float4(1.f, 1.f, 1.f, 1.f), stt = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.rope_rows > 1) table_row(1, ct, stt);  // cos / sin of theta_d
+    // (c, sn) at position p -> at p + 1
+    auto step = [&](float4& c, float4& sn) {
+      const float4 c0 = c;
+      c = make_float4(fmaf(c0.x, ct.x, -sn.x * stt.x), fmaf(c0.y, ct.y, -sn.y * stt.y),
+                      fmaf(c0.z, ct.z, -sn.z * stt.z), fmaf(c0.w, ct.w, -sn.w * stt.w));
+      sn = make_float4(fmaf(sn.x, ct.x, c0.x * stt.x), fmaf(sn.y, ct.y, c0.y * stt.y),
+                       fmaf(sn.z, ct.z, c0.z * stt.z), fmaf(sn.w, ct.w, c0.w * stt.w));
+    };
+    auto turn = [&](uint8_t* tile, int row, const float4 c, const float4 sn) {
+      const int off = row * 128 + (kbyte ^ ((row & 7) << 4));
+      uint2 x = *reinterpret_cast<const uint2*>(tile + off);
+      uint2 y = *reinterpret_cast<const uint2*>(tile + kHalf + off);
+      rope_pairs4<BF16>(x, y, c, sn);
+      *reinterpret_cast<uint2*>(tile + off) = x;
+      *reinterpret_cast<uint2*>(tile + kHalf + off) = y;
+    };
+    uint32_t ua = 0, jt = 0;
+    bool ok = true;
+    for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
+    for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok; ++ui) {
+      AGeo g = append_geo(a, ui);
+      g.nq = min(g.nq, NQ);
+      if (g.ntiles == 0) continue;
+      // ---- query rows: tile x, token tau (row tau * group + head) at
+      // position kv_len - qo_len + t * q_tile + x * tile_tokens + tau; a
+      // half-warp takes a quarter of each tile's tokens, all their heads
+      if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL)) {
+        ok = false;
+        break;
+      }
+      const int T = a.tile_tokens;
+      for (int x = 0; x < g.nq; ++x) {
+        uint8_t* qt = gbase + kOffQ + x * kTileBytes;
+        const int64_t qi0 = int64_t(g.t) * a.q_tile + int64_t(x) * T;
+        const int tau1 = min((hq + 1) * T / 4, int(max(int64_t(0), g.qo_len - qi0)));
+        float4 c, sn;
+        for (int tau = hq * T / 4; tau < tau1; ++tau) {
+          if ((tau - hq * T / 4) % 16 == 0) table_row(g.kv_len - g.qo_len + qi0 + tau, c, sn);
+#pragma unroll 1
+          for (int h = 0; h < group; ++h) turn(qt, tau * group + h, c, sn);
+          step(c, sn);
+        }
+      }
+      fence_proxy_async_smem();  // generic stores -> the MMA's operand reads
+      mbar_arrive(smem_u32(&bars.q_rot));
+      ++ua;
+      // ---- K tiles: half-warp hq takes rows [32 hq, 32 hq + 32), two at a time
+      for (int i = 0; i < g.ntiles && ok; ++i) {
+        const uint32_t kt = jt + i, use = 2 * kt;
+        if (!mbar_wait(smem_u32(&bars.slot_full[use % kSlots]), (use / kSlots) & 1u, err,
+                       ERR_WAIT_FULL)) {
+          ok = false;
+          break;
+        }
+        const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
+        const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
+        uint8_t* kt_tile = gbase + kOffRing + (use % kSlots) * kTileBytes;
+        const int r0 = 32 * hq;
+        float4 ca, sa, cb, sb;  // rows r0 + k and r0 + 16 + k
+        if (r0 < ntt) table_row(kv0 + r0, ca, sa);
+        if (r0 + 16 < ntt) table_row(kv0 + r0 + 16, cb, sb);
+#pragma unroll 1
+        for (int k = 0; k < 16; ++k) {
+          if (r0 + k < ntt) {
+            turn(kt_tile, r0 + k, ca, sa);
+            step(ca, sa);
+          }
+          if (r0 + 16 + k < ntt) {
+            turn(kt_tile, r0 + 16 + k, cb, sb);
+            step(cb, sb);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bars.k_rot[kt % kKRot]));
+      }
+      jt += g.ntiles;
+    }
   }
   } else {
     // ------------------------------------------------- softmax / epilogue
@@ -675,18 +891,20 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
 }
 
 // ------------------------------------------------------------------- host
-template <bool BF16, int NQ>
+template <bool BF16, int NQ, bool ROPE>
 cudaError_t launch_t(AppendParams& prm, int ctas, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(append_kernel<BF16, NQ>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Layout<NQ>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  append_kernel<BF16, NQ><<<ctas, kThreads, Layout<NQ>::SMEM, stream>>>(prm);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e =
+      ensure_smem_limit(append_kernel<BF16, NQ, ROPE>, Layout<NQ>::SMEM, configured);
+  if (e != cudaSuccess) return e;
+  append_kernel<BF16, NQ, ROPE><<<ctas, kThreads, Layout<NQ>::SMEM, stream>>>(prm);
   return cudaGetLastError();
+}
+
+template <bool BF16, bool ROPE>
+cudaError_t launch_nq(AppendParams& prm, int ctas, bool one_tile, cudaStream_t stream) {
+  return one_tile ? launch_t<BF16, 1, ROPE>(prm, ctas, stream)
+                  : launch_t<BF16, 2, ROPE>(prm, ctas, stream);
 }
 
 }  // namespace
@@ -701,8 +919,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
     *msg = "attn_append_run: num_qo_heads / num_kv_heads must divide 128";
     return cudaErrorNotSupported;
   }
-  if (a.page_size % kChunk != 0) {
-    *msg = "attn_append_run: page_size must be a multiple of 16";
+  if (a.page_size <= 0) {
+    *msg = "attn_append_run: page_size must be positive";
     return cudaErrorNotSupported;
   }
   if (a.num_ctas <= 0 || a.num_units == 0) return cudaSuccess;
@@ -719,6 +937,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
   prm.scale_log2 = a.sm_scale * kLog2e;
   prm.idesc_s = make_idesc(bf16, false);
   prm.idesc_pv = make_idesc(bf16, true);
+  prm.gather = a.page_size % kChunk != 0 ? 1 : 0;
+  prm.nhd = a.layout == ATTN_LAYOUT_NHD ? 1 : 0;
   {
     const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(a.num_qo_heads),
                                 cuuint64_t(a.total_qo)};
@@ -734,7 +954,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
     }
   }
   if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
-                    kTcChunk, false, &prm.tm_k, &prm.tm_v, msg))
+                    prm.gather ? 1u : uint32_t(kTcChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v,
+                    msg))
     return cudaErrorNotSupported;  // *msg says why
   // at most one CTA per SM (shared memory); extra plan CTAs are run in turn
   int sms = 0;
@@ -743,9 +964,16 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
   const int grid = a.num_ctas < sms ? a.num_ctas : sms;
   // one query tile per item suffices when no request has more queries than a tile
   const bool one_tile = decode_mode || a.max_qo_len <= a.tile_tokens;
+  const bool rope = a.rope_cos != nullptr;
+  if (rope && decode_mode) {
+    *msg = "attn_append_run: fused RoPE in the append kernel needs query rows (qo_indptr)";
+    return cudaErrorNotSupported;
+  }
   if (bf16)
-    return one_tile ? launch_t<true, 1>(prm, grid, stream) : launch_t<true, 2>(prm, grid, stream);
-  return one_tile ? launch_t<false, 1>(prm, grid, stream) : launch_t<false, 2>(prm, grid, stream);
+    return rope ? launch_nq<true, true>(prm, grid, one_tile, stream)
+                : launch_nq<true, false>(prm, grid, one_tile, stream);
+  return rope ? launch_nq<false, true>(prm, grid, one_tile, stream)
+              : launch_nq<false, false>(prm, grid, one_tile, stream);
 }
 
 }  // namespace attn

@@ -7,6 +7,9 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "internal.h"
 
@@ -25,12 +28,44 @@ attn_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(ATTN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+// NVTX range around an entry point (free when no profiler is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// ATTN_DEBUG_CHECKS=1: the run calls read the device page table back and
+// check it on the host before launching (slow: a synchronising copy).
+bool debug_checks_enabled() {
+  static int on = [] {
+    const char* v = std::getenv("ATTN_DEBUG_CHECKS");
+    return (v && v[0] && v[0] != '0') ? 1 : 0;
+  }();
+  return on != 0;
+}
+
 bool log_enabled() {
   static int on = [] {
     const char* v = std::getenv("ATTN_LOG");
     return (v && v[0] && v[0] != '0') ? 1 : 0;
   }();
   return on != 0;
+}
+
+// Pages a plan's requests hold in total (each item weighs its pages + 1).
+// (Sum over items of their visible pages: 0 exactly when no request holds kv.)
+int64_t plan_pages(const attn_plan_t& p) { return p.total_weight - p.num_items; }
+
+// A plan whose requests hold no kv tokens at all: every row gets O = 0 and
+// LSE = -inf without touching the (possibly empty) pool.
+attn_status_t run_empty(const attn_plan_t* plan, void* o, float* lse, int64_t rows,
+                        int32_t dtype, void* stream, const char* fn) {
+  cudaError_t e = launch_fill_empty(o, lse, rows * plan->num_qo_heads, dtype,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ATTN_OK;
 }
 
 attn_status_t check_plan_common(const attn_plan_t* plan, int32_t mode, const void* q,
@@ -52,8 +87,8 @@ attn_status_t check_plan_common(const attn_plan_t* plan, int32_t mode, const voi
   if (plan->batch > 0 && plan->total_qo > 0 &&
       (!q || !o || !kv_indptr || !last_page_len))
     return fail(ATTN_ERR_INVALID_ARG, f + ": null device pointer");
-  if (plan->num_units > 0 && (!k_pool || !v_pool || !kv_indices))
-    return fail(ATTN_ERR_INVALID_ARG, f + ": null KV pool or kv_indices");
+  if (plan_pages(*plan) > 0 && (!k_pool || !v_pool || !kv_indices || num_pages < 1))
+    return fail(ATTN_ERR_INVALID_ARG, f + ": null KV pool or kv_indices, or an empty pool");
   if (num_pages < 0) return fail(ATTN_ERR_INVALID_ARG, f + ": num_pages < 0");
   if (!dev_ws) return fail(ATTN_ERR_INVALID_ARG, f + ": dev_ws is NULL");
   if (size_t(plan->dev_bytes_needed) > dev_bytes)
@@ -64,6 +99,56 @@ attn_status_t check_plan_common(const attn_plan_t* plan, int32_t mode, const voi
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pool) |
        reinterpret_cast<uintptr_t>(v_pool) | reinterpret_cast<uintptr_t>(o)) & align_mask)
     return fail(ATTN_ERR_INVALID_ARG, f + ": q, k_pool, v_pool and o must be 16-byte aligned");
+  return ATTN_OK;
+}
+
+// The device page table a run will read, checked on the host against the
+// pool and the plan: kv_indptr, last_page_len (and qo_indptr for append) must
+// be the arrays the plan was made from (same fingerprint), and every
+// kv_indices entry the kernels will read must lie in [0, num_pages).
+// Skipped while `stream` is being captured into a graph.
+attn_status_t debug_check_table(const attn_plan_t* plan, const int32_t* qo_indptr,
+                                const int32_t* kv_indptr, const int32_t* kv_indices,
+                                const int32_t* last_page_len, int64_t num_pages, void* stream,
+                                const char* fn) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return ATTN_OK;
+  const std::string f(fn);
+  const int32_t B = plan->batch;
+  if (B == 0) return ATTN_OK;
+  std::vector<int32_t> indptr(static_cast<size_t>(B) + 1), last(static_cast<size_t>(B)), qo;
+  cudaError_t e = cudaMemcpyAsync(indptr.data(), kv_indptr, 4 * (size_t(B) + 1),
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(last.data(), last_page_len, 4 * size_t(B), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && qo_indptr) {
+    qo.resize(size_t(B) + 1);
+    e = cudaMemcpyAsync(qo.data(), qo_indptr, 4 * (size_t(B) + 1), cudaMemcpyDeviceToHost, st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, (f + ": debug check: page table read").c_str());
+  if (plan_fingerprint(qo_indptr ? qo.data() : nullptr, indptr.data(), last.data(), B,
+                       plan->page_size, plan->num_qo_heads, plan->num_kv_heads, plan->head_dim,
+                       plan->causal, plan->num_ctas) != plan->fingerprint)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": debug check: kv_indptr / last_page_len / qo_indptr "
+                                          "on the device differ from the plan's host copies");
+  const int64_t pages = int64_t(indptr[size_t(B)]) - indptr[0];
+  if (pages <= 0) return ATTN_OK;
+  std::vector<int32_t> idx(static_cast<size_t>(pages));
+  e = cudaMemcpyAsync(idx.data(), kv_indices + indptr[0], 4 * size_t(pages),
+                      cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, (f + ": debug check: kv_indices read").c_str());
+  for (int64_t i = 0; i < pages; ++i)
+    if (idx[size_t(i)] < 0 || idx[size_t(i)] >= num_pages) {
+      char buf[160];
+      std::snprintf(buf, sizeof buf,
+                    ": debug check: kv_indices[%lld] = %d is outside [0, num_pages = %lld)",
+                    (long long)(indptr[0] + i), idx[size_t(i)], (long long)num_pages);
+      return fail(ATTN_ERR_INVALID_ARG, f + buf);
+    }
   return ATTN_OK;
 }
 
@@ -130,15 +215,13 @@ attn_status_t check_append(const attn_plan_t* plan, const void* q, const int32_t
     return fail(ATTN_ERR_INVALID_ARG, std::string(fn) + ": causal differs from the plan's");
   if (plan->batch > 0 && !qo_indptr)
     return fail(ATTN_ERR_INVALID_ARG, std::string(fn) + ": qo_indptr is NULL");
-  if (layout != ATTN_LAYOUT_HND)
-    return fail(ATTN_ERR_UNSUPPORTED, std::string(fn) + ": only the HND layout is implemented");
   return ATTN_OK;
 }
 
 // Kernel arguments of an append run (no RoPE).
 attn::AppendArgs append_args(const attn_plan_t* plan, const void* q, const int32_t* qo_indptr,
                              const void* k_pool, const void* v_pool, int64_t num_pages,
-                             const int32_t* kv_indptr, const int32_t* kv_indices,
+                             int32_t layout, const int32_t* kv_indptr, const int32_t* kv_indices,
                              const int32_t* last_page_len, int32_t dtype, float sm_scale,
                              void* o, float* lse, void* dev_ws) {
   attn::AppendArgs a;
@@ -169,6 +252,7 @@ attn::AppendArgs append_args(const attn_plan_t* plan, const void* q, const int32
   a.max_qo_len = plan->max_qo_len;
   a.causal = plan->causal;
   a.sm_scale = sm_scale;
+  a.layout = layout;
   return a;
 }
 
@@ -183,6 +267,44 @@ attn_status_t check_rope(const attn_plan_t* plan, const float* rope_cos, const f
     return fail(ATTN_ERR_INVALID_ARG,
                 std::string(fn) + ": the cos / sin tables must cover every kv position "
                                   "(rope_max_pos >= the plan's longest kv length)");
+  return ATTN_OK;
+}
+
+// An append run: short appends (group x longest query count <= 16 packed
+// rows, e.g. the n generations of a shared prefix) on the few-row kernel,
+// which keeps the softmax off the critical path of an HBM-bound pass and
+// merges split items itself; longer ones on the append kernel, then the
+// merge of its split items.
+attn_status_t run_append_kernels(const attn_plan_t* plan, const attn::AppendArgs& a,
+                                 const int32_t* qo_indptr, void* o, float* lse, int32_t dtype,
+                                 void* stream, const char* fn) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* msg = "";
+  const std::string f(fn);
+  if (few_row_rows(a.group, a.max_qo_len) != 0) {
+    cudaError_t e = launch_decode_tc(a, st, &msg);
+    if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+    if (e != cudaSuccess) return cuda_fail(e, (f + ": few-row kernel launch").c_str());
+    return ATTN_OK;
+  }
+  cudaError_t e = launch_append(a, st, &msg);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+  if (e != cudaSuccess) return cuda_fail(e, (f + ": append kernel launch").c_str());
+  if (plan->num_split_items > 0) {
+    SplitMergeArgs m;
+    m.ws = a.ws;
+    m.num_split_items = plan->num_split_items;
+    m.rows_per_item = plan->rows_per_item;
+    m.group = a.group;
+    m.q_tile = plan->q_tile;
+    m.num_qo_heads = plan->num_qo_heads;
+    m.qo_indptr = qo_indptr;
+    m.o = o;
+    m.lse = lse;
+    m.dtype = dtype;
+    e = launch_split_merge(m, st);
+    if (e != cudaSuccess) return cuda_fail(e, (f + ": merge kernel launch").c_str());
+  }
   return ATTN_OK;
 }
 
@@ -250,6 +372,7 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                         int32_t causal, int32_t num_ctas, void* pinned_host_ws,
                         size_t pinned_bytes, void* dev_ws, size_t dev_bytes, void* stream,
                         attn_plan_t* plan_out) {
+  NvtxRange nvtx("attn_plan");
   const char* msg = "";
   attn_status_t s = build_plan(qo_indptr_h, kv_indptr_h, last_page_len_h, batch, page_size,
                                num_qo_heads, num_kv_heads, head_dim, causal, num_ctas,
@@ -282,14 +405,22 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
                               const int32_t* last_page_len, int32_t dtype, float sm_scale,
                               void* o, float* lse, void* dev_ws, size_t dev_bytes,
                               void* stream) {
+  NvtxRange nvtx("attn_decode_run");
   attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
                                       layout, kv_indptr, kv_indices, last_page_len, dtype, o,
                                       dev_ws, dev_bytes, "attn_decode_run");
   if (s != ATTN_OK) return s;
+  if (debug_checks_enabled()) {
+    s = debug_check_table(plan, nullptr, kv_indptr, kv_indices, last_page_len, num_pages,
+                          stream, "attn_decode_run");
+    if (s != ATTN_OK) return s;
+  }
   const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
   if (group > kMaxDecodeGroup)
     return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_run: group > 8 is not implemented");
   if (plan->batch == 0) return ATTN_OK;
+  if (plan_pages(*plan) == 0)
+    return run_empty(plan, o, lse, plan->batch, dtype, stream, "attn_decode_run");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (decode_tc_shape(plan, layout)) {
     // Tensor-core decode: Q K^T and P V run as M = 128 MMAs over 128-token
@@ -337,16 +468,24 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q, const
                                    const float* rope_cos, const float* rope_sin,
                                    int64_t rope_max_pos, void* o, float* lse, void* dev_ws,
                                    size_t dev_bytes, void* stream) {
+  NvtxRange nvtx("attn_decode_run_rope");
   attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
                                       layout, kv_indptr, kv_indices, last_page_len, dtype, o,
                                       dev_ws, dev_bytes, "attn_decode_run_rope");
   if (s != ATTN_OK) return s;
+  if (debug_checks_enabled()) {
+    s = debug_check_table(plan, nullptr, kv_indptr, kv_indices, last_page_len, num_pages,
+                          stream, "attn_decode_run_rope");
+    if (s != ATTN_OK) return s;
+  }
   s = check_rope(plan, rope_cos, rope_sin, rope_max_pos, "attn_decode_run_rope");
   if (s != ATTN_OK) return s;
   if (!decode_tc_shape(plan, layout))
     return fail(ATTN_ERR_UNSUPPORTED,
                 "attn_decode_run_rope: fused RoPE needs 2, 4 or 8 query heads per kv head");
   if (plan->batch == 0) return ATTN_OK;
+  if (plan_pages(*plan) == 0)
+    return run_empty(plan, o, lse, plan->batch, dtype, stream, "attn_decode_run_rope");
   AppendArgs a = decode_tc_args(plan, q, k_pool, v_pool, num_pages, layout, kv_indptr,
                                 kv_indices, last_page_len, dtype, sm_scale, o, lse, dev_ws);
   a.rope_cos = rope_cos;
@@ -366,47 +505,22 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
                               const int32_t* last_page_len, int32_t dtype, int32_t causal,
                               float sm_scale, void* o, float* lse, void* dev_ws,
                               size_t dev_bytes, void* stream) {
+  NvtxRange nvtx("attn_append_run");
   attn_status_t s = check_append(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout,
                                  kv_indptr, kv_indices, last_page_len, dtype, causal, o,
                                  dev_ws, dev_bytes, "attn_append_run");
   if (s != ATTN_OK) return s;
+  if (debug_checks_enabled()) {
+    s = debug_check_table(plan, qo_indptr, kv_indptr, kv_indices, last_page_len, num_pages,
+                          stream, "attn_append_run");
+    if (s != ATTN_OK) return s;
+  }
   if (plan->batch == 0 || plan->total_qo == 0) return ATTN_OK;
-  AppendArgs a = append_args(plan, q, qo_indptr, k_pool, v_pool, num_pages, kv_indptr,
+  if (plan_pages(*plan) == 0)
+    return run_empty(plan, o, lse, plan->total_qo, dtype, stream, "attn_append_run");
+  AppendArgs a = append_args(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout, kv_indptr,
                              kv_indices, last_page_len, dtype, sm_scale, o, lse, dev_ws);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const char* msg = "";
-  if (few_row_rows(a.group, a.max_qo_len) != 0) {
-    // Short appends (group x longest query count <= 16 packed rows, e.g. the
-    // n generations of a shared prefix): the few-row kernel keeps the
-    // softmax off the critical path of an HBM-bound pass and merges split
-    // items itself.
-    cudaError_t e = launch_decode_tc(a, st, &msg);
-    if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: few-row kernel launch");
-    return ATTN_OK;
-  }
-  if (plan->page_size % 16 != 0)
-    return fail(ATTN_ERR_UNSUPPORTED,
-                "attn_append_run: appends past 16 packed rows need page_size % 16 == 0");
-  cudaError_t e = launch_append(a, st, &msg);
-  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
-  if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: append kernel launch");
-  if (plan->num_split_items > 0) {
-    SplitMergeArgs m;
-    m.ws = a.ws;
-    m.num_split_items = plan->num_split_items;
-    m.rows_per_item = plan->rows_per_item;
-    m.group = a.group;
-    m.q_tile = plan->q_tile;
-    m.num_qo_heads = plan->num_qo_heads;
-    m.qo_indptr = qo_indptr;
-    m.o = o;
-    m.lse = lse;
-    m.dtype = dtype;
-    e = launch_split_merge(m, st);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_append_run: merge kernel launch");
-  }
-  return ATTN_OK;
+  return run_append_kernels(plan, a, qo_indptr, o, lse, dtype, stream, "attn_append_run");
 }
 
 attn_status_t attn_append_run_rope(const attn_plan_t* plan, const void* q,
@@ -417,38 +531,38 @@ attn_status_t attn_append_run_rope(const attn_plan_t* plan, const void* q,
                                    int32_t causal, float sm_scale, const float* rope_cos,
                                    const float* rope_sin, int64_t rope_max_pos, void* o,
                                    float* lse, void* dev_ws, size_t dev_bytes, void* stream) {
+  NvtxRange nvtx("attn_append_run_rope");
   attn_status_t s = check_append(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout,
                                  kv_indptr, kv_indices, last_page_len, dtype, causal, o,
                                  dev_ws, dev_bytes, "attn_append_run_rope");
   if (s != ATTN_OK) return s;
+  if (debug_checks_enabled()) {
+    s = debug_check_table(plan, qo_indptr, kv_indptr, kv_indices, last_page_len, num_pages,
+                          stream, "attn_append_run_rope");
+    if (s != ATTN_OK) return s;
+  }
   s = check_rope(plan, rope_cos, rope_sin, rope_max_pos, "attn_append_run_rope");
   if (s != ATTN_OK) return s;
   if (plan->min_kv_minus_qo < 0)
     return fail(ATTN_ERR_INVALID_ARG,
                 "attn_append_run_rope: a request has fewer kv tokens than queries, so a "
                 "query would sit before position 0");
-  const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
-  if (few_row_rows(group, plan->max_qo_len) == 0)
-    return fail(ATTN_ERR_UNSUPPORTED,
-                "attn_append_run_rope: fused RoPE runs on short appends (group x the longest "
-                "query count <= 16)");
   if (plan->batch == 0 || plan->total_qo == 0) return ATTN_OK;
-  AppendArgs a = append_args(plan, q, qo_indptr, k_pool, v_pool, num_pages, kv_indptr,
+  if (plan_pages(*plan) == 0)
+    return run_empty(plan, o, lse, plan->total_qo, dtype, stream, "attn_append_run_rope");
+  AppendArgs a = append_args(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout, kv_indptr,
                              kv_indices, last_page_len, dtype, sm_scale, o, lse, dev_ws);
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;
   a.rope_rows = rope_max_pos;
-  const char* msg = "";
-  cudaError_t e = launch_decode_tc(a, static_cast<cudaStream_t>(stream), &msg);
-  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
-  if (e != cudaSuccess) return cuda_fail(e, "attn_append_run_rope: kernel launch");
-  return ATTN_OK;
+  return run_append_kernels(plan, a, qo_indptr, o, lse, dtype, stream, "attn_append_run_rope");
 }
 
 attn_status_t attn_merge_states(const void* o_a, const float* lse_a, const void* o_b,
                                 const float* lse_b, void* o_out, float* lse_out, int32_t n,
                                 int32_t num_heads, int32_t head_dim, int32_t dtype,
                                 void* stream) {
+  NvtxRange nvtx("attn_merge_states");
   if (n < 0 || num_heads < 1 || head_dim < 1)
     return fail(ATTN_ERR_INVALID_ARG, "attn_merge_states: sizes must be positive");
   if (head_dim % 8 != 0)

@@ -178,9 +178,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
       for (int s = 0; s < g.nst; ++s, ++it) {
         const int stage = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
-        if (!mbar_wait(smem_u32(&sm.empty[stage]), ph ^ 1u, err, ERR_WAIT_EMPTY)) goto drain;
         const int tok0 = s * kStageTok;
         const int nt = min(kStageTok, g.ntok - tok0);
+        // HND: the page index of the stage's page (lane), loaded before the
+        // slot is free so that its latency hides behind the wait
+        int64_t phys_l = 0;
+        if (a.layout == ATTN_LAYOUT_HND && nt > 0) {
+          const int64_t pg = (g.tok_begin + tok0) / P + lane;
+          if (pg <= (g.tok_begin + tok0 + nt - 1) / P)
+            phys_l = __ldg(a.kv_indices + g.page_base + pg);
+        }
+        if (!mbar_wait(smem_u32(&sm.empty[stage]), ph ^ 1u, err, ERR_WAIT_EMPTY)) goto drain;
         const uint32_t full = smem_u32(&sm.full[stage]);
         const uint32_t bytes = uint32_t(max(nt, 0)) * 2u * kRowBytes +
                                (s == 0 ? uint32_t(group) * kRowBytes : 0u);
@@ -201,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             for (int64_t pg = pg_a + lane; pg <= pg_b; pg += 32) {
               const int64_t t_lo = max(pg * P, t_lo_all);
               const int64_t t_hi = min((pg + 1) * P, t_hi_all);
-              const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+              const int64_t phys =
+                  pg - pg_a < 32 ? phys_l : int64_t(__ldg(a.kv_indices + g.page_base + pg));
               const int64_t row = (phys * Hk + g.hk) * P + (t_lo - pg * P);
               const uint32_t off = uint32_t(t_lo - t_lo_all) * kRowBytes;
               const uint32_t nb = uint32_t(t_hi - t_lo) * kRowBytes;
@@ -427,18 +436,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             __threadfence();
             const int s0 = __ldg(a.ws.merge_indptr + g.split);
             const int s1 = __ldg(a.ws.merge_indptr + g.split + 1);
+            // loads in batches of kB slots (a few L2 round trips, not one per slot)
+            constexpr int kB = 16;
             for (int h = 0; h < group; ++h) {
               float M = -INFINITY;
-              for (int sl = s0; sl < s1; ++sl)
-                M = fmaxf(M, __ldcg(a.ws.partial_lse + int64_t(sl) * group + h));
+              for (int b0 = s0; b0 < s1; b0 += kB) {
+                float x[kB];
+#pragma unroll
+                for (int k = 0; k < kB; ++k)
+                  x[k] = b0 + k < s1 ? __ldcg(a.ws.partial_lse + int64_t(b0 + k) * group + h)
+                                     : -INFINITY;
+#pragma unroll
+                for (int k = 0; k < kB; ++k) M = fmaxf(M, x[k]);
+              }
               float out = 0.f, lse2 = -INFINITY;
               if (M != -INFINITY) {
                 float L = 0.f, acc_d = 0.f;
-                for (int sl = s0; sl < s1; ++sl) {
-                  const int64_t prow = int64_t(sl) * group + h;
-                  const float f = ex2(__ldcg(a.ws.partial_lse + prow) - M);
-                  L += f;
-                  acc_d += f * __ldcg(a.ws.partial_o + prow * kHeadDim + d);
+                for (int b0 = s0; b0 < s1; b0 += kB) {
+                  float ls[kB], ov[kB];
+#pragma unroll
+                  for (int k = 0; k < kB; ++k) {
+                    const int64_t prow = int64_t(b0 + k) * group + h;
+                    ls[k] = b0 + k < s1 ? __ldcg(a.ws.partial_lse + prow) : -INFINITY;
+                    ov[k] = b0 + k < s1 ? __ldcg(a.ws.partial_o + prow * kHeadDim + d) : 0.f;
+                  }
+#pragma unroll
+                  for (int k = 0; k < kB; ++k) {
+                    const float f = ex2(ls[k] - M);
+                    L += f;
+                    acc_d += f * ov[k];
+                  }
                 }
                 out = acc_d / L;
                 lse2 = M + lg2(L);
@@ -464,13 +491,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
 template <int GM, bool BF16>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
   const size_t smem = sizeof(Smem);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<GM, BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = ensure_smem_limit(decode_kernel<GM, BF16>, int(smem), configured);
+  if (e != cudaSuccess) return e;
   decode_kernel<GM, BF16><<<a.num_ctas, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }

@@ -249,26 +249,59 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
   const int rho = lane / LP, dl = lane % LP;
   const QRow qr = qrow<DEC, R>(a, g, rho);
   const int s0 = __ldg(a.ws.merge_indptr + g.split), s1 = __ldg(a.ws.merge_indptr + g.split + 1);
+  // The merge is a short chain of L2 round trips at the tail of the launch,
+  // so loads are issued in batches: the first kKeep slots' LSEs at once
+  // (kept in registers), then the O rows kBo slots at a time (8 float4 loads
+  // in flight per lane).
+  constexpr int kKeep = 16;
+  constexpr int kBo = DL >= 32 ? 1 : 32 / DL;
+  auto lse_at = [&](int sl) {
+    return __ldcg(a.ws.partial_lse + int64_t(sl) * a.rows_per_item + rho);
+  };
+  float keep[kKeep];
+#pragma unroll
+  for (int k = 0; k < kKeep; ++k) keep[k] = s0 + k < s1 ? lse_at(s0 + k) : -INFINITY;
   float M = -INFINITY;
-  for (int sl = s0; sl < s1; ++sl)
-    M = fmaxf(M, __ldcg(a.ws.partial_lse + int64_t(sl) * a.rows_per_item + rho));
+#pragma unroll
+  for (int k = 0; k < kKeep; ++k) M = fmaxf(M, keep[k]);
+  for (int sl = s0 + kKeep; sl < s1; ++sl) M = fmaxf(M, lse_at(sl));
   float acc[DL];
 #pragma unroll
   for (int j = 0; j < DL; ++j) acc[j] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
-    for (int sl = s0; sl < s1; ++sl) {
-      const int64_t prow = int64_t(sl) * a.rows_per_item + rho;
-      const float f = ex2(__ldcg(a.ws.partial_lse + prow) - M);
-      L += f;
-      const float4* src = reinterpret_cast<const float4*>(a.ws.partial_o + prow * kHeadDim + DL * dl);
+    for (int b0 = s0; b0 < s1; b0 += kBo) {
+      float4 x[kBo][DL / 4];
+      float f[kBo];
 #pragma unroll
-      for (int j = 0; j < DL / 4; ++j) {
-        const float4 x = __ldcg(src + j);
-        acc[4 * j] += f * x.x;
-        acc[4 * j + 1] += f * x.y;
-        acc[4 * j + 2] += f * x.z;
-        acc[4 * j + 3] += f * x.w;
+      for (int u = 0; u < kBo; ++u) {
+        const int sl = b0 + u;
+        f[u] = 0.f;
+        if (sl < s1) {
+          const int64_t prow = int64_t(sl) * a.rows_per_item + rho;
+          const float4* src =
+              reinterpret_cast<const float4*>(a.ws.partial_o + prow * kHeadDim + DL * dl);
+#pragma unroll
+          for (int j = 0; j < DL / 4; ++j) x[u][j] = __ldcg(src + j);
+          float ls = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < kKeep; ++k) ls = (sl - s0 == k) ? keep[k] : ls;
+          if (sl - s0 >= kKeep) ls = lse_at(sl);
+          f[u] = ex2(ls - M);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBo; ++u) {
+        if (b0 + u < s1) {
+          L += f[u];
+#pragma unroll
+          for (int j = 0; j < DL / 4; ++j) {
+            acc[4 * j] += f[u] * x[u][j].x;
+            acc[4 * j + 1] += f[u] * x[u][j].y;
+            acc[4 * j + 2] += f[u] * x[u][j].z;
+            acc[4 * j + 3] += f[u] * x[u][j].w;
+          }
+        }
       }
     }
   }
@@ -1226,13 +1259,9 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
 
 template <bool BF16, int R, bool DEC, bool ROPE = false>
 cudaError_t launch_k(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, R, DEC, ROPE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = ensure_smem_limit(decode_tc_kernel<BF16, R, DEC, ROPE>, kSmem, configured);
+  if (e != cudaSuccess) return e;
   decode_tc_kernel<BF16, R, DEC, ROPE><<<grid, block_threads<ROPE>(), kSmem, stream>>>(prm);
   return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
 // internal.h -- data shared between the host planner, the C ABI and the
 // kernels of libattn.so (not part of the public interface).
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <string>
@@ -80,6 +81,13 @@ struct PlanLayout {
 };
 PlanLayout plan_layout(int32_t num_ctas, int64_t num_units, int64_t num_split,
                        int64_t num_slots, int32_t rows_per_item, int32_t head_dim);
+
+// Hash of a plan's host inputs (attn_plan_t::fingerprint); qo_indptr is NULL
+// for decode.
+uint64_t plan_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                          int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t causal, int32_t num_ctas);
 
 // Builds the plan tables into `host_tables` (table_bytes of them).
 // Returns ATTN_OK or an error with a message in *msg.
@@ -184,6 +192,28 @@ cudaError_t launch_wait_selftest(int32_t* error_word, uint64_t limit_ns, cudaStr
 
 // Sets the text attn_last_error() returns on this thread.
 void set_last_error(const std::string& msg);
+
+// Sets a kernel's dynamic shared-memory limit on the current device before
+// its first launch there (the attribute belongs to a device context, so a
+// process that runs on several devices sets it once per device). `done` is
+// the kernel's bitmask of devices already set; devices 64 and up are set on
+// every launch.
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Writes O = 0 and LSE = -inf for `rows` rows of num_heads x head_dim (a
+// plan whose requests hold no kv tokens at all: every visible set is empty).
+cudaError_t launch_fill_empty(void* o, float* lse, int64_t rows, int32_t dtype,
+                              cudaStream_t stream);
 
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,
                                 const float* lse_b, void* o_out, float* lse_out,

@@ -153,7 +153,27 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const SplitMergeArgs a
   if (lane == 0 && a.lse) a.lse[orow] = lse2 * kLn2;
 }
 
+// O = 0 and LSE = -inf for rows whose visible set is empty: 16 bytes of a
+// row (8 elements) per thread.
+__global__ void __launch_bounds__(256) fill_empty_kernel(void* o, float* lse, int64_t rows) {
+  const int64_t total = rows * (kHeadDim / 8);
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    reinterpret_cast<uint4*>(o)[i] = make_uint4(0, 0, 0, 0);
+    if (lse && i % (kHeadDim / 8) == 0) lse[i / (kHeadDim / 8)] = -INFINITY;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fill_empty(void* o, float* lse, int64_t rows, int32_t /*dtype: both 16-bit*/,
+                              cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  int64_t blocks = (rows * (kHeadDim / 8) + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  fill_empty_kernel<<<int(blocks), 256, 0, stream>>>(o, lse, rows);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,
                                 const float* lse_b, void* o_out, float* lse_out, int64_t rows,

@@ -45,6 +45,25 @@ attn_status_t noalloc_fail(attn_status_t s, const std::string& msg) {
   return s;
 }
 
+// Device address of the scratch array on the current device, looked up on
+// the first use there (with that device current). The caller holds the mutex.
+attn_status_t scratch_of_current_device(void** ws, const char* fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return noalloc_fail(ATTN_ERR_CUDA, std::string(fn) + ": no usable current device");
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return noalloc_fail(ATTN_ERR_CUDA, std::string(fn) + ": cudaGetSymbolAddress: " +
+                                             cudaGetErrorString(e));
+    g_scratch_ptr[dev] = p;
+  }
+  *ws = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -93,7 +112,7 @@ extern "C" attn_status_t attn_decode_run_noalloc(
     return noalloc_fail(ATTN_ERR_UNSUPPORTED, "attn_decode_run_noalloc: group > 8");
   if (batch > 0 && (!q || !o || !kv_indptr || !last_page_len))
     return noalloc_fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_noalloc: null device pointer");
-  if (plan.num_units > 0 && (!k_pool || !v_pool || !kv_indices))
+  if (plan.total_weight > plan.num_items && (!k_pool || !v_pool || !kv_indices))
     return noalloc_fail(ATTN_ERR_INVALID_ARG,
                         "attn_decode_run_noalloc: null KV pool or kv_indices");
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pool) |
@@ -103,16 +122,9 @@ extern "C" attn_status_t attn_decode_run_noalloc(
   if (batch == 0) return ATTN_OK;
 
   // One-time set-up per device: the device address of the scratch array.
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p)
-      return noalloc_fail(ATTN_ERR_CUDA,
-                          std::string("attn_decode_run_noalloc: cudaGetSymbolAddress: ") +
-                              cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
-  }
-  void* ws = g_scratch_ptr[dev];
+  void* ws = nullptr;
+  s = scratch_of_current_device(&ws, "attn_decode_run_noalloc");
+  if (s != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The table copy also zeroes the error word and the split-item counters.
   // The source is pageable static memory, so the call returns only once the
@@ -146,6 +158,49 @@ extern "C" attn_status_t attn_decode_run_noalloc(
   e = launch_decode(a, st);
   if (e != cudaSuccess)
     return noalloc_fail(ATTN_ERR_CUDA, std::string("attn_decode_run_noalloc: launch: ") +
+                                           cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+// Reads the error word at the head of the current device's scratch area.
+extern "C" attn_status_t attn_decode_run_noalloc_status(void* stream, int32_t* code_out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!code_out)
+    return noalloc_fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_noalloc_status: null output");
+  void* ws = nullptr;
+  attn_status_t s = scratch_of_current_device(&ws, "attn_decode_run_noalloc_status");
+  if (s != ATTN_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return noalloc_fail(ATTN_ERR_CUDA, std::string("attn_decode_run_noalloc_status: stream: ") +
+                                           cudaGetErrorString(e));
+  int32_t code = 0;
+  e = cudaMemcpy(&code, ws, sizeof code, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess)
+    return noalloc_fail(ATTN_ERR_CUDA, std::string("attn_decode_run_noalloc_status: read: ") +
+                                           cudaGetErrorString(e));
+  *code_out = code;
+  if (code != 0)
+    return noalloc_fail(ATTN_ERR_TIMEOUT,
+                        "attn_decode_run_noalloc: a kernel gave up a bounded wait (code " +
+                            std::to_string(code) + ")");
+  return ATTN_OK;
+}
+
+// The failure-detection self-test of attn_wait_selftest, aimed at the
+// no-allocation scratch area's error word.
+extern "C" attn_status_t attn_wait_selftest_noalloc(int32_t limit_us, void* stream) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (limit_us < 1 || limit_us > 10000000)
+    return noalloc_fail(ATTN_ERR_INVALID_ARG,
+                        "attn_wait_selftest_noalloc: limit_us must be in [1, 10^7]");
+  void* ws = nullptr;
+  attn_status_t s = scratch_of_current_device(&ws, "attn_wait_selftest_noalloc");
+  if (s != ATTN_OK) return s;
+  cudaError_t e = launch_wait_selftest(static_cast<int32_t*>(ws), uint64_t(limit_us) * 1000u,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return noalloc_fail(ATTN_ERR_CUDA, std::string("attn_wait_selftest_noalloc: launch: ") +
                                            cudaGetErrorString(e));
   return ATTN_OK;
 }

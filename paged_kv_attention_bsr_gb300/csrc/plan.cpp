@@ -12,12 +12,15 @@
 //   * decode: the costs are laid end to end and CTA c takes the contiguous
 //     positions [floor(c W / C), floor((c+1) W / C)) (Stream-K's equal cut);
 //     an item crossed by a boundary becomes several units;
-//   * append: items are dealt in order to the CTA with the least work so
-//     far (ties to the lowest index), each CTA capped at ceil(W / C) + 1; an
-//     item that does not fit is cut at the cap and continues on the next CTA.
-//     CTAs then run items in roughly the order of the list, so the query
+//   * append: the items of requests with at most 16 query rows (group x
+//     qo_len; decode-like) and the rest are interleaved by weight (prefill
+//     and decode requests of one batch run side by side, POD-style). Items
+//     are then dealt in that order to the CTA with the least work so far
+//     (ties to the lowest index), each CTA capped at ceil(W / C) + 1; an
+//     item that does not fit is cut at the cap and continues on the next
+//     CTA. CTAs run items in roughly the order of the list, so the query
 //     tiles of a kv head are in flight together and share its K/V pages
-//     through L2, while every CTA still gets an equal share;
+//     through L2, while every CTA gets an equal share;
 //   * units of an item cut in several ("split") write partial (o, lse)
 //     states that are merged by log-sum-exp.
 // Every CTA gets at most ceil(W/C) + 1 of the cost and the cut adds at most
@@ -63,6 +66,7 @@ namespace {
 struct Item {
   int32_t r, hk, t, n;
   int32_t page_base, kv_len, qo_start, qo_len;
+  int32_t few;  // the request has at most kFewRowMax query rows: decode-like
 };
 
 // Per-thread scratch reused across calls (a plan runs every step). One
@@ -76,7 +80,7 @@ struct Scratch {
   std::vector<int32_t> gen_cta;  // and their CTA and item
   std::vector<int32_t> gen_item;
   std::vector<int64_t> load;
-  std::vector<int32_t> n_units, split_of, merge_indptr, next, work_indptr, at;
+  std::vector<int32_t> n_units, split_of, merge_indptr, next, work_indptr, at, order;
   std::vector<int4> merge_items;
   std::vector<Unit> units;       // CTA order (append)
 };
@@ -95,6 +99,18 @@ uint64_t fnv1a(uint64_t h, const void* data, size_t bytes) {
 }
 
 }  // namespace
+
+uint64_t plan_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                          int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t causal, int32_t num_ctas) {
+  uint64_t h = 1469598103934665603ull;
+  h = fnv1a(h, kv_indptr, 4 * (size_t(batch) + 1));
+  if (batch) h = fnv1a(h, last_page_len, 4 * size_t(batch));
+  if (qo_indptr) h = fnv1a(h, qo_indptr, 4 * (size_t(batch) + 1));
+  const int32_t shape[6] = {page_size, num_qo_heads, num_kv_heads, head_dim, causal, num_ctas};
+  return fnv1a(h, shape, sizeof shape);
+}
 
 attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
                          const int32_t* last_page_len, int32_t batch, int32_t page_size,
@@ -187,7 +203,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
         }
         const int64_t n = (vis + page_size - 1) / page_size;
         items.push_back({r, hk, int32_t(t), int32_t(n), kv_indptr[r], int32_t(kv_len),
-                         decode ? r : qo_indptr[r], int32_t(qo_len)});
+                         decode ? r : qo_indptr[r], int32_t(qo_len),
+                         int64_t(group) * qo_len <= kFewRowMax ? 1 : 0});
       }
     }
   }
@@ -278,14 +295,51 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
     }
     for (int64_t i = 0; i < C; ++i) load[size_t(i)] = bound(i + 1) - bound(i);
   } else {
-    // Time-ordered fill: items go, in order, to the CTA with the least work
-    // so far (ties: lowest index), each CTA capped at ceil(W / C) + 1; an item
-    // that does not fit is cut at the cap and continues on the next CTA.
+    // Visiting order (prefill and decode in one plan, POD-style): the items
+    // of requests with at most kFewRowMax query rows (decode-like,
+    // memory-bound) and the other items (tensor-bound) keep their own order
+    // and are interleaved by weight -- the next item comes from the class
+    // that has used the smaller fraction of its total weight, ties to the
+    // tensor-bound class -- so that every CTA's list mixes both kinds over
+    // time and HBM streaming overlaps the tensor work across the SMs.
+    std::vector<int32_t>& order = sc.order;
+    order.clear();
+    {
+      int64_t wd = 0, wf = 0;
+      for (const Item& it : items) (it.few ? wf : wd) += it.n + kAlpha;
+      size_t id = 0, jf = 0;
+      int64_t dd = 0, df = 0;
+      auto next_of = [&](size_t i, int32_t few) {
+        while (i < items.size() && items[i].few != few) ++i;
+        return i;
+      };
+      id = next_of(0, 0);
+      jf = next_of(0, 1);
+      while (id < items.size() || jf < items.size()) {
+        const bool dense = jf >= items.size() || (id < items.size() && dd * wf <= df * wd);
+        const size_t k = dense ? id : jf;
+        const int64_t w = items[k].n + kAlpha;
+        order.push_back(int32_t(k));
+        if (dense) {
+          dd += w;
+          id = next_of(id + 1, 0);
+        } else {
+          df += w;
+          jf = next_of(jf + 1, 1);
+        }
+      }
+    }
+    // Time-ordered fill: items go, in that order, to the CTA with the least
+    // work so far (ties: lowest index), each CTA capped at ceil(W / C) + 1;
+    // an item that does not fit is cut at the cap and continues on the next
+    // CTA. (A page weighs the same for one or two live query tiles: the two
+    // tiles' softmax warpgroups run side by side, and they set the pace.)
     const int64_t cap = (W + C - 1) / C + kAlpha;
     typedef std::pair<int64_t, int32_t> Slot;
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> ready;
     for (int32_t c = 0; c < num_ctas; ++c) ready.push(Slot(0, c));
-    for (size_t k = 0; k < items.size(); ++k) {
+    for (const int32_t k32 : order) {
+      const size_t k = size_t(k32);
       const Item& it = items[k];
       int64_t p = 0;
       for (;;) {
@@ -408,12 +462,8 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   p.off_partial_lse = L.off_partial_lse;
   p.table_bytes = L.table_bytes;
   p.dev_bytes_needed = L.dev_bytes;
-  uint64_t h = 1469598103934665603ull;
-  h = fnv1a(h, kv_indptr, 4 * (size_t(batch) + 1));
-  if (batch) h = fnv1a(h, last_page_len, 4 * size_t(batch));
-  if (!decode) h = fnv1a(h, qo_indptr, 4 * (size_t(batch) + 1));
-  const int32_t shape[6] = {page_size, num_qo_heads, num_kv_heads, head_dim, p.causal, num_ctas};
-  p.fingerprint = fnv1a(h, shape, sizeof shape);
+  p.fingerprint = plan_fingerprint(qo_indptr, kv_indptr, last_page_len, batch, page_size,
+                                   num_qo_heads, num_kv_heads, head_dim, p.causal, num_ctas);
   p.max_kv_len = max_kv_len;
   p.min_kv_minus_qo = min_kv_minus_qo;
   *plan = p;

@@ -252,6 +252,58 @@ def causal_append(seed: int = SEED_BASE + 5, batch: int = 16,
                            pool_pages, 32, 8, torch.bfloat16, seed, causal=True)
 
 
+def pod_mixed_batch(seed: int = SEED_BASE + 7, n_prefill: int = 16, n_decode: int = 64,
+                    pool_pages: int = 30000) -> Workload:
+    """One serving batch with both kinds of request (POD-style prefill +
+    decode): the causal-append shape (16 chunks of U[128, 1024] new tokens on
+    U[0, 8192] existing ones) and the uniform GQA decode shape (64 requests,
+    kv_len U[1024, 4096], one new token), Hq = 32, Hk = 8, bf16, P = 16, in
+    one shuffled pool and one request order (shuffled). ``extra`` lists which
+    requests are prefill and which decode, so that the same batch can also
+    be run as two separate launches."""
+    rng = np.random.default_rng(seed)
+    qo_p = rng.integers(128, 1024, size=n_prefill, endpoint=True)
+    kv_p = rng.integers(0, 8192, size=n_prefill, endpoint=True) + qo_p
+    kv_d = rng.integers(1024, 4096, size=n_decode, endpoint=True)
+    qo_lens = np.concatenate([qo_p, np.ones(n_decode, np.int64)])
+    kv_lens = np.concatenate([kv_p, kv_d])
+    perm = rng.permutation(len(qo_lens))
+    w = append_workload("pod_mixed_prefill16_decode64_h32kv8_p16_bf16", qo_lens[perm],
+                        kv_lens[perm], 16, pool_pages, 32, 8, torch.bfloat16, seed, causal=True)
+    w.extra["prefill"] = np.nonzero(qo_lens[perm] > 1)[0]
+    w.extra["decode"] = np.nonzero(qo_lens[perm] == 1)[0]
+    return w
+
+
+def sub_batch(w: Workload, rows, as_decode: bool = False) -> Workload:
+    """The requests `rows` of an append workload as a batch of their own, on
+    the same pool (page table and queries gathered; values shared). With
+    as_decode, every request must have one query row and the result is a
+    decode workload."""
+    c = w.cache
+    rows = np.asarray(rows, np.int64)
+    n = np.diff(c.kv_indptr)[rows]
+    indptr = np.zeros(len(rows) + 1, np.int32)
+    indptr[1:] = np.cumsum(n)
+    indices = np.concatenate([c.kv_indices[c.kv_indptr[r]:c.kv_indptr[r + 1]] for r in rows]
+                             ) if len(rows) else np.zeros(0, np.int32)
+    cache = BSRCache(c.page_size, c.num_kv_heads, c.head_dim, c.k_pool, c.v_pool, indptr,
+                     indices.astype(np.int32), c.last_page_len[rows].copy(),
+                     c.kv_lens[rows].copy())
+    qo = np.diff(w.qo_indptr)[rows]
+    q_rows = np.concatenate([np.arange(w.qo_indptr[r], w.qo_indptr[r + 1]) for r in rows])
+    q = w.q[torch.from_numpy(q_rows)]
+    if as_decode:
+        if np.any(qo != 1):
+            raise ValueError("a decode sub-batch needs one query row per request")
+        return Workload(w.name + "_decode", "decode", w.dtype, w.num_qo_heads, w.num_kv_heads,
+                        w.head_dim, w.sm_scale, q, cache)
+    qo_indptr = np.zeros(len(rows) + 1, np.int32)
+    qo_indptr[1:] = np.cumsum(qo)
+    return Workload(w.name + "_sub", "append", w.dtype, w.num_qo_heads, w.num_kv_heads,
+                    w.head_dim, w.sm_scale, q, cache, qo_indptr=qo_indptr, causal=w.causal)
+
+
 def flat_layout_of_composable(w: Workload, page_size: int = 16) -> BSRCache:
     """The same logical KV as a shared-prefix workload, in one pool with one page
     size: each generation's table lists its prompt's prefix pages (shared by
@@ -298,4 +350,5 @@ WORKLOADS = {
     "shared_prefix": shared_prefix_decode,
     "causal_append": causal_append,
     "sparse_decode": vector_sparse_decode,
+    "pod_mixed": pod_mixed_batch,
 }

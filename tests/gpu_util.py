@@ -54,3 +54,57 @@ def poison_unused_slots(cache):
     bad = ~valid  # [pages, P] -> HND pools [pages, Hk, P, D]
     for pool in (cache.k_pool, cache.v_pool):
         pool.permute(0, 2, 1, 3)[bad] = float("nan")
+
+
+def oracle_decode_threaded(oracle_mod, w, threads=16):
+    """The fp64 oracle over every row of a decode batch, requests split across
+    host threads (the C oracle releases the GIL). Returns (o, lse) like
+    oracle_mod.batch_attention."""
+    import concurrent.futures as cf
+    c = w.cache
+    dt = oracle_dtype(oracle_mod, w.dtype)
+    chunks = [x for x in np.array_split(np.arange(w.batch), threads) if len(x)]
+
+    def job(rs):
+        a, b = int(rs[0]), int(rs[-1]) + 1
+        return oracle_mod.batch_attention(w.q[a:b], c.k_pool, c.v_pool, c.kv_indptr[a:b + 1],
+                                          c.kv_indices, c.last_page_len[a:b], c.page_size,
+                                          w.num_qo_heads, w.num_kv_heads, w.head_dim, dt,
+                                          w.sm_scale)
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(job, chunks))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
+def oracle_rows_threaded(oracle_mod, w, rows, causal, qo_indptr=None, threads=16):
+    """The fp64 oracle on selected (request, query index, query head) rows,
+    across host threads. Returns (o [n, D], lse [n])."""
+    import concurrent.futures as cf
+    c = w.cache
+    dt = oracle_dtype(oracle_mod, w.dtype)
+    chunks = [x for x in np.array_split(np.arange(len(rows)), threads) if len(x)]
+
+    def job(idx):
+        out_o = np.zeros((len(idx), w.head_dim))
+        out_l = np.zeros(len(idx))
+        for j, k in enumerate(idx):
+            r, i, h = rows[k]
+            out_o[j], out_l[j] = oracle_mod.attention_row(
+                w.q, c.k_pool, c.v_pool, c.kv_indptr, c.kv_indices, c.last_page_len,
+                c.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, dt, w.sm_scale, r, i,
+                h, causal=causal, qo_indptr=qo_indptr)
+        return out_o, out_l
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(job, chunks))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
+def split_items_of_plan(att):
+    """(r, hk, t, n_units) of every split item of the plan `att` (a
+    PagedAttention) last made, read from its pinned host copy of the tables."""
+    p = att.plan_info
+    buf = att._pinned[(att._turn - 1) % att.RING].numpy()
+    raw = buf[p.off_merge_items:p.off_merge_items + 16 * p.num_split_items]
+    return raw.view(np.int32).reshape(-1, 4).copy()

@@ -81,7 +81,7 @@ def test_workspace_size_and_validation_without_gpu():
     assert C.lib.attn_decode_run_rope(ctypes.byref(pr3), fake, fake, fake, 8, 0, fake, fake,
                                       fake, 1, ctypes.c_float(0.1), fake, fake, 48, fake, None,
                                       fake, 1 << 30, None) == C.ERR_UNSUPPORTED
-    # fused RoPE append: kv_len >= qo_len, short appends only
+    # fused RoPE append: kv_len >= qo_len
     def append_rope(qo, causal, cos=fake):
         pa = C.plan(np.array(qo, np.int32), kvi, lpl, 16, 8, 2, 128, causal, 4, buf)
         return pa, C.lib.attn_append_run_rope(
@@ -89,8 +89,6 @@ def test_workspace_size_and_validation_without_gpu():
             ctypes.c_float(0.1), cos, cos, 48, fake, None, fake, 1 << 30, None)
     pa, st = append_rope([0, 30, 31], False)  # request 0: 19 kv tokens, 30 queries
     assert pa.min_kv_minus_qo == -11 and st == C.ERR_INVALID_ARG
-    pa, st = append_rope([0, 5, 6], True)  # group 4 x 5 queries = 20 rows > 16
-    assert pa.min_kv_minus_qo == 14 and st == C.ERR_UNSUPPORTED
     _, st = append_rope([0, 2, 3], True, ctypes.c_void_p(260))  # misaligned tables
     assert st == C.ERR_INVALID_ARG
     # a pool past 2^31 (page, head, slot) rows: UNSUPPORTED with the reason,
@@ -151,6 +149,61 @@ def test_run_size_checks_in_the_binding():
     for qq, kp, vp, oo, ll, n in bad:
         with pytest.raises(ValueError):
             C._check_sizes(p, qq, kp, vp, oo, ll, n, p.batch)
+    # a plan whose requests hold no kv tokens runs without a pool
+    pe = C.plan(None, np.array([0, 0, 0], np.int32), np.array([0, 0], np.int32), 16, 8, 2, 128,
+                False, 4, np.zeros(host, np.uint8))
+    empty = torch.zeros(0, 2, 16, 128, dtype=bf)
+    C._check_sizes(pe, q, empty, empty, q, lse, 0, pe.batch)
+
+
+def test_strided_views_are_rejected_by_the_binding():
+    """The kernels read every tensor as a dense block from its data pointer:
+    strided views (a K slice of a [L, 2, H, D] tensor, a transposed q, a
+    sliced pool) are rejected instead of being read with the wrong layout."""
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    import torch
+    _, host = C.workspace_size(4, 4, 8, 2, 128, 4)
+    p = C.plan(None, np.array([0, 2, 3], np.int32), np.array([5, 16], np.int32), 16, 8, 2, 128,
+               False, 4, np.zeros(host, np.uint8))
+    bf = torch.bfloat16
+    q = torch.zeros(2, 8, 128, dtype=bf)
+    pool = torch.zeros(3, 2, 16, 128, dtype=bf)
+    lse = torch.zeros(2, 8)
+    kv = torch.zeros(3, 2, 2, 16, 128, dtype=bf)  # [pages, K/V, Hk, P, D]
+    q_t = torch.zeros(8, 2, 128, dtype=bf).transpose(0, 1)
+    big = torch.zeros(4, 2, 16, 256, dtype=bf)[..., :128]
+    for args in [(q, kv[:, 0], pool, q, lse), (q, pool, kv[:, 1], q, lse),
+                 (q_t, pool, pool, q, lse), (q, big, big, q, lse),
+                 (q, pool, pool, q_t, lse), (q, pool, pool, q, torch.zeros(8, 2).t())]:
+        with pytest.raises(ValueError, match="contiguous"):
+            C._check_sizes(p, *args, 3, p.batch)
+    o = torch.zeros(4, 2, 128, dtype=bf)
+    l = torch.zeros(4, 2)
+    with pytest.raises(ValueError, match="contiguous"):
+        C.merge_states(o, l, torch.zeros(2, 4, 128, dtype=bf).transpose(0, 1), l, o, l)
+    with pytest.raises(ValueError, match="contiguous"):
+        C.merge_states(o, torch.zeros(2, 4).t(), o, l, o, l)
+
+
+def test_noalloc_binding_checks_sizes():
+    """decode_run_noalloc checks its tensors against the explicit shapes
+    before the library is called (the C side only sees raw pointers)."""
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    import torch
+    bf = torch.bfloat16
+    kvi = np.array([0, 2, 3], np.int32)
+    lpl = np.array([5, 16], np.int32)
+    q = torch.zeros(2, 8, 128, dtype=bf)
+    pool = torch.zeros(3, 2, 16, 128, dtype=bf)
+    lse = torch.zeros(2, 8)
+    d32 = torch.zeros(3, dtype=torch.int32)
+    for qq, kp, vp, oo, ll in [(q, pool[:, :1].contiguous(), pool, q, lse),
+                               (q[:1], pool, pool, q, lse), (q, pool, pool, q[:1], lse),
+                               (q, pool, pool, q, lse[:1]), (q, pool.half(), pool, q, lse),
+                               (q, pool[:2], pool, q, lse)]:
+        with pytest.raises(ValueError):
+            C.decode_run_noalloc(kvi, lpl, 16, 8, 2, 128, qq, kp, vp, d32, d32, d32, 0.1, oo,
+                                 ll, num_pages=3)
 
 
 def test_merge_shape_checks_in_the_binding():

@@ -110,14 +110,32 @@ def test_sparse_short_append_parity(oracle_mod, case, num_ctas):
     assert_attn_close(o, lse, o_ref, lse_ref, f"sparse short append {case} ctas {num_ctas}")
 
 
-def test_sparse_long_append_is_unsupported():
-    from paged_kv_attention_bsr_gb300 import _capi as C
-    from tests.test_gpu_append import run_append
-    w = synth.append_workload("sparselong", [40], [100], 3, 40, 32, 8, torch.bfloat16,
-                              seed=970, causal=True)
-    with pytest.raises(C.AttnError) as ei:
-        run_append(w)
-    assert ei.value.status == C.ERR_UNSUPPORTED
+LONG_APPEND_CASES = [
+    # (P, Hq, Hk, dtype, qo_lens, extra kv, causal, layout): past 16 packed
+    # rows, so the append kernel gathers rows four at a time
+    (1, 32, 8, torch.bfloat16, [40, 130, 1, 257], [0, 300, 1000, 17], True, 0),
+    (3, 32, 8, torch.bfloat16, [100, 33, 7], [100, 700, 2], True, 0),
+    (3, 16, 4, torch.float16, [64, 200], [500, 3], False, 0),
+    (5, 32, 8, torch.bfloat16, [90, 20], [77, 400], True, 1),
+    (1, 16, 2, torch.bfloat16, [300], [129], True, 1),
+]
+
+
+@pytest.mark.parametrize("case", range(len(LONG_APPEND_CASES)))
+@pytest.mark.parametrize("num_ctas", [1, 5, None])
+def test_sparse_long_append_parity(oracle_mod, case, num_ctas):
+    """Causal and non-causal appends past 16 packed rows at page sizes 1, 3
+    and 5 (HND and NHD), stale pool slots set to NaN."""
+    from tests.test_gpu_append import oracle_full as append_oracle, run_append
+    P, Hq, Hk, dtype, qo_lens, extra, causal, layout = LONG_APPEND_CASES[case]
+    kv_lens = [q + e for q, e in zip(qo_lens, extra)]
+    pool = sum(-(-L // P) for L in kv_lens) + 9
+    w = synth.append_workload(f"sparselong{case}", qo_lens, kv_lens, P, pool, Hq, Hk, dtype,
+                              seed=970 + case, causal=causal)
+    poison_unused_slots(w.cache)
+    o_ref, lse_ref = append_oracle(oracle_mod, w)
+    o, lse, _ = run_append(w, num_ctas, layout=layout)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"sparse long append {case} ctas {num_ctas}")
 
 
 @pytest.mark.parametrize("P", [1, 5])

@@ -129,6 +129,8 @@ def test_plan_properties(decode):
             assert segs[0][0] == 0 and segs[-1][1] == n
             for (a0, a1), (b0, b1) in zip(segs, segs[1:]):
                 assert a1 == b0 and a0 < a1
+        # weights: pages + 1 per item
+        assert p.total_weight == sum(n + 1 for n in items.values())
         # balance: the page share of every CTA is at most ceil(W / C)
         W = p.total_weight
         wi = t["work_indptr"]
@@ -226,3 +228,39 @@ def test_plan_length_summaries(decode):
         has_kv = kv_len > 0
         want = int((kv_len - qo_len)[has_kv].min()) if has_kv.any() else np.iinfo(np.int64).max
         assert p.min_kv_minus_qo == want
+
+
+def test_plan_mixed_prefill_and_decode_batch():
+    """A batch of long prefill chunks and single-token decodes in one append
+    plan (POD-style): bit-exact against the reference, the decode-like items
+    spread through every part of the visiting order, and the two classes'
+    weights interleaved so that no CTA list is all of one kind at its start."""
+    rng = np.random.default_rng(20260020)
+    for ctas in (7, 152):
+        qo_lens = np.concatenate([rng.integers(128, 1024, 6), np.ones(40, np.int64)])
+        perm = rng.permutation(len(qo_lens))
+        qo_lens = qo_lens[perm]
+        kv_lens = qo_lens + rng.integers(0, 4000, len(qo_lens))
+        n = (kv_lens + 15) // 16
+        kv_indptr = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+        last = (kv_lens - 16 * (n - 1)).astype(np.int32)
+        qo = np.concatenate([[0], np.cumsum(qo_lens)]).astype(np.int32)
+        p, t, _ = _lib_plan(kv_indptr, last, 16, 32, 8, ctas, qo, True)
+        ref = plan_ref.make_plan(kv_indptr.tolist(), last.tolist(), 16, 32, 8, ctas,
+                                 qo_indptr=qo.tolist(), causal=True)
+        assert t["work_indptr"] == ref.work_indptr
+        u = t["units"]
+        assert u[:, 0].tolist() == ref.unit_r and u[:, 3].tolist() == ref.unit_p0
+        assert u[:, 4].tolist() == ref.unit_p1 and u[:, 5].tolist() == ref.unit_slot
+        # decode requests (qo_len 1) are spread over the CTAs and through
+        # their lists (interleaved with the prefill tiles, not all at the end)
+        decode_r = set(np.nonzero(qo_lens == 1)[0].tolist())
+        wi = t["work_indptr"]
+        holders, pos = 0, []
+        for c in range(ctas):
+            rs = [int(x) for x in u[wi[c]:wi[c + 1], 0]]
+            at = [i / max(len(rs) - 1, 1) for i, r in enumerate(rs) if r in decode_r]
+            holders += bool(at)
+            pos.extend(at)
+        assert holders >= ctas // 2
+        assert 0.3 <= float(np.mean(pos)) <= 0.7

@@ -137,6 +137,32 @@ def test_llama31_tables_match_sdpa_on_numpy_rotated_inputs(causal):
     assert np.abs(o - o0).max() > 1e-2
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_rope_matches_sdpa_on_numpy_rotated_inputs(causal):
+    """oracle_attention_row_rope (one row at a time) against the numpy
+    rotation + torch float64 SDPA reference, on every row of a small ragged
+    batch (and a few rows sit at positions near the end of the table)."""
+    cos, sin = synth.rope_tables(1200)
+    P = 3
+    qo, ex = [1, 9, 20], [0, 500, 1171]
+    kv = [a + b for a, b in zip(qo, ex)]
+    pool = sum(-(-L // P) for L in kv) + 3
+    w = synth.append_workload("rr", qo, kv, P, pool, 16, 4, torch.bfloat16, seed=13,
+                              causal=causal)
+    o_ref, l_ref = _reference(w, cos, sin, oracle.BF16, causal)
+    c = w.cache
+    for r in range(w.batch):
+        for i in range(qo[r]):
+            for h in (0, 5, 15):
+                o, l = oracle.attention_row_rope(
+                    w.q, c.k_pool, c.v_pool, c.kv_indptr, c.kv_indices, c.last_page_len, P,
+                    16, 4, 128, oracle.BF16, w.sm_scale, cos, sin, r, i, h, causal=causal,
+                    qo_indptr=w.qo_indptr)
+                row = int(w.qo_indptr[r]) + i
+                assert np.abs(o - o_ref[row, h]).max() < 1e-12
+                assert abs(l - l_ref[row, h]) < 1e-12
+
+
 def test_rounding_matches_torch_conversions():
     rng = np.random.default_rng(5)
     vals = np.concatenate([rng.normal(0, 10, 2000), rng.normal(0, 1e-6, 200),
