@@ -74,6 +74,12 @@ def _load():
             lib.oracle_attention_row_rope.argtypes = [
                 vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32, i32, i32,
                 i32, i32, dbl, vp, vp, i64, i32, i32, i32, vp, vp]
+            lib.oracle_widen_e4m3.restype = dbl
+            lib.oracle_widen_e4m3.argtypes = [ctypes.c_uint8]
+            lib.oracle_batch_attention_fp8kv.restype = i32
+            lib.oracle_batch_attention_fp8kv.argtypes = [
+                vp, vp, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                i32, i32, dbl, vp, vp, vp, vp]
             lib.oracle_round.restype = dbl
             lib.oracle_round.argtypes = [dbl, i32]
             lib.oracle_merge_states.restype = None
@@ -156,6 +162,45 @@ def batch_attention_rope(q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len
         float(sm_scale), _ptr(cos), _ptr(sin), cos.shape[0], _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_batch_attention_rope rejected its arguments (code {rc})")
+    return o, lse
+
+
+def widen_e4m3(bits: int) -> float:
+    return _load().oracle_widen_e4m3(int(bits) & 0xFF)
+
+
+def _u8(a) -> np.ndarray:
+    """Raw bytes of an FP8 tensor (torch float8 / uint8) or a uint8 array."""
+    if hasattr(a, "detach"):
+        import torch
+        a = a.detach().contiguous().cpu().view(torch.uint8).numpy()
+    return np.ascontiguousarray(a).view(np.uint8)
+
+
+def batch_attention_fp8kv(q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
+                          page_size, num_qo_heads, num_kv_heads, head_dim, q_dtype, sm_scale,
+                          k_scale, v_scale, causal=False, qo_indptr=None, layout=HND):
+    """All rows with an FP8 E4M3 K/V cache (bytes) and per-kv-head float
+    scales. Returns (o float64 [total_qo, Hq, D], lse float64 [total_qo, Hq])."""
+    lib = _load()
+    q16, k8, v8 = _u16(q), _u8(k_pool), _u8(v_pool)
+    kv_indptr, kv_indices = _i32(kv_indptr), _i32(kv_indices)
+    last_page_len, qo_indptr = _i32(last_page_len), _i32(qo_indptr)
+    ks = np.ascontiguousarray(k_scale, np.float32)
+    vs = np.ascontiguousarray(v_scale, np.float32)
+    assert ks.shape == (num_kv_heads,) and vs.shape == (num_kv_heads,)
+    batch = len(kv_indptr) - 1
+    total_qo = int(qo_indptr[-1]) if qo_indptr is not None else batch
+    num_pages = k8.size // (page_size * num_kv_heads * head_dim)
+    o = np.zeros((total_qo, num_qo_heads, head_dim), np.float64)
+    lse = np.zeros((total_qo, num_qo_heads), np.float64)
+    rc = lib.oracle_batch_attention_fp8kv(
+        _ptr(q16), _ptr(qo_indptr), _ptr(k8), _ptr(v8), num_pages, layout, _ptr(kv_indptr),
+        _ptr(kv_indices), _ptr(last_page_len), batch, page_size, num_qo_heads, num_kv_heads,
+        head_dim, q_dtype, int(bool(causal)), float(sm_scale), _ptr(ks), _ptr(vs), _ptr(o),
+        _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_batch_attention_fp8kv rejected its arguments (code {rc})")
     return o, lse
 
 

@@ -360,6 +360,122 @@ int32_t oracle_batch_attention_rope(const uint16_t* q, const int32_t* qo_indptr,
                          rope_cos, rope_sin, o, lse);
 }
 
+double oracle_widen_e4m3(uint8_t bits) {
+  /* FP8 E4M3 (the "fn" encoding: no infinities, S.1111.111 is NaN):
+     1 sign, 4 exponent (bias 7), 3 fraction bits. */
+  int sign = bits >> 7;
+  int e = (bits >> 3) & 0xf;
+  int m = bits & 7;
+  double v;
+  if (e == 15 && m == 7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)m, -9);             /* subnormal: (m / 8) * 2^-6 */
+  else
+    v = ldexp((double)(8 + m), e - 10);   /* (1 + m / 8) * 2^(e - 7) */
+  return sign ? -v : v;
+}
+
+/*
+ * One row with an FP8 (E4M3) K/V cache: the stored byte of kv head hk means
+ * widen(byte) * k_scale[hk] (keys) or * v_scale[hk] (values); q is 16-bit.
+ * Same definition and order as attention_row.
+ */
+static void attention_row_fp8(const uint16_t* q, const int32_t* qo_indptr,
+                              const uint8_t* k_pool, const uint8_t* v_pool, int32_t layout,
+                              const int32_t* kv_indptr, const int32_t* kv_indices,
+                              const int32_t* last_page_len, int32_t page_size,
+                              int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t q_dtype, int32_t causal, double sm_scale,
+                              const float* k_scale, const float* v_scale, int32_t r,
+                              int32_t i, int32_t h, double* x_buf, double* q_buf, double* o,
+                              double* lse) {
+  const int32_t group = num_qo_heads / num_kv_heads;
+  const int32_t hk = h / group;
+  const int64_t qo_start = qo_indptr ? qo_indptr[r] : r;
+  const int64_t qo_len = qo_indptr ? (int64_t)qo_indptr[r + 1] - qo_indptr[r] : 1;
+  const int64_t kv_len = bsr_kv_len(kv_indptr, last_page_len, page_size, r);
+  int64_t vis = kv_len;
+  if (causal) {
+    int64_t lim = kv_len - qo_len + i + 1;
+    if (lim < vis) vis = lim;
+  }
+  if (vis < 0) vis = 0;
+  const uint16_t* qrow = q + ((qo_start + i) * num_qo_heads + h) * head_dim;
+  for (int32_t d = 0; d < head_dim; ++d) q_buf[d] = oracle_widen(qrow[d], q_dtype);
+  for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+  if (vis <= 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  const double ks = k_scale[hk], vs = v_scale[hk];
+  double m = -INFINITY;
+  for (int64_t j = 0; j < vis; ++j) {
+    int64_t page = kv_indices[kv_indptr[r] + j / page_size];
+    int64_t slot = j % page_size;
+    int64_t row = layout == ORACLE_HND ? (page * num_kv_heads + hk) * page_size + slot
+                                       : (page * page_size + slot) * num_kv_heads + hk;
+    const uint8_t* krow = k_pool + row * head_dim;
+    double dot = 0.0;
+    for (int32_t d = 0; d < head_dim; ++d) dot += q_buf[d] * (oracle_widen_e4m3(krow[d]) * ks);
+    double x = sm_scale * dot;
+    x_buf[j] = x;
+    if (x > m) m = x;
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j < vis; ++j) {
+    int64_t page = kv_indices[kv_indptr[r] + j / page_size];
+    int64_t slot = j % page_size;
+    int64_t row = layout == ORACLE_HND ? (page * num_kv_heads + hk) * page_size + slot
+                                       : (page * page_size + slot) * num_kv_heads + hk;
+    const uint8_t* vrow = v_pool + row * head_dim;
+    double p = exp(x_buf[j] - m);
+    l += p;
+    for (int32_t d = 0; d < head_dim; ++d) o[d] += p * (oracle_widen_e4m3(vrow[d]) * vs);
+  }
+  for (int32_t d = 0; d < head_dim; ++d) o[d] /= l;
+  *lse = m + log(l);
+}
+
+int32_t oracle_batch_attention_fp8kv(const uint16_t* q, const int32_t* qo_indptr,
+                                     const uint8_t* k_pool, const uint8_t* v_pool,
+                                     int64_t num_pages, int32_t layout,
+                                     const int32_t* kv_indptr, const int32_t* kv_indices,
+                                     const int32_t* last_page_len, int32_t batch,
+                                     int32_t page_size, int32_t num_qo_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t q_dtype,
+                                     int32_t causal, double sm_scale, const float* k_scale,
+                                     const float* v_scale, double* o, double* lse) {
+  if (!k_scale || !v_scale) return -1;
+  int32_t rc = check_args(qo_indptr, num_pages, layout, kv_indptr, kv_indices,
+                          last_page_len, batch, page_size, num_qo_heads,
+                          num_kv_heads, head_dim, q_dtype);
+  if (rc) return rc;
+  int64_t mx = max_kv_len(kv_indptr, last_page_len, page_size, batch);
+  double* x_buf = (double*)malloc(sizeof(double) * (size_t)mx);
+  double* q_buf = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  if (!x_buf || !q_buf) {
+    free(x_buf);
+    free(q_buf);
+    return -100;
+  }
+  for (int32_t r = 0; r < batch; ++r) {
+    int64_t qo_start = qo_indptr ? qo_indptr[r] : r;
+    int64_t qo_len = qo_indptr ? (int64_t)qo_indptr[r + 1] - qo_indptr[r] : 1;
+    for (int64_t i = 0; i < qo_len; ++i)
+      for (int32_t h = 0; h < num_qo_heads; ++h) {
+        int64_t row = (qo_start + i) * num_qo_heads + h;
+        attention_row_fp8(q, qo_indptr, k_pool, v_pool, layout, kv_indptr, kv_indices,
+                          last_page_len, page_size, num_qo_heads, num_kv_heads, head_dim,
+                          q_dtype, causal, sm_scale, k_scale, v_scale, r, (int32_t)i, h,
+                          x_buf, q_buf, o + row * head_dim, lse + row);
+      }
+  }
+  free(x_buf);
+  free(q_buf);
+  return 0;
+}
+
 void oracle_merge_states(const double* o_in, const double* lse_in,
                          int32_t n_states, int64_t rows, int32_t head_dim,
                          double* o_out, double* lse_out) {

@@ -45,6 +45,25 @@ enum { ORACLE_HND = 0, ORACLE_NHD = 1 };
 /* Exact widening of one stored 16-bit value to double. */
 double oracle_widen(uint16_t bits, int32_t dtype);
 
+/* Exact widening of one FP8 E4M3 byte (no infinities; 0x7f / 0xff are NaN). */
+double oracle_widen_e4m3(uint8_t bits);
+
+/*
+ * All rows with an FP8 (E4M3) K/V cache and per-kv-head scales: the stored
+ * byte b of kv head hk stands for widen_e4m3(b) * k_scale[hk] (keys) or
+ * widen_e4m3(b) * v_scale[hk] (values); q is 16-bit (q_dtype). Pools are
+ * bytes in `layout`. Same definition as oracle_batch_attention otherwise.
+ */
+int32_t oracle_batch_attention_fp8kv(const uint16_t* q, const int32_t* qo_indptr,
+                                     const uint8_t* k_pool, const uint8_t* v_pool,
+                                     int64_t num_pages, int32_t layout,
+                                     const int32_t* kv_indptr, const int32_t* kv_indices,
+                                     const int32_t* last_page_len, int32_t batch,
+                                     int32_t page_size, int32_t num_qo_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t q_dtype,
+                                     int32_t causal, double sm_scale, const float* k_scale,
+                                     const float* v_scale, double* o, double* lse);
+
 /*
  * Attention output of one (request r, query row i, query head h).
  *   q            : [total_qo, Hq, D] raw 16-bit words (decode: total_qo = batch)

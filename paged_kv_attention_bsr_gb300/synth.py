@@ -38,6 +38,8 @@ class BSRCache:
     kv_indices: np.ndarray        # int32 [nnz]
     last_page_len: np.ndarray     # int32 [B]
     kv_lens: np.ndarray           # int64 [B] (the lengths the table was built from)
+    k_scale: Optional[torch.Tensor] = None  # FP8 pools: float32 [Hk] per-head scales
+    v_scale: Optional[torch.Tensor] = None
 
     @property
     def num_pages(self) -> int:
@@ -103,6 +105,38 @@ def make_cache(kv_lens, page_size: int, pool_pages: int, num_kv_heads: int,
     v_pool = normal_values(shape, dtype, seed * 4 + 2)
     return BSRCache(page_size, num_kv_heads, head_dim, k_pool, v_pool, kv_indptr,
                     kv_indices, last, np.asarray(kv_lens, np.int64))
+
+
+def make_fp8_cache(kv_lens, page_size: int, pool_pages: int, num_kv_heads: int, seed: int,
+                   head_dim: int = HEAD_DIM, shuffle_pool: bool = True) -> BSRCache:
+    """A pool stored as FP8 E4M3 bytes with one scale per kv head (for K and
+    for V): values drawn N(0, 1) in fp32, scale = the head's largest |value|
+    / 448 (the largest E4M3 magnitude), stored = value / scale rounded to E4M3
+    by torch's conversion. k_pool / v_pool are uint8 tensors of the bytes;
+    the scales (float32 [Hk]) are the cache's ``k_scale`` / ``v_scale``
+    attributes."""
+    rng = np.random.default_rng(seed)
+    kv_indptr, kv_indices, last = page_table(kv_lens, page_size, pool_pages, rng, shuffle_pool)
+    shape = (pool_pages, num_kv_heads, page_size, head_dim)
+    pools, scales = [], []
+    for k in (1, 2):
+        x = normal_values(shape, torch.float32, seed * 4 + k)
+        amax = x.abs().amax(dim=(0, 2, 3)).clamp_min(1e-30)
+        scale = (amax / 448.0).float()
+        q8 = (x / scale[None, :, None, None]).to(torch.float8_e4m3fn)
+        pools.append(q8.view(torch.uint8))
+        scales.append(scale)
+    return BSRCache(page_size, num_kv_heads, head_dim, pools[0], pools[1], kv_indptr,
+                    kv_indices, last, np.asarray(kv_lens, np.int64), scales[0], scales[1])
+
+
+def fp8_decode_workload(name, kv_lens, page_size, pool_pages, num_qo_heads, num_kv_heads,
+                        dtype, seed, head_dim=HEAD_DIM) -> Workload:
+    """Decode over an FP8 E4M3 KV cache (make_fp8_cache); q is 16-bit."""
+    cache = make_fp8_cache(kv_lens, page_size, pool_pages, num_kv_heads, seed, head_dim)
+    q = normal_values((len(kv_lens), num_qo_heads, head_dim), dtype, seed * 4 + 3)
+    return Workload(name, "decode_fp8kv", dtype, num_qo_heads, num_kv_heads, head_dim,
+                    1.0 / math.sqrt(head_dim), q, cache)
 
 
 def decode_workload(name, kv_lens, page_size, pool_pages, num_qo_heads, num_kv_heads,
@@ -181,6 +215,17 @@ def uniform_gqa_decode(seed: int = SEED_BASE + 2, batch: int = 64,
     w = decode_workload("uniform_gqa_decode_b64_h32kv8_p16_bf16", kv_lens, 16,
                         pool_pages, 32, 8, torch.bfloat16, seed)
     return w
+
+
+def fp8_uniform_gqa_decode(seed: int = SEED_BASE + 8, batch: int = 64,
+                           pool_pages: int = 20000) -> Workload:
+    """The uniform GQA decode shape (B = 64, Hq = 32, Hk = 8, kv_len
+    U[1024, 4096], P = 16, shuffled 20000-page pool) over an FP8 E4M3 KV
+    cache with per-head scales; q and the output are bf16."""
+    rng = np.random.default_rng(seed)
+    kv_lens = rng.integers(1024, 4096, size=batch, endpoint=True)
+    return fp8_decode_workload("fp8kv_uniform_gqa_decode_b64_h32kv8_p16", kv_lens, 16,
+                               pool_pages, 32, 8, torch.bfloat16, seed)
 
 
 def vector_sparse_decode(seed: int = SEED_BASE + 6, batch: int = 64,
@@ -351,4 +396,5 @@ WORKLOADS = {
     "causal_append": causal_append,
     "sparse_decode": vector_sparse_decode,
     "pod_mixed": pod_mixed_batch,
+    "fp8_decode": fp8_uniform_gqa_decode,
 }
