@@ -253,9 +253,9 @@ def bench_decode_workload(key, hbm_peak, bf16_peak, flush, steps, warmup):
     st = DecodeStep(w)
     step_ms, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
     b = decode_bytes(w)
-    k_s = float(np.mean(kern_ms)) * 1e-3
+    k_s = float(np.median(kern_ms)) * 1e-3
     res = {"kind": "decode", "bytes": b, "kernel_us": k_s * 1e6,
-           "step_us": float(np.mean(step_ms)) * 1e3,
+           "step_us": float(np.median(step_ms)) * 1e3,
            "GB/s": b / k_s / 1e9, "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak,
            "units": st.att.plan_info.num_units,
            "split_items": st.att.plan_info.num_split_items}
@@ -287,9 +287,9 @@ def bench_causal_append(hbm_peak, bf16_peak, flush, steps, warmup):
 
     step_ms, kern_ms = time_steps([plan_a, run_a], steps, warmup, flush)
     fl = append_flops(w)
-    k_s = float(np.mean(kern_ms)) * 1e-3
+    k_s = float(np.median(kern_ms)) * 1e-3
     res = {"kind": "append", "flops": fl, "kernel_us": k_s * 1e6,
-           "step_us": float(np.mean(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
+           "step_us": float(np.median(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
            "roofline_frac_bf16": fl / k_s / 1e12 / bf16_peak,
            "units": att.plan_info.num_units, "split_items": att.plan_info.num_split_items,
            "launches_per_step": 1 + (att.plan_info.num_split_items > 0)}
@@ -330,9 +330,9 @@ def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
     b_pre = int(pre.kv_lens.sum()) * kvb
     b_suf = int(suf.kv_lens.sum()) * kvb
     b_flat = int(pre.kv_lens.sum()) * w.extra["n"] * kvb + b_suf
-    k_s = float(np.mean(kern_ms)) * 1e-3
+    k_s = float(np.median(kern_ms)) * 1e-3
     res = {"kind": "composable", "bytes": b_pre + b_suf, "flat_layout_bytes": b_flat,
-           "kernel_us": k_s * 1e6, "step_us": float(np.mean(step_ms)) * 1e3,
+           "kernel_us": k_s * 1e6, "step_us": float(np.median(step_ms)) * 1e3,
            "GB/s": (b_pre + b_suf) / k_s / 1e9,
            "roofline_frac_hbm": (b_pre + b_suf) / k_s / 1e9 / hbm_peak,
            "launches_per_step": 3 + (att_p.plan_info.num_split_items > 0),
@@ -343,7 +343,7 @@ def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
     wf = Workload("flat", "decode", torch.bfloat16, 32, 8, 128, w.sm_scale, w.q, flat)
     st = DecodeStep(wf)
     _, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
-    res["flat_layout_kernel_us"] = float(np.mean(kern_ms)) * 1e3
+    res["flat_layout_kernel_us"] = float(np.median(kern_ms)) * 1e3
     del st
     torch.cuda.empty_cache()
     return w.name, res
@@ -361,17 +361,54 @@ def bench_rope_decode(hbm_peak, bf16_peak, flush, steps, warmup):
     st = DecodeStep(w, rope=rope)
     step_ms, kern_ms = time_steps([st.plan, st.run], steps, warmup, flush)
     b = decode_bytes(w) + 2 * max_pos * 64 * 4  # + the cos / sin rows
-    k_s = float(np.mean(kern_ms)) * 1e-3
+    k_s = float(np.median(kern_ms)) * 1e-3
     res = {"kind": "decode+rope", "bytes": b, "kernel_us": k_s * 1e6,
-           "step_us": float(np.mean(step_ms)) * 1e3,
+           "step_us": float(np.median(step_ms)) * 1e3,
            "GB/s": b / k_s / 1e9, "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak}
     assert st.att.status() == 0
     plain = DecodeStep(w)
     _, kern_plain = time_steps([plain.plan, plain.run], steps, warmup, flush)
-    res["without_rope_kernel_us"] = float(np.mean(kern_plain)) * 1e3
+    res["without_rope_kernel_us"] = float(np.median(kern_plain)) * 1e3
     del st, plain
     torch.cuda.empty_cache()
     return w.name + "_rope", res
+
+
+def bench_fp8_decode(hbm_peak, bf16_peak, flush, steps, warmup):
+    """The uniform GQA decode shape over an FP8 E4M3 KV cache (per-head
+    scales), beside the bf16 cache's time for the same lengths."""
+    from paged_kv_attention_bsr_gb300 import synth
+    from paged_kv_attention_bsr_gb300.api import PagedAttention
+    w = synth.fp8_uniform_gqa_decode()
+    c = w.cache
+    att = PagedAttention(w.num_qo_heads, w.num_kv_heads, 128, "decode", max_batch=w.batch)
+    d = dev_cache(c)
+    scales = (c.k_scale.cuda(), c.v_scale.cuda())
+    q = w.q.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+
+    def plan_f():
+        att.plan(c.kv_indptr, c.last_page_len, 16)
+
+    def run_f():
+        att.run(q, d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"], d["last_page_len"],
+                w.sm_scale, out=o, lse=lse, kv_scales=scales)
+
+    step_ms, kern_ms = time_steps([plan_f, run_f], steps, warmup, flush)
+    assert att.status() == 0
+    kv = int(c.kv_lens.sum()) * 2 * w.num_kv_heads * w.head_dim  # one byte per element
+    qo = 2 * w.batch * w.num_qo_heads * w.head_dim * 2 + 4 * w.batch * w.num_qo_heads
+    idx = 4 * len(c.kv_indices) + 8 * w.batch + 4 + 8 * w.num_kv_heads
+    b = kv + qo + idx
+    k_s = float(np.median(kern_ms)) * 1e-3
+    res = {"kind": "decode_fp8kv", "bytes": b, "kernel_us": k_s * 1e6,
+           "step_us": float(np.median(step_ms)) * 1e3, "GB/s": b / k_s / 1e9,
+           "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak,
+           "kernel": "decode_kernel<group 4, bf16 q, E4M3 K/V> (CUDA cores)"}
+    del d, att
+    torch.cuda.empty_cache()
+    return w.name, res
 
 
 def bench_rope_append(hbm_peak, bf16_peak, flush, steps, warmup):
@@ -407,11 +444,11 @@ def bench_rope_append(hbm_peak, bf16_peak, flush, steps, warmup):
     assert att.status() == 0
     _, kern_plain = time_steps([plan_a, run_plain], steps, warmup, flush)
     fl = append_flops(w)
-    k_s = float(np.mean(kern_ms)) * 1e-3
+    k_s = float(np.median(kern_ms)) * 1e-3
     res = {"kind": "append+rope", "flops": fl, "kernel_us": k_s * 1e6,
-           "step_us": float(np.mean(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
+           "step_us": float(np.median(step_ms)) * 1e3, "TFLOP/s": fl / k_s / 1e12,
            "roofline_frac_bf16": fl / k_s / 1e12 / bf16_peak,
-           "without_rope_kernel_us": float(np.mean(kern_plain)) * 1e3}
+           "without_rope_kernel_us": float(np.median(kern_plain)) * 1e3}
     del d, att
     torch.cuda.empty_cache()
     return w.name + "_rope", res
@@ -443,7 +480,7 @@ def bench_pod_mixed(hbm_peak, bf16_peak, flush, steps, warmup):
 
     step_ms, kern_ms = time_steps([plan_f, run_f], steps, warmup, flush)
     assert att.status() == 0
-    fused_us = float(np.mean(kern_ms)) * 1e3
+    fused_us = float(np.median(kern_ms)) * 1e3
     # the same requests as two batches: prefill (append kernel), decode (decode kernel)
     wa = synth.sub_batch(w, w.extra["prefill"])
     wd = synth.sub_batch(w, w.extra["decode"], as_decode=True)
@@ -473,11 +510,11 @@ def bench_pod_mixed(hbm_peak, bf16_peak, flush, steps, warmup):
 
     _, kern_sep = time_steps([plans, runs], steps, warmup, flush)
     assert att_a.status() == 0 and att_d.status() == 0
-    sep_us = float(np.mean(kern_sep)) * 1e3
+    sep_us = float(np.median(kern_sep)) * 1e3
     fl = append_flops(wa)
     kv_dec = int(wd.cache.kv_lens.sum()) * 2 * 8 * 128 * 2
     res = {"kind": "pod", "prefill_flops": fl, "decode_kv_bytes": kv_dec,
-           "kernel_us": fused_us, "step_us": float(np.mean(step_ms)) * 1e3,
+           "kernel_us": fused_us, "step_us": float(np.median(step_ms)) * 1e3,
            "separate_two_launches_kernel_us": sep_us, "fused_speedup": sep_us / fused_us,
            "launches_per_step": 1 + (att.plan_info.num_split_items > 0),
            "units": att.plan_info.num_units, "split_items": att.plan_info.num_split_items}
@@ -496,13 +533,16 @@ WORKLOAD_BENCH = {
     "sparse_decode": lambda *a: bench_decode_workload("sparse_decode", *a),
     "pod_mixed": bench_pod_mixed,
     "rope_append": bench_rope_append,
+    "fp8_decode": bench_fp8_decode,
 }
 
 
 def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
+    """Every other workload of the pages; per workload the median over
+    `steps` CUDA-event-timed steps (kernel_us: the run's launches only)."""
     out = {}
     for key in ("single_decode", "skewed_decode", "causal_append", "shared_prefix",
-                "rope_decode", "rope_append", "sparse_decode", "pod_mixed"):
+                "rope_decode", "rope_append", "sparse_decode", "pod_mixed", "fp8_decode"):
         name, res = WORKLOAD_BENCH[key](hbm_peak, bf16_peak, flush, steps, warmup)
         out[name] = res
     return out

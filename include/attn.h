@@ -197,6 +197,32 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q,
                               size_t dev_bytes, void* stream);
 
 /*
+ * attn_decode_run over an FP8 KV cache: the pools hold FP8 E4M3 bytes (the
+ * "fn" encoding: no infinities) with one scale per kv head, so a token row
+ * is 128 bytes instead of 256 and a decode step reads half the bytes. The
+ * pages list FP8 KV-cache support among the features (gittoolsai.com README
+ * copy, feature list); the scale reading is this library's: the byte b of kv
+ * head hk stands for e4m3(b) * k_scale[hk] in K and e4m3(b) * v_scale[hk] in
+ * V. The kernel widens the bytes exactly as it reads them from shared memory,
+ * folds k_scale into q and v_scale into the output.
+ *   k_pool, v_pool   : device bytes, [num_pages, Hk, P, 128] (HND) or
+ *                      [num_pages, P, Hk, 128] (NHD), 16-byte aligned
+ *   k_scale, v_scale : device float[num_kv_heads]
+ *   dtype            : the type of q and o (ATTN_F16 / ATTN_BF16)
+ *   other arguments  : as attn_decode_run (same decode plan)
+ * Supported: head_dim 128, group 1..8, any page size, both layouts; the
+ * CUDA-core streaming decode kernel runs every group.
+ * Errors: as attn_decode_run; INVALID_ARG for null scales.
+ */
+attn_status_t attn_decode_run_fp8(const attn_plan_t* plan, const void* q, const void* k_pool,
+                                  const void* v_pool, int64_t num_pages, int32_t layout,
+                                  const int32_t* kv_indptr, const int32_t* kv_indices,
+                                  const int32_t* last_page_len, int32_t dtype,
+                                  const float* k_scale, const float* v_scale, float sm_scale,
+                                  void* o, float* lse, void* dev_ws, size_t dev_bytes,
+                                  void* stream);
+
+/*
  * attn_decode_run with rotary position embedding fused in: the kernel turns
  * q and each key as it streams the pages, so the cache keeps keys without
  * RoPE and no separate RoPE pass reads or writes them. The pages count

@@ -29,7 +29,7 @@ EXPORTS = ("attn_workspace_size", "attn_default_num_ctas", "attn_plan", "attn_de
            "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error",
            "attn_decode_run_noalloc", "attn_wait_selftest", "attn_decode_run_rope",
            "attn_append_run_rope", "attn_decode_run_noalloc_status",
-           "attn_wait_selftest_noalloc")
+           "attn_wait_selftest_noalloc", "attn_decode_run_fp8")
 
 
 class AttnError(RuntimeError):
@@ -78,6 +78,8 @@ def _load():
         "attn_decode_run_noalloc": [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64, i32, vp,
                                     vp, vp, i32, f32, vp, vp, vp],
         "attn_decode_run_noalloc_status": [vp, P(i32)],
+        "attn_decode_run_fp8": [P(Plan), vp, vp, vp, i64, i32, vp, vp, vp, i32, vp, vp, f32, vp,
+                                vp, vp, sz, vp],
         "attn_wait_selftest_noalloc": [i32, vp],
     }
     for name, args in sig.items():
@@ -217,6 +219,41 @@ def decode_run(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len,
                                _ptr(last_page_len), dtype_code(q.dtype), float(sm_scale),
                                _ptr(o), _ptr(lse), _ptr(dev_ws),
                                dev_ws.numel() * dev_ws.element_size(), _stream(stream)))
+
+
+def decode_run_fp8(p: Plan, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, k_scale,
+                   v_scale, sm_scale, o, lse, dev_ws, layout=LAYOUT_HND, num_pages=None,
+                   stream=None):
+    """attn_decode_run_fp8: k_pool / v_pool hold FP8 E4M3 bytes (uint8 or
+    torch.float8_e4m3fn tensors), k_scale / v_scale device float32
+    [num_kv_heads]."""
+    if num_pages is None:
+        num_pages = k_pool.shape[0]
+    _check_dense(q=q, k_pool=k_pool, v_pool=v_pool, out=o, lse=lse, k_scale=k_scale,
+                 v_scale=v_scale)
+    for t in (k_pool, v_pool):
+        if t.element_size() != 1:
+            raise ValueError("FP8 pools must be 1-byte tensors (uint8 or float8_e4m3fn)")
+    need_kv = int(num_pages) * p.num_kv_heads * p.page_size * p.head_dim
+    if ((p.total_weight > p.num_items and num_pages < 1) or k_pool.numel() < need_kv or
+            v_pool.numel() < need_kv):
+        raise ValueError(f"k_pool / v_pool hold fewer than num_pages ({num_pages}) x "
+                         f"{p.num_kv_heads} heads x {p.page_size} slots x {p.head_dim} bytes")
+    for t in (k_scale, v_scale):
+        if t.dtype != torch.float32 or t.numel() < p.num_kv_heads:
+            raise ValueError("k_scale / v_scale must be float32 with num_kv_heads elements")
+    per_row = p.num_qo_heads * p.head_dim
+    if o.dtype != q.dtype or q.numel() < p.batch * per_row or o.numel() < p.batch * per_row:
+        raise ValueError(f"q / out need {p.batch} rows x {p.num_qo_heads} heads x {p.head_dim}"
+                         " of one dtype")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() < p.batch * p.num_qo_heads):
+        raise ValueError(f"lse must be float32 with {p.batch} x {p.num_qo_heads} elements")
+    _check(lib.attn_decode_run_fp8(ctypes.byref(p), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                   int(num_pages), layout, _ptr(kv_indptr), _ptr(kv_indices),
+                                   _ptr(last_page_len), dtype_code(q.dtype), _ptr(k_scale),
+                                   _ptr(v_scale), float(sm_scale), _ptr(o), _ptr(lse),
+                                   _ptr(dev_ws), dev_ws.numel() * dev_ws.element_size(),
+                                   _stream(stream)))
 
 
 def _check_rope_tables(rope_cos, rope_sin):

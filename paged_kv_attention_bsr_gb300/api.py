@@ -69,10 +69,12 @@ class PagedAttention:
 
     def run(self, q, k_pool, v_pool, kv_indptr, kv_indices, last_page_len, sm_scale=None,
             out=None, lse=None, qo_indptr=None, layout: int = C.LAYOUT_HND, num_pages=None,
-            return_lse: bool = False, stream=None, rope=None):
+            return_lse: bool = False, stream=None, rope=None, kv_scales=None):
         """rope: optional (cos, sin) device float32 tables [max_pos, head_dim / 2]
         of the angles pos * theta_d: rotary position embedding fused into the
-        kernel (decode; append when group x the longest query count <= 16)."""
+        kernels (decode and append).
+        kv_scales: optional (k_scale, v_scale) device float32 [num_kv_heads]:
+        the pools hold FP8 E4M3 bytes with these per-head scales (decode)."""
         if self.plan_info is None:
             raise RuntimeError("run() before plan()")
         if sm_scale is None:
@@ -81,7 +83,13 @@ class PagedAttention:
             out = torch.empty_like(q)
         if lse is None and return_lse:
             lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-        if self.mode == "decode" and rope is not None:
+        if kv_scales is not None:
+            if self.mode != "decode" or rope is not None:
+                raise ValueError("FP8 K/V pools are supported by decode without RoPE")
+            C.decode_run_fp8(self.plan_info, q, k_pool, v_pool, kv_indptr, kv_indices,
+                             last_page_len, kv_scales[0], kv_scales[1], sm_scale, out, lse,
+                             self.dev_ws, layout, num_pages, stream)
+        elif self.mode == "decode" and rope is not None:
             C.decode_run_rope(self.plan_info, q, k_pool, v_pool, kv_indptr, kv_indices,
                               last_page_len, sm_scale, rope[0], rope[1], out, lse,
                               self.dev_ws, layout, num_pages, stream)

@@ -456,8 +456,64 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
   a.group = group;
   a.batch = plan->batch;
   a.sm_scale = sm_scale;
+  a.kv_fp8 = 0;
+  a.k_scale = nullptr;
+  a.v_scale = nullptr;
   cudaError_t e = launch_decode(a, st);  // split items are merged inside the kernel
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run: decode kernel launch");
+  return ATTN_OK;
+}
+
+attn_status_t attn_decode_run_fp8(const attn_plan_t* plan, const void* q, const void* k_pool,
+                                  const void* v_pool, int64_t num_pages, int32_t layout,
+                                  const int32_t* kv_indptr, const int32_t* kv_indices,
+                                  const int32_t* last_page_len, int32_t dtype,
+                                  const float* k_scale, const float* v_scale, float sm_scale,
+                                  void* o, float* lse, void* dev_ws, size_t dev_bytes,
+                                  void* stream) {
+  NvtxRange nvtx("attn_decode_run_fp8");
+  attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
+                                      layout, kv_indptr, kv_indices, last_page_len, dtype, o,
+                                      dev_ws, dev_bytes, "attn_decode_run_fp8");
+  if (s != ATTN_OK) return s;
+  if (debug_checks_enabled()) {
+    s = debug_check_table(plan, nullptr, kv_indptr, kv_indices, last_page_len, num_pages,
+                          stream, "attn_decode_run_fp8");
+    if (s != ATTN_OK) return s;
+  }
+  if (plan->num_qo_heads / plan->num_kv_heads > kMaxDecodeGroup)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_run_fp8: group > 8 is not implemented");
+  if (plan_pages(*plan) > 0 && (!k_scale || !v_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_fp8: null k_scale / v_scale");
+  if (plan->batch == 0) return ATTN_OK;
+  if (plan_pages(*plan) == 0)
+    return run_empty(plan, o, lse, plan->batch, dtype, stream, "attn_decode_run_fp8");
+  DecodeArgs a;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.last_page_len = last_page_len;
+  a.o = o;
+  a.lse = lse;
+  a.ws = ws_view(*plan, dev_ws);
+  a.num_ctas = plan->num_ctas;
+  a.num_units = plan->num_units;
+  a.num_split_items = plan->num_split_items;
+  a.layout = layout;
+  a.dtype = dtype;
+  a.page_size = plan->page_size;
+  a.num_qo_heads = plan->num_qo_heads;
+  a.num_kv_heads = plan->num_kv_heads;
+  a.group = plan->num_qo_heads / plan->num_kv_heads;
+  a.batch = plan->batch;
+  a.sm_scale = sm_scale;
+  a.kv_fp8 = 1;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run_fp8: decode kernel launch");
   return ATTN_OK;
 }
 

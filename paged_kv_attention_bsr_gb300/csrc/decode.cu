@@ -25,10 +25,15 @@
 //    items write an fp32 partial state (o, log2-LSE) to the workspace slot
 //    the plan assigned; the last of an item's units to finish (an atomic
 //    arrival count in the workspace) merges them, so a run is one launch;
+//  * K/V may be stored as FP8 E4M3 with a scale per kv head (half the bytes
+//    per token): rows are widened to floats as they are read from shared
+//    memory, the key scale is folded into q and the value scale into the
+//    output;
 //  * every wait is bounded (ptx.cuh) and reports through the workspace
 //    error word instead of hanging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -39,22 +44,32 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageTok = 64;
-constexpr int kStages = 3;
 constexpr int kTokPerWarp = kStageTok / kConsumerWarps;  // 16
-constexpr int kRowBytes = kHeadDim * 2;                  // one token's 128 x 16-bit
+constexpr int kQRowBytes = kHeadDim * 2;                 // one q / o row, 16-bit
 
+// K/V storage: 16-bit (a token row is 256 B) or FP8 E4M3 (128 B, with a
+// scale per kv head). An FP8 stage holds half the bytes, so the ring has
+// twice the stages and keeps as many bytes in flight.
+template <bool FP8>
+struct Kv {
+  static constexpr int kRowBytes = FP8 ? kHeadDim : kHeadDim * 2;
+  static constexpr int kStages = FP8 ? 6 : 3;
+};
+
+template <bool FP8>
 struct __align__(128) Stage {
-  uint16_t k[kStageTok * kHeadDim];
-  uint16_t v[kStageTok * kHeadDim];
+  uint8_t k[kStageTok * Kv<FP8>::kRowBytes];
+  uint8_t v[kStageTok * Kv<FP8>::kRowBytes];
   uint16_t q[kMaxDecodeGroup * kHeadDim];
 };
 
+template <bool FP8>
 struct __align__(128) Smem {
-  Stage st[kStages];
+  Stage<FP8> st[Kv<FP8>::kStages];
   float pbuf[kConsumerWarps][kTokPerWarp * kMaxDecodeGroup];
   float sbuf[kConsumerWarps][kMaxDecodeGroup];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[Kv<FP8>::kStages];
+  uint64_t empty[Kv<FP8>::kStages];
   uint64_t cbar;
 };
 
@@ -72,6 +87,31 @@ __device__ __forceinline__ void cvt8(const uint4 raw, float (&f)[8]) {
       f[2 * i] = t.x;
       f[2 * i + 1] = t.y;
     }
+  }
+}
+
+// Eight consecutive dims of a K / V row at `p` (shared memory) as floats:
+// 16-byte loads of 16-bit values, or 8-byte loads of E4M3 bytes widened
+// through f16 (exact: every E4M3 value is an f16 value).
+template <bool BF16, bool FP8>
+__device__ __forceinline__ void load_kv8(const uint8_t* p, float (&f)[8]) {
+  if constexpr (FP8) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(p);
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const __nv_fp8x2_storage_t pair =
+            static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hh)) & 0xffffu);
+        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&h));
+        f[4 * i + 2 * hh] = t.x;
+        f[4 * i + 2 * hh + 1] = t.y;
+      }
+    }
+  } else {
+    cvt8<BF16>(*reinterpret_cast<const uint4*>(p), f);
   }
 }
 
@@ -143,10 +183,12 @@ __device__ __forceinline__ Geo unit_geo(const DecodeArgs& a, int ui) {
   return g;
 }
 
-template <int GM, bool BF16>
+template <int GM, bool BF16, bool FP8>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+  constexpr int kStages = Kv<FP8>::kStages;
+  constexpr int kRowBytes = Kv<FP8>::kRowBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  Smem<FP8>& sm = *reinterpret_cast<Smem<FP8>*>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int32_t* err = a.ws.error;
@@ -191,14 +233,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         if (!mbar_wait(smem_u32(&sm.empty[stage]), ph ^ 1u, err, ERR_WAIT_EMPTY)) goto drain;
         const uint32_t full = smem_u32(&sm.full[stage]);
         const uint32_t bytes = uint32_t(max(nt, 0)) * 2u * kRowBytes +
-                               (s == 0 ? uint32_t(group) * kRowBytes : 0u);
+                               (s == 0 ? uint32_t(group) * kQRowBytes : 0u);
         if (lane == 0) mbar_arrive_expect_tx(full, bytes);
         __syncwarp();
-        Stage& S = sm.st[stage];
+        Stage<FP8>& S = sm.st[stage];
         if (s == 0 && lane == 0) {
           const char* qsrc = static_cast<const char*>(a.q) +
-                             (int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * group) * kRowBytes;
-          bulk_g2s(smem_u32(S.q), qsrc, uint32_t(group) * kRowBytes, full);
+                             (int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * group) * kQRowBytes;
+          bulk_g2s(smem_u32(S.q), qsrc, uint32_t(group) * kQRowBytes, full);
         }
         if (nt > 0) {
           const int64_t t_lo_all = g.tok_begin + tok0;
@@ -250,7 +292,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
   const int hf = lane >> 4;
   const int li = lane & 15;
   const int hsel = li >> (4 - LG);
-  const float qscale = a.sm_scale * kLog2e;
+  // FP8: the key scale of the unit's kv head folds into q, the value scale
+  // into the output (o = v_scale * sum p widen(v) / l)
+  const float qscale0 = a.sm_scale * kLog2e;
   const int wt0 = warp * kTokPerWarp;
   uint32_t it = 0;
   uint32_t cph = 0;
@@ -265,11 +309,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[h][j] = 0.f;
 
+    const float qscale = FP8 ? qscale0 * __ldg(a.k_scale + g.hk) : qscale0;
     for (int s = 0; s < g.nst; ++s, ++it) {
       const int stage = it % kStages;
       const uint32_t ph = (it / kStages) & 1u;
       if (!mbar_wait(smem_u32(&sm.full[stage]), ph, err, ERR_WAIT_FULL)) return;
-      const Stage& S = sm.st[stage];
+      const Stage<FP8>& S = sm.st[stage];
       if (s == 0) {
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
@@ -292,9 +337,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
 #pragma unroll
         for (int p = 0; p < kTokPerWarp / 2; ++p) {
           const int tt = wt0 + 2 * p + hf;
-          const uint4 raw = *reinterpret_cast<const uint4*>(&S.k[tt * kHeadDim + li * 8]);
           float kf[8];
-          cvt8<BF16>(raw, kf);
+          load_kv8<BF16, FP8>(S.k + tt * kRowBytes + li * 8 * (kRowBytes / kHeadDim), kf);
           float part[GM];
 #pragma unroll
           for (int h = 0; h < GM; ++h) {
@@ -347,9 +391,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         for (int p = 0; p < kTokPerWarp / 2; ++p) {
           const int tt = wt0 + 2 * p + hf;
           if (tt < nt) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(&S.v[tt * kHeadDim + li * 8]);
             float vf[8];
-            cvt8<BF16>(raw, vf);
+            load_kv8<BF16, FP8>(S.v + tt * kRowBytes + li * 8 * (kRowBytes / kHeadDim), vf);
             float pr[GM];
 #pragma unroll
             for (int h = 0; h < GM; ++h) pr[h] = pb[(2 * p + hf) * GM + h];
@@ -372,8 +415,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         mbar_arrive(cbar);  // everyone is done with this stage's K/V
         if (!mbar_wait(cbar, cph, err, ERR_WAIT_CONSUMER)) return;
         cph ^= 1u;
-        float* comb = reinterpret_cast<float*>(const_cast<uint16_t*>(S.k));  // [4][GM][128]
-        float* ml = reinterpret_cast<float*>(const_cast<uint16_t*>(S.v));    // [4][GM][2]
+        // the stage's K (and, for FP8, V) bytes hold the warps' accumulators
+        // [4][GM][128] floats; the row states [4][GM][2] and a flag follow in
+        // V (16-bit) or in the stage's q rows (FP8; q already sits in registers)
+        static_assert(sizeof(float) * kConsumerWarps * kMaxDecodeGroup * kHeadDim <=
+                          sizeof(S.k) + (FP8 ? sizeof(S.v) : 0),
+                      "combine buffer fits the stage");
+        float* comb = reinterpret_cast<float*>(const_cast<uint8_t*>(S.k));
+        float* ml = FP8 ? reinterpret_cast<float*>(const_cast<uint16_t*>(S.q))
+                        : reinterpret_cast<float*>(const_cast<uint8_t*>(S.v));
+        const float out_scale = FP8 ? __ldg(a.v_scale + g.hk) : 1.f;
         if (hf == 0) {
 #pragma unroll
           for (int h = 0; h < GM; ++h) {
@@ -408,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
           }
           if (g.slot < 0) {
             const int64_t row = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * group + h;
-            store_out<BF16>(a.o, row * kHeadDim + d, out);
+            store_out<BF16>(a.o, row * kHeadDim + d, out * out_scale);
             if (d == 0 && a.lse) a.lse[row] = lse2 * kLn2;
           } else {
             const int64_t row = int64_t(g.slot) * group + h;
@@ -471,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                 lse2 = M + lg2(L);
               }
               const int64_t row = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * group + h;
-              store_out<BF16>(a.o, row * kHeadDim + d, out);
+              store_out<BF16>(a.o, row * kHeadDim + d, out * out_scale);
               if (d == 0 && a.lse) a.lse[row] = lse2 * kLn2;
             }
             if (threadIdx.x == 0) a.ws.counters[g.split] = 0;
@@ -488,22 +539,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
   }
 }
 
-template <int GM, bool BF16>
+template <int GM, bool BF16, bool FP8>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem);
+  const size_t smem = sizeof(Smem<FP8>);
   static std::atomic<uint64_t> configured{0};
-  cudaError_t e = ensure_smem_limit(decode_kernel<GM, BF16>, int(smem), configured);
+  cudaError_t e = ensure_smem_limit(decode_kernel<GM, BF16, FP8>, int(smem), configured);
   if (e != cudaSuccess) return e;
-  decode_kernel<GM, BF16><<<a.num_ctas, kThreads, smem, stream>>>(a);
+  decode_kernel<GM, BF16, FP8><<<a.num_ctas, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <bool BF16>
+template <bool BF16, bool FP8>
 cudaError_t launch_dtype(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.group <= 1) return launch_t<1, BF16>(a, stream);
-  if (a.group <= 2) return launch_t<2, BF16>(a, stream);
-  if (a.group <= 4) return launch_t<4, BF16>(a, stream);
-  return launch_t<8, BF16>(a, stream);
+  if (a.group <= 1) return launch_t<1, BF16, FP8>(a, stream);
+  if (a.group <= 2) return launch_t<2, BF16, FP8>(a, stream);
+  if (a.group <= 4) return launch_t<4, BF16, FP8>(a, stream);
+  return launch_t<8, BF16, FP8>(a, stream);
 }
 
 }  // namespace
@@ -512,7 +563,11 @@ int decode_ctas_per_sm() { return 2; }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_ctas <= 0) return cudaSuccess;
-  return a.dtype == ATTN_BF16 ? launch_dtype<true>(a, stream) : launch_dtype<false>(a, stream);
+  if (a.kv_fp8)
+    return a.dtype == ATTN_BF16 ? launch_dtype<true, true>(a, stream)
+                                : launch_dtype<false, true>(a, stream);
+  return a.dtype == ATTN_BF16 ? launch_dtype<true, false>(a, stream)
+                              : launch_dtype<false, false>(a, stream);
 }
 
 }  // namespace attn

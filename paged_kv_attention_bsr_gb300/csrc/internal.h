@@ -119,6 +119,11 @@ struct DecodeArgs {
   int32_t group;
   int32_t batch;
   float sm_scale;
+  // FP8 E4M3 K/V pools (kv_fp8 = 1) and their per-kv-head scales
+  // (device float[num_kv_heads]); q and o keep `dtype`
+  int32_t kv_fp8;
+  const float* k_scale;
+  const float* v_scale;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 int decode_ctas_per_sm();

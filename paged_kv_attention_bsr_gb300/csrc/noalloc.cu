@@ -155,6 +155,9 @@ extern "C" attn_status_t attn_decode_run_noalloc(
   a.group = plan.num_qo_heads / plan.num_kv_heads;
   a.batch = plan.batch;
   a.sm_scale = sm_scale;
+  a.kv_fp8 = 0;
+  a.k_scale = nullptr;
+  a.v_scale = nullptr;
   e = launch_decode(a, st);
   if (e != cudaSuccess)
     return noalloc_fail(ATTN_ERR_CUDA, std::string("attn_decode_run_noalloc: launch: ") +
