@@ -405,7 +405,7 @@ def bench_fp8_decode(hbm_peak, bf16_peak, flush, steps, warmup):
     res = {"kind": "decode_fp8kv", "bytes": b, "kernel_us": k_s * 1e6,
            "step_us": float(np.median(step_ms)) * 1e3, "GB/s": b / k_s / 1e9,
            "roofline_frac_hbm": b / k_s / 1e9 / hbm_peak,
-           "kernel": "decode_kernel<group 4, bf16 q, E4M3 K/V> (CUDA cores)"}
+           "kernel": "decode_tc_kernel<bf16 q, 4 rows, decode, FP8 K/V> (tensor cores; E4M3 tiles staged by TMA and widened to f16 in shared memory)"}
     del d, att
     torch.cuda.empty_cache()
     return w.name, res

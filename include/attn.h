@@ -210,8 +210,12 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q,
  *   k_scale, v_scale : device float[num_kv_heads]
  *   dtype            : the type of q and o (ATTN_F16 / ATTN_BF16)
  *   other arguments  : as attn_decode_run (same decode plan)
- * Supported: head_dim 128, group 1..8, any page size, both layouts; the
- * CUDA-core streaming decode kernel runs every group.
+ * Supported: head_dim 128, group 1..8, any page size, both layouts. Groups
+ * 2, 4 and 8 over HND pools with page_size % 16 == 0 run on the tensor-core
+ * decode kernel: TMA stages the E4M3 tiles, four warps widen them to f16 in
+ * shared memory, and the MMAs multiply f16 operands (a bf16 q is rounded to
+ * f16 first: |q| must stay below 65504). The other shapes run on the
+ * CUDA-core streaming kernel, which widens rows to fp32 as it reads them.
  * Errors: as attn_decode_run; INVALID_ARG for null scales.
  */
 attn_status_t attn_decode_run_fp8(const attn_plan_t* plan, const void* q, const void* k_pool,

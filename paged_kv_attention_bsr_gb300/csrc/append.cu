@@ -138,10 +138,14 @@ template <bool BF16>
 __device__ __forceinline__ void rope_pairs4(uint2& x, uint2& y, const float4 c, const float4 s) {
   const float2 x0 = unpack2<BF16>(x.x), x1 = unpack2<BF16>(x.y);
   const float2 y0 = unpack2<BF16>(y.x), y1 = unpack2<BF16>(y.y);
-  x = make_uint2(pack2<BF16>(fmaf(-y0.x, s.x, x0.x * c.x), fmaf(-y0.y, s.y, x0.y * c.y)),
-                 pack2<BF16>(fmaf(-y1.x, s.z, x1.x * c.z), fmaf(-y1.y, s.w, x1.y * c.w)));
-  y = make_uint2(pack2<BF16>(fmaf(x0.x, s.x, y0.x * c.x), fmaf(x0.y, s.y, y0.y * c.y)),
-                 pack2<BF16>(fmaf(x1.x, s.z, y1.x * c.z), fmaf(x1.y, s.w, y1.y * c.w)));
+  const float2 c0 = make_float2(c.x, c.y), c1 = make_float2(c.z, c.w);
+  const float2 s0 = make_float2(s.x, s.y), s1 = make_float2(s.z, s.w);
+  const float2 ns0 = make_float2(-s.x, -s.y), ns1 = make_float2(-s.z, -s.w);
+  // packed fp32x2: x' = x cos - y sin, y' = y cos + x sin
+  const float2 xr0 = ffma2(y0, ns0, fmul2(x0, c0)), xr1 = ffma2(y1, ns1, fmul2(x1, c1));
+  const float2 yr0 = ffma2(x0, s0, fmul2(y0, c0)), yr1 = ffma2(x1, s1, fmul2(y1, c1));
+  x = make_uint2(pack2<BF16>(xr0.x, xr0.y), pack2<BF16>(xr1.x, xr1.y));
+  y = make_uint2(pack2<BF16>(yr0.x, yr0.y), pack2<BF16>(yr1.x, yr1.y));
 }
 
 // --------------------------------------------------------- unit geometry
@@ -560,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
     // one 8-byte piece in each 64-dim half of the 128B-swizzled tile, at the
     // same offset in both halves. The tables hold cos / sin of pos * theta_d,
     // so a half-warp walks consecutive positions by turning its (cos, sin)
-    // by theta_d (table row 1) at each step and reloads the table every 16
-    // positions: one table row per 16 tile rows. The MMA warp waits on
+    // by theta_d (table row 1) at each step and reloads the table every 8-16
+    // positions: one table row per 8 K rows and per 16 query tokens. The MMA warp waits on
     // q_rot / k_rot instead of the TMA barriers.
     const int hq = (warp - kWarpRope0) * 2 + (lane >> 4);  // half-warp 0..3
     const int l16 = lane & 15;
@@ -573,12 +577,16 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
     float4 ct = make_float4(1.f, 1.f, 1.f, 1.f), stt = make_float4(0.f, 0.f, 0.f, 0.f);
     if (a.rope_rows > 1) table_row(1, ct, stt);  // cos / sin of theta_d
     // (c, sn) at position p -> at p + 1
-    auto step = [&](float4& c, float4& sn) {
-      const float4 c0 = c;
-      c = make_float4(fmaf(c0.x, ct.x, -sn.x * stt.x), fmaf(c0.y, ct.y, -sn.y * stt.y),
-                      fmaf(c0.z, ct.z, -sn.z * stt.z), fmaf(c0.w, ct.w, -sn.w * stt.w));
-      sn = make_float4(fmaf(sn.x, ct.x, c0.x * stt.x), fmaf(sn.y, ct.y, c0.y * stt.y),
-                       fmaf(sn.z, ct.z, c0.z * stt.z), fmaf(sn.w, ct.w, c0.w * stt.w));
+    const float2 ct0 = make_float2(ct.x, ct.y), ct1 = make_float2(ct.z, ct.w);
+    const float2 st0 = make_float2(stt.x, stt.y), st1 = make_float2(stt.z, stt.w);
+    const float2 nst0 = make_float2(-stt.x, -stt.y), nst1 = make_float2(-stt.z, -stt.w);
+    auto step = [&](float4& c, float4& sn) {  // packed fp32x2 angle sums
+      const float2 c0 = make_float2(c.x, c.y), c1 = make_float2(c.z, c.w);
+      const float2 s0 = make_float2(sn.x, sn.y), s1 = make_float2(sn.z, sn.w);
+      const float2 cn0 = ffma2(s0, nst0, fmul2(c0, ct0)), cn1 = ffma2(s1, nst1, fmul2(c1, ct1));
+      const float2 sn0 = ffma2(c0, st0, fmul2(s0, ct0)), sn1 = ffma2(c1, st1, fmul2(s1, ct1));
+      c = make_float4(cn0.x, cn0.y, cn1.x, cn1.y);
+      sn = make_float4(sn0.x, sn0.y, sn1.x, sn1.y);
     };
     auto turn = [&](uint8_t* tile, int row, const float4 c, const float4 sn) {
       const int off = row * 128 + (kbyte ^ ((row & 7) << 4));
@@ -629,19 +637,34 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
         const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
         uint8_t* kt_tile = gbase + kOffRing + (use % kSlots) * kTileBytes;
+        // four runs of 8 consecutive rows, one row of each per step: the
+        // four rows' shared-memory loads are in flight together
         const int r0 = 32 * hq;
-        float4 ca, sa, cb, sb;  // rows r0 + k and r0 + 16 + k
-        if (r0 < ntt) table_row(kv0 + r0, ca, sa);
-        if (r0 + 16 < ntt) table_row(kv0 + r0 + 16, cb, sb);
+        float4 cg[4], sg[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (r0 + 8 * q < ntt) table_row(kv0 + r0 + 8 * q, cg[q], sg[q]);
 #pragma unroll 1
-        for (int k = 0; k < 16; ++k) {
-          if (r0 + k < ntt) {
-            turn(kt_tile, r0 + k, ca, sa);
-            step(ca, sa);
+        for (int k = 0; k < 8; ++k) {
+          uint2 x[4], y[4];
+          int off[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int row = r0 + 8 * q + k;
+            off[q] = row * 128 + (kbyte ^ ((row & 7) << 4));
+            if (row < ntt) {
+              x[q] = *reinterpret_cast<const uint2*>(kt_tile + off[q]);
+              y[q] = *reinterpret_cast<const uint2*>(kt_tile + kHalf + off[q]);
+            }
           }
-          if (r0 + 16 + k < ntt) {
-            turn(kt_tile, r0 + 16 + k, cb, sb);
-            step(cb, sb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (r0 + 8 * q + k < ntt) {
+              rope_pairs4<BF16>(x[q], y[q], cg[q], sg[q]);
+              *reinterpret_cast<uint2*>(kt_tile + off[q]) = x[q];
+              *reinterpret_cast<uint2*>(kt_tile + kHalf + off[q]) = y[q];
+              step(cg[q], sg[q]);
+            }
           }
         }
         fence_proxy_async_smem();
@@ -953,9 +976,9 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream, const char**
       return cudaErrorInvalidValue;
     }
   }
-  if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
-                    prm.gather ? 1u : uint32_t(kTcChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v,
-                    msg))
+  if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size,
+                    bf16 ? kKvElemBF16 : kKvElemF16, prm.gather ? 1u : uint32_t(kTcChunk),
+                    prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorNotSupported;  // *msg says why
   // at most one CTA per SM (shared memory); extra plan CTAs are run in turn
   int sms = 0;

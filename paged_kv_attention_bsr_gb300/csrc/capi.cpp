@@ -488,6 +488,20 @@ attn_status_t attn_decode_run_fp8(const attn_plan_t* plan, const void* q, const 
   if (plan->batch == 0) return ATTN_OK;
   if (plan_pages(*plan) == 0)
     return run_empty(plan, o, lse, plan->batch, dtype, stream, "attn_decode_run_fp8");
+  if (decode_tc_shape(plan, layout) && layout == ATTN_LAYOUT_HND && plan->page_size % 16 == 0) {
+    // Tensor cores: TMA stages the E4M3 tiles, warps widen them to f16 in
+    // shared memory, the MMAs multiply f16 (q converted when bf16).
+    AppendArgs t = decode_tc_args(plan, q, k_pool, v_pool, num_pages, layout, kv_indptr,
+                                  kv_indices, last_page_len, dtype, sm_scale, o, lse, dev_ws);
+    t.kv_fp8 = 1;
+    t.k_scale = k_scale;
+    t.v_scale = v_scale;
+    const char* msg = "";
+    cudaError_t e = launch_decode_tc(t, static_cast<cudaStream_t>(stream), &msg);
+    if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_run_fp8: tensor-core kernel launch");
+    return ATTN_OK;
+  }
   DecodeArgs a;
   a.q = q;
   a.k_pool = k_pool;

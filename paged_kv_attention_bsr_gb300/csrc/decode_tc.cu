@@ -66,9 +66,29 @@ constexpr int kWarpMma = 2;
 constexpr int kWarpQ = 3;
 constexpr int kWarpEpi = 4;  // TMEM lanes 0-31, like the softmax warp
 constexpr int kWarpRope0 = 5;  // warps 5-8 turn K tiles when RoPE is fused in
-template <bool ROPE>
-constexpr int block_threads() { return ROPE ? 288 : 160; }
+// warps 5-8 turn K tiles (RoPE); warps 5-7 widen FP8 tiles (eight warps in
+// all, two per scheduler: the register budget stays at 255 per thread)
+template <bool ROPE, bool FP8 = false>
+constexpr int block_threads() { return ROPE ? 288 : FP8 ? 256 : 160; }
+constexpr int kConvThreads = 96;  // FP8 converter warps 5-7
+
+// Two E4M3 values (the low byte first) as an f16x2 word (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(pair)));
+  return d;
+}
 constexpr int kSlots = 6;
+// FP8 K/V (E4M3 bytes): TMA lands 128-row tiles of 128-byte rows (128B
+// swizzle, the same row pattern as one 64-dim half of a 16-bit tile) in a
+// four-slot staging ring that takes the place of two 16-bit slots; warps 5-7
+// widen each staged tile into one of the remaining four 16-bit slots. (Six
+// staging slots and three 16-bit slots were slower: 130 against 112 us on
+// the uniform batch; the widened ring must run a tile pair ahead.)
+constexpr int kF8Slots = 4;
+constexpr int kF8SlotBytes = kTcTile * 128;
+template <bool FP8>
+constexpr int ring_slots() { return FP8 ? 4 : kSlots; }
 constexpr int kOffQ = 0;
 // RoPE key angles: cos / sin of the offset rows o = 0, 2, .., 14 (8 x 64
 // floats each) in query-tile rows 32-63 of the lower half, which hold no
@@ -86,8 +106,10 @@ constexpr int kIdxSlots = kIdxDepth + 1;
 constexpr int kOffIdxRing = kOffQ + 64 * 128;
 static_assert(kOffIdxRing + kIdxSlots * kTcTile * 4 <= kOffQ + kTcHalf, "index ring fits the spare query rows");
 constexpr int kOffRing = kTileBytes;
+constexpr int kOffF8 = kOffRing + 4 * kTileBytes;  // FP8 staging ring
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
-constexpr int kOffHand = kOffBar + 256;         // softmax -> epilogue row state
+static_assert(kOffF8 + kF8Slots * kF8SlotBytes <= kOffBar, "FP8 staging fits two slots");
+constexpr int kOffHand = kOffBar + 512;         // softmax -> epilogue row state
 constexpr int kSmem = kOffHand + 512 + 1024;    // + alignment slack
 constexpr uint32_t kTmemCols = 512;  // S buffers at 0 and 128, O buffers at 256 and 384
 constexpr uint32_t kColO = 256;
@@ -100,10 +122,12 @@ struct Bars {
   uint64_t ounit[2];    // a unit's last P.V into O[b] is done (commit)
   uint64_t ep_full[2];  // softmax wrote the row state of a unit with O[b] (count 32)
   uint64_t k_rot[kSlots / 2];  // RoPE: K tile k is turned in its slot (count 128)
+  uint64_t f8_full[kF8Slots];  // FP8: a staged tile has landed (TMA bytes)
+  uint64_t f8_empty[kF8Slots]; // FP8: the converters have read it (count 96)
   uint64_t drain;
   uint32_t tmem_base;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 struct Hand {
   float m[2][32];  // per O buffer and TMEM lane: running max (log2 units)
   float l[2][32];  // and the copy's partial sum
@@ -119,6 +143,14 @@ struct DecodeTcParams {
   int32_t gather;  // K / V rows gathered 4 at a time (page_size % 16 != 0)
   int32_t nhd;     // pools are NHD [pages, P, Hk, 128] (else HND [pages, Hk, P, 128])
 };
+
+// f16 bits of two bf16 values (FP8 kernels multiply in f16: the MMA's two
+// operands share one type, and every E4M3 value is an f16 value)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 struct DGeo {
   int32_t r, hk, t, slot, split, page_base, ntiles;
@@ -538,12 +570,15 @@ __device__ __noinline__ void produce_nhd_box(const DecodeTcParams& prm, Bars& ba
     }
 }
 
-template <bool BF16, int R, bool DEC, bool ROPE>
-__global__ void __launch_bounds__(block_threads<ROPE>(), 1)
+template <bool BF16, int R, bool DEC, bool ROPE, bool FP8 = false>
+__global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
   constexpr int C = 32 / R;     // copies of each query row
   constexpr int W = kTile / C;  // kv columns per copy and tile
   constexpr int LC = ILog2<C>::value;
+  constexpr int kRing = ring_slots<FP8>();  // 16-bit K/V slots
+  constexpr bool kMmaBF16 = FP8 ? false : BF16;  // operand type of the MMAs (and of P)
+  static_assert(!(FP8 && ROPE), "FP8 K/V and fused RoPE are separate kernels");
   extern __shared__ uint8_t smem_raw[];
   const AppendArgs& a = prm.a;
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -558,9 +593,13 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars.q_full), 32);
     mbar_init(smem_u32(&bars.q_empty), 1);
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(smem_u32(&bars.slot_full[i]), 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(smem_u32(&bars.slot_full[i]), FP8 ? kConvThreads : 1);  // FP8: converters fill it
       mbar_init(smem_u32(&bars.slot_empty[i]), 1);
+    }
+    for (int i = 0; i < kF8Slots; ++i) {
+      mbar_init(smem_u32(&bars.f8_full[i]), 1);
+      mbar_init(smem_u32(&bars.f8_empty[i]), kConvThreads);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
@@ -602,9 +641,9 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     // their latency hides behind the wait. Other page sizes: produce_gather.
     uint32_t uses = 0;
     bool ok = true;
-    if (prm.gather) {
+    if (!FP8 && prm.gather) {
       produce_gather<DEC>(prm, bars, base, gbase, lane, err, uses, ok);
-    } else if (prm.nhd) {
+    } else if (!FP8 && prm.nhd) {
       produce_nhd_box<DEC>(prm, bars, base, lane, err, uses, ok);
     } else {
       const int P = a.page_size;
@@ -627,25 +666,33 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
             const int nch = (ntt + kChunk - 1) / kChunk;
             const int32_t row_next = i + 1 < g.ntiles ? chunk_row(g, i + 1) : 0;
             for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
-              const int slot = int(uses % kSlots);
+              // 16-bit: a ring slot; FP8: a staging slot (128-byte rows)
+              const int nslot = FP8 ? kF8Slots : kRing;
+              const int slot = int(uses % nslot);
               bool r = true;
               if (lane == 0)
-                r = mbar_wait(smem_u32(&bars.slot_empty[slot]), ((uses / kSlots) & 1u) ^ 1u, err,
-                              ERR_WAIT_EMPTY);
+                r = mbar_wait(smem_u32(FP8 ? &bars.f8_empty[slot] : &bars.slot_empty[slot]),
+                              ((uses / nslot) & 1u) ^ 1u, err, ERR_WAIT_EMPTY);
               if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) {
                 ok = false;
                 break;
               }
-              const uint32_t full = smem_u32(&bars.slot_full[slot]);
-              if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * 256u);
+              const uint32_t full = smem_u32(FP8 ? &bars.f8_full[slot] : &bars.slot_full[slot]);
+              if (lane == 0)
+                mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * (FP8 ? 128u : 256u));
               __syncwarp();
               if (lane < nch) {
-                const uint32_t dst =
-                    base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
                 const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
                                          : static_cast<const void*>(&prm.tm_v);
-                tma_load_2d(dst, tm, 0, row, full);
-                tma_load_2d(dst + kHalf, tm, 64, row, full);
+                if constexpr (FP8) {
+                  tma_load_2d(base + kOffF8 + slot * kF8SlotBytes + uint32_t(lane) * kChunk * 128u,
+                              tm, 0, row, full);
+                } else {
+                  const uint32_t dst =
+                      base + kOffRing + slot * kTileBytes + uint32_t(lane) * kChunk * 128u;
+                  tma_load_2d(dst, tm, 0, row, full);
+                  tma_load_2d(dst + kHalf, tm, 64, row, full);
+                }
               }
             }
             row = row_next;
@@ -655,9 +702,11 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     // drain: every issued copy has landed before the CTA can exit
     cp_async_wait<0>();  // this lane's index copies (they always complete)
     if (lane == 0) {
-      for (uint32_t sl = 0; sl < uint32_t(kSlots) && sl < uses; ++sl) {
-        const uint32_t last = uses - 1 - ((uses - 1 - sl) % kSlots);
-        mbar_wait(smem_u32(&bars.slot_full[sl]), (last / kSlots) & 1u, err, ERR_WAIT_DRAIN);
+      const uint32_t nslot = FP8 ? kF8Slots : kRing;
+      for (uint32_t sl = 0; sl < nslot && sl < uses; ++sl) {
+        const uint32_t last = uses - 1 - ((uses - 1 - sl) % nslot);
+        mbar_wait(smem_u32(FP8 ? &bars.f8_full[sl] : &bars.slot_full[sl]), (last / nslot) & 1u,
+                  err, ERR_WAIT_DRAIN);
       }
     }
     __syncwarp();
@@ -732,6 +781,9 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
             val = rope8<BF16>(val, oth, ch < 8, __ldg(cp), __ldg(cp + 1), __ldg(sp), __ldg(sp + 1));
           }
         }
+        if constexpr (FP8 && BF16)
+          val = make_uint4(bf16x2_to_f16x2(val.x), bf16x2_to_f16x2(val.y),
+                           bf16x2_to_f16x2(val.z), bf16x2_to_f16x2(val.w));
         if (idx < kVec) {
           const int rho = idx >> 4, ch = idx & 15;
           const int half = ch >> 3, j8 = ch & 7;
@@ -757,9 +809,9 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     if (lane == 0) {
       uint32_t ua = 0, jt = 0, n_u = 0;
       bool ok = true;
-      auto slot_of = [](uint32_t use) { return use % kSlots; };
+      auto slot_of = [](uint32_t use) { return use % kRing; };
       auto wait_slot = [&](uint32_t use) -> bool {
-        return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kSlots) & 1u, err,
+        return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kRing) & 1u, err,
                          ERR_WAIT_FULL);
       };
       // K tile k in its slot (and, with RoPE, turned by the rope warps)
@@ -861,7 +913,6 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
     // .sync.aligned.
     const int rho = lane % R;
     const int c = lane / R;
-    const float c2 = prm.scale_log2;
     uint32_t n_t = 0, n_u = 0;  // tiles and units with tiles so far
     bool ok = true;
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
@@ -869,6 +920,8 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
            ++ui) {
         const DGeo g = decode_geo<DEC>(a, ui);
         const QRow qr = qrow<DEC, R>(a, g, rho);
+        // log2-domain logit scale (FP8: the kv head's key scale folded in)
+        const float c2 = FP8 ? prm.scale_log2 * __ldg(a.k_scale + g.hk) : prm.scale_log2;
         const uint32_t ob = n_u & 1u;  // this unit's O buffer
         const uint32_t col_o = kColO + 128u * ob;
         const int64_t orow = qr.orow;
@@ -972,7 +1025,7 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
               p1 = (live && W * c + j + 1 < nvalid) ? p1 : 0.f;
             }
             lsum += p0 + p1;
-            pk[j / 2] = pack2<BF16>(p0, p1);
+            pk[j / 2] = pack2<kMmaBF16>(p0, p1);
           }
           l += lsum;
           // the P row: this thread's W/2 packed columns at (W/2) c, zeros elsewhere
@@ -995,12 +1048,12 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
           const int nrow = ((ntt + kChunk - 1) / kChunk) * kChunk;
           if (ntt < nrow) {
             const uint32_t vuse = 2 * n_t + 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.slot_full[vuse % kSlots]),
-                                                   (vuse / kSlots) & 1u, err, ERR_WAIT_FULL))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.slot_full[vuse % kRing]),
+                                                   (vuse / kRing) & 1u, err, ERR_WAIT_FULL))) {
               ok = false;
               break;
             }
-            uint8_t* vslot = gbase + kOffRing + (vuse % kSlots) * kTileBytes;
+            uint8_t* vslot = gbase + kOffRing + (vuse % kRing) * kTileBytes;
             for (int e = lane; e < (nrow - ntt) * 16; e += 32) {
               const int rr = ntt + (e >> 4), q = e & 15;
               *reinterpret_cast<uint4*>(vslot + (q >> 3) * kHalf + rr * 128 + (q & 7) * 16) =
@@ -1057,7 +1110,8 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
 #pragma unroll
         for (int st = 0; st < LC; ++st) lt += __shfl_xor_sync(0xffffffffu, lt, R << st);
         const bool any = lt > 0.f;
-        const float inv = any ? 1.f / lt : 0.f;
+        // 1 / l (FP8: times the kv head's value scale)
+        const float inv = any ? (FP8 ? __ldg(a.v_scale + g.hk) : 1.f) / lt : 0.f;
         const float lse2 = any ? m_ref + lg2(lt) : -INFINITY;
         // first dim (within a 32-column chunk) that this thread holds after
         // the transposing reduction, and how many
@@ -1108,6 +1162,85 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
           break;
         }
       }
+  }
+
+  if constexpr (FP8) {
+    if (warp >= kWarpRope0 && warp < kWarpRope0 + kConvThreads / 32) {
+      // ------------------------------------------------------- FP8 converters
+      // Warps 5-7 widen every staged K / V tile (128 rows of 128 E4M3 bytes,
+      // 128B-swizzled) into a 16-bit ring slot (two 128B-swizzled 64-dim
+      // halves) for the MMAs: thread t takes the 16-byte pieces t, t + 96,
+      // ... (row = piece / 8, dims 16 (piece % 8) .. + 15), so a warp reads
+      // four whole rows at a time. E4M3 -> f16 is exact (one cvt per pair).
+      // Rows past a unit's end are widened too: the softmax masks those keys
+      // and zeroes those V rows, as it does for 16-bit pools.
+      const int t = threadIdx.x - kWarpRope0 * 32;  // 0..95
+      int vc = blockIdx.x, ui = vc < a.num_ctas ? __ldg(a.ws.work_indptr + vc) : 0;
+      auto next_unit = [&](DGeo& g) -> bool {
+        while (vc < a.num_ctas) {
+          if (ui < __ldg(a.ws.work_indptr + vc + 1)) {
+            g = decode_geo<DEC>(a, ui++);
+            if (g.ntiles > 0) return true;
+          } else {
+            vc += gridDim.x;
+            if (vc < a.num_ctas) ui = __ldg(a.ws.work_indptr + vc);
+          }
+        }
+        return false;
+      };
+      uint32_t use = 0;
+      bool ok = true;
+      DGeo g;
+      while (ok && next_unit(g)) {
+        for (int i = 0; i < 2 * g.ntiles && ok; ++i, ++use) {  // K then V of each tile
+          const uint32_t fs = use % kF8Slots, rs = use % kRing;
+          if (!mbar_wait(smem_u32(&bars.f8_full[fs]), (use / kF8Slots) & 1u, err,
+                         ERR_WAIT_FULL) ||
+              !mbar_wait(smem_u32(&bars.slot_empty[rs]), ((use / kRing) & 1u) ^ 1u, err,
+                         ERR_WAIT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = gbase + kOffF8 + fs * kF8SlotBytes;
+          uint8_t* dst = gbase + kOffRing + rs * kTileBytes;
+          constexpr int kPieces = kTile * 8;  // 16-byte pieces of a staged tile
+          constexpr int kPer = (kPieces + kConvThreads - 1) / kConvThreads;
+          // all of this thread's pieces are loaded before any is widened
+          uint4 raws[kPer];
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int piece = t + kConvThreads * k;
+            const int row = piece >> 3, c = piece & 7;
+            if (piece < kPieces)
+              raws[k] = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+          }
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int piece = t + kConvThreads * k;
+            if (piece >= kPieces) break;
+            const int row = piece >> 3, c = piece & 7;
+            const uint4 raw = raws[k];
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              h[2 * q] = e4m3x2_to_f16x2(w[q] & 0xffffu);
+              h[2 * q + 1] = e4m3x2_to_f16x2(w[q] >> 16);
+            }
+            // dims 16 c .. 16 c + 15: half c / 4, 8-dim chunks 2 (c % 4) and + 1
+            uint8_t* rowp = dst + (c >> 2) * kHalf + row * 128;
+            const int j0 = 2 * (c & 3);
+            *reinterpret_cast<uint4*>(rowp + ((j0 ^ (row & 7)) << 4)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(rowp + (((j0 + 1) ^ (row & 7)) << 4)) =
+                make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          fence_proxy_async_smem();  // generic stores -> the MMA's operand reads
+          mbar_arrive(smem_u32(&bars.slot_full[rs]));
+          mbar_arrive(smem_u32(&bars.f8_empty[fs]));
+        }
+      }
+    }
   }
 
   if constexpr (ROPE) {
@@ -1257,17 +1390,26 @@ __global__ void __launch_bounds__(block_threads<ROPE>(), 1)
   }
 }
 
-template <bool BF16, int R, bool DEC, bool ROPE = false>
+template <bool BF16, int R, bool DEC, bool ROPE = false, bool FP8 = false>
 cudaError_t launch_k(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};
-  cudaError_t e = ensure_smem_limit(decode_tc_kernel<BF16, R, DEC, ROPE>, kSmem, configured);
+  cudaError_t e =
+      ensure_smem_limit(decode_tc_kernel<BF16, R, DEC, ROPE, FP8>, kSmem, configured);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<BF16, R, DEC, ROPE><<<grid, block_threads<ROPE>(), kSmem, stream>>>(prm);
+  decode_tc_kernel<BF16, R, DEC, ROPE, FP8>
+      <<<grid, block_threads<ROPE, FP8>(), kSmem, stream>>>(prm);
   return cudaGetLastError();
 }
 // decode runs with R = group in {2, 4, 8}; short appends with R in {1..16}
 template <bool BF16>
 cudaError_t launch_dt(const DecodeTcParams& prm, int rows, int grid, cudaStream_t stream) {
+  if (prm.a.kv_fp8) {  // decode over an FP8 cache (HND, page_size % 16 == 0)
+    switch (rows) {
+      case 2: return launch_k<BF16, 2, true, false, true>(prm, grid, stream);
+      case 4: return launch_k<BF16, 4, true, false, true>(prm, grid, stream);
+      default: return launch_k<BF16, 8, true, false, true>(prm, grid, stream);
+    }
+  }
   if (!prm.a.qo_indptr && prm.a.rope_cos) {  // decode with fused RoPE
     switch (rows) {
       case 2: return launch_k<BF16, 2, true, true>(prm, grid, stream);
@@ -1326,11 +1468,17 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
   std::memset(&prm, 0, sizeof prm);
   prm.a = a;
   prm.scale_log2 = a.sm_scale * kLog2e;
-  prm.idesc_s = make_idesc(bf16, false);
-  prm.idesc_pv = make_idesc(bf16, true);
+  // FP8 K/V: the MMAs multiply f16 operands (q is converted when it is bf16)
+  prm.idesc_s = make_idesc(bf16 && !a.kv_fp8, false);
+  prm.idesc_pv = make_idesc(bf16 && !a.kv_fp8, true);
   prm.gather = a.page_size % kChunk != 0 ? 1 : 0;
   prm.nhd = a.layout == ATTN_LAYOUT_NHD ? 1 : 0;
-  if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, bf16,
+  if (a.kv_fp8 && (prm.gather || prm.nhd || a.qo_indptr || a.rope_cos)) {
+    *msg = "attn: the tensor-core FP8 decode takes HND pools with page_size % 16 == 0";
+    return cudaErrorNotSupported;
+  }
+  const int elem = a.kv_fp8 ? kKvElemU8 : (bf16 ? kKvElemBF16 : kKvElemF16);
+  if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, elem,
                     prm.gather ? 1u : uint32_t(kChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorNotSupported;  // *msg says why
   int sms = 0;

@@ -161,6 +161,11 @@ struct AppendArgs {
   const float* rope_sin;
   int64_t rope_rows;
   int32_t layout;  // KV pool layout (few-row kernel): ATTN_LAYOUT_HND or ATTN_LAYOUT_NHD
+  // FP8 E4M3 K/V pools with per-kv-head scales (few-row decode, HND,
+  // page_size % 16 == 0); q / o keep `dtype`
+  int32_t kv_fp8;
+  const float* k_scale;
+  const float* v_scale;
 };
 // qo_indptr == NULL runs the kernel in decode mode (one query row per
 // request; q is [batch, Hq, D]). Returns cudaErrorNotSupported for shapes the

@@ -207,9 +207,15 @@ inline uint32_t make_idesc(bool bf16, bool b_mn_major) {
 }
 
 
+// Element types of the K / V pools: 16-bit (f16, bf16) or FP8 bytes.
+constexpr int kKvElemF16 = 0;
+constexpr int kKvElemBF16 = 1;
+constexpr int kKvElemU8 = 2;
+
 // The paged K and V pools as 2-D tensors [pages * kv heads * page_size, 128]
-// with 16-row x 64-column boxes and the 128-byte swizzle. Returns false when
-// the driver cannot describe them (message in *msg).
+// with 16-row x 64-column boxes and the 128-byte swizzle (FP8 bytes: 128-byte
+// rows, a box is 16 whole rows). Returns false when the driver cannot
+// describe them (message in *msg).
 // box_rows: 16 (16-row boxes within a page) or 1 (rows gathered one by one
 // with tile::gather4, for page sizes that are not a multiple of 16). Rows are
 // the 256-byte (token, head) vectors: HND [pages, Hk, P, 128] and NHD
@@ -217,7 +223,7 @@ inline uint32_t make_idesc(bool bf16, bool b_mn_major) {
 // 16-row boxes of one head in NHD take a 3-D map [tokens, Hk, 128] (box
 // 16 x 1 x 64), which lands the same 16 swizzled rows.
 inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
-                         int32_t num_kv_heads, int32_t page_size, bool bf16, uint32_t box_rows,
+                         int32_t num_kv_heads, int32_t page_size, int elem, uint32_t box_rows,
                          bool nhd, CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
   const cuuint64_t rows = cuuint64_t(num_pages) * num_kv_heads * page_size;
   if (rows == 0 || rows > 0x7fffffffull) {
@@ -230,18 +236,21 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
     *msg = "attn: cuTensorMapEncodeTiled is unavailable";
     return false;
   }
-  const CUtensorMapDataType dt =
-      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = elem == kKvElemU8     ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem == kKvElemBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t esz = elem == kKvElemU8 ? 1 : 2;
+  const cuuint32_t box_in = elem == kKvElemU8 ? 128u : 64u;  // 128 bytes either way
   const bool three_d = nhd && box_rows > 1;
   for (int which = 0; which < 2; ++which) {
     const cuuint64_t dims2[2] = {cuuint64_t(kHeadDim), rows};
-    const cuuint64_t strides2[1] = {cuuint64_t(kHeadDim) * 2};
-    const cuuint32_t box2[2] = {64u, box_rows};
+    const cuuint64_t strides2[1] = {cuuint64_t(kHeadDim) * esz};
+    const cuuint32_t box2[2] = {box_in, box_rows};
     const cuuint64_t dims3[3] = {cuuint64_t(kHeadDim), cuuint64_t(num_kv_heads),
                                  cuuint64_t(num_pages) * page_size};
-    const cuuint64_t strides3[2] = {cuuint64_t(kHeadDim) * 2,
-                                    cuuint64_t(kHeadDim) * 2 * cuuint64_t(num_kv_heads)};
-    const cuuint32_t box3[3] = {64u, 1u, box_rows};
+    const cuuint64_t strides3[2] = {cuuint64_t(kHeadDim) * esz,
+                                    cuuint64_t(kHeadDim) * esz * cuuint64_t(num_kv_heads)};
+    const cuuint32_t box3[3] = {box_in, 1u, box_rows};
     const cuuint32_t es[3] = {1, 1, 1};
     CUtensorMap* tm = which == 0 ? tm_k : tm_v;
     void* ptr = const_cast<void*>(which == 0 ? k_pool : v_pool);
@@ -260,27 +269,27 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
 // encode_kv_maps, remembering the last pools described on this thread (a
 // serving loop runs over the same pools step after step).
 inline bool make_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
-                         int32_t num_kv_heads, int32_t page_size, bool bf16, uint32_t box_rows,
+                         int32_t num_kv_heads, int32_t page_size, int elem, uint32_t box_rows,
                          bool nhd, CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
   struct Key {
     const void *k, *v;
     int64_t pages;
-    int32_t heads, page_size, bf16;
+    int32_t heads, page_size, elem;
     uint32_t box_rows;
     int32_t nhd;
   };
   thread_local Key last = {nullptr, nullptr, -1, 0, 0, 0, 0, 0};
   thread_local CUtensorMap last_k, last_v;
-  const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16 ? 1 : 0, box_rows,
+  const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, elem, box_rows,
                    nhd ? 1 : 0};
   if (key.k == last.k && key.v == last.v && key.pages == last.pages && key.heads == last.heads &&
-      key.page_size == last.page_size && key.bf16 == last.bf16 && key.box_rows == last.box_rows &&
+      key.page_size == last.page_size && key.elem == last.elem && key.box_rows == last.box_rows &&
       key.nhd == last.nhd) {
     *tm_k = last_k;
     *tm_v = last_v;
     return true;
   }
-  if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, bf16, box_rows, nhd,
+  if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, elem, box_rows, nhd,
                       tm_k, tm_v, msg))
     return false;
   last = key;
