@@ -818,12 +818,52 @@ def run_ours(args, rank, world):
             t0 = time.perf_counter()
             e2e_step()
             tot += time.perf_counter() - t0
-        e2e = {"value": b / (tot / n_e2e) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+        serial = b / (tot / n_e2e) / 1e9
+
+        # The same steps as a serving loop issues them: step k + 1's input
+        # copy, planning and launch are enqueued while step k runs, and the
+        # host reads step k's output (from one of two pinned buffers) once
+        # step k + 1 is enqueued. Every step still copies its inputs in and
+        # its output out; one stream orders copies and kernels.
+        out_hs = [out_h, torch.empty(out_bytes, dtype=torch.uint8).pin_memory()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        lse_off = out_offs[1]
+
+        def enqueue(k):
+            in_d.copy_(in_h, non_blocking=True)
+            att.plan(c.kv_indptr, c.last_page_len, c.page_size)
+            att.run(q_d, st.d["k_pool"], st.d["v_pool"], kvi_d, kvx_d, lpl_d, w.sm_scale,
+                    out=o_d, lse=lse_d)
+            out_hs[k % 2].copy_(out_d, non_blocking=True)
+            done[k % 2].record()
+
+        def consume(k):
+            done[k % 2].synchronize()
+            return float(out_hs[k % 2][lse_off:lse_off + 4].view(torch.float32)[0])
+
+        for k in range(4):
+            enqueue(k)
+        consume(3)
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in range(n_e2e):
+            enqueue(k)
+            if k > 0:
+                consume(k - 1)
+        last = consume(n_e2e - 1)
+        tot_p = time.perf_counter() - t0
+        assert math.isfinite(last)
+        e2e = {"value": b * n_e2e / tot_p / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "serialized_value": serial,
                "note": "KV pool stays resident in HBM (it is the cache); per-step inputs "
                        "(q and the page table, packed in one pinned buffer, plus the plan "
                        "tables attn_plan uploads) and outputs (o and lse, one buffer) cross "
-                       "the host link every step"}
+                       "the host link every step. value: steps pipelined as a serving loop "
+                       "issues them (step k + 1 enqueued while step k runs, step k's output "
+                       "read after that), wall clock over all steps; serialized_value: each "
+                       "step enqueued, run and read back before the next starts"}
 
     if rank != 0:
         return None
