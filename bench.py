@@ -300,11 +300,12 @@ def bench_causal_append(hbm_peak, bf16_peak, flush, steps, warmup):
 
 
 def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
-    """Prefix append (P = 128, once per prompt) and suffix decode on two
-    streams (CascadeAttention) + LSE merge, next to the same logical KV as one
-    flat P = 16 decode."""
+    """Composable formats in one launch (CascadeAttention: prefix pages at
+    P = 128 read once per prompt and suffix pages at P = 16 balanced together
+    by attn_plan_cascade, merged inside the kernel), beside the two-pass
+    variant (prefix append and suffix decode on two streams + LSE merge) and
+    the same logical KV as one flat P = 16 decode."""
     from paged_kv_attention_bsr_gb300 import synth
-    from paged_kv_attention_bsr_gb300.api import PagedAttention
     from paged_kv_attention_bsr_gb300.synth import Workload
     w = synth.shared_prefix_decode()
     pre, suf = w.extra["prefix"], w.cache
@@ -313,32 +314,45 @@ def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
     pqo_h = w.extra["prefix_qo_indptr"]
     pqo = torch.from_numpy(pqo_h).cuda()
     from paged_kv_attention_bsr_gb300.api import CascadeAttention
-    ca = CascadeAttention(32, 8, 128, max_prompts=w.extra["prompts"], max_batch=w.batch)
-    att_p, att_s = ca.prefix, ca.suffix
     o_m = torch.empty_like(q)
     l_m = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
-
-    def plans():
-        ca.plan(pqo_h, pre.kv_indptr, pre.last_page_len, pre.page_size, suf.kv_indptr,
-                suf.last_page_len, suf.page_size)
-
-    def runs():
-        ca.run(q, dp, ds, pqo, w.sm_scale, out=o_m, lse=l_m)
-
-    step_ms, kern_ms = time_steps([plans, runs], steps, warmup, flush)
     kvb = 2 * 8 * 128 * 2
     b_pre = int(pre.kv_lens.sum()) * kvb
     b_suf = int(suf.kv_lens.sum()) * kvb
     b_flat = int(pre.kv_lens.sum()) * w.extra["n"] * kvb + b_suf
-    k_s = float(np.median(kern_ms)) * 1e-3
+
+    def timed(mode):
+        ca = CascadeAttention(32, 8, 128, max_prompts=w.extra["prompts"], max_batch=w.batch,
+                              mode=mode)
+
+        def plans():
+            ca.plan(pqo_h, pre.kv_indptr, pre.last_page_len, pre.page_size, suf.kv_indptr,
+                    suf.last_page_len, suf.page_size)
+
+        def runs():
+            ca.run(q, dp, ds, pqo, w.sm_scale, out=o_m, lse=l_m)
+
+        step_ms, kern_ms = time_steps([plans, runs], steps, warmup, flush)
+        assert ca.status() == 0
+        return ca, float(np.median(step_ms)) * 1e3, float(np.median(kern_ms)) * 1e-3
+
+    ca, step_us, k_s = timed("one_launch")
     res = {"kind": "composable", "bytes": b_pre + b_suf, "flat_layout_bytes": b_flat,
-           "kernel_us": k_s * 1e6, "step_us": float(np.median(step_ms)) * 1e3,
+           "kernel_us": k_s * 1e6, "step_us": step_us,
            "GB/s": (b_pre + b_suf) / k_s / 1e9,
            "roofline_frac_hbm": (b_pre + b_suf) / k_s / 1e9 / hbm_peak,
-           "launches_per_step": 3 + (att_p.plan_info.num_split_items > 0),
-           "streams": "prefix pass and suffix pass on two streams, merge after the join"}
-    assert att_p.status() == 0 and att_s.status() == 0
-    del dp, ds
+           "launches_per_step": 1,
+           "path": "one launch: prefix and suffix units of every (prompt, kv head) in one "
+                   "persistent few-row kernel, merged in the kernel",
+           "plan_units": ca.plan_info.num_units}
+    ca2, step2_us, k2_s = timed("two_pass")
+    res["two_pass"] = {"kernel_us": k2_s * 1e6, "step_us": step2_us,
+                       "GB/s": (b_pre + b_suf) / k2_s / 1e9,
+                       "roofline_frac_hbm": (b_pre + b_suf) / k2_s / 1e9 / hbm_peak,
+                       "launches_per_step": 3 + (ca2.prefix.plan_info.num_split_items > 0),
+                       "streams": "prefix pass and suffix pass on two streams, merge after "
+                                  "the join"}
+    del dp, ds, ca, ca2
     flat = synth.flat_layout_of_composable(w)
     wf = Workload("flat", "decode", torch.bfloat16, 32, 8, 128, w.sm_scale, w.q, flat)
     st = DecodeStep(wf)

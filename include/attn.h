@@ -62,7 +62,7 @@ typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
  * NHD: [num_pages, page_size, num_kv_heads, head_dim]. Both row-major. */
 typedef enum { ATTN_LAYOUT_HND = 0, ATTN_LAYOUT_NHD = 1 } attn_kv_layout_t;
 
-typedef enum { ATTN_MODE_DECODE = 0, ATTN_MODE_APPEND = 1 } attn_mode_t;
+typedef enum { ATTN_MODE_DECODE = 0, ATTN_MODE_APPEND = 1, ATTN_MODE_CASCADE = 2 } attn_mode_t;
 
 /*
  * A work plan: plain data produced by attn_plan. It records the shapes the
@@ -87,7 +87,8 @@ typedef struct attn_plan {
   int32_t total_qo;         /* query rows (decode: batch)                      */
   int32_t max_qo_len;       /* longest query row count of a request (decode: 1) */
   int64_t total_weight;     /* sum over items of (pages + 1)                   */
-  int64_t max_cta_weight;   /* largest per-CTA share of total_weight           */
+  int64_t max_cta_weight;   /* largest per-CTA share of the weights the cut
+                               balances (cascade: tokens + 16 per segment)     */
   int64_t off_work_indptr;  /* byte offsets of the tables in the workspaces    */
   int64_t off_units;
   int64_t off_merge_indptr;
@@ -101,6 +102,8 @@ typedef struct attn_plan {
   int64_t max_kv_len;       /* longest kv length of a request                  */
   int64_t min_kv_minus_qo;  /* smallest kv_len - qo_len over requests with kv
                                tokens (INT64_MAX if none)                      */
+  int32_t page_size_suffix; /* cascade: page size of the suffix table (else 0) */
+  int32_t reserved;         /* 0                                               */
 } attn_plan_t;
 
 /*
@@ -119,7 +122,7 @@ attn_status_t attn_workspace_size(int32_t max_batch, int32_t max_total_qo,
 
 /*
  * Default persistent grid for `mode` on CUDA device `device`: the number of
- * SMs times the CTAs of the run kernel that fit on one SM.
+ * SMs times the CTAs of the run kernel that fit on one SM (cascade: one).
  * Errors: CUDA if the device cannot be queried; INVALID_ARG for bad mode.
  */
 attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_ctas);
@@ -336,6 +339,81 @@ attn_status_t attn_merge_states(const void* o_a, const float* lse_a,
                                 const void* o_b, const float* lse_b, void* o_out,
                                 float* lse_out, int32_t n, int32_t num_heads,
                                 int32_t head_dim, int32_t dtype, void* stream);
+
+/*
+ * Composable formats in one launch ("可组合格式": a shared prefix stored once in
+ * a table with large pages, each generation's own suffix in a second table
+ * with small pages; the partial attention over the two is combined by
+ * log-sum-exp). Decode shape: prompt p has n_p generations, rows
+ * qo_indptr[p] .. qo_indptr[p+1] of q, one query row each. Generation b of
+ * prompt p attends to the prompt's prefix (prefix table row p) followed by
+ * its own suffix (suffix table row b); the result equals decode over the flat
+ * layout prefix ++ suffix.
+ *
+ * attn_cascade_workspace_size: workspace sizes for any cascade plan with at
+ * most max_prompts prompts, max_batch generations and num_ctas CTAs.
+ *
+ * attn_plan_cascade: items are (prompt, kv head) pairs; an item's segments are
+ * its prefix row and then one suffix row per generation. A segment weighs
+ * its tokens (pages x page size) + 16; the weights are laid end to end and
+ * CTA c takes the positions [floor(c W / C), floor((c+1) W / C)), a page
+ * going to the CTA that owns its first position (pages of one segment on one
+ * CTA form a unit; a segment without pages keeps one empty unit). Every item
+ * with generations is merged inside the run kernel: each unit writes a
+ * partial state (the prefix unit for all n_p rows, a suffix unit for its
+ * generation's row) and the last unit to finish combines them.
+ *   qo_indptr_h             : host int32[num_prompts+1], generations per
+ *                             prompt, starting at 0 (batch = its last entry)
+ *   kv_indptr_prefix_h,
+ *   last_page_len_prefix_h  : host prefix table, num_prompts rows, pages of
+ *                             page_size_prefix tokens
+ *   kv_indptr_suffix_h,
+ *   last_page_len_suffix_h  : host suffix table, batch rows, pages of
+ *                             page_size_suffix tokens
+ *   other arguments as attn_plan (dev_ws NULL plans on the host only).
+ * group x (the largest n_p) must be at most 16 (rows of one MMA item).
+ * Errors: INVALID_ARG, UNSUPPORTED (head_dim, group x n_p > 16),
+ * WORKSPACE_TOO_SMALL, CUDA.
+ *
+ * attn_cascade_run: one persistent launch of the few-row tensor-core kernel
+ * over both tables, merging inside the kernel.
+ *   q                  : device [batch, num_qo_heads, head_dim] of `dtype`
+ *   qo_indptr          : device copy of qo_indptr_h
+ *   k_prefix, v_prefix : device HND pools of num_pages_prefix pages of
+ *                        page_size_prefix tokens, `dtype`
+ *   kv_indptr_prefix, kv_indices_prefix, last_page_len_prefix : device copies
+ *                        of the prefix table (indices in [0, num_pages_prefix))
+ *   k_suffix ... last_page_len_suffix : the same for the suffix table
+ *   o                  : device [batch, num_qo_heads, head_dim] (out)
+ *   lse                : device float[batch, num_qo_heads] (out) or NULL
+ * Supported: HND pools, both page sizes multiples of 16, group 1..16 with
+ * group x n_p <= 16, fp16 / bf16. ATTN_DEBUG_CHECKS applies to both tables.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
+ */
+attn_status_t attn_cascade_workspace_size(int32_t max_prompts, int32_t max_batch,
+                                          int32_t num_qo_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t num_ctas,
+                                          size_t* dev_bytes, size_t* pinned_host_bytes);
+
+attn_status_t attn_plan_cascade(const int32_t* qo_indptr_h, const int32_t* kv_indptr_prefix_h,
+                                const int32_t* last_page_len_prefix_h, int32_t page_size_prefix,
+                                const int32_t* kv_indptr_suffix_h,
+                                const int32_t* last_page_len_suffix_h, int32_t page_size_suffix,
+                                int32_t num_prompts, int32_t num_qo_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t num_ctas, void* pinned_host_ws,
+                                size_t pinned_bytes, void* dev_ws, size_t dev_bytes,
+                                void* stream, attn_plan_t* plan_out);
+
+attn_status_t attn_cascade_run(const attn_plan_t* plan, const void* q, const int32_t* qo_indptr,
+                               const void* k_prefix, const void* v_prefix,
+                               int64_t num_pages_prefix, const int32_t* kv_indptr_prefix,
+                               const int32_t* kv_indices_prefix,
+                               const int32_t* last_page_len_prefix, const void* k_suffix,
+                               const void* v_suffix, int64_t num_pages_suffix,
+                               const int32_t* kv_indptr_suffix, const int32_t* kv_indices_suffix,
+                               const int32_t* last_page_len_suffix, int32_t dtype,
+                               float sm_scale, void* o, float* lse, void* dev_ws,
+                               size_t dev_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads the error word that kernels set in a

@@ -28,6 +28,8 @@ pseudo-code; the exact cut below is the reading used throughout this project:
   slots      items with >= 2 units are split; their units get partial-state
              slots numbered in (item, page) order; merge_indptr lists them.
 
+  cascade    composable formats in one launch: make_cascade_plan below.
+
 It is written independently of the library's C++ planner; the tests require
 the two to agree bit for bit.
 """
@@ -192,4 +194,127 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
         plan.unit_p0.append(u[4])
         plan.unit_p1.append(u[5])
         plan.unit_slot.append(slot_of[i])
+    return plan
+
+
+CASCADE_ALPHA = 16  # tokens of overhead per segment
+
+
+def few_rows(group: int, max_rows: int) -> int:
+    """Rows of one few-row item: the smallest power of two >= group x
+    max_rows, at most FEW_ROWS (0 if it does not fit)."""
+    need = group * max(max_rows, 1)
+    r = 1
+    while r <= FEW_ROWS:
+        if need <= r:
+            return r
+        r *= 2
+    return 0
+
+
+def make_cascade_plan(qo_indptr: Sequence[int], kv_indptr_prefix: Sequence[int],
+                      last_prefix: Sequence[int], page_size_prefix: int,
+                      kv_indptr_suffix: Sequence[int], last_suffix: Sequence[int],
+                      page_size_suffix: int, num_qo_heads: int, num_kv_heads: int,
+                      num_ctas: int) -> Plan:
+    """Composable formats in one launch (modb.pro digest, "可组合格式": a shared
+    prefix stored once, per-generation suffixes in a second table, partial
+    states combined by log-sum-exp). Reading used:
+
+      items      (prompt p, kv head hk) for prompts with generations, p-major
+      segments   per item: the prompt's prefix row (t = -1), then the suffix
+                 row of each generation j (t = j), in that order
+      weight     a segment weighs pages x page size + 16 tokens; laid end to
+                 end (total W), CTA c owns positions [floor(c W / C),
+                 floor((c+1) W / C)); page k of a segment at base b sits at
+                 position b + 16 + k P and belongs to the CTA owning it; the
+                 pages of a segment on one CTA form a unit; a segment without
+                 pages is one empty unit, owned by the CTA owning b
+      slots      every unit has one, numbered in unit order; every item is merged
+
+    Extra fields: unit_kind (0 prefix, 1 suffix), unit_page_base, unit_kv_len,
+    unit_qo_start, unit_qo_len; merge_count per item; rows_per_item.
+    """
+    import bisect
+    prompts = len(qo_indptr) - 1
+    group = num_qo_heads // num_kv_heads
+    C = num_ctas
+
+    def length(indptr, last, P, row):
+        n = indptr[row + 1] - indptr[row]
+        return n, (0 if n == 0 else (n - 1) * P + last[row])
+
+    segs = []  # (item, p, hk, t, kind, n, kv_len, page_base, P)
+    items = []
+    max_n = max([qo_indptr[p + 1] - qo_indptr[p] for p in range(prompts)] + [0])
+    for p in range(prompts):
+        n_p = qo_indptr[p + 1] - qo_indptr[p]
+        if n_p == 0:
+            continue
+        for hk in range(num_kv_heads):
+            it = len(items)
+            items.append((p, hk))
+            n, kv = length(kv_indptr_prefix, last_prefix, page_size_prefix, p)
+            segs.append((it, p, hk, -1, 0, n, kv, kv_indptr_prefix[p], page_size_prefix))
+            for j in range(n_p):
+                b = qo_indptr[p] + j
+                n, kv = length(kv_indptr_suffix, last_suffix, page_size_suffix, b)
+                segs.append((it, p, hk, j, 1, n, kv, kv_indptr_suffix[b], page_size_suffix))
+    W = sum(s[5] * s[8] + CASCADE_ALPHA for s in segs)
+    bounds = [(c * W) // C for c in range(C)]
+
+    def owner(pos):  # the last CTA whose range starts at or before pos
+        return bisect.bisect_right(bounds, pos) - 1
+
+    per_cta = [[] for _ in range(C)]
+    base = 0
+    for (it, p, hk, t, kind, n, kv, pb, P) in segs:
+        rec = dict(item=it, r=p, hk=hk, t=t, kind=kind, kv_len=kv, page_base=pb,
+                   qo_start=qo_indptr[p], qo_len=qo_indptr[p + 1] - qo_indptr[p])
+        if n == 0:
+            per_cta[owner(base)].append(dict(rec, p0=0, p1=0))
+        else:
+            owners = [owner(base + CASCADE_ALPHA + k * P) for k in range(n)]
+            k0 = 0
+            for k in range(1, n + 1):
+                if k == n or owners[k] != owners[k0]:
+                    per_cta[owners[k0]].append(dict(rec, p0=k0, p1=k))
+                    k0 = k
+        base += n * P + CASCADE_ALPHA
+
+    plan = Plan(work_indptr=[0] * (C + 1), num_items=len(items), q_tile=max_n)
+    flat = []
+    for c in range(C):
+        plan.work_indptr[c + 1] = plan.work_indptr[c] + len(per_cta[c])
+        flat.extend(per_cta[c])
+    count = [0] * len(items)
+    for u in flat:
+        count[u["item"]] += 1
+    plan.merge_indptr = [0]
+    for k in range(len(items)):
+        plan.merge_indptr.append(plan.merge_indptr[-1] + count[k])
+        plan.merge_r.append(items[k][0])
+        plan.merge_hk.append(items[k][1])
+        plan.merge_t.append(0)
+    plan.merge_count = count
+    seen = [0] * len(items)
+    plan.unit_kind, plan.unit_page_base, plan.unit_kv_len = [], [], []
+    plan.unit_qo_start, plan.unit_qo_len, plan.unit_split = [], [], []
+    for u in flat:
+        k = u["item"]
+        plan.unit_r.append(u["r"])
+        plan.unit_hk.append(u["hk"])
+        plan.unit_t.append(u["t"])
+        plan.unit_p0.append(u["p0"])
+        plan.unit_p1.append(u["p1"])
+        plan.unit_slot.append(plan.merge_indptr[k] + seen[k])
+        seen[k] += 1
+        plan.unit_split.append(k)
+        plan.unit_kind.append(u["kind"])
+        plan.unit_page_base.append(u["page_base"])
+        plan.unit_kv_len.append(u["kv_len"])
+        plan.unit_qo_start.append(u["qo_start"])
+        plan.unit_qo_len.append(u["qo_len"])
+    plan.total_weight = sum(s[5] for s in segs) + len(items)
+    plan.rows_per_item = few_rows(group, max_n)
     return plan

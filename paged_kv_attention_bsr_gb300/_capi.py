@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libattn.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT = range(6)
 F16, BF16 = 0, 1
 LAYOUT_HND, LAYOUT_NHD = 0, 1
-MODE_DECODE, MODE_APPEND = 0, 1
+MODE_DECODE, MODE_APPEND, MODE_CASCADE = 0, 1, 2
 
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
                 4: "CUDA", 5: "TIMEOUT"}
@@ -29,7 +29,8 @@ EXPORTS = ("attn_workspace_size", "attn_default_num_ctas", "attn_plan", "attn_de
            "attn_append_run", "attn_merge_states", "attn_workspace_status", "attn_last_error",
            "attn_decode_run_noalloc", "attn_wait_selftest", "attn_decode_run_rope",
            "attn_append_run_rope", "attn_decode_run_noalloc_status",
-           "attn_wait_selftest_noalloc", "attn_decode_run_fp8")
+           "attn_wait_selftest_noalloc", "attn_decode_run_fp8", "attn_cascade_workspace_size",
+           "attn_plan_cascade", "attn_cascade_run")
 
 
 class AttnError(RuntimeError):
@@ -47,7 +48,8 @@ class Plan(ctypes.Structure):
         "total_weight", "max_cta_weight", "off_work_indptr", "off_units", "off_merge_indptr",
         "off_merge_items", "off_counters", "off_partial_o", "off_partial_lse", "table_bytes",
         "dev_bytes_needed")] + [("fingerprint", ctypes.c_uint64), ("max_kv_len", ctypes.c_int64),
-                              ("min_kv_minus_qo", ctypes.c_int64)]
+                              ("min_kv_minus_qo", ctypes.c_int64),
+                              ("page_size_suffix", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 def _load():
@@ -81,6 +83,11 @@ def _load():
         "attn_decode_run_fp8": [P(Plan), vp, vp, vp, i64, i32, vp, vp, vp, i32, vp, vp, f32, vp,
                                 vp, vp, sz, vp],
         "attn_wait_selftest_noalloc": [i32, vp],
+        "attn_cascade_workspace_size": [i32, i32, i32, i32, i32, i32, P(sz), P(sz)],
+        "attn_plan_cascade": [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, sz, vp,
+                              sz, vp, P(Plan)],
+        "attn_cascade_run": [P(Plan), vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, vp, vp, vp,
+                             i32, f32, vp, vp, vp, sz, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -171,6 +178,62 @@ def plan(qo_indptr_h, kv_indptr_h, last_page_len_h, page_size, num_qo_heads, num
                          num_ctas, _ptr(pinned_ws), host_bytes, _ptr(dev_ws), dev_bytes,
                          _stream(stream) if dev_ws is not None else None, ctypes.byref(p)))
     return p
+
+
+def cascade_workspace_size(max_prompts, max_batch, num_qo_heads, num_kv_heads, head_dim,
+                           num_ctas):
+    dev = ctypes.c_size_t()
+    host = ctypes.c_size_t()
+    _check(lib.attn_cascade_workspace_size(max_prompts, max_batch, num_qo_heads, num_kv_heads,
+                                           head_dim, num_ctas, ctypes.byref(dev),
+                                           ctypes.byref(host)))
+    return dev.value, host.value
+
+
+def plan_cascade(qo_indptr_h, kv_indptr_prefix_h, last_prefix_h, page_size_prefix,
+                 kv_indptr_suffix_h, last_suffix_h, page_size_suffix, num_qo_heads, num_kv_heads,
+                 head_dim, num_ctas, pinned_ws, dev_ws=None, stream=None) -> Plan:
+    """attn_plan_cascade. Host arrays; dev_ws None plans on the host only."""
+    qo_indptr_h = _host_i32(qo_indptr_h)
+    kv_indptr_prefix_h, last_prefix_h = _host_i32(kv_indptr_prefix_h), _host_i32(last_prefix_h)
+    kv_indptr_suffix_h, last_suffix_h = _host_i32(kv_indptr_suffix_h), _host_i32(last_suffix_h)
+    prompts = len(qo_indptr_h) - 1
+    if len(kv_indptr_prefix_h) != prompts + 1 or len(last_prefix_h) < prompts:
+        raise ValueError("the prefix table needs one row per prompt")
+    batch = int(qo_indptr_h[-1]) if prompts > 0 else 0
+    if len(kv_indptr_suffix_h) != batch + 1 or len(last_suffix_h) < batch:
+        raise ValueError("the suffix table needs one row per generation (qo_indptr[-1])")
+    host_bytes = pinned_ws.numel() * pinned_ws.element_size() if isinstance(
+        pinned_ws, torch.Tensor) else pinned_ws.nbytes
+    dev_bytes = 0 if dev_ws is None else dev_ws.numel() * dev_ws.element_size()
+    p = Plan()
+    _check(lib.attn_plan_cascade(_ptr(qo_indptr_h), _ptr(kv_indptr_prefix_h), _ptr(last_prefix_h),
+                                 page_size_prefix, _ptr(kv_indptr_suffix_h), _ptr(last_suffix_h),
+                                 page_size_suffix, prompts, num_qo_heads, num_kv_heads, head_dim,
+                                 num_ctas, _ptr(pinned_ws), host_bytes, _ptr(dev_ws), dev_bytes,
+                                 _stream(stream) if dev_ws is not None else None,
+                                 ctypes.byref(p)))
+    return p
+
+
+def cascade_run(p: Plan, q, qo_indptr, prefix, suffix, sm_scale, o, lse, dev_ws, stream=None):
+    """attn_cascade_run. prefix / suffix: dicts of device tensors k_pool,
+    v_pool (HND), kv_indptr, kv_indices, last_page_len and optionally
+    num_pages (default: the pool's first dimension)."""
+    n0 = int(prefix.get("num_pages", prefix["k_pool"].shape[0]))
+    n1 = int(suffix.get("num_pages", suffix["k_pool"].shape[0]))
+    has_kv = p.total_weight > p.num_items
+    _check_shapes(p.num_qo_heads, p.num_kv_heads, p.page_size, p.head_dim, has_kv, q,
+                  prefix["k_pool"], prefix["v_pool"], o, lse, n0, p.total_qo)
+    _check_shapes(p.num_qo_heads, p.num_kv_heads, p.page_size_suffix, p.head_dim, has_kv, q,
+                  suffix["k_pool"], suffix["v_pool"], o, lse, n1, p.total_qo)
+    _check(lib.attn_cascade_run(
+        ctypes.byref(p), _ptr(q), _ptr(qo_indptr), _ptr(prefix["k_pool"]),
+        _ptr(prefix["v_pool"]), n0, _ptr(prefix["kv_indptr"]), _ptr(prefix["kv_indices"]),
+        _ptr(prefix["last_page_len"]), _ptr(suffix["k_pool"]), _ptr(suffix["v_pool"]), n1,
+        _ptr(suffix["kv_indptr"]), _ptr(suffix["kv_indices"]), _ptr(suffix["last_page_len"]),
+        dtype_code(q.dtype), float(sm_scale), _ptr(o), _ptr(lse), _ptr(dev_ws),
+        dev_ws.numel() * dev_ws.element_size(), _stream(stream)))
 
 
 def _check_dense(**tensors):

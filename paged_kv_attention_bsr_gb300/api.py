@@ -116,44 +116,113 @@ class CascadeAttention:
     """Composable formats (shared prefix + unique suffix) for decode.
 
     The prompt's common prefix is stored once in a pool with large pages and
-    read once for its n generations: a non-causal short append with the n
-    generations' query rows per prompt (qo_indptr_prefix). Each generation's
-    own suffix lives in a second pool (small pages) and is read by a decode
-    pass. The two partial states are combined by attn_merge_states. The
-    prefix and suffix passes are independent, so they are enqueued on two
-    streams (the suffix on a side stream forked from and joined back into the
-    caller's stream): the second launch fills the SMs the first one's tail
-    leaves idle instead of waiting for it. The merge runs on the caller's
-    stream after the join.
+    read once for its n generations; each generation's own suffix lives in a
+    second pool (small pages). Two ways to run it:
+
+    * one launch (attn_plan_cascade / attn_cascade_run), taken when both
+      pools are HND with page sizes that are multiples of 16 and
+      group x n <= 16: one persistent few-row kernel balances the prefix and
+      suffix pages of every (prompt, kv head) together and merges the partial
+      states inside the kernel;
+    * otherwise two passes: a non-causal short append for the prefix (the n
+      generations' rows per prompt) and a decode for the suffixes, enqueued
+      on two streams (the suffix on a side stream forked from and joined back
+      into the caller's stream), then attn_merge_states.
+
+    mode: "auto" (one launch when the shapes allow it), "one_launch" (raise
+    if they do not) or "two_pass".
     """
 
+    RING = 4
+
     def __init__(self, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
-                 max_prompts: int = 64, max_batch: int = 256, device=None):
+                 max_prompts: int = 64, max_batch: int = 256, device=None, mode: str = "auto",
+                 num_ctas: Optional[int] = None):
+        if mode not in ("auto", "one_launch", "two_pass"):
+            raise ValueError("mode must be 'auto', 'one_launch' or 'two_pass'")
+        self.mode = mode
+        self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
         self.prefix = PagedAttention(num_qo_heads, num_kv_heads, head_dim, "append",
                                      max_batch=max_prompts, max_total_qo=max_batch,
                                      device=device)
         self.suffix = PagedAttention(num_qo_heads, num_kv_heads, head_dim, "decode",
                                      max_batch=max_batch, device=device)
-        self.side = torch.cuda.Stream(device=self.prefix.device)
+        self.device = self.prefix.device
+        self.side = torch.cuda.Stream(device=self.device)
         self._fork = torch.cuda.Event()
         self._join = torch.cuda.Event()
         self._bufs = None
+        self.one_launch = False
+        self.plan_info: Optional[C.Plan] = None
+        if mode != "two_pass":
+            dev_index = self.device.index if self.device.index is not None else \
+                torch.cuda.current_device()
+            self.num_ctas = num_ctas or C.default_num_ctas(dev_index, C.MODE_CASCADE)
+            dev_bytes, host_bytes = C.cascade_workspace_size(max_prompts, max_batch,
+                                                             num_qo_heads, num_kv_heads,
+                                                             head_dim, self.num_ctas)
+            self.dev_ws = torch.empty(dev_bytes, dtype=torch.uint8, device=self.device)
+            self._pinned = [torch.empty(host_bytes, dtype=torch.uint8).pin_memory()
+                            for _ in range(self.RING)]
+            self._events = [None] * self.RING
+            self._turn = 0
+
+    def _fits_one_launch(self, qo_indptr_h, page_size_prefix, page_size_suffix) -> bool:
+        qo = np.asarray(qo_indptr_h)
+        max_n = int(np.diff(qo).max()) if len(qo) > 1 else 0
+        group = self.num_qo_heads // self.num_kv_heads
+        return (group * max(max_n, 1) <= 16 and page_size_prefix % 16 == 0 and
+                page_size_suffix % 16 == 0)
 
     def plan(self, qo_indptr_prefix_h, kv_indptr_prefix_h, last_page_len_prefix_h,
              page_size_prefix: int, kv_indptr_suffix_h, last_page_len_suffix_h,
              page_size_suffix: int, stream=None):
-        """Plans both passes; the tables are uploaded on `stream`."""
+        """Plans the run; the tables are uploaded on `stream`."""
+        fits = self._fits_one_launch(qo_indptr_prefix_h, page_size_prefix, page_size_suffix)
+        if self.mode == "one_launch" and not fits:
+            raise ValueError("one launch needs group x generations <= 16 and page sizes that "
+                             "are multiples of 16")
+        self.one_launch = self.mode != "two_pass" and fits
+        if self.one_launch:
+            i = self._turn
+            self._turn = (self._turn + 1) % self.RING
+            ev = self._events[i]
+            if ev is None:
+                ev = self._events[i] = torch.cuda.Event()
+            else:
+                ev.synchronize()  # the previous upload from this staging buffer has run
+            if stream is None:
+                stream = torch.cuda.current_stream()
+            self.plan_info = C.plan_cascade(
+                qo_indptr_prefix_h, kv_indptr_prefix_h, last_page_len_prefix_h,
+                page_size_prefix, kv_indptr_suffix_h, last_page_len_suffix_h, page_size_suffix,
+                self.num_qo_heads, self.num_kv_heads, self.head_dim, self.num_ctas,
+                self._pinned[i], self.dev_ws, stream)
+            ev.record(stream)
+            return self.plan_info
         self.prefix.plan(kv_indptr_prefix_h, last_page_len_prefix_h, page_size_prefix,
                          qo_indptr_h=qo_indptr_prefix_h, causal=False, stream=stream)
         self.suffix.plan(kv_indptr_suffix_h, last_page_len_suffix_h, page_size_suffix,
                          stream=stream)
+        self.plan_info = None
+        return None
 
     def run(self, q, prefix, suffix, qo_indptr_prefix, sm_scale=None, out=None, lse=None,
             return_lse: bool = False):
         """q [batch, Hq, D] (one row per generation, grouped by prompt);
         prefix / suffix: dicts with k_pool, v_pool, kv_indptr, kv_indices,
-        last_page_len device tensors. Returns o (and lse)."""
+        last_page_len device tensors (HND pools). Returns o (and lse)."""
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.head_dim)
         stream = torch.cuda.current_stream()
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        if self.one_launch:
+            C.cascade_run(self.plan_info, q, qo_indptr_prefix, prefix, suffix, sm_scale, out,
+                          lse, self.dev_ws, stream)
+            return (out, lse) if return_lse else out
         if self._bufs is None or self._bufs[0].shape != q.shape or \
                 self._bufs[0].dtype != q.dtype:
             mk = lambda: torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
@@ -170,14 +239,16 @@ class CascadeAttention:
                         prefix["kv_indices"], prefix["last_page_len"], sm_scale, out=o_p,
                         lse=l_p, qo_indptr=qo_indptr_prefix, stream=stream)
         stream.wait_event(self._join)
-        if out is None:
-            out = torch.empty_like(q)
-        if lse is None and return_lse:
-            lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
         if lse is None:
             lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
         C.merge_states(o_p, l_p, o_s, l_s, out, lse, stream=stream)
         return (out, lse) if return_lse else out
+
+    def status(self, stream=None) -> int:
+        """Synchronise and return the one-launch workspace's error word (0 = none)."""
+        if self.mode == "two_pass":
+            return max(self.prefix.status(stream), self.suffix.status(stream))
+        return C.workspace_status(self.dev_ws, stream)
 
 
 _single_cache = {}

@@ -152,6 +152,80 @@ attn_status_t debug_check_table(const attn_plan_t* plan, const int32_t* qo_indpt
   return ATTN_OK;
 }
 
+// debug_check_table for a composable-format run: both tables and qo_indptr
+// must be the plan's (fingerprint), every index the run reads in range.
+attn_status_t debug_check_cascade(const attn_plan_t* plan, const int32_t* qo_indptr,
+                                  const int32_t* kv_indptr0, const int32_t* kv_indices0,
+                                  const int32_t* last0, int64_t num_pages0,
+                                  const int32_t* kv_indptr1, const int32_t* kv_indices1,
+                                  const int32_t* last1, int64_t num_pages1, void* stream,
+                                  const char* fn) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return ATTN_OK;
+  const std::string f(fn);
+  const int32_t prompts = plan->batch, B = plan->total_qo;
+  if (prompts == 0) return ATTN_OK;
+  auto read = [&](std::vector<int32_t>& dst, const int32_t* src, int64_t n) -> cudaError_t {
+    dst.resize(static_cast<size_t>(n));
+    if (n == 0) return cudaSuccess;
+    return cudaMemcpyAsync(dst.data(), src, 4 * size_t(n), cudaMemcpyDeviceToHost, st);
+  };
+  std::vector<int32_t> qo, ip0, l0, ip1, l1;
+  cudaError_t e = read(qo, qo_indptr, int64_t(prompts) + 1);
+  if (e == cudaSuccess) e = read(ip0, kv_indptr0, int64_t(prompts) + 1);
+  if (e == cudaSuccess) e = read(l0, last0, prompts);
+  if (e == cudaSuccess) e = read(ip1, kv_indptr1, int64_t(B) + 1);
+  if (e == cudaSuccess) e = read(l1, last1, B);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, (f + ": debug check: page table read").c_str());
+  if (qo[size_t(prompts)] != B ||
+      cascade_fingerprint(qo.data(), ip0.data(), l0.data(), plan->page_size, ip1.data(),
+                          l1.data(), plan->page_size_suffix, prompts, plan->num_qo_heads,
+                          plan->num_kv_heads, plan->head_dim, plan->num_ctas) != plan->fingerprint)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": debug check: qo_indptr / kv_indptr / last_page_len "
+                                          "on the device differ from the plan's host copies");
+  const int32_t* tabs[2] = {kv_indices0, kv_indices1};
+  const std::vector<int32_t>* ips[2] = {&ip0, &ip1};
+  const int64_t lim[2] = {num_pages0, num_pages1};
+  for (int t = 0; t < 2; ++t) {
+    const std::vector<int32_t>& ip = *ips[t];
+    const int64_t pages = int64_t(ip.back()) - ip.front();
+    if (pages <= 0) continue;
+    std::vector<int32_t> idx;
+    e = read(idx, tabs[t] + ip.front(), pages);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, (f + ": debug check: kv_indices read").c_str());
+    for (int64_t i = 0; i < pages; ++i)
+      if (idx[size_t(i)] < 0 || idx[size_t(i)] >= lim[t]) {
+        char buf[200];
+        std::snprintf(buf, sizeof buf,
+                      ": debug check: %s kv_indices[%lld] = %d is outside [0, num_pages = %lld)",
+                      t == 0 ? "prefix" : "suffix", (long long)(ip.front() + i), idx[size_t(i)],
+                      (long long)lim[t]);
+        return fail(ATTN_ERR_INVALID_ARG, f + buf);
+      }
+  }
+  return ATTN_OK;
+}
+
+// Copies a plan's tables from the pinned staging area into the device
+// workspace (after the shared checks); dev_ws NULL = host-only planning.
+attn_status_t upload_plan(const attn_plan_t* plan, const void* pinned_host_ws, void* dev_ws,
+                          size_t dev_bytes, void* stream, const char* fn) {
+  if (!dev_ws) return ATTN_OK;
+  const std::string f(fn);
+  if (size_t(plan->dev_bytes_needed) > dev_bytes)
+    return fail(ATTN_ERR_WORKSPACE_TOO_SMALL, f + ": device workspace too small");
+  if (reinterpret_cast<uintptr_t>(dev_ws) % 256 != 0)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": dev_ws must be 256-byte aligned");
+  cudaError_t e = cudaMemcpyAsync(dev_ws, pinned_host_ws, size_t(plan->table_bytes),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, (f + ": table upload").c_str());
+  return ATTN_OK;
+}
+
 }  // namespace
 
 namespace attn {
@@ -356,12 +430,15 @@ attn_status_t attn_workspace_size(int32_t max_batch, int32_t max_total_qo,
 
 attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_ctas) {
   if (!num_ctas) return fail(ATTN_ERR_INVALID_ARG, "attn_default_num_ctas: null output");
-  if (mode != ATTN_MODE_DECODE && mode != ATTN_MODE_APPEND)
+  if (mode != ATTN_MODE_DECODE && mode != ATTN_MODE_APPEND && mode != ATTN_MODE_CASCADE)
     return fail(ATTN_ERR_INVALID_ARG, "attn_default_num_ctas: unknown mode");
   int sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "attn_default_num_ctas");
-  const int per_sm = mode == ATTN_MODE_DECODE ? decode_ctas_per_sm() : append_ctas_per_sm();
+  // cascade: the few-row kernel, one CTA per SM
+  const int per_sm = mode == ATTN_MODE_DECODE   ? decode_ctas_per_sm()
+                     : mode == ATTN_MODE_APPEND ? append_ctas_per_sm()
+                                                : 1;
   *num_ctas = sms * per_sm;
   return ATTN_OK;
 }
@@ -388,14 +465,112 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                  (long long)p.total_weight, (long long)p.max_cta_weight,
                  double(p.total_weight) / p.num_ctas);
   }
-  if (!dev_ws) return ATTN_OK;  // host-only planning
-  if (size_t(plan_out->dev_bytes_needed) > dev_bytes)
-    return fail(ATTN_ERR_WORKSPACE_TOO_SMALL, "attn_plan: device workspace too small");
-  if (reinterpret_cast<uintptr_t>(dev_ws) % 256 != 0)
-    return fail(ATTN_ERR_INVALID_ARG, "attn_plan: dev_ws must be 256-byte aligned");
-  cudaError_t e = cudaMemcpyAsync(dev_ws, pinned_host_ws, size_t(plan_out->table_bytes),
-                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "attn_plan: table upload");
+  return upload_plan(plan_out, pinned_host_ws, dev_ws, dev_bytes, stream, "attn_plan");
+}
+
+attn_status_t attn_cascade_workspace_size(int32_t max_prompts, int32_t max_batch,
+                                          int32_t num_qo_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t num_ctas,
+                                          size_t* dev_bytes, size_t* pinned_host_bytes) {
+  if (!dev_bytes || !pinned_host_bytes)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_cascade_workspace_size: null output pointer");
+  if (max_prompts < 1 || max_batch < 0 || num_qo_heads < 1 || num_kv_heads < 1 || num_ctas < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_cascade_workspace_size: sizes must be positive");
+  if (num_qo_heads % num_kv_heads)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_cascade_workspace_size: num_qo_heads must be a "
+                                      "multiple of num_kv_heads");
+  if (head_dim != kHeadDim)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_cascade_workspace_size: only head_dim == 128");
+  // a segment per (prompt, kv head) and per (generation, kv head); each CTA
+  // boundary cuts at most one segment in two; every unit has a slot
+  const int64_t items = int64_t(max_prompts) * num_kv_heads;
+  const int64_t units = (int64_t(max_prompts) + max_batch) * num_kv_heads + num_ctas;
+  const PlanLayout L = plan_layout(num_ctas, units, items, units, kFewRowMax, head_dim);
+  *dev_bytes = size_t(L.dev_bytes);
+  *pinned_host_bytes = size_t(L.table_bytes);
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan_cascade(const int32_t* qo_indptr_h, const int32_t* kv_indptr_prefix_h,
+                                const int32_t* last_page_len_prefix_h, int32_t page_size_prefix,
+                                const int32_t* kv_indptr_suffix_h,
+                                const int32_t* last_page_len_suffix_h, int32_t page_size_suffix,
+                                int32_t num_prompts, int32_t num_qo_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t num_ctas, void* pinned_host_ws,
+                                size_t pinned_bytes, void* dev_ws, size_t dev_bytes,
+                                void* stream, attn_plan_t* plan_out) {
+  NvtxRange nvtx("attn_plan_cascade");
+  const char* msg = "";
+  attn_status_t s = build_cascade_plan(
+      qo_indptr_h, kv_indptr_prefix_h, last_page_len_prefix_h, page_size_prefix,
+      kv_indptr_suffix_h, last_page_len_suffix_h, page_size_suffix, num_prompts, num_qo_heads,
+      num_kv_heads, head_dim, num_ctas, pinned_host_ws, pinned_bytes, plan_out, &msg);
+  if (s != ATTN_OK) return fail(s, msg);
+  if (log_enabled()) {
+    const attn_plan_t& p = *plan_out;
+    std::fprintf(stderr,
+                 "[attn] plan mode=cascade prompts=%d batch=%d items=%d units=%d rows=%d "
+                 "ctas=%d max_cta_tokens=%lld\n",
+                 p.batch, p.total_qo, p.num_items, p.num_units, p.rows_per_item, p.num_ctas,
+                 (long long)p.max_cta_weight);
+  }
+  return upload_plan(plan_out, pinned_host_ws, dev_ws, dev_bytes, stream, "attn_plan_cascade");
+}
+
+attn_status_t attn_cascade_run(const attn_plan_t* plan, const void* q, const int32_t* qo_indptr,
+                               const void* k_prefix, const void* v_prefix,
+                               int64_t num_pages_prefix, const int32_t* kv_indptr_prefix,
+                               const int32_t* kv_indices_prefix,
+                               const int32_t* last_page_len_prefix, const void* k_suffix,
+                               const void* v_suffix, int64_t num_pages_suffix,
+                               const int32_t* kv_indptr_suffix, const int32_t* kv_indices_suffix,
+                               const int32_t* last_page_len_suffix, int32_t dtype,
+                               float sm_scale, void* o, float* lse, void* dev_ws,
+                               size_t dev_bytes, void* stream) {
+  NvtxRange nvtx("attn_cascade_run");
+  const char* fn = "attn_cascade_run";
+  const std::string f(fn);
+  attn_status_t s = check_plan_common(plan, ATTN_MODE_CASCADE, q, k_prefix, v_prefix,
+                                      num_pages_prefix, ATTN_LAYOUT_HND, kv_indptr_prefix,
+                                      kv_indices_prefix, last_page_len_prefix, dtype, o, dev_ws,
+                                      dev_bytes, fn);
+  if (s != ATTN_OK) return s;
+  if (plan_pages(*plan) > 0 &&
+      (!k_suffix || !v_suffix || !kv_indices_suffix || num_pages_suffix < 1))
+    return fail(ATTN_ERR_INVALID_ARG, f + ": null suffix pool or kv_indices, or an empty pool");
+  if (num_pages_suffix < 0) return fail(ATTN_ERR_INVALID_ARG, f + ": num_pages_suffix < 0");
+  if ((reinterpret_cast<uintptr_t>(k_suffix) | reinterpret_cast<uintptr_t>(v_suffix)) & 15u)
+    return fail(ATTN_ERR_INVALID_ARG, f + ": the suffix pools must be 16-byte aligned");
+  if (plan->batch > 0 && plan->total_qo > 0 &&
+      (!qo_indptr || !kv_indptr_suffix || !last_page_len_suffix))
+    return fail(ATTN_ERR_INVALID_ARG, f + ": null device pointer");
+  if (plan->page_size % 16 != 0 || plan->page_size_suffix % 16 != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, f + ": both page sizes must be multiples of 16 (use a "
+                                          "prefix append, a suffix decode and "
+                                          "attn_merge_states for other page sizes)");
+  if (debug_checks_enabled()) {
+    s = debug_check_cascade(plan, qo_indptr, kv_indptr_prefix, kv_indices_prefix,
+                            last_page_len_prefix, num_pages_prefix, kv_indptr_suffix,
+                            kv_indices_suffix, last_page_len_suffix, num_pages_suffix, stream,
+                            fn);
+    if (s != ATTN_OK) return s;
+  }
+  if (plan->batch == 0 || plan->total_qo == 0) return ATTN_OK;
+  if (plan_pages(*plan) == 0)
+    return run_empty(plan, o, lse, plan->total_qo, dtype, stream, fn);
+  AppendArgs a = append_args(plan, q, qo_indptr, k_prefix, v_prefix, num_pages_prefix,
+                             ATTN_LAYOUT_HND, kv_indptr_prefix, kv_indices_prefix,
+                             last_page_len_prefix, dtype, sm_scale, o, lse, dev_ws);
+  a.cascade = 1;
+  a.page_size2 = plan->page_size_suffix;
+  a.k_pool2 = k_suffix;
+  a.v_pool2 = v_suffix;
+  a.num_pages2 = num_pages_suffix;
+  a.kv_indices2 = kv_indices_suffix;
+  const char* msg = "";
+  cudaError_t e = launch_decode_tc(a, static_cast<cudaStream_t>(stream), &msg);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, msg);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_cascade_run: kernel launch");
   return ATTN_OK;
 }
 

@@ -136,6 +136,8 @@ struct Hand {
 struct DecodeTcParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_k2;  // composable formats: the suffix pool
+  CUtensorMap tm_v2;
   AppendArgs a;
   float scale_log2;
   uint32_t idesc_s;
@@ -153,7 +155,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 struct DGeo {
-  int32_t r, hk, t, slot, split, page_base, ntiles;
+  int32_t r, hk, t, slot, split, page_base, ntiles, pad;
   int64_t qo_start, qo_len, kv_len;
   int64_t tok_begin, tok_end;
 };
@@ -175,13 +177,16 @@ __device__ __forceinline__ DGeo decode_geo(const AppendArgs& a, int ui) {
   g.kv_len = z.x;
   g.qo_start = z.y;
   g.qo_len = DEC ? 1 : z.z;
+  // composable formats: 1 = the unit reads the suffix table (0 in other plans)
+  g.pad = (!DEC && a.cascade) ? z.w : 0;
   int64_t vis = g.kv_len;
   if (!DEC && a.causal) {  // the item's last query row sees the most
     const int64_t last_row = min(int64_t(g.t + 1) * a.q_tile, g.qo_len) - 1;
     vis = min(g.kv_len, max(int64_t(0), g.kv_len - g.qo_len + last_row + 1));
   }
-  g.tok_begin = int64_t(x.w) * a.page_size;
-  g.tok_end = min(int64_t(y.x) * a.page_size, vis);
+  const int64_t P = g.pad ? a.page_size2 : a.page_size;
+  g.tok_begin = int64_t(x.w) * P;
+  g.tok_end = min(int64_t(y.x) * P, vis);
   const int64_t nt = g.tok_end - g.tok_begin;
   g.ntiles = nt > 0 ? int32_t((nt + kTile - 1) / kTile) : 0;
   return g;
@@ -203,6 +208,15 @@ __device__ __forceinline__ QRow qrow(const AppendArgs& a, const DGeo& g, int rho
     q.orow = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * R + rho;
     q.limit = g.kv_len - 1;
     q.pos = g.kv_len - 1;
+  } else if (a.cascade) {
+    // composable formats: rows are the generations of prompt r (token tok =
+    // generation tok); a prefix unit (t < 0) serves every generation, a
+    // suffix unit only its own (t): the other rows see nothing
+    const int tok = rho / a.group, hh = rho - tok * a.group;
+    q.ok = tok < g.qo_len;
+    q.orow = (g.qo_start + tok) * a.num_qo_heads + int64_t(g.hk) * a.group + hh;
+    q.limit = (g.t < 0 || g.t == tok) ? g.kv_len - 1 : -1;
+    q.pos = 0;
   } else {
     const int tok = rho / a.group, hh = rho - tok * a.group;
     const int64_t qi = int64_t(g.t) * a.q_tile + tok;
@@ -618,6 +632,10 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
   if (warp == kWarpLoad && lane == 0) {
     prefetch_tmap(&prm.tm_k);
     prefetch_tmap(&prm.tm_v);
+    if (!DEC && a.cascade) {
+      prefetch_tmap(&prm.tm_k2);
+      prefetch_tmap(&prm.tm_v2);
+    }
   }
   if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -646,12 +664,14 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     } else if (!FP8 && prm.nhd) {
       produce_nhd_box<DEC>(prm, bars, base, lane, err, uses, ok);
     } else {
-      const int P = a.page_size;
+      // composable formats: a unit with pad = 1 reads the suffix table / pool
       auto chunk_row = [&](const DGeo& g, int i) -> int32_t {
         const int64_t kvt = g.tok_begin + int64_t(i) * kTile + int64_t(lane) * kChunk;
         if (kvt >= g.tok_end) return 0;
+        const bool second = g.pad != 0;
+        const int P = second ? a.page_size2 : a.page_size;
         const int64_t pg = kvt / P;
-        const int64_t phys = __ldg(a.kv_indices + g.page_base + pg);
+        const int64_t phys = __ldg((second ? a.kv_indices2 : a.kv_indices) + g.page_base + pg);
         return int32_t((phys * a.num_kv_heads + g.hk) * P + (kvt - pg * P));
       };
       for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
@@ -682,8 +702,11 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
                 mbar_arrive_expect_tx(full, uint32_t(nch) * kChunk * (FP8 ? 128u : 256u));
               __syncwarp();
               if (lane < nch) {
-                const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
-                                         : static_cast<const void*>(&prm.tm_v);
+                const bool second = g.pad != 0;
+                const void* tm = kv == 0 ? (second ? static_cast<const void*>(&prm.tm_k2)
+                                                   : static_cast<const void*>(&prm.tm_k))
+                                         : (second ? static_cast<const void*>(&prm.tm_v2)
+                                                   : static_cast<const void*>(&prm.tm_v));
                 if constexpr (FP8) {
                   tma_load_2d(base + kOffF8 + slot * kF8SlotBytes + uint32_t(lane) * kChunk * 128u,
                               tm, 0, row, full);
@@ -1477,10 +1500,20 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
     *msg = "attn: the tensor-core FP8 decode takes HND pools with page_size % 16 == 0";
     return cudaErrorNotSupported;
   }
+  if (a.cascade && (!a.qo_indptr || prm.gather || prm.nhd || a.page_size2 <= 0 ||
+                    a.page_size2 % kChunk != 0 || a.kv_fp8 || a.rope_cos || a.causal)) {
+    *msg = "attn: composable formats in one launch take HND pools with both page sizes "
+           "multiples of 16";
+    return cudaErrorNotSupported;
+  }
   const int elem = a.kv_fp8 ? kKvElemU8 : (bf16 ? kKvElemBF16 : kKvElemF16);
   if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, elem,
                     prm.gather ? 1u : uint32_t(kChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorNotSupported;  // *msg says why
+  if (a.cascade &&
+      !make_kv_maps(a.k_pool2, a.v_pool2, a.num_pages2, a.num_kv_heads, a.page_size2, elem,
+                    uint32_t(kChunk), false, &prm.tm_k2, &prm.tm_v2, msg))
+    return cudaErrorNotSupported;
   int sms = 0;
   cudaError_t e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;

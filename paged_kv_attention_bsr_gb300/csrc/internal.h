@@ -89,6 +89,25 @@ uint64_t plan_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr,
                           int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t causal, int32_t num_ctas);
 
+// Composable-format (cascade) plan over a prefix table (prompts rows, page
+// size P0) and a suffix table (qo_indptr[prompts] rows, page size P1); unit
+// t = -1 reads the prefix row of prompt r, t = j >= 0 the suffix row of its
+// generation j (unit.pad = 0 prefix / 1 suffix). A segment weighs its
+// tokens + kCascadeAlpha.
+constexpr int64_t kCascadeAlpha = 16;
+attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_indptr0,
+                                 const int32_t* last0, int32_t page_size0,
+                                 const int32_t* kv_indptr1, const int32_t* last1,
+                                 int32_t page_size1, int32_t prompts, int32_t num_qo_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t num_ctas,
+                                 void* host_tables, size_t host_bytes, attn_plan_t* plan,
+                                 const char** msg);
+uint64_t cascade_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr0,
+                             const int32_t* last0, int32_t page_size0, const int32_t* kv_indptr1,
+                             const int32_t* last1, int32_t page_size1, int32_t prompts,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t num_ctas);
+
 // Builds the plan tables into `host_tables` (table_bytes of them).
 // Returns ATTN_OK or an error with a message in *msg.
 attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
@@ -166,6 +185,15 @@ struct AppendArgs {
   int32_t kv_fp8;
   const float* k_scale;
   const float* v_scale;
+  // composable formats in one launch (few-row kernel, HND, page sizes % 16
+  // == 0): units with pad = 1 read the second table (suffix pool, page size
+  // page_size2); query rows are the generations of a prompt
+  int32_t cascade;
+  int32_t page_size2;
+  const void* k_pool2;
+  const void* v_pool2;
+  int64_t num_pages2;
+  const int32_t* kv_indices2;
 };
 // qo_indptr == NULL runs the kernel in decode mode (one query row per
 // request; q is [batch, Hq, D]). Returns cudaErrorNotSupported for shapes the

@@ -470,4 +470,260 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   return ATTN_OK;
 }
 
+uint64_t cascade_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr0,
+                             const int32_t* last0, int32_t page_size0, const int32_t* kv_indptr1,
+                             const int32_t* last1, int32_t page_size1, int32_t prompts,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t num_ctas) {
+  uint64_t h = plan_fingerprint(qo_indptr, kv_indptr0, last0, prompts, page_size0, num_qo_heads,
+                                num_kv_heads, head_dim, 0, num_ctas);
+  const int32_t B = prompts > 0 ? qo_indptr[prompts] : 0;
+  h = fnv1a(h, kv_indptr1, 4 * (size_t(B) + 1));
+  if (B) h = fnv1a(h, last1, 4 * size_t(B));
+  return fnv1a(h, &page_size1, sizeof page_size1);
+}
+
+// Composable-format (cascade) plan: items are (prompt p, kv head hk); an
+// item's segments are the prompt's shared prefix row (prefix table, page
+// size P0) and then one suffix row per generation of the prompt (suffix
+// table, page size P1). Weights are in tokens: a page weighs its page size,
+// a segment adds kCascadeAlpha. The weights are laid end to end and CTA c
+// takes the positions [floor(c W / C), floor((c+1) W / C)); a page belongs
+// to the CTA that owns its first position, and the pages of a segment owned
+// by one CTA form a unit; a segment without pages keeps one zero-page unit,
+// owned by the CTA of its overhead position. Every item with generations is
+// merged (its prefix state and its generations' suffix states), so all of
+// its units write partial slots, numbered in (item, segment, page) order.
+attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_indptr0,
+                                 const int32_t* last0, int32_t page_size0,
+                                 const int32_t* kv_indptr1, const int32_t* last1,
+                                 int32_t page_size1, int32_t prompts, int32_t num_qo_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t num_ctas,
+                                 void* host_tables, size_t host_bytes, attn_plan_t* plan,
+                                 const char** msg) {
+  *msg = "";
+  if (!qo_indptr || !kv_indptr0 || !kv_indptr1 || !plan || !host_tables ||
+      (prompts > 0 && !last0)) {
+    *msg = "attn_plan_cascade: null pointer argument";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  if (prompts < 0 || page_size0 < 1 || page_size1 < 1 || num_qo_heads < 1 ||
+      num_kv_heads < 1 || num_ctas < 1) {
+    *msg = "attn_plan_cascade: sizes, page sizes, head counts and num_ctas must be positive";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  if (num_qo_heads % num_kv_heads != 0) {
+    *msg = "attn_plan_cascade: num_qo_heads must be a multiple of num_kv_heads";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  if (head_dim != kHeadDim) {
+    *msg = "attn_plan_cascade: only head_dim == 128 is implemented";
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  if (qo_indptr[0] != 0) {
+    *msg = "attn_plan_cascade: qo_indptr must start at 0";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  const int32_t group = num_qo_heads / num_kv_heads;
+  const int32_t B = qo_indptr[prompts];
+  if (B > 0 && !last1) {
+    *msg = "attn_plan_cascade: null pointer argument";
+    return ATTN_ERR_INVALID_ARG;
+  }
+  int64_t max_n = 0, max_kv = 0, pages = 0;
+  auto seg_len = [](const int32_t* indptr, const int32_t* last, int32_t P, int32_t r,
+                    int64_t* n_pages, int64_t* kv_len) -> bool {
+    const int64_t n = int64_t(indptr[r + 1]) - indptr[r];
+    if (n < 0) return false;
+    if (n > 0 && (last[r] < 1 || last[r] > P)) return false;
+    *n_pages = n;
+    *kv_len = n > 0 ? (n - 1) * P + last[r] : 0;
+    return *kv_len <= INT32_MAX;
+  };
+  for (int32_t p = 0; p < prompts; ++p) {
+    const int64_t n = int64_t(qo_indptr[p + 1]) - qo_indptr[p];
+    if (n < 0) {
+      *msg = "attn_plan_cascade: qo_indptr must be non-decreasing";
+      return ATTN_ERR_INVALID_ARG;
+    }
+    max_n = std::max(max_n, n);
+  }
+  const int32_t rows = few_row_rows(group, int32_t(std::max<int64_t>(max_n, 1)));
+  if (rows == 0) {
+    *msg = "attn_plan_cascade: num_qo_heads / num_kv_heads x the generations of a prompt must "
+           "be at most 16";
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  // segments in order: (item, segment) with their table row geometry
+  struct Seg {
+    int32_t item, r, kind, j;  // kind 0: prefix row r = p; 1: suffix row r, generation j
+    int64_t n, kv_len;
+    int32_t page_base;
+  };
+  std::vector<Seg> segs;
+  std::vector<int4> item_of;  // (p, hk, qo_start, n_p)
+  segs.reserve(size_t(B + prompts) * num_kv_heads);
+  int64_t W = 0;
+  for (int32_t p = 0; p < prompts; ++p) {
+    const int32_t n_p = qo_indptr[p + 1] - qo_indptr[p];
+    int64_t n0, len0;
+    if (!seg_len(kv_indptr0, last0, page_size0, p, &n0, &len0)) {
+      *msg = "attn_plan_cascade: bad prefix table (kv_indptr decreasing or last_page_len out "
+             "of [1, page_size])";
+      return ATTN_ERR_INVALID_ARG;
+    }
+    if (n_p == 0) continue;  // no generations, no rows
+    max_kv = std::max(max_kv, len0);
+    for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
+      const int32_t item = int32_t(item_of.size());
+      item_of.push_back(make_int4(p, hk, qo_indptr[p], n_p));
+      segs.push_back({item, p, 0, -1, n0, len0, kv_indptr0[p]});
+      W += n0 * page_size0 + kCascadeAlpha;
+      pages += n0;
+      for (int32_t j = 0; j < n_p; ++j) {
+        const int32_t b = qo_indptr[p] + j;
+        int64_t n1, len1;
+        if (!seg_len(kv_indptr1, last1, page_size1, b, &n1, &len1)) {
+          *msg = "attn_plan_cascade: bad suffix table (kv_indptr decreasing or last_page_len "
+                 "out of [1, page_size])";
+          return ATTN_ERR_INVALID_ARG;
+        }
+        max_kv = std::max(max_kv, len1);
+        segs.push_back({item, b, 1, j, n1, len1, kv_indptr1[b]});
+        W += n1 * page_size1 + kCascadeAlpha;
+        pages += n1;
+      }
+    }
+  }
+  const int64_t C = num_ctas;
+  auto bound = [&](int64_t c) -> int64_t {
+    // floor(c W / C) without overflow for W < 2^62 / C
+    return (c * (W / C)) + (c * (W % C)) / C;
+  };
+  // units in CTA order: the cut walks the segments in order, so the CTA
+  // index never decreases
+  std::vector<Unit> units;
+  std::vector<int32_t> unit_cta, unit_item;
+  units.reserve(segs.size() + size_t(C));
+  int64_t base = 0;
+  int64_t c = 0;
+  auto owner = [&](int64_t pos) {
+    while (c + 1 < C && bound(c + 1) <= pos) ++c;
+    return c;
+  };
+  for (const Seg& sg : segs) {
+    const int4 it = item_of[size_t(sg.item)];
+    const int64_t P = sg.kind == 0 ? page_size0 : page_size1;
+    auto emit = [&](int64_t p0, int64_t p1, int64_t cta) {
+      Unit u;
+      u.r = it.x;
+      u.hk = it.y;
+      u.t = sg.j;  // -1: prefix segment; j: generation j's suffix
+      u.p0 = int32_t(p0);
+      u.p1 = int32_t(p1);
+      u.slot = -1;
+      u.split = -1;
+      u.page_base = sg.page_base;
+      u.kv_len = int32_t(sg.kv_len);
+      u.qo_start = it.z;
+      u.qo_len = it.w;
+      u.pad = sg.kind;
+      units.push_back(u);
+      unit_cta.push_back(int32_t(cta));
+      unit_item.push_back(sg.item);
+    };
+    if (sg.n == 0) {
+      emit(0, 0, owner(base));
+    } else {
+      int64_t k0 = 0;
+      int64_t cur = owner(base + kCascadeAlpha);
+      for (int64_t k = 1; k < sg.n; ++k) {
+        const int64_t o = owner(base + kCascadeAlpha + k * P);
+        if (o != cur) {
+          emit(k0, k, cur);
+          k0 = k;
+          cur = o;
+        }
+      }
+      emit(k0, sg.n, cur);
+    }
+    base += sg.n * P + kCascadeAlpha;
+  }
+  // merge tables: every item is merged; slots in unit order within an item
+  const int64_t num_items = int64_t(item_of.size());
+  std::vector<int32_t> merge_indptr(static_cast<size_t>(num_items) + 1, 0),
+      next(static_cast<size_t>(num_items), 0);
+  for (size_t i = 0; i < units.size(); ++i) merge_indptr[size_t(unit_item[i]) + 1]++;
+  for (int64_t i = 0; i < num_items; ++i) merge_indptr[size_t(i) + 1] += merge_indptr[size_t(i)];
+  // units are generated in (item, segment, page) order, so slot = position
+  for (size_t i = 0; i < units.size(); ++i) {
+    const int32_t it = unit_item[i];
+    units[i].split = it;
+    units[i].slot = merge_indptr[size_t(it)] + next[size_t(it)]++;
+  }
+  std::vector<int4> merge_items(static_cast<size_t>(num_items));
+  for (int64_t i = 0; i < num_items; ++i) {
+    const int4 it = item_of[size_t(i)];
+    merge_items[size_t(i)] = make_int4(it.x, it.y, 0, merge_indptr[size_t(i) + 1] -
+                                                         merge_indptr[size_t(i)]);
+  }
+  std::vector<int32_t> work_indptr(size_t(C) + 1, 0);
+  for (size_t i = 0; i < units.size(); ++i) work_indptr[size_t(unit_cta[i]) + 1]++;
+  for (int64_t i = 0; i < C; ++i) work_indptr[size_t(i) + 1] += work_indptr[size_t(i)];
+  int64_t max_load = 0;
+  for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, bound(i + 1) - bound(i));
+
+  const int64_t S = num_items;
+  const int64_t slots = int64_t(units.size());
+  const PlanLayout L = plan_layout(num_ctas, int64_t(units.size()), S, slots, rows, head_dim);
+  if (size_t(L.table_bytes) > host_bytes) {
+    *msg = "attn_plan_cascade: pinned host workspace too small for the plan tables";
+    return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  }
+  char* hb = static_cast<char*>(host_tables);
+  std::memset(hb, 0, size_t(L.table_bytes));
+  std::memcpy(hb + L.off_work_indptr, work_indptr.data(), 4 * work_indptr.size());
+  if (!units.empty()) std::memcpy(hb + L.off_units, units.data(), sizeof(Unit) * units.size());
+  std::memcpy(hb + L.off_merge_indptr, merge_indptr.data(), 4 * merge_indptr.size());
+  if (S) std::memcpy(hb + L.off_merge_items, merge_items.data(), 16 * size_t(S));
+
+  attn_plan_t pl;
+  std::memset(&pl, 0, sizeof pl);
+  pl.mode = ATTN_MODE_CASCADE;
+  pl.batch = prompts;
+  pl.page_size = page_size0;
+  pl.page_size_suffix = page_size1;
+  pl.num_qo_heads = num_qo_heads;
+  pl.num_kv_heads = num_kv_heads;
+  pl.head_dim = head_dim;
+  pl.causal = 0;
+  pl.num_ctas = num_ctas;
+  pl.q_tile = int32_t(max_n);
+  pl.rows_per_item = rows;
+  pl.num_items = int32_t(num_items);
+  pl.num_units = int32_t(units.size());
+  pl.num_split_items = int32_t(S);
+  pl.num_slots = int32_t(slots);
+  pl.total_qo = B;
+  pl.max_qo_len = int32_t(max_n);
+  pl.total_weight = pages + num_items;
+  pl.max_cta_weight = max_load;
+  pl.off_work_indptr = L.off_work_indptr;
+  pl.off_units = L.off_units;
+  pl.off_merge_indptr = L.off_merge_indptr;
+  pl.off_merge_items = L.off_merge_items;
+  pl.off_counters = L.off_counters;
+  pl.off_partial_o = L.off_partial_o;
+  pl.off_partial_lse = L.off_partial_lse;
+  pl.table_bytes = L.table_bytes;
+  pl.dev_bytes_needed = L.dev_bytes;
+  pl.fingerprint = cascade_fingerprint(qo_indptr, kv_indptr0, last0, page_size0, kv_indptr1,
+                                       last1, page_size1, prompts, num_qo_heads, num_kv_heads,
+                                       head_dim, num_ctas);
+  pl.max_kv_len = max_kv;
+  pl.min_kv_minus_qo = INT64_MAX;
+  *plan = pl;
+  return ATTN_OK;
+}
+
 }  // namespace attn

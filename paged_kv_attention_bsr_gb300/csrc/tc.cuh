@@ -271,30 +271,39 @@ inline bool encode_kv_maps(const void* k_pool, const void* v_pool, int64_t num_p
 inline bool make_kv_maps(const void* k_pool, const void* v_pool, int64_t num_pages,
                          int32_t num_kv_heads, int32_t page_size, int elem, uint32_t box_rows,
                          bool nhd, CUtensorMap* tm_k, CUtensorMap* tm_v, const char** msg) {
+  // two entries per thread: a composable-format run encodes two pools per call
   struct Key {
     const void *k, *v;
     int64_t pages;
     int32_t heads, page_size, elem;
     uint32_t box_rows;
     int32_t nhd;
+    bool operator==(const Key& o) const {
+      return k == o.k && v == o.v && pages == o.pages && heads == o.heads &&
+             page_size == o.page_size && elem == o.elem && box_rows == o.box_rows && nhd == o.nhd;
+    }
   };
-  thread_local Key last = {nullptr, nullptr, -1, 0, 0, 0, 0, 0};
-  thread_local CUtensorMap last_k, last_v;
+  struct Entry {
+    Key key;
+    CUtensorMap k, v;
+  };
+  thread_local Entry cache[2] = {{{nullptr, nullptr, -1, 0, 0, 0, 0, 0}, {}, {}},
+                                 {{nullptr, nullptr, -1, 0, 0, 0, 0, 0}, {}, {}}};
+  thread_local int oldest = 0;
   const Key key = {k_pool, v_pool, num_pages, num_kv_heads, page_size, elem, box_rows,
                    nhd ? 1 : 0};
-  if (key.k == last.k && key.v == last.v && key.pages == last.pages && key.heads == last.heads &&
-      key.page_size == last.page_size && key.elem == last.elem && key.box_rows == last.box_rows &&
-      key.nhd == last.nhd) {
-    *tm_k = last_k;
-    *tm_v = last_v;
-    return true;
-  }
+  for (int i = 0; i < 2; ++i)
+    if (cache[i].key == key) {
+      *tm_k = cache[i].k;
+      *tm_v = cache[i].v;
+      oldest = 1 - i;
+      return true;
+    }
   if (!encode_kv_maps(k_pool, v_pool, num_pages, num_kv_heads, page_size, elem, box_rows, nhd,
                       tm_k, tm_v, msg))
     return false;
-  last = key;
-  last_k = *tm_k;
-  last_v = *tm_v;
+  cache[oldest] = {key, *tm_k, *tm_v};
+  oldest = 1 - oldest;
   return true;
 }
 

@@ -349,13 +349,40 @@ def sub_batch(w: Workload, rows, as_decode: bool = False) -> Workload:
                     w.head_dim, w.sm_scale, q, cache, qo_indptr=qo_indptr, causal=w.causal)
 
 
+def cascade_workload(name: str, gens, prefix_lens, suffix_lens, prefix_page: int,
+                     suffix_page: int, num_qo_heads: int, num_kv_heads: int,
+                     dtype: torch.dtype, seed: int, slack_pages: int = 7) -> Workload:
+    """A composable-format batch with ragged shapes: prompt p has gens[p]
+    generations (0 allowed), a prefix of prefix_lens[p] tokens (pool at
+    prefix_page) and generation b a suffix of suffix_lens[b] tokens (pool at
+    suffix_page); both pools shuffled, with slack_pages unused pages each.
+    Same field layout as shared_prefix_decode."""
+    gens = np.asarray(gens, np.int64)
+    prompts, B = len(gens), int(gens.sum())
+    prefix_lens = np.asarray(prefix_lens, np.int64)
+    suffix_lens = np.asarray(suffix_lens, np.int64)
+    pages0 = int(((prefix_lens + prefix_page - 1) // prefix_page).sum()) + slack_pages
+    pages1 = int(((suffix_lens + suffix_page - 1) // suffix_page).sum()) + slack_pages
+    prefix = make_cache(prefix_lens, prefix_page, pages0, num_kv_heads, dtype, seed + 1000)
+    suffix = make_cache(suffix_lens, suffix_page, pages1, num_kv_heads, dtype, seed)
+    q = normal_values((B, num_qo_heads, HEAD_DIM), dtype, seed * 4 + 3)
+    qo_indptr = np.concatenate([[0], np.cumsum(gens)]).astype(np.int32)
+    return Workload(name, "composable", dtype, num_qo_heads, num_kv_heads, HEAD_DIM,
+                    1.0 / math.sqrt(HEAD_DIM), q, suffix,
+                    extra={"prefix": prefix, "prefix_qo_indptr": qo_indptr, "n": None,
+                           "prompts": prompts})
+
+
 def flat_layout_of_composable(w: Workload, page_size: int = 16) -> BSRCache:
     """The same logical KV as a shared-prefix workload, in one pool with one page
     size: each generation's table lists its prompt's prefix pages (shared by
-    the n generations) followed by its own suffix pages."""
+    its generations) followed by its own suffix pages. A prefix followed by a
+    non-empty suffix must fill whole small pages (its length a multiple of
+    page_size)."""
     prefix: BSRCache = w.extra["prefix"]
     suffix = w.cache
-    n, prompts = w.extra["n"], w.extra["prompts"]
+    qo_indptr = w.extra["prefix_qo_indptr"]
+    prompts = w.extra["prompts"]
     Hk, D = suffix.num_kv_heads, suffix.head_dim
     if suffix.page_size != page_size or prefix.page_size % page_size:
         raise ValueError("flat layout needs the suffix page size to divide the prefix's")
@@ -374,15 +401,23 @@ def flat_layout_of_composable(w: Workload, page_size: int = 16) -> BSRCache:
     lens = []
     for p in range(prompts):
         big = prefix.kv_indices[prefix.kv_indptr[p]:prefix.kv_indptr[p + 1]]
+        len0 = int(prefix.kv_lens[p])
         small = (big[:, None].astype(np.int64) * ratio + np.arange(ratio)[None, :]).reshape(-1)
-        for j in range(n):
-            r = p * n + j
+        small = small[:(len0 + page_size - 1) // page_size]
+        for r in range(int(qo_indptr[p]), int(qo_indptr[p + 1])):
             own = suffix.kv_indices[suffix.kv_indptr[r]:suffix.kv_indptr[r + 1]] + base
+            if len(own) and len0 % page_size:
+                raise ValueError("a prefix followed by a suffix must fill whole small pages")
             indices.extend(small.tolist())
             indices.extend(own.tolist())
             indptr.append(len(indices))
-            last.append(int(suffix.last_page_len[r]))
-            lens.append(int(prefix.kv_lens[p] + suffix.kv_lens[r]))
+            if len(own):
+                last.append(int(suffix.last_page_len[r]))
+            elif len(small):
+                last.append(len0 - page_size * (len(small) - 1))
+            else:
+                last.append(0)
+            lens.append(len0 + int(suffix.kv_lens[r]))
     return BSRCache(page_size, Hk, D, k_pool, v_pool, np.array(indptr, np.int32),
                     np.array(indices, np.int32), np.array(last, np.int32),
                     np.array(lens, np.int64))

@@ -264,3 +264,126 @@ def test_plan_mixed_prefill_and_decode_batch():
             pos.extend(at)
         assert holders >= ctas // 2
         assert 0.3 <= float(np.mean(pos)) <= 0.7
+
+
+def _random_cascade(rng):
+    prompts = int(rng.integers(0, 12))
+    Hk = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8, 16]))
+    max_n = 16 // g
+    n = rng.integers(0, max_n + 1, size=prompts)
+    qo = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    B = int(qo[-1])
+    P0 = int(rng.choice([16, 64, 128]))
+    P1 = int(rng.choice([16, 32]))
+
+    def table(lens, P):
+        pages = (lens + P - 1) // P
+        ip = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+        last = np.where(pages > 0, lens - P * (pages - 1), 0).astype(np.int32)
+        return ip, last
+
+    pre_lens = rng.integers(0, 9000, size=prompts)
+    if prompts and rng.random() < 0.3:
+        pre_lens[rng.integers(0, prompts)] = 0
+    suf_lens = rng.integers(0, 1500, size=B)
+    if B and rng.random() < 0.3:
+        suf_lens[rng.integers(0, B)] = 0
+    ip0, l0 = table(pre_lens, P0)
+    ip1, l1 = table(suf_lens, P1)
+    ctas = int(rng.choice([1, 3, 152, 304, 3000]))
+    return qo, ip0, l0, P0, ip1, l1, P1, Hk * g, Hk, ctas
+
+
+def _lib_cascade(qo, ip0, l0, P0, ip1, l1, P1, Hq, Hk, ctas):
+    prompts = len(qo) - 1
+    _, host = C.cascade_workspace_size(max(prompts, 1), int(qo[-1]), Hq, Hk, 128, ctas)
+    buf = np.zeros(host, np.uint8)
+    p = C.plan_cascade(qo, ip0, l0, P0, ip1, l1, P1, Hq, Hk, 128, ctas, buf)
+    return p, _tables(p, buf)
+
+
+def test_cascade_plan_bit_exact_vs_reference():
+    rng = np.random.default_rng(20260011)
+    for _ in range(80):
+        case = _random_cascade(rng)
+        qo, ip0, l0, P0, ip1, l1, P1, Hq, Hk, ctas = case
+        p, t = _lib_cascade(*case)
+        ref = plan_ref.make_cascade_plan(qo.tolist(), ip0.tolist(), l0.tolist(), P0,
+                                         ip1.tolist(), l1.tolist(), P1, Hq, Hk, ctas)
+        assert p.mode == C.MODE_CASCADE and p.page_size == P0 and p.page_size_suffix == P1
+        assert t["work_indptr"] == ref.work_indptr
+        u = t["units"]
+        cols = (ref.unit_r, ref.unit_hk, ref.unit_t, ref.unit_p0, ref.unit_p1, ref.unit_slot,
+                ref.unit_split, ref.unit_page_base, ref.unit_kv_len, ref.unit_qo_start,
+                ref.unit_qo_len, ref.unit_kind)
+        for k, col in enumerate(cols):
+            assert u[:, k].tolist() == col, k
+        assert t["merge_indptr"] == ref.merge_indptr
+        mi = t["merge_items"]
+        assert mi[:, 0].tolist() == ref.merge_r
+        assert mi[:, 1].tolist() == ref.merge_hk
+        assert mi[:, 3].tolist() == ref.merge_count
+        assert p.total_weight == ref.total_weight
+        assert p.num_items == ref.num_items == p.num_split_items
+        assert p.q_tile == ref.q_tile
+        assert p.rows_per_item == ref.rows_per_item
+        assert p.num_slots == p.num_units == len(ref.unit_r)
+
+
+def test_cascade_plan_covers_every_page_once_and_balances():
+    rng = np.random.default_rng(20260012)
+    for _ in range(40):
+        case = _random_cascade(rng)
+        qo, ip0, l0, P0, ip1, l1, P1, Hq, Hk, ctas = case
+        p, t = _lib_cascade(*case)
+        u = t["units"]
+        prompts = len(qo) - 1
+        # every page of every segment exactly once, in one unit per CTA visit
+        seen = {}
+        for row in u:
+            r, hk, tt, p0, p1 = (int(x) for x in row[:5])
+            key = (r, hk, tt)
+            seen.setdefault(key, []).append((p0, p1))
+        for pp in range(prompts):
+            n_p = int(qo[pp + 1] - qo[pp])
+            if n_p == 0:
+                assert not any(k[0] == pp for k in seen)
+                continue
+            for hk in range(Hk):
+                for tt in range(-1, n_p):
+                    ip = ip0 if tt < 0 else ip1
+                    row_i = pp if tt < 0 else int(qo[pp]) + tt
+                    n = int(ip[row_i + 1] - ip[row_i])
+                    spans = sorted(seen[(pp, hk, tt)])
+                    if n == 0:
+                        assert spans == [(0, 0)]
+                        continue
+                    assert spans[0][0] == 0 and spans[-1][1] == n
+                    for a, b in zip(spans, spans[1:]):
+                        assert a[1] == b[0]
+        # per-CTA token load within one page (+ overhead) of the ideal share
+        w = np.zeros(ctas)
+        wi = t["work_indptr"]
+        for c in range(ctas):
+            for row in u[wi[c]:wi[c + 1]]:
+                P = P0 if row[11] == 0 else P1
+                w[c] += (row[4] - row[3]) * P
+        total = w.sum()
+        assert w.max() <= total / ctas + max(P0, P1) + 16 * (len(u) + 1)
+
+
+def test_cascade_plan_rejects_bad_input():
+    qo = np.array([0, 2], np.int32)
+    ip0, l0 = np.array([0, 4], np.int32), np.array([16], np.int32)
+    ip1, l1 = np.array([0, 1, 2], np.int32), np.array([3, 17], np.int32)  # 17 > P1
+    buf = np.zeros(1 << 20, np.uint8)
+    with pytest.raises(C.AttnError) as e:
+        C.plan_cascade(qo, ip0, l0, 16, ip1, l1, 16, 8, 2, 128, 4, buf)
+    assert e.value.status == 1
+    # 8 heads per kv head x 4 generations = 32 rows > 16
+    qo4 = np.array([0, 4], np.int32)
+    ip1b, l1b = np.array([0, 1, 2, 3, 4], np.int32), np.full(4, 5, np.int32)
+    with pytest.raises(C.AttnError) as e:
+        C.plan_cascade(qo4, ip0, l0, 16, ip1b, l1b, 16, 16, 2, 128, 4, buf)
+    assert e.value.status == 2
