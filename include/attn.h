@@ -358,10 +358,13 @@ attn_status_t attn_merge_states(const void* o_a, const float* lse_a,
  * its tokens (pages x page size) + 16; the weights are laid end to end and
  * CTA c takes the positions [floor(c W / C), floor((c+1) W / C)), a page
  * going to the CTA that owns its first position (pages of one segment on one
- * CTA form a unit; a segment without pages keeps one empty unit). Every item
- * with generations is merged inside the run kernel: each unit writes a
- * partial state (the prefix unit for all n_p rows, a suffix unit for its
- * generation's row) and the last unit to finish combines them.
+ * CTA form a unit; segments without pages add none, and an item without any
+ * page keeps one empty unit). The units of one item on one CTA run as a
+ * chain that carries one online-softmax state per row (the prefix for all
+ * n_p generations, a suffix only for its own generation's rows), so an item
+ * on one CTA needs no merge; an item cut across CTAs writes one partial
+ * state per chain and the last chain to finish merges them by log-sum-exp.
+ * Within a CTA the chains of cut items run first.
  *   qo_indptr_h             : host int32[num_prompts+1], generations per
  *                             prompt, starting at 0 (batch = its last entry)
  *   kv_indptr_prefix_h,

@@ -27,6 +27,8 @@ pseudo-code; the exact cut below is the reading used throughout this project:
              continues on the next CTA
   slots      items with >= 2 units are split; their units get partial-state
              slots numbered in (item, page) order; merge_indptr lists them.
+  order      decode: within each CTA's list the units of split items come
+             first, the others after them, each group in cut order.
 
   cascade    composable formats in one launch: make_cascade_plan below.
 
@@ -187,6 +189,18 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
     if last_item is not None:
         plan.merge_indptr.append(next_slot)
 
+    if decode:
+        # split-item units first within each CTA (stable)
+        reordered, slot_re = [], []
+        for c in range(C):
+            idx = list(range(plan.work_indptr[c], plan.work_indptr[c + 1]))
+            first = [i for i in idx if slot_of[i] >= 0]
+            rest = [i for i in idx if slot_of[i] < 0]
+            for i in first + rest:
+                reordered.append(flat[i])
+                slot_re.append(slot_of[i])
+        flat, slot_of = reordered, slot_re
+
     for i, u in enumerate(flat):
         plan.unit_r.append(u[1])
         plan.unit_hk.append(u[2])
@@ -228,12 +242,20 @@ def make_cascade_plan(qo_indptr: Sequence[int], kv_indptr_prefix: Sequence[int],
                  end (total W), CTA c owns positions [floor(c W / C),
                  floor((c+1) W / C)); page k of a segment at base b sits at
                  position b + 16 + k P and belongs to the CTA owning it; the
-                 pages of a segment on one CTA form a unit; a segment without
-                 pages is one empty unit, owned by the CTA owning b
-      slots      every unit has one, numbered in unit order; every item is merged
+                 pages of a segment on one CTA form a unit; segments without
+                 pages give no unit, except that an item with no page at all
+                 keeps one empty prefix unit, on the CTA owning its base
+      chains     consecutive units of one item on one CTA; flags: continues
+                 the previous unit (2), continued by the next (4), OR-ed
+                 into the kind (0 prefix, 1 suffix)
+      slots      items with >= 2 chains are split: one slot per chain, in
+                 chain order
+      order      within a CTA, the units of split items first, each group in
+                 cut order
 
-    Extra fields: unit_kind (0 prefix, 1 suffix), unit_page_base, unit_kv_len,
-    unit_qo_start, unit_qo_len; merge_count per item; rows_per_item.
+    Extra fields: unit_kind (kind | flags), unit_page_base, unit_kv_len,
+    unit_qo_start, unit_qo_len, unit_split; merge_count per split item;
+    rows_per_item.
     """
     import bisect
     prompts = len(qo_indptr) - 1
@@ -260,61 +282,88 @@ def make_cascade_plan(qo_indptr: Sequence[int], kv_indptr_prefix: Sequence[int],
                 b = qo_indptr[p] + j
                 n, kv = length(kv_indptr_suffix, last_suffix, page_size_suffix, b)
                 segs.append((it, p, hk, j, 1, n, kv, kv_indptr_suffix[b], page_size_suffix))
-    W = sum(s[5] * s[8] + CASCADE_ALPHA for s in segs)
+    item_pages = [0] * len(items)
+    for sg in segs:
+        item_pages[sg[0]] += sg[5]
+    W = sum(s_[5] * s_[8] + CASCADE_ALPHA for s_ in segs)
     bounds = [(c * W) // C for c in range(C)]
 
     def owner(pos):  # the last CTA whose range starts at or before pos
         return bisect.bisect_right(bounds, pos) - 1
 
-    per_cta = [[] for _ in range(C)]
+    gen = []  # units in cut order, with their CTA
     base = 0
     for (it, p, hk, t, kind, n, kv, pb, P) in segs:
         rec = dict(item=it, r=p, hk=hk, t=t, kind=kind, kv_len=kv, page_base=pb,
                    qo_start=qo_indptr[p], qo_len=qo_indptr[p + 1] - qo_indptr[p])
         if n == 0:
-            per_cta[owner(base)].append(dict(rec, p0=0, p1=0))
+            if item_pages[it] == 0 and kind == 0:
+                gen.append(dict(rec, p0=0, p1=0, cta=owner(base)))
         else:
             owners = [owner(base + CASCADE_ALPHA + k * P) for k in range(n)]
             k0 = 0
             for k in range(1, n + 1):
                 if k == n or owners[k] != owners[k0]:
-                    per_cta[owners[k0]].append(dict(rec, p0=k0, p1=k))
+                    gen.append(dict(rec, p0=k0, p1=k, cta=owners[k0]))
                     k0 = k
         base += n * P + CASCADE_ALPHA
 
+    # chains and their slots
+    chain = []
+    for i, u in enumerate(gen):
+        same = i > 0 and gen[i - 1]["item"] == u["item"] and gen[i - 1]["cta"] == u["cta"]
+        chain.append(chain[-1] if same else (chain[-1] + 1 if chain else 0))
+    chains_of_item = {}
+    for i, u in enumerate(gen):
+        lst = chains_of_item.setdefault(u["item"], [])
+        if chain[i] not in lst:
+            lst.append(chain[i])
     plan = Plan(work_indptr=[0] * (C + 1), num_items=len(items), q_tile=max_n)
-    flat = []
-    for c in range(C):
-        plan.work_indptr[c + 1] = plan.work_indptr[c] + len(per_cta[c])
-        flat.extend(per_cta[c])
-    count = [0] * len(items)
-    for u in flat:
-        count[u["item"]] += 1
     plan.merge_indptr = [0]
+    plan.merge_count = []
+    split_of = {}
     for k in range(len(items)):
-        plan.merge_indptr.append(plan.merge_indptr[-1] + count[k])
+        lst = chains_of_item.get(k, [])
+        if len(lst) < 2:
+            continue
+        split_of[k] = len(plan.merge_count)
         plan.merge_r.append(items[k][0])
         plan.merge_hk.append(items[k][1])
         plan.merge_t.append(0)
-    plan.merge_count = count
-    seen = [0] * len(items)
+        plan.merge_count.append(len(lst))
+        plan.merge_indptr.append(plan.merge_indptr[-1] + len(lst))
+    for i, u in enumerate(gen):
+        sid = split_of.get(u["item"], -1)
+        u["split"] = sid
+        u["slot"] = -1 if sid < 0 else \
+            plan.merge_indptr[sid] + chains_of_item[u["item"]].index(chain[i])
+        flags = (2 if i > 0 and chain[i - 1] == chain[i] else 0) | \
+                (4 if i + 1 < len(gen) and chain[i + 1] == chain[i] else 0)
+        u["flags"] = flags
+
+    per_cta = [[] for _ in range(C)]
+    for u in gen:
+        per_cta[u["cta"]].append(u)
+    flat = []
+    for c in range(C):
+        lst = [u for u in per_cta[c] if u["slot"] >= 0] + [u for u in per_cta[c] if u["slot"] < 0]
+        plan.work_indptr[c + 1] = plan.work_indptr[c] + len(lst)
+        flat.extend(lst)
     plan.unit_kind, plan.unit_page_base, plan.unit_kv_len = [], [], []
     plan.unit_qo_start, plan.unit_qo_len, plan.unit_split = [], [], []
     for u in flat:
-        k = u["item"]
         plan.unit_r.append(u["r"])
         plan.unit_hk.append(u["hk"])
         plan.unit_t.append(u["t"])
         plan.unit_p0.append(u["p0"])
         plan.unit_p1.append(u["p1"])
-        plan.unit_slot.append(plan.merge_indptr[k] + seen[k])
-        seen[k] += 1
-        plan.unit_split.append(k)
-        plan.unit_kind.append(u["kind"])
+        plan.unit_slot.append(u["slot"])
+        plan.unit_split.append(u["split"])
+        plan.unit_kind.append(u["kind"] | u["flags"])
         plan.unit_page_base.append(u["page_base"])
         plan.unit_kv_len.append(u["kv_len"])
         plan.unit_qo_start.append(u["qo_start"])
         plan.unit_qo_len.append(u["qo_len"])
-    plan.total_weight = sum(s[5] for s in segs) + len(items)
+    plan.total_weight = sum(s_[5] for s_ in segs) + len(items)
     plan.rows_per_item = few_rows(group, max_n)
     return plan

@@ -155,7 +155,9 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 struct DGeo {
-  int32_t r, hk, t, slot, split, page_base, ntiles, pad;
+  int32_t r, hk, t, slot, split, page_base, ntiles;
+  int32_t pad;           // composable formats: 1 = the unit reads the suffix table
+  bool cprev, cnext;     // chain: continues the previous unit / continued by the next
   int64_t qo_start, qo_len, kv_len;
   int64_t tok_begin, tok_end;
 };
@@ -177,8 +179,11 @@ __device__ __forceinline__ DGeo decode_geo(const AppendArgs& a, int ui) {
   g.kv_len = z.x;
   g.qo_start = z.y;
   g.qo_len = DEC ? 1 : z.z;
-  // composable formats: 1 = the unit reads the suffix table (0 in other plans)
-  g.pad = (!DEC && a.cascade) ? z.w : 0;
+  // composable formats: table bit and chain flags (0 in other plans)
+  const int32_t flags = (!DEC && a.cascade) ? z.w : 0;
+  g.pad = flags & 1;
+  g.cprev = (flags & 2) != 0;
+  g.cnext = (flags & 4) != 0;
   int64_t vis = g.kv_len;
   if (!DEC && a.causal) {  // the item's last query row sees the most
     const int64_t last_row = min(int64_t(g.t + 1) * a.q_tile, g.qo_len) - 1;
@@ -279,9 +284,18 @@ __device__ __forceinline__ void store_out32(float* dst, const float* v, float sc
 // item's units to arrive (atomic count in the workspace) merges every
 // partial state of the item by log-sum-exp and resets the count to 0.
 // One warp: lane = row rho * (32 / R) + dl, dims [4 R dl, 4 R dl + 4 R).
+// The merge is a chain of L2 round trips (about 1.7 us each while the other
+// SMs stream K / V), so the loads are issued in batches. With `land` (shared
+// memory nothing else uses any more, land_cap bytes) every slot's O rows
+// are copied there by cp.async in one round trip, the LSEs loaded
+// meanwhile; rows are stored with their 16-byte pieces XOR-swizzled by the
+// reading lane (R >= 4) so the reads are free of bank conflicts.
 template <bool BF16, int R, bool DEC>
-__device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo& g) {
+__device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo& g,
+                                                 uint8_t* land = nullptr,
+                                                 uint32_t land_cap = 0) {
   constexpr int LP = 32 / R, DL = 4 * R, kS = DL < 8 ? DL : 8;
+  constexpr bool kSw = R >= 4;
   const int lane = threadIdx.x & 31;
   __threadfence();  // every lane's partial stores before the arrival
   __syncwarp();
@@ -295,10 +309,26 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
   const int rho = lane / LP, dl = lane % LP;
   const QRow qr = qrow<DEC, R>(a, g, rho);
   const int s0 = __ldg(a.ws.merge_indptr + g.split), s1 = __ldg(a.ws.merge_indptr + g.split + 1);
-  // The merge is a short chain of L2 round trips at the tail of the launch,
-  // so loads are issued in batches: the first kKeep slots' LSEs at once
-  // (kept in registers), then the O rows kBo slots at a time (8 float4 loads
-  // in flight per lane).
+  const uint32_t obytes = uint32_t(s1 - s0) * R * kHeadDim * 4;
+  const bool staged = land != nullptr && obytes <= land_cap;
+  if (staged) {
+    // row k of the landing area = (slot s0 + k / R, row k % R) (a slot's
+    // rows start every rows_per_item rows); this lane copies piece `lane`
+    // (bytes 16 lane ..) of every row
+    const char* src = reinterpret_cast<const char*>(a.ws.partial_o) + lane * 16;
+    const uint32_t dst = smem_u32(land);
+    const int nrows = (s1 - s0) * R;
+    for (int k = 0; k < nrows; ++k) {
+      const int sl = s0 + k / R, rr = k % R;
+      const uint32_t key = kSw ? uint32_t((rr * LP + (lane * 4) / DL) & 7) : 0u;
+      cp_async16_cg(dst + uint32_t(k) * 512u + ((uint32_t(lane) * 16u) ^ (key << 4)),
+                    src + (int64_t(sl) * a.rows_per_item + rr) * (kHeadDim * 4));
+    }
+    cp_async_commit();
+  }
+  // The first kKeep slots' LSEs at once (kept in registers); without the
+  // landing area, the O rows kBo slots at a time (8 float4 loads in flight
+  // per lane).
   constexpr int kKeep = 16;
   constexpr int kBo = DL >= 32 ? 1 : 32 / DL;
   auto lse_at = [&](int sl) {
@@ -311,11 +341,38 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
 #pragma unroll
   for (int k = 0; k < kKeep; ++k) M = fmaxf(M, keep[k]);
   for (int sl = s0 + kKeep; sl < s1; ++sl) M = fmaxf(M, lse_at(sl));
+  auto lse_of = [&](int sl) {
+    float ls = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k) ls = (sl - s0 == k) ? keep[k] : ls;
+    if (sl - s0 >= kKeep) ls = lse_at(sl);
+    return ls;
+  };
   float acc[DL];
 #pragma unroll
   for (int j = 0; j < DL; ++j) acc[j] = 0.f;
   float L = 0.f;
-  if (M != -INFINITY) {
+  if (staged) {
+    cp_async_wait<0>();
+    __syncwarp();  // every lane's pieces have landed
+    if (M != -INFINITY) {
+      const uint32_t key = kSw ? uint32_t(lane & 7) : 0u;
+      for (int sl = s0; sl < s1; ++sl) {
+        const float f = ex2(lse_of(sl) - M);
+        L += f;
+        const uint8_t* row = land + (uint32_t(sl - s0) * R + rho) * 512u;
+#pragma unroll
+        for (int j = 0; j < DL / 4; ++j) {
+          const float4 x = *reinterpret_cast<const float4*>(
+              row + ((uint32_t(DL * dl + 4 * j) * 4u) ^ (key << 4)));
+          acc[4 * j] += f * x.x;
+          acc[4 * j + 1] += f * x.y;
+          acc[4 * j + 2] += f * x.z;
+          acc[4 * j + 3] += f * x.w;
+        }
+      }
+    }
+  } else if (M != -INFINITY) {
     for (int b0 = s0; b0 < s1; b0 += kBo) {
       float4 x[kBo][DL / 4];
       float f[kBo];
@@ -329,11 +386,7 @@ __device__ __forceinline__ bool merge_split_impl(const AppendArgs& a, const DGeo
               reinterpret_cast<const float4*>(a.ws.partial_o + prow * kHeadDim + DL * dl);
 #pragma unroll
           for (int j = 0; j < DL / 4; ++j) x[u][j] = __ldcg(src + j);
-          float ls = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < kKeep; ++k) ls = (sl - s0 == k) ? keep[k] : ls;
-          if (sl - s0 >= kKeep) ls = lse_at(sl);
-          f[u] = ex2(ls - M);
+          f[u] = ex2(lse_of(sl) - M);
         }
       }
 #pragma unroll
@@ -762,11 +815,12 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     };
     // the units of this CTA that have kv tokens, in order
     int vc = blockIdx.x, ui = vc < a.num_ctas ? __ldg(a.ws.work_indptr + vc) : 0;
+    // (a chain of units shares its first unit's query tile)
     auto next_unit = [&](DGeo& g) -> bool {
       while (vc < a.num_ctas) {
         if (ui < __ldg(a.ws.work_indptr + vc + 1)) {
           g = decode_geo<DEC>(a, ui++);
-          if (g.ntiles > 0) return true;
+          if (g.ntiles > 0 && !g.cprev) return true;
         } else {
           vc += gridDim.x;
           if (vc < a.num_ctas) ui = __ldg(a.ws.work_indptr + vc);
@@ -883,7 +937,11 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
           const DGeo g = decode_geo<DEC>(a, ui);
           if (g.ntiles == 0) continue;
           const int n = g.ntiles;
-          if (!mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL) || !wait_k(jt)) {
+          // a chain (composable formats) keeps its query tile and O buffer:
+          // the query is awaited at its first unit and released after its
+          // last S, O is overwritten only by its first P.V
+          if ((!g.cprev && !mbar_wait(smem_u32(&bars.q_full), ua & 1u, err, ERR_WAIT_FULL)) ||
+              !wait_k(jt)) {
             ok = false;
             break;
           }
@@ -897,7 +955,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
             tc_fence_after();
             issue_s(jt + 1);
           }
-          if (n <= 2) mma_commit(smem_u32(&bars.q_empty));  // last S issued
+          if (n <= 2 && !g.cnext) mma_commit(smem_u32(&bars.q_empty));  // last S issued
           for (int i = 0; i < n && ok; ++i) {
             const uint32_t k = jt + i;
             const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
@@ -906,7 +964,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
               ok = false;
               break;
             }
-            ok = issue_pv(k, (ntt + kChunk - 1) / kChunk, i == 0);
+            ok = issue_pv(k, (ntt + kChunk - 1) / kChunk, i == 0 && !g.cprev);
             if (ok && i + 2 < n) {
               if (!wait_k(k + 2)) {
                 ok = false;
@@ -914,13 +972,14 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
               }
               tc_fence_after();
               issue_s(k + 2);
-              if (i + 3 == n) mma_commit(smem_u32(&bars.q_empty));  // last S issued
+              if (i + 3 == n && !g.cnext) mma_commit(smem_u32(&bars.q_empty));  // last S issued
             }
           }
           if (!ok) break;
+          jt += n;
+          if (g.cnext) continue;  // the chain goes on in the next unit
           mma_commit(smem_u32(&bars.ounit[n_u & 1u]));  // the unit's O is complete
           ++n_u;
-          jt += n;
           ++ua;
         }
       // drain: no MMA may still be writing TMEM when it is freed
@@ -938,6 +997,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     const int c = lane / R;
     uint32_t n_t = 0, n_u = 0;  // tiles and units with tiles so far
     bool ok = true;
+    float m_ref = -INFINITY, l = 0.f;  // row state (carried along a chain)
     for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
       for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
            ++ui) {
@@ -970,7 +1030,10 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
         }
         // kv positions this row sees: [tok_begin, row_end)
         const int64_t row_end = qr.ok ? min(g.tok_end, qr.limit + 1) : g.tok_begin;
-        float m_ref = -INFINITY, l = 0.f;
+        if (!g.cprev) {
+          m_ref = -INFINITY;
+          l = 0.f;
+        }
         for (int i = 0; i < g.ntiles; ++i, ++n_t) {
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[n_t & 1u]),
                                                  (n_t >> 1) & 1u, err, ERR_WAIT_MMA))) {
@@ -1012,7 +1075,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
           bool rescale_o = false;
           if (m_tile > m_ref + 8.f) {
             alpha = ex2(m_ref - m_tile);  // 0 when m_ref = -inf
-            rescale_o = (i > 0) && (m_ref != -INFINITY);
+            rescale_o = (i > 0 || g.cprev) && (m_ref != -INFINITY);
             l *= alpha;
             m_ref = m_tile;
           }
@@ -1088,6 +1151,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
           mbar_arrive(smem_u32(&bars.p_full[n_t & 1u]));
         }
         if (!ok) break;
+        if (g.cnext) continue;  // the chain goes on: keep the row state
         // ---- hand the row state to the epilogue warp; the slot of O[ob]
         // is free once the epilogue has finished unit n_u - 2
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_free[ob]),
@@ -1115,6 +1179,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
            ++ui) {
         const DGeo g = decode_geo<DEC>(a, ui);
         if (g.ntiles == 0) continue;  // written by the softmax warp
+        if (g.cnext) continue;        // not the end of its chain
         const QRow qr = qrow<DEC, R>(a, g, rho);
         const int64_t orow = qr.orow;
         const int64_t prow = int64_t(g.slot) * a.rows_per_item + rho;  // split items
@@ -1180,7 +1245,13 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.o_free[ob]));
         ++n_u;
-        if (g.slot >= 0 && !merge_split_impl<BF16, R, DEC>(a, g)) {
+        // the CTA's last unit: every tile has been consumed, so the K / V
+        // ring is idle and serves as the merge's landing area
+        const bool final_unit = vc + int(gridDim.x) >= a.num_ctas &&
+                                ui + 1 == __ldg(a.ws.work_indptr + vc + 1);
+        if (g.slot >= 0 &&
+            !merge_split_impl<BF16, R, DEC>(a, g, final_unit ? gbase + kOffRing : nullptr,
+                                            final_unit ? 4u * kTileBytes : 0u)) {
           ok = false;
           break;
         }

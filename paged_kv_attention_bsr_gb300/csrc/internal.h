@@ -92,8 +92,9 @@ uint64_t plan_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr,
 // Composable-format (cascade) plan over a prefix table (prompts rows, page
 // size P0) and a suffix table (qo_indptr[prompts] rows, page size P1); unit
 // t = -1 reads the prefix row of prompt r, t = j >= 0 the suffix row of its
-// generation j (unit.pad = 0 prefix / 1 suffix). A segment weighs its
-// tokens + kCascadeAlpha.
+// generation j (unit.pad bit 0: 0 prefix / 1 suffix; bit 1: the unit
+// continues the previous unit's row state, bit 2: the next unit continues
+// this one's). A segment weighs its tokens + kCascadeAlpha.
 constexpr int64_t kCascadeAlpha = 16;
 attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_indptr0,
                                  const int32_t* last0, int32_t page_size0,

@@ -407,7 +407,18 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   for (size_t i = 0; i < num_units; ++i) work_indptr[size_t(gen_cta[i]) + 1]++;
   for (int64_t i = 0; i < C; ++i) work_indptr[i + 1] += work_indptr[i];
   const Unit* unit_table = gen.data();  // decode: the cut emits units in CTA order
-  if (!decode) {
+  if (decode) {
+    // Within a CTA, the units of split items go first (stable): a CTA's
+    // list holds at most two of them, the end of the item shared with the
+    // previous CTA and the start of the one shared with the next, so both
+    // pieces of every shared item run early on their CTAs and the merge
+    // (by whichever finishes second) overlaps later units instead of
+    // trailing the CTA's last one.
+    for (int64_t c = 0; c < C; ++c)
+      std::stable_partition(gen.begin() + work_indptr[size_t(c)],
+                            gen.begin() + work_indptr[size_t(c) + 1],
+                            [](const Unit& u) { return u.slot >= 0; });
+  } else {
     std::vector<Unit>& units = sc.units;
     units.resize(num_units);
     std::vector<int32_t>& at = sc.at;
@@ -491,9 +502,10 @@ uint64_t cascade_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr0
 // takes the positions [floor(c W / C), floor((c+1) W / C)); a page belongs
 // to the CTA that owns its first position, and the pages of a segment owned
 // by one CTA form a unit; a segment without pages keeps one zero-page unit,
-// owned by the CTA of its overhead position. Every item with generations is
-// merged (its prefix state and its generations' suffix states), so all of
-// its units write partial slots, numbered in (item, segment, page) order.
+// owned by the CTA of its overhead position -- kept only when the whole
+// item has no page. The units of one item on one CTA form a chain (one row
+// state); an item on several CTAs is merged from one partial state per
+// chain.
 attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_indptr0,
                                  const int32_t* last0, int32_t page_size0,
                                  const int32_t* kv_indptr1, const int32_t* last1,
@@ -600,6 +612,8 @@ attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     // floor(c W / C) without overflow for W < 2^62 / C
     return (c * (W / C)) + (c * (W % C)) / C;
   };
+  std::vector<int64_t> item_pages(item_of.size(), 0);
+  for (const Seg& sg : segs) item_pages[size_t(sg.item)] += sg.n;
   // units in CTA order: the cut walks the segments in order, so the CTA
   // index never decreases
   std::vector<Unit> units;
@@ -633,7 +647,9 @@ attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_ind
       unit_item.push_back(sg.item);
     };
     if (sg.n == 0) {
-      emit(0, 0, owner(base));
+      // a segment without pages adds nothing; an item without any page
+      // keeps one empty unit (its rows get O = 0, LSE = -inf)
+      if (item_pages[size_t(sg.item)] == 0 && sg.kind == 0) emit(0, 0, owner(base));
     } else {
       int64_t k0 = 0;
       int64_t cur = owner(base + kCascadeAlpha);
@@ -649,32 +665,57 @@ attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     }
     base += sg.n * P + kCascadeAlpha;
   }
-  // merge tables: every item is merged; slots in unit order within an item
+  // Chains: consecutive units of one item on one CTA run as one row state
+  // (unit.pad bit 1: continues the previous unit, bit 2: continued by the
+  // next). An item on several CTAs (one chain on each) is split: each chain
+  // writes a partial state to its own slot, numbered in chain order, and
+  // the last to finish merges them.
   const int64_t num_items = int64_t(item_of.size());
-  std::vector<int32_t> merge_indptr(static_cast<size_t>(num_items) + 1, 0),
-      next(static_cast<size_t>(num_items), 0);
-  for (size_t i = 0; i < units.size(); ++i) merge_indptr[size_t(unit_item[i]) + 1]++;
-  for (int64_t i = 0; i < num_items; ++i) merge_indptr[size_t(i) + 1] += merge_indptr[size_t(i)];
-  // units are generated in (item, segment, page) order, so slot = position
-  for (size_t i = 0; i < units.size(); ++i) {
-    const int32_t it = unit_item[i];
-    units[i].split = it;
-    units[i].slot = merge_indptr[size_t(it)] + next[size_t(it)]++;
+  const size_t nu = units.size();
+  std::vector<int32_t> chain_of(nu), first_chain(static_cast<size_t>(num_items), -1),
+      item_chains(static_cast<size_t>(num_items), 0);
+  int32_t nchains = 0;
+  for (size_t i = 0; i < nu; ++i) {
+    const bool cont = i > 0 && unit_item[i] == unit_item[i - 1] && unit_cta[i] == unit_cta[i - 1];
+    chain_of[i] = cont ? chain_of[i - 1] : nchains++;
+    const size_t it = size_t(unit_item[i]);
+    if (!cont) {
+      if (first_chain[it] < 0) first_chain[it] = chain_of[i];
+      item_chains[it]++;
+    }
   }
-  std::vector<int4> merge_items(static_cast<size_t>(num_items));
-  for (int64_t i = 0; i < num_items; ++i) {
-    const int4 it = item_of[size_t(i)];
-    merge_items[size_t(i)] = make_int4(it.x, it.y, 0, merge_indptr[size_t(i) + 1] -
-                                                         merge_indptr[size_t(i)]);
+  std::vector<int32_t> split_of(static_cast<size_t>(num_items), -1);
+  std::vector<int32_t> merge_indptr(1, 0);
+  std::vector<int4> merge_items;
+  for (int64_t k = 0; k < num_items; ++k) {
+    if (item_chains[size_t(k)] < 2) continue;
+    split_of[size_t(k)] = int32_t(merge_items.size());
+    const int4 it = item_of[size_t(k)];
+    merge_items.push_back(make_int4(it.x, it.y, 0, item_chains[size_t(k)]));
+    merge_indptr.push_back(merge_indptr.back() + item_chains[size_t(k)]);
+  }
+  for (size_t i = 0; i < nu; ++i) {
+    const size_t it = size_t(unit_item[i]);
+    const int32_t sid = split_of[it];
+    units[i].split = sid;
+    units[i].slot = sid < 0 ? -1 : merge_indptr[size_t(sid)] + (chain_of[i] - first_chain[it]);
+    const bool cprev = i > 0 && chain_of[i - 1] == chain_of[i];
+    const bool cnext = i + 1 < nu && chain_of[i + 1] == chain_of[i];
+    units[i].pad |= (cprev ? 2 : 0) | (cnext ? 4 : 0);
   }
   std::vector<int32_t> work_indptr(size_t(C) + 1, 0);
-  for (size_t i = 0; i < units.size(); ++i) work_indptr[size_t(unit_cta[i]) + 1]++;
+  for (size_t i = 0; i < nu; ++i) work_indptr[size_t(unit_cta[i]) + 1]++;
   for (int64_t i = 0; i < C; ++i) work_indptr[size_t(i) + 1] += work_indptr[size_t(i)];
+  // within a CTA, the chains of split items first (stable; chains stay whole)
+  for (int64_t i = 0; i < C; ++i)
+    std::stable_partition(units.begin() + work_indptr[size_t(i)],
+                          units.begin() + work_indptr[size_t(i) + 1],
+                          [](const Unit& u) { return u.slot >= 0; });
   int64_t max_load = 0;
   for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, bound(i + 1) - bound(i));
 
-  const int64_t S = num_items;
-  const int64_t slots = int64_t(units.size());
+  const int64_t S = int64_t(merge_items.size());
+  const int64_t slots = merge_indptr.back();
   const PlanLayout L = plan_layout(num_ctas, int64_t(units.size()), S, slots, rows, head_dim);
   if (size_t(L.table_bytes) > host_bytes) {
     *msg = "attn_plan_cascade: pinned host workspace too small for the plan tables";

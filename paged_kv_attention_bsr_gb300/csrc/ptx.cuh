@@ -142,6 +142,11 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int3
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// 16-byte asynchronous copy global -> shared through L2 only (.cg: reads
+// the L2 copy that other SMs' stores reached, never a stale L1 line).
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

@@ -216,12 +216,12 @@ def composable_run(w):
 
 
 def cascade_run(w):
-    """The same composable pass through CascadeAttention (prefix and suffix
-    on two streams, then the merge)."""
+    """The same composable pass through CascadeAttention's two-pass mode
+    (prefix and suffix on two streams, then the merge)."""
     from paged_kv_attention_bsr_gb300.api import CascadeAttention
     pre, suf = w.extra["prefix"], w.cache
     ca = CascadeAttention(w.num_qo_heads, w.num_kv_heads, 128, max_prompts=w.extra["prompts"],
-                          max_batch=w.batch)
+                          max_batch=w.batch, mode="two_pass")
     ca.plan(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, pre.page_size,
             suf.kv_indptr, suf.last_page_len, suf.page_size)
     o, l = ca.run(w.q.cuda(), to_device(pre), to_device(suf),
@@ -246,8 +246,9 @@ def test_composable_small_vs_flat(oracle_mod):
 
 
 def test_composable_full_size(oracle_mod):
-    """The full-size shared-prefix workload through CascadeAttention, every
-    row against the oracle on the flat single-format layout (host threads)."""
+    """The full-size shared-prefix workload through CascadeAttention's
+    two-pass mode, every row against the oracle on the flat single-format
+    layout (host threads)."""
     from tests.gpu_util import oracle_decode_threaded
     w = synth.shared_prefix_decode()
     o, l = cascade_run(w)
