@@ -220,8 +220,24 @@ attn_status_t upload_plan(const attn_plan_t* plan, const void* pinned_host_ws, v
     return fail(ATTN_ERR_WORKSPACE_TOO_SMALL, f + ": device workspace too small");
   if (reinterpret_cast<uintptr_t>(dev_ws) % 256 != 0)
     return fail(ATTN_ERR_INVALID_ARG, f + ": dev_ws must be 256-byte aligned");
-  cudaError_t e = cudaMemcpyAsync(dev_ws, pinned_host_ws, size_t(plan->table_bytes),
-                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  // Pinned memory that the device can address (every page-locked
+  // allocation on a system with unified addressing, such as a Grace-Blackwell
+  // node) is read by a copy kernel, so that the run kernel behind it on the
+  // stream starts without a copy-engine -> compute hand-off (3 to 4 us per
+  // run); other memory goes through cudaMemcpyAsync.
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = size_t(plan->table_bytes);
+  cudaPointerAttributes attr;
+  const void* src_dev = nullptr;
+  if (bytes % 16 == 0 && reinterpret_cast<uintptr_t>(pinned_host_ws) % 16 == 0 &&
+      cudaPointerGetAttributes(&attr, pinned_host_ws) == cudaSuccess &&
+      attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr)
+    src_dev = attr.devicePointer;
+  else
+    cudaGetLastError();  // clear a lookup failure on unregistered memory
+  cudaError_t e = src_dev ? launch_copy_tables(dev_ws, src_dev, bytes, st)
+                          : cudaMemcpyAsync(dev_ws, pinned_host_ws, bytes,
+                                            cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, (f + ": table upload").c_str());
   return ATTN_OK;
 }

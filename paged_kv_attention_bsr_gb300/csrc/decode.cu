@@ -487,9 +487,39 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             __threadfence();
             const int s0 = __ldg(a.ws.merge_indptr + g.split);
             const int s1 = __ldg(a.ws.merge_indptr + g.split + 1);
-            // loads in batches of kB slots (a few L2 round trips, not one per slot)
-            constexpr int kB = 16;
+            // loads in batches of kB slots (a few L2 round trips, not one per
+            // slot); with one head per kv head and up to kB1 slots, LSEs
+            // and O values come in one batch
+            constexpr int kB = 16, kB1 = 16;
             for (int h = 0; h < group; ++h) {
+              if (GM == 1 && s1 - s0 <= kB1) {  // (one head: registers to spare)
+                float ls[kB1], ov[kB1];
+#pragma unroll
+                for (int k = 0; k < kB1; ++k) {
+                  const int64_t prow = int64_t(s0 + k) * group + h;
+                  ls[k] = s0 + k < s1 ? __ldcg(a.ws.partial_lse + prow) : -INFINITY;
+                  ov[k] = s0 + k < s1 ? __ldcg(a.ws.partial_o + prow * kHeadDim + d) : 0.f;
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < kB1; ++k) M = fmaxf(M, ls[k]);
+                float out = 0.f, lse2 = -INFINITY;
+                if (M != -INFINITY) {
+                  float L = 0.f, acc_d = 0.f;
+#pragma unroll
+                  for (int k = 0; k < kB1; ++k) {
+                    const float f = ex2(ls[k] - M);
+                    L += f;
+                    acc_d += f * ov[k];
+                  }
+                  out = acc_d / L;
+                  lse2 = M + lg2(L);
+                }
+                const int64_t row = int64_t(g.r) * a.num_qo_heads + int64_t(g.hk) * group + h;
+                store_out<BF16>(a.o, row * kHeadDim + d, out * out_scale);
+                if (d == 0 && a.lse) a.lse[row] = lse2 * kLn2;
+                continue;
+              }
               float M = -INFINITY;
               for (int b0 = s0; b0 < s1; b0 += kB) {
                 float x[kB];

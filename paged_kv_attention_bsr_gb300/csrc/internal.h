@@ -249,6 +249,12 @@ cudaError_t ensure_smem_limit(Kernel kernel, int bytes, std::atomic<uint64_t>& d
   return e;
 }
 
+// Copies `bytes` (a multiple of 16) from `src_dev` -- pinned host memory
+// seen through its device mapping -- to device memory, with a kernel: the
+// run that follows on the stream then waits on no other engine.
+cudaError_t launch_copy_tables(void* dst, const void* src_dev, size_t bytes,
+                               cudaStream_t stream);
+
 // Writes O = 0 and LSE = -inf for `rows` rows of num_heads x head_dim (a
 // plan whose requests hold no kv tokens at all: every visible set is empty).
 cudaError_t launch_fill_empty(void* o, float* lse, int64_t rows, int32_t dtype,

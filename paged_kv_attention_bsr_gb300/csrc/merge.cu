@@ -164,7 +164,27 @@ __global__ void __launch_bounds__(256) fill_empty_kernel(void* o, float* lse, in
   }
 }
 
+// Plan-table upload: 16 bytes per thread from device-mapped pinned host
+// memory into the workspace.
+__global__ void __launch_bounds__(256) copy_tables_kernel(uint4* dst, const uint4* src,
+                                                          int64_t n16) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n16;
+       i += int64_t(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_copy_tables(void* dst, const void* src_dev, size_t bytes,
+                               cudaStream_t stream) {
+  const int64_t n16 = int64_t(bytes / 16);
+  if (n16 <= 0) return cudaSuccess;
+  int64_t blocks = (n16 + 255) / 256;
+  if (blocks > 152) blocks = 152;
+  copy_tables_kernel<<<int(blocks), 256, 0, stream>>>(static_cast<uint4*>(dst),
+                                                      static_cast<const uint4*>(src_dev), n16);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fill_empty(void* o, float* lse, int64_t rows, int32_t /*dtype: both 16-bit*/,
                               cudaStream_t stream) {
