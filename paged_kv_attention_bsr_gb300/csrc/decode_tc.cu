@@ -68,8 +68,10 @@ constexpr int kWarpEpi = 4;  // TMEM lanes 0-31, like the softmax warp
 constexpr int kWarpRope0 = 5;  // warps 5-8 turn K tiles when RoPE is fused in
 // warps 5-8 turn K tiles (RoPE); warps 5-7 widen FP8 tiles (eight warps in
 // all, two per scheduler: the register budget stays at 255 per thread)
-template <bool ROPE, bool FP8 = false>
-constexpr int block_threads() { return ROPE ? 288 : FP8 ? 256 : 160; }
+// warps 1 and 5-7 copy gathered rows (plain decode at page sizes that are
+// not a multiple of 16; eight warps keep the register budget at 255)
+template <bool ROPE, bool FP8 = false, bool GW = false>
+constexpr int block_threads() { return ROPE ? 288 : FP8 ? 256 : GW ? 256 : 160; }
 constexpr int kConvThreads = 96;  // FP8 converter warps 5-7
 
 // Two E4M3 values (the low byte first) as an f16x2 word (exact).
@@ -97,14 +99,14 @@ constexpr int kOffQ = 0;
 constexpr int kOffRopeCos = kOffQ + 32 * 128;
 constexpr int kOffRopeSin = kOffRopeCos + 8 * 64 * 4;
 static_assert(kOffRopeSin + 8 * 64 * 4 <= kOffQ + 64 * 128, "RoPE offset rows fit query rows 32-63");
-// Gathered rows: the page index of each token of a tile (128 int32), copied
-// kIdxDepth tiles ahead into a ring of kIdxDepth + 1 slots (the slot being
-// read is never the one being filled) in query-tile rows 64-127 of the
+// Gathered rows: the pool row of each token of a tile (128 int32), stored
+// kRowLead - 1 tiles ahead into a ring of kRowSlots tiles (the slot being
+// read is never the one being written) in query-tile rows 64-127 of the
 // lower half.
-constexpr int kIdxDepth = 4;
-constexpr int kIdxSlots = kIdxDepth + 1;
-constexpr int kOffIdxRing = kOffQ + 64 * 128;
-static_assert(kOffIdxRing + kIdxSlots * kTcTile * 4 <= kOffQ + kTcHalf, "index ring fits the spare query rows");
+constexpr int kRowLead = 4;
+constexpr int kRowSlots = kRowLead + 1;
+constexpr int kOffRowRing = kOffQ + 64 * 128;
+static_assert(kOffRowRing + kRowSlots * kTcTile * 4 <= kOffQ + kTcHalf, "row ring fits the spare query rows");
 constexpr int kOffRing = kTileBytes;
 constexpr int kOffF8 = kOffRing + 4 * kTileBytes;  // FP8 staging ring
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
@@ -490,73 +492,88 @@ __device__ __forceinline__ void rope_key4(uint2& x, uint2& y, float4 cb, float4 
   y = make_uint2(pack2<BF16>(yr0.x, yr0.y), pack2<BF16>(yr1.x, yr1.y));
 }
 
-// Producer of gathered rows (page sizes that are not a multiple of 16): lane
-// c gathers the rows of tokens 4 c .. 4 c + 3 of each 128-token tile with one
-// tile::gather4 per 64-dim half; a group's tokens past the unit's end repeat
-// its last token (every row read lies in the pool; those columns are
-// masked, and such V rows are zeroed before P.V). Each lane's page indices
-// are copied kIdxDepth tiles ahead with cp.async into a shared ring (its own
-// 16 bytes per tile), so no index load waits on the critical path. Kept out
-// of line: the kernel body (nine warps' loops) stays as compact as without
-// this mode.
-template <bool DEC>
+// Producer of gathered rows (page sizes that are not a multiple of 16, down
+// to one token per page): the rows are copied with 16-byte cp.async (the
+// load-store unit, not the TMA engine: a TMA gather moves four 128-byte rows
+// per instruction, and at one token per page its per-instruction cost, not
+// DRAM, set the pace) straight into the slot's 128B-swizzled layout. NW
+// warps share the work, warp cw taking rows [cw RW, cw RW + RW) of every
+// tile (RW = 128 / NW): the copies of random rows are issue-bound in one
+// warp (address translation per row), so the plain decode kernel spreads
+// them over four warps, one per scheduler.
+//  - Pool rows: lane c loads the page indices of the warp's tokens
+//    c TPL .. c TPL + TPL - 1 (TPL = RW / 32) of tile i + kRowLead at tile
+//    i and, one tile later (the load has landed meanwhile), stores their
+//    pool rows (-1 past the unit's end) into the warp's shared ring of
+//    kRowSlots tiles x RW rows.
+//  - Copies: per 16-byte piece of a row, lanes 0-15 take one row and 16-31
+//    the next; a lane reads 8 rows' pool indices from the ring, then issues
+//    their 8 copies.
+//  - Every lane arrives on the slot's full barrier (count 32 NW) through
+//    cp.async.mbarrier.arrive, i.e. once its copies have landed; the MMA
+//    thread fences into the async proxy after its wait. Nothing here waits
+//    for its own copies, so the whole ring stays in flight.
+//  - Rows past a unit's end are not copied: the softmax masks those keys
+//    and zeroes those V rows.
+// Kept out of line: the kernel body stays as compact as without this mode.
+template <bool DEC, int NW>
 __device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bars, uint32_t base,
-                                            const uint8_t* gbase, int lane,
+                                            uint8_t* gbase, int lane, int cw,
                                             volatile int32_t* err, uint32_t& uses, bool& ok) {
+  constexpr int RW = kTile / NW;  // rows of a tile this warp copies
+  constexpr int TPL = RW / 32;    // tokens whose pool rows a lane looks up
+  static_assert(RW % 32 == 0 && RW % 16 == 0, "rows per warp");
   const AppendArgs& a = prm.a;
-  const int P = a.page_size;
-  // (page, slot) of lane c's tokens kv0 + u of tile i, u < 4, clamped to the
-  // unit's last token (positions < 2^31: 32-bit division)
-  const uint32_t idx_lane = base + kOffIdxRing + uint32_t(lane) * 16u;
-  auto for_group = [&](const DGeo& g, int i, auto&& f) {
-    const int64_t kv0 = g.tok_begin + int64_t(i) * kTile + 4 * lane;
-    uint32_t pg = uint32_t(kv0) / uint32_t(P), sl = uint32_t(kv0) - pg * uint32_t(P);
+  const uint32_t P = uint32_t(a.page_size);
+  const char* pools[2] = {static_cast<const char*>(a.k_pool), static_cast<const char*>(a.v_pool)};
+  int32_t* ring = reinterpret_cast<int32_t*>(gbase + kOffRowRing) + cw * (kRowSlots * RW);
+  // page indices of lane's tokens of tile i (positions < 2^31: 32-bit
+  // division); tokens past the unit's end load nothing
+  auto load_pages = [&](const DGeo& g, int i, int32_t (&ph)[TPL]) {
+    const int64_t kv0 = g.tok_begin + int64_t(i) * kTile + cw * RW + lane * TPL;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (u > 0 && kv0 + u < g.tok_end && ++sl == uint32_t(P)) {
-        sl = 0;
-        ++pg;
+    for (int u = 0; u < TPL; ++u) {
+      ph[u] = 0;
+      if (i < g.ntiles && kv0 + u < g.tok_end)
+        ph[u] = __ldg(a.kv_indices + g.page_base + uint32_t(kv0 + u) / P);
+    }
+  };
+  // their pool rows into ring slot i % kRowSlots
+  auto store_rows = [&](const DGeo& g, int i, const int32_t (&ph)[TPL]) {
+    const int64_t kv0 = g.tok_begin + int64_t(i) * kTile + cw * RW + lane * TPL;
+#pragma unroll
+    for (int u = 0; u < TPL; ++u) {
+      int32_t rw = -1;
+      if (i < g.ntiles && kv0 + u < g.tok_end) {
+        const uint32_t sl = uint32_t(kv0 + u) % P;
+        const int64_t phys = ph[u];
+        rw = prm.nhd ? int32_t((phys * P + sl) * a.num_kv_heads + g.hk)
+                     : int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
       }
-      f(u, pg, sl);
+      ring[(i % kRowSlots) * RW + lane * TPL + u] = rw;
     }
   };
-  // copy tile i's page indices into ring slot i % kIdxSlots (one commit
-  // group per call, empty past the unit's tiles)
-  auto idx_issue = [&](const DGeo& g, int i) {
-    if (i < g.ntiles && g.tok_begin + int64_t(i) * kTile + 4 * lane < g.tok_end)
-      for_group(g, i, [&](int u, uint32_t pg, uint32_t) {
-        cp_async4(idx_lane + uint32_t(i % kIdxSlots) * (kTile * 4) + 4u * u,
-                  a.kv_indices + g.page_base + pg);
-      });
-    cp_async_commit();
-  };
-  // the 4 pool rows of lane c's tokens of tile i (its indices have landed)
-  auto group_rows = [&](const DGeo& g, int i, int32_t (&rw)[4]) {
-    if (g.tok_begin + int64_t(i) * kTile + 4 * lane >= g.tok_end) {
-      rw[0] = rw[1] = rw[2] = rw[3] = 0;
-      return;
-    }
-    const uint8_t* ring = gbase + kOffIdxRing + lane * 16 + (i % kIdxSlots) * (kTile * 4);
-    for_group(g, i, [&](int u, uint32_t, uint32_t sl) {
-      const int64_t phys = *reinterpret_cast<const int32_t*>(ring + 4 * u);
-      rw[u] = prm.nhd ? int32_t((phys * P + sl) * a.num_kv_heads + g.hk)
-                      : int32_t((phys * a.num_kv_heads + g.hk) * P + sl);
-    });
-  };
+  const int hb = lane >> 4, pc = lane & 15;  // row of the pair, 16-byte piece
+  const uint32_t piece_off = uint32_t(pc >> 3) * kHalf;
   for (int vc = blockIdx.x; vc < a.num_ctas && ok; vc += gridDim.x)
     for (int ui = __ldg(a.ws.work_indptr + vc); ui < __ldg(a.ws.work_indptr + vc + 1) && ok;
          ++ui) {
       const DGeo g = decode_geo<DEC>(a, ui);
       if (g.ntiles == 0) continue;
-      int32_t grow[4] = {0, 0, 0, 0};
-      for (int j = 0; j < kIdxDepth; ++j) idx_issue(g, j);
+      int32_t ph[TPL];
+      for (int j = 0; j + 1 < kRowLead; ++j) {  // the first tiles' rows, directly
+        load_pages(g, j, ph);
+        store_rows(g, j, ph);
+      }
+      load_pages(g, kRowLead - 1, ph);
       for (int i = 0; i < g.ntiles && ok; ++i) {
+        store_rows(g, i + kRowLead - 1, ph);  // loaded a tile ago
+        load_pages(g, i + kRowLead, ph);
+        __syncwarp();  // the ring rows of tile i (stored kRowLead - 1 tiles ago)
         const int64_t kv0 = g.tok_begin + int64_t(i) * kTile;
-        const int ntt = int(min(int64_t(kTile), g.tok_end - kv0));
-        const int ngr = (ntt + 3) / 4;  // gathered groups of 4 rows
-        idx_issue(g, i + kIdxDepth);
-        cp_async_wait<kIdxDepth>();  // tile i's indices have landed
-        group_rows(g, i, grow);
+        // rows of this warp's share that hold tokens
+        const int nr = int(max(int64_t(0), min(int64_t(RW), g.tok_end - kv0 - cw * RW)));
+        const int32_t* rows = ring + (i % kRowSlots) * RW;
         for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
           const int slot = int(uses % kSlots);
           bool r = true;
@@ -567,19 +584,26 @@ __device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bar
             ok = false;
             break;
           }
-          const uint32_t full = smem_u32(&bars.slot_full[slot]);
-          if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(ngr) * 4u * 256u);
-          __syncwarp();
-          if (lane < ngr) {
-            const uint32_t dst = base + kOffRing + slot * kTileBytes + uint32_t(lane) * 4u * 128u;
-            const void* tm = kv == 0 ? static_cast<const void*>(&prm.tm_k)
-                                     : static_cast<const void*>(&prm.tm_v);
-            tma_gather4(dst, tm, 0, grow[0], grow[1], grow[2], grow[3], full);
-            tma_gather4(dst + kHalf, tm, 64, grow[0], grow[1], grow[2], grow[3], full);
+          const char* pool = pools[kv] + pc * 16;
+          const uint32_t dst0 = base + kOffRing + slot * kTileBytes + piece_off;
+          for (int r0 = 0; r0 < nr; r0 += 16) {  // rows r0 .. r0 + 15, two per step
+            int32_t gr[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) gr[k] = rows[r0 + 2 * k + hb];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int rl = r0 + 2 * k + hb;  // row within the share
+              const int row = cw * RW + rl;    // row within the tile
+              if (rl < nr && gr[k] >= 0)
+                cp_async16_cg(dst0 + uint32_t(row) * 128u + (uint32_t((pc & 7) ^ (row & 7)) << 4),
+                              pool + int64_t(gr[k]) * (kHeadDim * 2));
+            }
           }
+          cp_async_mbar_arrive_noinc(smem_u32(&bars.slot_full[slot]));
         }
       }
     }
+  cp_async_wait<0>();  // every copy has landed before the CTA can exit
 }
 
 // Producer of 16-row boxes from NHD pools (page sizes that are a multiple of
@@ -637,8 +661,8 @@ __device__ __noinline__ void produce_nhd_box(const DecodeTcParams& prm, Bars& ba
     }
 }
 
-template <bool BF16, int R, bool DEC, bool ROPE, bool FP8 = false>
-__global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
+template <bool BF16, int R, bool DEC, bool ROPE, bool FP8 = false, bool GW = false>
+__global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
   constexpr int C = 32 / R;     // copies of each query row
   constexpr int W = kTile / C;  // kv columns per copy and tile
@@ -646,6 +670,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
   constexpr int kRing = ring_slots<FP8>();  // 16-bit K/V slots
   constexpr bool kMmaBF16 = FP8 ? false : BF16;  // operand type of the MMAs (and of P)
   static_assert(!(FP8 && ROPE), "FP8 K/V and fused RoPE are separate kernels");
+  static_assert(!(GW && (FP8 || ROPE)), "gather copy warps only in the plain kernel");
   extern __shared__ uint8_t smem_raw[];
   const AppendArgs& a = prm.a;
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -661,7 +686,10 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     mbar_init(smem_u32(&bars.q_full), 32);
     mbar_init(smem_u32(&bars.q_empty), 1);
     for (int i = 0; i < kRing; ++i) {
-      mbar_init(smem_u32(&bars.slot_full[i]), FP8 ? kConvThreads : 1);  // FP8: converters fill it
+      // FP8: the converters fill it; gathered rows: each producer lane's
+      // copies arrive on it; else one TMA arrival with its byte count
+      mbar_init(smem_u32(&bars.slot_full[i]),
+                FP8 ? kConvThreads : prm.gather ? (GW ? 4 * 32 : 32) : 1);
       mbar_init(smem_u32(&bars.slot_empty[i]), 1);
     }
     for (int i = 0; i < kF8Slots; ++i) {
@@ -682,7 +710,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     mbar_init(smem_u32(&bars.drain), 1);
     fence_mbar_init();
   }
-  if (warp == kWarpLoad && lane == 0) {
+  if (warp == kWarpLoad && lane == 0 && !prm.gather) {
     prefetch_tmap(&prm.tm_k);
     prefetch_tmap(&prm.tm_v);
     if (!DEC && a.cascade) {
@@ -713,7 +741,10 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     uint32_t uses = 0;
     bool ok = true;
     if (!FP8 && prm.gather) {
-      produce_gather<DEC>(prm, bars, base, gbase, lane, err, uses, ok);
+      if constexpr (GW)  // with warps 5-7: a quarter of every tile's rows each
+        produce_gather<DEC, 4>(prm, bars, base, gbase, lane, 0, err, uses, ok);
+      else
+        produce_gather<DEC, 1>(prm, bars, base, gbase, lane, 0, err, uses, ok);
     } else if (!FP8 && prm.nhd) {
       produce_nhd_box<DEC>(prm, bars, base, lane, err, uses, ok);
     } else {
@@ -887,9 +918,13 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
       uint32_t ua = 0, jt = 0, n_u = 0;
       bool ok = true;
       auto slot_of = [](uint32_t use) { return use % kRing; };
+      // (gathered rows land through cp.async, i.e. the generic proxy: fence
+      // them into the async proxy before the MMAs read the slot)
       auto wait_slot = [&](uint32_t use) -> bool {
-        return mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kRing) & 1u, err,
-                         ERR_WAIT_FULL);
+        const bool r = mbar_wait(smem_u32(&bars.slot_full[slot_of(use)]), (use / kRing) & 1u,
+                                 err, ERR_WAIT_FULL);
+        if (prm.gather) fence_proxy_async_smem();
+        return r;
       };
       // K tile k in its slot (and, with RoPE, turned by the rope warps)
       auto wait_k = [&](uint32_t k) -> bool {
@@ -1258,6 +1293,16 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
       }
   }
 
+  if constexpr (GW) {
+    if (warp >= kWarpRope0 && warp < kWarpRope0 + 3) {
+      // ------------------------------------------------- gathered-row copies
+      // (quarters 1-3 of every tile; warp 1 copies quarter 0)
+      uint32_t uses = 0;
+      bool ok = true;
+      produce_gather<DEC, 4>(prm, bars, base, gbase, lane, warp - kWarpRope0 + 1, err, uses, ok);
+    }
+  }
+
   if constexpr (FP8) {
     if (warp >= kWarpRope0 && warp < kWarpRope0 + kConvThreads / 32) {
       // ------------------------------------------------------- FP8 converters
@@ -1484,14 +1529,14 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
   }
 }
 
-template <bool BF16, int R, bool DEC, bool ROPE = false, bool FP8 = false>
+template <bool BF16, int R, bool DEC, bool ROPE = false, bool FP8 = false, bool GW = false>
 cudaError_t launch_k(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};
   cudaError_t e =
-      ensure_smem_limit(decode_tc_kernel<BF16, R, DEC, ROPE, FP8>, kSmem, configured);
+      ensure_smem_limit(decode_tc_kernel<BF16, R, DEC, ROPE, FP8, GW>, kSmem, configured);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<BF16, R, DEC, ROPE, FP8>
-      <<<grid, block_threads<ROPE, FP8>(), kSmem, stream>>>(prm);
+  decode_tc_kernel<BF16, R, DEC, ROPE, FP8, GW>
+      <<<grid, block_threads<ROPE, FP8, GW>(), kSmem, stream>>>(prm);
   return cudaGetLastError();
 }
 // decode runs with R = group in {2, 4, 8}; short appends with R in {1..16}
@@ -1518,6 +1563,13 @@ cudaError_t launch_dt(const DecodeTcParams& prm, int rows, int grid, cudaStream_
       case 4: return launch_k<BF16, 4, false, true>(prm, grid, stream);
       case 8: return launch_k<BF16, 8, false, true>(prm, grid, stream);
       default: return launch_k<BF16, 16, false, true>(prm, grid, stream);
+    }
+  }
+  if (!prm.a.qo_indptr && prm.gather) {  // decode of gathered rows: four copy warps
+    switch (rows) {
+      case 2: return launch_k<BF16, 2, true, false, false, true>(prm, grid, stream);
+      case 4: return launch_k<BF16, 4, true, false, false, true>(prm, grid, stream);
+      default: return launch_k<BF16, 8, true, false, false, true>(prm, grid, stream);
     }
   }
   if (!prm.a.qo_indptr) {
@@ -1578,8 +1630,10 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
     return cudaErrorNotSupported;
   }
   const int elem = a.kv_fp8 ? kKvElemU8 : (bf16 ? kKvElemBF16 : kKvElemF16);
-  if (!make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, elem,
-                    prm.gather ? 1u : uint32_t(kChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
+  // (gathered rows are copied with cp.async: no tensor map)
+  if (!prm.gather &&
+      !make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, elem,
+                    uint32_t(kChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorNotSupported;  // *msg says why
   if (a.cascade &&
       !make_kv_maps(a.k_pool2, a.v_pool2, a.num_pages2, a.num_kv_heads, a.page_size2, elem,
