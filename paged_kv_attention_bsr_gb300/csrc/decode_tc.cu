@@ -1081,7 +1081,24 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
           const int nvalid = int(max(int64_t(0), min(int64_t(kTile), row_end - kv0)));
           // this thread's W scores: columns [W c, W c + W) of its row
           float s[W];
-          {
+          if constexpr (ROPE) {
+            // nine warps leave 168 registers a thread: 32 columns at a time
+#pragma unroll
+            for (int j = 0; j < W; ++j) s[j] = 0.f;
+#pragma unroll
+            for (int q4 = 0; q4 < kTile / 32; ++q4) {
+              float v[32];
+              tmem_ld32(tmem + col_s + 32u * q4, v);
+#pragma unroll
+              for (int b = 0; b < C; ++b) {
+                const bool mine = c == b;
+#pragma unroll
+                for (int j = 0; j < W; ++j)
+                  if (W * b + j >= 32 * q4 && W * b + j < 32 * q4 + 32)
+                    s[j] = mine ? v[W * b + j - 32 * q4] : s[j];
+              }
+            }
+          } else {
             float v[kTile];
             tmem_ld128(tmem + col_s, v);
 #pragma unroll
