@@ -81,16 +81,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
   return d;
 }
 constexpr int kSlots = 6;
-// FP8 K/V (E4M3 bytes): TMA lands 128-row tiles of 128-byte rows (128B
-// swizzle, the same row pattern as one 64-dim half of a 16-bit tile) in a
-// four-slot staging ring that takes the place of two 16-bit slots; warps 5-7
-// widen each staged tile into one of the remaining four 16-bit slots. (Six
-// staging slots and three 16-bit slots were slower: 130 against 112 us on
-// the uniform batch; the widened ring must run a tile pair ahead.)
-constexpr int kF8Slots = 4;
-constexpr int kF8SlotBytes = kTcTile * 128;
+// FP8 K/V (E4M3 bytes): TMA lands a 128-row tile of 128-byte rows (128B
+// swizzle, the same row pattern as one 64-dim half of a 16-bit tile) in the
+// upper 64-dim half of its own 16-bit slot, and warps 5-7 widen it there in
+// place: row r's E4M3 bytes occupy exactly the bytes of row r's upper f16
+// half, and a warp reads whole rows before it writes them. So FP8 keeps
+// the six-slot ring of 16-bit pools, with up to six tiles of E4M3 bytes in
+// flight (a separate four-slot staging ring beside four 16-bit slots held
+// it to about 0.48 of the HBM peak).
+constexpr int kF8TileBytes = kTcTile * 128;
 template <bool FP8>
-constexpr int ring_slots() { return FP8 ? 4 : kSlots; }
+constexpr int ring_slots() { return kSlots; }
 constexpr int kOffQ = 0;
 // RoPE key angles: cos / sin of the offset rows o = 0, 2, .., 14 (8 x 64
 // floats each) in query-tile rows 32-63 of the lower half, which hold no
@@ -108,9 +109,8 @@ constexpr int kRowSlots = kRowLead + 1;
 constexpr int kOffRowRing = kOffQ + 64 * 128;
 static_assert(kOffRowRing + kRowSlots * kTcTile * 4 <= kOffQ + kTcHalf, "row ring fits the spare query rows");
 constexpr int kOffRing = kTileBytes;
-constexpr int kOffF8 = kOffRing + 4 * kTileBytes;  // FP8 staging ring
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
-static_assert(kOffF8 + kF8Slots * kF8SlotBytes <= kOffBar, "FP8 staging fits two slots");
+static_assert(kF8TileBytes == kHalf, "an E4M3 tile fills the upper half of a 16-bit slot");
 constexpr int kOffHand = kOffBar + 512;         // softmax -> epilogue row state
 constexpr int kSmem = kOffHand + 512 + 1024;    // + alignment slack
 constexpr uint32_t kTmemCols = 512;  // S buffers at 0 and 128, O buffers at 256 and 384
@@ -124,8 +124,7 @@ struct Bars {
   uint64_t ounit[2];    // a unit's last P.V into O[b] is done (commit)
   uint64_t ep_full[2];  // softmax wrote the row state of a unit with O[b] (count 32)
   uint64_t k_rot[kSlots / 2];  // RoPE: K tile k is turned in its slot (count 128)
-  uint64_t f8_full[kF8Slots];  // FP8: a staged tile has landed (TMA bytes)
-  uint64_t f8_empty[kF8Slots]; // FP8: the converters have read it (count 96)
+  uint64_t f8_full[kSlots];    // FP8: a tile's E4M3 bytes have landed (TMA bytes)
   uint64_t drain;
   uint32_t tmem_base;
 };
@@ -692,10 +691,8 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
                 FP8 ? kConvThreads : prm.gather ? (GW ? 4 * 32 : 32) : 1);
       mbar_init(smem_u32(&bars.slot_empty[i]), 1);
     }
-    for (int i = 0; i < kF8Slots; ++i) {
-      mbar_init(smem_u32(&bars.f8_full[i]), 1);
-      mbar_init(smem_u32(&bars.f8_empty[i]), kConvThreads);
-    }
+    if (FP8)
+      for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars.f8_full[i]), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
       mbar_init(smem_u32(&bars.p_full[i]), 32);
@@ -770,12 +767,12 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
             const int nch = (ntt + kChunk - 1) / kChunk;
             const int32_t row_next = i + 1 < g.ntiles ? chunk_row(g, i + 1) : 0;
             for (int kv = 0; kv < 2; ++kv, ++uses) {  // K then V
-              // 16-bit: a ring slot; FP8: a staging slot (128-byte rows)
-              const int nslot = FP8 ? kF8Slots : kRing;
+              // a ring slot (FP8: its upper half receives the 128-byte rows)
+              const int nslot = kRing;
               const int slot = int(uses % nslot);
               bool r = true;
               if (lane == 0)
-                r = mbar_wait(smem_u32(FP8 ? &bars.f8_empty[slot] : &bars.slot_empty[slot]),
+                r = mbar_wait(smem_u32(&bars.slot_empty[slot]),
                               ((uses / nslot) & 1u) ^ 1u, err, ERR_WAIT_EMPTY);
               if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0) == 0) {
                 ok = false;
@@ -792,7 +789,8 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
                                          : (second ? static_cast<const void*>(&prm.tm_v2)
                                                    : static_cast<const void*>(&prm.tm_v));
                 if constexpr (FP8) {
-                  tma_load_2d(base + kOffF8 + slot * kF8SlotBytes + uint32_t(lane) * kChunk * 128u,
+                  tma_load_2d(base + kOffRing + slot * kTileBytes + kHalf +
+                                  uint32_t(lane) * kChunk * 128u,
                               tm, 0, row, full);
                 } else {
                   const uint32_t dst =
@@ -809,7 +807,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
     // drain: every issued copy has landed before the CTA can exit
     cp_async_wait<0>();  // this lane's index copies (they always complete)
     if (lane == 0) {
-      const uint32_t nslot = FP8 ? kF8Slots : kRing;
+      const uint32_t nslot = kRing;
       for (uint32_t sl = 0; sl < nslot && sl < uses; ++sl) {
         const uint32_t last = uses - 1 - ((uses - 1 - sl) % nslot);
         mbar_wait(smem_u32(FP8 ? &bars.f8_full[sl] : &bars.slot_full[sl]), (last / nslot) & 1u,
@@ -1323,11 +1321,13 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
   if constexpr (FP8) {
     if (warp >= kWarpRope0 && warp < kWarpRope0 + kConvThreads / 32) {
       // ------------------------------------------------------- FP8 converters
-      // Warps 5-7 widen every staged K / V tile (128 rows of 128 E4M3 bytes,
-      // 128B-swizzled) into a 16-bit ring slot (two 128B-swizzled 64-dim
-      // halves) for the MMAs: thread t takes the 16-byte pieces t, t + 96,
-      // ... (row = piece / 8, dims 16 (piece % 8) .. + 15), so a warp reads
-      // four whole rows at a time. E4M3 -> f16 is exact (one cvt per pair).
+      // Warps 5-7 widen every K / V tile in place: its 128 rows of 128 E4M3
+      // bytes (128B-swizzled) sit in the upper half of the slot, and become
+      // two 128B-swizzled 64-dim halves of f16 for the MMAs. Thread t takes
+      // the 16-byte pieces t, t + 96, ... (row = piece / 8, dims
+      // 16 (piece % 8) .. + 15): a warp holds whole rows, reads all of its
+      // pieces, syncs, then writes (the upper f16 half of a row overwrites
+      // that row's E4M3 bytes). E4M3 -> f16 is exact (one cvt per pair).
       // Rows past a unit's end are widened too: the softmax masks those keys
       // and zeroes those V rows, as it does for 16-bit pools.
       const int t = threadIdx.x - kWarpRope0 * 32;  // 0..95
@@ -1349,16 +1349,14 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
       DGeo g;
       while (ok && next_unit(g)) {
         for (int i = 0; i < 2 * g.ntiles && ok; ++i, ++use) {  // K then V of each tile
-          const uint32_t fs = use % kF8Slots, rs = use % kRing;
-          if (!mbar_wait(smem_u32(&bars.f8_full[fs]), (use / kF8Slots) & 1u, err,
-                         ERR_WAIT_FULL) ||
-              !mbar_wait(smem_u32(&bars.slot_empty[rs]), ((use / kRing) & 1u) ^ 1u, err,
-                         ERR_WAIT_EMPTY)) {
+          const uint32_t rs = use % kRing;
+          // (the producer loads a slot only once it is free)
+          if (!mbar_wait(smem_u32(&bars.f8_full[rs]), (use / kRing) & 1u, err, ERR_WAIT_FULL)) {
             ok = false;
             break;
           }
-          const uint8_t* src = gbase + kOffF8 + fs * kF8SlotBytes;
           uint8_t* dst = gbase + kOffRing + rs * kTileBytes;
+          const uint8_t* src = dst + kHalf;
           constexpr int kPieces = kTile * 8;  // 16-byte pieces of a staged tile
           constexpr int kPer = (kPieces + kConvThreads - 1) / kConvThreads;
           // all of this thread's pieces are loaded before any is widened
@@ -1370,6 +1368,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
             if (piece < kPieces)
               raws[k] = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
           }
+          __syncwarp();  // the warp's rows are read before any is overwritten
 #pragma unroll
           for (int k = 0; k < kPer; ++k) {
             const int piece = t + kConvThreads * k;
@@ -1393,7 +1392,6 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
           }
           fence_proxy_async_smem();  // generic stores -> the MMA's operand reads
           mbar_arrive(smem_u32(&bars.slot_full[rs]));
-          mbar_arrive(smem_u32(&bars.f8_empty[fs]));
         }
       }
     }
