@@ -90,6 +90,24 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
+# ncu summaries under profiles/ per workload, with the sources whose hash
+# they record (the kernel's own files and the planner, whose cut sets the
+# split items' partial-state traffic)
+_TC = ["decode_tc.cu", "tc.cuh", "ptx.cuh", "plan.cpp", "internal.h"]
+PROFILES = {
+    "uniform_decode": ("decode_tc_kernel_uniform_gqa_b64.md", _TC),
+    "skewed_decode": ("decode_tc_kernel_skewed_b128.md", _TC),
+    "shared_prefix": ("decode_tc_kernel_cascade_16x4.md", _TC),
+    "sparse_decode": ("decode_tc_kernel_sparse_p1_b64.md", _TC),
+    "rope_decode": ("decode_tc_kernel_rope_uniform_gqa_b64.md", _TC),
+    "fp8_decode": ("decode_tc_kernel_fp8_uniform_gqa_b64.md", _TC),
+    "single_decode": ("decode_kernel_single_h32_kv2048.md",
+                      ["decode.cu", "ptx.cuh", "plan.cpp", "internal.h"]),
+    "causal_append": ("append_kernel_causal_b16.md",
+                      ["append.cu", "tc.cuh", "ptx.cuh", "plan.cpp", "internal.h"]),
+}
+
+
 def profile_traffic(profile_name, kernel_sources):
     """DRAM bytes per launch recorded by an ncu capture, if the kernel source
     has not changed since (profiles/<name> lists the source hash)."""
@@ -558,6 +576,11 @@ def extra_workloads(hbm_peak, bf16_peak, flush, steps=30, warmup=3):
     for key in ("single_decode", "skewed_decode", "causal_append", "shared_prefix",
                 "rope_decode", "rope_append", "sparse_decode", "pod_mixed", "fp8_decode"):
         name, res = WORKLOAD_BENCH[key](hbm_peak, bf16_peak, flush, steps, warmup)
+        if key in PROFILES:  # DRAM bytes per launch from the ncu capture at this source
+            t = profile_traffic(*PROFILES[key])
+            res["traffic_bytes_per_launch"] = t
+            if t is not None and "bytes" in res:
+                res["traffic_over_algorithmic"] = t / res["bytes"]
         out[name] = res
     return out
 
@@ -881,8 +904,7 @@ def run_ours(args, rank, world):
 
     if rank != 0:
         return None
-    traffic = profile_traffic("decode_tc_kernel_uniform_gqa_b64.md",
-                              ["decode_tc.cu", "tc.cuh", "ptx.cuh"])
+    traffic = profile_traffic(*PROFILES["uniform_decode"])
     achieved = b / kern_s / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
