@@ -927,7 +927,9 @@ def run_ours(args, rank, world):
                      "kernel": "decode_tc_kernel<bf16, group 4> (one launch per run; "
                                "split items merged inside it)",
                      "kernel_us": kern_s * 1e6, "algorithmic_bytes_per_launch": b},
-        "gpu_launches": args.steps,
+        # per timed step: attn_plan's table upload (copy_tables_kernel) and
+        # the decode kernel
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "e2e": e2e,
     }
