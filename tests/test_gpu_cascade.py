@@ -149,3 +149,94 @@ def test_one_launch_rejects_unsupported_shapes():
                       to_device(suf), w.sm_scale, o, None, dev)
     assert e.value.status == 2
     torch.cuda.synchronize()
+
+
+def test_one_launch_graph_replay_is_bit_identical(oracle_mod):
+    """attn_cascade_run captured in a CUDA graph and replayed three times
+    (the arrival counters reset inside the kernel) gives the eager result
+    bit for bit."""
+    w = synth.cascade_workload("graph", [3, 2, 4], [700, 2000, 130], [50, 0, 300, 17, 900, 64,
+                                                                     1, 640, 260],
+                               128, 16, 32, 8, torch.bfloat16, seed=905)
+    o0, l0, ca = run_one_launch(w, num_ctas=5)
+    pre, suf = w.extra["prefix"], w.cache
+    q = w.q.cuda()
+    dp, ds = to_device(pre), to_device(suf)
+    qo = torch.from_numpy(w.extra["prefix_qo_indptr"]).cuda()
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up off the default stream, as capture requires
+        ca.run(q, dp, ds, qo, w.sm_scale, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    o.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ca.run(q, dp, ds, qo, w.sm_scale, out=o, lse=lse)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ca.status() == 0
+    assert torch.equal(o, o0) and torch.equal(lse, l0)
+
+
+DEBUG_SCRIPT = """
+import sys
+import torch
+sys.path.insert(0, {root!r})
+from paged_kv_attention_bsr_gb300 import _capi as C, synth
+from paged_kv_attention_bsr_gb300.api import CascadeAttention
+from tests.gpu_util import to_device
+w = synth.cascade_workload("dbg", [2, 1], [300, 40], [20, 0, 90], 16, 16, 16, 4,
+                           torch.bfloat16, seed=907)
+pre, suf = w.extra["prefix"], w.cache
+ca = CascadeAttention(16, 4, 128, max_prompts=2, max_batch=3, mode="one_launch")
+ca.plan(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, 16, suf.kv_indptr,
+        suf.last_page_len, 16)
+q = w.q.cuda()
+qo = torch.from_numpy(w.extra["prefix_qo_indptr"]).cuda()
+dp, ds = to_device(pre), to_device(suf)
+used_p = int(pre.kv_indices.max()) + 1
+used_s = int(suf.kv_indices.max()) + 1
+dp["num_pages"], ds["num_pages"] = used_p, used_s
+ca.run(q, dp, ds, qo, w.sm_scale)  # consistent tables: passes the checks
+torch.cuda.synchronize()
+out = []
+bad = dict(ds)
+bad["kv_indices"] = ds["kv_indices"].clone()
+bad["kv_indices"][1] = used_s  # one past the declared suffix pages (inside the pool)
+try:
+    ca.run(q, dp, bad, qo, w.sm_scale)
+    out.append("suffix index: accepted")
+except C.AttnError as e:
+    out.append(f"suffix index: {{e.status}} {{C.last_error()}}")
+qo2 = qo.clone()
+qo2[1] = 1  # a device qo_indptr that is not the plan's
+try:
+    ca.run(q, dp, ds, qo2, w.sm_scale)
+    out.append("qo: accepted")
+except C.AttnError as e:
+    out.append(f"qo: {{e.status}} {{C.last_error()}}")
+torch.cuda.synchronize()
+assert ca.status() == 0
+print("|".join(out))
+"""
+
+
+def test_one_launch_debug_checks_reject_bad_tables():
+    """ATTN_DEBUG_CHECKS=1: an out-of-range suffix index and a device qo_indptr
+    that differs from the plan's are rejected on the host before any launch
+    (child process: the variable is read once per process)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, ATTN_DEBUG_CHECKS="1")
+    r = subprocess.run([sys.executable, "-c", DEBUG_SCRIPT.format(root=root)],
+                       capture_output=True, text=True, env=env, cwd=root, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    idx, qo = r.stdout.strip().splitlines()[-1].split("|")
+    assert idx.startswith("suffix index: 1 ") and "suffix kv_indices" in idx, idx
+    assert qo.startswith("qo: 1 ") and "differ from the plan" in qo, qo
