@@ -382,15 +382,18 @@ attn_status_t attn_merge_states(const void* o_a, const float* lse_a,
  * over both tables, merging inside the kernel.
  *   q                  : device [batch, num_qo_heads, head_dim] of `dtype`
  *   qo_indptr          : device copy of qo_indptr_h
- *   k_prefix, v_prefix : device HND pools of num_pages_prefix pages of
- *                        page_size_prefix tokens, `dtype`
+ *   k_prefix, v_prefix : device pools of num_pages_prefix pages of
+ *                        page_size_prefix tokens in `layout`, `dtype`
  *   kv_indptr_prefix, kv_indices_prefix, last_page_len_prefix : device copies
  *                        of the prefix table (indices in [0, num_pages_prefix))
  *   k_suffix ... last_page_len_suffix : the same for the suffix table
  *   o                  : device [batch, num_qo_heads, head_dim] (out)
  *   lse                : device float[batch, num_qo_heads] (out) or NULL
- * Supported: HND pools, both page sizes multiples of 16, group 1..16 with
- * group x n_p <= 16, fp16 / bf16. ATTN_DEBUG_CHECKS applies to both tables.
+ *   layout             : ATTN_LAYOUT_HND or ATTN_LAYOUT_NHD (both pools)
+ * Supported: any page sizes, both layouts, group 1..16 with group x n_p <= 16,
+ * fp16 / bf16. K / V rows load in 16-row TMA boxes when the pools are HND
+ * and both page sizes are multiples of 16, else row by row (cp.async).
+ * ATTN_DEBUG_CHECKS applies to both tables.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
  */
 attn_status_t attn_cascade_workspace_size(int32_t max_prompts, int32_t max_batch,
@@ -414,9 +417,9 @@ attn_status_t attn_cascade_run(const attn_plan_t* plan, const void* q, const int
                                const int32_t* last_page_len_prefix, const void* k_suffix,
                                const void* v_suffix, int64_t num_pages_suffix,
                                const int32_t* kv_indptr_suffix, const int32_t* kv_indices_suffix,
-                               const int32_t* last_page_len_suffix, int32_t dtype,
-                               float sm_scale, void* o, float* lse, void* dev_ws,
-                               size_t dev_bytes, void* stream);
+                               const int32_t* last_page_len_suffix, int32_t layout,
+                               int32_t dtype, float sm_scale, void* o, float* lse,
+                               void* dev_ws, size_t dev_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads the error word that kernels set in a

@@ -87,7 +87,7 @@ def _load():
         "attn_plan_cascade": [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, sz, vp,
                               sz, vp, P(Plan)],
         "attn_cascade_run": [P(Plan), vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, vp, vp, vp,
-                             i32, f32, vp, vp, vp, sz, vp],
+                             i32, i32, f32, vp, vp, vp, sz, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -216,10 +216,11 @@ def plan_cascade(qo_indptr_h, kv_indptr_prefix_h, last_prefix_h, page_size_prefi
     return p
 
 
-def cascade_run(p: Plan, q, qo_indptr, prefix, suffix, sm_scale, o, lse, dev_ws, stream=None):
+def cascade_run(p: Plan, q, qo_indptr, prefix, suffix, sm_scale, o, lse, dev_ws,
+                layout=LAYOUT_HND, stream=None):
     """attn_cascade_run. prefix / suffix: dicts of device tensors k_pool,
-    v_pool (HND), kv_indptr, kv_indices, last_page_len and optionally
-    num_pages (default: the pool's first dimension)."""
+    v_pool (both in `layout`), kv_indptr, kv_indices, last_page_len and
+    optionally num_pages (default: the pool's first dimension)."""
     n0 = int(prefix.get("num_pages", prefix["k_pool"].shape[0]))
     n1 = int(suffix.get("num_pages", suffix["k_pool"].shape[0]))
     has_kv = p.total_weight > p.num_items
@@ -232,7 +233,7 @@ def cascade_run(p: Plan, q, qo_indptr, prefix, suffix, sm_scale, o, lse, dev_ws,
         _ptr(prefix["v_pool"]), n0, _ptr(prefix["kv_indptr"]), _ptr(prefix["kv_indices"]),
         _ptr(prefix["last_page_len"]), _ptr(suffix["k_pool"]), _ptr(suffix["v_pool"]), n1,
         _ptr(suffix["kv_indptr"]), _ptr(suffix["kv_indices"]), _ptr(suffix["last_page_len"]),
-        dtype_code(q.dtype), float(sm_scale), _ptr(o), _ptr(lse), _ptr(dev_ws),
+        int(layout), dtype_code(q.dtype), float(sm_scale), _ptr(o), _ptr(lse), _ptr(dev_ws),
         dev_ws.numel() * dev_ws.element_size(), _stream(stream)))
 
 

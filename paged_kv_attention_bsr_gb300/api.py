@@ -119,12 +119,11 @@ class CascadeAttention:
     read once for its n generations; each generation's own suffix lives in a
     second pool (small pages). Two ways to run it:
 
-    * one launch (attn_plan_cascade / attn_cascade_run), taken when both
-      pools are HND with page sizes that are multiples of 16 and
-      group x n <= 16: one persistent few-row kernel balances the prefix and
-      suffix pages of every (prompt, kv head) together and merges the partial
-      states inside the kernel;
-    * otherwise two passes: a non-causal short append for the prefix (the n
+    * one launch (attn_plan_cascade / attn_cascade_run), taken when
+      group x n <= 16 (any page sizes, either layout): one persistent
+      few-row kernel balances the prefix and suffix pages of every (prompt,
+      kv head) together and merges the partial states inside the kernel;
+    * otherwise two passes: a non-causal append for the prefix (the n
       generations' rows per prompt) and a decode for the suffixes, enqueued
       on two streams (the suffix on a side stream forked from and joined back
       into the caller's stream), then attn_merge_states.
@@ -167,21 +166,20 @@ class CascadeAttention:
             self._events = [None] * self.RING
             self._turn = 0
 
-    def _fits_one_launch(self, qo_indptr_h, page_size_prefix, page_size_suffix) -> bool:
+    def _fits_one_launch(self, qo_indptr_h) -> bool:
         qo = np.asarray(qo_indptr_h)
         max_n = int(np.diff(qo).max()) if len(qo) > 1 else 0
         group = self.num_qo_heads // self.num_kv_heads
-        return (group * max(max_n, 1) <= 16 and page_size_prefix % 16 == 0 and
-                page_size_suffix % 16 == 0)
+        return group * max(max_n, 1) <= 16
 
     def plan(self, qo_indptr_prefix_h, kv_indptr_prefix_h, last_page_len_prefix_h,
              page_size_prefix: int, kv_indptr_suffix_h, last_page_len_suffix_h,
              page_size_suffix: int, stream=None):
         """Plans the run; the tables are uploaded on `stream`."""
-        fits = self._fits_one_launch(qo_indptr_prefix_h, page_size_prefix, page_size_suffix)
+        fits = self._fits_one_launch(qo_indptr_prefix_h)
         if self.mode == "one_launch" and not fits:
-            raise ValueError("one launch needs group x generations <= 16 and page sizes that "
-                             "are multiples of 16")
+            raise ValueError("one launch needs num_qo_heads / num_kv_heads x the generations "
+                             "of a prompt <= 16")
         self.one_launch = self.mode != "two_pass" and fits
         if self.one_launch:
             i = self._turn
@@ -208,10 +206,11 @@ class CascadeAttention:
         return None
 
     def run(self, q, prefix, suffix, qo_indptr_prefix, sm_scale=None, out=None, lse=None,
-            return_lse: bool = False):
+            return_lse: bool = False, layout: int = C.LAYOUT_HND):
         """q [batch, Hq, D] (one row per generation, grouped by prompt);
         prefix / suffix: dicts with k_pool, v_pool, kv_indptr, kv_indices,
-        last_page_len device tensors (HND pools). Returns o (and lse)."""
+        last_page_len device tensors (both pools in `layout`). Returns o
+        (and lse)."""
         if sm_scale is None:
             sm_scale = 1.0 / math.sqrt(self.head_dim)
         stream = torch.cuda.current_stream()
@@ -221,7 +220,7 @@ class CascadeAttention:
             lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
         if self.one_launch:
             C.cascade_run(self.plan_info, q, qo_indptr_prefix, prefix, suffix, sm_scale, out,
-                          lse, self.dev_ws, stream)
+                          lse, self.dev_ws, layout, stream)
             return (out, lse) if return_lse else out
         if self._bufs is None or self._bufs[0].shape != q.shape or \
                 self._bufs[0].dtype != q.dtype:
@@ -233,11 +232,11 @@ class CascadeAttention:
         with torch.cuda.stream(self.side):
             self.suffix.run(q, suffix["k_pool"], suffix["v_pool"], suffix["kv_indptr"],
                             suffix["kv_indices"], suffix["last_page_len"], sm_scale, out=o_s,
-                            lse=l_s, stream=self.side)
+                            lse=l_s, layout=layout, stream=self.side)
             self._join.record(self.side)
         self.prefix.run(q, prefix["k_pool"], prefix["v_pool"], prefix["kv_indptr"],
                         prefix["kv_indices"], prefix["last_page_len"], sm_scale, out=o_p,
-                        lse=l_p, qo_indptr=qo_indptr_prefix, stream=stream)
+                        lse=l_p, qo_indptr=qo_indptr_prefix, layout=layout, stream=stream)
         stream.wait_event(self._join)
         if lse is None:
             lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)

@@ -540,14 +540,14 @@ attn_status_t attn_cascade_run(const attn_plan_t* plan, const void* q, const int
                                const int32_t* last_page_len_prefix, const void* k_suffix,
                                const void* v_suffix, int64_t num_pages_suffix,
                                const int32_t* kv_indptr_suffix, const int32_t* kv_indices_suffix,
-                               const int32_t* last_page_len_suffix, int32_t dtype,
-                               float sm_scale, void* o, float* lse, void* dev_ws,
-                               size_t dev_bytes, void* stream) {
+                               const int32_t* last_page_len_suffix, int32_t layout,
+                               int32_t dtype, float sm_scale, void* o, float* lse,
+                               void* dev_ws, size_t dev_bytes, void* stream) {
   NvtxRange nvtx("attn_cascade_run");
   const char* fn = "attn_cascade_run";
   const std::string f(fn);
   attn_status_t s = check_plan_common(plan, ATTN_MODE_CASCADE, q, k_prefix, v_prefix,
-                                      num_pages_prefix, ATTN_LAYOUT_HND, kv_indptr_prefix,
+                                      num_pages_prefix, layout, kv_indptr_prefix,
                                       kv_indices_prefix, last_page_len_prefix, dtype, o, dev_ws,
                                       dev_bytes, fn);
   if (s != ATTN_OK) return s;
@@ -560,10 +560,6 @@ attn_status_t attn_cascade_run(const attn_plan_t* plan, const void* q, const int
   if (plan->batch > 0 && plan->total_qo > 0 &&
       (!qo_indptr || !kv_indptr_suffix || !last_page_len_suffix))
     return fail(ATTN_ERR_INVALID_ARG, f + ": null device pointer");
-  if (plan->page_size % 16 != 0 || plan->page_size_suffix % 16 != 0)
-    return fail(ATTN_ERR_UNSUPPORTED, f + ": both page sizes must be multiples of 16 (use a "
-                                          "prefix append, a suffix decode and "
-                                          "attn_merge_states for other page sizes)");
   if (debug_checks_enabled()) {
     s = debug_check_cascade(plan, qo_indptr, kv_indptr_prefix, kv_indices_prefix,
                             last_page_len_prefix, num_pages_prefix, kv_indptr_suffix,
@@ -575,7 +571,7 @@ attn_status_t attn_cascade_run(const attn_plan_t* plan, const void* q, const int
   if (plan_pages(*plan) == 0)
     return run_empty(plan, o, lse, plan->total_qo, dtype, stream, fn);
   AppendArgs a = append_args(plan, q, qo_indptr, k_prefix, v_prefix, num_pages_prefix,
-                             ATTN_LAYOUT_HND, kv_indptr_prefix, kv_indices_prefix,
+                             layout, kv_indptr_prefix, kv_indices_prefix,
                              last_page_len_prefix, dtype, sm_scale, o, lse, dev_ws);
   a.cascade = 1;
   a.page_size2 = plan->page_size_suffix;

@@ -523,9 +523,18 @@ __device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bar
   constexpr int TPL = RW / 32;    // tokens whose pool rows a lane looks up
   static_assert(RW % 32 == 0 && RW % 16 == 0, "rows per warp");
   const AppendArgs& a = prm.a;
-  const uint32_t P = uint32_t(a.page_size);
-  const char* pools[2] = {static_cast<const char*>(a.k_pool), static_cast<const char*>(a.v_pool)};
   int32_t* ring = reinterpret_cast<int32_t*>(gbase + kOffRowRing) + cw * (kRowSlots * RW);
+  // a unit's table (composable formats: pad = 1 reads the suffix table)
+  uint32_t P = 1;
+  const char* pools[2] = {nullptr, nullptr};
+  const int32_t* indices = nullptr;
+  auto table_of = [&](const DGeo& g) {
+    const bool second = g.pad != 0;
+    P = uint32_t(second ? a.page_size2 : a.page_size);
+    pools[0] = static_cast<const char*>(second ? a.k_pool2 : a.k_pool);
+    pools[1] = static_cast<const char*>(second ? a.v_pool2 : a.v_pool);
+    indices = second ? a.kv_indices2 : a.kv_indices;
+  };
   // page indices of lane's tokens of tile i (positions < 2^31: 32-bit
   // division); tokens past the unit's end load nothing
   auto load_pages = [&](const DGeo& g, int i, int32_t (&ph)[TPL]) {
@@ -534,7 +543,7 @@ __device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bar
     for (int u = 0; u < TPL; ++u) {
       ph[u] = 0;
       if (i < g.ntiles && kv0 + u < g.tok_end)
-        ph[u] = __ldg(a.kv_indices + g.page_base + uint32_t(kv0 + u) / P);
+        ph[u] = __ldg(indices + g.page_base + uint32_t(kv0 + u) / P);
     }
   };
   // their pool rows into ring slot i % kRowSlots
@@ -559,6 +568,7 @@ __device__ __noinline__ void produce_gather(const DecodeTcParams& prm, Bars& bar
          ++ui) {
       const DGeo g = decode_geo<DEC>(a, ui);
       if (g.ntiles == 0) continue;
+      table_of(g);
       int32_t ph[TPL];
       for (int j = 0; j + 1 < kRowLead; ++j) {  // the first tiles' rows, directly
         load_pages(g, j, ph);
@@ -1634,14 +1644,15 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
   prm.idesc_pv = make_idesc(bf16 && !a.kv_fp8, true);
   prm.gather = a.page_size % kChunk != 0 ? 1 : 0;
   prm.nhd = a.layout == ATTN_LAYOUT_NHD ? 1 : 0;
+  // composable formats: 16-row boxes when both tables allow them (HND, page
+  // sizes that are multiples of 16), else rows copied one by one for both
+  if (a.cascade && (prm.nhd || a.page_size2 % kChunk != 0)) prm.gather = 1;
   if (a.kv_fp8 && (prm.gather || prm.nhd || a.qo_indptr || a.rope_cos)) {
     *msg = "attn: the tensor-core FP8 decode takes HND pools with page_size % 16 == 0";
     return cudaErrorNotSupported;
   }
-  if (a.cascade && (!a.qo_indptr || prm.gather || prm.nhd || a.page_size2 <= 0 ||
-                    a.page_size2 % kChunk != 0 || a.kv_fp8 || a.rope_cos || a.causal)) {
-    *msg = "attn: composable formats in one launch take HND pools with both page sizes "
-           "multiples of 16";
+  if (a.cascade && (!a.qo_indptr || a.page_size2 <= 0 || a.kv_fp8 || a.rope_cos || a.causal)) {
+    *msg = "attn: composable formats in one launch take 16-bit pools without RoPE";
     return cudaErrorNotSupported;
   }
   const int elem = a.kv_fp8 ? kKvElemU8 : (bf16 ? kKvElemBF16 : kKvElemF16);
@@ -1650,7 +1661,7 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
       !make_kv_maps(a.k_pool, a.v_pool, a.num_pages, a.num_kv_heads, a.page_size, elem,
                     uint32_t(kChunk), prm.nhd != 0, &prm.tm_k, &prm.tm_v, msg))
     return cudaErrorNotSupported;  // *msg says why
-  if (a.cascade &&
+  if (a.cascade && !prm.gather &&
       !make_kv_maps(a.k_pool2, a.v_pool2, a.num_pages2, a.num_kv_heads, a.page_size2, elem,
                     uint32_t(kChunk), false, &prm.tm_k2, &prm.tm_v2, msg))
     return cudaErrorNotSupported;

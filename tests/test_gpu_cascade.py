@@ -128,27 +128,71 @@ def test_one_launch_full_size(oracle_mod):
     assert_attn_close(o, l, o_ref, lse_ref, w.name)
 
 
-def test_one_launch_rejects_unsupported_shapes():
+def _nhd(cache):
+    """The same pool in the NHD layout [pages, P, Hk, D]."""
+    return (cache.k_pool.permute(0, 2, 1, 3).contiguous(),
+            cache.v_pool.permute(0, 2, 1, 3).contiguous())
+
+
+# (gens, prefix lens, suffix lens, P0, P1, Hq, Hk, dtype, layout): page sizes
+# that are not multiples of 16 and NHD pools copy rows one by one
+ANY_PAGE = [
+    ([2, 3], [100, 37], [5, 0, 70, 16, 200], 8, 16, 16, 4, torch.bfloat16, 0),
+    ([4, 1], [1000, 0], [33, 1, 0, 90, 256], 128, 3, 32, 8, torch.float16, 0),
+    ([3, 2], [512, 80], [16, 17, 0, 300, 40], 16, 16, 32, 8, torch.bfloat16, 1),
+    ([2, 2], [45, 9], [1, 30, 7, 0], 1, 1, 16, 4, torch.bfloat16, 1),
+    ([5], [333], [24, 48, 5, 0, 99], 24, 5, 6, 2, torch.float16, 1),
+]
+
+
+@pytest.mark.parametrize("case", range(len(ANY_PAGE)))
+@pytest.mark.parametrize("num_ctas", [3, None])
+def test_one_launch_any_page_size_and_layout(oracle_mod, case, num_ctas):
+    from paged_kv_attention_bsr_gb300.api import CascadeAttention
+    gens, pre_lens, suf_lens, P0, P1, Hq, Hk, dtype, layout = ANY_PAGE[case]
+    w = synth.cascade_workload(f"anyp{case}", gens, pre_lens, suf_lens, P0, P1, Hq, Hk, dtype,
+                               seed=950 + case)
+    pre, suf = w.extra["prefix"], w.cache
+    poison_unused_slots(pre)
+    poison_unused_slots(suf)
+    o_ref, lse_ref = oracle_two_part(oracle_mod, w)  # on the HND pools: same logical cache
+    dp, ds = to_device(pre), to_device(suf)
+    if layout == 1:
+        for d, c in ((dp, pre), (ds, suf)):
+            kn, vn = _nhd(c)
+            d["k_pool"], d["v_pool"] = kn.cuda(), vn.cuda()
+    ca = CascadeAttention(Hq, Hk, 128, max_prompts=len(gens), max_batch=w.batch,
+                          mode="one_launch", num_ctas=num_ctas)
+    ca.plan(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, P0, suf.kv_indptr,
+            suf.last_page_len, P1)
+    o, l = ca.run(w.q.cuda(), dp, ds, torch.from_numpy(w.extra["prefix_qo_indptr"]).cuda(),
+                  w.sm_scale, return_lse=True, layout=layout)
+    torch.cuda.synchronize()
+    assert ca.status() == 0
+    assert_attn_close(o, l, o_ref, lse_ref, f"any page size case {case}")
+
+
+def test_one_launch_rejects_more_than_16_rows():
     from paged_kv_attention_bsr_gb300 import _capi as C
     from paged_kv_attention_bsr_gb300.api import CascadeAttention
-    w = synth.cascade_workload("p8", [2], [100], [10, 20], 8, 16, 8, 2, torch.bfloat16, seed=5)
+    # 8 query heads per kv head x 3 generations = 24 packed rows
+    w = synth.cascade_workload("rows24", [3], [100], [10, 20, 30], 16, 16, 16, 2,
+                               torch.bfloat16, seed=5)
     pre, suf = w.extra["prefix"], w.cache
-    ca = CascadeAttention(8, 2, 128, max_prompts=1, max_batch=2, mode="one_launch")
+    ca = CascadeAttention(16, 2, 128, max_prompts=1, max_batch=3, mode="one_launch")
     with pytest.raises(ValueError):
-        ca.plan(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, pre.page_size,
-                suf.kv_indptr, suf.last_page_len, suf.page_size)
-    # the C entry point refuses a page size that is not a multiple of 16
+        ca.plan(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, 16,
+                suf.kv_indptr, suf.last_page_len, 16)
     host = torch.zeros(1 << 16, dtype=torch.uint8)
-    dev = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
-    p = C.plan_cascade(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, 8,
-                       suf.kv_indptr, suf.last_page_len, 16, 8, 2, 128, 4, host, dev)
-    q = w.q.cuda()
-    o = torch.empty_like(q)
     with pytest.raises(C.AttnError) as e:
-        C.cascade_run(p, q, torch.from_numpy(w.extra["prefix_qo_indptr"]).cuda(), to_device(pre),
-                      to_device(suf), w.sm_scale, o, None, dev)
+        C.plan_cascade(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, 16,
+                       suf.kv_indptr, suf.last_page_len, 16, 16, 2, 128, 4, host)
     assert e.value.status == 2
-    torch.cuda.synchronize()
+    # "auto" falls back to the two passes and still matches the flat result
+    ca2 = CascadeAttention(16, 2, 128, max_prompts=1, max_batch=3, mode="auto")
+    ca2.plan(w.extra["prefix_qo_indptr"], pre.kv_indptr, pre.last_page_len, 16,
+             suf.kv_indptr, suf.last_page_len, 16)
+    assert not ca2.one_launch
 
 
 def test_one_launch_graph_replay_is_bit_identical(oracle_mod):
