@@ -151,10 +151,12 @@ attn_status_t attn_default_num_ctas(int32_t device, int32_t mode, int32_t* num_c
  *   dev_ws          : device workspace of dev_bytes bytes, or NULL to only
  *                     compute the tables on the host (no CUDA call is made).
  *   plan_out        : receives the plan.
- * The tables are written to pinned_host_ws and copied to dev_ws with one
- * cudaMemcpyAsync on `stream`; the copy also clears the workspace's error
- * word. The plan depends only on the host inputs and num_ctas and is
- * identical run to run.
+ * The tables are written to pinned_host_ws and copied to dev_ws on `stream`
+ * in one go: by a small copy kernel that reads pinned_host_ws through its
+ * device mapping when the memory is page-locked and mapped (so the run
+ * kernel behind it waits on no copy engine), else by one cudaMemcpyAsync.
+ * The copy also clears the workspace's error word. The plan depends only on
+ * the host inputs and num_ctas and is identical run to run.
  * Errors: INVALID_ARG (negative lengths, last_page_len out of range, heads not
  * divisible, append with kv_len < qo_len), UNSUPPORTED (head_dim != 128,
  * group too large), WORKSPACE_TOO_SMALL, CUDA.

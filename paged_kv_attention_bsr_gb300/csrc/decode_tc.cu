@@ -27,10 +27,11 @@
 // and are never read back. A causal short append masks each row at its own
 // end-aligned limit (token i of qo_len sees kv positions <= kv_len - qo_len + i).
 //
-// Warps (160 threads, one CTA per SM): 0 softmax; 1 TMA producer of the K/V
-// ring (six 32 KB slots; 16-row boxes by page index when the page size is a
-// multiple of 16, else rows gathered four at a time, down to one token per
-// page); 2 TMEM
+// Warps (160 threads, one CTA per SM): 0 softmax; 1 producer of the K/V
+// ring (six 32 KB slots; TMA 16-row boxes by page index when the page size is
+// a multiple of 16, else rows copied one by one with cp.async, down to one
+// token per page -- in plain decode together with warps 5-7, 256 threads);
+// 2 TMEM
 // allocation and the MMAs (one thread: S of tile k+1 runs under the softmax
 // of tile k, S double-buffered in TMEM); 3 query loader (plain loads of the
 // next unit's R query rows into registers, stored into the swizzled query
@@ -1367,7 +1368,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
           }
           uint8_t* dst = gbase + kOffRing + rs * kTileBytes;
           const uint8_t* src = dst + kHalf;
-          constexpr int kPieces = kTile * 8;  // 16-byte pieces of a staged tile
+          constexpr int kPieces = kTile * 8;  // 16-byte pieces of an E4M3 tile
           constexpr int kPer = (kPieces + kConvThreads - 1) / kConvThreads;
           // all of this thread's pieces are loaded before any is widened
           uint4 raws[kPer];

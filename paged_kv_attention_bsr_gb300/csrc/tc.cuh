@@ -217,7 +217,8 @@ constexpr int kKvElemU8 = 2;
 // rows, a box is 16 whole rows). Returns false when the driver cannot
 // describe them (message in *msg).
 // box_rows: 16 (16-row boxes within a page) or 1 (rows gathered one by one
-// with tile::gather4, for page sizes that are not a multiple of 16). Rows are
+// with tile::gather4: the append kernel at page sizes that are not a
+// multiple of 16). Rows are
 // the 256-byte (token, head) vectors: HND [pages, Hk, P, 128] and NHD
 // [pages, P, Hk, 128] pools are both [pages * Hk * P, 128] row arrays, and
 // 16-row boxes of one head in NHD take a 3-D map [tokens, Hk, 128] (box
