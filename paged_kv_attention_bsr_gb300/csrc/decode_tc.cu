@@ -27,10 +27,10 @@
 // and are never read back. A causal short append masks each row at its own
 // end-aligned limit (token i of qo_len sees kv positions <= kv_len - qo_len + i).
 //
-// Warps (160 threads, one CTA per SM): 0 softmax; 1 producer of the K/V
+// Warps (256 threads, one CTA per SM): 0 softmax; 1 producer of the K/V
 // ring (six 32 KB slots; TMA 16-row boxes by page index when the page size is
 // a multiple of 16, else rows copied one by one with cp.async, down to one
-// token per page -- in plain decode together with warps 5-7, 256 threads);
+// token per page, together with warps 5-7 in the kernels without RoPE);
 // 2 TMEM
 // allocation and the MMAs (one thread: S of tile k+1 runs under the softmax
 // of tile k, S double-buffered in TMEM); 3 query loader (plain loads of the
@@ -69,10 +69,11 @@ constexpr int kWarpEpi = 4;  // TMEM lanes 0-31, like the softmax warp
 constexpr int kWarpRope0 = 5;  // warps 5-8 turn K tiles when RoPE is fused in
 // warps 5-8 turn K tiles (RoPE); warps 5-7 widen FP8 tiles (eight warps in
 // all, two per scheduler: the register budget stays at 255 per thread)
-// warps 1 and 5-7 copy gathered rows (plain decode at page sizes that are
-// not a multiple of 16; eight warps keep the register budget at 255)
-template <bool ROPE, bool FP8 = false, bool GW = false>
-constexpr int block_threads() { return ROPE ? 288 : FP8 ? 256 : GW ? 256 : 160; }
+// warps 5-7: FP8 converters, or (page sizes that are not a multiple of 16)
+// copiers of gathered rows beside warp 1; idle otherwise. Eight warps keep
+// the register budget at 255 a thread.
+template <bool ROPE, bool FP8 = false>
+constexpr int block_threads() { return ROPE ? 288 : 256; }
 constexpr int kConvThreads = 96;  // FP8 converter warps 5-7
 
 // Two E4M3 values (the low byte first) as an f16x2 word (exact).
@@ -671,8 +672,8 @@ __device__ __noinline__ void produce_nhd_box(const DecodeTcParams& prm, Bars& ba
     }
 }
 
-template <bool BF16, int R, bool DEC, bool ROPE, bool FP8 = false, bool GW = false>
-__global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
+template <bool BF16, int R, bool DEC, bool ROPE, bool FP8 = false>
+__global__ void __launch_bounds__(block_threads<ROPE, FP8>(), 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
   constexpr int C = 32 / R;     // copies of each query row
   constexpr int W = kTile / C;  // kv columns per copy and tile
@@ -680,7 +681,6 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
   constexpr int kRing = ring_slots<FP8>();  // 16-bit K/V slots
   constexpr bool kMmaBF16 = FP8 ? false : BF16;  // operand type of the MMAs (and of P)
   static_assert(!(FP8 && ROPE), "FP8 K/V and fused RoPE are separate kernels");
-  static_assert(!(GW && (FP8 || ROPE)), "gather copy warps only in the plain kernel");
   extern __shared__ uint8_t smem_raw[];
   const AppendArgs& a = prm.a;
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
       // FP8: the converters fill it; gathered rows: each producer lane's
       // copies arrive on it; else one TMA arrival with its byte count
       mbar_init(smem_u32(&bars.slot_full[i]),
-                FP8 ? kConvThreads : prm.gather ? (GW ? 4 * 32 : 32) : 1);
+                FP8 ? kConvThreads : prm.gather ? (ROPE ? 32 : 4 * 32) : 1);
       mbar_init(smem_u32(&bars.slot_empty[i]), 1);
     }
     if (FP8)
@@ -749,10 +749,10 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
     uint32_t uses = 0;
     bool ok = true;
     if (!FP8 && prm.gather) {
-      if constexpr (GW)  // with warps 5-7: a quarter of every tile's rows each
-        produce_gather<DEC, 4>(prm, bars, base, gbase, lane, 0, err, uses, ok);
-      else
+      if constexpr (ROPE)  // (warps 5-8 turn K tiles)
         produce_gather<DEC, 1>(prm, bars, base, gbase, lane, 0, err, uses, ok);
+      else  // with warps 5-7: a quarter of every tile's rows each
+        produce_gather<DEC, 4>(prm, bars, base, gbase, lane, 0, err, uses, ok);
     } else if (!FP8 && prm.nhd) {
       produce_nhd_box<DEC>(prm, bars, base, lane, err, uses, ok);
     } else {
@@ -1319,8 +1319,8 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
       }
   }
 
-  if constexpr (GW) {
-    if (warp >= kWarpRope0 && warp < kWarpRope0 + 3) {
+  if constexpr (!ROPE && !FP8) {
+    if (prm.gather && warp >= kWarpRope0 && warp < kWarpRope0 + 3) {
       // ------------------------------------------------- gathered-row copies
       // (quarters 1-3 of every tile; warp 1 copies quarter 0)
       uint32_t uses = 0;
@@ -1555,14 +1555,14 @@ __global__ void __launch_bounds__(block_threads<ROPE, FP8, GW>(), 1)
   }
 }
 
-template <bool BF16, int R, bool DEC, bool ROPE = false, bool FP8 = false, bool GW = false>
+template <bool BF16, int R, bool DEC, bool ROPE = false, bool FP8 = false>
 cudaError_t launch_k(const DecodeTcParams& prm, int grid, cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};
   cudaError_t e =
-      ensure_smem_limit(decode_tc_kernel<BF16, R, DEC, ROPE, FP8, GW>, kSmem, configured);
+      ensure_smem_limit(decode_tc_kernel<BF16, R, DEC, ROPE, FP8>, kSmem, configured);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<BF16, R, DEC, ROPE, FP8, GW>
-      <<<grid, block_threads<ROPE, FP8, GW>(), kSmem, stream>>>(prm);
+  decode_tc_kernel<BF16, R, DEC, ROPE, FP8>
+      <<<grid, block_threads<ROPE, FP8>(), kSmem, stream>>>(prm);
   return cudaGetLastError();
 }
 // decode runs with R = group in {2, 4, 8}; short appends with R in {1..16}
@@ -1589,13 +1589,6 @@ cudaError_t launch_dt(const DecodeTcParams& prm, int rows, int grid, cudaStream_
       case 4: return launch_k<BF16, 4, false, true>(prm, grid, stream);
       case 8: return launch_k<BF16, 8, false, true>(prm, grid, stream);
       default: return launch_k<BF16, 16, false, true>(prm, grid, stream);
-    }
-  }
-  if (!prm.a.qo_indptr && prm.gather) {  // decode of gathered rows: four copy warps
-    switch (rows) {
-      case 2: return launch_k<BF16, 2, true, false, false, true>(prm, grid, stream);
-      case 4: return launch_k<BF16, 4, true, false, false, true>(prm, grid, stream);
-      default: return launch_k<BF16, 8, true, false, false, true>(prm, grid, stream);
     }
   }
   if (!prm.a.qo_indptr) {
