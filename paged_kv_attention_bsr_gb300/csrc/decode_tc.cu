@@ -1649,6 +1649,15 @@ cudaError_t launch_decode_tc(const AppendArgs& a, cudaStream_t stream, const cha
     *msg = "attn: composable formats in one launch take 16-bit pools without RoPE";
     return cudaErrorNotSupported;
   }
+  // gathered rows are addressed by 32-bit (page, head, slot) row indices
+  if (prm.gather) {
+    const int64_t rows1 = a.num_pages * a.num_kv_heads * int64_t(a.page_size);
+    const int64_t rows2 = a.cascade ? a.num_pages2 * a.num_kv_heads * int64_t(a.page_size2) : 0;
+    if (rows1 >= (int64_t(1) << 31) || rows2 >= (int64_t(1) << 31)) {
+      *msg = "attn: the pool has 2^31 or more (page, head, slot) rows";
+      return cudaErrorNotSupported;
+    }
+  }
   const int elem = a.kv_fp8 ? kKvElemU8 : (bf16 ? kKvElemBF16 : kKvElemF16);
   // (gathered rows are copied with cp.async: no tensor map)
   if (!prm.gather &&

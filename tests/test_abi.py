@@ -215,3 +215,36 @@ def test_merge_shape_checks_in_the_binding():
                  (o, l, o, l.double(), o, l)]:
         with pytest.raises(ValueError):
             C.merge_states(*args)
+
+
+def test_cascade_entry_points_validate_without_gpu():
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    dev, host = C.cascade_workspace_size(4, 8, 32, 8, 128, 152)
+    assert dev > host > 0
+    with pytest.raises(C.AttnError) as ei:
+        C.cascade_workspace_size(0, 8, 32, 8, 128, 152)
+    assert ei.value.status == C.ERR_INVALID_ARG
+    qo = np.array([0, 2, 3], np.int32)
+    ip0, l0 = np.array([0, 4, 5], np.int32), np.array([16, 3], np.int32)
+    ip1, l1 = np.array([0, 1, 3, 3], np.int32), np.array([5, 8, 0], np.int32)
+    buf = np.zeros(host, np.uint8)
+    p = C.plan_cascade(qo, ip0, l0, 16, ip1, l1, 8, 32, 8, 128, 152, buf)
+    assert p.mode == C.MODE_CASCADE and p.total_qo == 3 and p.page_size_suffix == 8
+    fake = ctypes.c_void_p(256)
+
+    def run(plan, dev_ws=fake, dev_bytes=1 << 30, suffix_pool=fake, layout=0, pages=8):
+        return C.lib.attn_cascade_run(ctypes.byref(plan), fake, fake, fake, fake, pages, fake,
+                                      fake, fake, suffix_pool, suffix_pool, pages, fake, fake,
+                                      fake, layout, 1, ctypes.c_float(0.1), fake, None, dev_ws,
+                                      dev_bytes, None)
+    assert run(p, dev_ws=None) == C.ERR_INVALID_ARG and "dev_ws" in C.last_error()
+    assert run(p, dev_bytes=16) == C.ERR_WORKSPACE_TOO_SMALL
+    assert run(p, suffix_pool=None) == C.ERR_INVALID_ARG and "suffix" in C.last_error()
+    assert run(p, layout=7) == C.ERR_INVALID_ARG
+    # a decode plan is not a cascade plan
+    pd = C.plan(None, np.array([0, 1], np.int32), np.array([5], np.int32), 16, 32, 8, 128,
+                False, 152, np.zeros(1 << 20, np.uint8))
+    assert run(pd) == C.ERR_INVALID_ARG and "mode" in C.last_error()
+    # gathered rows (suffix page size 8): 32-bit row indices, checked on the host
+    huge = (1 << 31) // (8 * 8) + 1
+    assert run(p, pages=huge) == C.ERR_UNSUPPORTED and "2^31" in C.last_error()
