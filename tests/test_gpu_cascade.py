@@ -63,7 +63,7 @@ def oracle_flat(oracle_mod, w):
         w.num_qo_heads, w.num_kv_heads, 128, oracle_dtype(oracle_mod, w.dtype), w.sm_scale)
 
 
-@pytest.mark.parametrize("num_ctas", [1, 7, None])
+@pytest.mark.parametrize("num_ctas", [1, 7, None, 304])
 def test_one_launch_small_vs_flat(oracle_mod, num_ctas):
     w = synth.shared_prefix_decode(seed=99, prompts=3, n=4, prefix_len=512)
     o, l, _ = run_one_launch(w, num_ctas)
@@ -88,7 +88,7 @@ RAGGED = [
 
 
 @pytest.mark.parametrize("case", range(len(RAGGED)))
-@pytest.mark.parametrize("num_ctas", [3, None])
+@pytest.mark.parametrize("num_ctas", [3, None, 304])
 def test_one_launch_ragged_vs_oracle(oracle_mod, case, num_ctas):
     gens, pre_lens, suf_lens, P0, P1, Hq, Hk, dtype = RAGGED[case]
     rng = np.random.default_rng(700 + case)
@@ -146,7 +146,7 @@ ANY_PAGE = [
 
 
 @pytest.mark.parametrize("case", range(len(ANY_PAGE)))
-@pytest.mark.parametrize("num_ctas", [3, None])
+@pytest.mark.parametrize("num_ctas", [3, None, 304])
 def test_one_launch_any_page_size_and_layout(oracle_mod, case, num_ctas):
     from paged_kv_attention_bsr_gb300.api import CascadeAttention
     gens, pre_lens, suf_lens, P0, P1, Hq, Hk, dtype, layout = ANY_PAGE[case]
