@@ -355,7 +355,20 @@ def bench_shared_prefix(hbm_peak, bf16_peak, flush, steps, warmup):
         return ca, float(np.median(step_ms)) * 1e3, float(np.median(kern_ms)) * 1e-3
 
     ca, step_us, k_s = timed("one_launch")
+    # host planning time of attn_plan_cascade alone (tables into host memory)
+    from paged_kv_attention_bsr_gb300 import _capi as C
+    _, host_bytes = C.cascade_workspace_size(w.extra["prompts"], w.batch, 32, 8, 128,
+                                             ca.num_ctas)
+    hbuf = np.zeros(host_bytes, np.uint8)
+    pts = []
+    for _ in range(200):
+        t0 = time.perf_counter()
+        C.plan_cascade(pqo_h, pre.kv_indptr, pre.last_page_len, pre.page_size, suf.kv_indptr,
+                       suf.last_page_len, suf.page_size, 32, 8, 128, ca.num_ctas, hbuf)
+        pts.append(time.perf_counter() - t0)
+    res_plan_us = float(np.median(pts)) * 1e6
     res = {"kind": "composable", "bytes": b_pre + b_suf, "flat_layout_bytes": b_flat,
+           "plan_us_host": res_plan_us,
            "kernel_us": k_s * 1e6, "step_us": step_us,
            "GB/s": (b_pre + b_suf) / k_s / 1e9,
            "roofline_frac_hbm": (b_pre + b_suf) / k_s / 1e9 / hbm_peak,
