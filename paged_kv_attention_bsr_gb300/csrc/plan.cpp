@@ -98,6 +98,29 @@ uint64_t fnv1a(uint64_t h, const void* data, size_t bytes) {
   return h;
 }
 
+// Within each CTA's range of `v` (bounds in indptr), the units of split
+// items (slot >= 0) first, each group in its order; `tmp` is scratch. One
+// pass per CTA with no allocation (std::stable_partition may allocate on
+// every call).
+void split_units_first(std::vector<Unit>& v, const std::vector<int32_t>& indptr, int64_t C,
+                       std::vector<Unit>& tmp) {
+  for (int64_t c = 0; c < C; ++c) {
+    const size_t b = size_t(indptr[size_t(c)]), e = size_t(indptr[size_t(c) + 1]);
+    bool need = false;  // an unsplit unit before a split one
+    for (size_t i = b, seen_unsplit = 0; i < e; ++i) {
+      if (v[i].slot < 0) seen_unsplit = 1;
+      else if (seen_unsplit) need = true;
+    }
+    if (!need) continue;
+    tmp.clear();
+    for (size_t i = b; i < e; ++i)
+      if (v[i].slot >= 0) tmp.push_back(v[i]);
+    for (size_t i = b; i < e; ++i)
+      if (v[i].slot < 0) tmp.push_back(v[i]);
+    std::copy(tmp.begin(), tmp.end(), v.begin() + std::ptrdiff_t(b));
+  }
+}
+
 }  // namespace
 
 uint64_t plan_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr,
@@ -414,10 +437,7 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
     // pieces of every shared item run early on their CTAs and the merge
     // (by whichever finishes second) overlaps later units instead of
     // trailing the CTA's last one.
-    for (int64_t c = 0; c < C; ++c)
-      std::stable_partition(gen.begin() + work_indptr[size_t(c)],
-                            gen.begin() + work_indptr[size_t(c) + 1],
-                            [](const Unit& u) { return u.slot >= 0; });
+    split_units_first(gen, work_indptr, C, sc.units);
   } else {
     std::vector<Unit>& units = sc.units;
     units.resize(num_units);
@@ -608,10 +628,11 @@ attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     }
   }
   const int64_t C = num_ctas;
-  auto bound = [&](int64_t c) -> int64_t {
-    // floor(c W / C) without overflow for W < 2^62 / C
-    return (c * (W / C)) + (c * (W % C)) / C;
-  };
+  // floor(c W / C) without overflow for W < 2^62 / C, computed once
+  std::vector<int64_t>& bounds = scratch().bounds;
+  bounds.resize(size_t(C) + 1);
+  for (int64_t c = 0; c <= C; ++c) bounds[size_t(c)] = (c * (W / C)) + (c * (W % C)) / C;
+  auto bound = [&](int64_t c) -> int64_t { return bounds[size_t(c)]; };
   std::vector<int64_t> item_pages(item_of.size(), 0);
   for (const Seg& sg : segs) item_pages[size_t(sg.item)] += sg.n;
   // units in CTA order: the cut walks the segments in order, so the CTA
@@ -651,17 +672,21 @@ attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_ind
       // keeps one empty unit (its rows get O = 0, LSE = -inf)
       if (item_pages[size_t(sg.item)] == 0 && sg.kind == 0) emit(0, 0, owner(base));
     } else {
+      // the pages of CTA `cur` are those before the first page whose
+      // position reaches bound(cur + 1): jump from boundary to boundary
       int64_t k0 = 0;
       int64_t cur = owner(base + kCascadeAlpha);
-      for (int64_t k = 1; k < sg.n; ++k) {
-        const int64_t o = owner(base + kCascadeAlpha + k * P);
-        if (o != cur) {
-          emit(k0, k, cur);
-          k0 = k;
-          cur = o;
+      while (true) {
+        int64_t k1 = sg.n;
+        if (cur + 1 < C) {
+          const int64_t rel = bound(cur + 1) - base - kCascadeAlpha;  // > k0 P
+          k1 = std::min<int64_t>(sg.n, std::max<int64_t>(k0 + 1, (rel + P - 1) / P));
         }
+        emit(k0, k1, cur);
+        if (k1 >= sg.n) break;
+        k0 = k1;
+        cur = owner(base + kCascadeAlpha + k0 * P);
       }
-      emit(k0, sg.n, cur);
     }
     base += sg.n * P + kCascadeAlpha;
   }
@@ -707,10 +732,7 @@ attn_status_t build_cascade_plan(const int32_t* qo_indptr, const int32_t* kv_ind
   for (size_t i = 0; i < nu; ++i) work_indptr[size_t(unit_cta[i]) + 1]++;
   for (int64_t i = 0; i < C; ++i) work_indptr[size_t(i) + 1] += work_indptr[size_t(i)];
   // within a CTA, the chains of split items first (stable; chains stay whole)
-  for (int64_t i = 0; i < C; ++i)
-    std::stable_partition(units.begin() + work_indptr[size_t(i)],
-                          units.begin() + work_indptr[size_t(i) + 1],
-                          [](const Unit& u) { return u.slot >= 0; });
+  split_units_first(units, work_indptr, C, scratch().units);
   int64_t max_load = 0;
   for (int64_t i = 0; i < C; ++i) max_load = std::max(max_load, bound(i + 1) - bound(i));
 
