@@ -1001,6 +1001,10 @@ def run_reference(args):
             t0 = time.perf_counter()
             list(ex.map(lambda rh: item_job(*rh), sel))
             dt = time.perf_counter() - t0
+            if k == 0 and args.warmup > 0:
+                # re-size the sample from a whole parallel step (threads share
+                # the host's memory bandwidth, so one item alone is optimistic)
+                n_items = max(1, int(n_items * budget_s / max(dt, 1e-6)))
             if k >= args.warmup:
                 total_t += dt
                 total_b += sum(int(c.kv_lens[r]) * kvb + 2 * g * 256 for r, _ in sel)
