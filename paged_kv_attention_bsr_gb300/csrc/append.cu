@@ -737,13 +737,18 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
         if (warp_live) {
           float v[kTile];
           tmem_ld128(tmem + lane_off + col_sx, v);
-          // Tiles without masked columns (all but the causal diagonal and the
-          // unit's last tile) skip the per-element selects; rows without a
-          // query may take that path too (their P row only feeds their own O
-          // row, which is never stored).
+          // Tiles with masked columns (the causal diagonal, the unit's last
+          // tile) first set those scores to -inf with selects, no branches
+          // (nvalid differs from row to row on the diagonal); every tile then
+          // takes the same path. Rows without a query may skip the masking
+          // (their P row only feeds their own O row, which is never stored).
           const bool full = __all_sync(0xffffffffu, !row_ok || nvalid == kTile);
-          float mx = -INFINITY;
-          if (full) {
+          if (!full) {
+#pragma unroll
+            for (int c = 0; c < kTile; ++c) v[c] = (c < nvalid) ? v[c] : -INFINITY;
+          }
+          float mx;
+          {
             float m0 = fmax3(v[0], v[1], v[2]), m1 = fmax3(v[3], v[4], v[5]);
 #pragma unroll
             for (int c = 6; c + 3 < kTile; c += 4) {
@@ -751,9 +756,6 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
               m1 = fmax3(m1, v[c + 2], v[c + 3]);
             }
             mx = fmax3(m0, m1, fmaxf(v[kTile - 2], v[kTile - 1]));
-          } else {
-#pragma unroll
-            for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, (c < nvalid) ? v[c] : -INFINITY);
           }
           const float m_tile = mx * c2;  // -inf stays -inf
           float alpha = 1.f;
@@ -788,11 +790,13 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
           }
           // probabilities, packed to the MMA input type, written over S_x in
           // TMEM (column c holds elements 2c, 2c+1 of the row)
+          // (a row with no unmasked score yet keeps m_ref = -inf: its scores
+          // are all -inf and come out as 0 with a zero offset)
           float2 lsum2 = make_float2(0.f, 0.f);
-          const bool live = m_ref != -INFINITY;
-          if (full && __all_sync(0xffffffffu, live || !row_ok)) {
+          {
             const float2 c2x2 = make_float2(c2, c2);
-            const float2 negm = make_float2(-m_ref, -m_ref);
+            const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+            const float2 negm = make_float2(nm, nm);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t pk[16];
@@ -800,21 +804,6 @@ __global__ void __launch_bounds__(kThreads, 1) append_kernel(const __grid_consta
               for (int q = 0; q < 32; q += 2) {
                 const float2 t = ffma2(make_float2(v[c * 32 + q], v[c * 32 + q + 1]), c2x2, negm);
                 const float2 pr = make_float2(ex2(t.x), ex2(t.y));
-                lsum2 = fadd2(lsum2, pr);
-                pk[q / 2] = pack2<BF16>(pr.x, pr.y);
-              }
-              tmem_st16_nowait(tmem + lane_off + col_sx + c * 16, pk);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int q = 0; q < 32; q += 2) {
-                const int col = c * 32 + q;
-                float2 pr;
-                pr.x = (live && col < nvalid) ? ex2(fmaf(v[col], c2, -m_ref)) : 0.f;
-                pr.y = (live && col + 1 < nvalid) ? ex2(fmaf(v[col + 1], c2, -m_ref)) : 0.f;
                 lsum2 = fadd2(lsum2, pr);
                 pk[q / 2] = pack2<BF16>(pr.x, pr.y);
               }
