@@ -157,8 +157,13 @@ struct AGeo {
   int64_t tok_begin, tok_end;
 };
 
+// Every role prefetches the next unit's records into L1 when it starts a
+// unit, so that their global-load latency is spent under the current unit's
+// work and not between two units, where it would delay the next first tile.
 __device__ __forceinline__ AGeo append_geo(const AppendArgs& a, int ui) {
   const int4* rec = reinterpret_cast<const int4*>(a.ws.units + ui);
+  prefetch_l1(rec + 3);
+  prefetch_l1(rec + 5);
   const int4 x = __ldg(rec);
   const int4 y = __ldg(rec + 1);
   const int4 z = __ldg(rec + 2);
