@@ -10,6 +10,8 @@ pseudo-code; the exact cut below is the reading used throughout this project:
              decode has one tile per request, append tiles hold
              tq = 256 // group query tokens (group heads x tq tokens = 256 packed
              rows: two 128-row MMA tiles), group must divide 128
+  weights    an item costs its pages n plus alpha (its unit's start and end,
+             in pages): alpha = 1 in decode plans, 16 in append plans
   decode     the costs w = n + alpha are laid end to end (total W) and CTA c
              takes the positions [floor(c W / C), floor((c+1) W / C)); inside
              an item at base b, position b is its overhead slot and b + alpha
@@ -40,7 +42,8 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 from typing import List, Optional, Sequence
 
-ALPHA = 1
+ALPHA = 1           # decode: cost of a unit beyond its pages, in pages
+APPEND_ALPHA = 16   # append (and POD) plans
 ITEM_ROWS = 256
 FEW_ROWS = 16
 
@@ -94,7 +97,8 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
                 few.append(group * qo_len <= FEW_ROWS)
 
     # 2. weights
-    weight = [it[3] + ALPHA for it in items]
+    alpha = ALPHA if decode else APPEND_ALPHA
+    weight = [it[3] + alpha for it in items]
     total = sum(weight)
     C = num_ctas
     plan = Plan(work_indptr=[0] * (C + 1), total_weight=total, num_items=len(items),
@@ -108,7 +112,7 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
 
         base = 0
         for k, (r, hk, t, n) in enumerate(items):
-            w = n + ALPHA
+            w = n + alpha
             for c in range(C):
                 a, e = lo(c), lo(c + 1)
                 if e <= base or a >= base + w:
@@ -117,8 +121,8 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
                     if a <= base < e:
                         per_cta_units[c].append([k, r, hk, t, 0, 0])
                     continue
-                p0 = max(0, a - base - ALPHA)
-                p1 = min(n, e - base - ALPHA)
+                p0 = max(0, a - base - alpha)
+                p1 = min(n, e - base - alpha)
                 if p1 > p0:
                     per_cta_units[c].append([k, r, hk, t, p0, p1])
             base += w
@@ -140,7 +144,7 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
                 order.append(light[j])
                 df += weight[light[j]]
                 j += 1
-        cap = -(-total // C) + ALPHA
+        cap = -(-total // C) + alpha
         ready = [(0, c) for c in range(C)]
         heapq.heapify(ready)
         for k in order:
@@ -149,13 +153,13 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
             while True:
                 used, c = heapq.heappop(ready)
                 avail = cap - used
-                need = ALPHA + (n - p)
+                need = alpha + (n - p)
                 if need <= avail:
                     per_cta_units[c].append([k, r, hk, t, p, n])
                     if used + need < cap:
                         heapq.heappush(ready, (used + need, c))
                     break
-                take = avail - ALPHA
+                take = avail - alpha
                 if take > 0:
                     per_cta_units[c].append([k, r, hk, t, p, p + take])
                     p += take

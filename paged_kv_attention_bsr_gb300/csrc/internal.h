@@ -109,6 +109,11 @@ uint64_t cascade_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr0
                              int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t num_ctas);
 
+// Cost of a unit beyond its pages, in pages, for the plan's balanced cut:
+// decode items, append (and POD) items.
+constexpr int64_t kDecodeAlpha = 1;
+constexpr int64_t kAppendAlpha = 16;
+
 // Builds the plan tables into `host_tables` (table_bytes of them).
 // Returns ATTN_OK or an error with a message in *msg.
 attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,

@@ -233,7 +233,10 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   }
 
   // ---- cut the work into units
-  constexpr int64_t kAlpha = 1;
+  // cost of a unit beyond its pages, in pages: a decode unit's start and
+  // end are cheap next to its pages; an append unit's epilogue (O out of
+  // tensor memory) and next-unit start cost about two KV tiles of MMAs
+  const int64_t kAlpha = decode ? kDecodeAlpha : kAppendAlpha;
   int64_t W = 0;
   for (const Item& it : items) W += it.n + kAlpha;
   const int64_t C = num_ctas;

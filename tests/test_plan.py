@@ -129,8 +129,9 @@ def test_plan_properties(decode):
             assert segs[0][0] == 0 and segs[-1][1] == n
             for (a0, a1), (b0, b1) in zip(segs, segs[1:]):
                 assert a1 == b0 and a0 < a1
-        # weights: pages + 1 per item
-        assert p.total_weight == sum(n + 1 for n in items.values())
+        # weights: pages + alpha per item (1 decode, 16 append)
+        alpha = 1 if qo is None else 16
+        assert p.total_weight == sum(n + alpha for n in items.values())
         # balance: the page share of every CTA is at most ceil(W / C)
         W = p.total_weight
         wi = t["work_indptr"]
@@ -138,7 +139,7 @@ def test_plan_properties(decode):
         for c in range(ctas):
             pages = int((u[wi[c]:wi[c + 1], 4] - u[wi[c]:wi[c + 1], 3]).sum())
             assert pages <= cap
-        assert p.max_cta_weight <= cap + (0 if qo is None else 1)
+        assert p.max_cta_weight <= cap + (0 if qo is None else alpha)
         # the cut adds at most C - 1 units (decode) / C units (append);
         # split items carry slots in order
         extra = ctas - 1 if qo is None else ctas
