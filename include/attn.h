@@ -86,8 +86,9 @@ typedef struct attn_plan {
   int32_t num_slots;        /* partial-state slots used by split items         */
   int32_t total_qo;         /* query rows (decode: batch)                      */
   int32_t max_qo_len;       /* longest query row count of a request (decode: 1) */
-  int64_t total_weight;     /* sum over items of (pages + alpha): alpha 1 in
-                               decode plans, 16 in append plans               */
+  int64_t total_weight;     /* sum over items of (pages + alpha): alpha 1 if
+                               the few-row kernel runs the plan (decode,
+                               short appends), else 16                       */
   int64_t max_cta_weight;   /* largest per-CTA share of the weights the cut
                                balances (cascade: tokens + 16 per segment)     */
   int64_t off_work_indptr;  /* byte offsets of the tables in the workspaces    */

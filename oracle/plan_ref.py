@@ -11,7 +11,9 @@ pseudo-code; the exact cut below is the reading used throughout this project:
              tq = 256 // group query tokens (group heads x tq tokens = 256 packed
              rows: two 128-row MMA tiles), group must divide 128
   weights    an item costs its pages n plus alpha (its unit's start and end,
-             in pages): alpha = 1 in decode plans, 16 in append plans
+             in pages): alpha = 1 in plans of the few-row kernel (decode, and
+             appends whose requests all have at most 16 query rows), 16 in
+             plans of the append kernel
   decode     the costs w = n + alpha are laid end to end (total W) and CTA c
              takes the positions [floor(c W / C), floor((c+1) W / C)); inside
              an item at base b, position b is its overhead slot and b + alpha
@@ -42,8 +44,8 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 from typing import List, Optional, Sequence
 
-ALPHA = 1           # decode: cost of a unit beyond its pages, in pages
-APPEND_ALPHA = 16   # append (and POD) plans
+ALPHA = 1           # few-row kernel plans: cost of a unit beyond its pages
+APPEND_ALPHA = 16   # append-kernel plans (long appends, POD batches)
 ITEM_ROWS = 256
 FEW_ROWS = 16
 
@@ -97,7 +99,7 @@ def make_plan(kv_indptr: Sequence[int], last_page_len: Sequence[int], page_size:
                 few.append(group * qo_len <= FEW_ROWS)
 
     # 2. weights
-    alpha = ALPHA if decode else APPEND_ALPHA
+    alpha = ALPHA if (decode or all(few)) else APPEND_ALPHA  # all(few): the few-row kernel runs it
     weight = [it[3] + alpha for it in items]
     total = sum(weight)
     C = num_ctas

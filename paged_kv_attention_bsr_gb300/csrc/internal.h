@@ -110,7 +110,8 @@ uint64_t cascade_fingerprint(const int32_t* qo_indptr, const int32_t* kv_indptr0
                              int32_t num_ctas);
 
 // Cost of a unit beyond its pages, in pages, for the plan's balanced cut:
-// decode items, append (and POD) items.
+// plans the few-row kernel runs (decode, short appends), plans the append
+// kernel runs (long appends, POD batches).
 constexpr int64_t kDecodeAlpha = 1;
 constexpr int64_t kAppendAlpha = 16;
 

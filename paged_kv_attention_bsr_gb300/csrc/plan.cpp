@@ -233,10 +233,12 @@ attn_status_t build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
   }
 
   // ---- cut the work into units
-  // cost of a unit beyond its pages, in pages: a decode unit's start and
-  // end are cheap next to its pages; an append unit's epilogue (O out of
-  // tensor memory) and next-unit start cost about two KV tiles of MMAs
-  const int64_t kAlpha = decode ? kDecodeAlpha : kAppendAlpha;
+  // cost of a unit beyond its pages, in pages: a unit of the few-row kernel
+  // (decode, short appends) starts and ends cheaply next to its pages; an
+  // append-kernel unit's epilogue (O out of tensor memory) and next-unit
+  // start cost about two KV tiles of MMAs
+  const bool few_kernel = decode || int64_t(group) * max_qo_len <= kFewRowMax;
+  const int64_t kAlpha = few_kernel ? kDecodeAlpha : kAppendAlpha;
   int64_t W = 0;
   for (const Item& it : items) W += it.n + kAlpha;
   const int64_t C = num_ctas;
