@@ -181,7 +181,9 @@ attn_status_t attn_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
  *   kv_indptr, kv_indices, last_page_len : device copies of the BSR table
  *                (kv_indptr and last_page_len equal to the plan's host copies;
  *                every kv_indices entry in [0, num_pages))
- *   sm_scale   : logit scale (1/sqrt(head_dim) is the usual choice)
+ *   sm_scale   : logit scale (1/sqrt(head_dim) is the usual choice), finite
+ *                and >= 0 (every run entry point rejects other values with
+ *                INVALID_ARG); 0 weighs the visible keys equally
  *   o          : device [batch, num_qo_heads, head_dim] of `dtype` (out)
  *   lse        : device float[batch, num_qo_heads] (out) or NULL
  *   dev_ws     : the workspace given to attn_plan (holds the plan tables)

@@ -2,6 +2,8 @@
 // workspace sizing, plan upload and kernel dispatch. Declarations and the
 // contract of every entry point are in include/attn.h.
 #include <algorithm>
+#include <cfloat>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -249,6 +251,16 @@ void set_last_error(const std::string& msg) { g_err = msg; }
 }  // namespace attn
 
 namespace {
+
+// sm_scale as the kernels take it. The kernels scale a row's maximum over the
+// unscaled scores, so the scale must be finite and >= 0. A zero scale (equal
+// weights over the visible keys) runs as the smallest normal float: the same
+// weights, while masked scores (-inf) still scale to -inf rather than NaN.
+bool scale_for_kernels(float* sm_scale) {
+  if (!std::isfinite(*sm_scale) || *sm_scale < 0.f) return false;
+  if (*sm_scale == 0.f) *sm_scale = FLT_MIN;
+  return true;
+}
 
 // Arguments of the few-row tensor-core kernel for a decode plan.
 attn::AppendArgs decode_tc_args(const attn_plan_t* plan, const void* q, const void* k_pool,
@@ -544,6 +556,8 @@ attn_status_t attn_cascade_run(const attn_plan_t* plan, const void* q, const int
                                int32_t dtype, float sm_scale, void* o, float* lse,
                                void* dev_ws, size_t dev_bytes, void* stream) {
   NvtxRange nvtx("attn_cascade_run");
+  if (!scale_for_kernels(&sm_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_cascade_run: sm_scale must be finite and >= 0");
   const char* fn = "attn_cascade_run";
   const std::string f(fn);
   attn_status_t s = check_plan_common(plan, ATTN_MODE_CASCADE, q, k_prefix, v_prefix,
@@ -593,6 +607,8 @@ attn_status_t attn_decode_run(const attn_plan_t* plan, const void* q, const void
                               void* o, float* lse, void* dev_ws, size_t dev_bytes,
                               void* stream) {
   NvtxRange nvtx("attn_decode_run");
+  if (!scale_for_kernels(&sm_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run: sm_scale must be finite and >= 0");
   attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
                                       layout, kv_indptr, kv_indices, last_page_len, dtype, o,
                                       dev_ws, dev_bytes, "attn_decode_run");
@@ -659,6 +675,8 @@ attn_status_t attn_decode_run_fp8(const attn_plan_t* plan, const void* q, const 
                                   void* o, float* lse, void* dev_ws, size_t dev_bytes,
                                   void* stream) {
   NvtxRange nvtx("attn_decode_run_fp8");
+  if (!scale_for_kernels(&sm_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_fp8: sm_scale must be finite and >= 0");
   attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
                                       layout, kv_indptr, kv_indices, last_page_len, dtype, o,
                                       dev_ws, dev_bytes, "attn_decode_run_fp8");
@@ -726,6 +744,8 @@ attn_status_t attn_decode_run_rope(const attn_plan_t* plan, const void* q, const
                                    int64_t rope_max_pos, void* o, float* lse, void* dev_ws,
                                    size_t dev_bytes, void* stream) {
   NvtxRange nvtx("attn_decode_run_rope");
+  if (!scale_for_kernels(&sm_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_rope: sm_scale must be finite and >= 0");
   attn_status_t s = check_plan_common(plan, ATTN_MODE_DECODE, q, k_pool, v_pool, num_pages,
                                       layout, kv_indptr, kv_indices, last_page_len, dtype, o,
                                       dev_ws, dev_bytes, "attn_decode_run_rope");
@@ -763,6 +783,8 @@ attn_status_t attn_append_run(const attn_plan_t* plan, const void* q,
                               float sm_scale, void* o, float* lse, void* dev_ws,
                               size_t dev_bytes, void* stream) {
   NvtxRange nvtx("attn_append_run");
+  if (!scale_for_kernels(&sm_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_append_run: sm_scale must be finite and >= 0");
   attn_status_t s = check_append(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout,
                                  kv_indptr, kv_indices, last_page_len, dtype, causal, o,
                                  dev_ws, dev_bytes, "attn_append_run");
@@ -789,6 +811,8 @@ attn_status_t attn_append_run_rope(const attn_plan_t* plan, const void* q,
                                    const float* rope_sin, int64_t rope_max_pos, void* o,
                                    float* lse, void* dev_ws, size_t dev_bytes, void* stream) {
   NvtxRange nvtx("attn_append_run_rope");
+  if (!scale_for_kernels(&sm_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_append_run_rope: sm_scale must be finite and >= 0");
   attn_status_t s = check_append(plan, q, qo_indptr, k_pool, v_pool, num_pages, layout,
                                  kv_indptr, kv_indices, last_page_len, dtype, causal, o,
                                  dev_ws, dev_bytes, "attn_append_run_rope");

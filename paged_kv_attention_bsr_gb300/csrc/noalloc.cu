@@ -20,6 +20,8 @@
 //    calls on a single stream are ordered and safe;
 //  * the plan tables, partial states and arrival counters must fit in
 //    kNoAllocScratchBytes; larger batches are rejected before any GPU work.
+#include <cfloat>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -76,6 +78,12 @@ extern "C" attn_status_t attn_decode_run_noalloc(
     const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* last_page_len,
     int32_t dtype, float sm_scale, void* o, float* lse, void* stream) {
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  // the scale rule of the other run entry points: finite and >= 0, zero run
+  // as the smallest normal float (equal weights, masked scores stay -inf)
+  if (!std::isfinite(sm_scale) || sm_scale < 0.f)
+    return noalloc_fail(ATTN_ERR_INVALID_ARG,
+                        "attn_decode_run_noalloc: sm_scale must be finite and >= 0");
+  if (sm_scale == 0.f) sm_scale = FLT_MIN;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16)
     return noalloc_fail(ATTN_ERR_INVALID_ARG, "attn_decode_run_noalloc: bad dtype");
   if (layout != ATTN_LAYOUT_HND && layout != ATTN_LAYOUT_NHD)

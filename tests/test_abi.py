@@ -248,3 +248,29 @@ def test_cascade_entry_points_validate_without_gpu():
     # gathered rows (suffix page size 8): 32-bit row indices, checked on the host
     huge = (1 << 31) // (8 * 8) + 1
     assert run(p, pages=huge) == C.ERR_UNSUPPORTED and "2^31" in C.last_error()
+
+
+@pytest.mark.parametrize("bad", [-0.125, float("nan"), float("inf")])
+def test_run_entry_points_reject_bad_sm_scale_without_gpu(bad):
+    """Every run entry point checks sm_scale first (finite, >= 0): a bad scale
+    returns INVALID_ARG naming sm_scale before anything touches a device."""
+    C = pytest.importorskip("paged_kv_attention_bsr_gb300._capi")
+    plan = C.Plan()
+    fake = ctypes.c_void_p(256)
+    names = ["attn_decode_run", "attn_decode_run_rope", "attn_decode_run_fp8",
+             "attn_append_run", "attn_append_run_rope", "attn_cascade_run",
+             "attn_decode_run_noalloc"]
+    for name in names:
+        fn = getattr(C.lib, name)
+        args = []
+        for t in fn.argtypes:
+            if t is ctypes.c_float:
+                args.append(ctypes.c_float(bad))
+            elif t is ctypes.c_void_p:
+                args.append(fake)
+            elif t in (ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t):
+                args.append(t(1))
+            else:  # the plan
+                args.append(ctypes.byref(plan))
+        assert fn(*args) == C.ERR_INVALID_ARG, name
+        assert "sm_scale" in C.last_error(), (name, C.last_error())

@@ -67,6 +67,20 @@ def test_append_small_parity(oracle_mod, case, num_ctas):
     assert_attn_close(o, lse, o_ref, lse_ref, f"append case {case} ctas {num_ctas}")
 
 
+@pytest.mark.parametrize("case", [0, 3])
+def test_append_zero_scale(oracle_mod, case):
+    """sm_scale = 0 weighs every visible key equally; masked columns (the
+    causal diagonal, ragged last tiles) stay out, split items merge."""
+    P, Hq, Hk, dtype, qo_lens, extra, causal = CASES[case]
+    kv_lens = [q + e for q, e in zip(qo_lens, extra)]
+    pool = sum(-(-L // P) for L in kv_lens) + 9
+    w = synth.append_workload(f"app_s0_{case}", qo_lens, kv_lens, P, pool, Hq, Hk, dtype,
+                              seed=700 + case, causal=causal, sm_scale=0.0)
+    o_ref, lse_ref = oracle_full(oracle_mod, w)
+    o, lse, _ = run_append(w, 5)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"append sm_scale 0 case {case}")
+
+
 # Short appends (group x longest query count <= 16 packed rows) run on the
 # few-row tensor-core kernel: causal and not, groups 1 to 8, empty kv.
 SHORT_CASES = [

@@ -206,3 +206,14 @@ def test_single_decode_strided_inputs(oracle_mod):
         np.array([4], np.int32), 4, 16, 4, 128, oracle_mod.F16, 1 / math.sqrt(128),
         layout=oracle_mod.NHD)
     assert_attn_close(o.reshape(1, 16, 128), lse.reshape(1, 16), o_ref, lse_ref, "strided")
+
+
+@pytest.mark.parametrize("hq,hk", [(32, 8), (32, 32)])
+def test_decode_zero_scale(oracle_mod, hq, hk):
+    """sm_scale = 0 weighs every key of a request equally (tensor-core kernel
+    at group 4, CUDA-core kernel at group 1), ragged last pages included."""
+    w = synth.decode_workload(f"dec_s0_{hq}_{hk}", [1, 17, 300, 1000], 16, 120, hq, hk,
+                              torch.bfloat16, seed=811, sm_scale=0.0)
+    o_ref, lse_ref = oracle_decode_threaded(oracle_mod, w)
+    o, lse, _ = run_decode(w, num_ctas=7)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"decode sm_scale 0 group {hq // hk}")
